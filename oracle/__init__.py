@@ -1,0 +1,190 @@
+"""fp64 CPU oracle for the fused attention forward pass.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  The product library
+(``attention_forward_10_gb300``) never imports it, and this package imports
+nothing from the product: the two share no code.
+
+The arithmetic lives in ``attn_ref.c`` (plain C, double precision, one OpenMP
+loop over query rows); this module only compiles it and marshals arguments.
+What is computed, per (b, h, i):
+
+    J(i)  = all keys (full) or keys 0..i (causal)
+    s_ij  = scale * q_i . k_j
+    LSE_i = max_j s_ij + ln sum_j exp(s_ij - max_j s_ij)      (natural log)
+    O_i   = sum_j exp(s_ij - LSE_i) v_j
+
+following LeetCUDA "flash_attn_mma_tiling_qk.cu" (kernel body: scaled scores,
+softmax along keys, final division by the row sum) and flash-attention
+"hopper/mainloop_bwd_sm90_tma_gmma_ws.hpp" (causal masking loop; LSE is the
+log-normaliser of the scaled scores) and "hopper/flash_fwd_kernel.h" (an empty
+row stores O = 0 and LSE = -inf).
+
+Pins (checked by ``tests/test_oracle.py`` against facts other than this code):
+closed forms (N = 1, Q = 0, hand-derived golden example), invariants (row
+probabilities sum to one, constant V, key/value permutation, per-row shift of
+the scores, causal row independence), library routines (PyTorch CPU float64
+``scaled_dot_product_attention`` / ``logsumexp`` / ``softmax``), a separately
+written blockwise online-softmax evaluation, and an exhaustive check of the
+16-bit decoders against PyTorch's conversions.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_ref.c")
+_LIB_PATH = os.path.join(_HERE, "libattn_ref.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``attn_ref.c`` into ``libattn_ref.so`` beside it (gcc, OpenMP)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    base = ["gcc", "-O2", "-std=c99", "-shared", "-fPIC", _SRC, "-o", tmp, "-lm"]
+    try:
+        subprocess.run(base[:2] + ["-fopenmp"] + base[2:], check=True,
+                       capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)  # no OpenMP
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _bind(path: str):
+    lib = ctypes.CDLL(path)
+    c_long, c_int, c_double = ctypes.c_long, ctypes.c_int, ctypes.c_double
+    vp = ctypes.c_void_p
+    lib.attn_ref_fwd_u16.argtypes = [vp, vp, vp, c_int, c_long, c_long,
+                                     c_long, c_long, c_double, c_int,
+                                     vp, vp, c_int]
+    lib.attn_ref_fwd_u16.restype = c_int
+    lib.attn_ref_rows_u16.argtypes = [vp, vp, vp, c_int, c_long, c_long,
+                                      c_long, c_long, c_double, c_int,
+                                      vp, c_long, vp, vp, c_int]
+    lib.attn_ref_rows_u16.restype = c_int
+    lib.attn_ref_fwd_f64.argtypes = [vp, vp, vp, c_long, c_long, c_long,
+                                     c_long, c_double, c_int, vp, vp,
+                                     c_int]
+    lib.attn_ref_fwd_f64.restype = c_int
+    lib.attn_ref_widen.argtypes = [ctypes.c_uint16, c_int]
+    lib.attn_ref_widen.restype = c_double
+    lib.attn_ref_max_threads.argtypes = []
+    lib.attn_ref_max_threads.restype = c_int
+    return lib
+
+
+_override = None
+
+
+def use_library(path: str | None) -> None:
+    """Point this module at another build of ``attn_ref.c`` (None: the default).
+
+    The oracle's own tests use this to plant deliberate mistakes in a copy of
+    the C source and check that the pins catch each one.
+    """
+    global _override
+    with _lock:
+        _override = None if path is None else _bind(path)
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _override is not None:
+            return _override
+        if _lib is None:
+            _lib = _bind(build())
+    return _lib
+
+
+def max_threads() -> int:
+    """Number of OpenMP threads the oracle uses by default."""
+    return int(_load().attn_ref_max_threads())
+
+
+def widen(bits: int, is_bf16: bool) -> float:
+    """Decode one 16-bit word (binary16 or bfloat16) to a Python float."""
+    return float(_load().attn_ref_widen(int(bits) & 0xFFFF, int(bool(is_bf16))))
+
+
+def _u16_view(t) -> tuple[np.ndarray, bool]:
+    """Raw 16-bit words of a CPU torch tensor (float16/bfloat16), C-contiguous."""
+    import torch
+    if t.dtype not in (torch.float16, torch.bfloat16):
+        raise TypeError(f"oracle expects float16/bfloat16 inputs, got {t.dtype}")
+    words = t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    return np.ascontiguousarray(words), t.dtype == torch.bfloat16
+
+
+def _ptr(a: np.ndarray) -> int:
+    return a.ctypes.data
+
+
+def attention(q, k, v, scale: float, causal: bool, nthreads: int = 0):
+    """Full O [B,H,N,d] and LSE [B,H,N] (float64 numpy) for 16-bit CPU tensors."""
+    qw, is_bf16 = _u16_view(q)
+    kw, kb = _u16_view(k)
+    vw, vb = _u16_view(v)
+    if not (is_bf16 == kb == vb):
+        raise TypeError("q, k, v must share one dtype")
+    B, H, N, d = (int(x) for x in q.shape)
+    if tuple(k.shape) != (B, H, N, d) or tuple(v.shape) != (B, H, N, d):
+        raise ValueError("q, k, v must all be [B,H,N,d]")
+    o = np.empty((B, H, N, d), dtype=np.float64)
+    lse = np.empty((B, H, N), dtype=np.float64)
+    rc = _load().attn_ref_fwd_u16(_ptr(qw), _ptr(kw), _ptr(vw), int(is_bf16),
+                                  B, H, N, d, float(scale), int(bool(causal)),
+                                  _ptr(o), _ptr(lse), int(nthreads))
+    if rc != 0:
+        raise RuntimeError("oracle attn_ref_fwd_u16 failed")
+    return o, lse
+
+
+def attention_rows(q, k, v, scale: float, causal: bool, rows, nthreads: int = 0):
+    """O rows [n,d] and LSE [n] (float64) for the listed (b, h, i) triples."""
+    qw, is_bf16 = _u16_view(q)
+    kw, _ = _u16_view(k)
+    vw, _ = _u16_view(v)
+    B, H, N, d = (int(x) for x in q.shape)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 3))
+    n = rows.shape[0]
+    o = np.empty((n, d), dtype=np.float64)
+    lse = np.empty((n,), dtype=np.float64)
+    if n == 0:
+        return o, lse
+    rc = _load().attn_ref_rows_u16(_ptr(qw), _ptr(kw), _ptr(vw), int(is_bf16),
+                                   B, H, N, d, float(scale), int(bool(causal)),
+                                   _ptr(rows), n, _ptr(o), _ptr(lse),
+                                   int(nthreads))
+    if rc != 0:
+        raise RuntimeError("oracle attn_ref_rows_u16 failed")
+    return o, lse
+
+
+def attention_f64(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float,
+                  causal: bool, nthreads: int = 0):
+    """Same definition on float64 numpy inputs [B,H,N,d]."""
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    k = np.ascontiguousarray(k, dtype=np.float64)
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    B, H, N, d = q.shape
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must all be [B,H,N,d]")
+    o = np.empty((B, H, N, d), dtype=np.float64)
+    lse = np.empty((B, H, N), dtype=np.float64)
+    rc = _load().attn_ref_fwd_f64(_ptr(q), _ptr(k), _ptr(v), B, H, N, d,
+                                  float(scale), int(bool(causal)), _ptr(o),
+                                  _ptr(lse), int(nthreads))
+    if rc != 0:
+        raise RuntimeError("oracle attn_ref_fwd_f64 failed")
+    return o, lse

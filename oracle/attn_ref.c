@@ -1,0 +1,271 @@
+/*
+ * attn_ref.c -- the fp64 CPU oracle for the fused attention forward pass.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the plain, slow, obviously correct
+ * definition that the CUDA path is checked against.  Only the tests, the smoke
+ * check and the CPU-baseline leg of the benchmark may load it; the product
+ * library never links, includes or calls it, and it shares no code with it.
+ *
+ * What it computes (for every batch b, head h and query row i):
+ *
+ *   J(i)   = {0 .. N-1}              (full attention)
+ *          = {0 .. i}                (causal: query i sees keys 0..i)
+ *   s_ij   = scale * sum_k q_ik k_jk                      for j in J(i)
+ *   m_i    = max_{j in J(i)} s_ij
+ *   LSE_i  = m_i + ln sum_{j in J(i)} exp(s_ij - m_i)      (natural log)
+ *   O_i    = sum_{j in J(i)} exp(s_ij - LSE_i) v_j
+ *
+ * Sources (the pages this follows):
+ *   - LeetCUDA "flash_attn_mma_tiling_qk.cu", kernel body: the scores are the
+ *     Q.K^T products multiplied by the softmax scale before the exponential
+ *     ("P = Exp(S - m_new)" with S already scaled), the softmax is taken along
+ *     the key axis and the final output is divided by the row sum
+ *     ("O_output = (1/l_final) * O_final").
+ *   - flash-attention "hopper/mainloop_bwd_sm90_tma_gmma_ws.hpp", causal
+ *     masking loop of CollectiveMainloopBwd::mma: a key column is masked when
+ *     it lies past the query row (bottom-right alignment; with one sequence
+ *     length for queries and keys this is "key j allowed iff j <= i"); and
+ *     scale_apply_exp2 against the stored LSE, which shows the LSE is the
+ *     log-normaliser of the *scaled* scores.
+ *   - flash-attention "hopper/flash_fwd_kernel.h", consumer path: a row with
+ *     no admissible key gets O = 0 and LSE = -inf (store_zero).
+ *
+ * The LSE is reported in natural-log units (the Hopper pages keep a base-2
+ * copy for their backward pass; ln 2 times that is the same quantity).
+ *
+ * Inputs are the caller's 16-bit words (IEEE binary16 or bfloat16), widened
+ * exactly to double here; every product, sum and exponential is in double.
+ * The computation is the textbook two-pass softmax per row -- no tiling, no
+ * online recurrence, no reordering beyond the definition above.
+ *
+ * Build: gcc -O2 -fopenmp -shared -fPIC attn_ref.c -o libattn_ref.so -lm
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------ */
+/* 16-bit float decoding, written from the IEEE 754 binary16 and the   */
+/* bfloat16 (upper half of binary32) bit layouts.                      */
+/* ------------------------------------------------------------------ */
+
+/* IEEE binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+static double half_to_double(uint16_t h) {
+    int sign = (h >> 15) & 1;
+    int expo = (h >> 10) & 0x1f;
+    int frac = h & 0x3ff;
+    double mag;
+    if (expo == 0) {
+        mag = ldexp((double)frac, -24);            /* zero or subnormal */
+    } else if (expo == 31) {
+        mag = frac ? NAN : INFINITY;
+    } else {
+        mag = ldexp((double)(1024 + frac), expo - 25);
+    }
+    return sign ? -mag : mag;
+}
+
+/* bfloat16: the upper 16 bits of an IEEE binary32 value. */
+static double bf16_to_double(uint16_t b) {
+    uint32_t bits = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+double attn_ref_widen(uint16_t bits, int is_bf16) {
+    return is_bf16 ? bf16_to_double(bits) : half_to_double(bits);
+}
+
+int attn_ref_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* ------------------------------------------------------------------ */
+/* One query row against one (b,h) slice, all in double.                */
+/*   q_row [d], kmat [N][d], vmat [N][d], scores: scratch of N doubles. */
+/* ------------------------------------------------------------------ */
+static void attend_row(const double *q_row, const double *kmat,
+                       const double *vmat, long N, long d, long i,
+                       double scale, int causal, double *scores,
+                       double *o_row, double *lse_out) {
+    long nkeys = causal ? (i + 1 < N ? i + 1 : N) : N; /* |J(i)| */
+    if (nkeys <= 0) {                 /* no admissible key: O = 0, LSE = -inf */
+        for (long c = 0; c < d; ++c) o_row[c] = 0.0;
+        *lse_out = -INFINITY;
+        return;
+    }
+    /* pass 1: scaled scores and their maximum */
+    double m = -INFINITY;
+    for (long j = 0; j < nkeys; ++j) {
+        const double *k_row = kmat + j * d;
+        double dot = 0.0;
+        for (long c = 0; c < d; ++c) dot += q_row[c] * k_row[c];
+        double s = scale * dot;
+        scores[j] = s;
+        if (s > m) m = s;
+    }
+    /* pass 2: log-normaliser */
+    double sum = 0.0;
+    for (long j = 0; j < nkeys; ++j) sum += exp(scores[j] - m);
+    double lse = m + log(sum);
+    /* pass 3: probability-weighted sum of value rows */
+    for (long c = 0; c < d; ++c) o_row[c] = 0.0;
+    for (long j = 0; j < nkeys; ++j) {
+        double p = exp(scores[j] - lse);
+        const double *v_row = vmat + j * d;
+        for (long c = 0; c < d; ++c) o_row[c] += p * v_row[c];
+    }
+    *lse_out = lse;
+}
+
+static void widen_slice(const uint16_t *src, double *dst, long count,
+                        int is_bf16) {
+    for (long t = 0; t < count; ++t) dst[t] = attn_ref_widen(src[t], is_bf16);
+}
+
+static void set_threads(int nthreads) {
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+}
+
+/*
+ * Full problem on 16-bit inputs.
+ *   q, k, v : [B][H][N][d] 16-bit words; is_bf16 selects the format
+ *   o       : [B][H][N][d] double (written)
+ *   lse     : [B][H][N]    double (written)
+ * Returns 0, or -1 on bad arguments / allocation failure.
+ */
+int attn_ref_fwd_u16(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                     int is_bf16, long B, long H, long N, long d, double scale,
+                     int causal, double *o, double *lse, int nthreads) {
+    if (!q || !k || !v || !o || !lse || B < 0 || H < 0 || N < 0 || d <= 0)
+        return -1;
+    set_threads(nthreads);
+    long slice = N * d;
+    double *qd = (double *)malloc(sizeof(double) * (size_t)(slice > 0 ? slice : 1));
+    double *kd = (double *)malloc(sizeof(double) * (size_t)(slice > 0 ? slice : 1));
+    double *vd = (double *)malloc(sizeof(double) * (size_t)(slice > 0 ? slice : 1));
+    if (!qd || !kd || !vd) { free(qd); free(kd); free(vd); return -1; }
+    int rc = 0;
+    for (long bh = 0; bh < B * H && rc == 0; ++bh) {
+        widen_slice(q + bh * slice, qd, slice, is_bf16);
+        widen_slice(k + bh * slice, kd, slice, is_bf16);
+        widen_slice(v + bh * slice, vd, slice, is_bf16);
+#pragma omp parallel
+        {
+            double *scores = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+            if (!scores) {
+#pragma omp atomic write
+                rc = -1;
+            } else {
+#pragma omp for schedule(dynamic, 4)
+                for (long i = 0; i < N; ++i)
+                    attend_row(qd + i * d, kd, vd, N, d, i, scale, causal,
+                               scores, o + (bh * N + i) * d, lse + bh * N + i);
+                free(scores);
+            }
+        }
+    }
+    free(qd); free(kd); free(vd);
+    return rc;
+}
+
+/*
+ * Selected rows only, for problems too large to evaluate in full.
+ *   rows    : n_rows triples (b, h, i), row-major [n_rows][3]
+ *   o_rows  : [n_rows][d] double (written);  lse_rows: [n_rows] (written)
+ * The K/V slice of each (b,h) is widened once per call and shared by every
+ * requested row of that head.  Returns 0, or -1 on bad arguments.
+ */
+int attn_ref_rows_u16(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                      int is_bf16, long B, long H, long N, long d,
+                      double scale, int causal, const long *rows, long n_rows,
+                      double *o_rows, double *lse_rows, int nthreads) {
+    if (!q || !k || !v || !rows || !o_rows || !lse_rows || N <= 0 || d <= 0)
+        return -1;
+    for (long r = 0; r < n_rows; ++r) {
+        long b = rows[3 * r], h = rows[3 * r + 1], i = rows[3 * r + 2];
+        if (b < 0 || b >= B || h < 0 || h >= H || i < 0 || i >= N) return -1;
+    }
+    set_threads(nthreads);
+    long slice = N * d;
+    double *kd = (double *)malloc(sizeof(double) * (size_t)slice);
+    double *vd = (double *)malloc(sizeof(double) * (size_t)slice);
+    char *done = (char *)calloc((size_t)(n_rows > 0 ? n_rows : 1), 1);
+    if (!kd || !vd || !done) { free(kd); free(vd); free(done); return -1; }
+    int rc = 0;
+    for (long r0 = 0; r0 < n_rows && rc == 0; ++r0) {
+        if (done[r0]) continue;
+        long bh = rows[3 * r0] * H + rows[3 * r0 + 1];
+        widen_slice(k + bh * slice, kd, slice, is_bf16);
+        widen_slice(v + bh * slice, vd, slice, is_bf16);
+#pragma omp parallel
+        {
+            double *scores = (double *)malloc(sizeof(double) * (size_t)N);
+            double *qrow = (double *)malloc(sizeof(double) * (size_t)d);
+            if (!scores || !qrow) {
+#pragma omp atomic write
+                rc = -1;
+            } else {
+#pragma omp for schedule(dynamic, 1)
+                for (long r = r0; r < n_rows; ++r) {
+                    if (done[r] || rows[3 * r] * H + rows[3 * r + 1] != bh)
+                        continue;
+                    long i = rows[3 * r + 2];
+                    widen_slice(q + (bh * N + i) * d, qrow, d, is_bf16);
+                    attend_row(qrow, kd, vd, N, d, i, scale, causal, scores,
+                               o_rows + r * d, lse_rows + r);
+                }
+            }
+            free(scores); free(qrow);
+        }
+        for (long r = r0; r < n_rows; ++r)
+            if (rows[3 * r] * H + rows[3 * r + 1] == bh) done[r] = 1;
+    }
+    free(kd); free(vd); free(done);
+    return rc;
+}
+
+/*
+ * Same definition on double inputs (q, k, v as [B][H][N][d] doubles), for
+ * checks whose inputs are not 16-bit representable.
+ */
+int attn_ref_fwd_f64(const double *q, const double *k, const double *v,
+                     long B, long H, long N, long d, double scale, int causal,
+                     double *o, double *lse, int nthreads) {
+    if (!q || !k || !v || !o || !lse || B < 0 || H < 0 || N < 0 || d <= 0)
+        return -1;
+    set_threads(nthreads);
+    long slice = N * d;
+    int rc = 0;
+    for (long bh = 0; bh < B * H && rc == 0; ++bh) {
+#pragma omp parallel
+        {
+            double *scores = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+            if (!scores) {
+#pragma omp atomic write
+                rc = -1;
+            } else {
+#pragma omp for schedule(dynamic, 4)
+                for (long i = 0; i < N; ++i)
+                    attend_row(q + bh * slice + i * d, k + bh * slice,
+                               v + bh * slice, N, d, i, scale, causal, scores,
+                               o + (bh * N + i) * d, lse + bh * N + i);
+                free(scores);
+            }
+        }
+    }
+    return rc;
+}

@@ -1,0 +1,290 @@
+"""Pins for the fp64 oracle: each check ties it to something other than itself.
+
+Every test here runs on the CPU.  The checks are chosen so that a plausible
+mistake in the oracle (a dropped scale, a wrong sign, swapped Q/K roles, the
+causal mask pointing the wrong way, a missing max subtraction, the LSE in the
+wrong base, a wrong 16-bit decoder) fails at least one of them.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from workloads import make_random_qkv
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_worked.json")
+
+
+def _num(x):
+    """Parse the fixture's closed forms: numbers, 'lnK' and 'a/b'."""
+    if isinstance(x, (int, float)):
+        return float(x)
+    if x.startswith("ln"):
+        return math.log(float(x[2:]))
+    if "/" in x:
+        a, b = x.split("/")
+        return float(a) / float(b)
+    return float(x)
+
+
+def _as4d(rows):
+    return np.asarray(rows, dtype=np.float64)[None, None]
+
+
+# --------------------------------------------------------------------------
+# Closed forms worked by hand (tests/golden/hand_worked.json).
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("path", ["f64", "bf16", "fp16"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_golden_hand_worked(path, causal):
+    with open(GOLDEN) as f:
+        cases = json.load(f)["cases"]
+    for case in cases:
+        scale = _num(case["scale"])
+        q, k, v = (_as4d(case[n]) for n in ("q", "k", "v"))
+        want = case["causal" if causal else "full"]
+        want_o = np.array([[_num(x) for x in r] for r in want["o"]])
+        want_lse = np.array([_num(x) for x in want["lse"]])
+        if path == "f64":
+            o, lse = oracle.attention_f64(q, k, v, scale, causal)
+        else:
+            dt = torch.bfloat16 if path == "bf16" else torch.float16
+            tq, tk, tv = (torch.from_numpy(a).to(dt) for a in (q, k, v))
+            o, lse = oracle.attention(tq, tk, tv, scale, causal)
+        np.testing.assert_allclose(o[0, 0], want_o, rtol=0, atol=1e-12,
+                                   err_msg=case["name"])
+        np.testing.assert_allclose(lse[0, 0], want_lse, rtol=0, atol=1e-12,
+                                   err_msg=case["name"])
+
+
+# --------------------------------------------------------------------------
+# The 16-bit decoders, exhaustively, against PyTorch's own conversions.
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+def test_decoder_exhaustive(dtype):
+    words = torch.arange(0, 65536, dtype=torch.int32).to(torch.int16)
+    ref = words.view(dtype).to(torch.float64).numpy()
+    is_bf16 = dtype == torch.bfloat16
+    got = np.array([oracle.widen(w, is_bf16) for w in range(65536)])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+# --------------------------------------------------------------------------
+# Library routines: PyTorch CPU float64 attention, logsumexp, softmax.
+# --------------------------------------------------------------------------
+def _torch_ref(q, k, v, scale, causal):
+    qt, kt, vt = (torch.from_numpy(np.asarray(a, dtype=np.float64)) for a in (q, k, v))
+    o = torch.nn.functional.scaled_dot_product_attention(
+        qt, kt, vt, is_causal=causal, scale=scale)
+    s = scale * torch.matmul(qt, kt.transpose(-1, -2))
+    if causal:
+        n = s.shape[-1]
+        mask = torch.ones(n, n, dtype=torch.bool).triu(1)
+        s = s.masked_fill(mask, float("-inf"))
+    return o.numpy(), torch.logsumexp(s, dim=-1).numpy()
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 1, 4), (1, 2, 7, 8), (2, 3, 33, 16),
+                                   (1, 1, 130, 64)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_matches_torch_sdpa_f64(shape, causal):
+    rng = np.random.default_rng(7)
+    q, k, v = (rng.standard_normal(shape) for _ in range(3))
+    scale = 0.37
+    o, lse = oracle.attention_f64(q, k, v, scale, causal)
+    o_ref, lse_ref = _torch_ref(q, k, v, scale, causal)
+    np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_ref, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("causal", [False, True])
+def test_matches_torch_sdpa_16bit(dtype, causal):
+    q, k, v = make_random_qkv(2, 2, 45, 32, dtype, seed=11)
+    scale = 1 / math.sqrt(32)
+    o, lse = oracle.attention(q, k, v, scale, causal)
+    o_ref, lse_ref = _torch_ref(q.double().numpy(), k.double().numpy(),
+                                v.double().numpy(), scale, causal)
+    np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_ref, rtol=0, atol=1e-12)
+
+
+def test_large_scores_no_overflow():
+    """Scores near 1e3 overflow exp() unless the row maximum is subtracted."""
+    rng = np.random.default_rng(3)
+    q = rng.standard_normal((1, 1, 20, 8)) * 30
+    k = rng.standard_normal((1, 1, 20, 8)) * 30
+    v = rng.standard_normal((1, 1, 20, 8))
+    o, lse = oracle.attention_f64(q, k, v, 1.0, False)
+    o_ref, lse_ref = _torch_ref(q, k, v, 1.0, False)
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_ref, rtol=1e-14, atol=0)
+
+
+# --------------------------------------------------------------------------
+# Invariants of the definition.
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("causal", [False, True])
+def test_probabilities_sum_to_one(causal):
+    """V = identity makes O_i the probability row P_i itself."""
+    n = 24
+    rng = np.random.default_rng(5)
+    q = rng.standard_normal((1, 1, n, n))
+    k = rng.standard_normal((1, 1, n, n))
+    v = np.eye(n)[None, None]
+    scale = 0.5
+    p, lse = oracle.attention_f64(q, k, v, scale, causal)
+    np.testing.assert_allclose(p.sum(-1), 1.0, rtol=0, atol=1e-12)
+    assert (p >= 0).all()
+    s = scale * torch.from_numpy(q[0, 0]) @ torch.from_numpy(k[0, 0]).T
+    if causal:
+        s = s.masked_fill(torch.ones(n, n, dtype=torch.bool).triu(1), float("-inf"))
+    np.testing.assert_allclose(p[0, 0], torch.softmax(s, -1).numpy(), rtol=0,
+                               atol=1e-12)
+    if causal:
+        assert np.all(np.triu(p[0, 0], 1) == 0.0)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_constant_values(causal):
+    q, k, _ = make_random_qkv(1, 2, 40, 16, torch.bfloat16, seed=21)
+    v = torch.full_like(q, 1.75)
+    o, _ = oracle.attention(q, k, v, 0.25, causal)
+    np.testing.assert_allclose(o, 1.75, rtol=0, atol=1e-12)
+
+
+def test_causal_row_zero():
+    q, k, v = make_random_qkv(2, 2, 19, 16, torch.float16, seed=22)
+    scale = 0.3
+    o, lse = oracle.attention(q, k, v, scale, True)
+    np.testing.assert_array_equal(o[:, :, 0, :], v[:, :, 0, :].double().numpy())
+    want = scale * (q[:, :, 0, :].double() * k[:, :, 0, :].double()).sum(-1)
+    np.testing.assert_allclose(lse[:, :, 0], want.numpy(), rtol=0, atol=1e-13)
+
+
+def test_causal_row_independent_of_later_keys():
+    q, k, v = make_random_qkv(1, 1, 32, 16, torch.bfloat16, seed=23)
+    o1, l1 = oracle.attention(q, k, v, 0.25, True)
+    k2, v2 = k.clone(), v.clone()
+    k2[:, :, 20:] = -k2[:, :, 20:] * 3
+    v2[:, :, 20:] = 5.0
+    o2, l2 = oracle.attention(q, k2, v2, 0.25, True)
+    np.testing.assert_array_equal(o1[:, :, :20], o2[:, :, :20])
+    np.testing.assert_array_equal(l1[:, :, :20], l2[:, :, :20])
+    assert not np.allclose(o1[:, :, 20:], o2[:, :, 20:])
+
+
+def test_key_value_permutation_invariance():
+    q, k, v = make_random_qkv(1, 2, 50, 32, torch.bfloat16, seed=24)
+    perm = torch.randperm(50, generator=torch.Generator().manual_seed(1))
+    o1, l1 = oracle.attention(q, k, v, 0.2, False)
+    o2, l2 = oracle.attention(q, k[:, :, perm], v[:, :, perm], 0.2, False)
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-12)
+
+
+def test_score_shift():
+    """Adding u to every key adds scale*q_i.u to row i: O fixed, LSE shifted."""
+    rng = np.random.default_rng(9)
+    q = rng.standard_normal((1, 1, 30, 8))
+    k = rng.standard_normal((1, 1, 30, 8))
+    v = rng.standard_normal((1, 1, 30, 8))
+    u = rng.standard_normal(8)
+    scale = 0.7
+    for causal in (False, True):
+        o1, l1 = oracle.attention_f64(q, k, v, scale, causal)
+        o2, l2 = oracle.attention_f64(q, k + u, v, scale, causal)
+        np.testing.assert_allclose(o2, o1, rtol=0, atol=1e-12)
+        np.testing.assert_allclose((l2 - l1)[0, 0], scale * q[0, 0] @ u, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_zero_queries_closed_form(causal):
+    """Q = 0: uniform weights, O_i = mean of admissible v_j, LSE_i = ln |J(i)|."""
+    n, d = 37, 8
+    rng = np.random.default_rng(4)
+    q = np.zeros((1, 1, n, d))
+    k = rng.standard_normal((1, 1, n, d))
+    v = rng.standard_normal((1, 1, n, d))
+    o, lse = oracle.attention_f64(q, k, v, 1.3, causal)
+    for i in range(n):
+        cnt = i + 1 if causal else n
+        np.testing.assert_allclose(o[0, 0, i], v[0, 0, :cnt].mean(0), rtol=0, atol=1e-13)
+        assert abs(lse[0, 0, i] - math.log(cnt)) < 1e-13
+
+
+def test_single_key_closed_form():
+    """N = 1: O = V and LSE = scale * q.k, whatever the mask."""
+    q, k, v = make_random_qkv(3, 2, 1, 64, torch.float16, seed=25)
+    for causal in (False, True):
+        o, lse = oracle.attention(q, k, v, 0.125, causal)
+        np.testing.assert_array_equal(o, v.double().numpy())
+        want = 0.125 * (q.double() * k.double()).sum(-1)
+        np.testing.assert_allclose(lse, want.numpy(), rtol=0, atol=1e-13)
+
+
+# --------------------------------------------------------------------------
+# Brute force by a different route: blockwise online softmax (test-only).
+# --------------------------------------------------------------------------
+def _online_softmax_attention(q, k, v, scale, causal, block=7):
+    """Separately written tiled evaluation with a running max and sum."""
+    B, H, N, d = q.shape
+    o = np.zeros((B, H, N, d))
+    lse = np.zeros((B, H, N))
+    for b in range(B):
+        for h in range(H):
+            for i in range(N):
+                run_max, run_sum = -np.inf, 0.0
+                acc = np.zeros(d)
+                last = i if causal else N - 1
+                for j0 in range(0, last + 1, block):
+                    j1 = min(j0 + block, last + 1)
+                    sc = scale * (k[b, h, j0:j1] @ q[b, h, i])
+                    new_max = max(run_max, sc.max())
+                    corr = math.exp(run_max - new_max) if run_max > -np.inf else 0.0
+                    w = np.exp(sc - new_max)
+                    acc = acc * corr + w @ v[b, h, j0:j1]
+                    run_sum = run_sum * corr + w.sum()
+                    run_max = new_max
+                o[b, h, i] = acc / run_sum
+                lse[b, h, i] = run_max + math.log(run_sum)
+    return o, lse
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_matches_online_softmax(causal):
+    q, k, v = make_random_qkv(1, 2, 29, 16, torch.bfloat16, seed=26, qk_mult=2.0)
+    qd, kd, vd = (t.double().numpy() for t in (q, k, v))
+    o, lse = oracle.attention(q, k, v, 0.25, causal)
+    o2, l2 = _online_softmax_attention(qd, kd, vd, 0.25, causal)
+    np.testing.assert_allclose(o, o2, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, l2, rtol=0, atol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# The row-sampling entry agrees with the full evaluation.
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("causal", [False, True])
+def test_rows_match_full(causal):
+    q, k, v = make_random_qkv(2, 3, 70, 32, torch.bfloat16, seed=27)
+    o, lse = oracle.attention(q, k, v, 0.17, causal)
+    rows = [(0, 0, 0), (1, 2, 69), (0, 1, 33), (1, 0, 5), (0, 0, 64)]
+    o_r, l_r = oracle.attention_rows(q, k, v, 0.17, causal, rows)
+    for t, (b, h, i) in enumerate(rows):
+        np.testing.assert_array_equal(o_r[t], o[b, h, i])
+        assert l_r[t] == lse[b, h, i]
+
+
+def test_bad_arguments_rejected():
+    q, k, v = make_random_qkv(1, 1, 8, 16, torch.bfloat16, seed=28)
+    with pytest.raises(RuntimeError):
+        oracle.attention_rows(q, k, v, 0.1, False, [(0, 0, 8)])
+    with pytest.raises(TypeError):
+        oracle.attention(q.float(), k, v, 0.1, False)

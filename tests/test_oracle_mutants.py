@@ -1,0 +1,90 @@
+"""Planted mistakes: each mutant copy of the oracle must fail at least one pin.
+
+A copy of ``oracle/attn_ref.c`` is edited in a temporary directory (one
+plausible slip per mutant), compiled with gcc, swapped in through
+``oracle.use_library`` and run through the pins of ``test_oracle.py``.  The
+real oracle source is never modified.  CPU only.
+"""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import test_oracle as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "attn_ref.c")
+
+MUTANTS = {
+    "scale_dropped": ("double s = scale * dot;", "double s = dot;"),
+    "score_sign": ("double s = scale * dot;", "double s = -scale * dot;"),
+    "values_as_keys": ("const double *k_row = kmat + j * d;",
+                       "const double *k_row = vmat + j * d;"),
+    "causal_reversed": ("long nkeys = causal ? (i + 1 < N ? i + 1 : N) : N;",
+                        "long nkeys = causal ? N - i : N;"),
+    "causal_no_diagonal": ("long nkeys = causal ? (i + 1 < N ? i + 1 : N) : N;",
+                           "long nkeys = causal ? (i < N ? (i > 0 ? i : 1) : N) : N;"),
+    "lse_base2": ("double lse = m + log(sum);", "double lse = m + log2(sum);"),
+    "lse_without_max": ("double lse = m + log(sum);", "double lse = log(sum);"),
+    "no_max_subtraction": ("sum += exp(scores[j] - m);", "sum += exp(scores[j]);"),
+    "unnormalised_output": ("double p = exp(scores[j] - lse);",
+                            "double p = exp(scores[j] - m);"),
+    "bf16_decoder_shift": ("uint32_t bits = (uint32_t)b << 16;",
+                           "uint32_t bits = (uint32_t)b << 15;"),
+    "half_decoder_bias": ("expo - 25", "expo - 24"),
+}
+
+PIN_CALLS = [
+    (pins.test_golden_hand_worked, dict(path="f64", causal=False)),
+    (pins.test_golden_hand_worked, dict(path="f64", causal=True)),
+    (pins.test_golden_hand_worked, dict(path="bf16", causal=True)),
+    (pins.test_golden_hand_worked, dict(path="fp16", causal=False)),
+    (pins.test_decoder_exhaustive, dict(dtype=pins.torch.float16)),
+    (pins.test_decoder_exhaustive, dict(dtype=pins.torch.bfloat16)),
+    (pins.test_matches_torch_sdpa_f64, dict(shape=(2, 3, 33, 16), causal=False)),
+    (pins.test_matches_torch_sdpa_f64, dict(shape=(2, 3, 33, 16), causal=True)),
+    (pins.test_large_scores_no_overflow, {}),
+    (pins.test_probabilities_sum_to_one, dict(causal=True)),
+    (pins.test_causal_row_zero, {}),
+    (pins.test_zero_queries_closed_form, dict(causal=True)),
+    (pins.test_single_key_closed_form, {}),
+]
+
+
+def _build_mutant(tmp_path, old, new):
+    with open(SRC) as f:
+        text = f.read()
+    assert text.count(old) >= 1, f"mutation anchor not found: {old!r}"
+    src = tmp_path / "attn_ref_mutant.c"
+    src.write_text(text.replace(old, new))
+    lib = tmp_path / "libattn_ref_mutant.so"
+    subprocess.run(["gcc", "-O1", "-std=c99", "-shared", "-fPIC", str(src), "-o",
+                    str(lib), "-lm"], check=True, capture_output=True)
+    return str(lib)
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    path = _build_mutant(tmp_path, old, new)
+    caught = []
+    oracle.use_library(path)
+    try:
+        for fn, kwargs in PIN_CALLS:
+            try:
+                fn(**kwargs)
+            except AssertionError:
+                caught.append(fn.__name__)
+    finally:
+        oracle.use_library(None)
+    assert caught, f"mutant {name!r} passed every pin"
+
+
+def test_unmutated_copy_passes_every_pin(tmp_path):
+    path = _build_mutant(tmp_path, "double s = scale * dot;", "double s = scale * dot;")
+    oracle.use_library(path)
+    try:
+        for fn, kwargs in PIN_CALLS:
+            fn(**kwargs)
+    finally:
+        oracle.use_library(None)
