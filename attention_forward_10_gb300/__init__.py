@@ -1,0 +1,167 @@
+"""GB300 (sm_103a) fused attention forward: thin Python binding of libfa_gb300.so.
+
+Every entry point of the C ABI (``include/fa.h``) is exposed here under the
+same name with plain-integer arguments (device pointers, sizes, a CUDA stream
+handle); the binding only marshals arguments.  ``fwd()`` is the PyTorch
+convenience on top: it allocates O and LSE with torch on the inputs' device
+and passes ``data_ptr()`` values and the current stream to ``fa_fwd``.
+
+All compute runs in the library's CUDA kernels.  There is no fallback: the
+library is loaded on the first call, and if it has not been built that call
+raises ImportError.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfa_gb300.so")
+
+FA_DTYPE_F16 = 0
+FA_DTYPE_BF16 = 1
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_MISALIGNED = 3
+FA_ERR_CUDA = 4
+FA_ERR_DEVICE_TIMEOUT = 5
+
+# Every exported symbol of include/fa.h, with its ctypes signature.
+_vp, _i, _f, _ll = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_longlong
+SIGNATURES = {
+    "fa_fwd": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _vp], _i),
+    "fa_status_string": ([_i], ctypes.c_char_p),
+    "fa_get_device_status": ([_vp, ctypes.POINTER(_i)], _i),
+    "fa_set_wait_timeout_us": ([_ll], _i),
+    "fa_set_max_ctas": ([_i], _i),
+    "fa_selftest_watchdog": ([_ll, _vp], _i),
+    "fa_num_sms": ([], _i),
+}
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {fa_status_string(status)} ({status})")
+
+
+_lib_handle = None
+
+
+def _load():
+    global _lib_handle
+    if _lib_handle is not None:
+        return _lib_handle
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it first with "
+            "`python -c 'import __graft_entry__ as g; g.build()'` "
+            "(or attention_forward_10_gb300/build.py); there is no fallback path")
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, (args, res) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib_handle = lib
+    return lib
+
+
+class _LazyLib:
+    def __getattr__(self, name):
+        return getattr(_load(), name)
+
+
+_lib = _LazyLib()
+
+
+# ---------------------------------------------------------------- raw C ABI
+def fa_fwd(q: int, k: int, v: int, o: int, lse: int | None, B: int, H: int, N: int,
+           d: int, scale: float, causal: int, dtype: int, stream: int | None) -> int:
+    return int(_lib.fa_fwd(q, k, v, o, lse or None, B, H, N, d, scale, causal, dtype,
+                           stream or None))
+
+
+def fa_status_string(status: int) -> str:
+    return _lib.fa_status_string(int(status)).decode()
+
+
+def fa_get_device_status(stream: int | None = None) -> tuple[int, int]:
+    """(status, site) after synchronising ``stream``; clears the status word."""
+    site = ctypes.c_int(0)
+    st = int(_lib.fa_get_device_status(stream or None, ctypes.byref(site)))
+    return st, int(site.value)
+
+
+def fa_set_wait_timeout_us(timeout_us: int) -> int:
+    return int(_lib.fa_set_wait_timeout_us(int(timeout_us)))
+
+
+def fa_set_max_ctas(max_ctas: int) -> int:
+    return int(_lib.fa_set_max_ctas(int(max_ctas)))
+
+
+def fa_selftest_watchdog(timeout_us: int, stream: int | None = None) -> int:
+    return int(_lib.fa_selftest_watchdog(int(timeout_us), stream or None))
+
+
+def fa_num_sms() -> int:
+    return int(_lib.fa_num_sms())
+
+
+# ------------------------------------------------------- torch convenience
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float16:
+        return FA_DTYPE_F16
+    if t.dtype == torch.bfloat16:
+        return FA_DTYPE_BF16
+    raise TypeError(f"q/k/v must be float16 or bfloat16, got {t.dtype}")
+
+
+def fwd(q, k, v, *, scale: float | None = None, causal: bool = False,
+        out=None, lse=None, return_lse: bool = True, stream=None):
+    """Attention forward on CUDA tensors q, k, v of shape [B, H, N, d].
+
+    Returns ``(o, lse)``: o in the input dtype [B,H,N,d], lse float32 [B,H,N]
+    (natural-log log-sum-exp of the scaled scores; None if ``return_lse`` is
+    False).  ``scale`` defaults to 1/sqrt(d).  Runs on ``stream`` (default:
+    torch's current stream of the inputs' device) and does not synchronise.
+    """
+    import torch
+    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must share one [B, H, N, d] shape")
+    if not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise ValueError("q, k, v must be CUDA tensors (no CPU path)")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k, v must share one dtype")
+    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("q, k, v must be contiguous")
+    B, H, N, d = (int(x) for x in q.shape)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if return_lse and lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    with torch.cuda.device(q.device):
+        st = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                    lse.data_ptr() if (return_lse and lse is not None) else None,
+                    B, H, N, d, float(scale), int(bool(causal)), _dtype_code(q), handle)
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd")
+    return out, (lse if return_lse else None)
+
+
+__all__ = [
+    "LIB_PATH", "SIGNATURES", "FaError", "fwd", "fa_fwd", "fa_status_string",
+    "fa_get_device_status", "fa_set_wait_timeout_us", "fa_set_max_ctas",
+    "fa_selftest_watchdog", "fa_num_sms",
+    "FA_DTYPE_F16", "FA_DTYPE_BF16", "FA_OK", "FA_ERR_INVALID_ARG",
+    "FA_ERR_UNSUPPORTED", "FA_ERR_MISALIGNED", "FA_ERR_CUDA", "FA_ERR_DEVICE_TIMEOUT",
+]

@@ -1,0 +1,249 @@
+// fa_api.cu -- the C ABI of libfa_gb300.so: argument validation, TMA tensor
+// maps, persistent-grid sizing and the launch.  Declarations and the full
+// contract are in include/fa.h.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "fa.h"
+#include "fa_fwd_kernel.cuh"
+#include "fa_launch.h"
+
+namespace fa {
+
+// Device status word: the kernels' bounded waits record a timeout here.
+__device__ int g_status_word;
+
+int fwd_smem_bytes(int d) {
+  return d == 64 ? static_cast<int>(Layout<64>::kSmemBytes)
+                 : static_cast<int>(Layout<128>::kSmemBytes);
+}
+
+// One CTA waits on a barrier nobody arrives on; the bounded wait must give
+// up, record the timeout and return.
+__global__ void fa_watchdog_selftest_kernel(int* status, unsigned long long timeout_ns) {
+  __shared__ __align__(8) uint64_t bar_storage;
+  __shared__ int abort_storage;
+  const uint32_t b = smem_u32(&bar_storage);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    abort_storage = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const Ctl ctl{reinterpret_cast<volatile int*>(&abort_storage), status, timeout_ns};
+    wait_bar(b, 0, ctl, kSiteSelftest);
+  }
+  __syncthreads();
+}
+
+cudaError_t launch_watchdog_selftest(int* status, unsigned long long timeout_ns,
+                                     cudaStream_t stream) {
+  fa_watchdog_selftest_kernel<<<1, 32, 0, stream>>>(status, timeout_ns);
+  return cudaGetLastError();
+}
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
+std::atomic<int> g_max_ctas{0};
+
+struct DeviceInfo {
+  std::once_flag once;
+  int ok = 0;           // 1: usable sm_103 device
+  int num_sms = 0;
+  int* status = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+
+// Per-device set-up with that device current: capability check, SM count and
+// the device address of the status word.
+DeviceInfo* device_info(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  DeviceInfo& info = g_dev[dev];
+  std::call_once(info.once, [&] {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return;
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess) return;
+    info.num_sms = sms;
+    info.status = static_cast<int*>(addr);
+    info.ok = (major == 10 && minor == 3) ? 1 : 0;
+  });
+  return &info;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      ptr = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }();
+  return fn;
+}
+
+// 4-D view of a contiguous [BH][N][d] 16-bit tensor for 128-byte-swizzled
+// tiles: dim0 = 64 elements (128 B, innermost), dim1 = N rows (stride d*2 B),
+// dim2 = d/64 column blocks (stride 128 B), dim3 = BH heads (stride N*d*2 B).
+// A box {64, 128, d/64, 1} lands in shared memory as [d/64][128][64], the
+// K-major layout the MMA descriptors expect; rows past N read as zero and
+// are not written by stores.
+bool encode_qkvo_map(CUtensorMap* map, const void* base, int N, int d, int bh,
+                     bool bf16) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(d / 64),
+                        static_cast<cuuint64_t>(bh)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2, 128,
+                           static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
+  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(kBlockM),
+                       static_cast<cuuint32_t>(d / 64), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                  4, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned(const void* ptr, uintptr_t a) {
+  return (reinterpret_cast<uintptr_t>(ptr) % a) == 0;
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" {
+
+const char* fa_status_string(int status) {
+  switch (status) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+    case FA_ERR_MISALIGNED: return "FA_ERR_MISALIGNED";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA";
+    case FA_ERR_DEVICE_TIMEOUT: return "FA_ERR_DEVICE_TIMEOUT";
+    default: return "FA_ERR_UNKNOWN";
+  }
+}
+
+int fa_set_wait_timeout_us(long long timeout_us) {
+  if (timeout_us < 1) return FA_ERR_INVALID_ARG;
+  fa::g_timeout_ns.store(static_cast<unsigned long long>(timeout_us) * 1000ull);
+  return FA_OK;
+}
+
+int fa_set_max_ctas(int max_ctas) {
+  if (max_ctas < 0) return FA_ERR_INVALID_ARG;
+  fa::g_max_ctas.store(max_ctas);
+  return FA_OK;
+}
+
+int fa_num_sms(void) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  fa::DeviceInfo* info = fa::device_info(dev);
+  return (info != nullptr && info->num_sms > 0) ? info->num_sms : -1;
+}
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+           int N, int d, float scale, int causal, int dtype, void* stream) {
+  using namespace fa;
+  if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_DTYPE_F16 && dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (B == 0 || H == 0 || N == 0) return FA_OK;
+  if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return FA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
+    return FA_ERR_MISALIGNED;
+  if (lse != nullptr && !aligned(lse, 4)) return FA_ERR_MISALIGNED;
+  const long long bh = static_cast<long long>(B) * H;
+  const long long pairs = (static_cast<long long>(N) + kRowsPerUnit - 1) / kRowsPerUnit;
+  if (bh >= (1ll << 31) || bh * pairs >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  DeviceInfo* info = device_info(dev);
+  if (info == nullptr || info->status == nullptr) return FA_ERR_CUDA;
+  if (!info->ok) return FA_ERR_UNSUPPORTED;
+
+  const bool bf16 = dtype == FA_DTYPE_BF16;
+  FaParams p;
+  if (!encode_qkvo_map(&p.tm_q, q, N, d, static_cast<int>(bh), bf16) ||
+      !encode_qkvo_map(&p.tm_k, k, N, d, static_cast<int>(bh), bf16) ||
+      !encode_qkvo_map(&p.tm_v, v, N, d, static_cast<int>(bh), bf16) ||
+      !encode_qkvo_map(&p.tm_o, o, N, d, static_cast<int>(bh), bf16))
+    return FA_ERR_CUDA;
+  p.lse = lse;
+  p.status = info->status;
+  p.timeout_ns = g_timeout_ns.load();
+  p.N = N;
+  p.num_bh = static_cast<int>(bh);
+  p.num_pairs = static_cast<int>(pairs);
+  p.num_units = static_cast<int>(bh * pairs);
+  p.n_ktiles = (N + kBlockN - 1) / kBlockN;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+
+  int grid = info->num_sms;
+  const int cap = g_max_ctas.load();
+  if (cap > 0 && cap < grid) grid = cap;
+  if (p.num_units < grid) grid = p.num_units;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = (d == 64) ? launch_fwd_d64(p, causal != 0, bf16, grid, s)
+                            : launch_fwd_d128(p, causal != 0, bf16, grid, s);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_get_device_status(void* stream, int* site) {
+  using namespace fa;
+  if (site != nullptr) *site = 0;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FA_ERR_CUDA;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  DeviceInfo* info = device_info(dev);
+  if (info == nullptr || info->status == nullptr) return FA_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpy(&word, info->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return FA_ERR_CUDA;
+  if (word == 0) return FA_OK;
+  const int zero = 0;
+  if (cudaMemcpy(info->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+    return FA_ERR_CUDA;
+  if (site != nullptr) *site = word >> 8;
+  return word & 0xff;
+}
+
+int fa_selftest_watchdog(long long timeout_us, void* stream) {
+  using namespace fa;
+  if (timeout_us < 1) return FA_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  DeviceInfo* info = device_info(dev);
+  if (info == nullptr || info->status == nullptr) return FA_ERR_CUDA;
+  if (!info->ok) return FA_ERR_UNSUPPORTED;
+  cudaError_t e = launch_watchdog_selftest(
+      info->status, static_cast<unsigned long long>(timeout_us) * 1000ull,
+      static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,416 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 attention forward (one JSON line on stdout).
+
+Default workload: B=4, H=16, N=2048, d=128, bf16, full (non-causal) attention,
+scale 1/sqrt(128) -- the headline configuration of the metric.  A step is one
+full forward pass (one launch of the persistent kernel) over that batch.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload I]
+                  [--impl ours|reference]
+
+Timing: W >= 3 untimed warm-up steps, then exactly K steps on the launching
+stream bracketed by CUDA events, with a barrier + synchronize on both sides;
+inputs rotate over enough copies (> 2x the 129 MB L2) that no step reads
+another step's inputs from L2.  Under torchrun every rank runs an independent
+replica on its own GPU (the forward pass has no cross-GPU exchange); the
+reported value is all ranks' FLOPs over the slowest rank's time.
+
+``--impl reference`` times the fp64 CPU oracle (the only other place this
+script runs it) on rank 0, on bounded row samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("attention fwd TFLOP/s (4·B·H·N²·d, ×½ causal) and % of GB300 BF16 "
+          "tensor peak")
+UNIT = "TFLOP/s"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
+                  "bf16_tflops_sustained": 1700.0}
+
+
+def _dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def _kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "attention_forward_10_gb300", "csrc")
+    for f in sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh"))
+                    + glob.glob(os.path.join(csrc, "*.h"))):
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _profiled_traffic(wl_name: str):
+    """DRAM bytes per launch from the committed ncu summary, if still current.
+
+    The summary records the kernel-source hash it was captured with; once the
+    kernel changes the figure no longer applies and None is returned.
+    """
+    for path in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
+        with open(path) as f:
+            text = f.read()
+        m_w = re.search(r"^workload:\s*(\S+)", text, re.M)
+        m_h = re.search(r"^kernel_source_hash:\s*(\S+)", text, re.M)
+        m_t = re.search(r"^dram_bytes_per_launch:\s*([0-9.eE+]+)", text, re.M)
+        if m_w and m_h and m_t and m_w.group(1) == wl_name:
+            if m_h.group(1) == _kernel_source_hash():
+                return float(m_t.group(1)), os.path.relpath(path, ROOT)
+            return None, os.path.relpath(path, ROOT) + " (stale: kernel changed)"
+    return None, None
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms in the background (host timestamps)."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.samples = []
+        self.proc = None
+        self.error = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if gpu_id is not None:
+            cmd += ["-i", gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except OSError as e:
+            self.error = str(e)
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "note": f"nvidia-smi unavailable: {self.error}"}
+        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
+        note = "sampled during the timed region"
+        if not inside:
+            inside = [p for (_, p) in self.samples]
+            note = "timed region shorter than one sample; all samples of the run"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "no samples"}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for p in inside if num(p[1]) is not None]
+        mx = [num(p[2]) for p in inside if num(p[2]) is not None]
+        pw = [num(p[3]) for p in inside if num(p[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in inside for i in range(4)
+                          if p[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None,
+                "reasons": reasons, "samples": len(inside), "note": note}
+
+
+def _gpu_id_for_smi(torch, dev_index: int):
+    try:
+        props = torch.cuda.get_device_properties(dev_index)
+        dom = getattr(props, "pci_domain_id", None)
+        bus = getattr(props, "pci_bus_id", None)
+        devn = getattr(props, "pci_device_id", None)
+        if bus is not None and devn is not None:
+            return f"{dom or 0:08X}:{bus:02X}:{devn:02X}.0"
+    except Exception:
+        pass
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    ids = [x for x in vis.split(",") if x.strip()]
+    if ids and dev_index < len(ids) and ids[dev_index].strip().isdigit():
+        return ids[dev_index].strip()
+    return None
+
+
+def _cpu_baseline(wl, budget_s: float = 12.0):
+    """Time the fp64 oracle on whole heads of the workload, about `budget_s`."""
+    import oracle
+    from workloads import make_qkv
+    q, k, v = make_qkv(wl)
+    per_row = 4.0 * wl.N * wl.d * (0.5 if wl.causal else 1.0)
+    # calibrate on 64 rows of head (0,0), then size the sample to the budget
+    probe = [(0, 0, i) for i in range(0, wl.N, max(1, wl.N // 64))][:64]
+    t0 = time.perf_counter()
+    oracle.attention_rows(q, k, v, wl.scale, wl.causal, probe)
+    rate = len(probe) * per_row / max(time.perf_counter() - t0, 1e-6)
+    n_rows = int(min(wl.B * wl.H * wl.N, max(256, budget_s * rate / per_row)))
+    rows = []
+    for bh in range(wl.B * wl.H):
+        b, h = divmod(bh, wl.H)
+        for i in range(wl.N):
+            rows.append((b, h, i))
+            if len(rows) >= n_rows:
+                break
+        if len(rows) >= n_rows:
+            break
+    t0 = time.perf_counter()
+    oracle.attention_rows(q, k, v, wl.scale, wl.causal, rows)
+    dt = time.perf_counter() - t0
+    flops = sum(4.0 * wl.d * ((i + 1) if wl.causal else wl.N) for (_, _, i) in rows)
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": f"{len(rows)} query rows (first rows of heads in order) of "
+                      f"{wl.describe()}, fp64, {dt:.1f} s"}
+
+
+def run_reference(args, wl):
+    rank, world, _ = _dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    from workloads import make_qkv
+    q, k, v = make_qkv(wl)
+    rows_per_step = 128
+    rng = __import__("random").Random(1234)
+    step_rows = []
+    for s in range(args.warmup + args.steps):
+        step_rows.append([(rng.randrange(wl.B), rng.randrange(wl.H), rng.randrange(wl.N))
+                          for _ in range(rows_per_step)])
+    for s in range(args.warmup):
+        oracle.attention_rows(q, k, v, wl.scale, wl.causal, step_rows[s])
+    flops = 0.0
+    t0 = time.perf_counter()
+    for s in range(args.warmup, args.warmup + args.steps):
+        oracle.attention_rows(q, k, v, wl.scale, wl.causal, step_rows[s])
+        flops += sum(4.0 * wl.d * ((i + 1) if wl.causal else wl.N)
+                     for (_, _, i) in step_rows[s])
+    dt = time.perf_counter() - t0
+    value = flops / dt / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": _config(wl, "host cores, fp64 oracle"),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(),
+                         "kind": "oracle",
+                         "sample": f"{rows_per_step} seeded random query rows per step of "
+                                   f"{wl.describe()}"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _config(wl, l2_note):
+    return {"workload": f"{wl.name}: {wl.describe()}, scale=1/sqrt(d)", "B": wl.B,
+            "H": wl.H, "N": wl.N, "d": wl.d, "causal": wl.causal,
+            "input_dtype": wl.dtype, "l2": l2_note, "parallelism": "replicas"}
+
+
+def run_ours(args, wl):
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = _dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    dev = torch.device(f"cuda:{local}" if world > 1 else "cuda:0")
+    torch.cuda.set_device(dev)
+
+    import attention_forward_10_gb300 as fa
+    from workloads import make_qkv
+
+    fa.fa_set_max_ctas(0)
+    warmup = max(3, args.warmup)
+    q, k, v = make_qkv(wl)
+    B, H, N, d = wl.B, wl.H, wl.N, wl.d
+    set_bytes = 4 * q.numel() * q.element_size() + B * H * N * 4
+    n_sets = max(1, min(8, math.ceil(2.2 * L2_BYTES / set_bytes)))
+    sets = []
+    for i in range(n_sets):
+        qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+        if i > 0:   # distinct copies (same values) so that no step hits L2
+            qd, kd, vd = qd.clone(), kd.clone(), vd.clone()
+        sets.append((qd, kd, vd, torch.empty_like(qd),
+                     torch.empty((B, H, N), dtype=torch.float32, device=dev)))
+    stream = torch.cuda.Stream(device=dev)
+    handle = stream.cuda_stream
+    dcode = fa.FA_DTYPE_BF16 if wl.dtype == "bf16" else fa.FA_DTYPE_F16
+
+    def step(i):
+        qd, kd, vd, od, ld = sets[i % n_sets]
+        st = fa.fa_fwd(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), od.data_ptr(),
+                       ld.data_ptr(), B, H, N, d, wl.scale, int(wl.causal), dcode, handle)
+        if st != fa.FA_OK:
+            raise RuntimeError(f"fa_fwd failed: {fa.fa_status_string(st)}")
+
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            step(i)
+    stream.synchronize()
+    st, site = fa.fa_get_device_status(handle)
+    if st != fa.FA_OK:
+        raise RuntimeError(f"device status {fa.fa_status_string(st)} (site {site})")
+
+    sampler = ClockSampler(_gpu_id_for_smi(torch, dev.index)) if rank == 0 else None
+    time.sleep(0.25 if sampler else 0)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t_host0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        step(i)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    t_host1 = time.time()
+    if world > 1:
+        dist.barrier()
+    ms = start.elapsed_time(end)
+    st, site = fa.fa_get_device_status(handle)
+    if st != fa.FA_OK:
+        raise RuntimeError(f"device status {fa.fa_status_string(st)} (site {site})")
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    clocks = sampler.summary(t_host0, t_host1) if sampler else None
+    if sampler:
+        sampler.stop()
+
+    ms_per_step = ms / args.steps
+    value = world * wl.flops * args.steps / (ms / 1e3) / 1e12
+
+    # end to end through the public API: pinned host inputs in, O/LSE out
+    q_h, k_h, v_h = (t.pin_memory() for t in (q, k, v))
+    o_h = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    l_h = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    qd, kd, vd, od, ld = sets[0]
+    e2e_steps = max(1, min(args.steps, 20))
+
+    def e2e_step():
+        qd.copy_(q_h, non_blocking=True)
+        kd.copy_(k_h, non_blocking=True)
+        vd.copy_(v_h, non_blocking=True)
+        fa.fwd(qd, kd, vd, scale=wl.scale, causal=wl.causal, out=od, lse=ld, stream=stream)
+        o_h.copy_(od, non_blocking=True)
+        l_h.copy_(ld, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        e2e_step()
+        stream.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = 3 * q.numel() * q.element_size()
+    d2h = q.numel() * q.element_size() + B * H * N * 4
+
+    if rank == 0:
+        peaks, src = _peaks()
+        peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        achieved = wl.flops / (ms_per_step / 1e3) / 1e12
+        traffic, traffic_src = _profiled_traffic(wl.name)
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": wl.dtype, "data": "synthetic",
+            "config": _config(wl, f"{n_sets} rotating input sets "
+                                  f"({n_sets * set_bytes / 2**20:.0f} MiB) > L2"),
+            "pct_of_peak": 100.0 * achieved / peak,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak,
+                         "peak_source": f"{src} bf16_tflops (burst; kernel timed alone)",
+                         "traffic": traffic, "traffic_source": traffic_src,
+                         "algorithmic_hbm_bytes": wl.hbm_bytes},
+            "e2e": {"value": world * wl.flops / (e2e_ms / 1e3) / 1e12, "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_ms},
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = _cpu_baseline(wl)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", type=int, default=2,
+                    help="1..5 (default 2: B=4 H=16 N=2048 d=128 bf16 full)")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    from workloads import workload
+    wl = workload(args.workload)
+    if args.impl == "reference":
+        return run_reference(args, wl)
+    return run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

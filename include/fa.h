@@ -1,0 +1,131 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) fused attention forward library
+ * (libfa_gb300.so).
+ *
+ * The operation is scaled-dot-product attention, forward pass, with the
+ * log-sum-exp of every row:
+ *
+ *     S = scale * Q K^T             (per batch b and head h; N x N scores)
+ *     S[i][j] = -inf  for j > i     (causal only: query i sees keys 0..i)
+ *     LSE[i]  = ln sum_j exp(S[i][j])
+ *     O[i]    = sum_j exp(S[i][j] - LSE[i]) V[j]
+ *
+ * Sources: LeetCUDA "flash_attn_mma_tiling_qk.cu" (the FlashAttention-2
+ * forward: Q,K,V,O as [batch, heads, seq_len, head_dim]; scores scaled before
+ * the exponential; the online row max / row sum recurrence and the final
+ * division by the row sum); flash-attention "hopper/flash_fwd_kernel.h"
+ * (persistent warp-specialised forward that stores O together with the row
+ * log-sum-exp; an empty row stores O = 0, LSE = -inf) and
+ * "hopper/mainloop_bwd_sm90_tma_gmma_ws.hpp" (the causal mask and the meaning
+ * of the stored LSE: the log-normaliser of the scaled scores, consumed by the
+ * backward pass as exp2(S*scale_log2 - LSE_log2)).  The LSE written here is in
+ * natural-log units.
+ *
+ * All entry points are plain C: pointers and sizes, no C++ or framework types,
+ * no exceptions.  Every function returns an fa_status_t code (or a string).
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stdint.h>
+
+/* Exported from the shared library (built with hidden default visibility). */
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type of q, k, v and o. */
+typedef enum {
+  FA_DTYPE_F16 = 0,  /* IEEE binary16 */
+  FA_DTYPE_BF16 = 1  /* bfloat16 */
+} fa_dtype_t;
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,     /* null pointer, negative size, bad flag/scale */
+  FA_ERR_UNSUPPORTED = 2,     /* head dim / device not supported */
+  FA_ERR_MISALIGNED = 3,      /* a pointer breaks the alignment rule below */
+  FA_ERR_CUDA = 4,            /* a CUDA runtime call or the launch failed */
+  FA_ERR_DEVICE_TIMEOUT = 5   /* a device-side wait ran out (watchdog) */
+} fa_status_t;
+
+/*
+ * fa_fwd -- attention forward pass on the current CUDA device.
+ *
+ * Arguments
+ *   q, k, v  device pointers, each a contiguous row-major [B][H][N][d] tensor
+ *            of `dtype` (the layout of the LeetCUDA kernel's Q,K,V).
+ *   o        device pointer, contiguous [B][H][N][d] of `dtype`; written.
+ *   lse      device pointer, contiguous [B][H][N] float32 (natural-log
+ *            log-sum-exp of the scaled scores of each row); written.  May be
+ *            NULL, in which case no LSE is stored.
+ *   B, H, N  batch, heads, sequence length.  Any of them 0: nothing is done
+ *            and FA_OK is returned (pointers are not touched).  Negative:
+ *            FA_ERR_INVALID_ARG.  B*H must be < 2^31 and N < 2^31.
+ *   d        head dimension: 64 or 128 (other values: FA_ERR_UNSUPPORTED).
+ *   scale    softmax scale applied to Q.K^T; must be finite and > 0
+ *            (1/sqrt(d) is the usual choice).
+ *   causal   0: every query sees every key; 1: query i sees keys 0..i.
+ *   dtype    fa_dtype_t.
+ *   stream   a cudaStream_t (NULL: the legacy default stream).
+ *
+ * Alignment: q, k, v, o must be 16-byte aligned; lse 4-byte aligned
+ * (else FA_ERR_MISALIGNED).  Ownership: the caller owns every buffer; the
+ * call allocates no device memory.  The call enqueues one kernel on `stream`
+ * and returns without synchronising; argument errors are reported before
+ * anything is enqueued; a launch failure returns FA_ERR_CUDA.  A device-side
+ * wait that runs out (a hung pipeline) is reported later by
+ * fa_get_device_status().  Requires an sm_103 GPU (else FA_ERR_UNSUPPORTED).
+ */
+FA_API int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+           int B, int H, int N, int d, float scale, int causal, int dtype,
+           void* stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+FA_API const char* fa_status_string(int status);
+
+/*
+ * Synchronise `stream`, then read and clear the device status word that the
+ * kernels' bounded waits set when one runs out.  Returns FA_OK,
+ * FA_ERR_DEVICE_TIMEOUT, or FA_ERR_CUDA if the synchronisation failed.
+ * `site` (may be NULL) receives the code of the wait that ran out (0 if none).
+ */
+FA_API int fa_get_device_status(void* stream, int* site);
+
+/*
+ * Set the limit of every device-side wait of later launches, in
+ * microseconds (default 2,000,000 = 2 s; must be >= 1).  Not a compute
+ * setting: only bounds how long a stalled pipeline stage waits before the
+ * kernel gives up, records FA_ERR_DEVICE_TIMEOUT and returns.
+ */
+FA_API int fa_set_wait_timeout_us(long long timeout_us);
+
+/*
+ * Cap the persistent grid of later fa_fwd launches at `max_ctas` CTAs
+ * (0 = one CTA per SM, the default).  Used by tests to run many work units
+ * through each CTA on small inputs.
+ */
+FA_API int fa_set_max_ctas(int max_ctas);
+
+/*
+ * Watchdog self-test: launch one CTA that waits on an mbarrier nobody
+ * arrives on, with a wait limit of `timeout_us`.  The kernel must give up,
+ * record FA_ERR_DEVICE_TIMEOUT in the device status word and return; read it
+ * with fa_get_device_status().  Faults nothing and traps nothing.
+ */
+FA_API int fa_selftest_watchdog(long long timeout_us, void* stream);
+
+/* Number of SMs the persistent grid is sized from (current device), or -1. */
+FA_API int fa_num_sms(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

@@ -1,0 +1,106 @@
+"""Host-only checks of the C ABI: the library loads, exports every declared
+symbol, and rejects bad arguments with the documented status codes before
+touching the GPU.  No kernel is launched here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+@pytest.fixture(scope="module")
+def fa():
+    from attention_forward_10_gb300 import build
+    build.build()
+    import attention_forward_10_gb300 as fa_mod
+    return fa_mod
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_expected_entry_points():
+    names = _declared_functions()
+    for n in ("fa_fwd", "fa_status_string", "fa_get_device_status",
+              "fa_set_wait_timeout_us", "fa_set_max_ctas", "fa_selftest_watchdog",
+              "fa_num_sms"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(fa):
+    lib = ctypes.CDLL(fa.LIB_PATH)
+    for name in _declared_functions():
+        assert hasattr(lib, name), f"{name} declared in fa.h but not exported"
+    assert set(_declared_functions()) == set(fa.SIGNATURES)
+
+
+def test_status_strings(fa):
+    assert fa.fa_status_string(fa.FA_OK) == "FA_OK"
+    assert fa.fa_status_string(fa.FA_ERR_MISALIGNED) == "FA_ERR_MISALIGNED"
+    assert fa.fa_status_string(fa.FA_ERR_DEVICE_TIMEOUT) == "FA_ERR_DEVICE_TIMEOUT"
+    assert fa.fa_status_string(99) == "FA_ERR_UNKNOWN"
+
+
+GOOD = dict(q=0x1000, k=0x2000, v=0x3000, o=0x4000, lse=0x5000, B=1, H=2, N=256, d=128,
+            scale=0.088, causal=0, dtype=1, stream=None)
+
+
+def _call(fa, **kw):
+    a = dict(GOOD)
+    a.update(kw)
+    return fa.fa_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"],
+                     a["d"], a["scale"], a["causal"], a["dtype"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=-1), 1), (dict(H=-3), 1), (dict(N=-1), 1),
+    (dict(dtype=2), 1), (dict(dtype=-1), 1),
+    (dict(causal=2), 1),
+    (dict(scale=0.0), 1), (dict(scale=-0.5), 1), (dict(scale=float("nan")), 1),
+    (dict(scale=float("inf")), 1),
+    (dict(d=32), 2), (dict(d=96), 2), (dict(d=512), 2), (dict(d=0), 2),
+    (dict(q=0), 1), (dict(k=0), 1), (dict(v=0), 1), (dict(o=0), 1),
+    (dict(q=0x1008), 3), (dict(k=0x2004), 3), (dict(v=0x3002), 3), (dict(o=0x4001), 3),
+    (dict(lse=0x5002), 3),
+    (dict(B=1 << 16, H=1 << 16), 1),
+])
+def test_argument_errors(fa, kw, code):
+    assert _call(fa, **kw) == code
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(H=0), dict(N=0),
+                                dict(N=0, q=0, k=0, v=0, o=0, lse=0)])
+def test_empty_problem_is_a_noop(fa, kw):
+    assert _call(fa, **kw) == fa.FA_OK
+
+
+def test_setters_validate(fa):
+    assert fa.fa_set_wait_timeout_us(0) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_set_wait_timeout_us(2_000_000) == fa.FA_OK
+    assert fa.fa_set_max_ctas(-1) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_set_max_ctas(0) == fa.FA_OK
+    assert fa.fa_selftest_watchdog(0, None) == fa.FA_ERR_INVALID_ARG
+
+
+def test_fwd_wrapper_rejects_cpu_tensors(fa):
+    import torch
+    q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa.fwd(q, q, q)
+
+
+def test_product_does_not_import_oracle():
+    """The product package shares no code with the oracle."""
+    pkg = os.path.join(ROOT, "attention_forward_10_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "attn_ref" not in text, f

@@ -1,0 +1,206 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Tolerances (stated for bf16/fp16 inputs with fp32 accumulation): max |O - O_ref|
+<= 2e-2 and max |LSE - LSE_ref| <= 1e-3, element by element.  Small shapes
+are compared in full (several tiles plus ragged tails); the large workloads in
+full (tiny and N=2048) or on seeded row samples.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from workloads import WORKLOADS, make_qkv, make_random_qkv, sample_rows, workload
+
+pytestmark = pytest.mark.gpu
+
+O_TOL = 2e-2
+LSE_TOL = 1e-3
+
+
+@pytest.fixture(scope="module")
+def fa():
+    from attention_forward_10_gb300 import build
+    build.build()
+    import attention_forward_10_gb300 as fa_mod
+    fa_mod.fa_set_max_ctas(0)
+    fa_mod.fa_set_wait_timeout_us(2_000_000)
+    return fa_mod
+
+
+def _run(fa, q, k, v, scale, causal, dev="cuda:0", stream=None):
+    qd, kd, vd = (t.to(dev) for t in (q, k, v))
+    o, lse = fa.fwd(qd, kd, vd, scale=scale, causal=causal, stream=stream)
+    torch.cuda.synchronize()
+    st, site = fa.fa_get_device_status(None)
+    assert st == fa.FA_OK, f"device status {fa.fa_status_string(st)} at site {site}"
+    return o, lse
+
+
+def _check(o, lse, o_ref, lse_ref, what):
+    o_np = o.float().cpu().numpy() if torch.is_tensor(o) else o
+    l_np = lse.cpu().numpy() if torch.is_tensor(lse) else lse
+    assert np.isfinite(o_np).all(), f"{what}: non-finite O"
+    assert np.isfinite(l_np).all(), f"{what}: non-finite LSE"
+    err_o = float(np.abs(o_np - o_ref).max()) if o_np.size else 0.0
+    err_l = float(np.abs(l_np - lse_ref).max()) if l_np.size else 0.0
+    assert err_l <= LSE_TOL, f"{what}: max|dLSE| = {err_l:.3e} (O err {err_o:.3e})"
+    assert err_o <= O_TOL, f"{what}: max|dO| = {err_o:.3e} (LSE err {err_l:.3e})"
+    return err_o, err_l
+
+
+# ------------------------------------------------------------ small, full
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16], ids=["bf16", "fp16"])
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N", [1, 5, 64, 127, 128, 129, 255, 256, 257, 384, 640])
+def test_small_shapes_full_compare(fa, N, d, causal, dtype):
+    q, k, v = make_random_qkv(1, 2, N, d, dtype, seed=100 + N + d)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = _run(fa, q, k, v, scale, causal)
+    o_ref, lse_ref = oracle.attention(q, k, v, scale, causal)
+    _check(o, lse, o_ref, lse_ref, f"N={N} d={d} causal={causal} {dtype}")
+
+
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+def test_peaky_scores_trigger_rescale(fa, causal):
+    """Large scores make the running maximum jump across tiles (O rescales)."""
+    q, k, v = make_random_qkv(2, 2, 700, 128, torch.bfloat16, seed=31, qk_mult=4.0)
+    # a growing ramp of key norms so later tiles keep raising the maximum
+    ramp = torch.linspace(0.2, 3.0, 700).to(torch.bfloat16)[None, None, :, None]
+    k = (k * ramp).to(torch.bfloat16)
+    scale = 1.0 / math.sqrt(128)
+    o, lse = _run(fa, q, k, v, scale, causal)
+    o_ref, lse_ref = oracle.attention(q, k, v, scale, causal)
+    _check(o, lse, o_ref, lse_ref, "peaky")
+
+
+# ------------------------------------------------------ structured inputs
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+def test_constant_values_give_constant_output(fa, causal):
+    q, k, _ = make_random_qkv(1, 3, 300, 128, torch.bfloat16, seed=41)
+    v = torch.full_like(q, 0.625)
+    o, _ = _run(fa, q, k, v, 0.088, causal)
+    assert torch.all(o.float().cpu() == 0.625)
+
+
+def test_one_hot_values_expose_probabilities(fa):
+    """V = identity (N = d = 128): O_i is the probability row P_i."""
+    q, k, _ = make_random_qkv(1, 1, 128, 128, torch.bfloat16, seed=42)
+    v = torch.eye(128, dtype=torch.bfloat16)[None, None].contiguous()
+    o, lse = _run(fa, q, k, v, 0.1, False)
+    p_ref, lse_ref = oracle.attention(q, k, v, 0.1, False)
+    _check(o, lse, p_ref, lse_ref, "one-hot")
+    assert np.abs(o.float().cpu().numpy().sum(-1) - 1.0).max() < 2e-2
+
+
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+def test_zero_queries_uniform_weights(fa, causal):
+    _, k, v = make_random_qkv(1, 2, 333, 64, torch.float16, seed=43)
+    q = torch.zeros_like(k)
+    o, lse = _run(fa, q, k, v, 0.125, causal)
+    n = np.arange(1, 334) if causal else np.full(333, 333)
+    np.testing.assert_allclose(lse.cpu().numpy(), np.broadcast_to(np.log(n), (1, 2, 333)),
+                               rtol=0, atol=LSE_TOL)
+    o_ref, _ = oracle.attention(q, k, v, 0.125, causal)
+    _check(o, lse, o_ref, np.log(np.broadcast_to(n, (1, 2, 333)).astype(float)), "Q=0")
+
+
+def test_causal_first_row_is_first_value_row(fa):
+    q, k, v = make_random_qkv(2, 2, 200, 128, torch.bfloat16, seed=44)
+    o, _ = _run(fa, q, k, v, 0.088, True)
+    assert torch.equal(o[:, :, 0, :].cpu(), v[:, :, 0, :])
+
+
+# ------------------------------------------- persistent scheduler, streams
+@pytest.mark.parametrize("ctas", [1, 2, 3, 7])
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+def test_persistent_loop_many_units_per_cta(fa, ctas, causal):
+    q, k, v = make_random_qkv(2, 3, 1000, 128, torch.bfloat16, seed=50 + ctas)
+    scale = 1.0 / math.sqrt(128)
+    fa.fa_set_max_ctas(ctas)
+    try:
+        o, lse = _run(fa, q, k, v, scale, causal)
+    finally:
+        fa.fa_set_max_ctas(0)
+    o_ref, lse_ref = oracle.attention(q, k, v, scale, causal)
+    _check(o, lse, o_ref, lse_ref, f"ctas={ctas}")
+
+
+def test_side_stream_and_no_lse(fa):
+    q, k, v = make_random_qkv(1, 2, 260, 64, torch.bfloat16, seed=60)
+    qd, kd, vd = (t.cuda() for t in (q, k, v))
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        o, lse = fa.fwd(qd, kd, vd, scale=0.125, causal=True, return_lse=False)
+    s.synchronize()
+    assert lse is None
+    o_ref, _ = oracle.attention(q, k, v, 0.125, True)
+    assert float(np.abs(o.float().cpu().numpy() - o_ref).max()) <= O_TOL
+
+
+def test_deterministic_and_guard_bands(fa):
+    q, k, v = make_random_qkv(2, 2, 513, 128, torch.bfloat16, seed=61)
+    qd, kd, vd = (t.cuda() for t in (q, k, v))
+    G = 64
+    numel = q.numel()
+    pattern = torch.tensor([0x7FC1], dtype=torch.int16).view(torch.bfloat16)
+    obuf = pattern.repeat(numel + 2 * G).cuda()
+    lbuf = torch.full((2 * 2 * 513 + 2 * G,), -7.25, dtype=torch.float32, device="cuda")
+    o = obuf[G:G + numel].view(q.shape)
+    lse = lbuf[G:G + 2 * 2 * 513].view(2, 2, 513)
+    outs = []
+    for _ in range(2):
+        fa.fwd(qd, kd, vd, scale=0.09, causal=False, out=o, lse=lse)
+        torch.cuda.synchronize()
+        outs.append((o.clone(), lse.clone()))
+    assert torch.equal(outs[0][0].view(torch.int16), outs[1][0].view(torch.int16))
+    assert torch.equal(outs[0][1], outs[1][1])
+    guard = torch.cat([obuf[:G], obuf[G + numel:]]).view(torch.int16).cpu()
+    assert torch.all(guard == 0x7FC1)
+    lg = torch.cat([lbuf[:G], lbuf[G + 2 * 2 * 513:]]).cpu()
+    assert torch.all(lg == -7.25)
+
+
+# ------------------------------------------------------------- watchdog
+def test_watchdog_times_out_cleanly(fa):
+    st = fa.fa_selftest_watchdog(20_000, None)
+    assert st == fa.FA_OK
+    st, site = fa.fa_get_device_status(None)
+    assert st == fa.FA_ERR_DEVICE_TIMEOUT and site == 15
+    st, _ = fa.fa_get_device_status(None)       # the word was cleared
+    assert st == fa.FA_OK
+    # the context is still usable
+    q, k, v = make_random_qkv(1, 1, 130, 64, torch.bfloat16, seed=62)
+    o, lse = _run(fa, q, k, v, 0.125, False)
+    o_ref, lse_ref = oracle.attention(q, k, v, 0.125, False)
+    _check(o, lse, o_ref, lse_ref, "after watchdog")
+
+
+# ------------------------------------------------------- the workloads
+def _workload_case(fa, wl, full):
+    q, k, v = make_qkv(wl)
+    o, lse = _run(fa, q, k, v, wl.scale, wl.causal)
+    if full:
+        o_ref, lse_ref = oracle.attention(q, k, v, wl.scale, wl.causal)
+        return _check(o, lse, o_ref, lse_ref, wl.name)
+    rows = sample_rows(wl)
+    o_ref, lse_ref = oracle.attention_rows(q, k, v, wl.scale, wl.causal, rows)
+    idx = torch.tensor(rows, dtype=torch.long)
+    o_s = o[idx[:, 0], idx[:, 1], idx[:, 2]].float().cpu().numpy()
+    l_s = lse[idx[:, 0], idx[:, 1], idx[:, 2]].cpu().numpy()
+    err = _check(o_s, l_s, o_ref, lse_ref, wl.name + " (sampled)")
+    # properties that hold at any size, over every row
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+    if wl.causal:
+        assert torch.equal(o[:, :, 0, :].cpu(), v[:, :, 0, :])
+    return err
+
+
+@pytest.mark.parametrize("index", [w.index for w in WORKLOADS if w.d in (64, 128)])
+def test_workload(fa, index):
+    wl = workload(index)
+    full = wl.B * wl.H * wl.N * wl.N * wl.d <= 4 * 16 * 2048 * 2048 * 128
+    _workload_case(fa, wl, full)
