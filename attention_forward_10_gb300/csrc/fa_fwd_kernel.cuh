@@ -12,10 +12,25 @@
 // persistent work-tile loop, O stored with the row LSE) arrange it, and
 // re-designed for Blackwell's tensor memory:
 //
-//   warps 0-3  softmax warpgroup 0   (query tile 0 of the unit, row = thread)
+//   warps 0-3  softmax warpgroup 0   (query tile 0, one row per thread)
 //   warps 4-7  softmax warpgroup 1   (query tile 1)
 //   warp  8    TMA producer          (Q tiles, then K_j / V_j into a ring)
 //   warp  9    MMA issuer            (S_g = Q_g K_j^T, O_g += P_g V_j)
+//   warp  10   O store               (TMA store of each finished O tile)
+//   warp  11   spare (completes the third warpgroup, so that register
+//              budgets can move between warpgroups with setmaxnreg: the
+//              softmax warpgroups run with 216 registers, the third with 72)
+//
+// All synchronisation between roles goes through mbarriers with bounded
+// waits (no bar.sync among roles), so a stalled stage can always be
+// abandoned without leaving another one blocked.
+//
+// MMA issue order.  The MMAs are issued as alternating per-tile groups
+//   [P_0(j-1) V_(j-1), Q_0 K_j^T]  [P_1(j-1) V_(j-1), Q_1 K_j^T]  ...
+// over the stream of K/V tiles j (continuing across work units), so that
+// each tile's softmax runs while the other tile's two MMAs execute.  P_g lives
+// in S_g's tensor-memory columns, and tcgen05 orders only MMAs into the same
+// accumulator, so Q_g K_j^T is issued only after P_g(j-1) V has completed.
 //
 // Tensor memory (512 columns x 128 lanes, fp32):
 //   [0,128)    S_0 (scores of tile 0); P_0 (16-bit, packed in pairs) is
@@ -26,7 +41,8 @@
 // Shared memory (1024-byte aligned, 128-byte TMA swizzle everywhere):
 //   Q_0, Q_1       [D/64][128 rows][64]   one tile each
 //   K/V ring       STAGES slots of [D/64][128 keys][64]
-//   O staging      one tile per softmax warpgroup (TMA store source)
+//   O staging      one tile, shared by the two query tiles in turn (TMA
+//                  store source)
 //   mbarriers
 //
 // Online softmax in the log2 domain (scale folded into scale*log2 e, as the
@@ -48,9 +64,15 @@
 
 namespace fa {
 
-constexpr int kNumThreads = 320;
+constexpr int kNumThreads = 384;
+constexpr uint32_t kSoftmaxRegs = 216;  // per thread, warpgroups 0 and 1
+constexpr uint32_t kControlRegs = 72;   // per thread, warpgroup 2
+// Launch budget: 384 threads x 168 registers; 2*128*216 + 128*56 fits in it.
+static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kNumThreads * 168,
+              "register split exceeds the launch budget");
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+constexpr int kStoreWarp = 10;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kStatusTimeout = 5;           // == FA_ERR_DEVICE_TIMEOUT
@@ -59,11 +81,11 @@ template <int D>
 struct Layout {
   static_assert(D == 64 || D == 128, "head dim");
   static constexpr uint32_t kTileBytes = kBlockM * D * 2;  // == kBlockN * D * 2
-  static constexpr int kStages = (D == 64) ? 6 : 3;
+  static constexpr int kStages = (D == 64) ? 6 : 4;
   static constexpr uint32_t kQOff = 0;
   static constexpr uint32_t kKVOff = kQOff + 2 * kTileBytes;
   static constexpr uint32_t kStageOff = kKVOff + kStages * kTileBytes;
-  static constexpr uint32_t kBarOff = kStageOff + 2 * kTileBytes;
+  static constexpr uint32_t kBarOff = kStageOff + kTileBytes;
   // barrier indices
   static constexpr int kQFull = 0;
   static constexpr int kQEmpty = 2;
@@ -73,10 +95,13 @@ struct Layout {
   static constexpr int kPFull = kSFull + 2;
   static constexpr int kODone = kPFull + 2;
   static constexpr int kDrain = kODone + 2;
-  static constexpr int kNumBars = kDrain + 1;
+  static constexpr int kStageFull = kDrain + 1;       // O tile written to staging
+  static constexpr int kStageEmpty = kStageFull + 1;  // staging read by the store
+  static constexpr int kNumBars = kStageEmpty + 1;
   static constexpr uint32_t kCtlOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kUsedBytes = kCtlOff + 16;
   static constexpr uint32_t kSmemBytes = kUsedBytes + 1024;  // alignment slack
+  static_assert(kSmemBytes <= 232448, "exceeds the shared memory of one CTA");
   // tensor-memory columns of S_g / P_g and of O_g
   __device__ static constexpr uint32_t s_col(int g) { return g * 128u; }
   __device__ static constexpr uint32_t o_col(int g) { return 256u + g * D; }
@@ -127,13 +152,13 @@ struct Ctl {
   unsigned long long timeout_ns;
 };
 
-static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Ctl& c,
+static __device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Ctl& c,
                                        int site) {
   const uint64_t t0 = global_timer_ns();
   while (true) {
 #pragma unroll 1
-    for (int i = 0; i < 64; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    for (int i = 0; i < 8; ++i)
+      if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if (*c.abort_flag) return false;
     if (global_timer_ns() - t0 > c.timeout_ns) {
       *c.abort_flag = 1;
@@ -152,7 +177,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ct
 }
 
 // Bounded wait that ignores the abort flag (used while draining on exit).
-static __device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity,
+static __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity,
                                         unsigned long long limit_ns) {
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(bar, parity)) {
@@ -190,6 +215,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       mbar_init(bar(L::kKVEmpty + s), 1);
     }
     mbar_init(bar(L::kDrain), 1);
+    mbar_init(bar(L::kStageFull), 128);
+    mbar_init(bar(L::kStageEmpty), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -208,7 +235,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
+  // Each role changes its register budget inside its own branch, so that no
+  // code is reachable under two different budgets.
   if (warp == kProducerWarp) {
+    regs_decrease<kControlRegs>();
     // ---------------------------------------------------------------- TMA
     if (lane == 0) {
       uint32_t kv_it = 0, q_it[2] = {0, 0};
@@ -247,77 +277,97 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
+    regs_decrease<kControlRegs>();
     // ---------------------------------------------------------------- MMA
+    // The issuing thread does as little as possible between MMA groups: the
+    // tensor pipe holds only a couple of queued MMAs.
     if (lane == 0) {
       constexpr uint32_t kIdescS = make_idesc_f16(kBlockM, kBlockN, BF16, false);
       constexpr uint32_t kIdescO = make_idesc_f16(kBlockM, D, BF16, true);
-      uint32_t kv_it = 0, q_it[2] = {0, 0}, p_it[2] = {0, 0}, o_cnt[2] = {0, 0};
+      constexpr uint32_t kSlotStep = L::kTileBytes >> 4;  // descriptor units
+      // Descriptors of slot 0 / query tile 0; other slots and tiles are fixed
+      // offsets in the 14-bit start-address field (no carry: smem < 256 KB).
+      const uint64_t q_desc0 = smem_desc_sw128(sbase + L::kQOff, 16, 1024);
+      const uint64_t k_desc0 = smem_desc_sw128(sbase + L::kKVOff, 16, 1024);
+      // V is MN-major (d contiguous): 64-wide d blocks 128 keys apart (LBO),
+      // 8-key groups 1024 B apart (SBO).
+      const uint64_t v_desc0 = smem_desc_sw128(sbase + L::kKVOff, kBlockN * 128, 1024);
+      uint32_t slot = 0, phase = 0;  // next K/V ring position
+      uint32_t q_par[2] = {0, 0}, p_par[2] = {0, 0}, o_cnt[2] = {0, 0};
       bool ok = true;
-      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
-        const Unit w = decode_unit<CAUSAL>(u, p);
-        for (int g = 0; g < 2 && ok; ++g) {
-          if (w.nt[g] == 0) continue;
-          ok = wait_bar(bar(L::kQFull + g), q_it[g] & 1u, ctl, kSiteMmaQ);
-          ++q_it[g];
-        }
-        for (int n = 0; n < w.ntot && ok; ++n) {
-          // S_g = Q_g K_n^T for every query tile that still visits tile n
-          const uint32_t kslot = kv_it % L::kStages;
-          ok = wait_bar(bar(L::kKVFull + kslot), (kv_it / L::kStages) & 1u, ctl, kSiteMmaK);
-          ++kv_it;
-          if (!ok) break;
-          tc_fence_after_sync();
-          const uint32_t k_smem = sbase + L::kKVOff + kslot * L::kTileBytes;
-          for (int g = 0; g < 2; ++g) {
-            if (n >= w.nt[g]) continue;
-            // P_g (aliasing S_g) must have been consumed by the last O_g MMA
-            if (o_cnt[g] > 0) {
-              ok = wait_bar(bar(L::kODone + g), (o_cnt[g] - 1) & 1u, ctl, kSiteMmaO);
-              if (!ok) break;
-              tc_fence_after_sync();
-            }
-            const uint32_t q_smem = sbase + L::kQOff + g * L::kTileBytes;
-#pragma unroll
-            for (int k = 0; k < D / 16; ++k) {
-              // K-major operands: 64-element column blocks of 128 rows x 128 B;
-              // 16-element steps advance 32 B inside the swizzled row.
-              const uint32_t koff = (k / 4) * (kBlockM * 128) + (k % 4) * 32;
-              const uint64_t a = smem_desc_sw128(q_smem + koff, 16, 1024);
-              const uint64_t b = smem_desc_sw128(k_smem + koff, 16, 1024);
-              mma_ss(tmem + L::s_col(g), a, b, kIdescS, k > 0 ? 1u : 0u);
-            }
-            tc_commit(bar(L::kSFull + g));
-            if (n == w.nt[g] - 1) tc_commit(bar(L::kQEmpty + g));
+      // Step j of the K/V stream is (unit u, tile n); prev_* describe step
+      // j-1, whose P V products are issued in step j.
+      bool prev_valid = false, prev_acc = false;
+      bool prev_active[2] = {false, false};
+      uint32_t prev_vslot = 0;
+      int u = blockIdx.x, n = 0;
+      Unit w = decode_unit<CAUSAL>(u < p.num_units ? u : 0, p);
+      while (ok) {
+        const bool cur_valid = u < p.num_units;
+        if (!cur_valid && !prev_valid) break;
+        if (cur_valid && n == 0) {
+          for (int g = 0; g < 2 && ok; ++g) {
+            if (w.nt[g] == 0) continue;
+            ok = wait_bar(bar(L::kQFull + g), q_par[g], ctl, kSiteMmaQ);
+            q_par[g] ^= 1u;
           }
           if (!ok) break;
-          tc_commit(bar(L::kKVEmpty + kslot));
-
-          // O_g += P_g V_n
-          const uint32_t vslot = kv_it % L::kStages;
-          ok = wait_bar(bar(L::kKVFull + vslot), (kv_it / L::kStages) & 1u, ctl, kSiteMmaV);
-          ++kv_it;
-          if (!ok) break;
-          tc_fence_after_sync();
-          const uint32_t v_smem = sbase + L::kKVOff + vslot * L::kTileBytes;
-          for (int g = 0; g < 2; ++g) {
-            if (n >= w.nt[g]) continue;
-            ok = wait_bar(bar(L::kPFull + g), p_it[g] & 1u, ctl, kSiteMmaP);
-            ++p_it[g];
+        }
+        const uint32_t kslot = slot, kphase = phase;
+        bool k_ready = false;  // K(j) is waited for just before its first use
+        for (int g = 0; g < 2; ++g) {
+          // ---- O_g += P_g(j-1) V(j-1)
+          if (prev_valid && prev_active[g]) {
+            ok = wait_bar(bar(L::kPFull + g), p_par[g], ctl, kSiteMmaP);
+            p_par[g] ^= 1u;
             if (!ok) break;
             tc_fence_after_sync();
-#pragma unroll
-            for (int k = 0; k < kBlockN / 16; ++k) {
-              // V is MN-major (d contiguous): 64-wide d blocks 128 keys apart
-              // (LBO), 8-key groups 1024 B apart (SBO); 16 keys per step.
-              const uint64_t b = smem_desc_sw128(v_smem + k * 16 * 128, kBlockN * 128, 1024);
-              mma_ts(tmem + L::o_col(g), tmem + L::s_col(g) + k * 8, b, kIdescO,
-                     (n > 0 || k > 0) ? 1u : 0u);
-            }
+            mma_ts_mnmajor_x8(tmem + L::o_col(g), tmem + L::s_col(g),
+                              v_desc0 + prev_vslot * kSlotStep, kIdescO, prev_acc ? 1u : 0u);
             tc_commit(bar(L::kODone + g));
             ++o_cnt[g];
           }
-          if (!ok) break;
-          tc_commit(bar(L::kKVEmpty + vslot));
+          // ---- S_g = Q_g K_j^T (after P_g(j-1) V, which reads S_g's columns)
+          if (cur_valid && n < w.nt[g]) {
+            if (!k_ready) {
+              ok = wait_bar(bar(L::kKVFull + kslot), kphase, ctl, kSiteMmaK);
+              if (!ok) break;
+              k_ready = true;
+            }
+            if (o_cnt[g] > 0) {
+              ok = wait_bar(bar(L::kODone + g), (o_cnt[g] - 1) & 1u, ctl, kSiteMmaO);
+              if (!ok) break;
+            }
+            tc_fence_after_sync();
+            const uint64_t a = q_desc0 + g * kSlotStep;
+            const uint64_t b = k_desc0 + kslot * kSlotStep;
+            if constexpr (D == 128)
+              mma_ss_kmajor_x8(tmem + L::s_col(g), a, b, kIdescS, 0u);
+            else
+              mma_ss_kmajor_x4(tmem + L::s_col(g), a, b, kIdescS, 0u);
+            tc_commit(bar(L::kSFull + g));
+            if (n == w.nt[g] - 1) tc_commit(bar(L::kQEmpty + g));
+          }
+        }
+        if (!ok) break;
+        if (prev_valid) tc_commit(bar(L::kKVEmpty + prev_vslot));
+        if (!cur_valid) break;
+        tc_commit(bar(L::kKVEmpty + kslot));
+        if (++slot == (uint32_t)L::kStages) { slot = 0; phase ^= 1u; }
+        // V(j): waited for now, used (and released) in step j+1
+        const uint32_t vslot = slot;
+        ok = wait_bar(bar(L::kKVFull + vslot), phase, ctl, kSiteMmaV);
+        if (!ok) break;
+        if (++slot == (uint32_t)L::kStages) { slot = 0; phase ^= 1u; }
+        prev_valid = true;
+        prev_acc = n > 0;
+        prev_active[0] = n < w.nt[0];
+        prev_active[1] = n < w.nt[1];
+        prev_vslot = vslot;
+        if (++n == w.ntot) {
+          n = 0;
+          u += gridDim.x;
+          if (u < p.num_units) w = decode_unit<CAUSAL>(u, p);
         }
       }
       // Every MMA issued must complete before tensor memory is released.
@@ -325,34 +375,39 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       wait_drain(bar(L::kDrain), 0, p.timeout_ns);
     }
     __syncwarp();
-  } else {
+  } else if (warp < 8) {
+    regs_increase<kSoftmaxRegs>();
     // ------------------------------------------------------------ softmax
     const int g = warp / 4;
     const int t = threadIdx.x % 128;  // row within the query tile == TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>((warp % 4) * 32) << 16;
     const uint32_t tS = tmem + lane_base + L::s_col(g);
     const uint32_t tO = tmem + lane_base + L::o_col(g);
-    const uint32_t stage = sbase + L::kStageOff + g * L::kTileBytes;
+    const uint32_t stage = sbase + L::kStageOff;
     const float scale_log2 = p.scale_log2;
-    uint32_t s_it = 0, pv_cnt = 0;
-    bool ok = true, store_pending = false;
+    uint32_t s_par = 0, pv_cnt = 0;
+    uint32_t n_stores = 0;  // O tiles staged so far by both warpgroups, in order
+    bool ok = true;
 
     for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
       const Unit w = decode_unit<CAUSAL>(u, p);
+      // the staging tile is used by tile 0 then tile 1 of each unit
+      const uint32_t my_store = n_stores + ((g == 1 && w.nt[0] > 0) ? 1u : 0u);
+      n_stores += (w.nt[0] > 0 ? 1u : 0u) + (w.nt[1] > 0 ? 1u : 0u);
       if (w.nt[g] == 0) continue;
       const int row = w.row0[g] + t;
       float m_ref = -INFINITY;  // reference maximum (log2 units, scaled)
       float l = 0.f;            // running row sum relative to m_ref
 
       for (int n = 0; n < w.nt[g]; ++n) {
-        ok = wait_bar(bar(L::kSFull + g), s_it & 1u, ctl, kSiteSoftmaxS);
-        ++s_it;
+        ok = wait_bar(bar(L::kSFull + g), s_par, ctl, kSiteSoftmaxS);
+        s_par ^= 1u;
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after_sync();
 
         uint32_t sraw[kBlockN];
-        tmem_ld_x128_sync(tS, sraw);
+        tmem_ld_x32x4_sync(tS, sraw);
         float s[kBlockN];
 #pragma unroll
         for (int c = 0; c < kBlockN; ++c) s[c] = __uint_as_float(sraw[c]);
@@ -367,6 +422,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           for (int c = 0; c < kBlockN; ++c)
             if (c >= lim) s[c] = -INFINITY;
         }
+        // row maximum: four independent chains
         float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
         for (int c = 4; c < kBlockN; c += 4) {
@@ -403,23 +459,36 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           m_ref = m_new;
         }
 
+        // p = 2^(s*scale*log2e - m): one packed FMA per pair, then the
+        // exponentials; row sum kept as two packed partial sums.
         const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-        float sum0 = 0.f, sum1 = 0.f;
+        const uint64_t scale2 = pack_f32x2(scale_log2, scale_log2);
+        const uint64_t neg_m2 = pack_f32x2(-m_use, -m_use);
+        uint64_t acc_a = pack_f32x2(0.f, 0.f), acc_b = acc_a;
 #pragma unroll
         for (int c0 = 0; c0 < kBlockN; c0 += 32) {
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float p0 = ex2_approx(fmaf(s[c0 + 2 * e], scale_log2, -m_use));
-            const float p1 = ex2_approx(fmaf(s[c0 + 2 * e + 1], scale_log2, -m_use));
-            sum0 += p0;
-            sum1 += p1;
+            float x0, x1;
+            unpack_f32x2(fma_f32x2(pack_f32x2(s[c0 + 2 * e], s[c0 + 2 * e + 1]), scale2, neg_m2),
+                         x0, x1);
+            const float p0 = ex2_approx(x0);
+            const float p1 = ex2_approx(x1);
+            if (e & 1)
+              acc_b = add_f32x2(acc_b, pack_f32x2(p0, p1));
+            else
+              acc_a = add_f32x2(acc_a, pack_f32x2(p0, p1));
             pk[e] = pack2<BF16>(p0, p1);
           }
           tmem_st_x16(tS + c0 / 2, pk);
         }
         tmem_wait_st();
-        l += sum0 + sum1;
+        {
+          float a0, a1;
+          unpack_f32x2(add_f32x2(acc_a, acc_b), a0, a1);
+          l += a0 + a1;
+        }
         tc_fence_before_sync();
         mbar_arrive(bar(L::kPFull + g));
         ++pv_cnt;
@@ -428,11 +497,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
       // ---------------------------------------------------------- epilogue
       ok = wait_bar(bar(L::kODone + g), (pv_cnt - 1) & 1u, ctl, kSiteEpilogueO);
+      // the staging tile must have been read by the store before this one
+      ok = ok && wait_bar(bar(L::kStageEmpty), (my_store - 1) & 1u, ctl, kSiteEpilogueO);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after_sync();
-      if (t == 0 && store_pending) bulk_wait_read_all();  // staging tile free again
-      named_bar_sync(1 + g, 128);
 
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
 #pragma unroll
@@ -457,15 +526,33 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             (l > 0.f) ? (m_ref + log2f(l)) * 0.6931471805599453f : -INFINITY;
       }
       fence_proxy_async_smem();
-      named_bar_sync(1 + g, 128);
-      if (t == 0) {
-        tma_store_4d(&p.tm_o, stage, 0, w.row0[g], 0, w.bh);
-        bulk_commit_group();
-        store_pending = true;
-      }
+      mbar_arrive(bar(L::kStageFull));
     }
-    if (t == 0 && store_pending) bulk_wait_all();
     __syncwarp();
+  } else if (warp == kStoreWarp) {
+    regs_decrease<kControlRegs>();
+    // ------------------------------------------------------------ O store
+    if (lane == 0) {
+      uint32_t full_par = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+        const Unit w = decode_unit<CAUSAL>(u, p);
+        for (int g = 0; g < 2 && ok; ++g) {
+          if (w.nt[g] == 0) continue;
+          ok = wait_bar(bar(L::kStageFull), full_par, ctl, kSiteStore);
+          full_par ^= 1u;
+          if (!ok) break;
+          tma_store_4d(&p.tm_o, sbase + L::kStageOff, 0, w.row0[g], 0, w.bh);
+          bulk_commit_group();
+          bulk_wait_read_all();  // the staging tile may be rewritten
+          mbar_arrive(bar(L::kStageEmpty));
+        }
+      }
+      bulk_wait_all();
+    }
+    __syncwarp();
+  } else {
+    regs_decrease<kControlRegs>();  // spare warps of the third warpgroup
   }
 
   tc_fence_before_sync();

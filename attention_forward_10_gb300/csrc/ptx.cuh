@@ -49,6 +49,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Same test, but a thread whose phase is not complete may sleep up to
+// `hint_ns` nanoseconds (it wakes as soon as the phase completes).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -225,9 +240,152 @@ __host__ __device__ constexpr uint32_t make_idesc_f16(int M, int N, bool bf16,
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Warpgroup-wide register budget changes (all 4 warps of a warpgroup).
+template <uint32_t N>
+__device__ __forceinline__ void regs_increase() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_decrease() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// --------------------------------------------------------------------------
+// MMA bursts
+// --------------------------------------------------------------------------
+// 8 back-to-back K=16 MMAs D (+)= A*B^T, both operands K-major
+// 128B-swizzled tiles in shared memory: step k adds a fixed offset (in 16-byte
+// units) to both descriptors; the first step overwrites D when `accumulate` is
+// 0, later steps accumulate.  Issued as one burst so the tensor pipe is fed
+// without gaps.
+__device__ __forceinline__ void mma_ss_kmajor_x8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred pf, pt;\n\t.reg .b64 ak, bk;\n\t"
+      "setp.ne.b32 pf, %4, 0;\n\t"
+      "setp.eq.b32 pt, %4, %4;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, pf;\n\t"
+      "add.s64 ak, %1, 2;\n\t"
+      "add.s64 bk, %2, 2;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ak, bk, %3, pt;\n\t"
+      "add.s64 ak, %1, 4;\n\t"
+      "add.s64 bk, %2, 4;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ak, bk, %3, pt;\n\t"
+      "add.s64 ak, %1, 6;\n\t"
+      "add.s64 bk, %2, 6;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ak, bk, %3, pt;\n\t"
+      "add.s64 ak, %1, 1024;\n\t"
+      "add.s64 bk, %2, 1024;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ak, bk, %3, pt;\n\t"
+      "add.s64 ak, %1, 1026;\n\t"
+      "add.s64 bk, %2, 1026;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ak, bk, %3, pt;\n\t"
+      "add.s64 ak, %1, 1028;\n\t"
+      "add.s64 bk, %2, 1028;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ak, bk, %3, pt;\n\t"
+      "add.s64 ak, %1, 1030;\n\t"
+      "add.s64 bk, %2, 1030;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ak, bk, %3, pt;\n\t"
+      "}"
+      :
+      : "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 4 back-to-back K=16 MMAs D (+)= A*B^T, both operands K-major
+// 128B-swizzled tiles in shared memory: step k adds a fixed offset (in 16-byte
+// units) to both descriptors; the first step overwrites D when `accumulate` is
+// 0, later steps accumulate.  Issued as one burst so the tensor pipe is fed
+// without gaps.
+__device__ __forceinline__ void mma_ss_kmajor_x4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred pf, pt;\n\t.reg .b64 ak, bk;\n\t"
+      "setp.ne.b32 pf, %4, 0;\n\t"
+      "setp.eq.b32 pt, %4, %4;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, pf;\n\t"
+      "add.s64 ak, %1, 2;\n\t"
+      "add.s64 bk, %2, 2;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ak, bk, %3, pt;\n\t"
+      "add.s64 ak, %1, 4;\n\t"
+      "add.s64 bk, %2, 4;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ak, bk, %3, pt;\n\t"
+      "add.s64 ak, %1, 6;\n\t"
+      "add.s64 bk, %2, 6;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ak, bk, %3, pt;\n\t"
+      "}"
+      :
+      : "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 8 back-to-back K=16 MMAs D (+)= A*B with A in tensor memory (two
+// 16-bit elements per 32-bit column, so step k reads columns a_tmem + 8k) and
+// B an MN-major 128B-swizzled tile whose 16-row steps are 2048 bytes apart
+// (descriptor + 128 per step).  First step overwrites D unless `accumulate`.
+__device__ __forceinline__ void mma_ts_mnmajor_x8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred pf, pt;\n\t.reg .b64 bk;\n\t.reg .b32 ak;\n\t"
+      "setp.ne.b32 pf, %4, 0;\n\t"
+      "setp.eq.b32 pt, %4, %4;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pf;\n\t"
+      "add.u32 ak, %1, 8;\n\t"
+      "add.s64 bk, %2, 128;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ak], bk, %3, pt;\n\t"
+      "add.u32 ak, %1, 16;\n\t"
+      "add.s64 bk, %2, 256;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ak], bk, %3, pt;\n\t"
+      "add.u32 ak, %1, 24;\n\t"
+      "add.s64 bk, %2, 384;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ak], bk, %3, pt;\n\t"
+      "add.u32 ak, %1, 32;\n\t"
+      "add.s64 bk, %2, 512;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ak], bk, %3, pt;\n\t"
+      "add.u32 ak, %1, 40;\n\t"
+      "add.s64 bk, %2, 640;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ak], bk, %3, pt;\n\t"
+      "add.u32 ak, %1, 48;\n\t"
+      "add.s64 bk, %2, 768;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ak], bk, %3, pt;\n\t"
+      "add.u32 ak, %1, 56;\n\t"
+      "add.s64 bk, %2, 896;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ak], bk, %3, pt;\n\t"
+      "}"
+      :
+      : "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // --------------------------------------------------------------------------
 // Arithmetic helpers
 // --------------------------------------------------------------------------
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Packed pair arithmetic (two fp32 lanes per instruction).
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack_f32x2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+// (a.lo*b.lo + c.lo, a.hi*b.hi + c.hi), round to nearest
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -313,4 +471,18 @@ __device__ __forceinline__ void tmem_st_x32(uint32_t taddr, const uint32_t* r) {
       : "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
+// Load 128 consecutive columns as four 32-column loads (four independent
+// 32-register destination blocks), then wait once.
+__device__ __forceinline__ void tmem_ld_x32x4_sync(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%128];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%129];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95}, [%130];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%131];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63]), "=r"(r[64]), "=r"(r[65]), "=r"(r[66]), "=r"(r[67]), "=r"(r[68]), "=r"(r[69]), "=r"(r[70]), "=r"(r[71]), "=r"(r[72]), "=r"(r[73]), "=r"(r[74]), "=r"(r[75]), "=r"(r[76]), "=r"(r[77]), "=r"(r[78]), "=r"(r[79]), "=r"(r[80]), "=r"(r[81]), "=r"(r[82]), "=r"(r[83]), "=r"(r[84]), "=r"(r[85]), "=r"(r[86]), "=r"(r[87]), "=r"(r[88]), "=r"(r[89]), "=r"(r[90]), "=r"(r[91]), "=r"(r[92]), "=r"(r[93]), "=r"(r[94]), "=r"(r[95]), "=r"(r[96]), "=r"(r[97]), "=r"(r[98]), "=r"(r[99]), "=r"(r[100]), "=r"(r[101]), "=r"(r[102]), "=r"(r[103]), "=r"(r[104]), "=r"(r[105]), "=r"(r[106]), "=r"(r[107]), "=r"(r[108]), "=r"(r[109]), "=r"(r[110]), "=r"(r[111]), "=r"(r[112]), "=r"(r[113]), "=r"(r[114]), "=r"(r[115]), "=r"(r[116]), "=r"(r[117]), "=r"(r[118]), "=r"(r[119]), "=r"(r[120]), "=r"(r[121]), "=r"(r[122]), "=r"(r[123]), "=r"(r[124]), "=r"(r[125]), "=r"(r[126]), "=r"(r[127])
+      : "r"(taddr), "r"(taddr + 32), "r"(taddr + 64), "r"(taddr + 96)
+      : "memory");
+}
+
 }  // namespace fa

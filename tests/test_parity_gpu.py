@@ -111,7 +111,7 @@ def test_zero_queries_uniform_weights(fa, causal):
 def test_causal_first_row_is_first_value_row(fa):
     q, k, v = make_random_qkv(2, 2, 200, 128, torch.bfloat16, seed=44)
     o, _ = _run(fa, q, k, v, 0.088, True)
-    assert torch.equal(o[:, :, 0, :].cpu(), v[:, :, 0, :])
+    _assert_first_row_is_v0(o, v)
 
 
 # ------------------------------------------- persistent scheduler, streams
@@ -195,8 +195,18 @@ def _workload_case(fa, wl, full):
     # properties that hold at any size, over every row
     assert torch.isfinite(o).all() and torch.isfinite(lse).all()
     if wl.causal:
-        assert torch.equal(o[:, :, 0, :].cpu(), v[:, :, 0, :])
+        _assert_first_row_is_v0(o, v)
     return err
+
+
+def _assert_first_row_is_v0(o, v):
+    """Causal row 0 attends to key 0 alone: O_0 = V_0 up to the output rounding."""
+    got = o[:, :, 0, :].float().cpu()
+    want = v[:, :, 0, :].float()
+    diff = (got - want).abs()
+    bad = (diff > 0).nonzero()
+    assert bad.numel() == 0, (f"{bad.shape[0]} elements of O[:,:,0,:] differ from V[:,:,0,:]; "
+                              f"max |diff| {diff.max().item():.3e}; first {bad[:4].tolist()}")
 
 
 @pytest.mark.parametrize("index", [w.index for w in WORKLOADS if w.d in (64, 128)])
