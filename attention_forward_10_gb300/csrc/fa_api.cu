@@ -11,18 +11,13 @@
 #include <mutex>
 
 #include "fa.h"
-#include "fa_fwd_kernel.cuh"
+#include "fa_common.cuh"
 #include "fa_launch.h"
 
 namespace fa {
 
 // Device status word: the kernels' bounded waits record a timeout here.
 __device__ int g_status_word;
-
-int fwd_smem_bytes(int d) {
-  return d == 64 ? static_cast<int>(Layout<64>::kSmemBytes)
-                 : static_cast<int>(Layout<128>::kSmemBytes);
-}
 
 // One CTA waits on a barrier nobody arrives on; the bounded wait must give
 // up, record the timeout and return.
@@ -100,19 +95,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // 4-D view of a contiguous [BH][N][d] 16-bit tensor for 128-byte-swizzled
 // tiles: dim0 = 64 elements (128 B, innermost), dim1 = N rows (stride d*2 B),
 // dim2 = d/64 column blocks (stride 128 B), dim3 = BH heads (stride N*d*2 B).
-// A box {64, 128, d/64, 1} lands in shared memory as [d/64][128][64], the
-// K-major layout the MMA descriptors expect; rows past N read as zero and
+// A box {64, rows, blocks, 1} lands in shared memory as [blocks][rows][64],
+// the K-major layout the MMA descriptors expect; rows past N read as zero and
 // are not written by stores.
-bool encode_qkvo_map(CUtensorMap* map, const void* base, int N, int d, int bh,
-                     bool bf16) {
+bool encode_qkvo_map(CUtensorMap* map, const void* base, int N, int d, int bh, bool bf16,
+                     int box_rows, int box_blocks) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(d / 64),
                         static_cast<cuuint64_t>(bh)};
   cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2, 128,
                            static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
-  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(kBlockM),
-                       static_cast<cuuint32_t>(d / 64), 1};
+  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_rows),
+                       static_cast<cuuint32_t>(box_blocks), 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                   4, const_cast<void*>(base), dims, strides, box, estr,
@@ -168,14 +163,17 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   if (dtype != FA_DTYPE_F16 && dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
   if (B == 0 || H == 0 || N == 0) return FA_OK;
   if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return FA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
     return FA_ERR_MISALIGNED;
   if (lse != nullptr && !aligned(lse, 4)) return FA_ERR_MISALIGNED;
   const long long bh = static_cast<long long>(B) * H;
-  const long long pairs = (static_cast<long long>(N) + kRowsPerUnit - 1) / kRowsPerUnit;
+  // work units per (b,h): pairs of 128-row query tiles (d <= 128) or single
+  // 128-row tiles (d = 256)
+  const int rows_per_unit = (d == 256) ? kBlockM : kRowsPerUnit;
+  const long long pairs = (static_cast<long long>(N) + rows_per_unit - 1) / rows_per_unit;
   if (bh >= (1ll << 31) || bh * pairs >= (1ll << 31)) return FA_ERR_INVALID_ARG;
 
   int dev = 0;
@@ -186,10 +184,14 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
 
   const bool bf16 = dtype == FA_DTYPE_BF16;
   FaParams p;
-  if (!encode_qkvo_map(&p.tm_q, q, N, d, static_cast<int>(bh), bf16) ||
-      !encode_qkvo_map(&p.tm_k, k, N, d, static_cast<int>(bh), bf16) ||
-      !encode_qkvo_map(&p.tm_v, v, N, d, static_cast<int>(bh), bf16) ||
-      !encode_qkvo_map(&p.tm_o, o, N, d, static_cast<int>(bh), bf16))
+  const int ibh = static_cast<int>(bh);
+  // d = 256 streams 64-key K/V tiles and stores O in two 128-column halves
+  const int kv_rows = (d == 256) ? 64 : kBlockN;
+  const int o_blocks = (d == 256) ? 2 : d / 64;
+  if (!encode_qkvo_map(&p.tm_q, q, N, d, ibh, bf16, kBlockM, d / 64) ||
+      !encode_qkvo_map(&p.tm_k, k, N, d, ibh, bf16, kv_rows, d / 64) ||
+      !encode_qkvo_map(&p.tm_v, v, N, d, ibh, bf16, kv_rows, d / 64) ||
+      !encode_qkvo_map(&p.tm_o, o, N, d, ibh, bf16, kBlockM, o_blocks))
     return FA_ERR_CUDA;
   p.lse = lse;
   p.status = info->status;
@@ -198,7 +200,7 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   p.num_bh = static_cast<int>(bh);
   p.num_pairs = static_cast<int>(pairs);
   p.num_units = static_cast<int>(bh * pairs);
-  p.n_ktiles = (N + kBlockN - 1) / kBlockN;
+  p.n_ktiles = (N + kv_rows - 1) / kv_rows;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
 
   int grid = info->num_sms;
@@ -207,8 +209,9 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   if (p.num_units < grid) grid = p.num_units;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = (d == 64) ? launch_fwd_d64(p, causal != 0, bf16, grid, s)
-                            : launch_fwd_d128(p, causal != 0, bf16, grid, s);
+  cudaError_t e = (d == 64)    ? launch_fwd_d64(p, causal != 0, bf16, grid, s)
+                  : (d == 128) ? launch_fwd_d128(p, causal != 0, bf16, grid, s)
+                               : launch_fwd_d256(p, causal != 0, bf16, grid, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

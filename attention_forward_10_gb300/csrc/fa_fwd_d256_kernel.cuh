@@ -1,0 +1,447 @@
+// fa_fwd_d256_kernel.cuh -- attention forward for head dimension 256 on
+// sm_103a (tcgen05, tensor memory, TMA); persistent and warp-specialised.
+//
+// Same computation as the d <= 128 kernel (the FlashAttention-2 forward of
+// LeetCUDA "flash_attn_mma_tiling_qk.cu": tile Q by rows, stream K/V tiles,
+// online row max / row sum with the running output rescaled by
+// exp(m_old - m_new), division by the row sum at the end; O stored with the
+// row LSE as in flash-attention "hopper/flash_fwd_kernel.h"), with a layout
+// chosen for d = 256, where the fp32 output tile alone takes half of tensor
+// memory:
+//
+//   work unit  one 128-row query tile of one (b,h)
+//   K/V tiles  64 keys (32 KB each at d = 256), a 4-slot ring in shared memory
+//   tensor memory (512 columns):
+//     [0,64) [64,128) [128,192)   S buffers 0,1,2 (scores of three
+//                                  consecutive K tiles; P, packed 16-bit,
+//                                  is written over the first 32 columns)
+//     [256,512)                   O (running output, fp32)
+//
+//   warps 0-3  softmax (one query row per thread)
+//   warp  4    TMA producer
+//   warp  5    MMA issuer: S(G) = Q K_G^T into buffer G mod 3, then
+//              P(G-1) V_(G-1) into O, over the stream of K tiles G
+//   warp  6    O store (the 128x256 output leaves through a 128x128 staging
+//              tile, in two halves)
+//   warp  7    spare
+//
+// With three S buffers, S(G) overwrites the columns of P(G-3), whose P V
+// product was issued two MMA groups earlier, so the wait for it is hidden;
+// the softmax of tile G-1 runs while S(G) executes.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "fa_common.cuh"
+#include "fa_params.h"
+#include "ptx.cuh"
+
+namespace fa {
+
+namespace d256 {
+
+constexpr int D = 256;
+constexpr int kBN = 64;                 // keys per K/V tile
+constexpr int kThreads = 256;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kStoreWarp = 6;
+constexpr int kSBufs = 3;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+constexpr uint32_t kQBytes = kBlockM * D * 2;   // 64 KB
+constexpr uint32_t kKVBytes = kBN * D * 2;      // 32 KB
+constexpr int kStages = 4;
+constexpr uint32_t kQOff = 0;
+constexpr uint32_t kKVOff = kQOff + kQBytes;
+constexpr uint32_t kStageOff = kKVOff + kStages * kKVBytes;
+constexpr uint32_t kStageBytes = kBlockM * 128 * 2;  // two 64-column blocks
+constexpr uint32_t kBarOff = kStageOff + kStageBytes;
+// barrier indices
+constexpr int kQFull = 0;
+constexpr int kQEmpty = 1;
+constexpr int kKVFull = 2;
+constexpr int kKVEmpty = kKVFull + kStages;
+constexpr int kSFull = kKVEmpty + kStages;    // per S buffer
+constexpr int kPFull = kSFull + kSBufs;       // per S buffer
+constexpr int kODone = kPFull + kSBufs;       // per S buffer: P(G) V done
+constexpr int kStageFull = kODone + kSBufs;
+constexpr int kStageEmpty = kStageFull + 1;
+constexpr int kDrain = kStageEmpty + 1;
+constexpr int kNumBars = kDrain + 1;
+constexpr uint32_t kCtlOff = kBarOff + kNumBars * 8;
+constexpr uint32_t kUsedBytes = kCtlOff + 16;
+constexpr uint32_t kSmemBytes = kUsedBytes + 1024;  // alignment slack
+static_assert(kSmemBytes <= 232448, "exceeds the shared memory of one CTA");
+constexpr uint32_t kOCol = 256;
+
+struct Unit {
+  int bh;
+  int row0;  // first query row of the tile
+  int nt;    // K/V tiles visited
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ Unit decode_unit(int u, const FaParams& p) {
+  Unit w;
+  int qt;
+  if (CAUSAL) {
+    qt = p.num_pairs - 1 - u / p.num_bh;  // heaviest first
+    w.bh = u % p.num_bh;
+  } else {
+    w.bh = u / p.num_pairs;
+    qt = u % p.num_pairs;
+  }
+  w.row0 = qt * kBlockM;
+  if (CAUSAL) {
+    const int last = min(p.N, w.row0 + kBlockM);
+    w.nt = (last + kBN - 1) / kBN;
+  } else {
+    w.nt = p.n_ktiles;
+  }
+  return w;
+}
+
+}  // namespace d256
+
+// p.num_pairs holds the number of 128-row query tiles per (b,h) and
+// p.n_ktiles the number of 64-key tiles for this kernel.
+template <bool CAUSAL, bool BF16>
+__global__ void __launch_bounds__(d256::kThreads, 1)
+    fa_fwd_d256_kernel(const __grid_constant__ FaParams p) {
+  using namespace d256;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  auto bar = [&](int i) -> uint32_t { return sbase + kBarOff + 8u * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kCtlOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kCtlOff + 4);
+  const Ctl ctl{abort_flag, p.status, p.timeout_ns};
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(kQFull), 1);
+    mbar_init(bar(kQEmpty), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar(kKVFull + s), 1);
+      mbar_init(bar(kKVEmpty + s), 1);
+    }
+    for (int b = 0; b < kSBufs; ++b) {
+      mbar_init(bar(kSFull + b), 1);
+      mbar_init(bar(kPFull + b), 128);
+      mbar_init(bar(kODone + b), 1);
+    }
+    mbar_init(bar(kStageFull), 128);
+    mbar_init(bar(kStageEmpty), 1);
+    mbar_init(bar(kDrain), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    tma_prefetch_map(&p.tm_q);
+    tma_prefetch_map(&p.tm_k);
+    tma_prefetch_map(&p.tm_v);
+    tma_prefetch_map(&p.tm_o);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kProducerWarp) {
+    // ---------------------------------------------------------------- TMA
+    if (lane == 0) {
+      uint32_t slot = 0, phase = 0, q_it = 0, issued = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+        const Unit w = decode_unit<CAUSAL>(u, p);
+        ok = wait_bar(bar(kQEmpty), (q_it & 1u) ^ 1u, ctl, kSiteProducerQ);
+        if (!ok) break;
+        mbar_arrive_expect_tx(bar(kQFull), kQBytes);
+        tma_load_4d(sbase + kQOff, &p.tm_q, bar(kQFull), 0, w.row0, 0, w.bh);
+        ++q_it;
+        for (int n = 0; n < w.nt && ok; ++n) {
+          for (int kv = 0; kv < 2; ++kv) {
+            ok = wait_bar(bar(kKVEmpty + slot), phase ^ 1u, ctl, kSiteProducerKV);
+            if (!ok) break;
+            mbar_arrive_expect_tx(bar(kKVFull + slot), kKVBytes);
+            tma_load_4d(sbase + kKVOff + slot * kKVBytes, kv ? &p.tm_v : &p.tm_k,
+                        bar(kKVFull + slot), 0, n * kBN, 0, w.bh);
+            ++issued;
+            if (++slot == (uint32_t)kStages) { slot = 0; phase ^= 1u; }
+          }
+        }
+      }
+      // Let every copy this warp issued land before the CTA may exit.
+      const uint32_t first = issued > (uint32_t)kStages ? issued - kStages : 0u;
+      for (uint32_t it = first; it < issued; ++it)
+        wait_drain(bar(kKVFull + it % kStages), (it / kStages) & 1u, p.timeout_ns);
+      if (q_it > 0) wait_drain(bar(kQFull), (q_it - 1) & 1u, p.timeout_ns);
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------------- MMA
+    if (lane == 0) {
+      constexpr uint32_t kIdescS = make_idesc_f16(kBlockM, kBN, BF16, false);
+      constexpr uint32_t kIdescO = make_idesc_f16(kBlockM, D, BF16, true);
+      constexpr uint32_t kSlotStep = kKVBytes >> 4;  // descriptor units
+      const uint64_t q_desc = smem_desc_sw128(sbase + kQOff, 16, 1024);
+      const uint64_t k_desc0 = smem_desc_sw128(sbase + kKVOff, 16, 1024);
+      // V (64 keys x 256): MN-major, 64-wide d blocks 64 keys x 128 B apart
+      // (LBO), 8-key groups 1024 B apart (SBO)
+      const uint64_t v_desc0 = smem_desc_sw128(sbase + kKVOff, kBN * 128, 1024);
+      uint32_t slot = 0, phase = 0, q_par = 0;
+      uint32_t G = 0;  // global index of the next K tile (S tile) of this CTA
+      bool ok = true;
+      // pending P V product: the previous K tile
+      bool pv_pending = false, pv_acc = false;
+      uint32_t pv_vslot = 0, pv_vphase = 0;
+      int u = blockIdx.x, n = 0;
+      Unit w = decode_unit<CAUSAL>(u < p.num_units ? u : 0, p);
+      while (ok) {
+        const bool cur_valid = u < p.num_units;
+        if (cur_valid) {
+          // ---- S(G) = Q K_G^T into buffer G mod 3
+          const uint32_t b = G % kSBufs;
+          if (n == 0) {
+            ok = wait_bar(bar(kQFull), q_par, ctl, kSiteMmaQ);
+            q_par ^= 1u;
+            if (!ok) break;
+          }
+          const uint32_t kslot = slot;
+          ok = wait_bar(bar(kKVFull + kslot), phase, ctl, kSiteMmaK);
+          if (!ok) break;
+          if (++slot == (uint32_t)kStages) { slot = 0; phase ^= 1u; }
+          if (G >= (uint32_t)kSBufs) {
+            // P(G-3) occupied buffer b: its P V product must have completed
+            ok = wait_bar(bar(kODone + b), ((G - kSBufs) / kSBufs) & 1u, ctl, kSiteMmaO);
+            if (!ok) break;
+          }
+          tc_fence_after_sync();
+          mma_ss_kmajor_x16_q128_k64(tmem + b * kBN, q_desc, k_desc0 + kslot * kSlotStep,
+                                     kIdescS, 0u);
+          tc_commit(bar(kSFull + b));
+          tc_commit(bar(kKVEmpty + kslot));
+          if (n == w.nt - 1) tc_commit(bar(kQEmpty));
+        }
+        if (pv_pending) {
+          // ---- O += P(G-1) V_(G-1)
+          const uint32_t pb = (G - 1) % kSBufs;
+          ok = wait_bar(bar(kKVFull + pv_vslot), pv_vphase, ctl, kSiteMmaV);
+          ok = ok && wait_bar(bar(kPFull + pb), ((G - 1) / kSBufs) & 1u, ctl, kSiteMmaP);
+          if (!ok) break;
+          tc_fence_after_sync();
+          mma_ts_mnmajor_x4(tmem + kOCol, tmem + pb * kBN, v_desc0 + pv_vslot * kSlotStep,
+                            kIdescO, pv_acc ? 1u : 0u);
+          tc_commit(bar(kODone + pb));
+          tc_commit(bar(kKVEmpty + pv_vslot));
+          pv_pending = false;
+        }
+        if (!cur_valid) break;
+        // V(G) is used in the next iteration
+        pv_pending = true;
+        pv_acc = n > 0;
+        pv_vslot = slot;
+        pv_vphase = phase;
+        if (++slot == (uint32_t)kStages) { slot = 0; phase ^= 1u; }
+        ++G;
+        if (++n == w.nt) {
+          n = 0;
+          u += gridDim.x;
+          if (u < p.num_units) w = decode_unit<CAUSAL>(u, p);
+        }
+      }
+      tc_commit(bar(kDrain));
+      wait_drain(bar(kDrain), 0, p.timeout_ns);
+    }
+    __syncwarp();
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ softmax
+    const int t = threadIdx.x;  // row within the query tile == TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t tO = tmem + lane_base + kOCol;
+    const uint32_t stage = sbase + kStageOff;
+    const float scale_log2 = p.scale_log2;
+    uint32_t G = 0, n_stores = 0;
+    bool ok = true;
+
+    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+      const Unit w = decode_unit<CAUSAL>(u, p);
+      const int row = w.row0 + t;
+      float m_ref = -INFINITY, l = 0.f;
+      for (int n = 0; n < w.nt; ++n, ++G) {
+        const uint32_t b = G % kSBufs;
+        const uint32_t tS = tmem + lane_base + b * kBN;
+        ok = wait_bar(bar(kSFull + b), (G / kSBufs) & 1u, ctl, kSiteSoftmaxS);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after_sync();
+        float s[kBN];
+        {
+          uint32_t r[32];
+          tmem_ld_x32_sync(tS, r);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) s[c] = __uint_as_float(r[c]);
+          tmem_ld_x32_sync(tS + 32, r);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) s[32 + c] = __uint_as_float(r[c]);
+        }
+        const int kbase = n * kBN;
+        const bool need_mask =
+            (kbase + kBN > p.N) || (CAUSAL && kbase + kBN - 1 > w.row0);
+        if (need_mask) {
+          int lim = p.N - kbase;
+          if (CAUSAL) lim = min(lim, row - kbase + 1);
+#pragma unroll
+          for (int c = 0; c < kBN; ++c)
+            if (c >= lim) s[c] = -INFINITY;
+        }
+        float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+        for (int c = 4; c < kBN; c += 4) {
+          mx0 = fmaxf(mx0, s[c]);
+          mx1 = fmaxf(mx1, s[c + 1]);
+          mx2 = fmaxf(mx2, s[c + 2]);
+          mx3 = fmaxf(mx3, s[c + 3]);
+        }
+        const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * scale_log2;
+
+        const bool need = m_tile > m_ref + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, need)) {
+          const float m_new = fmaxf(m_ref, m_tile);
+          const float factor = (m_new == -INFINITY) ? 1.f : ex2_approx(m_ref - m_new);
+          if (n > 0) {
+            // O holds the previous tiles' sum: wait for P(G-1) V, rescale
+            const uint32_t pb = (G - 1) % kSBufs;
+            ok = wait_bar(bar(kODone + pb), ((G - 1) / kSBufs) & 1u, ctl, kSiteSoftmaxO);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after_sync();
+#pragma unroll 1
+            for (int c = 0; c < D; c += 32) {
+              uint32_t o[32];
+              tmem_ld_x32_sync(tO + c, o);
+#pragma unroll
+              for (int e = 0; e < 32; ++e)
+                o[e] = __float_as_uint(__uint_as_float(o[e]) * factor);
+              tmem_st_x32(tO + c, o);
+            }
+            tmem_wait_st();
+          }
+          l *= factor;
+          m_ref = m_new;
+        }
+
+        const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+        const uint64_t scale2 = pack_f32x2(scale_log2, scale_log2);
+        const uint64_t neg_m2 = pack_f32x2(-m_use, -m_use);
+        uint64_t acc_a = pack_f32x2(0.f, 0.f), acc_b = acc_a;
+#pragma unroll
+        for (int c0 = 0; c0 < kBN; c0 += 32) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            float x0, x1;
+            unpack_f32x2(fma_f32x2(pack_f32x2(s[c0 + 2 * e], s[c0 + 2 * e + 1]), scale2, neg_m2),
+                         x0, x1);
+            const float p0 = ex2_approx(x0);
+            const float p1 = ex2_approx(x1);
+            if (e & 1)
+              acc_b = add_f32x2(acc_b, pack_f32x2(p0, p1));
+            else
+              acc_a = add_f32x2(acc_a, pack_f32x2(p0, p1));
+            pk[e] = pack2<BF16>(p0, p1);
+          }
+          tmem_st_x16(tS + c0 / 2, pk);
+        }
+        tmem_wait_st();
+        {
+          float a0, a1;
+          unpack_f32x2(add_f32x2(acc_a, acc_b), a0, a1);
+          l += a0 + a1;
+        }
+        tc_fence_before_sync();
+        mbar_arrive(bar(kPFull + b));
+      }
+      if (!ok) break;
+
+      // ---------------------------------------------------------- epilogue
+      const uint32_t last = G - 1;
+      ok = wait_bar(bar(kODone + last % kSBufs), (last / kSBufs) & 1u, ctl, kSiteEpilogueO);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after_sync();
+      const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+      for (int half = 0; half < 2 && ok; ++half) {
+        // the staging tile must have been read by the store before this one
+        ok = wait_bar(bar(kStageEmpty), (n_stores - 1) & 1u, ctl, kSiteEpilogueO);
+        ok = __all_sync(0xffffffffu, ok);
+        ++n_stores;
+        if (!ok) break;
+#pragma unroll 1
+        for (int c = 0; c < 128; c += 32) {
+          uint32_t o[32];
+          tmem_ld_x32_sync(tO + half * 128 + c, o);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint32_t w4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              w4[e] = pack2<BF16>(__uint_as_float(o[8 * j + 2 * e]) * inv_l,
+                                  __uint_as_float(o[8 * j + 2 * e + 1]) * inv_l);
+            const int c16 = c / 8 + j;  // 16-byte chunk within the half row
+            const uint32_t addr = stage + (c16 / 8) * (kBlockM * 128) + t * 128 +
+                                  (((c16 % 8) ^ (t & 7)) << 4);
+            st_shared_v4(addr, w4[0], w4[1], w4[2], w4[3]);
+          }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bar(kStageFull));
+      }
+      if (p.lse != nullptr && row < p.N) {
+        p.lse[static_cast<size_t>(w.bh) * p.N + row] =
+            (l > 0.f) ? (m_ref + log2f(l)) * 0.6931471805599453f : -INFINITY;
+      }
+    }
+    __syncwarp();
+  } else if (warp == kStoreWarp) {
+    // ------------------------------------------------------------ O store
+    if (lane == 0) {
+      uint32_t full_par = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+        const Unit w = decode_unit<CAUSAL>(u, p);
+        for (int half = 0; half < 2 && ok; ++half) {
+          ok = wait_bar(bar(kStageFull), full_par, ctl, kSiteStore);
+          full_par ^= 1u;
+          if (!ok) break;
+          // columns [128*half, 128*half + 128) = d blocks 2*half, 2*half + 1
+          tma_store_4d(&p.tm_o, sbase + kStageOff, 0, w.row0, 2 * half, w.bh);
+          bulk_commit_group();
+          bulk_wait_read_all();
+          mbar_arrive(bar(kStageEmpty));
+        }
+      }
+      bulk_wait_all();
+    }
+    __syncwarp();
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace fa

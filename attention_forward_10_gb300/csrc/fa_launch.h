@@ -8,13 +8,15 @@
 
 namespace fa {
 
-// Dynamic shared memory one CTA of the forward kernel needs for head dim d.
-int fwd_smem_bytes(int d);
 
-// Enqueue the forward kernel for head dim 64 / 128 with `grid` persistent CTAs.
+// Enqueue the forward kernel for head dim 64 / 128 with `grid` persistent CTAs
+// (two 128-row query tiles per work unit, 128-key K/V tiles).
 cudaError_t launch_fwd_d64(const FaParams& p, bool causal, bool bf16, int grid,
                            cudaStream_t stream);
 cudaError_t launch_fwd_d128(const FaParams& p, bool causal, bool bf16, int grid,
+                            cudaStream_t stream);
+// Head dim 256: one 128-row query tile per work unit, 64-key K/V tiles.
+cudaError_t launch_fwd_d256(const FaParams& p, bool causal, bool bf16, int grid,
                             cudaStream_t stream);
 
 // Enqueue the watchdog self-test kernel (one CTA).

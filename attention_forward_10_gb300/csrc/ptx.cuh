@@ -357,6 +357,93 @@ __device__ __forceinline__ void mma_ts_mnmajor_x8(uint32_t d_tmem, uint32_t a_tm
       : "memory");
 }
 
+// 16 back-to-back K=16 MMAs D (+)= A*B^T over a 256-wide reduction: A a K-major
+// 128B-swizzled 128-row tile (64-element column blocks 16 KB apart), B a
+// K-major 64-row tile (column blocks 8 KB apart).  First step overwrites D
+// unless `accumulate`.
+__device__ __forceinline__ void mma_ss_kmajor_x16_q128_k64(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred pf, pt;\n\t.reg .b64 ak, bk;\n\t"
+      "setp.ne.b32 pf, %4, 0;\n\t"
+      "setp.eq.b32 pt, %4, %4;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, pf;\n\t"
+      "add.s64 ak, %1, 2;\n\t"
+      "add.s64 bk, %2, 2;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ak, bk, %3, pt;\n\t"
+      "add.s64 ak, %1, 4;\n\t"
+      "add.s64 bk, %2, 4;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ak, bk, %3, pt;\n\t"
+      "add.s64 ak, %1, 6;\n\t"
+      "add.s64 bk, %2, 6;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ak, bk, %3, pt;\n\t"
+      "add.s64 ak, %1, 1024;\n\t"
+      "add.s64 bk, %2, 512;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ak, bk, %3, pt;\n\t"
+      "add.s64 ak, %1, 1026;\n\t"
+      "add.s64 bk, %2, 514;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ak, bk, %3, pt;\n\t"
+      "add.s64 ak, %1, 1028;\n\t"
+      "add.s64 bk, %2, 516;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ak, bk, %3, pt;\n\t"
+      "add.s64 ak, %1, 1030;\n\t"
+      "add.s64 bk, %2, 518;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ak, bk, %3, pt;\n\t"
+      "add.s64 ak, %1, 2048;\n\t"
+      "add.s64 bk, %2, 1024;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ak, bk, %3, pt;\n\t"
+      "add.s64 ak, %1, 2050;\n\t"
+      "add.s64 bk, %2, 1026;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ak, bk, %3, pt;\n\t"
+      "add.s64 ak, %1, 2052;\n\t"
+      "add.s64 bk, %2, 1028;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ak, bk, %3, pt;\n\t"
+      "add.s64 ak, %1, 2054;\n\t"
+      "add.s64 bk, %2, 1030;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ak, bk, %3, pt;\n\t"
+      "add.s64 ak, %1, 3072;\n\t"
+      "add.s64 bk, %2, 1536;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ak, bk, %3, pt;\n\t"
+      "add.s64 ak, %1, 3074;\n\t"
+      "add.s64 bk, %2, 1538;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ak, bk, %3, pt;\n\t"
+      "add.s64 ak, %1, 3076;\n\t"
+      "add.s64 bk, %2, 1540;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ak, bk, %3, pt;\n\t"
+      "add.s64 ak, %1, 3078;\n\t"
+      "add.s64 bk, %2, 1542;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], ak, bk, %3, pt;\n\t"
+      "}"
+      :
+      : "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 4 back-to-back K=16 MMAs D (+)= A*B, A in tensor memory (step k reads
+// columns a_tmem + 8k), B an MN-major 128B-swizzled tile with 16-row steps
+// 2048 bytes apart.  First step overwrites D unless `accumulate`.
+__device__ __forceinline__ void mma_ts_mnmajor_x4(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred pf, pt;\n\t.reg .b64 bk;\n\t.reg .b32 ak;\n\t"
+      "setp.ne.b32 pf, %4, 0;\n\t"
+      "setp.eq.b32 pt, %4, %4;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, pf;\n\t"
+      "add.u32 ak, %1, 8;\n\t"
+      "add.s64 bk, %2, 128;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ak], bk, %3, pt;\n\t"
+      "add.u32 ak, %1, 16;\n\t"
+      "add.s64 bk, %2, 256;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ak], bk, %3, pt;\n\t"
+      "add.u32 ak, %1, 24;\n\t"
+      "add.s64 bk, %2, 384;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ak], bk, %3, pt;\n\t"
+      "}"
+      :
+      : "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // --------------------------------------------------------------------------
 // Arithmetic helpers
 // --------------------------------------------------------------------------

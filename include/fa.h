@@ -68,7 +68,7 @@ typedef enum {
  *   B, H, N  batch, heads, sequence length.  Any of them 0: nothing is done
  *            and FA_OK is returned (pointers are not touched).  Negative:
  *            FA_ERR_INVALID_ARG.  B*H must be < 2^31 and N < 2^31.
- *   d        head dimension: 64 or 128 (other values: FA_ERR_UNSUPPORTED).
+ *   d        head dimension: 64, 128 or 256 (other values: FA_ERR_UNSUPPORTED).
  *   scale    softmax scale applied to Q.K^T; must be finite and > 0
  *            (1/sqrt(d) is the usual choice).
  *   causal   0: every query sees every key; 1: query i sees keys 0..i.

@@ -54,8 +54,8 @@ def _check(o, lse, o_ref, lse_ref, what):
 # ------------------------------------------------------------ small, full
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16], ids=["bf16", "fp16"])
 @pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
-@pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("N", [1, 5, 64, 127, 128, 129, 255, 256, 257, 384, 640])
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("N", [1, 5, 63, 64, 65, 127, 128, 129, 255, 256, 257, 384, 640])
 def test_small_shapes_full_compare(fa, N, d, causal, dtype):
     q, k, v = make_random_qkv(1, 2, N, d, dtype, seed=100 + N + d)
     scale = 1.0 / math.sqrt(d)
@@ -64,23 +64,25 @@ def test_small_shapes_full_compare(fa, N, d, causal, dtype):
     _check(o, lse, o_ref, lse_ref, f"N={N} d={d} causal={causal} {dtype}")
 
 
+@pytest.mark.parametrize("d", [128, 256])
 @pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
-def test_peaky_scores_trigger_rescale(fa, causal):
+def test_peaky_scores_trigger_rescale(fa, causal, d):
     """Large scores make the running maximum jump across tiles (O rescales)."""
-    q, k, v = make_random_qkv(2, 2, 700, 128, torch.bfloat16, seed=31, qk_mult=4.0)
+    q, k, v = make_random_qkv(2, 2, 700, d, torch.bfloat16, seed=31, qk_mult=4.0)
     # a growing ramp of key norms so later tiles keep raising the maximum
     ramp = torch.linspace(0.2, 3.0, 700).to(torch.bfloat16)[None, None, :, None]
     k = (k * ramp).to(torch.bfloat16)
-    scale = 1.0 / math.sqrt(128)
+    scale = 1.0 / math.sqrt(d)
     o, lse = _run(fa, q, k, v, scale, causal)
     o_ref, lse_ref = oracle.attention(q, k, v, scale, causal)
     _check(o, lse, o_ref, lse_ref, "peaky")
 
 
 # ------------------------------------------------------ structured inputs
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
-def test_constant_values_give_constant_output(fa, causal):
-    q, k, _ = make_random_qkv(1, 3, 300, 128, torch.bfloat16, seed=41)
+def test_constant_values_give_constant_output(fa, causal, d):
+    q, k, _ = make_random_qkv(1, 3, 300, d, torch.bfloat16, seed=41)
     v = torch.full_like(q, 0.625)
     o, _ = _run(fa, q, k, v, 0.088, causal)
     assert torch.all(o.float().cpu() == 0.625)
@@ -108,18 +110,20 @@ def test_zero_queries_uniform_weights(fa, causal):
     _check(o, lse, o_ref, np.log(np.broadcast_to(n, (1, 2, 333)).astype(float)), "Q=0")
 
 
-def test_causal_first_row_is_first_value_row(fa):
-    q, k, v = make_random_qkv(2, 2, 200, 128, torch.bfloat16, seed=44)
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_causal_first_row_is_first_value_row(fa, d):
+    q, k, v = make_random_qkv(2, 2, 200, d, torch.bfloat16, seed=44)
     o, _ = _run(fa, q, k, v, 0.088, True)
     _assert_first_row_is_v0(o, v)
 
 
 # ------------------------------------------- persistent scheduler, streams
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("ctas", [1, 2, 3, 7])
 @pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
-def test_persistent_loop_many_units_per_cta(fa, ctas, causal):
-    q, k, v = make_random_qkv(2, 3, 1000, 128, torch.bfloat16, seed=50 + ctas)
-    scale = 1.0 / math.sqrt(128)
+def test_persistent_loop_many_units_per_cta(fa, ctas, causal, d):
+    q, k, v = make_random_qkv(2, 3, 1000, d, torch.bfloat16, seed=50 + ctas)
+    scale = 1.0 / math.sqrt(d)
     fa.fa_set_max_ctas(ctas)
     try:
         o, lse = _run(fa, q, k, v, scale, causal)
@@ -209,7 +213,7 @@ def _assert_first_row_is_v0(o, v):
                               f"max |diff| {diff.max().item():.3e}; first {bad[:4].tolist()}")
 
 
-@pytest.mark.parametrize("index", [w.index for w in WORKLOADS if w.d in (64, 128)])
+@pytest.mark.parametrize("index", [w.index for w in WORKLOADS])
 def test_workload(fa, index):
     wl = workload(index)
     full = wl.B * wl.H * wl.N * wl.N * wl.d <= 4 * 16 * 2048 * 2048 * 128
