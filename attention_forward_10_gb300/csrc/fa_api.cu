@@ -174,7 +174,8 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   // 128-row tiles (d = 256)
   const int rows_per_unit = (d == 256) ? kBlockM : kRowsPerUnit;
   const long long pairs = (static_cast<long long>(N) + rows_per_unit - 1) / rows_per_unit;
-  if (bh >= (1ll << 31) || bh * pairs >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+  // (headroom: the last-wave split below may add up to one wave of units)
+  if (bh >= (1ll << 31) || bh * pairs + 4096 >= (1ll << 31)) return FA_ERR_INVALID_ARG;
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
@@ -206,6 +207,17 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   int grid = info->num_sms;
   const int cap = g_max_ctas.load();
   if (cap > 0 && cap < grid) grid = cap;
+  p.num_pair_units = p.num_units;
+  if (d != 256) {
+    // Balance the last wave: its L pair units become 2L single-tile units
+    // when those fit in one wave.
+    const long long pair_units = bh * pairs;
+    const long long partial = pair_units % grid;
+    if (pair_units > grid && partial > 0 && 2 * partial <= grid) {
+      p.num_pair_units = static_cast<int>(pair_units - partial);
+      p.num_units = static_cast<int>(pair_units + partial);
+    }
+  }
   if (p.num_units < grid) grid = p.num_units;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -115,25 +115,36 @@ struct Unit {
   int ntot;     // K/V tiles streamed for the unit = max(nt)
 };
 
+// Units [0, num_pair_units) are query-tile pairs.  When the pairs do not
+// fill the last wave of CTAs evenly, the pairs of that partial wave are split
+// instead into single-tile units (tile 0 only), one per CTA, which halves
+// the length of the last wave.
 template <bool CAUSAL>
 __device__ __forceinline__ Unit decode_unit(int u, const FaParams& p) {
   Unit w;
+  int pu = u, single = -1;  // pair-unit index; tile of a single-tile unit
+  if (u >= p.num_pair_units) {
+    pu = p.num_pair_units + (u - p.num_pair_units) / 2;
+    single = (u - p.num_pair_units) % 2;
+  }
   int pair;
   if (CAUSAL) {
     // heaviest first: the last query pairs of every head come first
-    pair = p.num_pairs - 1 - u / p.num_bh;
-    w.bh = u % p.num_bh;
+    pair = p.num_pairs - 1 - pu / p.num_bh;
+    w.bh = pu % p.num_bh;
   } else {
     // consecutive units share a head, so its K/V stay hot in L2
-    w.bh = u / p.num_pairs;
-    pair = u % p.num_pairs;
+    w.bh = pu / p.num_pairs;
+    pair = pu % p.num_pairs;
   }
   w.ntot = 0;
 #pragma unroll
   for (int g = 0; g < 2; ++g) {
-    const int r0 = pair * kRowsPerUnit + g * kBlockM;
+    // a single-tile unit carries its tile in slot 0
+    const int r0 = (single < 0) ? pair * kRowsPerUnit + g * kBlockM
+                                : pair * kRowsPerUnit + single * kBlockM;
     w.row0[g] = r0;
-    if (r0 >= p.N) {
+    if (r0 >= p.N || (single >= 0 && g == 1)) {
       w.nt[g] = 0;
     } else if (CAUSAL) {
       const int last = min(p.N, r0 + kBlockM);  // rows r0..last-1 see keys < last
@@ -263,6 +274,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       uint32_t prev_vslot = 0;
       int u = blockIdx.x, n = 0;
       Unit w = decode_unit<CAUSAL>(u < p.num_units ? u : 0, p);
+      // units without K/V tiles (a split-off tile past N) stream nothing
+      while (u < p.num_units && w.ntot == 0) {
+        u += gridDim.x;
+        if (u < p.num_units) w = decode_unit<CAUSAL>(u, p);
+      }
       while (ok) {
         const bool cur_valid = u < p.num_units;
         if (!cur_valid && !prev_valid) break;
@@ -327,8 +343,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         prev_vslot = vslot;
         if (++n == w.ntot) {
           n = 0;
-          u += gridDim.x;
-          if (u < p.num_units) w = decode_unit<CAUSAL>(u, p);
+          do {
+            u += gridDim.x;
+            if (u < p.num_units) w = decode_unit<CAUSAL>(u, p);
+          } while (u < p.num_units && w.ntot == 0);
         }
       }
       // Every MMA issued must complete before tensor memory is released.

@@ -42,7 +42,9 @@ struct FaParams {  // 64-byte aligned through CUtensorMap
   int N;             // sequence length
   int num_bh;        // B*H
   int num_pairs;     // ceil(N / 256): work units per (b,h)
-  int num_units;     // num_bh * num_pairs
+  int num_units;     // work units (see num_pair_units)
+  int num_pair_units;  // units below this index are query-tile pairs; the
+                       // rest are single tiles (d <= 128 kernel)
   int n_ktiles;      // ceil(N / 128)
   float scale_log2;  // softmax scale * log2(e)
 };

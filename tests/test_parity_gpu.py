@@ -133,6 +133,21 @@ def test_persistent_loop_many_units_per_cta(fa, ctas, causal, d):
     _check(o, lse, o_ref, lse_ref, f"ctas={ctas}")
 
 
+@pytest.mark.parametrize("ctas,N", [(5, 1024), (5, 900), (5, 800), (7, 2000), (30, 4096)])
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+def test_last_wave_split_into_single_tiles(fa, ctas, N, causal):
+    """Pair units of a partial last wave run as single-tile units."""
+    q, k, v = make_random_qkv(1, 3, N, 128, torch.bfloat16, seed=70 + ctas + N)
+    scale = 1.0 / math.sqrt(128)
+    fa.fa_set_max_ctas(ctas)
+    try:
+        o, lse = _run(fa, q, k, v, scale, causal)
+    finally:
+        fa.fa_set_max_ctas(0)
+    o_ref, lse_ref = oracle.attention(q, k, v, scale, causal)
+    _check(o, lse, o_ref, lse_ref, f"ctas={ctas} N={N}")
+
+
 def test_side_stream_and_no_lse(fa):
     q, k, v = make_random_qkv(1, 2, 260, 64, torch.bfloat16, seed=60)
     qd, kd, vd = (t.cuda() for t in (q, k, v))
