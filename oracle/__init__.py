@@ -20,6 +20,11 @@ softmax along keys, final division by the row sum) and flash-attention
 log-normaliser of the scaled scores) and "hopper/flash_fwd_kernel.h" (an empty
 row stores O = 0 and LSE = -inf).
 
+``attention_ex`` adds grouped K/V heads (query head h reads K/V head
+h // (H / H_kv)) and a local window (keys i - window_left .. i + window_right),
+the ``qhead_per_khead`` and ``window_size_left/right`` options of the same
+backward page.
+
 Pins (checked by ``tests/test_oracle.py`` against facts other than this code):
 closed forms (N = 1, Q = 0, hand-derived golden example), invariants (row
 probabilities sum to one, constant V, key/value permutation, per-row shift of
@@ -76,6 +81,14 @@ def _bind(path: str):
                                      c_long, c_double, c_int, vp, vp,
                                      c_int]
     lib.attn_ref_fwd_f64.restype = c_int
+    lib.attn_ref_fwd_u16_ex.argtypes = [vp, vp, vp, c_int, c_long, c_long, c_long,
+                                        c_long, c_long, c_double, c_int, c_long,
+                                        c_long, vp, vp, c_int]
+    lib.attn_ref_fwd_u16_ex.restype = c_int
+    lib.attn_ref_rows_u16_ex.argtypes = [vp, vp, vp, c_int, c_long, c_long, c_long,
+                                         c_long, c_long, c_double, c_int, c_long,
+                                         c_long, vp, c_long, vp, vp, c_int]
+    lib.attn_ref_rows_u16_ex.restype = c_int
     lib.attn_ref_widen.argtypes = [ctypes.c_uint16, c_int]
     lib.attn_ref_widen.restype = c_double
     lib.attn_ref_max_threads.argtypes = []
@@ -187,4 +200,58 @@ def attention_f64(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float,
                                   _ptr(lse), int(nthreads))
     if rc != 0:
         raise RuntimeError("oracle attn_ref_fwd_f64 failed")
+    return o, lse
+
+
+def _check_ex(q, k, v):
+    B, H, N, d = (int(x) for x in q.shape)
+    Bk, H_kv, Nk, dk = (int(x) for x in k.shape)
+    if (Bk, Nk, dk) != (B, N, d) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("k, v must be [B, H_kv, N, d] matching q's B, N, d")
+    if H_kv <= 0 or H % H_kv != 0:
+        raise ValueError("H must be a multiple of H_kv")
+    return B, H, H_kv, N, d
+
+
+def attention_ex(q, k, v, scale: float, causal: bool, window_left: int = -1,
+                 window_right: int = -1, nthreads: int = 0):
+    """O and LSE with grouped K/V heads ([B, H_kv, N, d]) and a local window.
+
+    Query i sees keys j with i - window_left <= j <= i + window_right
+    (negative bound: unbounded), and j <= i when causal.
+    """
+    qw, is_bf16 = _u16_view(q)
+    kw, _ = _u16_view(k)
+    vw, _ = _u16_view(v)
+    B, H, H_kv, N, d = _check_ex(q, k, v)
+    o = np.empty((B, H, N, d), dtype=np.float64)
+    lse = np.empty((B, H, N), dtype=np.float64)
+    rc = _load().attn_ref_fwd_u16_ex(_ptr(qw), _ptr(kw), _ptr(vw), int(is_bf16), B, H,
+                                     H_kv, N, d, float(scale), int(bool(causal)),
+                                     int(window_left), int(window_right), _ptr(o),
+                                     _ptr(lse), int(nthreads))
+    if rc != 0:
+        raise RuntimeError("oracle attn_ref_fwd_u16_ex failed")
+    return o, lse
+
+
+def attention_rows_ex(q, k, v, scale: float, causal: bool, rows, window_left: int = -1,
+                      window_right: int = -1, nthreads: int = 0):
+    """attention_ex for the listed (b, h, i) triples only."""
+    qw, is_bf16 = _u16_view(q)
+    kw, _ = _u16_view(k)
+    vw, _ = _u16_view(v)
+    B, H, H_kv, N, d = _check_ex(q, k, v)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 3))
+    n = rows.shape[0]
+    o = np.empty((n, d), dtype=np.float64)
+    lse = np.empty((n,), dtype=np.float64)
+    if n == 0:
+        return o, lse
+    rc = _load().attn_ref_rows_u16_ex(_ptr(qw), _ptr(kw), _ptr(vw), int(is_bf16), B, H,
+                                      H_kv, N, d, float(scale), int(bool(causal)),
+                                      int(window_left), int(window_right), _ptr(rows), n,
+                                      _ptr(o), _ptr(lse), int(nthreads))
+    if rc != 0:
+        raise RuntimeError("oracle attn_ref_rows_u16_ex failed")
     return o, lse

@@ -33,6 +33,13 @@
  * The LSE is reported in natural-log units (the Hopper pages keep a base-2
  * copy for their backward pass; ln 2 times that is the same quantity).
  *
+ * Two generalisations, both from the same backward page: grouped K/V heads
+ * (query head h reads K/V head h / (H / H_kv): the page's
+ * qhead_per_khead) and a local window (query i sees keys j with
+ * i - window_left <= j <= i + window_right; a negative bound is unbounded:
+ * the page's window_size_left / window_size_right and its Is_local mask).
+ * With H_kv = H and both bounds negative they reduce to the definition above.
+ *
  * Inputs are the caller's 16-bit words (IEEE binary16 or bfloat16), widened
  * exactly to double here; every product, sum and exponential is in double.
  * The computation is the textbook two-pass softmax per row -- no tiling, no
@@ -92,20 +99,20 @@ int attn_ref_max_threads(void) {
 /* ------------------------------------------------------------------ */
 /* One query row against one (b,h) slice, all in double.                */
 /*   q_row [d], kmat [N][d], vmat [N][d], scores: scratch of N doubles. */
+/*   Admissible keys: j0 <= j < j1.                                     */
 /* ------------------------------------------------------------------ */
-static void attend_row(const double *q_row, const double *kmat,
-                       const double *vmat, long N, long d, long i,
-                       double scale, int causal, double *scores,
-                       double *o_row, double *lse_out) {
-    long nkeys = causal ? (i + 1 < N ? i + 1 : N) : N; /* |J(i)| */
-    if (nkeys <= 0) {                 /* no admissible key: O = 0, LSE = -inf */
+static void attend_range(const double *q_row, const double *kmat,
+                         const double *vmat, long d, long j0, long j1,
+                         double scale, double *scores, double *o_row,
+                         double *lse_out) {
+    if (j1 <= j0) {                   /* no admissible key: O = 0, LSE = -inf */
         for (long c = 0; c < d; ++c) o_row[c] = 0.0;
         *lse_out = -INFINITY;
         return;
     }
     /* pass 1: scaled scores and their maximum */
     double m = -INFINITY;
-    for (long j = 0; j < nkeys; ++j) {
+    for (long j = j0; j < j1; ++j) {
         const double *k_row = kmat + j * d;
         double dot = 0.0;
         for (long c = 0; c < d; ++c) dot += q_row[c] * k_row[c];
@@ -115,16 +122,36 @@ static void attend_row(const double *q_row, const double *kmat,
     }
     /* pass 2: log-normaliser */
     double sum = 0.0;
-    for (long j = 0; j < nkeys; ++j) sum += exp(scores[j] - m);
+    for (long j = j0; j < j1; ++j) sum += exp(scores[j] - m);
     double lse = m + log(sum);
     /* pass 3: probability-weighted sum of value rows */
     for (long c = 0; c < d; ++c) o_row[c] = 0.0;
-    for (long j = 0; j < nkeys; ++j) {
+    for (long j = j0; j < j1; ++j) {
         double p = exp(scores[j] - lse);
         const double *v_row = vmat + j * d;
         for (long c = 0; c < d; ++c) o_row[c] += p * v_row[c];
     }
     *lse_out = lse;
+}
+
+/* Admissible keys of query i: [j0, j1). */
+static void key_range(long N, long i, int causal, long wl, long wr,
+                      long *j0, long *j1) {
+    long lo = 0, hi = N;                          /* full attention */
+    if (causal && i + 1 < hi) hi = i + 1;         /* keys 0..i */
+    if (wl >= 0 && i - wl > lo) lo = i - wl;      /* keys >= i - wl */
+    if (wr >= 0 && i + wr + 1 < hi) hi = i + wr + 1;  /* keys <= i + wr */
+    *j0 = lo;
+    *j1 = hi;
+}
+
+static void attend_row(const double *q_row, const double *kmat,
+                       const double *vmat, long N, long d, long i,
+                       double scale, int causal, double *scores,
+                       double *o_row, double *lse_out) {
+    long j0, j1;
+    key_range(N, i, causal, -1, -1, &j0, &j1);
+    attend_range(q_row, kmat, vmat, d, j0, j1, scale, scores, o_row, lse_out);
 }
 
 static void widen_slice(const uint16_t *src, double *dst, long count,
@@ -267,5 +294,107 @@ int attn_ref_fwd_f64(const double *q, const double *k, const double *v,
             }
         }
     }
+    return rc;
+}
+
+/*
+ * Grouped heads and a local window.
+ *   q, o : [B][H][N][d];  k, v : [B][H_kv][N][d];  lse : [B][H][N]
+ *   H must be a multiple of H_kv; window bounds < 0 mean unbounded.
+ * Full evaluation (_fwd) or listed (b, h, i) rows (_rows), as above.
+ */
+int attn_ref_fwd_u16_ex(const uint16_t *q, const uint16_t *k,
+                        const uint16_t *v, int is_bf16, long B, long H,
+                        long H_kv, long N, long d, double scale, int causal,
+                        long wl, long wr, double *o, double *lse,
+                        int nthreads) {
+    if (!q || !k || !v || !o || !lse || B < 0 || H <= 0 || H_kv <= 0 ||
+        H % H_kv != 0 || N < 0 || d <= 0)
+        return -1;
+    set_threads(nthreads);
+    long slice = N * d, group = H / H_kv;
+    double *qd = (double *)malloc(sizeof(double) * (size_t)(slice > 0 ? slice : 1));
+    double *kd = (double *)malloc(sizeof(double) * (size_t)(slice > 0 ? slice : 1));
+    double *vd = (double *)malloc(sizeof(double) * (size_t)(slice > 0 ? slice : 1));
+    if (!qd || !kd || !vd) { free(qd); free(kd); free(vd); return -1; }
+    int rc = 0;
+    for (long b = 0; b < B && rc == 0; ++b) {
+        for (long h = 0; h < H && rc == 0; ++h) {
+            long bh = b * H + h, bkv = b * H_kv + h / group;
+            widen_slice(q + bh * slice, qd, slice, is_bf16);
+            widen_slice(k + bkv * slice, kd, slice, is_bf16);
+            widen_slice(v + bkv * slice, vd, slice, is_bf16);
+#pragma omp parallel
+            {
+                double *scores = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+                if (!scores) {
+#pragma omp atomic write
+                    rc = -1;
+                } else {
+#pragma omp for schedule(dynamic, 4)
+                    for (long i = 0; i < N; ++i) {
+                        long j0, j1;
+                        key_range(N, i, causal, wl, wr, &j0, &j1);
+                        attend_range(qd + i * d, kd, vd, d, j0, j1, scale, scores,
+                                     o + (bh * N + i) * d, lse + bh * N + i);
+                    }
+                    free(scores);
+                }
+            }
+        }
+    }
+    free(qd); free(kd); free(vd);
+    return rc;
+}
+
+int attn_ref_rows_u16_ex(const uint16_t *q, const uint16_t *k,
+                         const uint16_t *v, int is_bf16, long B, long H,
+                         long H_kv, long N, long d, double scale, int causal,
+                         long wl, long wr, const long *rows, long n_rows,
+                         double *o_rows, double *lse_rows, int nthreads) {
+    if (!q || !k || !v || !rows || !o_rows || !lse_rows || N <= 0 || d <= 0 ||
+        H <= 0 || H_kv <= 0 || H % H_kv != 0)
+        return -1;
+    for (long r = 0; r < n_rows; ++r) {
+        long b = rows[3 * r], h = rows[3 * r + 1], i = rows[3 * r + 2];
+        if (b < 0 || b >= B || h < 0 || h >= H || i < 0 || i >= N) return -1;
+    }
+    set_threads(nthreads);
+    long slice = N * d, group = H / H_kv;
+    double *kd = (double *)malloc(sizeof(double) * (size_t)slice);
+    double *vd = (double *)malloc(sizeof(double) * (size_t)slice);
+    char *done = (char *)calloc((size_t)(n_rows > 0 ? n_rows : 1), 1);
+    if (!kd || !vd || !done) { free(kd); free(vd); free(done); return -1; }
+    int rc = 0;
+    for (long r0 = 0; r0 < n_rows && rc == 0; ++r0) {
+        if (done[r0]) continue;
+        long bkv = rows[3 * r0] * H_kv + rows[3 * r0 + 1] / group;
+        widen_slice(k + bkv * slice, kd, slice, is_bf16);
+        widen_slice(v + bkv * slice, vd, slice, is_bf16);
+#pragma omp parallel
+        {
+            double *scores = (double *)malloc(sizeof(double) * (size_t)N);
+            double *qrow = (double *)malloc(sizeof(double) * (size_t)d);
+            if (!scores || !qrow) {
+#pragma omp atomic write
+                rc = -1;
+            } else {
+#pragma omp for schedule(dynamic, 1)
+                for (long r = r0; r < n_rows; ++r) {
+                    long b = rows[3 * r], h = rows[3 * r + 1], i = rows[3 * r + 2];
+                    if (done[r] || b * H_kv + h / group != bkv) continue;
+                    long j0, j1;
+                    key_range(N, i, causal, wl, wr, &j0, &j1);
+                    widen_slice(q + ((b * H + h) * N + i) * d, qrow, d, is_bf16);
+                    attend_range(qrow, kd, vd, d, j0, j1, scale, scores,
+                                 o_rows + r * d, lse_rows + r);
+                }
+            }
+            free(scores); free(qrow);
+        }
+        for (long r = r0; r < n_rows; ++r)
+            if (rows[3 * r] * H_kv + rows[3 * r + 1] / group == bkv) done[r] = 1;
+    }
+    free(kd); free(vd); free(done);
     return rc;
 }

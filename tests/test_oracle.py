@@ -288,3 +288,78 @@ def test_bad_arguments_rejected():
         oracle.attention_rows(q, k, v, 0.1, False, [(0, 0, 8)])
     with pytest.raises(TypeError):
         oracle.attention(q.float(), k, v, 0.1, False)
+
+
+# --------------------------------------------------------------------------
+# Grouped K/V heads and the local window.
+# --------------------------------------------------------------------------
+def _window_mask(n, causal, wl, wr):
+    i = torch.arange(n)[:, None]
+    j = torch.arange(n)[None, :]
+    ok = torch.ones(n, n, dtype=torch.bool)
+    if causal:
+        ok &= j <= i
+    if wl >= 0:
+        ok &= j >= i - wl
+    if wr >= 0:
+        ok &= j <= i + wr
+    return ok
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_window_matches_sdpa_mask(causal):
+    """Library routine with an explicit boolean mask."""
+    q, k, v = make_random_qkv(1, 2, 70, 16, torch.bfloat16, seed=81)
+    for wl, wr in ((5, 3), (0, 9), (17, -1), (-1, 4), (0, 0), (100, 100)):
+        o, lse = oracle.attention_ex(q, k, v, 0.3, causal, wl, wr)
+        mask = _window_mask(70, causal, wl, wr)
+        qd, kd, vd = (t.double() for t in (q, k, v))
+        o_ref = torch.nn.functional.scaled_dot_product_attention(qd, kd, vd, attn_mask=mask,
+                                                                 scale=0.3)
+        s = (0.3 * qd @ kd.transpose(-1, -2)).masked_fill(~mask, float("-inf"))
+        np.testing.assert_allclose(o, o_ref.numpy(), rtol=0, atol=1e-12, err_msg=str((wl, wr)))
+        np.testing.assert_allclose(lse, torch.logsumexp(s, -1).numpy(), rtol=0, atol=1e-12)
+
+
+def test_window_closed_forms():
+    q, k, v = make_random_qkv(1, 2, 40, 16, torch.float16, seed=82)
+    # a window of zero width leaves each row with its own key only
+    o, lse = oracle.attention_ex(q, k, v, 0.25, False, 0, 0)
+    np.testing.assert_array_equal(o, v.double().numpy())
+    np.testing.assert_allclose(lse, (0.25 * (q.double() * k.double()).sum(-1)).numpy(),
+                               rtol=0, atol=1e-13)
+    # windows wider than the sequence are full attention; right bound 0 is causal
+    o_full, l_full = oracle.attention(q, k, v, 0.25, False)
+    o_w, l_w = oracle.attention_ex(q, k, v, 0.25, False, 40, 40)
+    np.testing.assert_array_equal(o_w, o_full)
+    np.testing.assert_array_equal(l_w, l_full)
+    o_c, l_c = oracle.attention(q, k, v, 0.25, True)
+    o_r, l_r = oracle.attention_ex(q, k, v, 0.25, False, -1, 0)
+    np.testing.assert_array_equal(o_r, o_c)
+    np.testing.assert_array_equal(l_r, l_c)
+    # Q = 0: uniform weights over the window
+    z = torch.zeros_like(q)
+    o_z, l_z = oracle.attention_ex(z, k, v, 0.25, False, 3, 2)
+    vd = v.double().numpy()
+    for i in range(40):
+        lo, hi = max(0, i - 3), min(40, i + 3)
+        np.testing.assert_allclose(o_z[:, :, i], vd[:, :, lo:hi].mean(2), rtol=0, atol=1e-13)
+        np.testing.assert_allclose(l_z[:, :, i], math.log(hi - lo), rtol=0, atol=1e-13)
+
+
+def test_grouped_heads_equal_repeated_heads():
+    """H_kv < H equals repeating each K/V head H / H_kv times."""
+    q, _, _ = make_random_qkv(2, 6, 33, 16, torch.bfloat16, seed=83)
+    _, k, v = make_random_qkv(2, 2, 33, 16, torch.bfloat16, seed=84)
+    for causal in (False, True):
+        o, lse = oracle.attention_ex(q, k, v, 0.2, causal)
+        kr = k.repeat_interleave(3, dim=1)
+        vr = v.repeat_interleave(3, dim=1)
+        o_ref, l_ref = oracle.attention(q, kr, vr, 0.2, causal)
+        np.testing.assert_array_equal(o, o_ref)
+        np.testing.assert_array_equal(lse, l_ref)
+        rows = [(0, 0, 0), (1, 5, 32), (1, 2, 10), (0, 4, 7)]
+        o_r, l_r = oracle.attention_rows_ex(q, k, v, 0.2, causal, rows)
+        for t, (b, h, i) in enumerate(rows):
+            np.testing.assert_array_equal(o_r[t], o[b, h, i])
+            assert l_r[t] == lse[b, h, i]

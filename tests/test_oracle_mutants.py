@@ -20,10 +20,16 @@ MUTANTS = {
     "score_sign": ("double s = scale * dot;", "double s = -scale * dot;"),
     "values_as_keys": ("const double *k_row = kmat + j * d;",
                        "const double *k_row = vmat + j * d;"),
-    "causal_reversed": ("long nkeys = causal ? (i + 1 < N ? i + 1 : N) : N;",
-                        "long nkeys = causal ? N - i : N;"),
-    "causal_no_diagonal": ("long nkeys = causal ? (i + 1 < N ? i + 1 : N) : N;",
-                           "long nkeys = causal ? (i < N ? (i > 0 ? i : 1) : N) : N;"),
+    "causal_reversed": ("if (causal && i + 1 < hi) hi = i + 1;",
+                        "if (causal) lo = i;"),
+    "causal_no_diagonal": ("if (causal && i + 1 < hi) hi = i + 1;",
+                           "if (causal && i + 1 < hi) hi = (i > 0 ? i : 1);"),
+    "window_left_off_by_one": ("if (wl >= 0 && i - wl > lo) lo = i - wl;",
+                               "if (wl >= 0 && i - wl + 1 > lo) lo = i - wl + 1;"),
+    "window_right_ignored": ("if (wr >= 0 && i + wr + 1 < hi) hi = i + wr + 1;",
+                             "if (0) hi = i + wr + 1;"),
+    "gqa_head_mapping": ("long bh = b * H + h, bkv = b * H_kv + h / group;",
+                         "long bh = b * H + h, bkv = b * H_kv + h % H_kv;"),
     "lse_base2": ("double lse = m + log(sum);", "double lse = m + log2(sum);"),
     "lse_without_max": ("double lse = m + log(sum);", "double lse = log(sum);"),
     "no_max_subtraction": ("sum += exp(scores[j] - m);", "sum += exp(scores[j]);"),
@@ -48,6 +54,9 @@ PIN_CALLS = [
     (pins.test_causal_row_zero, {}),
     (pins.test_zero_queries_closed_form, dict(causal=True)),
     (pins.test_single_key_closed_form, {}),
+    (pins.test_window_matches_sdpa_mask, dict(causal=False)),
+    (pins.test_window_closed_forms, {}),
+    (pins.test_grouped_heads_equal_repeated_heads, {}),
 ]
 
 
