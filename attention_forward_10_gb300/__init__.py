@@ -33,6 +33,7 @@ FA_ERR_DEVICE_TIMEOUT = 5
 _vp, _i, _f, _ll = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_longlong
 SIGNATURES = {
     "fa_fwd": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _vp], _i),
+    "fa_fwd_ext": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _i, _i, _vp], _i),
     "fa_status_string": ([_i], ctypes.c_char_p),
     "fa_get_device_status": ([_vp, ctypes.POINTER(_i)], _i),
     "fa_set_wait_timeout_us": ([_ll], _i),
@@ -84,6 +85,13 @@ def fa_fwd(q: int, k: int, v: int, o: int, lse: int | None, B: int, H: int, N: i
                            stream or None))
 
 
+def fa_fwd_ext(q: int, k: int, v: int, o: int, lse: int | None, B: int, H: int, H_kv: int,
+               N: int, d: int, scale: float, causal: int, window_left: int,
+               window_right: int, dtype: int, stream: int | None) -> int:
+    return int(_lib.fa_fwd_ext(q, k, v, o, lse or None, B, H, H_kv, N, d, scale, causal,
+                               window_left, window_right, dtype, stream or None))
+
+
 def fa_status_string(status: int) -> str:
     return _lib.fa_status_string(int(status)).decode()
 
@@ -122,17 +130,22 @@ def _dtype_code(t) -> int:
 
 
 def fwd(q, k, v, *, scale: float | None = None, causal: bool = False,
-        out=None, lse=None, return_lse: bool = True, stream=None):
-    """Attention forward on CUDA tensors q, k, v of shape [B, H, N, d].
+        window: tuple[int, int] = (-1, -1), out=None, lse=None, return_lse: bool = True,
+        stream=None):
+    """Attention forward on CUDA tensors q [B, H, N, d] and k, v [B, H_kv, N, d].
 
     Returns ``(o, lse)``: o in the input dtype [B,H,N,d], lse float32 [B,H,N]
     (natural-log log-sum-exp of the scaled scores; None if ``return_lse`` is
-    False).  ``scale`` defaults to 1/sqrt(d).  Runs on ``stream`` (default:
+    False).  ``scale`` defaults to 1/sqrt(d).  H must be a multiple of H_kv
+    (grouped heads); ``window = (left, right)`` restricts query i to keys
+    i-left .. i+right (negative: unbounded).  Runs on ``stream`` (default:
     torch's current stream of the inputs' device) and does not synchronise.
     """
     import torch
-    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
-        raise ValueError("q, k, v must share one [B, H, N, d] shape")
+    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape:
+        raise ValueError("q must be [B, H, N, d] and k, v one [B, H_kv, N, d] shape")
+    if (k.shape[0], k.shape[2], k.shape[3]) != (q.shape[0], q.shape[2], q.shape[3]):
+        raise ValueError("k, v must match q in B, N and d")
     if not (q.is_cuda and k.is_cuda and v.is_cuda):
         raise ValueError("q, k, v must be CUDA tensors (no CPU path)")
     if not (q.dtype == k.dtype == v.dtype):
@@ -150,16 +163,17 @@ def fwd(q, k, v, *, scale: float | None = None, causal: bool = False,
         stream = torch.cuda.current_stream(q.device)
     handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
     with torch.cuda.device(q.device):
-        st = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                    lse.data_ptr() if (return_lse and lse is not None) else None,
-                    B, H, N, d, float(scale), int(bool(causal)), _dtype_code(q), handle)
+        st = fa_fwd_ext(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                        lse.data_ptr() if (return_lse and lse is not None) else None,
+                        B, H, int(k.shape[1]), N, d, float(scale), int(bool(causal)),
+                        int(window[0]), int(window[1]), _dtype_code(q), handle)
     if st != FA_OK:
         raise FaError(st, "fa_fwd")
     return out, (lse if return_lse else None)
 
 
 __all__ = [
-    "LIB_PATH", "SIGNATURES", "FaError", "fwd", "fa_fwd", "fa_status_string",
+    "LIB_PATH", "SIGNATURES", "FaError", "fwd", "fa_fwd", "fa_fwd_ext", "fa_status_string",
     "fa_get_device_status", "fa_set_wait_timeout_us", "fa_set_max_ctas",
     "fa_selftest_watchdog", "fa_num_sms",
     "FA_DTYPE_F16", "FA_DTYPE_BF16", "FA_OK", "FA_ERR_INVALID_ARG",

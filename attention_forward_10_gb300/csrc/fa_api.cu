@@ -158,8 +158,15 @@ int fa_num_sms(void) {
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
            int N, int d, float scale, int causal, int dtype, void* stream) {
+  return fa_fwd_ext(q, k, v, o, lse, B, H, H, N, d, scale, causal, -1, -1, dtype, stream);
+}
+
+int fa_fwd_ext(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+               int H, int H_kv, int N, int d, float scale, int causal, int window_left,
+               int window_right, int dtype, void* stream) {
   using namespace fa;
-  if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID_ARG;
+  if (B < 0 || H < 0 || N < 0 || H_kv < 0) return FA_ERR_INVALID_ARG;
+  if (H > 0 && (H_kv == 0 || H % H_kv != 0)) return FA_ERR_INVALID_ARG;
   if (dtype != FA_DTYPE_F16 && dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_INVALID_ARG;
@@ -186,12 +193,13 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   const bool bf16 = dtype == FA_DTYPE_BF16;
   FaParams p;
   const int ibh = static_cast<int>(bh);
+  const int ibh_kv = static_cast<int>(static_cast<long long>(B) * H_kv);
   // d = 256 streams 64-key K/V tiles and stores O in two 128-column halves
   const int kv_rows = (d == 256) ? 64 : kBlockN;
   const int o_blocks = (d == 256) ? 2 : d / 64;
   if (!encode_qkvo_map(&p.tm_q, q, N, d, ibh, bf16, kBlockM, d / 64) ||
-      !encode_qkvo_map(&p.tm_k, k, N, d, ibh, bf16, kv_rows, d / 64) ||
-      !encode_qkvo_map(&p.tm_v, v, N, d, ibh, bf16, kv_rows, d / 64) ||
+      !encode_qkvo_map(&p.tm_k, k, N, d, ibh_kv, bf16, kv_rows, d / 64) ||
+      !encode_qkvo_map(&p.tm_v, v, N, d, ibh_kv, bf16, kv_rows, d / 64) ||
       !encode_qkvo_map(&p.tm_o, o, N, d, ibh, bf16, kBlockM, o_blocks))
     return FA_ERR_CUDA;
   p.lse = lse;
@@ -202,6 +210,13 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   p.num_pairs = static_cast<int>(pairs);
   p.num_units = static_cast<int>(bh * pairs);
   p.n_ktiles = (N + kv_rows - 1) / kv_rows;
+  p.H = H;
+  p.group = H / H_kv;
+  // window bounds: negative or beyond N means unbounded (= N); causal caps
+  // the right bound at 0
+  p.win_left = (window_left < 0 || window_left > N) ? N : window_left;
+  p.win_right = (window_right < 0 || window_right > N) ? N : window_right;
+  if (causal) p.win_right = 0;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
 
   int grid = info->num_sms;

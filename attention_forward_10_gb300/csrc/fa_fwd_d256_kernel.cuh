@@ -77,9 +77,10 @@ static_assert(kSmemBytes <= 232448, "exceeds the shared memory of one CTA");
 constexpr uint32_t kOCol = 256;
 
 struct Unit {
-  int bh;
-  int row0;  // first query row of the tile
-  int nt;    // K/V tiles visited
+  int bh;     // query / output head
+  int bh_kv;  // K/V head it reads
+  int row0;   // first query row of the tile
+  int n0, n1; // K/V tiles visited: [n0, n1), never empty (a row sees itself)
 };
 
 template <bool CAUSAL>
@@ -94,12 +95,9 @@ __device__ __forceinline__ Unit decode_unit(int u, const FaParams& p) {
     qt = u % p.num_pairs;
   }
   w.row0 = qt * kBlockM;
-  if (CAUSAL) {
-    const int last = min(p.N, w.row0 + kBlockM);
-    w.nt = (last + kBN - 1) / kBN;
-  } else {
-    w.nt = p.n_ktiles;
-  }
+  w.bh_kv = kv_head(w.bh, p.H, p.group);
+  key_tile_range(w.row0, min(p.N, w.row0 + kBlockM), p.N, p.win_left, p.win_right, kBN,
+                 &w.n0, &w.n1);
   return w;
 }
 
@@ -169,13 +167,13 @@ __global__ void __launch_bounds__(d256::kThreads, 1)
         mbar_arrive_expect_tx(bar(kQFull), kQBytes);
         tma_load_4d(sbase + kQOff, &p.tm_q, bar(kQFull), 0, w.row0, 0, w.bh);
         ++q_it;
-        for (int n = 0; n < w.nt && ok; ++n) {
+        for (int n = w.n0; n < w.n1 && ok; ++n) {
           for (int kv = 0; kv < 2; ++kv) {
             ok = wait_bar(bar(kKVEmpty + slot), phase ^ 1u, ctl, kSiteProducerKV);
             if (!ok) break;
             mbar_arrive_expect_tx(bar(kKVFull + slot), kKVBytes);
             tma_load_4d(sbase + kKVOff + slot * kKVBytes, kv ? &p.tm_v : &p.tm_k,
-                        bar(kKVFull + slot), 0, n * kBN, 0, w.bh);
+                        bar(kKVFull + slot), 0, n * kBN, 0, w.bh_kv);
             ++issued;
             if (++slot == (uint32_t)kStages) { slot = 0; phase ^= 1u; }
           }
@@ -205,14 +203,15 @@ __global__ void __launch_bounds__(d256::kThreads, 1)
       // pending P V product: the previous K tile
       bool pv_pending = false, pv_acc = false;
       uint32_t pv_vslot = 0, pv_vphase = 0;
-      int u = blockIdx.x, n = 0;
+      int u = blockIdx.x;
       Unit w = decode_unit<CAUSAL>(u < p.num_units ? u : 0, p);
+      int n = w.n0;
       while (ok) {
         const bool cur_valid = u < p.num_units;
         if (cur_valid) {
           // ---- S(G) = Q K_G^T into buffer G mod 3
           const uint32_t b = G % kSBufs;
-          if (n == 0) {
+          if (n == w.n0) {
             ok = wait_bar(bar(kQFull), q_par, ctl, kSiteMmaQ);
             q_par ^= 1u;
             if (!ok) break;
@@ -231,7 +230,7 @@ __global__ void __launch_bounds__(d256::kThreads, 1)
                                      kIdescS, 0u);
           tc_commit(bar(kSFull + b));
           tc_commit(bar(kKVEmpty + kslot));
-          if (n == w.nt - 1) tc_commit(bar(kQEmpty));
+          if (n == w.n1 - 1) tc_commit(bar(kQEmpty));
         }
         if (pv_pending) {
           // ---- O += P(G-1) V_(G-1)
@@ -249,15 +248,15 @@ __global__ void __launch_bounds__(d256::kThreads, 1)
         if (!cur_valid) break;
         // V(G) is used in the next iteration
         pv_pending = true;
-        pv_acc = n > 0;
+        pv_acc = n > w.n0;
         pv_vslot = slot;
         pv_vphase = phase;
         if (++slot == (uint32_t)kStages) { slot = 0; phase ^= 1u; }
         ++G;
-        if (++n == w.nt) {
-          n = 0;
+        if (++n == w.n1) {
           u += gridDim.x;
           if (u < p.num_units) w = decode_unit<CAUSAL>(u, p);
+          n = w.n0;
         }
       }
       tc_commit(bar(kDrain));
@@ -278,7 +277,8 @@ __global__ void __launch_bounds__(d256::kThreads, 1)
       const Unit w = decode_unit<CAUSAL>(u, p);
       const int row = w.row0 + t;
       float m_ref = -INFINITY, l = 0.f;
-      for (int n = 0; n < w.nt; ++n, ++G) {
+      const int row_end = min(p.N, w.row0 + kBlockM);
+      for (int n = w.n0; n < w.n1; ++n, ++G) {
         const uint32_t b = G % kSBufs;
         const uint32_t tS = tmem + lane_base + b * kBN;
         ok = wait_bar(bar(kSFull + b), (G / kSBufs) & 1u, ctl, kSiteSoftmaxS);
@@ -295,15 +295,17 @@ __global__ void __launch_bounds__(d256::kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 32; ++c) s[32 + c] = __uint_as_float(r[c]);
         }
+        // keys row - win_left .. row + win_right, below N
         const int kbase = n * kBN;
-        const bool need_mask =
-            (kbase + kBN > p.N) || (CAUSAL && kbase + kBN - 1 > w.row0);
+        const bool need_mask = (kbase + kBN > p.N) ||
+                               (kbase + kBN - 1 > w.row0 + p.win_right) ||
+                               (kbase < row_end - 1 - p.win_left);
         if (need_mask) {
-          int lim = p.N - kbase;
-          if (CAUSAL) lim = min(lim, row - kbase + 1);
+          const int hi = min(p.N - kbase, row + p.win_right + 1 - kbase);  // c < hi
+          const int lo = row - p.win_left - kbase;                         // c >= lo
 #pragma unroll
           for (int c = 0; c < kBN; ++c)
-            if (c >= lim) s[c] = -INFINITY;
+            if (c >= hi || c < lo) s[c] = -INFINITY;
         }
         float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
@@ -319,7 +321,7 @@ __global__ void __launch_bounds__(d256::kThreads, 1)
         if (__any_sync(0xffffffffu, need)) {
           const float m_new = fmaxf(m_ref, m_tile);
           const float factor = (m_new == -INFINITY) ? 1.f : ex2_approx(m_ref - m_new);
-          if (n > 0) {
+          if (n > w.n0) {
             // O holds the previous tiles' sum: wait for P(G-1) V, rescale
             const uint32_t pb = (G - 1) % kSBufs;
             ok = wait_bar(bar(kODone + pb), ((G - 1) / kSBufs) & 1u, ctl, kSiteSoftmaxO);

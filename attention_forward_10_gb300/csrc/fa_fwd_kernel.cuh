@@ -108,11 +108,14 @@ struct Layout {
 };
 
 // One work unit: 256 query rows of one (b,h) = two 128-row query tiles.
+// Tile g visits K/V tiles [n0[g], n1[g]) (empty when n1 == n0); the unit
+// streams K/V tiles [n_beg, n_end), the union of the two ranges.
 struct Unit {
-  int bh;
+  int bh;       // query / output head (b*H + h)
+  int bh_kv;    // K/V head it reads
   int row0[2];  // first query row of each tile
-  int nt[2];    // K/V tiles each query tile visits (0 if the tile is empty)
-  int ntot;     // K/V tiles streamed for the unit = max(nt)
+  int n0[2], n1[2];
+  int n_beg, n_end;
 };
 
 // Units [0, num_pair_units) are query-tile pairs.  When the pairs do not
@@ -133,11 +136,14 @@ __device__ __forceinline__ Unit decode_unit(int u, const FaParams& p) {
     pair = p.num_pairs - 1 - pu / p.num_bh;
     w.bh = pu % p.num_bh;
   } else {
-    // consecutive units share a head, so its K/V stay hot in L2
+    // consecutive units share a head (and heads sharing K/V are adjacent),
+    // so K/V stay hot in L2
     w.bh = pu / p.num_pairs;
     pair = pu % p.num_pairs;
   }
-  w.ntot = 0;
+  w.bh_kv = kv_head(w.bh, p.H, p.group);
+  w.n_beg = 0x7fffffff;
+  w.n_end = 0;
 #pragma unroll
   for (int g = 0; g < 2; ++g) {
     // a single-tile unit carries its tile in slot 0
@@ -145,15 +151,17 @@ __device__ __forceinline__ Unit decode_unit(int u, const FaParams& p) {
                                 : pair * kRowsPerUnit + single * kBlockM;
     w.row0[g] = r0;
     if (r0 >= p.N || (single >= 0 && g == 1)) {
-      w.nt[g] = 0;
-    } else if (CAUSAL) {
-      const int last = min(p.N, r0 + kBlockM);  // rows r0..last-1 see keys < last
-      w.nt[g] = (last + kBlockN - 1) / kBlockN;
+      w.n0[g] = w.n1[g] = 0;
     } else {
-      w.nt[g] = p.n_ktiles;
+      key_tile_range(r0, min(p.N, r0 + kBlockM), p.N, p.win_left, p.win_right, kBlockN,
+                     &w.n0[g], &w.n1[g]);
     }
-    w.ntot = max(w.ntot, w.nt[g]);
+    if (w.n1[g] > w.n0[g]) {
+      w.n_beg = min(w.n_beg, w.n0[g]);
+      w.n_end = max(w.n_end, w.n1[g]);
+    }
   }
+  if (w.n_end == 0) w.n_beg = 0;  // nothing to stream
   return w;
 }
 
@@ -218,7 +226,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
         const Unit w = decode_unit<CAUSAL>(u, p);
         for (int g = 0; g < 2 && ok; ++g) {
-          if (w.nt[g] == 0) continue;
+          if (w.n1[g] == w.n0[g]) continue;
           ok = wait_bar(bar(L::kQEmpty + g), (q_it[g] & 1u) ^ 1u, ctl, kSiteProducerQ);
           if (!ok) break;
           mbar_arrive_expect_tx(bar(L::kQFull + g), L::kTileBytes);
@@ -226,7 +234,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                       w.row0[g], 0, w.bh);
           ++q_it[g];
         }
-        for (int n = 0; n < w.ntot && ok; ++n) {
+        for (int n = w.n_beg; n < w.n_end && ok; ++n) {
           for (int kv = 0; kv < 2; ++kv) {
             const uint32_t slot = kv_it % L::kStages;
             const uint32_t phase = (kv_it / L::kStages) & 1u;
@@ -234,7 +242,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             if (!ok) break;
             mbar_arrive_expect_tx(bar(L::kKVFull + slot), L::kTileBytes);
             tma_load_4d(sbase + L::kKVOff + slot * L::kTileBytes, kv ? &p.tm_v : &p.tm_k,
-                        bar(L::kKVFull + slot), 0, n * kBlockN, 0, w.bh);
+                        bar(L::kKVFull + slot), 0, n * kBlockN, 0, w.bh_kv);
             ++kv_it;
           }
         }
@@ -269,22 +277,23 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       bool ok = true;
       // Step j of the K/V stream is (unit u, tile n); prev_* describe step
       // j-1, whose P V products are issued in step j.
-      bool prev_valid = false, prev_acc = false;
-      bool prev_active[2] = {false, false};
+      bool prev_valid = false;
+      bool prev_active[2] = {false, false}, prev_acc[2] = {false, false};
       uint32_t prev_vslot = 0;
-      int u = blockIdx.x, n = 0;
+      int u = blockIdx.x;
       Unit w = decode_unit<CAUSAL>(u < p.num_units ? u : 0, p);
       // units without K/V tiles (a split-off tile past N) stream nothing
-      while (u < p.num_units && w.ntot == 0) {
+      while (u < p.num_units && w.n_end == w.n_beg) {
         u += gridDim.x;
         if (u < p.num_units) w = decode_unit<CAUSAL>(u, p);
       }
+      int n = w.n_beg;
       while (ok) {
         const bool cur_valid = u < p.num_units;
         if (!cur_valid && !prev_valid) break;
-        if (cur_valid && n == 0) {
+        if (cur_valid && n == w.n_beg) {
           for (int g = 0; g < 2 && ok; ++g) {
-            if (w.nt[g] == 0) continue;
+            if (w.n1[g] == w.n0[g]) continue;
             ok = wait_bar(bar(L::kQFull + g), q_par[g], ctl, kSiteMmaQ);
             q_par[g] ^= 1u;
           }
@@ -300,12 +309,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             if (!ok) break;
             tc_fence_after_sync();
             mma_ts_mnmajor_x8(tmem + L::o_col(g), tmem + L::s_col(g),
-                              v_desc0 + prev_vslot * kSlotStep, kIdescO, prev_acc ? 1u : 0u);
+                              v_desc0 + prev_vslot * kSlotStep, kIdescO, prev_acc[g] ? 1u : 0u);
             tc_commit(bar(L::kODone + g));
             ++o_cnt[g];
           }
           // ---- S_g = Q_g K_j^T (after P_g(j-1) V, which reads S_g's columns)
-          if (cur_valid && n < w.nt[g]) {
+          if (cur_valid && n >= w.n0[g] && n < w.n1[g]) {
             if (!k_ready) {
               ok = wait_bar(bar(L::kKVFull + kslot), kphase, ctl, kSiteMmaK);
               if (!ok) break;
@@ -323,7 +332,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             else
               mma_ss_kmajor_x4(tmem + L::s_col(g), a, b, kIdescS, 0u);
             tc_commit(bar(L::kSFull + g));
-            if (n == w.nt[g] - 1) tc_commit(bar(L::kQEmpty + g));
+            if (n == w.n1[g] - 1) tc_commit(bar(L::kQEmpty + g));
           }
         }
         if (!ok) break;
@@ -337,16 +346,18 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         if (!ok) break;
         if (++slot == (uint32_t)L::kStages) { slot = 0; phase ^= 1u; }
         prev_valid = true;
-        prev_acc = n > 0;
-        prev_active[0] = n < w.nt[0];
-        prev_active[1] = n < w.nt[1];
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          prev_active[g] = n >= w.n0[g] && n < w.n1[g];
+          prev_acc[g] = n > w.n0[g];  // the first tile of a unit overwrites O_g
+        }
         prev_vslot = vslot;
-        if (++n == w.ntot) {
-          n = 0;
+        if (++n == w.n_end) {
           do {
             u += gridDim.x;
             if (u < p.num_units) w = decode_unit<CAUSAL>(u, p);
-          } while (u < p.num_units && w.ntot == 0);
+          } while (u < p.num_units && w.n_end == w.n_beg);
+          n = w.n_beg;
         }
       }
       // Every MMA issued must complete before tensor memory is released.
@@ -371,14 +382,16 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
       const Unit w = decode_unit<CAUSAL>(u, p);
       // the staging tile is used by tile 0 then tile 1 of each unit
-      const uint32_t my_store = n_stores + ((g == 1 && w.nt[0] > 0) ? 1u : 0u);
-      n_stores += (w.nt[0] > 0 ? 1u : 0u) + (w.nt[1] > 0 ? 1u : 0u);
-      if (w.nt[g] == 0) continue;
+      const bool valid0 = w.n1[0] > w.n0[0], valid1 = w.n1[1] > w.n0[1];
+      const uint32_t my_store = n_stores + ((g == 1 && valid0) ? 1u : 0u);
+      n_stores += (valid0 ? 1u : 0u) + (valid1 ? 1u : 0u);
+      if (w.n1[g] == w.n0[g]) continue;
       const int row = w.row0[g] + t;
       float m_ref = -INFINITY;  // reference maximum (log2 units, scaled)
       float l = 0.f;            // running row sum relative to m_ref
 
-      for (int n = 0; n < w.nt[g]; ++n) {
+      const int row_end = min(p.N, w.row0[g] + kBlockM);
+      for (int n = w.n0[g]; n < w.n1[g]; ++n) {
         ok = wait_bar(bar(L::kSFull + g), s_par, ctl, kSiteSoftmaxS);
         s_par ^= 1u;
         ok = __all_sync(0xffffffffu, ok);
@@ -391,15 +404,17 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 #pragma unroll
         for (int c = 0; c < kBlockN; ++c) s[c] = __uint_as_float(sraw[c]);
 
+        // keys row - win_left .. row + win_right, below N
         const int kbase = n * kBlockN;
-        const bool need_mask =
-            (kbase + kBlockN > p.N) || (CAUSAL && kbase + kBlockN - 1 > w.row0[g]);
+        const bool need_mask = (kbase + kBlockN > p.N) ||
+                               (kbase + kBlockN - 1 > w.row0[g] + p.win_right) ||
+                               (kbase < row_end - 1 - p.win_left);
         if (need_mask) {
-          int lim = p.N - kbase;
-          if (CAUSAL) lim = min(lim, row - kbase + 1);
+          const int hi = min(p.N - kbase, row + p.win_right + 1 - kbase);  // c < hi
+          const int lo = row - p.win_left - kbase;                         // c >= lo
 #pragma unroll
           for (int c = 0; c < kBlockN; ++c)
-            if (c >= lim) s[c] = -INFINITY;
+            if (c >= hi || c < lo) s[c] = -INFINITY;
         }
         // row maximum: four independent chains
         float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
@@ -416,7 +431,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         if (__any_sync(0xffffffffu, need)) {
           const float m_new = fmaxf(m_ref, m_tile);
           const float factor = (m_new == -INFINITY) ? 1.f : ex2_approx(m_ref - m_new);
-          if (n > 0) {
+          if (n > w.n0[g]) {
             // O_g holds the previous tiles' sum: wait for the last P_g V MMA,
             // then rescale this warp's 32 rows in tensor memory.
             ok = wait_bar(bar(L::kODone + g), (pv_cnt - 1) & 1u, ctl, kSiteSoftmaxO);
@@ -517,7 +532,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
         const Unit w = decode_unit<CAUSAL>(u, p);
         for (int g = 0; g < 2 && ok; ++g) {
-          if (w.nt[g] == 0) continue;
+          if (w.n1[g] == w.n0[g]) continue;
           ok = wait_bar(bar(L::kStageFull), full_par, ctl, kSiteStore);
           full_par ^= 1u;
           if (!ok) break;

@@ -45,8 +45,29 @@ struct FaParams {  // 64-byte aligned through CUtensorMap
   int num_units;     // work units (see num_pair_units)
   int num_pair_units;  // units below this index are query-tile pairs; the
                        // rest are single tiles (d <= 128 kernel)
-  int n_ktiles;      // ceil(N / 128)
+  int n_ktiles;      // number of K/V tiles along N
+  int H;             // query heads per batch entry
+  int group;         // query heads per K/V head (H / H_kv)
+  int win_left;      // query i sees keys i - win_left .. i + win_right,
+  int win_right;     //   both clamped to [0, N]; win_right = 0 when causal
   float scale_log2;  // softmax scale * log2(e)
 };
+
+// K/V head of query head bh = b*H + h (grouped heads: h / group).
+__host__ __device__ inline int kv_head(int bh, int H, int group) {
+  const int H_kv = H / group;
+  return (bh / H) * H_kv + (bh % H) / group;
+}
+
+// K/V tiles [n0, n1) of `tile` keys that query rows [r0, r_end) can see.
+__host__ __device__ inline void key_tile_range(int r0, int r_end, int N, int win_left,
+                                               int win_right, int tile, int* n0, int* n1) {
+  const long long lo = r0 - static_cast<long long>(win_left);
+  const long long hi = static_cast<long long>(r_end) + win_right;  // exclusive
+  const int key_lo = lo < 0 ? 0 : static_cast<int>(lo);
+  const int key_hi = hi > N ? N : static_cast<int>(hi);
+  *n0 = key_lo / tile;
+  *n1 = key_hi > key_lo ? (key_hi + tile - 1) / tile : *n0;
+}
 
 }  // namespace fa

@@ -87,6 +87,31 @@ FA_API int fa_fwd(const void* q, const void* k, const void* v, void* o, float* l
            int B, int H, int N, int d, float scale, int causal, int dtype,
            void* stream);
 
+/*
+ * fa_fwd_ext -- fa_fwd with grouped K/V heads and a local window.
+ *
+ * Sources: flash-attention "hopper/mainloop_bwd_sm90_tma_gmma_ws.hpp", the
+ * qhead_per_khead (grouped-query / multi-query attention) and
+ * window_size_left / window_size_right (local attention, its Is_local mask)
+ * options of CollectiveMainloopBwd.
+ *
+ *   k, v     contiguous [B][H_kv][N][d]; query head h (of H) reads K/V head
+ *            h / (H / H_kv).  H must be a multiple of H_kv (else
+ *            FA_ERR_INVALID_ARG); H_kv = H is ordinary multi-head attention,
+ *            H_kv = 1 multi-query attention.
+ *   window_left, window_right
+ *            query i sees keys j with i - window_left <= j <= i + window_right;
+ *            a negative value leaves that side unbounded.  With causal = 1 the
+ *            right bound is 0 whatever window_right says.  Every row sees at
+ *            least its own key, so no row is empty.
+ * All other arguments, the layout of q, o, lse, alignment, ownership and
+ * error behaviour are those of fa_fwd (which is fa_fwd_ext with H_kv = H and
+ * both window bounds -1).
+ */
+FA_API int fa_fwd_ext(const void* q, const void* k, const void* v, void* o, float* lse,
+                      int B, int H, int H_kv, int N, int d, float scale, int causal,
+                      int window_left, int window_right, int dtype, void* stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 FA_API const char* fa_status_string(int status);
 

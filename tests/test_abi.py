@@ -27,7 +27,7 @@ def _declared_functions():
 
 def test_header_declares_expected_entry_points():
     names = _declared_functions()
-    for n in ("fa_fwd", "fa_status_string", "fa_get_device_status",
+    for n in ("fa_fwd", "fa_fwd_ext", "fa_status_string", "fa_get_device_status",
               "fa_set_wait_timeout_us", "fa_set_max_ctas", "fa_selftest_watchdog",
               "fa_num_sms"):
         assert n in names
@@ -104,3 +104,20 @@ def test_product_does_not_import_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "attn_ref" not in text, f
+
+
+def _call_ext(fa, H=4, H_kv=2, **kw):
+    a = dict(GOOD)
+    a.update(kw)
+    return fa.fa_fwd_ext(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], H, H_kv, a["N"],
+                         a["d"], a["scale"], a["causal"], -1, -1, a["dtype"], a["stream"])
+
+
+@pytest.mark.parametrize("H,H_kv,code", [(4, 3, 1), (4, 0, 1), (4, -1, 1), (6, 4, 1),
+                                         (4, 8, 1)])
+def test_ext_head_grouping_errors(fa, H, H_kv, code):
+    assert _call_ext(fa, H=H, H_kv=H_kv) == code
+
+
+def test_ext_empty_is_noop(fa):
+    assert _call_ext(fa, H=4, H_kv=2, N=0) == fa.FA_OK

@@ -183,6 +183,42 @@ def test_deterministic_and_guard_bands(fa):
     assert torch.all(lg == -7.25)
 
 
+# ------------------------------------------- grouped heads, local window
+def _run_ext(fa, q, k, v, scale, causal, window):
+    o, lse = fa.fwd(q.cuda(), k.cuda(), v.cuda(), scale=scale, causal=causal, window=window)
+    torch.cuda.synchronize()
+    st, site = fa.fa_get_device_status(None)
+    assert st == fa.FA_OK, f"device status {fa.fa_status_string(st)} at site {site}"
+    return o, lse
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("H,H_kv", [(4, 4), (4, 2), (4, 1)])
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+@pytest.mark.parametrize("window", [(-1, -1), (40, 40), (200, 0), (0, 0), (300, -1),
+                                    (-1, 130)])
+def test_grouped_heads_and_window(fa, d, H, H_kv, causal, window):
+    q, _, _ = make_random_qkv(2, H, 700, d, torch.bfloat16, seed=90 + d + H_kv)
+    _, k, v = make_random_qkv(2, H_kv, 700, d, torch.bfloat16, seed=91 + d + H_kv)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = _run_ext(fa, q, k, v, scale, causal, window)
+    o_ref, lse_ref = oracle.attention_ex(q, k, v, scale, causal, *window)
+    _check(o, lse, o_ref, lse_ref, f"d={d} H={H}/{H_kv} causal={causal} window={window}")
+
+
+@pytest.mark.parametrize("ctas", [1, 3])
+@pytest.mark.parametrize("window", [(64, 64), (500, 0)])
+def test_window_persistent_loop(fa, ctas, window):
+    q, k, v = make_random_qkv(1, 3, 1500, 128, torch.float16, seed=95 + ctas)
+    fa.fa_set_max_ctas(ctas)
+    try:
+        o, lse = _run_ext(fa, q, k, v, 0.09, False, window)
+    finally:
+        fa.fa_set_max_ctas(0)
+    o_ref, lse_ref = oracle.attention_ex(q, k, v, 0.09, False, *window)
+    _check(o, lse, o_ref, lse_ref, f"ctas={ctas} window={window}")
+
+
 # ------------------------------------------------------------- watchdog
 def test_watchdog_times_out_cleanly(fa):
     st = fa.fa_selftest_watchdog(20_000, None)
