@@ -31,9 +31,13 @@ FA_ERR_DEVICE_TIMEOUT = 5
 
 # Every exported symbol of include/fa.h, with its ctypes signature.
 _vp, _i, _f, _ll = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_longlong
+_ull = ctypes.c_ulonglong
 SIGNATURES = {
     "fa_fwd": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _vp], _i),
     "fa_fwd_ext": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _i, _i, _vp], _i),
+    "fa_fwd_splitkv": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _i, _i, _i,
+                        _vp, _ull, _vp], _i),
+    "fa_splitkv_workspace_bytes": ([_i, _i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(_ull)], _i),
     "fa_status_string": ([_i], ctypes.c_char_p),
     "fa_get_device_status": ([_vp, ctypes.POINTER(_i)], _i),
     "fa_set_wait_timeout_us": ([_ll], _i),
@@ -92,6 +96,24 @@ def fa_fwd_ext(q: int, k: int, v: int, o: int, lse: int | None, B: int, H: int, 
                                window_left, window_right, dtype, stream or None))
 
 
+def fa_fwd_splitkv(q: int, k: int, v: int, o: int, lse: int | None, B: int, H: int,
+                   H_kv: int, N: int, d: int, scale: float, causal: int, window_left: int,
+                   window_right: int, dtype: int, num_splits: int, workspace: int | None,
+                   workspace_bytes: int, stream: int | None) -> int:
+    return int(_lib.fa_fwd_splitkv(q, k, v, o, lse or None, B, H, H_kv, N, d, scale, causal,
+                                   window_left, window_right, dtype, num_splits,
+                                   workspace or None, int(workspace_bytes), stream or None))
+
+
+def fa_splitkv_workspace_bytes(B: int, H: int, N: int, d: int, causal: int, window_left: int,
+                               window_right: int, num_splits: int) -> tuple[int, int]:
+    """(status, bytes) of the scratch fa_fwd_splitkv needs."""
+    out = ctypes.c_ulonglong(0)
+    st = int(_lib.fa_splitkv_workspace_bytes(B, H, N, d, causal, window_left, window_right,
+                                             num_splits, ctypes.byref(out)))
+    return st, int(out.value)
+
+
 def fa_status_string(status: int) -> str:
     return _lib.fa_status_string(int(status)).decode()
 
@@ -129,6 +151,32 @@ def _dtype_code(t) -> int:
     raise TypeError(f"q/k/v must be float16 or bfloat16, got {t.dtype}")
 
 
+def _check_qkv(q, k, v):
+    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape:
+        raise ValueError("q must be [B, H, N, d] and k, v one [B, H_kv, N, d] shape")
+    if (k.shape[0], k.shape[2], k.shape[3]) != (q.shape[0], q.shape[2], q.shape[3]):
+        raise ValueError("k, v must match q in B, N and d")
+    if not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise ValueError("q, k, v must be CUDA tensors (no CPU path)")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k, v must share one dtype")
+    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("q, k, v must be contiguous")
+
+
+def _outputs(q, out, lse, return_lse, stream):
+    import torch
+    B, H, N, _ = (int(x) for x in q.shape)
+    if out is None:
+        out = torch.empty_like(q)
+    if return_lse and lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    return out, lse, handle
+
+
 def fwd(q, k, v, *, scale: float | None = None, causal: bool = False,
         window: tuple[int, int] = (-1, -1), out=None, lse=None, return_lse: bool = True,
         stream=None):
@@ -142,26 +190,11 @@ def fwd(q, k, v, *, scale: float | None = None, causal: bool = False,
     torch's current stream of the inputs' device) and does not synchronise.
     """
     import torch
-    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape:
-        raise ValueError("q must be [B, H, N, d] and k, v one [B, H_kv, N, d] shape")
-    if (k.shape[0], k.shape[2], k.shape[3]) != (q.shape[0], q.shape[2], q.shape[3]):
-        raise ValueError("k, v must match q in B, N and d")
-    if not (q.is_cuda and k.is_cuda and v.is_cuda):
-        raise ValueError("q, k, v must be CUDA tensors (no CPU path)")
-    if not (q.dtype == k.dtype == v.dtype):
-        raise TypeError("q, k, v must share one dtype")
-    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
-        raise ValueError("q, k, v must be contiguous")
+    _check_qkv(q, k, v)
     B, H, N, d = (int(x) for x in q.shape)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    if out is None:
-        out = torch.empty_like(q)
-    if return_lse and lse is None:
-        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    if stream is None:
-        stream = torch.cuda.current_stream(q.device)
-    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    out, lse, handle = _outputs(q, out, lse, return_lse, stream)
     with torch.cuda.device(q.device):
         st = fa_fwd_ext(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                         lse.data_ptr() if (return_lse and lse is not None) else None,
@@ -172,8 +205,44 @@ def fwd(q, k, v, *, scale: float | None = None, causal: bool = False,
     return out, (lse if return_lse else None)
 
 
+def fwd_splitkv(q, k, v, *, num_splits: int = 0, scale: float | None = None,
+                causal: bool = False, window: tuple[int, int] = (-1, -1), out=None,
+                lse=None, return_lse: bool = True, workspace=None, stream=None):
+    """``fwd`` with each row's keys cut into ``num_splits`` ranges run as
+    separate work units and merged (0: a count that fills the SMs).
+
+    ``workspace`` is an optional uint8 CUDA tensor of at least the bytes
+    ``fa_splitkv_workspace_bytes`` reports (256-byte aligned); without one it
+    is allocated with torch on the inputs' device.
+    """
+    import torch
+    _check_qkv(q, k, v)
+    B, H, N, d = (int(x) for x in q.shape)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out, lse, handle = _outputs(q, out, lse, return_lse, stream)
+    with torch.cuda.device(q.device):
+        st, need = fa_splitkv_workspace_bytes(B, H, N, d, int(bool(causal)), int(window[0]),
+                                              int(window[1]), int(num_splits))
+        if st != FA_OK:
+            raise FaError(st, "fa_splitkv_workspace_bytes")
+        if need > 0 and workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        ws_ptr = workspace.data_ptr() if workspace is not None else None
+        ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+        st = fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                            lse.data_ptr() if (return_lse and lse is not None) else None,
+                            B, H, int(k.shape[1]), N, d, float(scale), int(bool(causal)),
+                            int(window[0]), int(window[1]), _dtype_code(q), int(num_splits),
+                            ws_ptr, ws_bytes, handle)
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_splitkv")
+    return out, (lse if return_lse else None)
+
+
 __all__ = [
-    "LIB_PATH", "SIGNATURES", "FaError", "fwd", "fa_fwd", "fa_fwd_ext", "fa_status_string",
+    "LIB_PATH", "SIGNATURES", "FaError", "fwd", "fwd_splitkv", "fa_fwd", "fa_fwd_ext",
+    "fa_fwd_splitkv", "fa_splitkv_workspace_bytes", "fa_status_string",
     "fa_get_device_status", "fa_set_wait_timeout_us", "fa_set_max_ctas",
     "fa_selftest_watchdog", "fa_num_sms",
     "FA_DTYPE_F16", "FA_DTYPE_BF16", "FA_OK", "FA_ERR_INVALID_ARG",

@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -161,28 +162,65 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   return fa_fwd_ext(q, k, v, o, lse, B, H, H, N, d, scale, causal, -1, -1, dtype, stream);
 }
 
-int fa_fwd_ext(const void* q, const void* k, const void* v, void* o, float* lse, int B,
-               int H, int H_kv, int N, int d, float scale, int causal, int window_left,
-               int window_right, int dtype, void* stream) {
-  using namespace fa;
-  if (B < 0 || H < 0 || N < 0 || H_kv < 0) return FA_ERR_INVALID_ARG;
-  if (H > 0 && (H_kv == 0 || H % H_kv != 0)) return FA_ERR_INVALID_ARG;
-  if (dtype != FA_DTYPE_F16 && dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
-  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
-  if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_INVALID_ARG;
-  if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
-  if (B == 0 || H == 0 || N == 0) return FA_OK;
-  if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return FA_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16))
+}  // extern "C"
+
+namespace fa {
+namespace {
+
+// Everything fa_fwd_ext and fa_fwd_splitkv share: validation, tensor maps,
+// grid sizing, launch.  With num_splits > 1 the outputs are the split
+// partials: o_out / lse_out hold num_splits * B * H heads.
+struct ForwardCall {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  int B, H, H_kv, N, d;
+  float scale;
+  int causal, window_left, window_right, dtype;
+  void* stream;
+};
+
+int validate(const ForwardCall& c) {
+  if (c.B < 0 || c.H < 0 || c.N < 0 || c.H_kv < 0) return FA_ERR_INVALID_ARG;
+  if (c.H > 0 && (c.H_kv == 0 || c.H % c.H_kv != 0)) return FA_ERR_INVALID_ARG;
+  if (c.dtype != FA_DTYPE_F16 && c.dtype != FA_DTYPE_BF16) return FA_ERR_INVALID_ARG;
+  if (c.causal != 0 && c.causal != 1) return FA_ERR_INVALID_ARG;
+  if (!(std::isfinite(c.scale) && c.scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (c.d != 64 && c.d != 128 && c.d != 256) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+bool empty_problem(const ForwardCall& c) { return c.B == 0 || c.H == 0 || c.N == 0; }
+
+int check_pointers(const ForwardCall& c) {
+  if (c.q == nullptr || c.k == nullptr || c.v == nullptr || c.o == nullptr)
+    return FA_ERR_INVALID_ARG;
+  if (!aligned(c.q, 16) || !aligned(c.k, 16) || !aligned(c.v, 16) || !aligned(c.o, 16))
     return FA_ERR_MISALIGNED;
-  if (lse != nullptr && !aligned(lse, 4)) return FA_ERR_MISALIGNED;
-  const long long bh = static_cast<long long>(B) * H;
-  // work units per (b,h): pairs of 128-row query tiles (d <= 128) or single
-  // 128-row tiles (d = 256)
-  const int rows_per_unit = (d == 256) ? kBlockM : kRowsPerUnit;
-  const long long pairs = (static_cast<long long>(N) + rows_per_unit - 1) / rows_per_unit;
+  if (c.lse != nullptr && !aligned(c.lse, 4)) return FA_ERR_MISALIGNED;
+  return FA_OK;
+}
+
+// K/V tile length of the kernel that serves head dim d.
+int kv_tile_rows(int d) { return d == 256 ? 64 : kBlockN; }
+
+// Work units per (b,h): pairs of 128-row query tiles (d <= 128) or single
+// 128-row tiles (d = 256).
+long long units_per_head(int N, int d) {
+  const int rows = (d == 256) ? kBlockM : kRowsPerUnit;
+  return (static_cast<long long>(N) + rows - 1) / rows;
+}
+
+int launch_forward(const ForwardCall& c, void* o_out, float* lse_out, int num_splits,
+                   int split_tiles) {
+  using namespace fa;
+  const long long bh = static_cast<long long>(c.B) * c.H;
+  const long long pairs = units_per_head(c.N, c.d);
   // (headroom: the last-wave split below may add up to one wave of units)
-  if (bh >= (1ll << 31) || bh * pairs + 4096 >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+  if (bh >= (1ll << 31) || bh * pairs * num_splits + 4096 >= (1ll << 31))
+    return FA_ERR_INVALID_ARG;
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
@@ -190,40 +228,43 @@ int fa_fwd_ext(const void* q, const void* k, const void* v, void* o, float* lse,
   if (info == nullptr || info->status == nullptr) return FA_ERR_CUDA;
   if (!info->ok) return FA_ERR_UNSUPPORTED;
 
-  const bool bf16 = dtype == FA_DTYPE_BF16;
+  const int N = c.N, d = c.d;
+  const bool bf16 = c.dtype == FA_DTYPE_BF16;
   FaParams p;
   const int ibh = static_cast<int>(bh);
-  const int ibh_kv = static_cast<int>(static_cast<long long>(B) * H_kv);
+  const int ibh_kv = static_cast<int>(static_cast<long long>(c.B) * c.H_kv);
   // d = 256 streams 64-key K/V tiles and stores O in two 128-column halves
-  const int kv_rows = (d == 256) ? 64 : kBlockN;
+  const int kv_rows = kv_tile_rows(d);
   const int o_blocks = (d == 256) ? 2 : d / 64;
-  if (!encode_qkvo_map(&p.tm_q, q, N, d, ibh, bf16, kBlockM, d / 64) ||
-      !encode_qkvo_map(&p.tm_k, k, N, d, ibh_kv, bf16, kv_rows, d / 64) ||
-      !encode_qkvo_map(&p.tm_v, v, N, d, ibh_kv, bf16, kv_rows, d / 64) ||
-      !encode_qkvo_map(&p.tm_o, o, N, d, ibh, bf16, kBlockM, o_blocks))
+  if (!encode_qkvo_map(&p.tm_q, c.q, N, d, ibh, bf16, kBlockM, d / 64) ||
+      !encode_qkvo_map(&p.tm_k, c.k, N, d, ibh_kv, bf16, kv_rows, d / 64) ||
+      !encode_qkvo_map(&p.tm_v, c.v, N, d, ibh_kv, bf16, kv_rows, d / 64) ||
+      !encode_qkvo_map(&p.tm_o, o_out, N, d, ibh * num_splits, bf16, kBlockM, o_blocks))
     return FA_ERR_CUDA;
-  p.lse = lse;
+  p.lse = lse_out;
   p.status = info->status;
   p.timeout_ns = g_timeout_ns.load();
   p.N = N;
-  p.num_bh = static_cast<int>(bh);
+  p.num_bh = ibh;
   p.num_pairs = static_cast<int>(pairs);
-  p.num_units = static_cast<int>(bh * pairs);
+  p.num_units = static_cast<int>(bh * pairs * num_splits);
   p.n_ktiles = (N + kv_rows - 1) / kv_rows;
-  p.H = H;
-  p.group = H / H_kv;
+  p.H = c.H;
+  p.group = c.H / c.H_kv;
   // window bounds: negative or beyond N means unbounded (= N); causal caps
   // the right bound at 0
-  p.win_left = (window_left < 0 || window_left > N) ? N : window_left;
-  p.win_right = (window_right < 0 || window_right > N) ? N : window_right;
-  if (causal) p.win_right = 0;
-  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.win_left = (c.window_left < 0 || c.window_left > N) ? N : c.window_left;
+  p.win_right = (c.window_right < 0 || c.window_right > N) ? N : c.window_right;
+  if (c.causal) p.win_right = 0;
+  p.num_splits = num_splits;
+  p.split_tiles = split_tiles;
+  p.scale_log2 = static_cast<float>(static_cast<double>(c.scale) * 1.4426950408889634);
 
   int grid = info->num_sms;
   const int cap = g_max_ctas.load();
   if (cap > 0 && cap < grid) grid = cap;
   p.num_pair_units = p.num_units;
-  if (d != 256) {
+  if (d != 256 && num_splits == 1) {
     // Balance the last wave: its L pair units become 2L single-tile units
     // when those fit in one wave.
     const long long pair_units = bh * pairs;
@@ -235,11 +276,191 @@ int fa_fwd_ext(const void* q, const void* k, const void* v, void* o, float* lse,
   }
   if (p.num_units < grid) grid = p.num_units;
 
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = (d == 64)    ? launch_fwd_d64(p, causal != 0, bf16, grid, s)
-                  : (d == 128) ? launch_fwd_d128(p, causal != 0, bf16, grid, s)
-                               : launch_fwd_d256(p, causal != 0, bf16, grid, s);
+  cudaStream_t s = static_cast<cudaStream_t>(c.stream);
+  cudaError_t e = (d == 64)    ? launch_fwd_d64(p, c.causal != 0, bf16, grid, s)
+                  : (d == 128) ? launch_fwd_d128(p, c.causal != 0, bf16, grid, s)
+                               : launch_fwd_d256(p, c.causal != 0, bf16, grid, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+// Longest CTA of a persistent launch with `splits` key splits of
+// `split_tiles` K/V tiles each, in K/V tile steps: work item i (base unit
+// i / splits, split i % splits, in the kernels' unit order) runs on CTA
+// i % grid, and an item costs its tiles of each query tile plus one step of
+// set-up and epilogue.
+long long estimate_makespan(const ForwardCall& c, int win_left, int win_right, int splits,
+                            int split_tiles, int grid) {
+  const int rows = (c.d == 256) ? kBlockM : kRowsPerUnit;
+  const int tiles_per_unit = rows / kBlockM;
+  const int kv = kv_tile_rows(c.d);
+  const int num_bh = c.B * c.H;
+  const int per_head = static_cast<int>(units_per_head(c.N, c.d));
+  const long long base_units = static_cast<long long>(num_bh) * per_head;
+  long long cta_cost[1024] = {};
+  long long worst = 0;
+  for (long long u = 0; u < base_units; ++u) {
+    // causal launches take the last query rows of every head first
+    const int pair = c.causal ? per_head - 1 - static_cast<int>(u / num_bh)
+                              : static_cast<int>(u % per_head);
+    for (int sp = 0; sp < splits; ++sp) {
+      long long cost = 0;
+      for (int g = 0; g < tiles_per_unit; ++g) {
+        const int r0 = pair * rows + g * kBlockM;
+        if (r0 >= c.N) continue;
+        int n0 = 0, n1 = 0;
+        key_tile_range(r0, std::min(c.N, r0 + kBlockM), c.N, win_left, win_right, kv, &n0,
+                       &n1);
+        if (splits > 1) clip_to_split(sp, split_tiles, &n0, &n1);
+        cost += n1 - n0;
+      }
+      // d = 256 tiles hold 64 keys: count in 128-key steps
+      if (kv != kBlockN) cost = (cost + 1) / 2;
+      if (cost == 0) continue;
+      long long& t = cta_cost[(u * splits + sp) % grid];
+      t += cost + 1;
+      worst = std::max(worst, t);
+    }
+  }
+  return worst;
+}
+
+// Split count actually used for a requested one, and the K/V tiles per
+// split.  0 asks for a count that fills the SMs: when the query units alone
+// leave SMs idle (or unevenly loaded, as causal units are), the count with
+// the shortest estimated makespan, each extra split charged 2% for its
+// partial-output traffic and merge.
+void plan_splits(const ForwardCall& c, int requested, int num_sms, int* splits,
+                 int* split_tiles) {
+  const int n_ktiles = (c.N + kv_tile_rows(c.d) - 1) / kv_tile_rows(c.d);
+  int want = requested;
+  if (want <= 0) {
+    want = 1;
+    const long long units = static_cast<long long>(c.B) * c.H * units_per_head(c.N, c.d);
+    const int grid = std::min(num_sms, 1024);
+    if (units < grid && n_ktiles > 1) {
+      const int win_left = (c.window_left < 0 || c.window_left > c.N) ? c.N : c.window_left;
+      const int win_right =
+          c.causal ? 0 : ((c.window_right < 0 || c.window_right > c.N) ? c.N : c.window_right);
+      double best = static_cast<double>(estimate_makespan(c, win_left, win_right, 1, n_ktiles,
+                                                          grid));
+      for (int s = 2; s <= std::min(n_ktiles, 32); ++s) {
+        const int tiles = (n_ktiles + s - 1) / s;
+        const int used = (n_ktiles + tiles - 1) / tiles;
+        if (used != s) continue;  // same split as a smaller count
+        const double t = static_cast<double>(
+                             estimate_makespan(c, win_left, win_right, s, tiles, grid)) *
+                         (1.0 + 0.02 * (s - 1));
+        if (t < best) {
+          best = t;
+          want = s;
+        }
+      }
+    }
+  }
+  if (want > n_ktiles) want = n_ktiles;
+  if (want < 1) want = 1;
+  const int tiles = (n_ktiles + want - 1) / want;
+  *split_tiles = tiles;
+  *splits = (n_ktiles + tiles - 1) / tiles;
+}
+
+// Workspace layout: partial O [S][B*H][N][d] (16-bit), then partial LSE
+// [S][B*H][N] (fp32) at the next 256-byte boundary.
+unsigned long long workspace_o_bytes(const ForwardCall& c, int splits) {
+  return static_cast<unsigned long long>(splits) * c.B * c.H * c.N * c.d * 2ull;
+}
+unsigned long long workspace_bytes(const ForwardCall& c, int splits) {
+  const unsigned long long o_bytes = (workspace_o_bytes(c, splits) + 255ull) & ~255ull;
+  return o_bytes + static_cast<unsigned long long>(splits) * c.B * c.H * c.N * 4ull;
+}
+
+int splitkv_forward(const ForwardCall& c, int num_splits, void* workspace,
+                    unsigned long long ws_bytes) {
+  using namespace fa;
+  int st = validate(c);
+  if (st != FA_OK) return st;
+  if (num_splits < 0) return FA_ERR_INVALID_ARG;
+  if (empty_problem(c)) return FA_OK;
+  st = check_pointers(c);
+  if (st != FA_OK) return st;
+  // the SM count is needed only to choose the split count
+  int num_sms = 0;
+  if (num_splits == 0) {
+    num_sms = fa_num_sms();
+    if (num_sms <= 0) return FA_ERR_CUDA;
+  }
+  int splits = 1, split_tiles = 0;
+  plan_splits(c, num_splits, num_sms, &splits, &split_tiles);
+  if (splits == 1) return launch_forward(c, c.o, c.lse, 1, 0);
+  if (workspace == nullptr || ws_bytes < workspace_bytes(c, splits)) return FA_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return FA_ERR_MISALIGNED;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* lse_part = reinterpret_cast<float*>(ws + ((workspace_o_bytes(c, splits) + 255ull) & ~255ull));
+  st = launch_forward(c, ws, lse_part, splits, split_tiles);
+  if (st != FA_OK) return st;
+  CombineArgs a;
+  a.num_bh = c.B * c.H;
+  a.N = c.N;
+  a.d = c.d;
+  a.num_splits = splits;
+  a.split_keys = split_tiles * kv_tile_rows(c.d);
+  a.win_left = (c.window_left < 0 || c.window_left > c.N) ? c.N : c.window_left;
+  a.win_right = (c.window_right < 0 || c.window_right > c.N) ? c.N : c.window_right;
+  if (c.causal) a.win_right = 0;
+  cudaError_t e = launch_splitkv_combine(ws, lse_part, c.o, c.lse, a, c.dtype == FA_DTYPE_BF16,
+                                         fa_num_sms(), static_cast<cudaStream_t>(c.stream));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" {
+
+int fa_fwd_ext(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+               int H, int H_kv, int N, int d, float scale, int causal, int window_left,
+               int window_right, int dtype, void* stream) {
+  using namespace fa;
+  const ForwardCall c{q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, window_left,
+                      window_right, dtype, stream};
+  int st = validate(c);
+  if (st != FA_OK) return st;
+  if (empty_problem(c)) return FA_OK;
+  st = check_pointers(c);
+  if (st != FA_OK) return st;
+  return launch_forward(c, o, lse, 1, 0);
+}
+
+int fa_splitkv_workspace_bytes(int B, int H, int N, int d, int causal, int window_left,
+                               int window_right, int num_splits, unsigned long long* bytes) {
+  using namespace fa;
+  if (bytes == nullptr) return FA_ERR_INVALID_ARG;
+  *bytes = 0;
+  const ForwardCall c{nullptr, nullptr, nullptr, nullptr, nullptr, B, H, H > 0 ? H : 1, N,
+                      d, 1.f, causal, window_left, window_right, FA_DTYPE_BF16, nullptr};
+  int st = validate(c);
+  if (st != FA_OK) return st;
+  if (num_splits < 0) return FA_ERR_INVALID_ARG;
+  if (empty_problem(c)) return FA_OK;
+  int num_sms = 0;
+  if (num_splits == 0) {
+    num_sms = fa_num_sms();
+    if (num_sms <= 0) return FA_ERR_CUDA;
+  }
+  int splits = 1, split_tiles = 0;
+  plan_splits(c, num_splits, num_sms, &splits, &split_tiles);
+  *bytes = splits > 1 ? workspace_bytes(c, splits) : 0;
+  return FA_OK;
+}
+
+int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                   int H, int H_kv, int N, int d, float scale, int causal, int window_left,
+                   int window_right, int dtype, int num_splits, void* workspace,
+                   unsigned long long workspace_bytes, void* stream) {
+  using namespace fa;
+  const ForwardCall c{q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, window_left,
+                      window_right, dtype, stream};
+  return splitkv_forward(c, num_splits, workspace, workspace_bytes);
 }
 
 int fa_get_device_status(void* stream, int* site) {

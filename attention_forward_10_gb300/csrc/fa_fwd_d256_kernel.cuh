@@ -77,15 +77,22 @@ static_assert(kSmemBytes <= 232448, "exceeds the shared memory of one CTA");
 constexpr uint32_t kOCol = 256;
 
 struct Unit {
-  int bh;     // query / output head
+  int bh;     // query head
   int bh_kv;  // K/V head it reads
+  int bh_out; // output head (bh, or the split's partial-output head)
   int row0;   // first query row of the tile
-  int n0, n1; // K/V tiles visited: [n0, n1), never empty (a row sees itself)
+  int n0, n1; // K/V tiles visited: [n0, n1); empty only for a key split
+              // that the tile's rows cannot see
 };
 
 template <bool CAUSAL>
 __device__ __forceinline__ Unit decode_unit(int u, const FaParams& p) {
   Unit w;
+  int split = 0;
+  if (p.num_splits > 1) {
+    split = u % p.num_splits;
+    u /= p.num_splits;
+  }
   int qt;
   if (CAUSAL) {
     qt = p.num_pairs - 1 - u / p.num_bh;  // heaviest first
@@ -96,8 +103,10 @@ __device__ __forceinline__ Unit decode_unit(int u, const FaParams& p) {
   }
   w.row0 = qt * kBlockM;
   w.bh_kv = kv_head(w.bh, p.H, p.group);
+  w.bh_out = split * p.num_bh + w.bh;
   key_tile_range(w.row0, min(p.N, w.row0 + kBlockM), p.N, p.win_left, p.win_right, kBN,
                  &w.n0, &w.n1);
+  if (p.num_splits > 1) clip_to_split(split, p.split_tiles, &w.n0, &w.n1);
   return w;
 }
 
@@ -162,6 +171,7 @@ __global__ void __launch_bounds__(d256::kThreads, 1)
       bool ok = true;
       for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
         const Unit w = decode_unit<CAUSAL>(u, p);
+        if (w.n1 == w.n0) continue;
         ok = wait_bar(bar(kQEmpty), (q_it & 1u) ^ 1u, ctl, kSiteProducerQ);
         if (!ok) break;
         mbar_arrive_expect_tx(bar(kQFull), kQBytes);
@@ -205,6 +215,10 @@ __global__ void __launch_bounds__(d256::kThreads, 1)
       uint32_t pv_vslot = 0, pv_vphase = 0;
       int u = blockIdx.x;
       Unit w = decode_unit<CAUSAL>(u < p.num_units ? u : 0, p);
+      while (u < p.num_units && w.n1 == w.n0) {  // empty key split: nothing to do
+        u += gridDim.x;
+        if (u < p.num_units) w = decode_unit<CAUSAL>(u, p);
+      }
       int n = w.n0;
       while (ok) {
         const bool cur_valid = u < p.num_units;
@@ -254,8 +268,10 @@ __global__ void __launch_bounds__(d256::kThreads, 1)
         if (++slot == (uint32_t)kStages) { slot = 0; phase ^= 1u; }
         ++G;
         if (++n == w.n1) {
-          u += gridDim.x;
-          if (u < p.num_units) w = decode_unit<CAUSAL>(u, p);
+          do {
+            u += gridDim.x;
+            if (u < p.num_units) w = decode_unit<CAUSAL>(u, p);
+          } while (u < p.num_units && w.n1 == w.n0);
           n = w.n0;
         }
       }
@@ -275,6 +291,7 @@ __global__ void __launch_bounds__(d256::kThreads, 1)
 
     for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
       const Unit w = decode_unit<CAUSAL>(u, p);
+      if (w.n1 == w.n0) continue;
       const int row = w.row0 + t;
       float m_ref = -INFINITY, l = 0.f;
       const int row_end = min(p.N, w.row0 + kBlockM);
@@ -410,7 +427,7 @@ __global__ void __launch_bounds__(d256::kThreads, 1)
         mbar_arrive(bar(kStageFull));
       }
       if (p.lse != nullptr && row < p.N) {
-        p.lse[static_cast<size_t>(w.bh) * p.N + row] =
+        p.lse[static_cast<size_t>(w.bh_out) * p.N + row] =
             (l > 0.f) ? (m_ref + log2f(l)) * 0.6931471805599453f : -INFINITY;
       }
     }
@@ -422,12 +439,13 @@ __global__ void __launch_bounds__(d256::kThreads, 1)
       bool ok = true;
       for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
         const Unit w = decode_unit<CAUSAL>(u, p);
+        if (w.n1 == w.n0) continue;
         for (int half = 0; half < 2 && ok; ++half) {
           ok = wait_bar(bar(kStageFull), full_par, ctl, kSiteStore);
           full_par ^= 1u;
           if (!ok) break;
           // columns [128*half, 128*half + 128) = d blocks 2*half, 2*half + 1
-          tma_store_4d(&p.tm_o, sbase + kStageOff, 0, w.row0, 2 * half, w.bh);
+          tma_store_4d(&p.tm_o, sbase + kStageOff, 0, w.row0, 2 * half, w.bh_out);
           bulk_commit_group();
           bulk_wait_read_all();
           mbar_arrive(bar(kStageEmpty));

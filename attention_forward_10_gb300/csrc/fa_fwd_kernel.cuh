@@ -111,8 +111,9 @@ struct Layout {
 // Tile g visits K/V tiles [n0[g], n1[g]) (empty when n1 == n0); the unit
 // streams K/V tiles [n_beg, n_end), the union of the two ranges.
 struct Unit {
-  int bh;       // query / output head (b*H + h)
+  int bh;       // query head (b*H + h)
   int bh_kv;    // K/V head it reads
+  int bh_out;   // output head (bh, or the split's partial-output head)
   int row0[2];  // first query row of each tile
   int n0[2], n1[2];
   int n_beg, n_end;
@@ -125,6 +126,11 @@ struct Unit {
 template <bool CAUSAL>
 __device__ __forceinline__ Unit decode_unit(int u, const FaParams& p) {
   Unit w;
+  int split = 0;
+  if (p.num_splits > 1) {
+    split = u % p.num_splits;
+    u /= p.num_splits;
+  }
   int pu = u, single = -1;  // pair-unit index; tile of a single-tile unit
   if (u >= p.num_pair_units) {
     pu = p.num_pair_units + (u - p.num_pair_units) / 2;
@@ -142,6 +148,7 @@ __device__ __forceinline__ Unit decode_unit(int u, const FaParams& p) {
     pair = pu % p.num_pairs;
   }
   w.bh_kv = kv_head(w.bh, p.H, p.group);
+  w.bh_out = split * p.num_bh + w.bh;
   w.n_beg = 0x7fffffff;
   w.n_end = 0;
 #pragma unroll
@@ -155,6 +162,7 @@ __device__ __forceinline__ Unit decode_unit(int u, const FaParams& p) {
     } else {
       key_tile_range(r0, min(p.N, r0 + kBlockM), p.N, p.win_left, p.win_right, kBlockN,
                      &w.n0[g], &w.n1[g]);
+      if (p.num_splits > 1) clip_to_split(split, p.split_tiles, &w.n0[g], &w.n1[g]);
     }
     if (w.n1[g] > w.n0[g]) {
       w.n_beg = min(w.n_beg, w.n0[g]);
@@ -516,7 +524,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         }
       }
       if (p.lse != nullptr && row < p.N) {
-        p.lse[static_cast<size_t>(w.bh) * p.N + row] =
+        p.lse[static_cast<size_t>(w.bh_out) * p.N + row] =
             (l > 0.f) ? (m_ref + log2f(l)) * 0.6931471805599453f : -INFINITY;
       }
       fence_proxy_async_smem();
@@ -536,7 +544,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           ok = wait_bar(bar(L::kStageFull), full_par, ctl, kSiteStore);
           full_par ^= 1u;
           if (!ok) break;
-          tma_store_4d(&p.tm_o, sbase + L::kStageOff, 0, w.row0[g], 0, w.bh);
+          tma_store_4d(&p.tm_o, sbase + L::kStageOff, 0, w.row0[g], 0, w.bh_out);
           bulk_commit_group();
           bulk_wait_read_all();  // the staging tile may be rewritten
           mbar_arrive(bar(L::kStageEmpty));

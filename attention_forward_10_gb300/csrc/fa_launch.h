@@ -19,6 +19,21 @@ cudaError_t launch_fwd_d128(const FaParams& p, bool causal, bool bf16, int grid,
 cudaError_t launch_fwd_d256(const FaParams& p, bool causal, bool bf16, int grid,
                             cudaStream_t stream);
 
+// Shape of a split-KV merge: num_bh heads of N rows of d columns; split s
+// holds keys [s * split_keys, (s + 1) * split_keys); query i may see keys
+// i - win_left .. i + win_right (both already clamped to [0, N]).
+struct CombineArgs {
+  int num_bh, N, d;
+  int num_splits, split_keys;
+  int win_left, win_right;
+};
+
+// Enqueue the merge of split-KV partials (o_part [S][num_bh][N][d] 16-bit,
+// lse_part [S][num_bh][N] fp32) into o and lse (lse may be null).
+cudaError_t launch_splitkv_combine(const void* o_part, const float* lse_part, void* o,
+                                   float* lse, const CombineArgs& a, bool bf16, int num_sms,
+                                   cudaStream_t stream);
+
 // Enqueue the watchdog self-test kernel (one CTA).
 cudaError_t launch_watchdog_selftest(int* status, unsigned long long timeout_ns,
                                      cudaStream_t stream);

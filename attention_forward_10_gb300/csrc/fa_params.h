@@ -50,8 +50,20 @@ struct FaParams {  // 64-byte aligned through CUtensorMap
   int group;         // query heads per K/V head (H / H_kv)
   int win_left;      // query i sees keys i - win_left .. i + win_right,
   int win_right;     //   both clamped to [0, N]; win_right = 0 when causal
+  int num_splits;    // key splits per query tile (1: no split)
+  int split_tiles;   // K/V tiles per key split
   float scale_log2;  // softmax scale * log2(e)
 };
+
+// Split-KV: unit u is split u % num_splits of base unit u / num_splits; the
+// split covers K/V tiles [s * split_tiles, (s + 1) * split_tiles).  Its O and
+// LSE go to head s * num_bh + bh of the partial outputs.
+__host__ __device__ inline void clip_to_split(int s, int split_tiles, int* n0, int* n1) {
+  const int lo = s * split_tiles, hi = lo + split_tiles;
+  if (*n0 < lo) *n0 = lo;
+  if (*n1 > hi) *n1 = hi;
+  if (*n1 < *n0) *n1 = *n0;
+}
 
 // K/V head of query head bh = b*H + h (grouped heads: h / group).
 __host__ __device__ inline int kv_head(int bh, int H, int group) {

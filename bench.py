@@ -15,6 +15,11 @@ another step's inputs from L2.  Under torchrun every rank runs an independent
 replica on its own GPU (the forward pass has no cross-GPU exchange); the
 reported value is all ranks' FLOPs over the slowest rank's time.
 
+Workload 6 (one causal head of 32768 rows) runs through the split-KV entry
+point with the automatic split count (two launches per step: the split
+forward and the merge); its line adds the unsplit forward's time on the
+same inputs.
+
 ``--impl reference`` times the fp64 CPU oracle (the only other place this
 script runs it) on rank 0, on bounded row samples of the same workload.
 """
@@ -284,12 +289,43 @@ def run_ours(args, wl):
     handle = stream.cuda_stream
     dcode = fa.FA_DTYPE_BF16 if wl.dtype == "bf16" else fa.FA_DTYPE_F16
 
-    def step(i):
+    # Split-KV workloads go through fa_fwd_splitkv with the automatic split
+    # count; its scratch is allocated once, outside the timed region.
+    workspace, ws_bytes, launches_per_call = None, 0, 1
+
+    def ensure_workspace(Bc, Hc):
+        nonlocal workspace, ws_bytes, launches_per_call
+        st_, need = fa.fa_splitkv_workspace_bytes(Bc, Hc, N, d, int(wl.causal), -1, -1, 0)
+        if st_ != fa.FA_OK:
+            raise RuntimeError(f"workspace query failed: {fa.fa_status_string(st_)}")
+        if need > ws_bytes:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+            ws_bytes = need
+        if need > 0:
+            launches_per_call = 2
+        return need
+
+    def call(qp, kp, vp, op, lp, Bc, Hc, plain=False):
+        if wl.splitkv and not plain:
+            st_ = fa.fa_fwd_splitkv(qp, kp, vp, op, lp, Bc, Hc, Hc, N, d, wl.scale,
+                                    int(wl.causal), -1, -1, dcode, 0,
+                                    workspace.data_ptr() if workspace is not None else None,
+                                    ws_bytes, handle)
+        else:
+            st_ = fa.fa_fwd(qp, kp, vp, op, lp, Bc, Hc, N, d, wl.scale, int(wl.causal),
+                            dcode, handle)
+        if st_ != fa.FA_OK:
+            raise RuntimeError(f"forward failed: {fa.fa_status_string(st_)}")
+
+    splits_used = 1
+    if wl.splitkv:
+        need = ensure_workspace(B, H)
+        splits_used = max(1, round(need / (B * H * N * (2 * d + 4)))) if need else 1
+
+    def step(i, plain=False):
         qd, kd, vd, od, ld = sets[i % n_sets]
-        st = fa.fa_fwd(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), od.data_ptr(),
-                       ld.data_ptr(), B, H, N, d, wl.scale, int(wl.causal), dcode, handle)
-        if st != fa.FA_OK:
-            raise RuntimeError(f"fa_fwd failed: {fa.fa_status_string(st)}")
+        call(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), od.data_ptr(), ld.data_ptr(), B, H,
+             plain=plain)
 
     with torch.cuda.stream(stream):
         for i in range(warmup):
@@ -345,6 +381,19 @@ def run_ours(args, wl):
     ms_per_step = ms / args.steps
     value = world * wl.flops * args.steps / (ms / 1e3) / 1e12
 
+    plain_ms = None
+    if wl.splitkv:
+        # the same steps through the unsplit forward, for comparison
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                step(i, plain=True)
+        start.record(stream)
+        for i in range(args.steps):
+            step(i, plain=True)
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+        plain_ms = start.elapsed_time(end) / args.steps
+
     # End to end through the public API with host buffers: each step copies
     # Q, K, V from pinned host memory, runs the forward pass and copies O and
     # LSE back.  The B*H heads are cut into chunks and the copies of one chunk
@@ -368,11 +417,8 @@ def run_ours(args, wl):
                 ev_in = torch.cuda.Event()
                 ev_in.record(s_in)
             stream.wait_event(ev_in)
-            st_ = fa.fa_fwd(dq[a0].data_ptr(), dk[a0].data_ptr(), dv[a0].data_ptr(),
-                            do_[a0].data_ptr(), dl[a0].data_ptr(), 1, a1 - a0, N, d,
-                            wl.scale, int(wl.causal), dcode, handle)
-            if st_ != fa.FA_OK:
-                raise RuntimeError(f"fa_fwd failed: {fa.fa_status_string(st_)}")
+            call(dq[a0].data_ptr(), dk[a0].data_ptr(), dv[a0].data_ptr(),
+                 do_[a0].data_ptr(), dl[a0].data_ptr(), 1, a1 - a0)
             ev_c = torch.cuda.Event()
             ev_c.record(stream)
             with torch.cuda.stream(s_out):
@@ -380,6 +426,9 @@ def run_ours(args, wl):
                 o_h[a0:a1].copy_(do_[a0:a1], non_blocking=True)
                 l_h[a0:a1].copy_(dl[a0:a1], non_blocking=True)
 
+    if wl.splitkv:
+        for (a0, a1) in bounds:
+            ensure_workspace(1, a1 - a0)
     e2e_step()
     torch.cuda.synchronize(dev)
     e0 = torch.cuda.Event(enable_timing=True)
@@ -420,9 +469,13 @@ def run_ours(args, wl):
             "e2e": {"value": world * wl.flops / (e2e_ms / 1e3) / 1e12, "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms, "pipelined_chunks": n_chunks},
-            "gpu_launches": args.steps,
+            "gpu_launches": args.steps * launches_per_call,
             "clocks": clocks,
         }
+        if wl.splitkv:
+            line["splitkv"] = {"num_splits": splits_used,
+                               "unsplit_fa_fwd_ms_per_step": plain_ms,
+                               "unsplit_tflops": wl.flops / (plain_ms / 1e3) / 1e12}
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = _cpu_baseline(wl)
         print(json.dumps(line), flush=True)
@@ -438,7 +491,8 @@ def main():
                     help="timed steps (default: about two seconds of work)")
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", type=int, default=2,
-                    help="1..5 (default 2: B=4 H=16 N=2048 d=128 bf16 full)")
+                    help="1..6 (default 2: B=4 H=16 N=2048 d=128 bf16 full; "
+                         "6: the split-KV case)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

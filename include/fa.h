@@ -112,6 +112,59 @@ FA_API int fa_fwd_ext(const void* q, const void* k, const void* v, void* o, floa
                       int B, int H, int H_kv, int N, int d, float scale, int causal,
                       int window_left, int window_right, int dtype, void* stream);
 
+/*
+ * fa_fwd_splitkv -- fa_fwd_ext with the keys of every query row cut into
+ * `num_splits` contiguous ranges that run as separate work units, then merged.
+ *
+ * Source: flash-attention "hopper/flash_fwd_kernel.h" (the older
+ * FlashAttention-3 forward shell, compute_attn_ws): its work tiles carry a
+ * key-split index (n_split_idx, Is_split) so that few (b,h) query tiles can
+ * still fill the GPU.  The page stops at the split partials; the merge is
+ * the log-sum-exp mixture of per-split softmaxes:
+ *     LSE = ln sum_s exp(LSE_s),   O = sum_s exp(LSE_s - LSE) O_s,
+ * where split s holds the row's admissible keys of its range (a split with
+ * none of them is left out).
+ *
+ *   num_splits  requested split count; 0 picks one: 1 when the
+ *               B*H*ceil(N/256) query units (ceil(N/128) per head for
+ *               d = 256) are at least the SM count, else the count (up to 32)
+ *               with the shortest estimated persistent-grid makespan.
+ *               Clamped to the number of K/V tiles (128 keys; 64 for
+ *               d = 256); the splits cover equal whole tiles, so the count
+ *               used may be lower than asked.  Negative: FA_ERR_INVALID_ARG.
+ *   workspace   device scratch of at least fa_splitkv_workspace_bytes()
+ *               bytes for the same arguments, 256-byte
+ *               aligned (else FA_ERR_MISALIGNED).  Layout: the 16-bit partial
+ *               O of each split [S][B][H][N][d], then at the next 256-byte
+ *               boundary the fp32 partial LSE [S][B][H][N].  Nothing in it
+ *               needs to be initialised; it is overwritten.  May be NULL when
+ *               the split count used is 1 (the call is then fa_fwd_ext).
+ *   workspace_bytes  its size; smaller than required: FA_ERR_INVALID_ARG.
+ *
+ * The call enqueues two kernels on `stream` (the split forward, then the
+ * merge); the workspace must not be used by another call until both ran.
+ * O carries one more 16-bit rounding than fa_fwd_ext (of each partial).
+ * Every other argument and rule is that of fa_fwd_ext; the call allocates
+ * no device memory.
+ */
+FA_API int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                          int B, int H, int H_kv, int N, int d, float scale, int causal,
+                          int window_left, int window_right, int dtype, int num_splits,
+                          void* workspace, unsigned long long workspace_bytes,
+                          void* stream);
+
+/*
+ * Workspace bytes fa_fwd_splitkv needs for these arguments (the same values
+ * as its own; the split count chosen for num_splits = 0 depends on the mask
+ * and on the current device's SM count), written to *bytes: 0 when the split
+ * count used is 1 or the problem is empty.  Returns FA_OK, or
+ * FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED for the argument errors of
+ * fa_fwd_splitkv, FA_ERR_CUDA if the SM count cannot be read.
+ */
+FA_API int fa_splitkv_workspace_bytes(int B, int H, int N, int d, int causal,
+                                      int window_left, int window_right, int num_splits,
+                                      unsigned long long* bytes);
+
 /* Human-readable name of a status code (static string, never NULL). */
 FA_API const char* fa_status_string(int status);
 

@@ -121,3 +121,65 @@ def test_ext_head_grouping_errors(fa, H, H_kv, code):
 
 def test_ext_empty_is_noop(fa):
     assert _call_ext(fa, H=4, H_kv=2, N=0) == fa.FA_OK
+
+
+# ------------------------------------------------------------- split-KV
+def _ws_bytes(fa, B=1, H=2, N=1024, d=128, S=4):
+    st, n = fa.fa_splitkv_workspace_bytes(B, H, N, d, 0, -1, -1, S)
+    assert st == fa.FA_OK
+    return n
+
+
+def test_splitkv_workspace_size(fa):
+    # 4 splits of 1024 keys (8 tiles of 128 -> 2 tiles each): 16-bit O
+    # partials, then fp32 LSE partials at a 256-byte boundary
+    assert _ws_bytes(fa) == 4 * 2 * 1024 * 128 * 2 + 4 * 2 * 1024 * 4
+    # 3 splits of 8 tiles: 3 tiles per split -> still 3 splits
+    assert _ws_bytes(fa, S=3) == 3 * 2 * 1024 * 128 * 2 + 3 * 2 * 1024 * 4
+    # 7 requested of 8 tiles: 2 tiles per split -> 4 splits used
+    assert _ws_bytes(fa, S=7) == _ws_bytes(fa, S=4)
+    # more splits than tiles: one tile each
+    assert _ws_bytes(fa, S=100) == _ws_bytes(fa, S=8)
+    # d = 256 cuts 64-key tiles: 16 of them at N = 1024
+    assert _ws_bytes(fa, d=256, S=16) == 16 * 2 * 1024 * 256 * 2 + 16 * 2 * 1024 * 4
+    # odd sizes: the LSE part starts on a 256-byte boundary
+    o_bytes = 2 * 1 * 3 * 200 * 64 * 2
+    assert _ws_bytes(fa, B=1, H=3, N=200, d=64, S=2) == ((o_bytes + 255) // 256) * 256 \
+        + 2 * 3 * 200 * 4
+    # one split, or nothing to do: no workspace
+    assert _ws_bytes(fa, S=1) == 0
+    assert _ws_bytes(fa, N=100, S=4) == 0   # a single K/V tile
+    assert _ws_bytes(fa, N=0, S=4) == 0
+
+
+@pytest.mark.parametrize("args,code", [
+    ((1, 2, 1024, 128, 0, -1, -1, -1), 1), ((-1, 2, 1024, 128, 0, -1, -1, 2), 1),
+    ((1, 2, 1024, 96, 0, -1, -1, 2), 2), ((1, 2, 1024, 128, 2, -1, -1, 2), 1)])
+def test_splitkv_workspace_size_errors(fa, args, code):
+    assert fa.fa_splitkv_workspace_bytes(*args)[0] == code
+
+
+def _call_split(fa, S=4, ws=0x100000, ws_bytes=None, **kw):
+    a = dict(GOOD, N=1024, H=2)
+    a.update(kw)
+    if ws_bytes is None:
+        ws_bytes = _ws_bytes(fa, a["B"], a["H"], a["N"], a["d"], S)
+    return fa.fa_fwd_splitkv(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"],
+                             a.get("H_kv", a["H"]), a["N"], a["d"], a["scale"], a["causal"],
+                             -1, -1, a["dtype"], S, ws, ws_bytes, a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(S=-2, ws_bytes=1 << 30), 1),
+    (dict(ws=0), 1),                     # splits used > 1 but no workspace
+    (dict(ws_bytes=1024), 1),            # too small
+    (dict(ws=0x100010), 3),              # not 256-byte aligned
+    (dict(H_kv=3), 1), (dict(d=32, ws_bytes=1 << 30), 2), (dict(q=0x1008), 3),
+    (dict(scale=0.0), 1),
+])
+def test_splitkv_argument_errors(fa, kw, code):
+    assert _call_split(fa, **kw) == code
+
+
+def test_splitkv_empty_is_noop(fa):
+    assert _call_split(fa, N=0, ws=0, ws_bytes=0) == fa.FA_OK

@@ -237,7 +237,14 @@ def test_watchdog_times_out_cleanly(fa):
 # ------------------------------------------------------- the workloads
 def _workload_case(fa, wl, full):
     q, k, v = make_qkv(wl)
-    o, lse = _run(fa, q, k, v, wl.scale, wl.causal)
+    if wl.splitkv:
+        o, lse = fa.fwd_splitkv(q.cuda(), k.cuda(), v.cuda(), scale=wl.scale,
+                                causal=wl.causal, num_splits=0)
+        torch.cuda.synchronize()
+        st, site = fa.fa_get_device_status(None)
+        assert st == fa.FA_OK, f"device status {fa.fa_status_string(st)} at site {site}"
+    else:
+        o, lse = _run(fa, q, k, v, wl.scale, wl.causal)
     if full:
         o_ref, lse_ref = oracle.attention(q, k, v, wl.scale, wl.causal)
         return _check(o, lse, o_ref, lse_ref, wl.name)

@@ -31,6 +31,7 @@ class Workload:
     dtype: str            # "fp16" or "bf16"
     causal: bool
     qk_mult: float = 1.0  # Q and K multiplied by this after rounding
+    splitkv: bool = False  # run through the split-KV entry point (automatic count)
 
     @property
     def scale(self) -> float:
@@ -55,6 +56,7 @@ class Workload:
     def describe(self) -> str:
         mask = "causal" if self.causal else "full"
         extra = f", Q,K x{self.qk_mult:g}" if self.qk_mult != 1.0 else ""
+        extra += ", split-KV" if self.splitkv else ""
         return (f"B={self.B} H={self.H} N={self.N} d={self.d} {self.dtype} "
                 f"{mask}{extra}")
 
@@ -65,6 +67,10 @@ WORKLOADS = [
     Workload(3, "bf16_d128_n8192_causal", 2, 16, 8192, 128, "bf16", True),
     Workload(4, "bf16_d256_n4096_peaky", 4, 8, 4096, 256, "bf16", False, 2.0),
     Workload(5, "bf16_d128_n32768_causal", 1, 32, 32768, 128, "bf16", True),
+    # one long causal sequence with a single head: 128 query-tile pairs
+    # cannot fill the SMs on their own (the split-KV case)
+    Workload(6, "bf16_d128_n32768_h1_causal_splitkv", 1, 1, 32768, 128, "bf16", True,
+             splitkv=True),
 ]
 
 
