@@ -28,6 +28,10 @@ FA_ERR_UNSUPPORTED = 2
 FA_ERR_MISALIGNED = 3
 FA_ERR_CUDA = 4
 FA_ERR_DEVICE_TIMEOUT = 5
+FA_ERR_SCRATCH_LIMIT = 6
+
+# Size of the library's fixed per-device split-KV scratch (fa.h).
+FA_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 # Every exported symbol of include/fa.h, with its ctypes signature.
 _vp, _i, _f, _ll = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_longlong
@@ -38,6 +42,8 @@ SIGNATURES = {
     "fa_fwd_splitkv": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _i, _i, _i,
                         _vp, _ull, _vp], _i),
     "fa_splitkv_workspace_bytes": ([_i, _i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(_ull)], _i),
+    "fa_fwd_splitkv_noalloc": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _i, _i,
+                                _i, _vp], _i),
     "fa_status_string": ([_i], ctypes.c_char_p),
     "fa_get_device_status": ([_vp, ctypes.POINTER(_i)], _i),
     "fa_set_wait_timeout_us": ([_ll], _i),
@@ -103,6 +109,15 @@ def fa_fwd_splitkv(q: int, k: int, v: int, o: int, lse: int | None, B: int, H: i
     return int(_lib.fa_fwd_splitkv(q, k, v, o, lse or None, B, H, H_kv, N, d, scale, causal,
                                    window_left, window_right, dtype, num_splits,
                                    workspace or None, int(workspace_bytes), stream or None))
+
+
+def fa_fwd_splitkv_noalloc(q: int, k: int, v: int, o: int, lse: int | None, B: int, H: int,
+                           H_kv: int, N: int, d: int, scale: float, causal: int,
+                           window_left: int, window_right: int, dtype: int, num_splits: int,
+                           stream: int | None) -> int:
+    return int(_lib.fa_fwd_splitkv_noalloc(q, k, v, o, lse or None, B, H, H_kv, N, d, scale,
+                                           causal, window_left, window_right, dtype,
+                                           num_splits, stream or None))
 
 
 def fa_splitkv_workspace_bytes(B: int, H: int, N: int, d: int, causal: int, window_left: int,
@@ -242,9 +257,11 @@ def fwd_splitkv(q, k, v, *, num_splits: int = 0, scale: float | None = None,
 
 __all__ = [
     "LIB_PATH", "SIGNATURES", "FaError", "fwd", "fwd_splitkv", "fa_fwd", "fa_fwd_ext",
-    "fa_fwd_splitkv", "fa_splitkv_workspace_bytes", "fa_status_string",
+    "fa_fwd_splitkv", "fa_splitkv_workspace_bytes", "fa_fwd_splitkv_noalloc",
+    "fa_status_string",
     "fa_get_device_status", "fa_set_wait_timeout_us", "fa_set_max_ctas",
     "fa_selftest_watchdog", "fa_num_sms",
     "FA_DTYPE_F16", "FA_DTYPE_BF16", "FA_OK", "FA_ERR_INVALID_ARG",
     "FA_ERR_UNSUPPORTED", "FA_ERR_MISALIGNED", "FA_ERR_CUDA", "FA_ERR_DEVICE_TIMEOUT",
+    "FA_ERR_SCRATCH_LIMIT", "FA_NOALLOC_SCRATCH_BYTES",
 ]

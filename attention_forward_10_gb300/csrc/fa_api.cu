@@ -134,6 +134,7 @@ const char* fa_status_string(int status) {
     case FA_ERR_MISALIGNED: return "FA_ERR_MISALIGNED";
     case FA_ERR_CUDA: return "FA_ERR_CUDA";
     case FA_ERR_DEVICE_TIMEOUT: return "FA_ERR_DEVICE_TIMEOUT";
+    case FA_ERR_SCRATCH_LIMIT: return "FA_ERR_SCRATCH_LIMIT";
     default: return "FA_ERR_UNKNOWN";
   }
 }
@@ -461,6 +462,46 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
   const ForwardCall c{q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, window_left,
                       window_right, dtype, stream};
   return splitkv_forward(c, num_splits, workspace, workspace_bytes);
+}
+
+// Split-KV into the library's fixed per-device scratch (declared with its
+// limits and hazards in fa.h; the array and its look-up are in fa_noalloc.cu).
+int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int B, int H, int H_kv, int N, int d, float scale, int causal,
+                           int window_left, int window_right, int dtype, int num_splits,
+                           void* stream) {
+  using namespace fa;
+  const ForwardCall c{q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, window_left,
+                      window_right, dtype, stream};
+  int st = validate(c);
+  if (st != FA_OK) return st;
+  if (num_splits < 0) return FA_ERR_INVALID_ARG;
+  if (empty_problem(c)) return FA_OK;
+  st = check_pointers(c);
+  if (st != FA_OK) return st;
+  int num_sms = 0;
+  if (num_splits == 0) {
+    num_sms = fa_num_sms();
+    if (num_sms <= 0) return FA_ERR_CUDA;
+  }
+  const unsigned long long limit = FA_NOALLOC_SCRATCH_BYTES;
+  int splits = 1, split_tiles = 0;
+  plan_splits(c, num_splits, num_sms, &splits, &split_tiles);
+  if (num_splits == 0) {
+    // automatic count: the largest count at or below the planned one that fits
+    while (splits > 1 && workspace_bytes(c, splits) > limit)
+      plan_splits(c, splits - 1, num_sms, &splits, &split_tiles);
+  } else if (splits > 1 && workspace_bytes(c, splits) > limit) {
+    return FA_ERR_SCRATCH_LIMIT;
+  }
+  if (splits == 1) return splitkv_forward(c, 1, nullptr, 0);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  cudaError_t rc = cudaSuccess;
+  void* scratch = noalloc_scratch(dev, &rc);
+  if (scratch == nullptr || rc != cudaSuccess) return FA_ERR_CUDA;
+  // the count is passed explicitly, so it resolves to `splits` again
+  return splitkv_forward(c, splits, scratch, limit);
 }
 
 int fa_get_device_status(void* stream, int* site) {

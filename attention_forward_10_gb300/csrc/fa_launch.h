@@ -34,6 +34,11 @@ cudaError_t launch_splitkv_combine(const void* o_part, const float* lse_part, vo
                                    float* lse, const CombineArgs& a, bool bf16, int num_sms,
                                    cudaStream_t stream);
 
+// Device address of the fixed split-KV scratch of the current device `dev`
+// (FA_NOALLOC_SCRATCH_BYTES bytes, 256-byte aligned), looked up on the first
+// call per device; nullptr with the CUDA error in *rc if that fails.
+void* noalloc_scratch(int dev, cudaError_t* rc);
+
 // Enqueue the watchdog self-test kernel (one CTA).
 cudaError_t launch_watchdog_selftest(int* status, unsigned long long timeout_ns,
                                      cudaStream_t stream);

@@ -52,7 +52,9 @@ typedef enum {
   FA_ERR_UNSUPPORTED = 2,     /* head dim / device not supported */
   FA_ERR_MISALIGNED = 3,      /* a pointer breaks the alignment rule below */
   FA_ERR_CUDA = 4,            /* a CUDA runtime call or the launch failed */
-  FA_ERR_DEVICE_TIMEOUT = 5   /* a device-side wait ran out (watchdog) */
+  FA_ERR_DEVICE_TIMEOUT = 5,  /* a device-side wait ran out (watchdog) */
+  FA_ERR_SCRATCH_LIMIT = 6    /* the split partials would not fit in the
+                                 library's fixed scratch (fa_fwd_splitkv_noalloc) */
 } fa_status_t;
 
 /*
@@ -164,6 +166,44 @@ FA_API int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, 
 FA_API int fa_splitkv_workspace_bytes(int B, int H, int N, int d, int causal,
                                       int window_left, int window_right, int num_splits,
                                       unsigned long long* bytes);
+
+/*
+ * fa_fwd_splitkv_noalloc -- fa_fwd_splitkv without a caller workspace: the
+ * split partials go to a scratch array that the library keeps in static
+ * device memory, FA_NOALLOC_SCRATCH_BYTES (32 MiB) per device.  The pages
+ * have no counterpart: this entry point exists for callers that cannot
+ * allocate at call time (no cudaMalloc / cudaFree, which can synchronise the
+ * device, on a hot path; engines whose device memory is fixed at start-up;
+ * plain C callers without a caching allocator).  The call allocates nothing,
+ * through CUDA or any library.
+ *
+ *   num_splits  as for fa_fwd_splitkv, with the scratch as the workspace:
+ *               an explicit count whose partials need more than
+ *               FA_NOALLOC_SCRATCH_BYTES (fa_splitkv_workspace_bytes) is
+ *               rejected with FA_ERR_SCRATCH_LIMIT before anything is
+ *               enqueued; 0 takes the automatic count, lowered to the largest
+ *               count whose partials fit.  A count that resolves to 1 split
+ *               is the plain forward (no scratch used).
+ * Every other argument, layout, alignment rule and error is that of
+ * fa_fwd_splitkv.
+ *
+ * Set-up: the first call on each device looks up that device's scratch
+ * address (cudaGetSymbolAddress, which can load the library's device code);
+ * make that first call before capturing any stream.  A failed look-up
+ * returns FA_ERR_CUDA and is retried by the next call.
+ *
+ * Nothing in the scratch has to start at zero: each call writes every
+ * partial it later reads.  All calls on one device share the one scratch, so
+ * calls whose kernels may overlap (different streams without ordering
+ * between them, or several host threads) race on it and can return wrong
+ * results: order them on one stream or with events.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES (32ull << 20)
+
+FA_API int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
+                                  float* lse, int B, int H, int H_kv, int N, int d,
+                                  float scale, int causal, int window_left, int window_right,
+                                  int dtype, int num_splits, void* stream);
 
 /* Human-readable name of a status code (static string, never NULL). */
 FA_API const char* fa_status_string(int status);

@@ -183,3 +183,27 @@ def test_splitkv_argument_errors(fa, kw, code):
 
 def test_splitkv_empty_is_noop(fa):
     assert _call_split(fa, N=0, ws=0, ws_bytes=0) == fa.FA_OK
+
+
+# ----------------------------------------------- split-KV, fixed scratch
+def _call_noalloc(fa, S, **kw):
+    a = dict(GOOD, N=8192, H=8)
+    a.update(kw)
+    return fa.fa_fwd_splitkv_noalloc(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"],
+                                     a["H"], a["H"], a["N"], a["d"], a["scale"], a["causal"],
+                                     -1, -1, a["dtype"], S, a["stream"])
+
+
+def test_noalloc_rejects_partials_beyond_the_scratch(fa):
+    assert fa.fa_status_string(fa.FA_ERR_SCRATCH_LIMIT) == "FA_ERR_SCRATCH_LIMIT"
+    # 8 splits of 8 heads x 8192 rows x (256 + 4) bytes = 136 MB > 32 MiB
+    st, need = fa.fa_splitkv_workspace_bytes(1, 8, 8192, 128, 0, -1, -1, 8)
+    assert st == fa.FA_OK and need > fa.FA_NOALLOC_SCRATCH_BYTES
+    assert _call_noalloc(fa, 8) == fa.FA_ERR_SCRATCH_LIMIT
+
+
+@pytest.mark.parametrize("kw,code", [(dict(S=-1), 1), (dict(S=2, d=32), 2),
+                                     (dict(S=2, o=0x4001), 3), (dict(S=2, N=0), 0)])
+def test_noalloc_argument_errors(fa, kw, code):
+    S = kw.pop("S")
+    assert _call_noalloc(fa, S, **kw) == code
