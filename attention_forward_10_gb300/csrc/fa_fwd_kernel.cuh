@@ -29,8 +29,12 @@
 //   [P_0(j-1) V_(j-1), Q_0 K_j^T]  [P_1(j-1) V_(j-1), Q_1 K_j^T]  ...
 // over the stream of K/V tiles j (continuing across work units), so that
 // each tile's softmax runs while the other tile's two MMAs execute.  P_g lives
-// in S_g's tensor-memory columns, and tcgen05 orders only MMAs into the same
-// accumulator, so Q_g K_j^T is issued only after P_g(j-1) V has completed.
+// in S_g's tensor-memory columns; Q_g K_j^T follows P_g(j-1) V without a
+// completion wait, relying on the tensor pipe running one CTA's MMAs in issue
+// order (each has read its operands before a later one writes its
+// accumulator).  Waiting for the P V commit there instead left the pipe idle
+// for the commit's round trip twice per step (5% at N = 2048); repeated
+// full-size runs are checked to be bit-identical.
 //
 // Tensor memory (512 columns x 128 lanes, fp32):
 //   [0,128)    S_0 (scores of tile 0); P_0 (16-bit, packed in pairs) is
@@ -82,6 +86,7 @@ struct Layout {
   static_assert(D == 64 || D == 128, "head dim");
   static constexpr uint32_t kTileBytes = kBlockM * D * 2;  // == kBlockN * D * 2
   static constexpr int kStages = (D == 64) ? 6 : 4;
+  static_assert(kStages % 2 == 0, "K and V share the ring in pairs");
   static constexpr uint32_t kQOff = 0;
   static constexpr uint32_t kKVOff = kQOff + 2 * kTileBytes;
   static constexpr uint32_t kStageOff = kKVOff + kStages * kTileBytes;
@@ -90,8 +95,10 @@ struct Layout {
   static constexpr int kQFull = 0;
   static constexpr int kQEmpty = 2;
   static constexpr int kKVFull = 4;
+  // release groups: the commit of K/V step j frees K(j) and V(j-1) and
+  // arrives on group j % (kStages / 2)
   static constexpr int kKVEmpty = kKVFull + kStages;
-  static constexpr int kSFull = kKVEmpty + kStages;
+  static constexpr int kSFull = kKVEmpty + kStages / 2;
   static constexpr int kPFull = kSFull + 2;
   static constexpr int kODone = kPFull + 2;
   static constexpr int kDrain = kODone + 2;
@@ -173,6 +180,52 @@ __device__ __forceinline__ Unit decode_unit(int u, const FaParams& p) {
   return w;
 }
 
+// Maximum of a row of scores: four independent chains.
+__device__ __forceinline__ float tile_max(const float (&s)[kBlockN]) {
+  float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+  for (int c = 4; c < kBlockN; c += 4) {
+    mx0 = fmaxf(mx0, s[c]);
+    mx1 = fmaxf(mx1, s[c + 1]);
+    mx2 = fmaxf(mx2, s[c + 2]);
+    mx3 = fmaxf(mx3, s[c + 3]);
+  }
+  return fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+}
+
+// p = 2^(s*scale*log2e - m) for one row of a tile: one packed FMA per pair,
+// then the exponentials; P (16-bit, packed in pairs) goes to tensor memory
+// at tS, over the first half of the row's scores.  Returns the row sum of p
+// (kept as two packed partial sums).
+template <bool BF16>
+__device__ __forceinline__ float exp_tile_to_tmem(const float (&s)[kBlockN], float scale_log2,
+                                                  float m, uint32_t tS) {
+  const uint64_t scale2 = pack_f32x2(scale_log2, scale_log2);
+  const uint64_t neg_m2 = pack_f32x2(-m, -m);
+  uint64_t acc_a = pack_f32x2(0.f, 0.f), acc_b = acc_a;
+#pragma unroll
+  for (int c0 = 0; c0 < kBlockN; c0 += 32) {
+    uint32_t pk[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      float x0, x1;
+      unpack_f32x2(fma_f32x2(pack_f32x2(s[c0 + 2 * e], s[c0 + 2 * e + 1]), scale2, neg_m2), x0,
+                   x1);
+      const float p0 = ex2_approx(x0);
+      const float p1 = ex2_approx(x1);
+      if (e & 1)
+        acc_b = add_f32x2(acc_b, pack_f32x2(p0, p1));
+      else
+        acc_a = add_f32x2(acc_a, pack_f32x2(p0, p1));
+      pk[e] = pack2<BF16>(p0, p1);
+    }
+    tmem_st_x16(tS + c0 / 2, pk);
+  }
+  float a0, a1;
+  unpack_f32x2(add_f32x2(acc_a, acc_b), a0, a1);
+  return a0 + a1;
+}
+
 template <int D, bool CAUSAL, bool BF16>
 __global__ void __launch_bounds__(kNumThreads, 1)
     fa_fwd_kernel(const __grid_constant__ FaParams p) {
@@ -198,10 +251,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       mbar_init(bar(L::kPFull + g), 128);
       mbar_init(bar(L::kODone + g), 1);
     }
-    for (int s = 0; s < L::kStages; ++s) {
-      mbar_init(bar(L::kKVFull + s), 1);
-      mbar_init(bar(L::kKVEmpty + s), 1);
-    }
+    for (int s = 0; s < L::kStages; ++s) mbar_init(bar(L::kKVFull + s), 1);
+    for (int s = 0; s < L::kStages / 2; ++s) mbar_init(bar(L::kKVEmpty + s), 1);
     mbar_init(bar(L::kDrain), 1);
     mbar_init(bar(L::kStageFull), 128);
     mbar_init(bar(L::kStageEmpty), 1);
@@ -244,9 +295,18 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         }
         for (int n = w.n_beg; n < w.n_end && ok; ++n) {
           for (int kv = 0; kv < 2; ++kv) {
+            // K(j) goes to slot 2(j % h), V(j) to slot 2(j % h) + 1
             const uint32_t slot = kv_it % L::kStages;
-            const uint32_t phase = (kv_it / L::kStages) & 1u;
-            ok = wait_bar(bar(L::kKVEmpty + slot), phase ^ 1u, ctl, kSiteProducerKV);
+            {
+              // The slot's previous tenant, K(j-h) or V(j-h), was released by
+              // the one commit of step j-h or j-h+1 (release group step % h).
+              constexpr int h = L::kStages / 2;
+              const int j = static_cast<int>(kv_it / 2);
+              if (j >= h) {
+                const int rel = kv ? j - h + 1 : j - h;
+                ok = wait_bar(bar(L::kKVEmpty + rel % h), (rel / h) & 1, ctl, kSiteProducerKV);
+              }
+            }
             if (!ok) break;
             mbar_arrive_expect_tx(bar(L::kKVFull + slot), L::kTileBytes);
             tma_load_4d(sbase + L::kKVOff + slot * L::kTileBytes, kv ? &p.tm_v : &p.tm_k,
@@ -281,6 +341,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       // 8-key groups 1024 B apart (SBO).
       const uint64_t v_desc0 = smem_desc_sw128(sbase + L::kKVOff, kBlockN * 128, 1024);
       uint32_t slot = 0, phase = 0;  // next K/V ring position
+      uint32_t step = 0;             // K/V stream step (for the release groups)
       uint32_t q_par[2] = {0, 0}, p_par[2] = {0, 0}, o_cnt[2] = {0, 0};
       bool ok = true;
       // Step j of the K/V stream is (unit u, tile n); prev_* describe step
@@ -321,16 +382,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             tc_commit(bar(L::kODone + g));
             ++o_cnt[g];
           }
-          // ---- S_g = Q_g K_j^T (after P_g(j-1) V, which reads S_g's columns)
+          // ---- S_g = Q_g K_j^T, issued right behind P_g(j-1) V, which
+          //      reads P_g(j-1) from the columns this overwrites
           if (cur_valid && n >= w.n0[g] && n < w.n1[g]) {
             if (!k_ready) {
               ok = wait_bar(bar(L::kKVFull + kslot), kphase, ctl, kSiteMmaK);
               if (!ok) break;
               k_ready = true;
-            }
-            if (o_cnt[g] > 0) {
-              ok = wait_bar(bar(L::kODone + g), (o_cnt[g] - 1) & 1u, ctl, kSiteMmaO);
-              if (!ok) break;
             }
             tc_fence_after_sync();
             const uint64_t a = q_desc0 + g * kSlotStep;
@@ -344,9 +402,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           }
         }
         if (!ok) break;
-        if (prev_valid) tc_commit(bar(L::kKVEmpty + prev_vslot));
+        // one commit per step releases K(j) and V(j-1) (release group
+        // step % h); the last V goes with the final, K-less step
+        tc_commit(bar(L::kKVEmpty + step % (L::kStages / 2)));
+        ++step;
         if (!cur_valid) break;
-        tc_commit(bar(L::kKVEmpty + kslot));
         if (++slot == (uint32_t)L::kStages) { slot = 0; phase ^= 1u; }
         // V(j): waited for now, used (and released) in step j+1
         const uint32_t vslot = slot;
@@ -424,19 +484,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           for (int c = 0; c < kBlockN; ++c)
             if (c >= hi || c < lo) s[c] = -INFINITY;
         }
-        // row maximum: four independent chains
-        float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
-#pragma unroll
-        for (int c = 4; c < kBlockN; c += 4) {
-          mx0 = fmaxf(mx0, s[c]);
-          mx1 = fmaxf(mx1, s[c + 1]);
-          mx2 = fmaxf(mx2, s[c + 2]);
-          mx3 = fmaxf(mx3, s[c + 3]);
-        }
-        const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * scale_log2;
-
-        const bool need = m_tile > m_ref + kRescaleThreshold;
-        if (__any_sync(0xffffffffu, need)) {
+        const float m_tile = tile_max(s) * scale_log2;
+        if (__any_sync(0xffffffffu, m_tile > m_ref + kRescaleThreshold)) {
           const float m_new = fmaxf(m_ref, m_tile);
           const float factor = (m_new == -INFINITY) ? 1.f : ex2_approx(m_ref - m_new);
           if (n > w.n0[g]) {
@@ -460,37 +509,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           l *= factor;
           m_ref = m_new;
         }
-
-        // p = 2^(s*scale*log2e - m): one packed FMA per pair, then the
-        // exponentials; row sum kept as two packed partial sums.
-        const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-        const uint64_t scale2 = pack_f32x2(scale_log2, scale_log2);
-        const uint64_t neg_m2 = pack_f32x2(-m_use, -m_use);
-        uint64_t acc_a = pack_f32x2(0.f, 0.f), acc_b = acc_a;
-#pragma unroll
-        for (int c0 = 0; c0 < kBlockN; c0 += 32) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            float x0, x1;
-            unpack_f32x2(fma_f32x2(pack_f32x2(s[c0 + 2 * e], s[c0 + 2 * e + 1]), scale2, neg_m2),
-                         x0, x1);
-            const float p0 = ex2_approx(x0);
-            const float p1 = ex2_approx(x1);
-            if (e & 1)
-              acc_b = add_f32x2(acc_b, pack_f32x2(p0, p1));
-            else
-              acc_a = add_f32x2(acc_a, pack_f32x2(p0, p1));
-            pk[e] = pack2<BF16>(p0, p1);
-          }
-          tmem_st_x16(tS + c0 / 2, pk);
-        }
+        l += exp_tile_to_tmem<BF16>(s, scale_log2, (m_ref == -INFINITY) ? 0.f : m_ref, tS);
         tmem_wait_st();
-        {
-          float a0, a1;
-          unpack_f32x2(add_f32x2(acc_a, acc_b), a0, a1);
-          l += a0 + a1;
-        }
         tc_fence_before_sync();
         mbar_arrive(bar(L::kPFull + g));
         ++pv_cnt;

@@ -276,3 +276,19 @@ def test_workload(fa, index):
     wl = workload(index)
     full = wl.B * wl.H * wl.N * wl.N * wl.d <= 4 * 16 * 2048 * 2048 * 128
     _workload_case(fa, wl, full)
+
+
+@pytest.mark.parametrize("index", [2, 3])
+def test_repeat_runs_bit_identical_full_size(fa, index):
+    """Full-size launches repeated back to back give the same bits: the MMA
+    issue order (P V directly followed by the next Q K^T into the columns P
+    occupies) leaves no room for run-to-run variation."""
+    wl = workload(index)
+    q, k, v = (t.cuda() for t in make_qkv(wl))
+    o0, l0 = fa.fwd(q, k, v, scale=wl.scale, causal=wl.causal)
+    for _ in range(8):
+        o, lse = fa.fwd(q, k, v, scale=wl.scale, causal=wl.causal)
+        assert torch.equal(o, o0) and torch.equal(lse, l0)
+    torch.cuda.synchronize()
+    st, site = fa.fa_get_device_status(None)
+    assert st == fa.FA_OK, f"device status {fa.fa_status_string(st)} at site {site}"
