@@ -325,37 +325,53 @@ long long estimate_makespan(const ForwardCall& c, int win_left, int win_right, i
   return worst;
 }
 
+// The automatic split count of recent shapes: choosing one walks the whole
+// persistent schedule for every candidate count, far longer than a launch.
+struct PlanKey {
+  int B, H, N, d, causal, win_left, win_right, num_sms;
+  bool operator==(const PlanKey& o) const {
+    return B == o.B && H == o.H && N == o.N && d == o.d && causal == o.causal &&
+           win_left == o.win_left && win_right == o.win_right && num_sms == o.num_sms;
+  }
+};
+struct PlanEntry {
+  PlanKey key;
+  int want;
+  bool used;
+};
+constexpr int kPlanCacheSize = 64;
+std::mutex g_plan_mutex;
+PlanEntry g_plan_cache[kPlanCacheSize];
+int g_plan_next = 0;
+
+int automatic_split_count(const ForwardCall& c, int num_sms, int n_ktiles);
+
 // Split count actually used for a requested one, and the K/V tiles per
 // split.  0 asks for a count that fills the SMs: when the query units alone
 // leave SMs idle (or unevenly loaded, as causal units are), the count with
-// the shortest estimated makespan, each extra split charged 2% for its
-// partial-output traffic and merge.
+// the shortest estimated makespan plus merge time.
 void plan_splits(const ForwardCall& c, int requested, int num_sms, int* splits,
                  int* split_tiles) {
   const int n_ktiles = (c.N + kv_tile_rows(c.d) - 1) / kv_tile_rows(c.d);
   int want = requested;
   if (want <= 0) {
-    want = 1;
-    const long long units = static_cast<long long>(c.B) * c.H * units_per_head(c.N, c.d);
-    const int grid = std::min(num_sms, 1024);
-    if (units < grid && n_ktiles > 1) {
-      const int win_left = (c.window_left < 0 || c.window_left > c.N) ? c.N : c.window_left;
-      const int win_right =
-          c.causal ? 0 : ((c.window_right < 0 || c.window_right > c.N) ? c.N : c.window_right);
-      double best = static_cast<double>(estimate_makespan(c, win_left, win_right, 1, n_ktiles,
-                                                          grid));
-      for (int s = 2; s <= std::min(n_ktiles, 32); ++s) {
-        const int tiles = (n_ktiles + s - 1) / s;
-        const int used = (n_ktiles + tiles - 1) / tiles;
-        if (used != s) continue;  // same split as a smaller count
-        const double t = static_cast<double>(
-                             estimate_makespan(c, win_left, win_right, s, tiles, grid)) *
-                         (1.0 + 0.02 * (s - 1));
-        if (t < best) {
-          best = t;
-          want = s;
+    const PlanKey key{c.B, c.H, c.N, c.d, c.causal, c.window_left < 0 ? -1 : c.window_left,
+                      c.window_right < 0 ? -1 : c.window_right, num_sms};
+    bool hit = false;
+    {
+      std::lock_guard<std::mutex> lock(g_plan_mutex);
+      for (const PlanEntry& e : g_plan_cache)
+        if (e.used && e.key == key) {
+          want = e.want;
+          hit = true;
+          break;
         }
-      }
+    }
+    if (!hit) {
+      want = automatic_split_count(c, num_sms, n_ktiles);
+      std::lock_guard<std::mutex> lock(g_plan_mutex);
+      g_plan_cache[g_plan_next] = PlanEntry{key, want, true};
+      g_plan_next = (g_plan_next + 1) % kPlanCacheSize;
     }
   }
   if (want > n_ktiles) want = n_ktiles;
@@ -363,6 +379,41 @@ void plan_splits(const ForwardCall& c, int requested, int num_sms, int* splits,
   const int tiles = (n_ktiles + want - 1) / want;
   *split_tiles = tiles;
   *splits = (n_ktiles + tiles - 1) / tiles;
+}
+
+int automatic_split_count(const ForwardCall& c, int num_sms, int n_ktiles) {
+  int want = 1;
+  {
+    const long long units = static_cast<long long>(c.B) * c.H * units_per_head(c.N, c.d);
+    const int grid = std::min(num_sms, 1024);
+    if (units < grid && n_ktiles > 1) {
+      const int win_left = (c.window_left < 0 || c.window_left > c.N) ? c.N : c.window_left;
+      const int win_right =
+          c.causal ? 0 : ((c.window_right < 0 || c.window_right > c.N) ? c.N : c.window_right);
+      // Cost in 128-key tile steps of one query tile (about 1.1 us x d/128
+      // on a GB300 SM).  The split partials are written by the forward and
+      // read back by the merge (at about 5 TB/s), and the merge is one more
+      // launch (about 3 us).
+      const double step_us = 1.1 * c.d / 128.0;
+      const double row_bytes = static_cast<double>(c.B) * c.H * c.N * (2.0 * c.d + 4.0);
+      double best = static_cast<double>(estimate_makespan(c, win_left, win_right, 1, n_ktiles,
+                                                          grid));
+      for (int s = 2; s <= std::min(n_ktiles, 32); ++s) {
+        const int tiles = (n_ktiles + s - 1) / s;
+        const int used = (n_ktiles + tiles - 1) / tiles;
+        if (used != s) continue;  // same split as a smaller count
+        const double merge_us = (2.0 * s + 1.0) * row_bytes / 5.0e6 + 3.0;
+        const double t =
+            static_cast<double>(estimate_makespan(c, win_left, win_right, s, tiles, grid)) +
+            merge_us / step_us;
+        if (t < best) {
+          best = t;
+          want = s;
+        }
+      }
+    }
+  }
+  return want;
 }
 
 // Workspace layout: partial O [S][B*H][N][d] (16-bit), then partial LSE

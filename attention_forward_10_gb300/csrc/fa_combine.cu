@@ -30,6 +30,8 @@ __device__ __forceinline__ float to_float(uint32_t half_bits) {
 }
 
 // One thread per 8 output elements (16 bytes) of a row; d/8 threads per row.
+// The partials of up to four splits are loaded before any is accumulated, so
+// that several 16-byte reads per thread are in flight.
 template <bool BF16>
 __global__ void __launch_bounds__(256)
     fa_splitkv_combine_kernel(const uint16_t* __restrict__ o_part,
@@ -44,40 +46,45 @@ __global__ void __launch_bounds__(256)
     const long long row_id = gid / tpr;  // bh * N + i
     const int part = static_cast<int>(gid % tpr);
     const int i = static_cast<int>(row_id % a.N);
-    // keys query i may see
+    // keys query i may see: [lo, hi); split s holds [s*split_keys, +split_keys)
     const long long lo = static_cast<long long>(i) - a.win_left;
     const long long hi = static_cast<long long>(i) + a.win_right + 1;
+    const int s_first = static_cast<int>((lo > 0 ? lo : 0) / a.split_keys);
+    const long long last_key = (hi < a.N ? hi : a.N) - 1;
+    const int s_last = static_cast<int>(last_key / a.split_keys);  // splits [s_first, s_last]
     float m = -INFINITY;
-    for (int s = 0; s < a.num_splits; ++s) {
-      const long long k0 = static_cast<long long>(s) * a.split_keys;
-      const long long k1 = k0 + a.split_keys;
-      if ((lo > k0 ? lo : k0) < (hi < k1 ? hi : k1) && k0 < a.N)
-        m = fmaxf(m, lse_part[s * part_stride + row_id]);
-    }
+    for (int s = s_first; s <= s_last; ++s) m = fmaxf(m, lse_part[s * part_stride + row_id]);
     uint32_t packed[4] = {0, 0, 0, 0};
     float row_lse = -INFINITY;
     if (m != -INFINITY) {
       float sum = 0.f;
-      for (int s = 0; s < a.num_splits; ++s) {
-        const long long k0 = static_cast<long long>(s) * a.split_keys;
-        const long long k1 = k0 + a.split_keys;
-        if ((lo > k0 ? lo : k0) < (hi < k1 ? hi : k1) && k0 < a.N)
-          sum += expf(lse_part[s * part_stride + row_id] - m);
-      }
+      for (int s = s_first; s <= s_last; ++s) sum += expf(lse_part[s * part_stride + row_id] - m);
       row_lse = m + logf(sum);
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      for (int s = 0; s < a.num_splits; ++s) {
-        const long long k0 = static_cast<long long>(s) * a.split_keys;
-        const long long k1 = k0 + a.split_keys;
-        if (!((lo > k0 ? lo : k0) < (hi < k1 ? hi : k1) && k0 < a.N)) continue;
-        const float wgt = expf(lse_part[s * part_stride + row_id] - row_lse);
-        const uint4 v = *reinterpret_cast<const uint4*>(
-            o_part + (s * part_stride + row_id) * a.d + part * 8);
-        const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+      const uint16_t* src = o_part + row_id * a.d + part * 8;
+      const long long split_elems = part_stride * a.d;
+      for (int s0 = s_first; s0 <= s_last; s0 += 4) {
+        uint4 v[4];
+        float wgt[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          acc[2 * e] += wgt * to_float<BF16>(words[e] & 0xffffu);
-          acc[2 * e + 1] += wgt * to_float<BF16>(words[e] >> 16);
+        for (int k = 0; k < 4; ++k) {
+          const int s = s0 + k;
+          if (s <= s_last) {
+            v[k] = *reinterpret_cast<const uint4*>(src + s * split_elems);
+            wgt[k] = expf(lse_part[s * part_stride + row_id] - row_lse);
+          } else {
+            v[k] = make_uint4(0, 0, 0, 0);
+            wgt[k] = 0.f;
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t words[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            acc[2 * e] += wgt[k] * to_float<BF16>(words[e] & 0xffffu);
+            acc[2 * e + 1] += wgt[k] * to_float<BF16>(words[e] >> 16);
+          }
         }
       }
 #pragma unroll
