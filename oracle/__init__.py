@@ -23,7 +23,9 @@ row stores O = 0 and LSE = -inf).
 ``attention_ex`` adds grouped K/V heads (query head h reads K/V head
 h // (H / H_kv)) and a local window (keys i - window_left .. i + window_right),
 the ``qhead_per_khead`` and ``window_size_left/right`` options of the same
-backward page.
+backward page.  ``attention_varlen`` takes sequences of different lengths
+packed along the rows ([total, H, d], cu_seqlens offsets), the
+variable-length mode of the Hopper pages.
 
 Pins (checked by ``tests/test_oracle.py`` against facts other than this code):
 closed forms (N = 1, Q = 0, hand-derived golden example), invariants (row
@@ -89,6 +91,9 @@ def _bind(path: str):
                                          c_long, c_long, c_double, c_int, c_long,
                                          c_long, vp, c_long, vp, vp, c_int]
     lib.attn_ref_rows_u16_ex.restype = c_int
+    lib.attn_ref_varlen_u16.argtypes = [vp, vp, vp, c_int, vp, c_long, c_long, c_long, c_long,
+                                        c_long, c_double, c_int, c_long, c_long, vp, vp, c_int]
+    lib.attn_ref_varlen_u16.restype = c_int
     lib.attn_ref_widen.argtypes = [ctypes.c_uint16, c_int]
     lib.attn_ref_widen.restype = c_double
     lib.attn_ref_max_threads.argtypes = []
@@ -254,4 +259,32 @@ def attention_rows_ex(q, k, v, scale: float, causal: bool, rows, window_left: in
                                       _ptr(o), _ptr(lse), int(nthreads))
     if rc != 0:
         raise RuntimeError("oracle attn_ref_rows_u16_ex failed")
+    return o, lse
+
+
+def attention_varlen(q, k, v, cu_seqlens, scale: float, causal: bool, window_left: int = -1,
+                     window_right: int = -1, nthreads: int = 0):
+    """Sequences packed along the rows: q [total, H, d], k, v [total, H_kv, d],
+    sequence b = rows cu_seqlens[b] .. cu_seqlens[b+1]-1 (self-attention within
+    each sequence, mask and window counted from its start).  Returns O
+    [total, H, d] and LSE [H, total] (float64); rows outside every sequence
+    are NaN."""
+    qw, is_bf16 = _u16_view(q)
+    kw, kb = _u16_view(k)
+    vw, vb = _u16_view(v)
+    if not (is_bf16 == kb == vb):
+        raise TypeError("q, k, v must share one dtype")
+    total, H, d = (int(x) for x in q.shape)
+    if k.shape != v.shape or k.shape[0] != total or k.shape[2] != d or H % int(k.shape[1]):
+        raise ValueError("k, v must be [total, H_kv, d] with H a multiple of H_kv")
+    H_kv = int(k.shape[1])
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int64).reshape(-1))
+    o = np.full((total, H, d), np.nan, dtype=np.float64)
+    lse = np.full((H, total), np.nan, dtype=np.float64)
+    rc = _load().attn_ref_varlen_u16(_ptr(qw), _ptr(kw), _ptr(vw), int(is_bf16), _ptr(cu),
+                                     cu.size - 1, total, H, H_kv, d, float(scale),
+                                     int(bool(causal)), int(window_left), int(window_right),
+                                     _ptr(o), _ptr(lse), int(nthreads))
+    if rc != 0:
+        raise RuntimeError("oracle attn_ref_varlen_u16 failed")
     return o, lse

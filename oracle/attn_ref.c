@@ -40,6 +40,12 @@
  * the page's window_size_left / window_size_right and its Is_local mask).
  * With H_kv = H and both bounds negative they reduce to the definition above.
  *
+ * Variable-length batches (attn_ref_varlen_u16): sequences of different
+ * lengths packed along the rows of [total][H][d] tensors, sequence b being
+ * rows cu[b] .. cu[b+1]-1 -- the cu_seqlens mode of the Hopper pages.  Each
+ * sequence is the definition above on its own rows, positions counted from
+ * its first row.
+ *
  * Inputs are the caller's 16-bit words (IEEE binary16 or bfloat16), widened
  * exactly to double here; every product, sum and exponential is in double.
  * The computation is the textbook two-pass softmax per row -- no tiling, no
@@ -396,5 +402,76 @@ int attn_ref_rows_u16_ex(const uint16_t *q, const uint16_t *k,
             if (rows[3 * r] * H_kv + rows[3 * r + 1] / group == bkv) done[r] = 1;
     }
     free(kd); free(vd); free(done);
+    return rc;
+}
+
+/*
+ * Variable-length batch: sequences packed along the rows (self-attention,
+ * each sequence's queries see that sequence's keys only) -- the cu_seqlens
+ * mode of flash-attention "hopper/flash_fwd_kernel.h" and
+ * "hopper/mainloop_bwd_sm90_tma_gmma_ws.hpp".
+ *   q, o : [total][H][d];  k, v : [total][H_kv][d];  lse : [H][total]
+ *   cu   : batch + 1 row offsets; sequence b is rows cu[b] .. cu[b+1]-1,
+ *          and its row i (counted from the sequence start) sees the keys
+ *          J(i) of that sequence under the mask and window of the _ex path.
+ * Rows outside every sequence are not written.  Returns 0, or -1 on bad
+ * arguments (offsets not non-decreasing within [0, total]) or allocation
+ * failure.
+ */
+static void gather_rows(const uint16_t *src, long stride, long rows, long d,
+                        double *dst, int is_bf16) {
+    for (long r = 0; r < rows; ++r)
+        widen_slice(src + r * stride, dst + r * d, d, is_bf16);
+}
+
+int attn_ref_varlen_u16(const uint16_t *q, const uint16_t *k,
+                        const uint16_t *v, int is_bf16, const long *cu,
+                        long batch, long total, long H, long H_kv, long d,
+                        double scale, int causal, long wl, long wr, double *o,
+                        double *lse, int nthreads) {
+    if (!q || !k || !v || !cu || !o || !lse || batch < 0 || total < 0 ||
+        H <= 0 || H_kv <= 0 || H % H_kv != 0 || d <= 0)
+        return -1;
+    long longest = 0;
+    for (long b = 0; b < batch; ++b) {
+        if (cu[b] < 0 || cu[b + 1] < cu[b] || cu[b + 1] > total) return -1;
+        if (cu[b + 1] - cu[b] > longest) longest = cu[b + 1] - cu[b];
+    }
+    set_threads(nthreads);
+    long group = H / H_kv, cap = longest > 0 ? longest : 1;
+    double *qd = (double *)malloc(sizeof(double) * (size_t)(cap * d));
+    double *kd = (double *)malloc(sizeof(double) * (size_t)(cap * d));
+    double *vd = (double *)malloc(sizeof(double) * (size_t)(cap * d));
+    if (!qd || !kd || !vd) { free(qd); free(kd); free(vd); return -1; }
+    int rc = 0;
+    for (long b = 0; b < batch && rc == 0; ++b) {
+        long s0 = cu[b], n = cu[b + 1] - cu[b];
+        if (n == 0) continue;
+        for (long h = 0; h < H && rc == 0; ++h) {
+            long hk = h / group;
+            gather_rows(q + (s0 * H + h) * d, H * d, n, d, qd, is_bf16);
+            gather_rows(k + (s0 * H_kv + hk) * d, H_kv * d, n, d, kd, is_bf16);
+            gather_rows(v + (s0 * H_kv + hk) * d, H_kv * d, n, d, vd, is_bf16);
+#pragma omp parallel
+            {
+                double *scores = (double *)malloc(sizeof(double) * (size_t)n);
+                if (!scores) {
+#pragma omp atomic write
+                    rc = -1;
+                } else {
+#pragma omp for schedule(dynamic, 4)
+                    for (long i = 0; i < n; ++i) {
+                        long j0, j1;
+                        key_range(n, i, causal, wl, wr, &j0, &j1);
+                        attend_range(qd + i * d, kd, vd, d, j0, j1, scale, scores,
+                                     o + ((s0 + i) * H + h) * d,
+                                     lse + h * total + s0 + i);
+                    }
+                    free(scores);
+                }
+            }
+        }
+    }
+    free(qd); free(kd); free(vd);
     return rc;
 }

@@ -363,3 +363,116 @@ def test_grouped_heads_equal_repeated_heads():
         for t, (b, h, i) in enumerate(rows):
             np.testing.assert_array_equal(o_r[t], o[b, h, i])
             assert l_r[t] == lse[b, h, i]
+
+
+# ------------------------------------------------- variable-length batches
+def _pack(t):
+    """[B, H, N, d] -> [B*N, H, d] (sequences of equal length, packed)."""
+    B, H, N, d = t.shape
+    return t.permute(0, 2, 1, 3).reshape(B * N, H, d).contiguous()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("window", [(-1, -1), (5, 3), (0, -1)])
+def test_varlen_equal_lengths_is_the_batched_definition(causal, window):
+    """Equal-length sequences packed along the rows give the [B,H,N,d] result."""
+    q, _, _ = make_random_qkv(3, 4, 29, 16, torch.bfloat16, seed=400)
+    _, k, v = make_random_qkv(3, 2, 29, 16, torch.bfloat16, seed=401)
+    o, lse = oracle.attention_ex(q, k, v, 0.3, causal, *window)
+    cu = [0, 29, 58, 87]
+    o_v, l_v = oracle.attention_varlen(_pack(q), _pack(k), _pack(v), cu, 0.3, causal, *window)
+    np.testing.assert_array_equal(o_v, o.transpose(0, 2, 1, 3).reshape(87, 4, 16))
+    np.testing.assert_array_equal(l_v, lse.transpose(1, 0, 2).reshape(4, 87))
+
+
+def _sdpa_rows(qs, ks, vs, scale, causal, window):
+    """torch float64 attention of one sequence ([n, H, d] slices) with an
+    explicit boolean mask built from the window's definition."""
+    n, H, _ = qs.shape
+    group = H // ks.shape[1]
+    i = torch.arange(n)[:, None]
+    j = torch.arange(n)[None, :]
+    allowed = torch.ones(n, n, dtype=torch.bool)
+    if causal:
+        allowed &= j <= i
+    if window[0] >= 0:
+        allowed &= j >= i - window[0]
+    if window[1] >= 0:
+        allowed &= j <= i + window[1]
+    qd = qs.double().permute(1, 0, 2)
+    kd = ks.double().repeat_interleave(group, 1).permute(1, 0, 2)
+    vd = vs.double().repeat_interleave(group, 1).permute(1, 0, 2)
+    o = torch.nn.functional.scaled_dot_product_attention(
+        qd[None], kd[None], vd[None], attn_mask=allowed, scale=scale)[0]
+    s = scale * qd @ kd.transpose(-1, -2)
+    lse = torch.logsumexp(s.masked_fill(~allowed, float("-inf")), -1)
+    return o.permute(1, 0, 2).numpy(), lse.numpy()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("window", [(-1, -1), (4, 2)])
+def test_varlen_matches_torch_per_sequence(causal, window):
+    """Ragged lengths (with an empty and a one-row sequence) against torch's
+    float64 attention of each sequence on its own; rows after the last
+    sequence stay unwritten."""
+    lens = [5, 0, 17, 1, 33]
+    cu = np.concatenate([[0], np.cumsum(lens)]).tolist()
+    total = cu[-1] + 3
+    q = torch.randn(total, 6, 16, generator=torch.Generator().manual_seed(410)).to(torch.bfloat16)
+    k = torch.randn(total, 3, 16, generator=torch.Generator().manual_seed(411)).to(torch.bfloat16)
+    v = torch.randn(total, 3, 16, generator=torch.Generator().manual_seed(412)).to(torch.bfloat16)
+    o, lse = oracle.attention_varlen(q, k, v, cu, 0.27, causal, *window)
+    for b, n in enumerate(lens):
+        if n == 0:
+            continue
+        s0 = cu[b]
+        o_ref, l_ref = _sdpa_rows(q[s0:s0 + n], k[s0:s0 + n], v[s0:s0 + n], 0.27, causal,
+                                  window)
+        np.testing.assert_allclose(o[s0:s0 + n], o_ref, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse[:, s0:s0 + n], l_ref, rtol=0, atol=1e-12)
+    assert np.isnan(o[cu[-1]:]).all() and np.isnan(lse[:, cu[-1]:]).all()
+
+
+def test_varlen_sequences_are_isolated():
+    """Changing one sequence's tokens leaves every other sequence's rows bit
+    for bit unchanged."""
+    lens = [9, 14, 6]
+    cu = [0, 9, 23, 29]
+    q, k, v = (torch.randn(29, 2, 16, generator=torch.Generator().manual_seed(420 + t))
+               .to(torch.float16) for t in range(3))
+    o, lse = oracle.attention_varlen(q, k, v, cu, 0.25, False)
+    q2, k2, v2 = q.clone(), k.clone(), v.clone()
+    for t in (q2, k2, v2):
+        t[9:23] = -t[9:23] * 2
+    o2, l2 = oracle.attention_varlen(q2, k2, v2, cu, 0.25, False)
+    keep = np.r_[0:9, 23:29]
+    np.testing.assert_array_equal(o2[keep], o[keep])
+    np.testing.assert_array_equal(l2[:, keep], lse[:, keep])
+    assert not np.array_equal(o2[9:23], o[9:23])
+    assert sum(lens) == 29
+
+
+def test_varlen_zero_queries_closed_form():
+    """Q = 0: every admissible key of the row's own sequence weighs the same."""
+    cu = [0, 7, 20]
+    k = torch.randn(20, 1, 16, generator=torch.Generator().manual_seed(430)).to(torch.bfloat16)
+    v = torch.randn(20, 1, 16, generator=torch.Generator().manual_seed(431)).to(torch.bfloat16)
+    q = torch.zeros(20, 2, 16, dtype=torch.bfloat16)
+    o, lse = oracle.attention_varlen(q, k, v, cu, 0.5, True, 3, -1)
+    vd = v.double().numpy()[:, 0]
+    for b in range(2):
+        s0, n = cu[b], cu[b + 1] - cu[b]
+        for i in range(n):
+            lo = max(0, i - 3)
+            for h in range(2):
+                np.testing.assert_allclose(o[s0 + i, h], vd[s0 + lo:s0 + i + 1].mean(0),
+                                           rtol=0, atol=1e-13)
+                np.testing.assert_allclose(lse[h, s0 + i], math.log(i + 1 - lo), rtol=0,
+                                           atol=1e-13)
+
+
+def test_varlen_rejects_malformed_offsets():
+    q = torch.zeros(10, 1, 16, dtype=torch.bfloat16)
+    for cu in ([0, 6, 4], [0, 11], [-1, 5]):
+        with pytest.raises(RuntimeError):
+            oracle.attention_varlen(q, q, q, cu, 0.5, False)

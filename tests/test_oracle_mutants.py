@@ -35,6 +35,15 @@ MUTANTS = {
     "no_max_subtraction": ("sum += exp(scores[j] - m);", "sum += exp(scores[j]);"),
     "unnormalised_output": ("double p = exp(scores[j] - lse);",
                             "double p = exp(scores[j] - m);"),
+    "varlen_kv_head": ("gather_rows(k + (s0 * H_kv + hk) * d",
+                       "gather_rows(k + (s0 * H_kv + h % H_kv) * d"),
+    "varlen_row_stride": ("gather_rows(q + (s0 * H + h) * d, H * d,",
+                          "gather_rows(q + (s0 * H + h) * d, d,"),
+    "varlen_lse_layout": ("lse + h * total + s0 + i", "lse + (s0 + i) * H + h"),
+    "varlen_global_positions": ("key_range(n, i, causal, wl, wr, &j0, &j1);\n"
+                                "                        attend_range(qd + i * d, kd, vd, d, j0, j1",
+                                "key_range(n, i + s0 < n ? i + s0 : n - 1, causal, wl, wr, &j0, &j1);\n"
+                                "                        attend_range(qd + i * d, kd, vd, d, j0, j1"),
     "bf16_decoder_shift": ("uint32_t bits = (uint32_t)b << 16;",
                            "uint32_t bits = (uint32_t)b << 15;"),
     "half_decoder_bias": ("expo - 25", "expo - 24"),
@@ -57,6 +66,10 @@ PIN_CALLS = [
     (pins.test_window_matches_sdpa_mask, dict(causal=False)),
     (pins.test_window_closed_forms, {}),
     (pins.test_grouped_heads_equal_repeated_heads, {}),
+    (pins.test_varlen_equal_lengths_is_the_batched_definition,
+     dict(causal=True, window=(5, 3))),
+    (pins.test_varlen_matches_torch_per_sequence, dict(causal=True, window=(4, 2))),
+    (pins.test_varlen_zero_queries_closed_form, {}),
 ]
 
 
