@@ -39,6 +39,8 @@ _ull = ctypes.c_ulonglong
 SIGNATURES = {
     "fa_fwd": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _vp], _i),
     "fa_fwd_ext": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _i, _i, _vp], _i),
+    "fa_fwd_varlen": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _i, _i,
+                       _vp], _i),
     "fa_fwd_splitkv": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _i, _i, _i,
                         _vp, _ull, _vp], _i),
     "fa_splitkv_workspace_bytes": ([_i, _i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(_ull)], _i),
@@ -100,6 +102,15 @@ def fa_fwd_ext(q: int, k: int, v: int, o: int, lse: int | None, B: int, H: int, 
                window_right: int, dtype: int, stream: int | None) -> int:
     return int(_lib.fa_fwd_ext(q, k, v, o, lse or None, B, H, H_kv, N, d, scale, causal,
                                window_left, window_right, dtype, stream or None))
+
+
+def fa_fwd_varlen(q: int, k: int, v: int, o: int, lse: int | None, cu_seqlens: int,
+                  batch: int, max_seqlen: int, total: int, H: int, H_kv: int, d: int,
+                  scale: float, causal: int, window_left: int, window_right: int, dtype: int,
+                  stream: int | None) -> int:
+    return int(_lib.fa_fwd_varlen(q, k, v, o, lse or None, cu_seqlens or None, batch,
+                                  max_seqlen, total, H, H_kv, d, scale, causal, window_left,
+                                  window_right, dtype, stream or None))
 
 
 def fa_fwd_splitkv(q: int, k: int, v: int, o: int, lse: int | None, B: int, H: int,
@@ -220,6 +231,51 @@ def fwd(q, k, v, *, scale: float | None = None, causal: bool = False,
     return out, (lse if return_lse else None)
 
 
+def fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int, *, scale: float | None = None,
+               causal: bool = False, window: tuple[int, int] = (-1, -1), out=None, lse=None,
+               return_lse: bool = True, stream=None):
+    """Attention forward over sequences packed along the rows.
+
+    q is [total, H, d] and k, v are [total, H_kv, d] CUDA tensors; sequence b
+    is rows cu_seqlens[b] .. cu_seqlens[b+1]-1 (``cu_seqlens``: int32 CUDA
+    tensor of batch + 1 offsets; ``max_seqlen``: the longest length).
+    Returns ``(o, lse)`` with o [total, H, d] and lse float32 [H, total].
+    """
+    import torch
+    if q.dim() != 3 or k.dim() != 3 or v.shape != k.shape:
+        raise ValueError("q must be [total, H, d] and k, v one [total, H_kv, d] shape")
+    if (k.shape[0], k.shape[2]) != (q.shape[0], q.shape[2]):
+        raise ValueError("k, v must match q in total and d")
+    if not (q.is_cuda and k.is_cuda and v.is_cuda and cu_seqlens.is_cuda):
+        raise ValueError("q, k, v, cu_seqlens must be CUDA tensors (no CPU path)")
+    if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or not cu_seqlens.is_contiguous():
+        raise ValueError("cu_seqlens must be a contiguous 1-D int32 tensor")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k, v must share one dtype")
+    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("q, k, v must be contiguous")
+    total, H, d = (int(x) for x in q.shape)
+    batch = int(cu_seqlens.numel()) - 1
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if return_lse and lse is None:
+        lse = torch.empty((H, total), dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    with torch.cuda.device(q.device):
+        st = fa_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                           lse.data_ptr() if (return_lse and lse is not None) else None,
+                           cu_seqlens.data_ptr(), max(batch, 0), int(max_seqlen), total, H,
+                           int(k.shape[1]), d, float(scale), int(bool(causal)),
+                           int(window[0]), int(window[1]), _dtype_code(q), handle)
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_varlen")
+    return out, (lse if return_lse else None)
+
+
 def fwd_splitkv(q, k, v, *, num_splits: int = 0, scale: float | None = None,
                 causal: bool = False, window: tuple[int, int] = (-1, -1), out=None,
                 lse=None, return_lse: bool = True, workspace=None, stream=None):
@@ -256,7 +312,8 @@ def fwd_splitkv(q, k, v, *, num_splits: int = 0, scale: float | None = None,
 
 
 __all__ = [
-    "LIB_PATH", "SIGNATURES", "FaError", "fwd", "fwd_splitkv", "fa_fwd", "fa_fwd_ext",
+    "LIB_PATH", "SIGNATURES", "FaError", "fwd", "fwd_varlen", "fwd_splitkv", "fa_fwd",
+    "fa_fwd_ext", "fa_fwd_varlen",
     "fa_fwd_splitkv", "fa_splitkv_workspace_bytes", "fa_fwd_splitkv_noalloc",
     "fa_status_string",
     "fa_get_device_status", "fa_set_wait_timeout_us", "fa_set_max_ctas",

@@ -117,6 +117,29 @@ bool encode_qkvo_map(CUtensorMap* map, const void* base, int N, int d, int bh, b
   return r == CUDA_SUCCESS;
 }
 
+// 4-D view of a packed [rows][heads][d] 16-bit tensor (variable-length
+// batches): dim0 = 64 elements, dim1 = rows (stride heads*d*2 B), dim2 = d/64
+// column blocks (stride 128 B), dim3 = heads (stride d*2 B).  The same box
+// {64, rows, blocks, 1} lands in shared memory in the same [blocks][rows][64]
+// order as the [B][H][N][d] view above.
+bool encode_packed_map(CUtensorMap* map, const void* base, int rows, int heads, int d,
+                       bool bf16, int box_rows, int box_blocks) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[4] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(d / 64),
+                        static_cast<cuuint64_t>(heads)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(heads) * static_cast<cuuint64_t>(d) * 2,
+                           128, static_cast<cuuint64_t>(d) * 2};
+  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_rows),
+                       static_cast<cuuint32_t>(box_blocks), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                  4, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool aligned(const void* ptr, uintptr_t a) {
   return (reinterpret_cast<uintptr_t>(ptr) % a) == 0;
 }
@@ -181,6 +204,10 @@ struct ForwardCall {
   float scale;
   int causal, window_left, window_right, dtype;
   void* stream;
+  // variable-length batches: B sequences packed along the rows, N = the
+  // longest; nullptr / 0 for the [B][H][N][d] layout
+  const int* cu_seqlens;
+  int total;
 };
 
 int validate(const ForwardCall& c) {
@@ -237,11 +264,22 @@ int launch_forward(const ForwardCall& c, void* o_out, float* lse_out, int num_sp
   // d = 256 streams 64-key K/V tiles and stores O in two 128-column halves
   const int kv_rows = kv_tile_rows(d);
   const int o_blocks = (d == 256) ? 2 : d / 64;
-  if (!encode_qkvo_map(&p.tm_q, c.q, N, d, ibh, bf16, kBlockM, d / 64) ||
-      !encode_qkvo_map(&p.tm_k, c.k, N, d, ibh_kv, bf16, kv_rows, d / 64) ||
-      !encode_qkvo_map(&p.tm_v, c.v, N, d, ibh_kv, bf16, kv_rows, d / 64) ||
-      !encode_qkvo_map(&p.tm_o, o_out, N, d, ibh * num_splits, bf16, kBlockM, o_blocks))
+  const bool packed = c.cu_seqlens != nullptr;
+  if (packed) {
+    if (!encode_packed_map(&p.tm_q, c.q, c.total, c.H, d, bf16, kBlockM, d / 64) ||
+        !encode_packed_map(&p.tm_k, c.k, c.total, c.H_kv, d, bf16, kv_rows, d / 64) ||
+        !encode_packed_map(&p.tm_v, c.v, c.total, c.H_kv, d, bf16, kv_rows, d / 64) ||
+        !encode_packed_map(&p.tm_o, o_out, c.total, c.H, d, bf16, kBlockM, o_blocks))
+      return FA_ERR_CUDA;
+  } else if (!encode_qkvo_map(&p.tm_q, c.q, N, d, ibh, bf16, kBlockM, d / 64) ||
+             !encode_qkvo_map(&p.tm_k, c.k, N, d, ibh_kv, bf16, kv_rows, d / 64) ||
+             !encode_qkvo_map(&p.tm_v, c.v, N, d, ibh_kv, bf16, kv_rows, d / 64) ||
+             !encode_qkvo_map(&p.tm_o, o_out, N, d, ibh * num_splits, bf16, kBlockM, o_blocks)) {
     return FA_ERR_CUDA;
+  }
+  p.cu_seqlens = c.cu_seqlens;
+  p.total_rows = packed ? c.total : 0;
+  p.o_ptr = static_cast<uint16_t*>(o_out);
   p.lse = lse_out;
   p.status = info->status;
   p.timeout_ns = g_timeout_ns.load();
@@ -265,7 +303,7 @@ int launch_forward(const ForwardCall& c, void* o_out, float* lse_out, int num_sp
   const int cap = g_max_ctas.load();
   if (cap > 0 && cap < grid) grid = cap;
   p.num_pair_units = p.num_units;
-  if (d != 256 && num_splits == 1) {
+  if (d != 256 && num_splits == 1 && !packed) {
     // Balance the last wave: its L pair units become 2L single-tile units
     // when those fit in one wave.
     const long long pair_units = bh * pairs;
@@ -553,6 +591,25 @@ int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
   if (scratch == nullptr || rc != cudaSuccess) return FA_ERR_CUDA;
   // the count is passed explicitly, so it resolves to `splits` again
   return splitkv_forward(c, splits, scratch, limit);
+}
+
+int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                  const int* cu_seqlens, int batch, int max_seqlen, int total, int H, int H_kv,
+                  int d, float scale, int causal, int window_left, int window_right, int dtype,
+                  void* stream) {
+  using namespace fa;
+  // B = batch and N = max_seqlen in the shared checks
+  const ForwardCall c{q, k, v, o, lse, batch, H, H_kv, max_seqlen, d, scale, causal,
+                      window_left, window_right, dtype, stream, cu_seqlens, total};
+  if (total < 0) return FA_ERR_INVALID_ARG;
+  int st = validate(c);
+  if (st != FA_OK) return st;
+  if (empty_problem(c) || total == 0) return FA_OK;
+  st = check_pointers(c);
+  if (st != FA_OK) return st;
+  if (cu_seqlens == nullptr) return FA_ERR_INVALID_ARG;
+  if (!aligned(cu_seqlens, 4)) return FA_ERR_MISALIGNED;
+  return launch_forward(c, o, lse, 1, 0);
 }
 
 int fa_get_device_status(void* stream, int* site) {

@@ -8,7 +8,7 @@ namespace {
 template <bool CAUSAL, bool BF16>
 cudaError_t launch_one(const FaParams& p, int grid, cudaStream_t stream) {
   constexpr int kSmem = Layout<128>::kSmemBytes;
-  auto kernel = fa_fwd_kernel<128, CAUSAL, BF16>;
+  auto kernel = fa_fwd_kernel<128, CAUSAL, BF16, false>;
   cudaError_t e =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
@@ -19,7 +19,8 @@ cudaError_t launch_one(const FaParams& p, int grid, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_fwd_d128(const FaParams& p, bool causal, bool bf16, int grid,
-                           cudaStream_t stream) {
+                            cudaStream_t stream) {
+  if (p.cu_seqlens != nullptr) return launch_fwd_d128_packed(p, causal, bf16, grid, stream);
   if (causal) return bf16 ? launch_one<true, true>(p, grid, stream)
                           : launch_one<true, false>(p, grid, stream);
   return bf16 ? launch_one<false, true>(p, grid, stream)

@@ -1,0 +1,29 @@
+// fa_fwd_d128_packed.cu -- instantiations and launcher of the forward kernel, head dim 128 (packed variable-length batches).
+#include "fa_fwd_kernel.cuh"
+#include "fa_launch.h"
+
+namespace fa {
+namespace {
+
+template <bool CAUSAL, bool BF16>
+cudaError_t launch_one(const FaParams& p, int grid, cudaStream_t stream) {
+  constexpr int kSmem = Layout<128>::kSmemBytes;
+  auto kernel = fa_fwd_kernel<128, CAUSAL, BF16, true>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
+  kernel<<<grid, kNumThreads, kSmem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_d128_packed(const FaParams& p, bool causal, bool bf16, int grid,
+                                   cudaStream_t stream) {
+  if (causal) return bf16 ? launch_one<true, true>(p, grid, stream)
+                          : launch_one<true, false>(p, grid, stream);
+  return bf16 ? launch_one<false, true>(p, grid, stream)
+              : launch_one<false, false>(p, grid, stream);
+}
+
+}  // namespace fa

@@ -78,14 +78,13 @@ constexpr uint32_t kOCol = 256;
 
 struct Unit {
   int bh;     // query head
-  int bh_kv;  // K/V head it reads
-  int bh_out; // output head (bh, or the split's partial-output head)
-  int row0;   // first query row of the tile
+  SeqView sv; // its rows and tensor-map heads
+  int row0;   // first query row of the tile (within the sequence)
   int n0, n1; // K/V tiles visited: [n0, n1); empty only for a key split
               // that the tile's rows cannot see
 };
 
-template <bool CAUSAL>
+template <bool CAUSAL, bool PACKED>
 __device__ __forceinline__ Unit decode_unit(int u, const FaParams& p) {
   Unit w;
   int split = 0;
@@ -101,10 +100,20 @@ __device__ __forceinline__ Unit decode_unit(int u, const FaParams& p) {
     w.bh = u / p.num_pairs;
     qt = u % p.num_pairs;
   }
+  w.sv = seq_view<PACKED>(p, w.bh, split * p.num_bh + w.bh);
+  const int len = w.sv.len;
+  if (PACKED && CAUSAL) {
+    // sequences differ in length: count the tiles from each sequence's end,
+    // so that every sequence's heaviest (last) tiles come first
+    qt = (len + kBlockM - 1) / kBlockM - 1 - (p.num_pairs - 1 - qt);
+    if (qt < 0) qt = p.num_pairs;  // no such tile: an empty unit
+  }
   w.row0 = qt * kBlockM;
-  w.bh_kv = kv_head(w.bh, p.H, p.group);
-  w.bh_out = split * p.num_bh + w.bh;
-  key_tile_range(w.row0, min(p.N, w.row0 + kBlockM), p.N, p.win_left, p.win_right, kBN,
+  if (w.row0 >= len) {
+    w.n0 = w.n1 = 0;  // past the end of a shorter packed sequence
+    return w;
+  }
+  key_tile_range(w.row0, min(len, w.row0 + kBlockM), len, p.win_left, p.win_right, kBN,
                  &w.n0, &w.n1);
   if (p.num_splits > 1) clip_to_split(split, p.split_tiles, &w.n0, &w.n1);
   return w;
@@ -114,7 +123,7 @@ __device__ __forceinline__ Unit decode_unit(int u, const FaParams& p) {
 
 // p.num_pairs holds the number of 128-row query tiles per (b,h) and
 // p.n_ktiles the number of 64-key tiles for this kernel.
-template <bool CAUSAL, bool BF16>
+template <bool CAUSAL, bool BF16, bool PACKED>
 __global__ void __launch_bounds__(d256::kThreads, 1)
     fa_fwd_d256_kernel(const __grid_constant__ FaParams p) {
   using namespace d256;
@@ -170,12 +179,13 @@ __global__ void __launch_bounds__(d256::kThreads, 1)
       uint32_t slot = 0, phase = 0, q_it = 0, issued = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
-        const Unit w = decode_unit<CAUSAL>(u, p);
+        const Unit w = decode_unit<CAUSAL, PACKED>(u, p);
         if (w.n1 == w.n0) continue;
         ok = wait_bar(bar(kQEmpty), (q_it & 1u) ^ 1u, ctl, kSiteProducerQ);
         if (!ok) break;
         mbar_arrive_expect_tx(bar(kQFull), kQBytes);
-        tma_load_4d(sbase + kQOff, &p.tm_q, bar(kQFull), 0, w.row0, 0, w.bh);
+        tma_load_4d(sbase + kQOff, &p.tm_q, bar(kQFull), 0, w.sv.row_base + w.row0, 0,
+                    w.sv.q_head);
         ++q_it;
         for (int n = w.n0; n < w.n1 && ok; ++n) {
           for (int kv = 0; kv < 2; ++kv) {
@@ -183,7 +193,7 @@ __global__ void __launch_bounds__(d256::kThreads, 1)
             if (!ok) break;
             mbar_arrive_expect_tx(bar(kKVFull + slot), kKVBytes);
             tma_load_4d(sbase + kKVOff + slot * kKVBytes, kv ? &p.tm_v : &p.tm_k,
-                        bar(kKVFull + slot), 0, n * kBN, 0, w.bh_kv);
+                        bar(kKVFull + slot), 0, w.sv.row_base + n * kBN, 0, w.sv.kv_head);
             ++issued;
             if (++slot == (uint32_t)kStages) { slot = 0; phase ^= 1u; }
           }
@@ -214,10 +224,10 @@ __global__ void __launch_bounds__(d256::kThreads, 1)
       bool pv_pending = false, pv_acc = false;
       uint32_t pv_vslot = 0, pv_vphase = 0;
       int u = blockIdx.x;
-      Unit w = decode_unit<CAUSAL>(u < p.num_units ? u : 0, p);
+      Unit w = decode_unit<CAUSAL, PACKED>(u < p.num_units ? u : 0, p);
       while (u < p.num_units && w.n1 == w.n0) {  // empty key split: nothing to do
         u += gridDim.x;
-        if (u < p.num_units) w = decode_unit<CAUSAL>(u, p);
+        if (u < p.num_units) w = decode_unit<CAUSAL, PACKED>(u, p);
       }
       int n = w.n0;
       while (ok) {
@@ -270,7 +280,7 @@ __global__ void __launch_bounds__(d256::kThreads, 1)
         if (++n == w.n1) {
           do {
             u += gridDim.x;
-            if (u < p.num_units) w = decode_unit<CAUSAL>(u, p);
+            if (u < p.num_units) w = decode_unit<CAUSAL, PACKED>(u, p);
           } while (u < p.num_units && w.n1 == w.n0);
           n = w.n0;
         }
@@ -290,11 +300,12 @@ __global__ void __launch_bounds__(d256::kThreads, 1)
     bool ok = true;
 
     for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
-      const Unit w = decode_unit<CAUSAL>(u, p);
+      const Unit w = decode_unit<CAUSAL, PACKED>(u, p);
       if (w.n1 == w.n0) continue;
       const int row = w.row0 + t;
       float m_ref = -INFINITY, l = 0.f;
-      const int row_end = min(p.N, w.row0 + kBlockM);
+      const int len = w.sv.len;
+      const int row_end = min(len, w.row0 + kBlockM);
       for (int n = w.n0; n < w.n1; ++n, ++G) {
         const uint32_t b = G % kSBufs;
         const uint32_t tS = tmem + lane_base + b * kBN;
@@ -314,11 +325,11 @@ __global__ void __launch_bounds__(d256::kThreads, 1)
         }
         // keys row - win_left .. row + win_right, below N
         const int kbase = n * kBN;
-        const bool need_mask = (kbase + kBN > p.N) ||
+        const bool need_mask = (kbase + kBN > len) ||
                                (kbase + kBN - 1 > w.row0 + p.win_right) ||
                                (kbase < row_end - 1 - p.win_left);
         if (need_mask) {
-          const int hi = min(p.N - kbase, row + p.win_right + 1 - kbase);  // c < hi
+          const int hi = min(len - kbase, row + p.win_right + 1 - kbase);  // c < hi
           const int lo = row - p.win_left - kbase;                         // c >= lo
 #pragma unroll
           for (int c = 0; c < kBN; ++c)
@@ -426,33 +437,48 @@ __global__ void __launch_bounds__(d256::kThreads, 1)
         fence_proxy_async_smem();
         mbar_arrive(bar(kStageFull));
       }
-      if (p.lse != nullptr && row < p.N) {
-        p.lse[static_cast<size_t>(w.bh_out) * p.N + row] =
+      if (p.lse != nullptr && row < len) {
+        p.lse[lse_base<PACKED>(p, w.sv) + row] =
             (l > 0.f) ? (m_ref + log2f(l)) * 0.6931471805599453f : -INFINITY;
       }
     }
     __syncwarp();
   } else if (warp == kStoreWarp) {
     // ------------------------------------------------------------ O store
-    if (lane == 0) {
-      uint32_t full_par = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
-        const Unit w = decode_unit<CAUSAL>(u, p);
-        if (w.n1 == w.n0) continue;
-        for (int half = 0; half < 2 && ok; ++half) {
-          ok = wait_bar(bar(kStageFull), full_par, ctl, kSiteStore);
-          full_par ^= 1u;
-          if (!ok) break;
+    // Lane 0 waits and issues the TMA stores; the last query tile of a
+    // packed sequence, whose 128-row box would run into the next sequence's
+    // rows, is copied row by row by the whole warp instead.
+    uint32_t full_par = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+      const Unit w = decode_unit<CAUSAL, PACKED>(u, p);
+      if (w.n1 == w.n0) continue;
+      const int rows = w.sv.len - w.row0;
+      for (int half = 0; half < 2 && ok; ++half) {
+        if (lane == 0) ok = wait_bar(bar(kStageFull), full_par, ctl, kSiteStore);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        full_par ^= 1u;
+        if (!ok) break;
+        if (PACKED && rows < kBlockM) {
+          const long long row_stride = static_cast<long long>(p.H) * 256;
+          uint16_t* dst = p.o_ptr + (static_cast<long long>(w.sv.row_base) + w.row0) *
+                                        row_stride + static_cast<long long>(w.sv.o_head) * 256 +
+                          half * 128;
+          copy_staged_rows(sbase + kStageOff, rows, 16, dst, row_stride, lane);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kStageEmpty));
+        } else if (lane == 0) {
           // columns [128*half, 128*half + 128) = d blocks 2*half, 2*half + 1
-          tma_store_4d(&p.tm_o, sbase + kStageOff, 0, w.row0, 2 * half, w.bh_out);
+          tma_store_4d(&p.tm_o, sbase + kStageOff, 0, w.sv.row_base + w.row0, 2 * half,
+                       w.sv.o_head);
           bulk_commit_group();
           bulk_wait_read_all();
           mbar_arrive(bar(kStageEmpty));
         }
+        __syncwarp();
       }
-      bulk_wait_all();
     }
+    if (lane == 0) bulk_wait_all();
     __syncwarp();
   }
 

@@ -119,9 +119,8 @@ struct Layout {
 // streams K/V tiles [n_beg, n_end), the union of the two ranges.
 struct Unit {
   int bh;       // query head (b*H + h)
-  int bh_kv;    // K/V head it reads
-  int bh_out;   // output head (bh, or the split's partial-output head)
-  int row0[2];  // first query row of each tile
+  SeqView sv;   // its rows and tensor-map heads
+  int row0[2];  // first query row of each tile (within the sequence)
   int n0[2], n1[2];
   int n_beg, n_end;
 };
@@ -130,7 +129,7 @@ struct Unit {
 // fill the last wave of CTAs evenly, the pairs of that partial wave are split
 // instead into single-tile units (tile 0 only), one per CTA, which halves
 // the length of the last wave.
-template <bool CAUSAL>
+template <bool CAUSAL, bool PACKED>
 __device__ __forceinline__ Unit decode_unit(int u, const FaParams& p) {
   Unit w;
   int split = 0;
@@ -154,8 +153,14 @@ __device__ __forceinline__ Unit decode_unit(int u, const FaParams& p) {
     w.bh = pu / p.num_pairs;
     pair = pu % p.num_pairs;
   }
-  w.bh_kv = kv_head(w.bh, p.H, p.group);
-  w.bh_out = split * p.num_bh + w.bh;
+  w.sv = seq_view<PACKED>(p, w.bh, split * p.num_bh + w.bh);
+  const int len = w.sv.len;
+  if (PACKED && CAUSAL) {
+    // sequences differ in length: count the pairs from each sequence's end,
+    // so that every sequence's heaviest (last) pairs come first
+    pair = (len + kRowsPerUnit - 1) / kRowsPerUnit - 1 - (p.num_pairs - 1 - pair);
+    if (pair < 0) pair = p.num_pairs;  // no such pair: an empty unit
+  }
   w.n_beg = 0x7fffffff;
   w.n_end = 0;
 #pragma unroll
@@ -164,10 +169,10 @@ __device__ __forceinline__ Unit decode_unit(int u, const FaParams& p) {
     const int r0 = (single < 0) ? pair * kRowsPerUnit + g * kBlockM
                                 : pair * kRowsPerUnit + single * kBlockM;
     w.row0[g] = r0;
-    if (r0 >= p.N || (single >= 0 && g == 1)) {
+    if (r0 >= len || (single >= 0 && g == 1)) {
       w.n0[g] = w.n1[g] = 0;
     } else {
-      key_tile_range(r0, min(p.N, r0 + kBlockM), p.N, p.win_left, p.win_right, kBlockN,
+      key_tile_range(r0, min(len, r0 + kBlockM), len, p.win_left, p.win_right, kBlockN,
                      &w.n0[g], &w.n1[g]);
       if (p.num_splits > 1) clip_to_split(split, p.split_tiles, &w.n0[g], &w.n1[g]);
     }
@@ -226,7 +231,7 @@ __device__ __forceinline__ float exp_tile_to_tmem(const float (&s)[kBlockN], flo
   return a0 + a1;
 }
 
-template <int D, bool CAUSAL, bool BF16>
+template <int D, bool CAUSAL, bool BF16, bool PACKED>
 __global__ void __launch_bounds__(kNumThreads, 1)
     fa_fwd_kernel(const __grid_constant__ FaParams p) {
   using L = Layout<D>;
@@ -283,14 +288,14 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       uint32_t kv_it = 0, q_it[2] = {0, 0};
       bool ok = true;
       for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
-        const Unit w = decode_unit<CAUSAL>(u, p);
+        const Unit w = decode_unit<CAUSAL, PACKED>(u, p);
         for (int g = 0; g < 2 && ok; ++g) {
           if (w.n1[g] == w.n0[g]) continue;
           ok = wait_bar(bar(L::kQEmpty + g), (q_it[g] & 1u) ^ 1u, ctl, kSiteProducerQ);
           if (!ok) break;
           mbar_arrive_expect_tx(bar(L::kQFull + g), L::kTileBytes);
           tma_load_4d(sbase + L::kQOff + g * L::kTileBytes, &p.tm_q, bar(L::kQFull + g), 0,
-                      w.row0[g], 0, w.bh);
+                      w.sv.row_base + w.row0[g], 0, w.sv.q_head);
           ++q_it[g];
         }
         for (int n = w.n_beg; n < w.n_end && ok; ++n) {
@@ -310,7 +315,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             if (!ok) break;
             mbar_arrive_expect_tx(bar(L::kKVFull + slot), L::kTileBytes);
             tma_load_4d(sbase + L::kKVOff + slot * L::kTileBytes, kv ? &p.tm_v : &p.tm_k,
-                        bar(L::kKVFull + slot), 0, n * kBlockN, 0, w.bh_kv);
+                        bar(L::kKVFull + slot), 0, w.sv.row_base + n * kBlockN, 0,
+                        w.sv.kv_head);
             ++kv_it;
           }
         }
@@ -350,11 +356,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       bool prev_active[2] = {false, false}, prev_acc[2] = {false, false};
       uint32_t prev_vslot = 0;
       int u = blockIdx.x;
-      Unit w = decode_unit<CAUSAL>(u < p.num_units ? u : 0, p);
+      Unit w = decode_unit<CAUSAL, PACKED>(u < p.num_units ? u : 0, p);
       // units without K/V tiles (a split-off tile past N) stream nothing
       while (u < p.num_units && w.n_end == w.n_beg) {
         u += gridDim.x;
-        if (u < p.num_units) w = decode_unit<CAUSAL>(u, p);
+        if (u < p.num_units) w = decode_unit<CAUSAL, PACKED>(u, p);
       }
       int n = w.n_beg;
       while (ok) {
@@ -423,7 +429,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         if (++n == w.n_end) {
           do {
             u += gridDim.x;
-            if (u < p.num_units) w = decode_unit<CAUSAL>(u, p);
+            if (u < p.num_units) w = decode_unit<CAUSAL, PACKED>(u, p);
           } while (u < p.num_units && w.n_end == w.n_beg);
           n = w.n_beg;
         }
@@ -448,18 +454,23 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     bool ok = true;
 
     for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
-      const Unit w = decode_unit<CAUSAL>(u, p);
+      const Unit w = decode_unit<CAUSAL, PACKED>(u, p);
       // the staging tile is used by tile 0 then tile 1 of each unit
       const bool valid0 = w.n1[0] > w.n0[0], valid1 = w.n1[1] > w.n0[1];
       const uint32_t my_store = n_stores + ((g == 1 && valid0) ? 1u : 0u);
       n_stores += (valid0 ? 1u : 0u) + (valid1 ? 1u : 0u);
-      if (w.n1[g] == w.n0[g]) continue;
-      const int row = w.row0[g] + t;
+      // this warpgroup's tile (g is per warp: selects, not indexed loads)
+      const int t_n0 = g ? w.n0[1] : w.n0[0];
+      const int t_n1 = g ? w.n1[1] : w.n1[0];
+      const int t_row0 = g ? w.row0[1] : w.row0[0];
+      if (t_n1 == t_n0) continue;
+      const int row = t_row0 + t;
       float m_ref = -INFINITY;  // reference maximum (log2 units, scaled)
       float l = 0.f;            // running row sum relative to m_ref
 
-      const int row_end = min(p.N, w.row0[g] + kBlockM);
-      for (int n = w.n0[g]; n < w.n1[g]; ++n) {
+      const int len = w.sv.len;
+      const int row_end = min(len, t_row0 + kBlockM);
+      for (int n = t_n0; n < t_n1; ++n) {
         ok = wait_bar(bar(L::kSFull + g), s_par, ctl, kSiteSoftmaxS);
         s_par ^= 1u;
         ok = __all_sync(0xffffffffu, ok);
@@ -474,11 +485,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
         // keys row - win_left .. row + win_right, below N
         const int kbase = n * kBlockN;
-        const bool need_mask = (kbase + kBlockN > p.N) ||
-                               (kbase + kBlockN - 1 > w.row0[g] + p.win_right) ||
+        const bool need_mask = (kbase + kBlockN > len) ||
+                               (kbase + kBlockN - 1 > t_row0 + p.win_right) ||
                                (kbase < row_end - 1 - p.win_left);
         if (need_mask) {
-          const int hi = min(p.N - kbase, row + p.win_right + 1 - kbase);  // c < hi
+          const int hi = min(len - kbase, row + p.win_right + 1 - kbase);  // c < hi
           const int lo = row - p.win_left - kbase;                         // c >= lo
 #pragma unroll
           for (int c = 0; c < kBlockN; ++c)
@@ -488,7 +499,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         if (__any_sync(0xffffffffu, m_tile > m_ref + kRescaleThreshold)) {
           const float m_new = fmaxf(m_ref, m_tile);
           const float factor = (m_new == -INFINITY) ? 1.f : ex2_approx(m_ref - m_new);
-          if (n > w.n0[g]) {
+          if (n > t_n0) {
             // O_g holds the previous tiles' sum: wait for the last P_g V MMA,
             // then rescale this warp's 32 rows in tensor memory.
             ok = wait_bar(bar(L::kODone + g), (pv_cnt - 1) & 1u, ctl, kSiteSoftmaxO);
@@ -543,8 +554,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           st_shared_v4(addr, w4[0], w4[1], w4[2], w4[3]);
         }
       }
-      if (p.lse != nullptr && row < p.N) {
-        p.lse[static_cast<size_t>(w.bh_out) * p.N + row] =
+      if (p.lse != nullptr && row < len) {
+        p.lse[lse_base<PACKED>(p, w.sv) + row] =
             (l > 0.f) ? (m_ref + log2f(l)) * 0.6931471805599453f : -INFINITY;
       }
       fence_proxy_async_smem();
@@ -554,24 +565,41 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   } else if (warp == kStoreWarp) {
     regs_decrease<kControlRegs>();
     // ------------------------------------------------------------ O store
-    if (lane == 0) {
-      uint32_t full_par = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
-        const Unit w = decode_unit<CAUSAL>(u, p);
-        for (int g = 0; g < 2 && ok; ++g) {
-          if (w.n1[g] == w.n0[g]) continue;
-          ok = wait_bar(bar(L::kStageFull), full_par, ctl, kSiteStore);
-          full_par ^= 1u;
-          if (!ok) break;
-          tma_store_4d(&p.tm_o, sbase + L::kStageOff, 0, w.row0[g], 0, w.bh_out);
+    // Lane 0 waits and issues the TMA store of each staged tile.  The last
+    // query tile of a packed sequence, whose 128-row box would run into the
+    // next sequence's rows, is copied row by row by the whole warp instead.
+    uint32_t full_par = 0;
+    bool ok = true;
+    // (lanes other than 0 take part only for packed batches)
+    constexpr bool whole_warp = PACKED;
+    for (int u = blockIdx.x; u < p.num_units && ok && (whole_warp || lane == 0);
+         u += gridDim.x) {
+      const Unit w = decode_unit<CAUSAL, PACKED>(u, p);
+      for (int g = 0; g < 2 && ok; ++g) {
+        if (w.n1[g] == w.n0[g]) continue;
+        if (lane == 0) ok = wait_bar(bar(L::kStageFull), full_par, ctl, kSiteStore);
+        if (whole_warp) ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        full_par ^= 1u;
+        if (!ok) break;
+        const int rows = w.sv.len - w.row0[g];
+        if (whole_warp && rows < kBlockM) {
+          const long long row_stride = static_cast<long long>(p.H) * D;
+          uint16_t* dst = p.o_ptr + (static_cast<long long>(w.sv.row_base) + w.row0[g]) *
+                                        row_stride + static_cast<long long>(w.sv.o_head) * D;
+          copy_staged_rows(sbase + L::kStageOff, rows, D / 8, dst, row_stride, lane);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(L::kStageEmpty));
+        } else if (lane == 0) {
+          tma_store_4d(&p.tm_o, sbase + L::kStageOff, 0, w.sv.row_base + w.row0[g], 0,
+                       w.sv.o_head);
           bulk_commit_group();
           bulk_wait_read_all();  // the staging tile may be rewritten
           mbar_arrive(bar(L::kStageEmpty));
         }
+        if (whole_warp) __syncwarp();
       }
-      bulk_wait_all();
     }
+    if (lane == 0) bulk_wait_all();
     __syncwarp();
   } else {
     regs_decrease<kControlRegs>();  // spare warps of the third warpgroup

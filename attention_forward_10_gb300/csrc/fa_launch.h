@@ -18,6 +18,14 @@ cudaError_t launch_fwd_d128(const FaParams& p, bool causal, bool bf16, int grid,
 // Head dim 256: one 128-row query tile per work unit, 64-key K/V tiles.
 cudaError_t launch_fwd_d256(const FaParams& p, bool causal, bool bf16, int grid,
                             cudaStream_t stream);
+// The same for packed variable-length batches (p.cu_seqlens set); the
+// launchers above forward to these.
+cudaError_t launch_fwd_d64_packed(const FaParams& p, bool causal, bool bf16, int grid,
+                                  cudaStream_t stream);
+cudaError_t launch_fwd_d128_packed(const FaParams& p, bool causal, bool bf16, int grid,
+                                   cudaStream_t stream);
+cudaError_t launch_fwd_d256_packed(const FaParams& p, bool causal, bool bf16, int grid,
+                                   cudaStream_t stream);
 
 // Shape of a split-KV merge: num_bh heads of N rows of d columns; split s
 // holds keys [s * split_keys, (s + 1) * split_keys); query i may see keys

@@ -53,6 +53,13 @@ struct FaParams {  // 64-byte aligned through CUtensorMap
   int num_splits;    // key splits per query tile (1: no split)
   int split_tiles;   // K/V tiles per key split
   float scale_log2;  // softmax scale * log2(e)
+  // Variable-length batches (packed rows; nullptr / 0 otherwise): sequence
+  // b holds rows [cu_seqlens[b], cu_seqlens[b+1]) of the packed [rows][H][d]
+  // tensors; N is then the longest sequence and num_bh = batch * H.
+  const int* cu_seqlens;
+  int total_rows;    // rows of the packed tensors
+  uint16_t* o_ptr;   // O (packed rows), for the row-by-row store of the last
+                     // query tile of a sequence
 };
 
 // Split-KV: unit u is split u % num_splits of base unit u / num_splits; the
@@ -65,10 +72,56 @@ __host__ __device__ inline void clip_to_split(int s, int split_tiles, int* n0, i
   if (*n1 < *n0) *n1 = *n0;
 }
 
+// Rows of one (b, h) attention problem: its sequence's first packed row, its
+// length, and the head coordinates of its Q, O and K/V in the tensor maps.
+struct SeqView {
+  int row_base;   // 0, or the sequence's first packed row
+  int len;        // N, or the sequence's length (clamped to the buffers)
+  int q_head;     // head coordinate of Q (bh, or h when packed)
+  int o_head;     // head coordinate of O (out_head, or h when packed)
+  int kv_head;    // head coordinate of K and V
+};
+
 // K/V head of query head bh = b*H + h (grouped heads: h / group).
 __host__ __device__ inline int kv_head(int bh, int H, int group) {
   const int H_kv = H / group;
   return (bh / H) * H_kv + (bh % H) / group;
+}
+
+// Geometry of the (b,h) problem bh; `out_head` is the output head of the
+// non-packed layout (bh, or a split's partial head).  PACKED kernels serve
+// variable-length batches (cu_seqlens set).  For packed batches the
+// offsets are clamped so that a malformed cu_seqlens can only shorten a
+// sequence (to at most N rows), never move a row outside [0, total_rows).
+template <bool PACKED>
+__device__ __forceinline__ SeqView seq_view(const FaParams& p, int bh, int out_head) {
+  SeqView v;
+  if constexpr (!PACKED) {
+    v.row_base = 0;
+    v.len = p.N;
+    v.q_head = bh;
+    v.o_head = out_head;
+    v.kv_head = kv_head(bh, p.H, p.group);
+    return v;
+  }
+  const int b = bh / p.H, h = bh % p.H;
+  int r0 = p.cu_seqlens[b], r1 = p.cu_seqlens[b + 1];
+  r0 = r0 < 0 ? 0 : (r0 > p.total_rows ? p.total_rows : r0);
+  r1 = r1 < r0 ? r0 : (r1 > p.total_rows ? p.total_rows : r1);
+  v.row_base = r0;
+  v.len = (r1 - r0 < p.N) ? r1 - r0 : p.N;
+  v.q_head = h;
+  v.o_head = h;
+  v.kv_head = h / p.group;
+  return v;
+}
+
+// Index in the LSE output of row 0 of the problem seen through `v`:
+// [heads][N] rows, or [H][total_rows] for packed batches.
+template <bool PACKED>
+__device__ __forceinline__ long long lse_base(const FaParams& p, const SeqView& v) {
+  if constexpr (PACKED) return static_cast<long long>(v.o_head) * p.total_rows + v.row_base;
+  return static_cast<long long>(v.o_head) * p.N;
 }
 
 // K/V tiles [n0, n1) of `tile` keys that query rows [r0, r_end) can see.

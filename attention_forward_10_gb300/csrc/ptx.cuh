@@ -147,6 +147,30 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// Copy the first `rows` rows of a staged 128-row output tile to global
+// memory, 16 bytes per lane and step: the tile is [chunks/8 column blocks]
+// [128 rows][128 B] with the 128-byte swizzle (16-byte chunk c of row t at
+// chunk (c ^ t) mod 8 of its block); row t goes to dst + t * row_stride.
+__device__ __forceinline__ void copy_staged_rows(uint32_t stage, int rows, int chunks,
+                                                 uint16_t* dst, long long row_stride,
+                                                 int lane) {
+  for (int idx = lane; idx < rows * chunks; idx += 32) {
+    const int t = idx / chunks, c16 = idx % chunks;
+    const uint32_t addr = stage + (c16 / 8) * (128u * 128u) + t * 128u +
+                          (static_cast<uint32_t>((c16 % 8) ^ (t & 7)) << 4);
+    *reinterpret_cast<uint4*>(dst + t * row_stride + c16 * 8) = ld_shared_v4(addr);
+  }
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b,
                                              uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b),

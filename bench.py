@@ -18,7 +18,8 @@ reported value is all ranks' FLOPs over the slowest rank's time.
 Workload 6 (one causal head of 32768 rows) runs through the split-KV entry
 point with the automatic split count (two launches per step: the split
 forward and the merge); its line adds the unsplit forward's time on the
-same inputs.
+same inputs.  Workload 7 (16 causal sequences of 697..3646 rows packed along
+the rows) runs through the variable-length entry point.
 
 ``--impl reference`` times the fp64 CPU oracle (the only other place this
 script runs it) on rank 0, on bounded row samples of the same workload.
@@ -181,31 +182,48 @@ def _gpu_id_for_smi(torch, dev_index: int):
     return None
 
 
+def _oracle_rows(wl, q, k, v, rows):
+    """The oracle on listed (b, h, i) rows; packed (varlen) workloads are
+    evaluated sequence by sequence on [1, H, n, d] views of each sequence.
+    Returns the FLOPs of the rows (4*d per admissible key)."""
+    import oracle
+    lens = wl.seqlens()
+    if not wl.varlen:
+        oracle.attention_rows(q, k, v, wl.scale, wl.causal, rows)
+    else:
+        cu = wl.cu_seqlens()
+        for b in sorted(set(r[0] for r in rows)):
+            view = lambda t: t[cu[b]:cu[b + 1]].permute(1, 0, 2).unsqueeze(0).contiguous()
+            oracle.attention_rows(view(q), view(k), view(v), wl.scale, wl.causal,
+                                  [(0, h, i) for (bb, h, i) in rows if bb == b])
+    return sum(4.0 * wl.d * ((i + 1) if wl.causal else lens[b]) for (b, _, i) in rows)
+
+
 def _cpu_baseline(wl, budget_s: float = 12.0):
     """Time the fp64 oracle on whole heads of the workload, about `budget_s`."""
     import oracle
     from workloads import make_qkv
     q, k, v = make_qkv(wl)
-    per_row = 4.0 * wl.N * wl.d * (0.5 if wl.causal else 1.0)
+    lens = wl.seqlens()
     # calibrate on 64 rows of head (0,0), then size the sample to the budget
-    probe = [(0, 0, i) for i in range(0, wl.N, max(1, wl.N // 64))][:64]
+    probe = [(0, 0, i) for i in range(0, lens[0], max(1, lens[0] // 64))][:64]
     t0 = time.perf_counter()
-    oracle.attention_rows(q, k, v, wl.scale, wl.causal, probe)
-    rate = len(probe) * per_row / max(time.perf_counter() - t0, 1e-6)
-    n_rows = int(min(wl.B * wl.H * wl.N, max(256, budget_s * rate / per_row)))
-    rows = []
+    probe_flops = _oracle_rows(wl, q, k, v, probe)
+    rate = probe_flops / max(time.perf_counter() - t0, 1e-6)
+    budget_flops = budget_s * rate
+    rows, planned = [], 0.0
     for bh in range(wl.B * wl.H):
         b, h = divmod(bh, wl.H)
-        for i in range(wl.N):
+        for i in range(lens[b]):
             rows.append((b, h, i))
-            if len(rows) >= n_rows:
+            planned += 4.0 * wl.d * ((i + 1) if wl.causal else lens[b])
+            if planned >= budget_flops:
                 break
-        if len(rows) >= n_rows:
+        if planned >= budget_flops:
             break
     t0 = time.perf_counter()
-    oracle.attention_rows(q, k, v, wl.scale, wl.causal, rows)
+    flops = _oracle_rows(wl, q, k, v, rows)
     dt = time.perf_counter() - t0
-    flops = sum(4.0 * wl.d * ((i + 1) if wl.causal else wl.N) for (_, _, i) in rows)
     return {"value": flops / dt / 1e12, "unit": UNIT, "cores": oracle.max_threads(),
             "kind": "oracle",
             "sample": f"{len(rows)} query rows (first rows of heads in order) of "
@@ -219,20 +237,22 @@ def run_reference(args, wl):
     import oracle
     from workloads import make_qkv
     q, k, v = make_qkv(wl)
+    lens = wl.seqlens()
     rows_per_step = 128
     rng = __import__("random").Random(1234)
     step_rows = []
     for s in range(args.warmup + args.steps):
-        step_rows.append([(rng.randrange(wl.B), rng.randrange(wl.H), rng.randrange(wl.N))
-                          for _ in range(rows_per_step)])
+        rows = []
+        for _ in range(rows_per_step):
+            b = rng.randrange(wl.B)
+            rows.append((b, rng.randrange(wl.H), rng.randrange(lens[b])))
+        step_rows.append(rows)
     for s in range(args.warmup):
-        oracle.attention_rows(q, k, v, wl.scale, wl.causal, step_rows[s])
+        _oracle_rows(wl, q, k, v, step_rows[s])
     flops = 0.0
     t0 = time.perf_counter()
     for s in range(args.warmup, args.warmup + args.steps):
-        oracle.attention_rows(q, k, v, wl.scale, wl.causal, step_rows[s])
-        flops += sum(4.0 * wl.d * ((i + 1) if wl.causal else wl.N)
-                     for (_, _, i) in step_rows[s])
+        flops += _oracle_rows(wl, q, k, v, step_rows[s])
     dt = time.perf_counter() - t0
     value = flops / dt / 1e12
     line = {
@@ -276,7 +296,12 @@ def run_ours(args, wl):
     warmup = max(3, args.warmup)
     q, k, v = make_qkv(wl)
     B, H, N, d = wl.B, wl.H, wl.N, wl.d
-    set_bytes = 4 * q.numel() * q.element_size() + B * H * N * 4
+    # packed (varlen) workloads: [total, H, d] tensors, LSE [H, total]
+    total = sum(wl.seqlens())
+    lse_shape = (H, total) if wl.varlen else (B, H, N)
+    cu_dev = torch.tensor(wl.cu_seqlens(), dtype=torch.int32, device=dev) if wl.varlen else None
+    max_len = max(wl.seqlens())
+    set_bytes = 4 * q.numel() * q.element_size() + H * total * 4
     n_sets = max(1, min(8, math.ceil(2.2 * L2_BYTES / set_bytes)))
     sets = []
     for i in range(n_sets):
@@ -284,7 +309,7 @@ def run_ours(args, wl):
         if i > 0:   # distinct copies (same values) so that no step hits L2
             qd, kd, vd = qd.clone(), kd.clone(), vd.clone()
         sets.append((qd, kd, vd, torch.empty_like(qd),
-                     torch.empty((B, H, N), dtype=torch.float32, device=dev)))
+                     torch.empty(lse_shape, dtype=torch.float32, device=dev)))
     stream = torch.cuda.Stream(device=dev)
     handle = stream.cuda_stream
     dcode = fa.FA_DTYPE_BF16 if wl.dtype == "bf16" else fa.FA_DTYPE_F16
@@ -306,7 +331,10 @@ def run_ours(args, wl):
         return need
 
     def call(qp, kp, vp, op, lp, Bc, Hc, plain=False):
-        if wl.splitkv and not plain:
+        if wl.varlen:
+            st_ = fa.fa_fwd_varlen(qp, kp, vp, op, lp, cu_dev.data_ptr(), B, max_len, total, H,
+                                   H, d, wl.scale, int(wl.causal), -1, -1, dcode, handle)
+        elif wl.splitkv and not plain:
             st_ = fa.fa_fwd_splitkv(qp, kp, vp, op, lp, Bc, Hc, Hc, N, d, wl.scale,
                                     int(wl.causal), -1, -1, dcode, 0,
                                     workspace.data_ptr() if workspace is not None else None,
@@ -398,14 +426,21 @@ def run_ours(args, wl):
     # Q, K, V from pinned host memory, runs the forward pass and copies O and
     # LSE back.  The B*H heads are cut into chunks and the copies of one chunk
     # overlap the kernel of the previous one (three streams: H2D, compute, D2H).
-    q_h, k_h, v_h = (t.reshape(B * H, N, d).pin_memory() for t in (q, k, v))
-    o_h = torch.empty((B * H, N, d), dtype=q.dtype).pin_memory()
-    l_h = torch.empty((B * H, N), dtype=torch.float32).pin_memory()
-    n_chunks = max(1, min(8, B * H))
-    bounds = [(c * B * H // n_chunks, (c + 1) * B * H // n_chunks) for c in range(n_chunks)]
-    dq, dk, dv, do_, dl = (sets[0][0].view(B * H, N, d), sets[0][1].view(B * H, N, d),
-                           sets[0][2].view(B * H, N, d), sets[0][3].view(B * H, N, d),
-                           sets[0][4].view(B * H, N))
+    # Packed (varlen) batches interleave heads within rows: one chunk.
+    if wl.varlen:
+        rows_e2e, row_shape, l_shape = 1, (total * H * d,), (H * total,)
+    else:
+        rows_e2e, row_shape, l_shape = B * H, (B * H, N, d), (B * H, N)
+    q_h, k_h, v_h = (t.reshape(row_shape).pin_memory() for t in (q, k, v))
+    o_h = torch.empty(row_shape, dtype=q.dtype).pin_memory()
+    l_h = torch.empty(l_shape, dtype=torch.float32).pin_memory()
+    if wl.varlen:
+        q_h, k_h, v_h, o_h, l_h = (t.unsqueeze(0) for t in (q_h, k_h, v_h, o_h, l_h))
+    n_chunks = max(1, min(8, rows_e2e))
+    bounds = [(c * rows_e2e // n_chunks, (c + 1) * rows_e2e // n_chunks)
+              for c in range(n_chunks)]
+    dq, dk, dv, do_ = (sets[0][t].view(q_h.shape) for t in range(4))
+    dl = sets[0][4].view(l_h.shape)
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     e2e_steps = max(1, min(args.steps, 20))
 
@@ -446,7 +481,7 @@ def run_ours(args, wl):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_ms = float(t.item())
     h2d = 3 * q.numel() * q.element_size()
-    d2h = q.numel() * q.element_size() + B * H * N * 4
+    d2h = q.numel() * q.element_size() + H * total * 4
 
     if rank == 0:
         peaks, src = _peaks()
@@ -491,8 +526,8 @@ def main():
                     help="timed steps (default: about two seconds of work)")
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", type=int, default=2,
-                    help="1..6 (default 2: B=4 H=16 N=2048 d=128 bf16 full; "
-                         "6: the split-KV case)")
+                    help="1..7 (default 2: B=4 H=16 N=2048 d=128 bf16 full; "
+                         "6: the split-KV case; 7: a packed variable-length batch)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -115,6 +115,43 @@ FA_API int fa_fwd_ext(const void* q, const void* k, const void* v, void* o, floa
                       int window_left, int window_right, int dtype, void* stream);
 
 /*
+ * fa_fwd_varlen -- fa_fwd_ext over a batch of sequences of different
+ * lengths packed along the rows (self-attention: each sequence's queries
+ * attend to that sequence's keys only).
+ *
+ * Source: flash-attention "hopper/mainloop_bwd_sm90_tma_gmma_ws.hpp" and the
+ * older "hopper/flash_fwd_kernel.h" (their variable-length mode: cu_seqlens
+ * row offsets into packed tensors, per-sequence lengths through
+ * seqlen_traits, and the tile loops bounded by each sequence's own length).
+ *
+ *   q, o        device pointers, contiguous [total][H][d] of `dtype`.
+ *   k, v        contiguous [total][H_kv][d]; grouped heads as in fa_fwd_ext.
+ *   lse         contiguous [H][total] float32, or NULL.
+ *   cu_seqlens  device pointer to batch + 1 int32 row offsets, 4-byte
+ *               aligned: sequence b is rows [cu_seqlens[b], cu_seqlens[b+1]).
+ *               They must be non-decreasing, within [0, total], and no
+ *               sequence longer than max_seqlen; the kernels clamp offsets
+ *               and lengths to those bounds, so a malformed array can only
+ *               leave rows unwritten, never touch memory outside the tensors.
+ *               Rows outside every sequence are not written.
+ *   batch, max_seqlen, total
+ *               number of sequences, the longest length, and the packed row
+ *               count; any of them 0: nothing is done (FA_OK).  Negative:
+ *               FA_ERR_INVALID_ARG.
+ *   causal, window_left, window_right
+ *               as in fa_fwd_ext, with positions counted from the start of
+ *               each sequence.
+ * The last query tile of a sequence reads up to 127 rows of the following
+ * sequence as padding (masked out): the packed tensors must hold finite
+ * values.  Alignment, ownership, scale, dtype and error behaviour are those
+ * of fa_fwd.
+ */
+FA_API int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                         const int* cu_seqlens, int batch, int max_seqlen, int total, int H,
+                         int H_kv, int d, float scale, int causal, int window_left,
+                         int window_right, int dtype, void* stream);
+
+/*
  * fa_fwd_splitkv -- fa_fwd_ext with the keys of every query row cut into
  * `num_splits` contiguous ranges that run as separate work units, then merged.
  *

@@ -207,3 +207,27 @@ def test_noalloc_rejects_partials_beyond_the_scratch(fa):
 def test_noalloc_argument_errors(fa, kw, code):
     S = kw.pop("S")
     assert _call_noalloc(fa, S, **kw) == code
+
+
+# --------------------------------------------------- packed (varlen) batches
+def _call_varlen(fa, cu=0x6000, batch=2, max_seqlen=300, total=500, H=4, H_kv=2, **kw):
+    a = dict(GOOD)
+    a.update(kw)
+    return fa.fa_fwd_varlen(a["q"], a["k"], a["v"], a["o"], a["lse"], cu, batch, max_seqlen,
+                            total, H, H_kv, a["d"], a["scale"], a["causal"], -1, -1,
+                            a["dtype"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(cu=0), 1), (dict(cu=0x6002), 3), (dict(total=-1), 1), (dict(batch=-1), 1),
+    (dict(max_seqlen=-5), 1), (dict(H=4, H_kv=3), 1), (dict(d=96), 2), (dict(q=0x1008), 3),
+    (dict(scale=float("nan")), 1),
+])
+def test_varlen_argument_errors(fa, kw, code):
+    assert _call_varlen(fa, **kw) == code
+
+
+@pytest.mark.parametrize("kw", [dict(batch=0), dict(total=0), dict(max_seqlen=0),
+                                dict(batch=0, cu=0, q=0, k=0, v=0, o=0)])
+def test_varlen_empty_is_noop(fa, kw):
+    assert _call_varlen(fa, **kw) == fa.FA_OK

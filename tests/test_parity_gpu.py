@@ -235,7 +235,39 @@ def test_watchdog_times_out_cleanly(fa):
 
 
 # ------------------------------------------------------- the workloads
+def _varlen_workload_case(fa, wl):
+    """Packed sequences: every row of the sample is checked against the oracle
+    evaluated on its own sequence."""
+    q, k, v = make_qkv(wl)
+    cu = wl.cu_seqlens()
+    cu_t = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    o, lse = fa.fwd_varlen(q.cuda(), k.cuda(), v.cuda(), cu_t, max(wl.seqlens()),
+                           scale=wl.scale, causal=wl.causal)
+    torch.cuda.synchronize()
+    st, site = fa.fa_get_device_status(None)
+    assert st == fa.FA_OK, f"device status {fa.fa_status_string(st)} at site {site}"
+    rows = sample_rows(wl)
+    o_s, l_s, o_r, l_r = [], [], [], []
+    for b in sorted(set(r[0] for r in rows)):
+        s0, s1 = cu[b], cu[b + 1]
+        trip = [(0, h, i) for (bb, h, i) in rows if bb == b]
+        to_bhnd = lambda t: t[s0:s1].permute(1, 0, 2).unsqueeze(0).contiguous()
+        ref_o, ref_l = oracle.attention_rows(to_bhnd(q), to_bhnd(k), to_bhnd(v), wl.scale,
+                                             wl.causal, trip)
+        for t, (_, h, i) in enumerate(trip):
+            o_s.append(o[s0 + i, h].float().cpu().numpy())
+            l_s.append(lse[h, s0 + i].item())
+            o_r.append(ref_o[t])
+            l_r.append(ref_l[t])
+    err = _check(np.array(o_s), np.array(l_s), np.array(o_r), np.array(l_r),
+                 wl.name + " (sampled)")
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+    return err
+
+
 def _workload_case(fa, wl, full):
+    if wl.varlen:
+        return _varlen_workload_case(fa, wl)
     q, k, v = make_qkv(wl)
     if wl.splitkv:
         o, lse = fa.fwd_splitkv(q.cuda(), k.cuda(), v.cuda(), scale=wl.scale,

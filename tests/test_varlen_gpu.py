@@ -1,0 +1,171 @@
+"""GPU parity of the variable-length forward (fa_fwd_varlen) against the fp64
+oracle's packed-sequence evaluation.
+
+Sequences of different lengths are packed along the rows of [total, H, d]
+tensors; each is attended on its own.  Tolerances as for the plain forward
+(max |dO| <= 2e-2, max |dLSE| <= 1e-3), compared element by element over
+every row that belongs to a sequence; rows outside every sequence must stay
+untouched.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from workloads import make_random_qkv
+
+pytestmark = pytest.mark.gpu
+
+O_TOL = 2e-2
+LSE_TOL = 1e-3
+
+
+@pytest.fixture(scope="module")
+def fa():
+    from attention_forward_10_gb300 import build
+    build.build()
+    import attention_forward_10_gb300 as fa_mod
+    fa_mod.fa_set_max_ctas(0)
+    fa_mod.fa_set_wait_timeout_us(2_000_000)
+    return fa_mod
+
+
+def _packed(lens, H, H_kv, d, dtype, seed, extra_rows=0):
+    total = sum(lens) + extra_rows
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn(total, H, d, generator=g).to(dtype)
+    k = torch.randn(total, H_kv, d, generator=g).to(dtype)
+    v = torch.randn(total, H_kv, d, generator=g).to(dtype)
+    cu = [0]
+    for n in lens:
+        cu.append(cu[-1] + n)
+    return q, k, v, cu
+
+
+def _run(fa, q, k, v, cu, scale, causal, window=(-1, -1), out=None, lse=None, max_seqlen=None):
+    cu_t = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    lens = [cu[i + 1] - cu[i] for i in range(len(cu) - 1)]
+    ms = max(lens) if max_seqlen is None else max_seqlen
+    o, l = fa.fwd_varlen(q.cuda(), k.cuda(), v.cuda(), cu_t, ms, scale=scale, causal=causal,
+                         window=window, out=out, lse=lse)
+    torch.cuda.synchronize()
+    st, site = fa.fa_get_device_status(None)
+    assert st == fa.FA_OK, f"device status {fa.fa_status_string(st)} at site {site}"
+    return o, l
+
+
+def _check(o, lse, o_ref, l_ref, cu, what):
+    rows = np.concatenate([np.arange(cu[i], cu[i + 1]) for i in range(len(cu) - 1)])
+    o_np = o.float().cpu().numpy()[rows]
+    l_np = lse.cpu().numpy()[:, rows]
+    assert np.isfinite(o_np).all() and np.isfinite(l_np).all(), f"{what}: non-finite"
+    err_o = float(np.abs(o_np - o_ref[rows]).max())
+    err_l = float(np.abs(l_np - l_ref[:, rows]).max())
+    assert err_l <= LSE_TOL, f"{what}: max|dLSE| = {err_l:.3e} (O err {err_o:.3e})"
+    assert err_o <= O_TOL, f"{what}: max|dO| = {err_o:.3e} (LSE err {err_l:.3e})"
+
+
+LENS = [1, 127, 128, 129, 300, 0, 640, 5, 257]
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16], ids=["bf16", "fp16"])
+def test_ragged_batch(fa, d, causal, dtype):
+    q, k, v, cu = _packed(LENS, 4, 2, d, dtype, seed=600 + d)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = _run(fa, q, k, v, cu, scale, causal)
+    o_ref, l_ref = oracle.attention_varlen(q, k, v, cu, scale, causal)
+    _check(o, lse, o_ref, l_ref, cu, f"d={d} causal={causal}")
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+@pytest.mark.parametrize("window", [(40, 40), (200, 0), (0, 0), (-1, 130)])
+def test_windows(fa, d, causal, window):
+    q, k, v, cu = _packed([700, 3, 260, 128], 2, 1, d, torch.bfloat16, seed=610 + d)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = _run(fa, q, k, v, cu, scale, causal, window)
+    o_ref, l_ref = oracle.attention_varlen(q, k, v, cu, scale, causal, *window)
+    _check(o, lse, o_ref, l_ref, cu, f"d={d} causal={causal} window={window}")
+
+
+@pytest.mark.parametrize("ctas", [1, 3])
+@pytest.mark.parametrize("d", [128, 256])
+def test_persistent_loop(fa, ctas, d):
+    q, k, v, cu = _packed([900, 130, 1, 513, 256], 2, 2, d, torch.bfloat16, seed=620 + ctas)
+    fa.fa_set_max_ctas(ctas)
+    try:
+        o, lse = _run(fa, q, k, v, cu, 0.08, True)
+    finally:
+        fa.fa_set_max_ctas(0)
+    o_ref, l_ref = oracle.attention_varlen(q, k, v, cu, 0.08, True)
+    _check(o, lse, o_ref, l_ref, cu, f"ctas={ctas} d={d}")
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("N", [256, 333])
+def test_equal_lengths_equal_the_batched_forward(fa, d, N):
+    """Packing equal-length sequences gives the [B,H,N,d] forward bit for bit
+    (same tiles, same arithmetic; padding keys are masked either way)."""
+    q, k, v = make_random_qkv(3, 2, N, d, torch.bfloat16, seed=630 + N)
+    o_b, l_b = fa.fwd(q.cuda(), k.cuda(), v.cuda(), causal=True)
+    pack = lambda t: t.permute(0, 2, 1, 3).reshape(3 * N, 2, d).contiguous()
+    o_v, l_v = _run(fa, pack(q), pack(k), pack(v), [0, N, 2 * N, 3 * N], d ** -0.5, True)
+    assert torch.equal(o_v, pack(o_b))
+    assert torch.equal(l_v, l_b.permute(1, 0, 2).reshape(2, 3 * N))
+
+
+def test_rows_outside_sequences_and_guards_untouched(fa):
+    q, k, v, cu = _packed([200, 77], 2, 2, 128, torch.bfloat16, seed=640, extra_rows=50)
+    total = q.shape[0]
+    G = 256
+    pattern = torch.tensor([0x7FC1], dtype=torch.int16).view(torch.bfloat16)
+    obuf = pattern.repeat(q.numel() + 2 * G).cuda()
+    lbuf = torch.full((2 * total + 2 * G,), -7.25, dtype=torch.float32, device="cuda")
+    o = obuf[G:G + q.numel()].view(q.shape)
+    lse = lbuf[G:G + 2 * total].view(2, total)
+    _run(fa, q, k, v, cu, 0.1, False, out=o, lse=lse)
+    o_ref, l_ref = oracle.attention_varlen(q, k, v, cu, 0.1, False)
+    _check(o, lse, o_ref, l_ref, cu, "guarded")
+    tail = o[cu[-1]:].contiguous().view(torch.int16).cpu()
+    assert (tail == 0x7FC1).all()
+    assert (lse[:, cu[-1]:].cpu() == -7.25).all()
+    og = torch.cat([obuf[:G], obuf[G + q.numel():]]).view(torch.int16).cpu()
+    assert (og == 0x7FC1).all()
+    lg = torch.cat([lbuf[:G], lbuf[G + 2 * total:]]).cpu()
+    assert (lg == -7.25).all()
+
+
+def test_malformed_offsets_stay_in_bounds(fa):
+    """Offsets past `total`, a decreasing pair and a sequence longer than
+    max_seqlen are clamped by the kernels: the rows they still cover are
+    correct and nothing outside the tensors is written."""
+    total, H, d = 400, 2, 128
+    g = torch.Generator().manual_seed(650)
+    q, k, v = (torch.randn(total, H, d, generator=g).to(torch.bfloat16) for _ in range(3))
+    # seq 0: rows [0, 300) cut to max_seqlen = 256 rows; seq 1: decreasing
+    # offsets (empty); seq 2: rows [290, 350); seq 3: rows [350, 900) cut at
+    # total -> [350, 400)
+    cu = [0, 300, 290, 350, 900]
+    G = 256
+    pattern = torch.tensor([0x7FC1], dtype=torch.int16).view(torch.bfloat16)
+    obuf = pattern.repeat(q.numel() + 2 * G).cuda()
+    lbuf = torch.full((H * total + 2 * G,), -7.25, dtype=torch.float32, device="cuda")
+    o = obuf[G:G + q.numel()].view(q.shape)
+    lse = lbuf[G:G + H * total].view(H, total)
+    _run(fa, q, k, v, cu, 0.1, True, out=o, lse=lse, max_seqlen=256)
+    for (r0, r1, what) in ((0, 256, "first sequence, cut to max_seqlen"),
+                           (290, 350, "third sequence"),
+                           (350, 400, "last sequence, cut at total")):
+        o_ref, l_ref = oracle.attention_varlen(q[r0:r1], k[r0:r1], v[r0:r1], [0, r1 - r0],
+                                               0.1, True)
+        _check(o[r0:r1], lse[:, r0:r1], o_ref, l_ref, [0, r1 - r0], what)
+    assert (o[256:290].contiguous().view(torch.int16).cpu() == 0x7FC1).all()
+    assert (lse[:, 256:290].cpu() == -7.25).all()
+    og = torch.cat([obuf[:G], obuf[G + q.numel():]]).view(torch.int16).cpu()
+    assert (og == 0x7FC1).all()
+    lg = torch.cat([lbuf[:G], lbuf[G + H * total:]]).cpu()
+    assert (lg == -7.25).all()

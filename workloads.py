@@ -32,6 +32,22 @@ class Workload:
     causal: bool
     qk_mult: float = 1.0  # Q and K multiplied by this after rounding
     splitkv: bool = False  # run through the split-KV entry point (automatic count)
+    varlen: bool = False   # B sequences of seeded lengths in [N/16, N], packed along rows
+
+    def seqlens(self) -> list[int]:
+        """Lengths of the packed sequences (varlen workloads): B integers drawn
+        uniformly from [max(1, N/16), N] by a generator seeded with
+        3000 + index."""
+        if not self.varlen:
+            return [self.N] * self.B
+        g = torch.Generator().manual_seed(3000 + self.index)
+        return torch.randint(max(1, self.N // 16), self.N + 1, (self.B,), generator=g).tolist()
+
+    def cu_seqlens(self) -> list[int]:
+        out = [0]
+        for n in self.seqlens():
+            out.append(out[-1] + n)
+        return out
 
     @property
     def scale(self) -> float:
@@ -43,20 +59,25 @@ class Workload:
 
     @property
     def flops(self) -> float:
-        """Algorithmic FLOPs of the metric: 4*B*H*N^2*d, halved when causal."""
-        f = 4.0 * self.B * self.H * self.N * self.N * self.d
+        """Algorithmic FLOPs of the metric: 4*H*d*sum_b n_b^2 (4*B*H*N^2*d for
+        equal lengths), halved when causal."""
+        f = 4.0 * self.H * self.d * sum(float(n) * n for n in self.seqlens())
         return f / 2 if self.causal else f
 
     @property
     def hbm_bytes(self) -> int:
         """Algorithmic HBM bytes: read Q, K, V; write O (16-bit) and LSE (fp32)."""
-        bh_n = self.B * self.H * self.N
-        return 4 * bh_n * self.d * 2 + bh_n * 4
+        rows = self.H * sum(self.seqlens())
+        return 4 * rows * self.d * 2 + rows * 4
 
     def describe(self) -> str:
         mask = "causal" if self.causal else "full"
         extra = f", Q,K x{self.qk_mult:g}" if self.qk_mult != 1.0 else ""
         extra += ", split-KV" if self.splitkv else ""
+        if self.varlen:
+            return (f"{self.B} sequences of {min(self.seqlens())}..{max(self.seqlens())} rows "
+                    f"(total {sum(self.seqlens())}) packed, H={self.H} d={self.d} "
+                    f"{self.dtype} {mask}{extra}")
         return (f"B={self.B} H={self.H} N={self.N} d={self.d} {self.dtype} "
                 f"{mask}{extra}")
 
@@ -71,6 +92,9 @@ WORKLOADS = [
     # cannot fill the SMs on their own (the split-KV case)
     Workload(6, "bf16_d128_n32768_h1_causal_splitkv", 1, 1, 32768, 128, "bf16", True,
              splitkv=True),
+    # 16 causal sequences of 256..4096 rows packed along the rows (a
+    # variable-length training batch)
+    Workload(7, "bf16_d128_varlen16_causal", 16, 16, 4096, 128, "bf16", True, varlen=True),
 ]
 
 
@@ -79,9 +103,10 @@ def workload(index: int) -> Workload:
 
 
 def make_qkv(wl: Workload, seed: int | None = None):
-    """CPU tensors q, k, v in the workload's dtype, drawn as the recipe says."""
+    """CPU tensors q, k, v in the workload's dtype, drawn as the recipe says
+    ([B, H, N, d]; packed [total, H, d] for varlen workloads)."""
     g = torch.Generator().manual_seed(1000 + wl.index if seed is None else seed)
-    shape = (wl.B, wl.H, wl.N, wl.d)
+    shape = (sum(wl.seqlens()), wl.H, wl.d) if wl.varlen else (wl.B, wl.H, wl.N, wl.d)
     out = []
     for _ in range(3):
         out.append(torch.randn(shape, generator=g, dtype=torch.float32)
@@ -109,16 +134,19 @@ def sample_rows(wl: Workload, count: int = 512, seed: int | None = None):
     128-row query tile boundary up to 1024.
     """
     g = torch.Generator().manual_seed(2000 + wl.index if seed is None else seed)
+    lens = wl.seqlens()
     b = torch.randint(0, wl.B, (count,), generator=g)
     h = torch.randint(0, wl.H, (count,), generator=g)
     i = torch.randint(0, wl.N, (count,), generator=g)
-    rows = set(zip(b.tolist(), h.tolist(), i.tolist()))
-    fixed = {0, 1, 127, 128, wl.N - 1}
-    if wl.causal:
-        for t in range(128, min(wl.N, 1025), 128):
-            fixed.update({t - 1, t})
+    # rows of a shorter sequence are folded into its length
+    rows = set((bb, hh, ii % lens[bb]) for bb, hh, ii in zip(b.tolist(), h.tolist(), i.tolist()))
     for (bb, hh) in ((0, 0), (wl.B - 1, wl.H - 1)):
+        n = lens[bb]
+        fixed = {0, 1, 127, 128, n - 1}
+        if wl.causal:
+            for t in range(128, min(n, 1025), 128):
+                fixed.update({t - 1, t})
         for r in fixed:
-            if 0 <= r < wl.N:
+            if 0 <= r < n:
                 rows.add((bb, hh, r))
     return sorted(rows)
