@@ -23,7 +23,9 @@ row stores O = 0 and LSE = -inf).
 ``attention_ex`` adds grouped K/V heads (query head h reads K/V head
 h // (H / H_kv)) and a local window (keys i - window_left .. i + window_right),
 the ``qhead_per_khead`` and ``window_size_left/right`` options of the same
-backward page.  ``attention_varlen`` takes sequences of different lengths
+backward page.  ``attention_bwd`` gives the gradients dQ, dK, dV of that
+definition against dO (the backward page's P, dP, dPsum, dS recurrence
+written out in double).  ``attention_varlen`` takes sequences of different lengths
 packed along the rows ([total, H, d], cu_seqlens offsets), the
 variable-length mode of the Hopper pages.
 
@@ -94,6 +96,9 @@ def _bind(path: str):
     lib.attn_ref_varlen_u16.argtypes = [vp, vp, vp, c_int, vp, c_long, c_long, c_long, c_long,
                                         c_long, c_double, c_int, c_long, c_long, vp, vp, c_int]
     lib.attn_ref_varlen_u16.restype = c_int
+    lib.attn_ref_bwd_u16.argtypes = [vp, vp, vp, vp, c_int, c_long, c_long, c_long, c_long,
+                                     c_long, c_double, c_int, c_long, c_long, vp, vp, vp, c_int]
+    lib.attn_ref_bwd_u16.restype = c_int
     lib.attn_ref_widen.argtypes = [ctypes.c_uint16, c_int]
     lib.attn_ref_widen.restype = c_double
     lib.attn_ref_max_threads.argtypes = []
@@ -288,3 +293,30 @@ def attention_varlen(q, k, v, cu_seqlens, scale: float, causal: bool, window_lef
     if rc != 0:
         raise RuntimeError("oracle attn_ref_varlen_u16 failed")
     return o, lse
+
+
+def attention_bwd(q, k, v, dout, scale: float, causal: bool, window_left: int = -1,
+                  window_right: int = -1, nthreads: int = 0):
+    """Gradients (dQ [B,H,N,d], dK, dV [B,H_kv,N,d], float64) of the forward
+    definition against dO, for the mask, window and head grouping of
+    ``attention_ex``: P = exp(S - LSE), dV = P^T dO, dP = dO V^T,
+    D = rowsum(P * dP), dS = P * (dP - D), dQ = scale dS K, dK = scale dS^T Q."""
+    qw, is_bf16 = _u16_view(q)
+    kw, kb = _u16_view(k)
+    vw, vb = _u16_view(v)
+    gw, gb = _u16_view(dout)
+    if not (is_bf16 == kb == vb == gb):
+        raise TypeError("q, k, v, dout must share one dtype")
+    B, H, H_kv, N, d = _check_ex(q, k, v)
+    if tuple(dout.shape) != tuple(q.shape):
+        raise ValueError("dout must have q's shape")
+    dq = np.empty((B, H, N, d), dtype=np.float64)
+    dk = np.empty((B, H_kv, N, d), dtype=np.float64)
+    dv = np.empty((B, H_kv, N, d), dtype=np.float64)
+    rc = _load().attn_ref_bwd_u16(_ptr(qw), _ptr(kw), _ptr(vw), _ptr(gw), int(is_bf16), B, H,
+                                  H_kv, N, d, float(scale), int(bool(causal)),
+                                  int(window_left), int(window_right), _ptr(dq), _ptr(dk),
+                                  _ptr(dv), int(nthreads))
+    if rc != 0:
+        raise RuntimeError("oracle attn_ref_bwd_u16 failed")
+    return dq, dk, dv

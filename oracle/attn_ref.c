@@ -40,6 +40,10 @@
  * the page's window_size_left / window_size_right and its Is_local mask).
  * With H_kv = H and both bounds negative they reduce to the definition above.
  *
+ * Backward (attn_ref_bwd_u16): the gradients dQ, dK, dV of the definition
+ * above against dO, as the same backward page computes them (P, dP, the row
+ * sums D_i = sum_j P_ij dP_ij, dS = P (dP - D)), in double.
+ *
  * Variable-length batches (attn_ref_varlen_u16): sequences of different
  * lengths packed along the rows of [total][H][d] tensors, sequence b being
  * rows cu[b] .. cu[b+1]-1 -- the cu_seqlens mode of the Hopper pages.  Each
@@ -473,5 +477,138 @@ int attn_ref_varlen_u16(const uint16_t *q, const uint16_t *k,
         }
     }
     free(qd); free(kd); free(vd);
+    return rc;
+}
+
+/*
+ * Backward pass: the gradients of O = attention(Q, K, V) against dO, as
+ * flash-attention "hopper/mainloop_bwd_sm90_tma_gmma_ws.hpp"
+ * (CollectiveMainloopBwd::mma) computes them, written from the definition:
+ *
+ *   P_ij  = exp(s_ij - LSE_i)  for j in J(i), 0 otherwise
+ *   dV_j  = sum_i P_ij dO_i
+ *   dP_ij = dO_i . v_j
+ *   D_i   = sum_j P_ij dP_ij                 (the page's dPsum)
+ *   dS_ij = P_ij (dP_ij - D_i)
+ *   dQ_i  = scale * sum_j dS_ij k_j
+ *   dK_j  = scale * sum_i dS_ij q_i
+ *
+ * with s_ij and LSE_i those of the forward definition above (recomputed here
+ * in double from the 16-bit inputs).  With grouped heads, dK and dV of a K/V
+ * head sum over the query heads that read it.
+ *   q, dout, dq : [B][H][N][d];  k, v, dk, dv : [B][H_kv][N][d]
+ * Pass 1 (rows i in parallel): LSE_i, D_i and dQ_i.  Pass 2 (keys j in
+ * parallel): dK_j and dV_j from the stored LSE_i and D_i.
+ */
+int attn_ref_bwd_u16(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                     const uint16_t *dout, int is_bf16, long B, long H, long H_kv,
+                     long N, long d, double scale, int causal, long wl, long wr,
+                     double *dq, double *dk, double *dv, int nthreads) {
+    if (!q || !k || !v || !dout || !dq || !dk || !dv || B < 0 || H <= 0 ||
+        H_kv <= 0 || H % H_kv != 0 || N < 0 || d <= 0)
+        return -1;
+    set_threads(nthreads);
+    long slice = N * d, group = H / H_kv, cap = slice > 0 ? slice : 1;
+    double *kd = (double *)malloc(sizeof(double) * (size_t)cap);
+    double *vd = (double *)malloc(sizeof(double) * (size_t)cap);
+    double *qd = (double *)malloc(sizeof(double) * (size_t)(cap * group));
+    double *dod = (double *)malloc(sizeof(double) * (size_t)(cap * group));
+    double *lse = (double *)malloc(sizeof(double) * (size_t)((N > 0 ? N : 1) * group));
+    double *dsum = (double *)malloc(sizeof(double) * (size_t)((N > 0 ? N : 1) * group));
+    if (!kd || !vd || !qd || !dod || !lse || !dsum) {
+        free(kd); free(vd); free(qd); free(dod); free(lse); free(dsum);
+        return -1;
+    }
+    int rc = 0;
+    for (long b = 0; b < B && rc == 0; ++b) {
+        for (long hk = 0; hk < H_kv && rc == 0; ++hk) {
+            long bkv = b * H_kv + hk;
+            widen_slice(k + bkv * slice, kd, slice, is_bf16);
+            widen_slice(v + bkv * slice, vd, slice, is_bf16);
+            for (long g = 0; g < group; ++g) {
+                long bh = b * H + hk * group + g;
+                widen_slice(q + bh * slice, qd + g * slice, slice, is_bf16);
+                widen_slice(dout + bh * slice, dod + g * slice, slice, is_bf16);
+            }
+            /* pass 1: per query row i of every head of the group */
+#pragma omp parallel
+            {
+                double *s = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+                if (!s) {
+#pragma omp atomic write
+                    rc = -1;
+                } else {
+#pragma omp for schedule(dynamic, 4)
+                    for (long gi = 0; gi < group * N; ++gi) {
+                        long g = gi / N, i = gi % N;
+                        const double *qi = qd + g * slice + i * d;
+                        const double *doi = dod + g * slice + i * d;
+                        double *dqi = dq + ((b * H + hk * group + g) * N + i) * d;
+                        long j0, j1;
+                        key_range(N, i, causal, wl, wr, &j0, &j1);
+                        for (long c = 0; c < d; ++c) dqi[c] = 0.0;
+                        if (j1 <= j0) {
+                            lse[gi] = -INFINITY;
+                            dsum[gi] = 0.0;
+                            continue;
+                        }
+                        double m = -INFINITY;
+                        for (long j = j0; j < j1; ++j) {
+                            double dot = 0.0;
+                            for (long c = 0; c < d; ++c) dot += qi[c] * kd[j * d + c];
+                            s[j] = scale * dot;
+                            if (s[j] > m) m = s[j];
+                        }
+                        double sum = 0.0;
+                        for (long j = j0; j < j1; ++j) sum += exp(s[j] - m);
+                        double l = m + log(sum);
+                        double dsi = 0.0;   /* D_i = sum_j P_ij dP_ij */
+                        for (long j = j0; j < j1; ++j) {
+                            double dp = 0.0;
+                            for (long c = 0; c < d; ++c) dp += doi[c] * vd[j * d + c];
+                            dsi += exp(s[j] - l) * dp;
+                        }
+                        for (long j = j0; j < j1; ++j) {
+                            double dp = 0.0;
+                            for (long c = 0; c < d; ++c) dp += doi[c] * vd[j * d + c];
+                            double ds = exp(s[j] - l) * (dp - dsi);
+                            for (long c = 0; c < d; ++c) dqi[c] += scale * ds * kd[j * d + c];
+                        }
+                        lse[gi] = l;
+                        dsum[gi] = dsi;
+                    }
+                    free(s);
+                }
+            }
+            if (rc != 0) break;
+            /* pass 2: per key row j, summed over the group's query rows */
+#pragma omp parallel for schedule(dynamic, 4)
+            for (long j = 0; j < N; ++j) {
+                double *dkj = dk + (bkv * N + j) * d;
+                double *dvj = dv + (bkv * N + j) * d;
+                for (long c = 0; c < d; ++c) { dkj[c] = 0.0; dvj[c] = 0.0; }
+                for (long gi = 0; gi < group * N; ++gi) {
+                    long g = gi / N, i = gi % N;
+                    long j0, j1;
+                    key_range(N, i, causal, wl, wr, &j0, &j1);
+                    if (j < j0 || j >= j1) continue;
+                    const double *qi = qd + g * slice + i * d;
+                    const double *doi = dod + g * slice + i * d;
+                    double dot = 0.0, dp = 0.0;
+                    for (long c = 0; c < d; ++c) {
+                        dot += qi[c] * kd[j * d + c];
+                        dp += doi[c] * vd[j * d + c];
+                    }
+                    double p = exp(scale * dot - lse[gi]);
+                    double ds = p * (dp - dsum[gi]);
+                    for (long c = 0; c < d; ++c) {
+                        dvj[c] += p * doi[c];
+                        dkj[c] += scale * ds * qi[c];
+                    }
+                }
+            }
+        }
+    }
+    free(kd); free(vd); free(qd); free(dod); free(lse); free(dsum);
     return rc;
 }

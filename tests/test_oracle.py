@@ -476,3 +476,79 @@ def test_varlen_rejects_malformed_offsets():
     for cu in ([0, 6, 4], [0, 11], [-1, 5]):
         with pytest.raises(RuntimeError):
             oracle.attention_varlen(q, q, q, cu, 0.5, False)
+
+
+# --------------------------------------------------------------- backward
+def _torch_attention_f64(q, k, v, scale, causal, window):
+    """Reference forward in torch float64 with an explicit mask (autograd)."""
+    N = q.shape[-2]
+    group = q.shape[1] // k.shape[1]
+    i = torch.arange(N)[:, None]
+    j = torch.arange(N)[None, :]
+    allowed = torch.ones(N, N, dtype=torch.bool)
+    if causal:
+        allowed &= j <= i
+    if window[0] >= 0:
+        allowed &= j >= i - window[0]
+    if window[1] >= 0:
+        allowed &= j <= i + window[1]
+    kr = k.repeat_interleave(group, 1)
+    vr = v.repeat_interleave(group, 1)
+    s = scale * q @ kr.transpose(-1, -2)
+    p = torch.softmax(s.masked_fill(~allowed, float("-inf")), -1)
+    return p @ vr
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("window", [(-1, -1), (6, 3)])
+@pytest.mark.parametrize("H,H_kv", [(4, 4), (4, 2)])
+def test_bwd_matches_torch_autograd(causal, window, H, H_kv):
+    """dQ, dK, dV equal torch float64 autograd through softmax attention."""
+    q, _, _ = make_random_qkv(2, H, 37, 16, torch.bfloat16, seed=700 + H_kv)
+    _, k, v = make_random_qkv(2, H_kv, 37, 16, torch.bfloat16, seed=701 + H_kv)
+    do = torch.randn(q.shape, generator=torch.Generator().manual_seed(702)).to(torch.bfloat16)
+    dq, dk, dv = oracle.attention_bwd(q, k, v, do, 0.3, causal, *window)
+    qd, kd, vd = (t.double().requires_grad_() for t in (q, k, v))
+    o = _torch_attention_f64(qd, kd, vd, 0.3, causal, window)
+    o.backward(do.double())
+    np.testing.assert_allclose(dq, qd.grad.numpy(), rtol=0, atol=1e-11)
+    np.testing.assert_allclose(dk, kd.grad.numpy(), rtol=0, atol=1e-11)
+    np.testing.assert_allclose(dv, vd.grad.numpy(), rtol=0, atol=1e-11)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_directional_finite_difference(causal):
+    """<dQ,Eq> + <dK,Ek> + <dV,Ev> equals the central difference of
+    L = sum(O * dO) along (Eq, Ek, Ev), with O from the double forward."""
+    q, k, v = make_random_qkv(1, 2, 23, 8, torch.bfloat16, seed=710)
+    g = torch.Generator().manual_seed(711)
+    do = torch.randn(q.shape, generator=g).to(torch.bfloat16)
+    eq, ek, ev = (torch.randn(q.shape, generator=g, dtype=torch.float64) for _ in range(3))
+    dq, dk, dv = oracle.attention_bwd(q, k, v, do, 0.35, causal)
+    qd, kd, vd, dod = (t.double().numpy() for t in (q, k, v, do))
+    eps = 1e-4
+
+    def loss(sign):
+        o, _ = oracle.attention_f64(qd + sign * eps * eq.numpy(), kd + sign * eps * ek.numpy(),
+                                    vd + sign * eps * ev.numpy(), 0.35, causal)
+        return float((o * dod).sum())
+
+    fd = (loss(+1) - loss(-1)) / (2 * eps)
+    an = float((dq * eq.numpy()).sum() + (dk * ek.numpy()).sum() + (dv * ev.numpy()).sum())
+    assert abs(fd - an) <= 1e-7 * max(1.0, abs(an)), (fd, an)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("window", [(-1, -1), (5, 2)])
+def test_bwd_sum_identities(causal, window):
+    """Every row of P sums to one and every row of dS to zero, so
+    sum_j dV_j = sum_i dO_i (over the heads sharing a K/V head) and
+    sum_j dK_j = 0."""
+    q, _, _ = make_random_qkv(1, 4, 41, 16, torch.float16, seed=720)
+    _, k, v = make_random_qkv(1, 2, 41, 16, torch.float16, seed=721)
+    do = torch.randn(q.shape, generator=torch.Generator().manual_seed(722)).to(torch.float16)
+    dq, dk, dv = oracle.attention_bwd(q, k, v, do, 0.25, causal, *window)
+    dod = do.double().numpy().reshape(1, 2, 2, 41, 16)
+    np.testing.assert_allclose(dv.sum(2), dod.sum((2, 3)), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dk.sum(2), 0.0, rtol=0, atol=1e-12)
+    assert np.abs(dq).max() > 1e-3

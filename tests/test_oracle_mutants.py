@@ -44,6 +44,12 @@ MUTANTS = {
                                 "                        attend_range(qd + i * d, kd, vd, d, j0, j1",
                                 "key_range(n, i + s0 < n ? i + s0 : n - 1, causal, wl, wr, &j0, &j1);\n"
                                 "                        attend_range(qd + i * d, kd, vd, d, j0, j1"),
+    "bwd_dk_unscaled": ("dkj[c] += scale * ds * qi[c];", "dkj[c] += ds * qi[c];"),
+    "bwd_rowsum_without_p": ("dsi += exp(s[j] - l) * dp;", "dsi += dp;"),
+    "bwd_dv_from_ds": ("dvj[c] += p * doi[c];", "dvj[c] += ds * doi[c];"),
+    "bwd_key_mask_ignored": ("if (j < j0 || j >= j1) continue;", "if (j < 0) continue;"),
+    "bwd_dq_transposed": ("dqi[c] += scale * ds * kd[j * d + c];",
+                          "dqi[c] += scale * ds * vd[j * d + c];"),
     "bf16_decoder_shift": ("uint32_t bits = (uint32_t)b << 16;",
                            "uint32_t bits = (uint32_t)b << 15;"),
     "half_decoder_bias": ("expo - 25", "expo - 24"),
@@ -70,6 +76,9 @@ PIN_CALLS = [
      dict(causal=True, window=(5, 3))),
     (pins.test_varlen_matches_torch_per_sequence, dict(causal=True, window=(4, 2))),
     (pins.test_varlen_zero_queries_closed_form, {}),
+    (pins.test_bwd_matches_torch_autograd, dict(causal=True, window=(6, 3), H=4, H_kv=2)),
+    (pins.test_bwd_directional_finite_difference, dict(causal=True)),
+    (pins.test_bwd_sum_identities, dict(causal=False, window=(5, 2))),
 ]
 
 
