@@ -39,6 +39,9 @@ _ull = ctypes.c_ulonglong
 SIGNATURES = {
     "fa_fwd": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _vp], _i),
     "fa_fwd_ext": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _i, _i, _vp], _i),
+    "fa_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _ull, _i, _i, _i, _i, _i, _f,
+                _i, _i, _i, _i, _vp], _i),
+    "fa_bwd_workspace_bytes": ([_i, _i, _i, ctypes.POINTER(_ull)], _i),
     "fa_fwd_varlen": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _i, _i,
                        _vp], _i),
     "fa_fwd_splitkv": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _i, _i, _i,
@@ -102,6 +105,21 @@ def fa_fwd_ext(q: int, k: int, v: int, o: int, lse: int | None, B: int, H: int, 
                window_right: int, dtype: int, stream: int | None) -> int:
     return int(_lib.fa_fwd_ext(q, k, v, o, lse or None, B, H, H_kv, N, d, scale, causal,
                                window_left, window_right, dtype, stream or None))
+
+
+def fa_bwd(q: int, k: int, v: int, o: int, lse: int, dout: int, dq: int, dk: int, dv: int,
+           workspace: int, workspace_bytes: int, B: int, H: int, H_kv: int, N: int, d: int,
+           scale: float, causal: int, window_left: int, window_right: int, dtype: int,
+           stream: int | None) -> int:
+    return int(_lib.fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace or None,
+                           int(workspace_bytes), B, H, H_kv, N, d, scale, causal, window_left,
+                           window_right, dtype, stream or None))
+
+
+def fa_bwd_workspace_bytes(B: int, H: int, N: int) -> tuple[int, int]:
+    out = ctypes.c_ulonglong(0)
+    st = int(_lib.fa_bwd_workspace_bytes(B, H, N, ctypes.byref(out)))
+    return st, int(out.value)
 
 
 def fa_fwd_varlen(q: int, k: int, v: int, o: int, lse: int | None, cu_seqlens: int,
@@ -276,6 +294,41 @@ def fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int, *, scale: float | None = No
     return out, (lse if return_lse else None)
 
 
+def bwd(q, k, v, o, lse, dout, *, scale: float | None = None, causal: bool = False,
+        window: tuple[int, int] = (-1, -1), dq=None, dk=None, dv=None, workspace=None,
+        stream=None):
+    """Gradients (dq, dk, dv) of the forward pass ``fwd`` produced (o, lse) for,
+    against dout; shapes and dtype as in ``fwd``.  d must be 64 or 128."""
+    import torch
+    _check_qkv(q, k, v)
+    if o.shape != q.shape or dout.shape != q.shape or not (o.is_contiguous() and
+                                                            dout.is_contiguous()):
+        raise ValueError("o and dout must be contiguous and shaped like q")
+    B, H, N, d = (int(x) for x in q.shape)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    with torch.cuda.device(q.device):
+        st, need = fa_bwd_workspace_bytes(B, H, N)
+        if st != FA_OK:
+            raise FaError(st, "fa_bwd_workspace_bytes")
+        if workspace is None:
+            workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+        st = fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                    dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                    workspace.data_ptr(), workspace.numel(), B, H, int(k.shape[1]), N, d,
+                    float(scale), int(bool(causal)), int(window[0]), int(window[1]),
+                    _dtype_code(q), handle)
+    if st != FA_OK:
+        raise FaError(st, "fa_bwd")
+    return dq, dk, dv
+
+
 def fwd_splitkv(q, k, v, *, num_splits: int = 0, scale: float | None = None,
                 causal: bool = False, window: tuple[int, int] = (-1, -1), out=None,
                 lse=None, return_lse: bool = True, workspace=None, stream=None):
@@ -312,7 +365,8 @@ def fwd_splitkv(q, k, v, *, num_splits: int = 0, scale: float | None = None,
 
 
 __all__ = [
-    "LIB_PATH", "SIGNATURES", "FaError", "fwd", "fwd_varlen", "fwd_splitkv", "fa_fwd",
+    "LIB_PATH", "SIGNATURES", "FaError", "fwd", "bwd", "fwd_varlen", "fwd_splitkv", "fa_fwd",
+    "fa_bwd", "fa_bwd_workspace_bytes",
     "fa_fwd_ext", "fa_fwd_varlen",
     "fa_fwd_splitkv", "fa_splitkv_workspace_bytes", "fa_fwd_splitkv_noalloc",
     "fa_status_string",

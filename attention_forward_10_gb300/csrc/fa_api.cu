@@ -612,6 +612,95 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
   return launch_forward(c, o, lse, 1, 0);
 }
 
+int fa_bwd_workspace_bytes(int B, int H, int N, unsigned long long* bytes) {
+  if (bytes == nullptr) return FA_ERR_INVALID_ARG;
+  *bytes = 0;
+  if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID_ARG;
+  const unsigned long long n_pad = (static_cast<unsigned long long>(N) + 127ull) / 128ull * 128ull;
+  *bytes = 2ull * static_cast<unsigned long long>(B) * static_cast<unsigned long long>(H) * n_pad * 4ull;
+  return FA_OK;
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+           const void* dout, void* dq, void* dk, void* dv, void* workspace,
+           unsigned long long workspace_bytes, int B, int H, int H_kv, int N, int d,
+           float scale, int causal, int window_left, int window_right, int dtype,
+           void* stream) {
+  using namespace fa;
+  const ForwardCall c{q, k, v, dq, nullptr, B, H, H_kv, N, d, scale, causal, window_left,
+                      window_right, dtype, stream};
+  int st = validate(c);
+  if (st != FA_OK) return st;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (empty_problem(c)) return FA_OK;
+  st = check_pointers(c);
+  if (st != FA_OK) return st;
+  if (o == nullptr || lse == nullptr || dout == nullptr || dk == nullptr || dv == nullptr ||
+      workspace == nullptr)
+    return FA_ERR_INVALID_ARG;
+  if (!aligned(o, 16) || !aligned(dout, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
+      !aligned(lse, 4) || !aligned(workspace, 256))
+    return FA_ERR_MISALIGNED;
+  unsigned long long need = 0;
+  fa_bwd_workspace_bytes(B, H, N, &need);
+  if (workspace_bytes < need) return FA_ERR_INVALID_ARG;
+  const long long bh = static_cast<long long>(B) * H;
+  const long long n_tiles = (static_cast<long long>(N) + 127) / 128;
+  if (bh * n_tiles >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  DeviceInfo* info = device_info(dev);
+  if (info == nullptr || info->status == nullptr) return FA_ERR_CUDA;
+  if (!info->ok) return FA_ERR_UNSUPPORTED;
+  const bool bf16 = dtype == FA_DTYPE_BF16;
+  const int ibh = static_cast<int>(bh), ibkv = B * H_kv;
+  BwdParams p;
+  if (!encode_qkvo_map(&p.tm_q, q, N, d, ibh, bf16, 128, d / 64) ||
+      !encode_qkvo_map(&p.tm_k, k, N, d, ibkv, bf16, 128, d / 64) ||
+      !encode_qkvo_map(&p.tm_v, v, N, d, ibkv, bf16, 128, d / 64) ||
+      !encode_qkvo_map(&p.tm_do, dout, N, d, ibh, bf16, 128, d / 64))
+    return FA_ERR_CUDA;
+  const int n_pad = static_cast<int>(n_tiles * 128);
+  float* lse2 = static_cast<float*>(workspace);
+  float* dsum = lse2 + static_cast<long long>(ibh) * n_pad;
+  p.lse2 = lse2;
+  p.dsum = dsum;
+  p.dq = static_cast<uint16_t*>(dq);
+  p.dk = static_cast<uint16_t*>(dk);
+  p.dv = static_cast<uint16_t*>(dv);
+  p.status = info->status;
+  p.timeout_ns = g_timeout_ns.load();
+  p.N = N;
+  p.n_pad = n_pad;
+  p.n_tiles = static_cast<int>(n_tiles);
+  p.num_bh = ibh;
+  p.num_bkv = ibkv;
+  p.H = H;
+  p.H_kv = H_kv;
+  p.group = H / H_kv;
+  p.win_left = (window_left < 0 || window_left > N) ? N : window_left;
+  p.win_right = (window_right < 0 || window_right > N) ? N : window_right;
+  if (causal) p.win_right = 0;
+  p.scale = scale;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  BwdParams p_kv = p, p_q = p;
+  p_kv.num_units = static_cast<int>(static_cast<long long>(ibkv) * n_tiles);
+  p_q.num_units = static_cast<int>(bh * n_tiles);
+  int grid = info->num_sms;
+  const int cap = g_max_ctas.load();
+  if (cap > 0 && cap < grid) grid = cap;
+  const int grid_kv = p_kv.num_units < grid ? p_kv.num_units : grid;
+  const int grid_q = p_q.num_units < grid ? p_q.num_units : grid;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e =
+      (d == 64) ? launch_bwd_d64(p_kv, p_q, o, dout, lse, lse2, dsum, causal != 0, bf16, grid_kv,
+                                 grid_q, info->num_sms, s)
+                : launch_bwd_d128(p_kv, p_q, o, dout, lse, lse2, dsum, causal != 0, bf16,
+                                  grid_kv, grid_q, info->num_sms, s);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 int fa_get_device_status(void* stream, int* site) {
   using namespace fa;
   if (site != nullptr) *site = 0;

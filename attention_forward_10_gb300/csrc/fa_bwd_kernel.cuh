@@ -1,0 +1,645 @@
+// fa_bwd_kernel.cuh -- attention backward (dQ, dK, dV) for sm_103a, d <= 128.
+//
+// What is computed (flash-attention "hopper/mainloop_bwd_sm90_tma_gmma_ws.hpp",
+// CollectiveMainloopBwd::mma, with its LSE in natural-log units here):
+//   P_ij  = exp(s_ij - LSE_i)         (s = scale Q K^T, masked entries 0)
+//   dP_ij = dO_i . v_j,   D_i = rowsum(dO_i * O_i)  (the page's dPsum)
+//   dS_ij = P_ij (dP_ij - D_i)
+//   dV = P^T dO,   dK = scale dS^T Q,   dQ = scale dS K
+//
+// Two kernels and no atomics, so every gradient is deterministic:
+//   * dK/dV kernel: a work unit is one 128-key tile of one K/V head; it loops
+//     over the query tiles (and, for grouped heads, the query heads) that
+//     can see those keys, computing S^T = K Q^T and dP^T = V dO^T with one
+//     key per tensor-memory lane, so that P^T and dS^T are the A operands of
+//     dV += P^T dO and dK += dS^T Q straight from tensor memory.
+//   * dQ kernel: a work unit is one 128-row query tile; it loops over the
+//     key tiles that row tile sees, computing S = Q K^T and dP = dO V^T (one
+//     query per lane) and dQ += dS K.
+// A pre-pass writes -LSE_i * log2(e) and -D_i into a workspace padded to
+// whole 128-row tiles (padding: -inf and 0, so padded query rows get P = 0).
+//
+// Warp roles (320 threads): warps 0-7 compute P and dS, one tensor-memory
+// lane (row) per thread, warps 0-3 for the first 64 columns of a tile and
+// warps 4-7 for the last 64, and split the epilogue the same way; warp 8
+// issues TMA copies; warp 9 issues the MMAs.  Tensor memory, columns:
+// [0,128) S, [128,256) dP, then the fp32 accumulators: dV and dK (dK/dV
+// kernel) or dQ (dQ kernel), D columns each.  Each column half writes its
+// 16-bit P (or dS) packed over the first 32 of its own 64 S (or dP) columns,
+// so the P V-style products take their A operand in two 64-key pieces.  As in the forward kernels, an MMA that
+// overwrites columns an earlier MMA reads as its A operand is issued right
+// behind it without a completion wait (the tensor pipe runs one CTA's MMAs in
+// issue order).  Every mbarrier wait is bounded.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "fa_common.cuh"
+#include "fa_params.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace bwd {
+
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kEwThreads = 256;  // warps 0-7
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0, kColDP = 128, kColAcc = 256;
+
+// Shared memory layout of both kernels: two 128-row tiles that stay for the
+// whole unit (K,V or Q,dO), a 2-stage ring of the two streamed tiles, and
+// per stage 128 LSE2 and 128 D values (dK/dV kernel).
+template <int D>
+struct Layout {
+  static_assert(D == 64 || D == 128, "head dim");
+  static constexpr uint32_t kTile = 128 * D * 2;
+  static constexpr int kStages = 2;
+  static constexpr uint32_t kFixOff = 0;                       // 2 tiles
+  static constexpr uint32_t kRingOff = 2 * kTile;              // stage s: 2 tiles
+  static constexpr uint32_t kVecOff = kRingOff + kStages * 2 * kTile;  // stage s: 1 KB
+  static constexpr uint32_t kBarOff = kVecOff + kStages * 1024;
+  // barriers
+  static constexpr int kFixFull = 0, kFixEmpty = 1;
+  static constexpr int kRingFull = 2;   // + stage
+  static constexpr int kRingEmpty = 4;  // + stage
+  static constexpr int kSFull = 6, kPReady = 7, kAccDone = 8, kAccFree = 9, kDrain = 10;
+  static constexpr int kNumBars = 11;
+  static constexpr uint32_t kCtlOff = kBarOff + kNumBars * 8;
+  static constexpr uint32_t kSmemBytes = kCtlOff + 16 + 1024;
+  static_assert(kSmemBytes <= 232448, "exceeds the shared memory of one CTA");
+};
+
+// Masks of the backward: key j is admissible for query i when
+// i - win_left <= j <= i + win_right (causal: win_right = 0), both < N.
+__device__ __forceinline__ bool admissible(int i, int j, int N, int wl, int wr) {
+  return j < N && i < N && j <= i + wr && j >= i - wl;
+}
+
+// ---------------------------------------------------------------- pre-pass
+// nlse2[bh][i] = -LSE * log2(e) and ndsum[bh][i] = -sum_c dO[i][c] O[i][c]
+// for i < N; -inf and 0 for the padding rows up to n_pad.  d/8 threads per
+// row.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256)
+    fa_bwd_prepass_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
+                          const float* __restrict__ lse, float* __restrict__ lse2,
+                          float* __restrict__ dsum, int num_bh, int N, int n_pad) {
+  constexpr int kTpr = D / 8;
+  const long long rows = static_cast<long long>(num_bh) * n_pad;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  // every lane runs the same number of iterations (the shuffles need all)
+  const long long total = (rows * kTpr + 31) / 32 * 32;
+  for (long long gid = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+       gid < total; gid += stride) {
+    const long long r = gid / kTpr;
+    const int part = static_cast<int>(gid % kTpr);
+    const bool live = r < rows;
+    const int bh = live ? static_cast<int>(r / n_pad) : 0;
+    const int i = live ? static_cast<int>(r % n_pad) : N;
+    float acc = 0.f;
+    if (i < N) {
+      const long long off = (static_cast<long long>(bh) * N + i) * D + part * 8;
+      const uint4 a = *reinterpret_cast<const uint4*>(o + off);
+      const uint4 b = *reinterpret_cast<const uint4*>(dout + off);
+      const uint32_t wa[4] = {a.x, a.y, a.z, a.w};
+      const uint32_t wb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        acc += unpack_lo<BF16>(wa[e]) * unpack_lo<BF16>(wb[e]);
+        acc += unpack_hi<BF16>(wa[e]) * unpack_hi<BF16>(wb[e]);
+      }
+    }
+#pragma unroll
+    for (int off = kTpr / 2; off > 0; off /= 2) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (live && part == 0) {
+      lse2[r] = (i < N) ? lse[static_cast<long long>(bh) * N + i] * -1.4426950408889634f
+                        : -INFINITY;
+      dsum[r] = -acc;
+    }
+  }
+}
+
+// P and dS for one 64-column half of a tile, one row per thread:
+//   p  = 2^(s * scale_log2 + nlse2),   ds = p * (dp + ndsum)
+// (nlse2 = -LSE log2 e, ndsum = -D per column in the dK/dV kernel, per row in
+// the dQ kernel), in two 32-column steps whose S and dP columns (at tS + c,
+// tDP + c) arrive with one wait each; P (when WRITE_P) goes packed to tS + c
+// and dS to `tds`, over columns already read.  `keep(e)` is the mask of
+// column c + e (only called when MASK).
+template <bool BF16, bool MASK, bool WRITE_P, bool COLUMN_VECS, typename Keep>
+__device__ __forceinline__ void p_ds_half(uint32_t tS, uint32_t tDP, uint32_t tds, int c,
+                                          float sl2, const float* nlse2, const float* ndsum,
+                                          float nlse2_row, float ndsum_row, Keep keep) {
+  const uint64_t sl2x2 = pack_f32x2(sl2, sl2);
+  const uint64_t zero2 = pack_f32x2(0.f, 0.f);
+#pragma unroll 1
+  for (int q = 0; q < 64; q += 32) {
+    uint32_t sr[32], dpr[32];
+    tmem_ld_2x32_sync(tS + c + q, sr, tDP + c + q, dpr);
+    uint32_t pk[16], dk[16];
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      const int col = c + q + e;
+      const uint64_t nl = COLUMN_VECS ? *reinterpret_cast<const uint64_t*>(nlse2 + col)
+                                      : pack_f32x2(nlse2_row, nlse2_row);
+      const uint64_t nd = COLUMN_VECS ? *reinterpret_cast<const uint64_t*>(ndsum + col)
+                                      : pack_f32x2(ndsum_row, ndsum_row);
+      float x0, x1;
+      unpack_f32x2(fma_f32x2(pack_f32x2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
+                             sl2x2, nl),
+                   x0, x1);
+      float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+      if (MASK) {
+        if (!keep(q + e)) p0 = 0.f;
+        if (!keep(q + e + 1)) p1 = 0.f;
+      }
+      const uint64_t pp = pack_f32x2(p0, p1);
+      const uint64_t t = add_f32x2(
+          pack_f32x2(__uint_as_float(dpr[e]), __uint_as_float(dpr[e + 1])), nd);
+      float d0, d1;
+      unpack_f32x2(fma_f32x2(pp, t, zero2), d0, d1);
+      if (WRITE_P) pk[e / 2] = pack2<BF16>(p0, p1);
+      dk[e / 2] = pack2<BF16>(d0, d1);
+    }
+    if (WRITE_P) tmem_st_x16(tS + c + q / 2, pk);
+    tmem_st_x16(tds + q / 2, dk);
+  }
+}
+
+// ---------------------------------------------------------- dK / dV kernel
+struct KvUnit {
+  int bkv;        // K/V head (b * H_kv + h_kv)
+  int n;          // key tile
+  int m_lo, nm;   // query tiles [m_lo, m_lo + nm) per query head
+  int steps;      // group * nm
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ KvUnit decode_kv_unit(int u, const BwdParams& p) {
+  KvUnit w;
+  if (CAUSAL) {
+    // heaviest first: the first key tiles see the most query tiles
+    w.n = u / p.num_bkv;
+    w.bkv = u % p.num_bkv;
+  } else {
+    w.bkv = u / p.n_tiles;
+    w.n = u % p.n_tiles;
+  }
+  const long long lo = static_cast<long long>(w.n) * 128 - p.win_right;
+  const long long hi = static_cast<long long>(w.n) * 128 + 128 + p.win_left;  // exclusive
+  const int row_lo = lo < 0 ? 0 : static_cast<int>(lo);
+  const int row_hi = hi > p.N ? p.N : static_cast<int>(hi);
+  w.m_lo = row_lo / 128;
+  w.nm = row_hi > row_lo ? (row_hi + 127) / 128 - w.m_lo : 0;
+  w.steps = p.group * w.nm;
+  return w;
+}
+
+template <int D, bool CAUSAL, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
+  using L = Layout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  auto bar = [&](int i) -> uint32_t { return sbase + L::kBarOff + 8u * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kCtlOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kCtlOff + 4);
+  const Ctl ctl{abort_flag, p.status, p.timeout_ns};
+  constexpr uint32_t kKOff = L::kFixOff, kVOff = L::kFixOff + L::kTile;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(L::kFixFull), 1);
+    mbar_init(bar(L::kFixEmpty), 1);
+    for (int s = 0; s < L::kStages; ++s) {
+      mbar_init(bar(L::kRingFull + s), 1);
+      mbar_init(bar(L::kRingEmpty + s), 1);
+    }
+    mbar_init(bar(L::kSFull), 1);
+    mbar_init(bar(L::kPReady), kEwThreads);
+    mbar_init(bar(L::kAccDone), 1);
+    mbar_init(bar(L::kAccFree), kEwThreads);
+    mbar_init(bar(L::kDrain), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    tma_prefetch_map(&p.tm_q);
+    tma_prefetch_map(&p.tm_k);
+    tma_prefetch_map(&p.tm_v);
+    tma_prefetch_map(&p.tm_do);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kProducerWarp) {
+    // ---------------------------------------------------------------- TMA
+    if (lane == 0) {
+      uint32_t it = 0, units = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++units) {
+        const KvUnit w = decode_kv_unit<CAUSAL>(u, p);
+        ok = wait_bar(bar(L::kFixEmpty), (units & 1u) ^ 1u, ctl, kSiteProducerKV);
+        if (!ok) break;
+        mbar_arrive_expect_tx(bar(L::kFixFull), 2 * L::kTile);
+        tma_load_4d(sbase + kKOff, &p.tm_k, bar(L::kFixFull), 0, w.n * 128, 0, w.bkv);
+        tma_load_4d(sbase + kVOff, &p.tm_v, bar(L::kFixFull), 0, w.n * 128, 0, w.bkv);
+        const int b = w.bkv / p.H_kv, hk = w.bkv % p.H_kv;
+        for (int s = 0; s < w.steps && ok; ++s, ++it) {
+          const int bh = b * p.H + hk * p.group + s / w.nm;
+          const int m = w.m_lo + s % w.nm;
+          const uint32_t st = it % L::kStages;
+          ok = wait_bar(bar(L::kRingEmpty + st), ((it / L::kStages) & 1u) ^ 1u, ctl,
+                        kSiteProducerQ);
+          if (!ok) break;
+          const uint32_t ring = sbase + L::kRingOff + st * 2 * L::kTile;
+          const uint32_t vec = sbase + L::kVecOff + st * 1024;
+          mbar_arrive_expect_tx(bar(L::kRingFull + st), 2 * L::kTile + 1024);
+          tma_load_4d(ring, &p.tm_q, bar(L::kRingFull + st), 0, m * 128, 0, bh);
+          tma_load_4d(ring + L::kTile, &p.tm_do, bar(L::kRingFull + st), 0, m * 128, 0, bh);
+          const long long voff = static_cast<long long>(bh) * p.n_pad + m * 128;
+          bulk_load_1d(vec, p.lse2 + voff, 512, bar(L::kRingFull + st));
+          bulk_load_1d(vec + 512, p.dsum + voff, 512, bar(L::kRingFull + st));
+        }
+      }
+      // let the copies in flight land before the CTA may exit
+      const uint32_t first = it > (uint32_t)L::kStages ? it - L::kStages : 0u;
+      for (uint32_t j = first; j < it; ++j)
+        wait_drain(bar(L::kRingFull + j % L::kStages), (j / L::kStages) & 1u, p.timeout_ns);
+      if (units > 0) wait_drain(bar(L::kFixFull), (units - 1) & 1u, p.timeout_ns);
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------------- MMA
+    if (lane == 0) {
+      constexpr uint32_t kIdescS = make_idesc_f16(128, 128, BF16, false);
+      constexpr uint32_t kIdescAcc = make_idesc_f16(128, D, BF16, true);
+      const uint64_t k_desc = smem_desc_sw128(sbase + kKOff, 16, 1024);
+      const uint64_t v_desc = smem_desc_sw128(sbase + kVOff, 16, 1024);
+      uint32_t it = 0, units = 0, pr = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++units) {
+        const KvUnit w = decode_kv_unit<CAUSAL>(u, p);
+        ok = wait_bar(bar(L::kFixFull), units & 1u, ctl, kSiteMmaK);
+        if (!ok) break;
+        for (int s = 0; s < w.steps; ++s, ++it) {
+          const uint32_t st = it % L::kStages;
+          ok = wait_bar(bar(L::kRingFull + st), (it / L::kStages) & 1u, ctl, kSiteMmaQ);
+          if (!ok) break;
+          tc_fence_after_sync();
+          const uint32_t ring = sbase + L::kRingOff + st * 2 * L::kTile;
+          const uint64_t q_kdesc = smem_desc_sw128(ring, 16, 1024);
+          const uint64_t do_kdesc = smem_desc_sw128(ring + L::kTile, 16, 1024);
+          // S^T = K Q^T and dP^T = V dO^T (keys on the lanes)
+          if constexpr (D == 128) {
+            mma_ss_kmajor_x8(tmem + kColS, k_desc, q_kdesc, kIdescS, 0u);
+            mma_ss_kmajor_x8(tmem + kColDP, v_desc, do_kdesc, kIdescS, 0u);
+          } else {
+            mma_ss_kmajor_x4(tmem + kColS, k_desc, q_kdesc, kIdescS, 0u);
+            mma_ss_kmajor_x4(tmem + kColDP, v_desc, do_kdesc, kIdescS, 0u);
+          }
+          tc_commit(bar(L::kSFull));
+          ok = wait_bar(bar(L::kPReady), pr, ctl, kSiteMmaP);
+          pr ^= 1u;
+          if (!ok) break;
+          if (s == 0 && units > 0) {
+            // the previous unit's dK, dV must have been read out
+            ok = wait_bar(bar(L::kAccFree), (units - 1) & 1u, ctl, kSiteMmaO);
+            if (!ok) break;
+          }
+          tc_fence_after_sync();
+          // dV += P^T dO and dK += dS^T Q (dO, Q as MN-major B operands)
+          const uint64_t do_mdesc = smem_desc_sw128(ring + L::kTile, 128 * 128, 1024);
+          const uint64_t q_mdesc = smem_desc_sw128(ring, 128 * 128, 1024);
+          // (P^T and dS^T of queries 0-63 at columns +0, of 64-127 at +64;
+          //  the second half of dO / Q is 64 rows = 512 descriptor units on)
+          mma_ts_mnmajor_x4(tmem + kColAcc, tmem + kColS, do_mdesc, kIdescAcc, s > 0 ? 1u : 0u);
+          mma_ts_mnmajor_x4(tmem + kColAcc, tmem + kColS + 64, do_mdesc + 512, kIdescAcc, 1u);
+          mma_ts_mnmajor_x4(tmem + kColAcc + D, tmem + kColDP, q_mdesc, kIdescAcc,
+                            s > 0 ? 1u : 0u);
+          mma_ts_mnmajor_x4(tmem + kColAcc + D, tmem + kColDP + 64, q_mdesc + 512, kIdescAcc, 1u);
+          tc_commit(bar(L::kRingEmpty + st));
+        }
+        if (!ok) break;
+        tc_commit(bar(L::kAccDone));
+        tc_commit(bar(L::kFixEmpty));
+      }
+      tc_commit(bar(L::kDrain));
+      wait_drain(bar(L::kDrain), 0, p.timeout_ns);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------ P^T, dS^T and the epilogue
+    const int half = warp / 4;                 // query columns [64 half, +64)
+    const int t = (warp % 4) * 32 + lane;      // key row within the tile == lane
+    const uint32_t lane_base = static_cast<uint32_t>((warp % 4) * 32) << 16;
+    const uint32_t tS = tmem + lane_base + kColS;
+    const uint32_t tDP = tmem + lane_base + kColDP;
+    const int c = half * 64;
+    const float sl2 = p.scale_log2;
+    uint32_t it = 0, units = 0, sf = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++units) {
+      const KvUnit w = decode_kv_unit<CAUSAL>(u, p);
+      const int j = w.n * 128 + t;  // this thread's key
+      for (int s = 0; s < w.steps; ++s, ++it) {
+        const uint32_t st = it % L::kStages;
+        const int m = w.m_lo + s % w.nm;
+        ok = wait_bar(bar(L::kRingFull + st), (it / L::kStages) & 1u, ctl, kSiteSoftmaxS);
+        ok = ok && wait_bar(bar(L::kSFull), sf, ctl, kSiteSoftmaxS);
+        sf ^= 1u;
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after_sync();
+        const float* nlse2 = reinterpret_cast<const float*>(smem + L::kVecOff + st * 1024);
+        const float* ndsum = nlse2 + 128;
+        const int i0 = m * 128 + c;  // query of column c
+        const bool need_mask = (w.n * 128 + 127 - i0 > p.win_right) ||
+                               (w.n * 128 - (i0 + 63) < -p.win_left) || (w.n * 128 + 128 > p.N);
+        const int N = p.N, wl = p.win_left, wr = p.win_right;
+        auto keep = [&](int e) { return admissible(i0 + e, j, N, wl, wr); };
+        if (need_mask)
+          p_ds_half<BF16, true, true, true>(tS, tDP, tDP + c, c, sl2, nlse2, ndsum, 0.f, 0.f, keep);
+        else
+          p_ds_half<BF16, false, true, true>(tS, tDP, tDP + c, c, sl2, nlse2, ndsum, 0.f, 0.f,
+                                             keep);
+        tmem_wait_st();
+        tc_fence_before_sync();
+        mbar_arrive(bar(L::kPReady));
+      }
+      if (!ok) break;
+      // ---- epilogue: warps 0-3 write dV, warps 4-7 scale * dK (this thread's key row)
+      ok = wait_bar(bar(L::kAccDone), units & 1u, ctl, kSiteEpilogueO);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after_sync();
+      const long long row = static_cast<long long>(w.bkv) * p.N + j;
+      uint16_t* dst = (half == 0 ? p.dv : p.dk) + row * D;
+      const float mul = half == 0 ? 1.f : p.scale;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld_x32_sync(tmem + lane_base + kColAcc + half * D + c0, r);
+        uint32_t w4[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          w4[e] = pack2<BF16>(__uint_as_float(r[2 * e]) * mul, __uint_as_float(r[2 * e + 1]) * mul);
+        if (j < p.N) {
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4)
+            *reinterpret_cast<uint4*>(dst + c0 + q4 * 8) =
+                make_uint4(w4[4 * q4], w4[4 * q4 + 1], w4[4 * q4 + 2], w4[4 * q4 + 3]);
+        }
+      }
+      tc_fence_before_sync();
+      mbar_arrive(bar(L::kAccFree));
+    }
+    (void)it;
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// --------------------------------------------------------------- dQ kernel
+struct QUnit {
+  int bh;      // query head
+  int bkv;     // its K/V head
+  int m;       // query tile
+  int n0, n1;  // key tiles [n0, n1)
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ QUnit decode_q_unit(int u, const BwdParams& p) {
+  QUnit w;
+  if (CAUSAL) {
+    w.m = p.n_tiles - 1 - u / p.num_bh;  // heaviest first
+    w.bh = u % p.num_bh;
+  } else {
+    w.bh = u / p.n_tiles;
+    w.m = u % p.n_tiles;
+  }
+  w.bkv = kv_head(w.bh, p.H, p.group);
+  key_tile_range(w.m * 128, min(p.N, w.m * 128 + 128), p.N, p.win_left, p.win_right, 128,
+                 &w.n0, &w.n1);
+  return w;
+}
+
+template <int D, bool CAUSAL, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
+  using L = Layout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  auto bar = [&](int i) -> uint32_t { return sbase + L::kBarOff + 8u * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kCtlOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kCtlOff + 4);
+  const Ctl ctl{abort_flag, p.status, p.timeout_ns};
+  constexpr uint32_t kQOff = L::kFixOff, kDOOff = L::kFixOff + L::kTile;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(L::kFixFull), 1);
+    mbar_init(bar(L::kFixEmpty), 1);
+    for (int s = 0; s < L::kStages; ++s) {
+      mbar_init(bar(L::kRingFull + s), 1);
+      mbar_init(bar(L::kRingEmpty + s), 1);
+    }
+    mbar_init(bar(L::kSFull), 1);
+    mbar_init(bar(L::kPReady), kEwThreads);
+    mbar_init(bar(L::kAccDone), 1);
+    mbar_init(bar(L::kAccFree), kEwThreads);
+    mbar_init(bar(L::kDrain), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    tma_prefetch_map(&p.tm_q);
+    tma_prefetch_map(&p.tm_k);
+    tma_prefetch_map(&p.tm_v);
+    tma_prefetch_map(&p.tm_do);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kProducerWarp) {
+    // ---------------------------------------------------------------- TMA
+    if (lane == 0) {
+      uint32_t it = 0, units = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++units) {
+        const QUnit w = decode_q_unit<CAUSAL>(u, p);
+        ok = wait_bar(bar(L::kFixEmpty), (units & 1u) ^ 1u, ctl, kSiteProducerQ);
+        if (!ok) break;
+        mbar_arrive_expect_tx(bar(L::kFixFull), 2 * L::kTile);
+        tma_load_4d(sbase + kQOff, &p.tm_q, bar(L::kFixFull), 0, w.m * 128, 0, w.bh);
+        tma_load_4d(sbase + kDOOff, &p.tm_do, bar(L::kFixFull), 0, w.m * 128, 0, w.bh);
+        for (int n = w.n0; n < w.n1 && ok; ++n, ++it) {
+          const uint32_t st = it % L::kStages;
+          ok = wait_bar(bar(L::kRingEmpty + st), ((it / L::kStages) & 1u) ^ 1u, ctl,
+                        kSiteProducerKV);
+          if (!ok) break;
+          const uint32_t ring = sbase + L::kRingOff + st * 2 * L::kTile;
+          mbar_arrive_expect_tx(bar(L::kRingFull + st), 2 * L::kTile);
+          tma_load_4d(ring, &p.tm_k, bar(L::kRingFull + st), 0, n * 128, 0, w.bkv);
+          tma_load_4d(ring + L::kTile, &p.tm_v, bar(L::kRingFull + st), 0, n * 128, 0, w.bkv);
+        }
+      }
+      const uint32_t first = it > (uint32_t)L::kStages ? it - L::kStages : 0u;
+      for (uint32_t j = first; j < it; ++j)
+        wait_drain(bar(L::kRingFull + j % L::kStages), (j / L::kStages) & 1u, p.timeout_ns);
+      if (units > 0) wait_drain(bar(L::kFixFull), (units - 1) & 1u, p.timeout_ns);
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------------- MMA
+    if (lane == 0) {
+      constexpr uint32_t kIdescS = make_idesc_f16(128, 128, BF16, false);
+      constexpr uint32_t kIdescAcc = make_idesc_f16(128, D, BF16, true);
+      const uint64_t q_desc = smem_desc_sw128(sbase + kQOff, 16, 1024);
+      const uint64_t do_desc = smem_desc_sw128(sbase + kDOOff, 16, 1024);
+      uint32_t it = 0, units = 0, pr = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++units) {
+        const QUnit w = decode_q_unit<CAUSAL>(u, p);
+        ok = wait_bar(bar(L::kFixFull), units & 1u, ctl, kSiteMmaQ);
+        if (!ok) break;
+        for (int n = w.n0; n < w.n1; ++n, ++it) {
+          const uint32_t st = it % L::kStages;
+          ok = wait_bar(bar(L::kRingFull + st), (it / L::kStages) & 1u, ctl, kSiteMmaK);
+          if (!ok) break;
+          tc_fence_after_sync();
+          const uint32_t ring = sbase + L::kRingOff + st * 2 * L::kTile;
+          const uint64_t k_kdesc = smem_desc_sw128(ring, 16, 1024);
+          const uint64_t v_kdesc = smem_desc_sw128(ring + L::kTile, 16, 1024);
+          // S = Q K^T and dP = dO V^T (queries on the lanes)
+          if constexpr (D == 128) {
+            mma_ss_kmajor_x8(tmem + kColS, q_desc, k_kdesc, kIdescS, 0u);
+            mma_ss_kmajor_x8(tmem + kColDP, do_desc, v_kdesc, kIdescS, 0u);
+          } else {
+            mma_ss_kmajor_x4(tmem + kColS, q_desc, k_kdesc, kIdescS, 0u);
+            mma_ss_kmajor_x4(tmem + kColDP, do_desc, v_kdesc, kIdescS, 0u);
+          }
+          tc_commit(bar(L::kSFull));
+          if (n == w.n1 - 1) tc_commit(bar(L::kFixEmpty));  // Q and dO read for the last time
+          ok = wait_bar(bar(L::kPReady), pr, ctl, kSiteMmaP);
+          pr ^= 1u;
+          if (!ok) break;
+          if (n == w.n0 && units > 0) {
+            ok = wait_bar(bar(L::kAccFree), (units - 1) & 1u, ctl, kSiteMmaO);
+            if (!ok) break;
+          }
+          tc_fence_after_sync();
+          // dQ += dS K (K as the MN-major B operand)
+          const uint64_t k_mdesc = smem_desc_sw128(ring, 128 * 128, 1024);
+          mma_ts_mnmajor_x4(tmem + kColAcc, tmem + kColS, k_mdesc, kIdescAcc,
+                            n > w.n0 ? 1u : 0u);
+          mma_ts_mnmajor_x4(tmem + kColAcc, tmem + kColS + 64, k_mdesc + 512, kIdescAcc, 1u);
+          tc_commit(bar(L::kRingEmpty + st));
+        }
+        if (!ok) break;
+        tc_commit(bar(L::kAccDone));
+      }
+      tc_commit(bar(L::kDrain));
+      wait_drain(bar(L::kDrain), 0, p.timeout_ns);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------ dS and the epilogue
+    const int half = warp / 4;              // key columns [64 half, +64)
+    const int t = (warp % 4) * 32 + lane;   // query row within the tile == lane
+    const uint32_t lane_base = static_cast<uint32_t>((warp % 4) * 32) << 16;
+    const uint32_t tS = tmem + lane_base + kColS;
+    const uint32_t tDP = tmem + lane_base + kColDP;
+    const int c = half * 64;
+    const float sl2 = p.scale_log2;
+    uint32_t units = 0, sf = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++units) {
+      const QUnit w = decode_q_unit<CAUSAL>(u, p);
+      const int i = w.m * 128 + t;
+      const long long vrow = static_cast<long long>(w.bh) * p.n_pad + i;
+      const float nlse2 = p.lse2[vrow];
+      const float ndsum = p.dsum[vrow];
+      const int row_end = min(p.N, w.m * 128 + 128);
+      for (int n = w.n0; n < w.n1; ++n) {
+        ok = wait_bar(bar(L::kSFull), sf, ctl, kSiteSoftmaxS);
+        sf ^= 1u;
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after_sync();
+        const int kbase = n * 128 + c;  // key of column c
+        const bool need_mask = (kbase + 64 > p.N) || (kbase + 63 > w.m * 128 + p.win_right) ||
+                               (kbase < row_end - 1 - p.win_left);
+        const int N = p.N, wl = p.win_left, wr = p.win_right;
+        auto keep = [&](int e) { return admissible(i, kbase + e, N, wl, wr); };
+        if (need_mask)
+          p_ds_half<BF16, true, false, false>(tS, tDP, tS + c, c, sl2, nullptr, nullptr, nlse2,
+                                              ndsum, keep);
+        else
+          p_ds_half<BF16, false, false, false>(tS, tDP, tS + c, c, sl2, nullptr, nullptr, nlse2,
+                                               ndsum, keep);
+        tmem_wait_st();
+        tc_fence_before_sync();
+        mbar_arrive(bar(L::kPReady));
+      }
+      if (!ok) break;
+      // ---- epilogue: scale * dQ, columns [D/2 half, +D/2) of this thread's row
+      ok = wait_bar(bar(L::kAccDone), units & 1u, ctl, kSiteEpilogueO);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after_sync();
+      uint16_t* dst = p.dq + (static_cast<long long>(w.bh) * p.N + i) * D + half * (D / 2);
+#pragma unroll 1
+      for (int c0 = 0; c0 < D / 2; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld_x32_sync(tmem + lane_base + kColAcc + half * (D / 2) + c0, r);
+        uint32_t w4[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          w4[e] = pack2<BF16>(__uint_as_float(r[2 * e]) * p.scale,
+                              __uint_as_float(r[2 * e + 1]) * p.scale);
+        if (i < p.N) {
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4)
+            *reinterpret_cast<uint4*>(dst + c0 + q4 * 8) =
+                make_uint4(w4[4 * q4], w4[4 * q4 + 1], w4[4 * q4 + 2], w4[4 * q4 + 3]);
+        }
+      }
+      tc_fence_before_sync();
+      mbar_arrive(bar(L::kAccFree));
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace bwd
+}  // namespace fa

@@ -27,6 +27,19 @@ cudaError_t launch_fwd_d128_packed(const FaParams& p, bool causal, bool bf16, in
 cudaError_t launch_fwd_d256_packed(const FaParams& p, bool causal, bool bf16, int grid,
                                    cudaStream_t stream);
 
+// Backward: the pre-pass (LSE * log2 e and rowsum(dO * O) into the padded
+// workspace), then the dK/dV and dQ kernels, all on `stream`.
+// p_kv / p_q: the parameters of the dK/dV and dQ kernels (their unit counts
+// differ); grid_kv / grid_q their persistent grids.
+cudaError_t launch_bwd_d64(const BwdParams& p_kv, const BwdParams& p_q, const void* o,
+                           const void* dout, const float* lse, float* lse2, float* dsum,
+                           bool causal, bool bf16, int grid_kv, int grid_q, int num_sms,
+                           cudaStream_t stream);
+cudaError_t launch_bwd_d128(const BwdParams& p_kv, const BwdParams& p_q, const void* o,
+                            const void* dout, const float* lse, float* lse2, float* dsum,
+                            bool causal, bool bf16, int grid_kv, int grid_q, int num_sms,
+                            cudaStream_t stream);
+
 // Shape of a split-KV merge: num_bh heads of N rows of d columns; split s
 // holds keys [s * split_keys, (s + 1) * split_keys); query i may see keys
 // i - win_left .. i + win_right (both already clamped to [0, N]).

@@ -72,6 +72,27 @@ __host__ __device__ inline void clip_to_split(int s, int split_tiles, int* n0, i
   if (*n1 < *n0) *n1 = *n0;
 }
 
+// Launch parameters of the backward kernels ([B][H][N][d] layout, d <= 128).
+struct BwdParams {  // 64-byte aligned through CUtensorMap
+  CUtensorMap tm_q;   // {64, N, d/64, B*H}, box {64, 128, d/64, 1}
+  CUtensorMap tm_k;   // {64, N, d/64, B*H_kv}
+  CUtensorMap tm_v;
+  CUtensorMap tm_do;  // like tm_q
+  const float* lse2;  // [B*H][n_pad]: -LSE * log2(e); -inf on padding rows
+  const float* dsum;  // [B*H][n_pad]: -rowsum(dO * O); 0 on padding rows
+  uint16_t* dq;       // [B*H][N][d]
+  uint16_t* dk;       // [B*H_kv][N][d]
+  uint16_t* dv;
+  int* status;
+  unsigned long long timeout_ns;
+  int N, n_pad, n_tiles;  // rows, rows rounded up to 128, 128-row tiles
+  int num_bh, num_bkv;    // B*H, B*H_kv
+  int num_units;          // work units of the launched kernel
+  int H, H_kv, group;
+  int win_left, win_right;  // clamped to [0, N]; win_right = 0 when causal
+  float scale, scale_log2;
+};
+
 // Rows of one (b, h) attention problem: its sequence's first packed row, its
 // length, and the head coordinates of its Q, O and K/V in the tensor maps.
 struct SeqView {

@@ -118,6 +118,17 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
 }
 
 // 4-D tiled store shared -> global (bulk-group completion).
+// 1-D bulk copy global -> shared, completing `bytes` on mbarrier `bar`
+// (both addresses 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint32_t bytes,
+                                             uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      :
+      : "r"(dst), "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_store_4d(const void* map, uint32_t src, int c0, int c1,
                                              int c2, int c3) {
   asm volatile(
@@ -505,6 +516,24 @@ __device__ __forceinline__ float ex2_approx(float x) {
 
 // Pack two floats (round to nearest even) into one 32-bit word: `lo` in the
 // low half, `hi` in the high half.
+// The low / high 16-bit element of a packed pair, widened to fp32 (exact).
+template <bool BF16>
+__device__ __forceinline__ float unpack_lo(uint32_t w) {
+  if constexpr (BF16) return __uint_as_float(w << 16);
+  float f;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.f32.f16 %0, lo;\n\t}"
+      : "=f"(f) : "r"(w));
+  return f;
+}
+template <bool BF16>
+__device__ __forceinline__ float unpack_hi(uint32_t w) {
+  if constexpr (BF16) return __uint_as_float(w & 0xffff0000u);
+  float f;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.f32.f16 %0, hi;\n\t}"
+      : "=f"(f) : "r"(w));
+  return f;
+}
+
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   uint32_t r;
@@ -566,6 +595,34 @@ __device__ __forceinline__ void tmem_ld_x128_sync(uint32_t taddr, uint32_t* r) {
 }
 
 // Store 16 consecutive 32-bit TMEM columns of this thread's lane (32x32b).
+// 32 consecutive columns at `ta` into ra and 32 at `tb` into rb (this warp's
+// 32 lanes), with a single wait for both loads.
+__device__ __forceinline__ void tmem_ld_2x32_sync(uint32_t ta, uint32_t* ra, uint32_t tb,
+                                                  uint32_t* rb) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(ra[0]), "=r"(ra[1]), "=r"(ra[2]), "=r"(ra[3]), "=r"(ra[4]), "=r"(ra[5]), "=r"(ra[6]), "=r"(ra[7]), "=r"(ra[8]), "=r"(ra[9]), "=r"(ra[10]), "=r"(ra[11]), "=r"(ra[12]), "=r"(ra[13]), "=r"(ra[14]), "=r"(ra[15]), "=r"(ra[16]), "=r"(ra[17]), "=r"(ra[18]), "=r"(ra[19]), "=r"(ra[20]), "=r"(ra[21]), "=r"(ra[22]), "=r"(ra[23]), "=r"(ra[24]), "=r"(ra[25]), "=r"(ra[26]), "=r"(ra[27]), "=r"(ra[28]), "=r"(ra[29]), "=r"(ra[30]), "=r"(ra[31]), "=r"(rb[0]), "=r"(rb[1]), "=r"(rb[2]), "=r"(rb[3]), "=r"(rb[4]), "=r"(rb[5]), "=r"(rb[6]), "=r"(rb[7]), "=r"(rb[8]), "=r"(rb[9]), "=r"(rb[10]), "=r"(rb[11]), "=r"(rb[12]), "=r"(rb[13]), "=r"(rb[14]), "=r"(rb[15]), "=r"(rb[16]), "=r"(rb[17]), "=r"(rb[18]), "=r"(rb[19]), "=r"(rb[20]), "=r"(rb[21]), "=r"(rb[22]), "=r"(rb[23]), "=r"(rb[24]), "=r"(rb[25]), "=r"(rb[26]), "=r"(rb[27]), "=r"(rb[28]), "=r"(rb[29]), "=r"(rb[30]), "=r"(rb[31])
+      : "r"(ta), "r"(tb)
+      : "memory");
+}
+
+// 64 consecutive columns at `ta` into ra and 64 at `tb` into rb (this warp's
+// 32 lanes), with a single wait for all four loads.
+__device__ __forceinline__ void tmem_ld_2x64_sync(uint32_t ta, uint32_t* ra, uint32_t tb,
+                                                  uint32_t* rb) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%128];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%129];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95}, [%130];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%131];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(ra[0]), "=r"(ra[1]), "=r"(ra[2]), "=r"(ra[3]), "=r"(ra[4]), "=r"(ra[5]), "=r"(ra[6]), "=r"(ra[7]), "=r"(ra[8]), "=r"(ra[9]), "=r"(ra[10]), "=r"(ra[11]), "=r"(ra[12]), "=r"(ra[13]), "=r"(ra[14]), "=r"(ra[15]), "=r"(ra[16]), "=r"(ra[17]), "=r"(ra[18]), "=r"(ra[19]), "=r"(ra[20]), "=r"(ra[21]), "=r"(ra[22]), "=r"(ra[23]), "=r"(ra[24]), "=r"(ra[25]), "=r"(ra[26]), "=r"(ra[27]), "=r"(ra[28]), "=r"(ra[29]), "=r"(ra[30]), "=r"(ra[31]), "=r"(ra[32]), "=r"(ra[33]), "=r"(ra[34]), "=r"(ra[35]), "=r"(ra[36]), "=r"(ra[37]), "=r"(ra[38]), "=r"(ra[39]), "=r"(ra[40]), "=r"(ra[41]), "=r"(ra[42]), "=r"(ra[43]), "=r"(ra[44]), "=r"(ra[45]), "=r"(ra[46]), "=r"(ra[47]), "=r"(ra[48]), "=r"(ra[49]), "=r"(ra[50]), "=r"(ra[51]), "=r"(ra[52]), "=r"(ra[53]), "=r"(ra[54]), "=r"(ra[55]), "=r"(ra[56]), "=r"(ra[57]), "=r"(ra[58]), "=r"(ra[59]), "=r"(ra[60]), "=r"(ra[61]), "=r"(ra[62]), "=r"(ra[63]), "=r"(rb[0]), "=r"(rb[1]), "=r"(rb[2]), "=r"(rb[3]), "=r"(rb[4]), "=r"(rb[5]), "=r"(rb[6]), "=r"(rb[7]), "=r"(rb[8]), "=r"(rb[9]), "=r"(rb[10]), "=r"(rb[11]), "=r"(rb[12]), "=r"(rb[13]), "=r"(rb[14]), "=r"(rb[15]), "=r"(rb[16]), "=r"(rb[17]), "=r"(rb[18]), "=r"(rb[19]), "=r"(rb[20]), "=r"(rb[21]), "=r"(rb[22]), "=r"(rb[23]), "=r"(rb[24]), "=r"(rb[25]), "=r"(rb[26]), "=r"(rb[27]), "=r"(rb[28]), "=r"(rb[29]), "=r"(rb[30]), "=r"(rb[31]), "=r"(rb[32]), "=r"(rb[33]), "=r"(rb[34]), "=r"(rb[35]), "=r"(rb[36]), "=r"(rb[37]), "=r"(rb[38]), "=r"(rb[39]), "=r"(rb[40]), "=r"(rb[41]), "=r"(rb[42]), "=r"(rb[43]), "=r"(rb[44]), "=r"(rb[45]), "=r"(rb[46]), "=r"(rb[47]), "=r"(rb[48]), "=r"(rb[49]), "=r"(rb[50]), "=r"(rb[51]), "=r"(rb[52]), "=r"(rb[53]), "=r"(rb[54]), "=r"(rb[55]), "=r"(rb[56]), "=r"(rb[57]), "=r"(rb[58]), "=r"(rb[59]), "=r"(rb[60]), "=r"(rb[61]), "=r"(rb[62]), "=r"(rb[63])
+      : "r"(ta), "r"(ta + 32), "r"(tb), "r"(tb + 32)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint32_t* r) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"

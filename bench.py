@@ -519,6 +519,90 @@ def run_ours(args, wl):
     return 0
 
 
+BWD_METRIC = ("attention bwd TFLOP/s (10·B·H·N²·d = 2.5x the forward's FLOPs, ×½ causal) "
+              "and % of GB300 BF16 tensor peak")
+
+
+def run_backward(args, wl):
+    """Time fa_bwd (pre-pass + dK/dV + dQ kernels) on the workload's shapes,
+    with Q, K, V, O, LSE and dO resident on the device."""
+    import torch
+    rank, world, local = _dist_env()
+    dev = torch.device(f"cuda:{local}" if world > 1 else "cuda:0")
+    torch.cuda.set_device(dev)
+    import attention_forward_10_gb300 as fa
+    from workloads import make_qkv
+    if wl.varlen or wl.splitkv or wl.d not in (64, 128):
+        raise SystemExit("--backward runs the [B,H,N,d] workloads with d = 64 or 128")
+    fa.fa_set_max_ctas(0)
+    warmup = max(3, args.warmup)
+    q, k, v = (t.to(dev) for t in make_qkv(wl))
+    dout = torch.randn(q.shape, generator=torch.Generator().manual_seed(4000 + wl.index))
+    dout = dout.to(q.dtype).to(dev)
+    o, lse = fa.fwd(q, k, v, scale=wl.scale, causal=wl.causal)
+    st, need = fa.fa_bwd_workspace_bytes(wl.B, wl.H, wl.N)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    stream = torch.cuda.Stream(device=dev)
+    dcode = fa.FA_DTYPE_BF16 if wl.dtype == "bf16" else fa.FA_DTYPE_F16
+
+    def step():
+        st_ = fa.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                        dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                        ws.data_ptr(), ws.numel(), wl.B, wl.H, wl.H, wl.N, wl.d, wl.scale,
+                        int(wl.causal), -1, -1, dcode, stream.cuda_stream)
+        if st_ != fa.FA_OK:
+            raise RuntimeError(f"fa_bwd failed: {fa.fa_status_string(st_)}")
+
+    torch.cuda.synchronize(dev)
+    for _ in range(warmup):
+        step()
+    stream.synchronize()
+    if args.steps is None:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(3):
+            step()
+        e1.record(stream)
+        e1.synchronize()
+        args.steps = int(min(5000, max(10, 2000.0 / max(e0.elapsed_time(e1) / 3, 1e-3))))
+    sampler = ClockSampler(_gpu_id_for_smi(torch, dev.index))
+    time.sleep(0.25)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    start.record(stream)
+    for _ in range(args.steps):
+        step()
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    clocks = sampler.summary(t0, t1)
+    sampler.stop()
+    st, site = fa.fa_get_device_status(stream.cuda_stream)
+    if st != fa.FA_OK:
+        raise RuntimeError(f"device status {fa.fa_status_string(st)} (site {site})")
+    ms = start.elapsed_time(end) / args.steps
+    flops = 2.5 * wl.flops
+    peaks, src = _peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    achieved = flops / (ms / 1e3) / 1e12
+    line = {
+        "metric": BWD_METRIC, "value": achieved, "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "config": _config(wl, "inputs resident; each step reads the same inputs"),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak,
+                     "peak_source": f"{src} bf16_tflops (burst)",
+                     "executed_mma_flops_per_algorithmic": 1.4},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -530,9 +614,13 @@ def main():
                          "6: the split-KV case; 7: a packed variable-length batch)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the backward pass (fa_bwd) instead of the forward")
     args = ap.parse_args()
     from workloads import workload
     wl = workload(args.workload)
+    if args.backward:
+        return run_backward(args, wl)
     if args.impl == "reference":
         if args.steps is None:
             args.steps = 20

@@ -242,6 +242,39 @@ FA_API int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, v
                                   float scale, int causal, int window_left, int window_right,
                                   int dtype, int num_splits, void* stream);
 
+/*
+ * fa_bwd -- attention backward pass: dQ, dK, dV from Q, K, V, the forward's
+ * O and LSE, and dO.
+ *
+ * Source: flash-attention "hopper/mainloop_bwd_sm90_tma_gmma_ws.hpp"
+ * (CollectiveMainloopBwd::mma): P = exp(scale Q K^T - LSE), dP = dO V^T,
+ * D = rowsum(dO * O) (the page's dPsum), dS = P (dP - D), dV = P^T dO,
+ * dK = scale dS^T Q, dQ = scale dS K; grouped K/V heads sum their query
+ * heads' dK and dV; masks and windows as in fa_fwd_ext.
+ *
+ *   q, o, dout, dq   contiguous [B][H][N][d] of `dtype` (o and lse as written
+ *                    by fa_fwd_ext for the same arguments).
+ *   k, v, dk, dv     contiguous [B][H_kv][N][d].
+ *   lse              contiguous [B][H][N] float32 (natural log).
+ *   workspace        device scratch of at least fa_bwd_workspace_bytes()
+ *                    bytes, 256-byte aligned; overwritten, need not be
+ *                    initialised.
+ *   d                64 or 128 (else FA_ERR_UNSUPPORTED).
+ * Every other argument, alignment rule and error is that of fa_fwd_ext (q,
+ * k, v, o, dout, dq, dk, dv 16-byte aligned; lse 4-byte).  Enqueues three
+ * kernels on `stream` (a row-sum pre-pass, the dK/dV kernel, the dQ kernel);
+ * no atomics, so the gradients are bit-for-bit reproducible.  Allocates no
+ * device memory.
+ */
+FA_API int fa_bwd(const void* q, const void* k, const void* v, const void* o,
+                  const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                  void* workspace, unsigned long long workspace_bytes, int B, int H,
+                  int H_kv, int N, int d, float scale, int causal, int window_left,
+                  int window_right, int dtype, void* stream);
+
+/* Workspace bytes of fa_bwd for these sizes (written to *bytes). */
+FA_API int fa_bwd_workspace_bytes(int B, int H, int N, unsigned long long* bytes);
+
 /* Human-readable name of a status code (static string, never NULL). */
 FA_API const char* fa_status_string(int status);
 

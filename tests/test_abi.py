@@ -231,3 +231,32 @@ def test_varlen_argument_errors(fa, kw, code):
                                 dict(batch=0, cu=0, q=0, k=0, v=0, o=0)])
 def test_varlen_empty_is_noop(fa, kw):
     assert _call_varlen(fa, **kw) == fa.FA_OK
+
+
+# ---------------------------------------------------------------- backward
+def _call_bwd(fa, ws=0x100000, ws_bytes=1 << 30, **kw):
+    a = dict(GOOD, H=2)
+    a.update(kw)
+    return fa.fa_bwd(a["q"], a["k"], a["v"], a.get("o", 0x7000), a.get("lse_", 0x8000),
+                     a.get("do", 0x9000), a.get("dq", 0xA000), a.get("dk", 0xB000),
+                     a.get("dv", 0xC000), ws, ws_bytes, a["B"], a["H"], a.get("H_kv", a["H"]),
+                     a["N"], a["d"], a["scale"], a["causal"], -1, -1, a["dtype"], a["stream"])
+
+
+def test_bwd_workspace_size(fa):
+    st, n = fa.fa_bwd_workspace_bytes(2, 3, 300)
+    assert st == fa.FA_OK and n == 2 * 2 * 3 * 384 * 4
+    assert fa.fa_bwd_workspace_bytes(-1, 3, 300)[0] == fa.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=256), 2), (dict(d=32), 2), (dict(ws=0), 1), (dict(ws_bytes=64), 1),
+    (dict(ws=0x100010), 3), (dict(do=0), 1), (dict(o=0x7008), 3), (dict(lse_=0x8002), 3),
+    (dict(dk=0xB004), 3), (dict(H_kv=3), 1), (dict(causal=3), 1),
+])
+def test_bwd_argument_errors(fa, kw, code):
+    assert _call_bwd(fa, **kw) == code
+
+
+def test_bwd_empty_is_noop(fa):
+    assert _call_bwd(fa, N=0, ws=0, ws_bytes=0) == fa.FA_OK
