@@ -25,7 +25,8 @@ h // (H / H_kv)) and a local window (keys i - window_left .. i + window_right),
 the ``qhead_per_khead`` and ``window_size_left/right`` options of the same
 backward page.  ``attention_bwd`` gives the gradients dQ, dK, dV of that
 definition against dO (the backward page's P, dP, dPsum, dS recurrence
-written out in double).  ``attention_varlen`` takes sequences of different lengths
+written out in double).  ``attention_fp8`` takes FP8 E4M3 inputs with
+descale factors (the FP8 forward of the Hopper forward page).  ``attention_varlen`` takes sequences of different lengths
 packed along the rows ([total, H, d], cu_seqlens offsets), the
 variable-length mode of the Hopper pages.
 
@@ -99,6 +100,12 @@ def _bind(path: str):
     lib.attn_ref_bwd_u16.argtypes = [vp, vp, vp, vp, c_int, c_long, c_long, c_long, c_long,
                                      c_long, c_double, c_int, c_long, c_long, vp, vp, vp, c_int]
     lib.attn_ref_bwd_u16.restype = c_int
+    lib.attn_ref_e4m3.argtypes = [ctypes.c_uint8]
+    lib.attn_ref_e4m3.restype = c_double
+    lib.attn_ref_fwd_fp8.argtypes = [vp, vp, vp, c_long, c_long, c_long, c_long, c_long,
+                                     c_double, c_double, c_double, c_double, c_int, c_long,
+                                     c_long, vp, vp, c_int]
+    lib.attn_ref_fwd_fp8.restype = c_int
     lib.attn_ref_widen.argtypes = [ctypes.c_uint16, c_int]
     lib.attn_ref_widen.restype = c_double
     lib.attn_ref_max_threads.argtypes = []
@@ -320,3 +327,35 @@ def attention_bwd(q, k, v, dout, scale: float, causal: bool, window_left: int = 
     if rc != 0:
         raise RuntimeError("oracle attn_ref_bwd_u16 failed")
     return dq, dk, dv
+
+
+def e4m3(code: int) -> float:
+    """The oracle's decoding of one OCP FP8 E4M3 byte."""
+    return float(_load().attn_ref_e4m3(int(code)))
+
+
+def _u8_view(t) -> np.ndarray:
+    import torch
+    if t.dtype != torch.float8_e4m3fn:
+        raise TypeError("expected a torch.float8_e4m3fn tensor")
+    return np.ascontiguousarray(t.contiguous().view(torch.uint8).numpy())
+
+
+def attention_fp8(q, k, v, scale: float, descale_q: float, descale_k: float,
+                  descale_v: float, causal: bool, window_left: int = -1,
+                  window_right: int = -1, nthreads: int = 0):
+    """O [B,H,N,d] and LSE [B,H,N] (float64) of attention on FP8 E4M3 inputs
+    (torch.float8_e4m3fn, k/v may have fewer heads) scaled by their descale
+    factors: the definition on q = descale_q * Q, k = descale_k * K,
+    v = descale_v * V."""
+    B, H, H_kv, N, d = _check_ex(q, k, v)
+    qw, kw, vw = _u8_view(q), _u8_view(k), _u8_view(v)
+    o = np.empty((B, H, N, d), dtype=np.float64)
+    lse = np.empty((B, H, N), dtype=np.float64)
+    rc = _load().attn_ref_fwd_fp8(_ptr(qw), _ptr(kw), _ptr(vw), B, H, H_kv, N, d, float(scale),
+                                  float(descale_q), float(descale_k), float(descale_v),
+                                  int(bool(causal)), int(window_left), int(window_right),
+                                  _ptr(o), _ptr(lse), int(nthreads))
+    if rc != 0:
+        raise RuntimeError("oracle attn_ref_fwd_fp8 failed")
+    return o, lse

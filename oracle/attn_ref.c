@@ -40,6 +40,9 @@
  * the page's window_size_left / window_size_right and its Is_local mask).
  * With H_kv = H and both bounds negative they reduce to the definition above.
  *
+ * FP8 inputs (attn_ref_fwd_fp8): E4M3 bytes times one descale factor per
+ * tensor, decoded exactly here; then the same definition.
+ *
  * Backward (attn_ref_bwd_u16): the gradients dQ, dK, dV of the definition
  * above against dO, as the same backward page computes them (P, dP, the row
  * sums D_i = sum_j P_ij dP_ij, dS = P (dP - D)), in double.
@@ -610,5 +613,71 @@ int attn_ref_bwd_u16(const uint16_t *q, const uint16_t *k, const uint16_t *v,
         }
     }
     free(kd); free(vd); free(qd); free(dod); free(lse); free(dsum);
+    return rc;
+}
+
+/*
+ * FP8 forward: Q, K, V given as OCP FP8 E4M3 bytes (1 sign bit, 4 exponent
+ * bits with bias 7, 3 mantissa bits; exponent 0 is subnormal, m/8 * 2^-6; the
+ * all-ones code S.1111.111 is NaN and there is no infinity) with one
+ * descale factor per tensor, as flash-attention "hopper/flash_fwd_kernel.h"
+ * takes them (descale_q/k/v: the stored values times the descale are the
+ * real inputs).  The result is the definition above on q = dq * Q8,
+ * k = dk * K8, v = dv * V8:
+ *   q, k, v : [B][H or H_kv][N][d] bytes;  o : [B][H][N][d];  lse : [B][H][N]
+ */
+static double e4m3_to_double(uint8_t b) {
+    int sign = (b >> 7) & 1, expo = (b >> 3) & 0xF, mant = b & 7;
+    double mag;
+    if (expo == 0xF && mant == 7) return NAN;
+    if (expo == 0) mag = ldexp((double)mant, -9);          /* (m/8) 2^-6 */
+    else mag = ldexp(8.0 + mant, expo - 10);               /* (1+m/8) 2^(e-7) */
+    return sign ? -mag : mag;
+}
+
+double attn_ref_e4m3(uint8_t code) { return e4m3_to_double(code); }
+
+int attn_ref_fwd_fp8(const uint8_t *q, const uint8_t *k, const uint8_t *v,
+                     long B, long H, long H_kv, long N, long d, double scale,
+                     double dq, double dk, double dv, int causal, long wl, long wr,
+                     double *o, double *lse, int nthreads) {
+    if (!q || !k || !v || !o || !lse || B < 0 || H <= 0 || H_kv <= 0 ||
+        H % H_kv != 0 || N < 0 || d <= 0)
+        return -1;
+    set_threads(nthreads);
+    long slice = N * d, group = H / H_kv, cap = slice > 0 ? slice : 1;
+    double *qd = (double *)malloc(sizeof(double) * (size_t)cap);
+    double *kd = (double *)malloc(sizeof(double) * (size_t)cap);
+    double *vd = (double *)malloc(sizeof(double) * (size_t)cap);
+    if (!qd || !kd || !vd) { free(qd); free(kd); free(vd); return -1; }
+    int rc = 0;
+    for (long b = 0; b < B && rc == 0; ++b) {
+        for (long h = 0; h < H && rc == 0; ++h) {
+            long bh = b * H + h, bkv = b * H_kv + h / group;
+            for (long t = 0; t < slice; ++t) {
+                qd[t] = dq * e4m3_to_double(q[bh * slice + t]);
+                kd[t] = dk * e4m3_to_double(k[bkv * slice + t]);
+                vd[t] = dv * e4m3_to_double(v[bkv * slice + t]);
+            }
+#pragma omp parallel
+            {
+                double *scores = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+                if (!scores) {
+#pragma omp atomic write
+                    rc = -1;
+                } else {
+#pragma omp for schedule(dynamic, 4)
+                    for (long i = 0; i < N; ++i) {
+                        long j0, j1;
+                        key_range(N, i, causal, wl, wr, &j0, &j1);
+                        attend_range(qd + i * d, kd, vd, d, j0, j1, scale, scores,
+                                     o + (bh * N + i) * d, lse + bh * N + i);
+                    }
+                    free(scores);
+                }
+            }
+        }
+    }
+    free(qd); free(kd); free(vd);
     return rc;
 }

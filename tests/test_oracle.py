@@ -552,3 +552,58 @@ def test_bwd_sum_identities(causal, window):
     np.testing.assert_allclose(dv.sum(2), dod.sum((2, 3)), rtol=0, atol=1e-12)
     np.testing.assert_allclose(dk.sum(2), 0.0, rtol=0, atol=1e-12)
     assert np.abs(dq).max() > 1e-3
+
+
+# ------------------------------------------------------------ FP8 inputs
+def test_e4m3_decoder_exhaustive():
+    """All 256 E4M3 codes decode as PyTorch's float8_e4m3fn does (NaN codes
+    included)."""
+    codes = torch.arange(256, dtype=torch.uint8)
+    want = codes.view(torch.float8_e4m3fn).double().numpy()
+    got = np.array([oracle.e4m3(c) for c in range(256)])
+    np.testing.assert_array_equal(np.isnan(got), np.isnan(want))
+    ok = ~np.isnan(want)
+    np.testing.assert_array_equal(got[ok], want[ok])
+    assert oracle.e4m3(0x7E) == 448.0 and oracle.e4m3(0x01) == 2.0 ** -9
+
+
+def _fp8_inputs(B, H, H_kv, N, d, seed):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn(B, H, N, d, generator=g).to(torch.float8_e4m3fn)
+    k = torch.randn(B, H_kv, N, d, generator=g).to(torch.float8_e4m3fn)
+    v = torch.randn(B, H_kv, N, d, generator=g).to(torch.float8_e4m3fn)
+    return q, k, v
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_matches_torch_on_decoded_inputs(causal):
+    """The FP8 definition equals torch float64 attention of the decoded,
+    descaled inputs (library routine on PyTorch's own FP8 decoding)."""
+    q, k, v = _fp8_inputs(2, 4, 2, 33, 16, seed=900)
+    o, lse = oracle.attention_fp8(q, k, v, 0.2, 0.5, 2.0, 0.25, causal, 5, -1)
+    qd, kd, vd = q.double() * 0.5, k.double() * 2.0, v.double() * 0.25
+    o_ref = _torch_attention_f64(qd, kd, vd, 0.2, causal, (5, -1))
+    np.testing.assert_allclose(o, o_ref.numpy(), rtol=0, atol=1e-12)
+    kr = kd.repeat_interleave(2, 1)
+    s = 0.2 * qd @ kr.transpose(-1, -2)
+    N = 33
+    i = torch.arange(N)[:, None]
+    j = torch.arange(N)[None, :]
+    allowed = j >= i - 5
+    if causal:
+        allowed &= j <= i
+    l_ref = torch.logsumexp(s.masked_fill(~allowed, float("-inf")), -1)
+    np.testing.assert_allclose(lse, l_ref.numpy(), rtol=0, atol=1e-12)
+
+
+def test_fp8_descale_folds_into_scale():
+    """Scaling Q's descale by c equals scaling the softmax scale by c, and V's
+    descale scales O linearly (the descales are plain multipliers)."""
+    q, k, v = _fp8_inputs(1, 2, 2, 40, 32, seed=910)
+    o1, l1 = oracle.attention_fp8(q, k, v, 0.3, 2.0, 1.0, 1.0, False)
+    o2, l2 = oracle.attention_fp8(q, k, v, 0.6, 1.0, 1.0, 1.0, False)
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-13)
+    o3, l3 = oracle.attention_fp8(q, k, v, 0.6, 1.0, 1.0, 4.0, False)
+    np.testing.assert_allclose(o3, 4.0 * o2, rtol=0, atol=1e-12)
+    np.testing.assert_array_equal(l3, l2)

@@ -50,6 +50,12 @@ MUTANTS = {
     "bwd_key_mask_ignored": ("if (j < j0 || j >= j1) continue;", "if (j < 0) continue;"),
     "bwd_dq_transposed": ("dqi[c] += scale * ds * kd[j * d + c];",
                           "dqi[c] += scale * ds * vd[j * d + c];"),
+    "e4m3_bias": ("else mag = ldexp(8.0 + mant, expo - 10);",
+                  "else mag = ldexp(8.0 + mant, expo - 11);"),
+    "e4m3_subnormal": ("if (expo == 0) mag = ldexp((double)mant, -9);",
+                       "if (expo == 0) mag = ldexp((double)mant, -10);"),
+    "fp8_descale_v_dropped": ("vd[t] = dv * e4m3_to_double(v[bkv * slice + t]);",
+                              "vd[t] = e4m3_to_double(v[bkv * slice + t]);"),
     "bf16_decoder_shift": ("uint32_t bits = (uint32_t)b << 16;",
                            "uint32_t bits = (uint32_t)b << 15;"),
     "half_decoder_bias": ("expo - 25", "expo - 24"),
@@ -79,6 +85,9 @@ PIN_CALLS = [
     (pins.test_bwd_matches_torch_autograd, dict(causal=True, window=(6, 3), H=4, H_kv=2)),
     (pins.test_bwd_directional_finite_difference, dict(causal=True)),
     (pins.test_bwd_sum_identities, dict(causal=False, window=(5, 2))),
+    (pins.test_e4m3_decoder_exhaustive, {}),
+    (pins.test_fp8_matches_torch_on_decoded_inputs, dict(causal=True)),
+    (pins.test_fp8_descale_folds_into_scale, {}),
 ]
 
 
