@@ -39,6 +39,9 @@ _ull = ctypes.c_ulonglong
 SIGNATURES = {
     "fa_fwd": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _vp], _i),
     "fa_fwd_ext": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _i, _i, _vp], _i),
+    "fa_fwd_fp8": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _f, _f, _f, _i, _i, _i,
+                    _vp, _ull, _vp], _i),
+    "fa_fwd_fp8_workspace_bytes": ([_i, _i, _i, _i, ctypes.POINTER(_ull)], _i),
     "fa_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _ull, _i, _i, _i, _i, _i, _f,
                 _i, _i, _i, _i, _vp], _i),
     "fa_bwd_workspace_bytes": ([_i, _i, _i, ctypes.POINTER(_ull)], _i),
@@ -105,6 +108,21 @@ def fa_fwd_ext(q: int, k: int, v: int, o: int, lse: int | None, B: int, H: int, 
                window_right: int, dtype: int, stream: int | None) -> int:
     return int(_lib.fa_fwd_ext(q, k, v, o, lse or None, B, H, H_kv, N, d, scale, causal,
                                window_left, window_right, dtype, stream or None))
+
+
+def fa_fwd_fp8(q: int, k: int, v: int, o: int, lse: int | None, B: int, H: int, H_kv: int,
+               N: int, d: int, scale: float, descale_q: float, descale_k: float,
+               descale_v: float, causal: int, window_left: int, window_right: int,
+               workspace: int | None, workspace_bytes: int, stream: int | None) -> int:
+    return int(_lib.fa_fwd_fp8(q, k, v, o, lse or None, B, H, H_kv, N, d, scale, descale_q,
+                               descale_k, descale_v, causal, window_left, window_right,
+                               workspace or None, int(workspace_bytes), stream or None))
+
+
+def fa_fwd_fp8_workspace_bytes(B: int, H_kv: int, N: int, d: int) -> tuple[int, int]:
+    out = ctypes.c_ulonglong(0)
+    st = int(_lib.fa_fwd_fp8_workspace_bytes(B, H_kv, N, d, ctypes.byref(out)))
+    return st, int(out.value)
 
 
 def fa_bwd(q: int, k: int, v: int, o: int, lse: int, dout: int, dq: int, dk: int, dv: int,
@@ -294,6 +312,48 @@ def fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int, *, scale: float | None = No
     return out, (lse if return_lse else None)
 
 
+def fwd_fp8(q, k, v, *, scale: float | None = None, descale_q: float = 1.0,
+            descale_k: float = 1.0, descale_v: float = 1.0, causal: bool = False,
+            window: tuple[int, int] = (-1, -1), out=None, lse=None, return_lse: bool = True,
+            workspace=None, stream=None):
+    """Attention forward on torch.float8_e4m3fn CUDA tensors q [B,H,N,128] and
+    k, v [B,H_kv,N,128] with descale factors; returns (o bf16, lse fp32)."""
+    import torch
+    if not (q.dtype == k.dtype == v.dtype == torch.float8_e4m3fn):
+        raise TypeError("q, k, v must be torch.float8_e4m3fn")
+    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape:
+        raise ValueError("q must be [B, H, N, d] and k, v one [B, H_kv, N, d] shape")
+    if not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise ValueError("q, k, v must be CUDA tensors (no CPU path)")
+    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("q, k, v must be contiguous")
+    B, H, N, d = (int(x) for x in q.shape)
+    H_kv = int(k.shape[1])
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=q.device)
+    if return_lse and lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    with torch.cuda.device(q.device):
+        st, need = fa_fwd_fp8_workspace_bytes(B, H_kv, N, d)
+        if st != FA_OK:
+            raise FaError(st, "fa_fwd_fp8_workspace_bytes")
+        if workspace is None:
+            workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+        st = fa_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                        lse.data_ptr() if (return_lse and lse is not None) else None, B, H,
+                        H_kv, N, d, float(scale), float(descale_q), float(descale_k),
+                        float(descale_v), int(bool(causal)), int(window[0]), int(window[1]),
+                        workspace.data_ptr(), workspace.numel(), handle)
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_fp8")
+    return out, (lse if return_lse else None)
+
+
 def bwd(q, k, v, o, lse, dout, *, scale: float | None = None, causal: bool = False,
         window: tuple[int, int] = (-1, -1), dq=None, dk=None, dv=None, workspace=None,
         stream=None):
@@ -365,7 +425,8 @@ def fwd_splitkv(q, k, v, *, num_splits: int = 0, scale: float | None = None,
 
 
 __all__ = [
-    "LIB_PATH", "SIGNATURES", "FaError", "fwd", "bwd", "fwd_varlen", "fwd_splitkv", "fa_fwd",
+    "LIB_PATH", "SIGNATURES", "FaError", "fwd", "bwd", "fwd_fp8", "fwd_varlen", "fwd_splitkv",
+    "fa_fwd", "fa_fwd_fp8", "fa_fwd_fp8_workspace_bytes",
     "fa_bwd", "fa_bwd_workspace_bytes",
     "fa_fwd_ext", "fa_fwd_varlen",
     "fa_fwd_splitkv", "fa_splitkv_workspace_bytes", "fa_fwd_splitkv_noalloc",

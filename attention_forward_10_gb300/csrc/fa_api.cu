@@ -140,6 +140,25 @@ bool encode_packed_map(CUtensorMap* map, const void* base, int rows, int heads, 
   return r == CUDA_SUCCESS;
 }
 
+// 4-D byte view for the FP8 kernel's 128-byte-row tiles: dim0 = 128 bytes
+// (innermost), dim1 = rows (stride row_stride), dim2 = 128-byte blocks
+// (stride 128), dim3 = heads (stride head_stride); box {128, box_rows, 1, 1}.
+bool encode_e4m3_map(CUtensorMap* map, const void* base, int rows, int row_bytes,
+                     unsigned long long row_stride, unsigned long long head_stride, int heads,
+                     int box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[4] = {128, static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(row_bytes / 128), static_cast<cuuint64_t>(heads)};
+  cuuint64_t strides[3] = {row_stride, 128, head_stride};
+  cuuint32_t box[4] = {128, static_cast<cuuint32_t>(box_rows), 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool aligned(const void* ptr, uintptr_t a) {
   return (reinterpret_cast<uintptr_t>(ptr) % a) == 0;
 }
@@ -208,6 +227,11 @@ struct ForwardCall {
   // longest; nullptr / 0 for the [B][H][N][d] layout
   const int* cu_seqlens;
   int total;
+  // FP8 (E4M3) inputs: descale factors and the V^T workspace
+  bool fp8;
+  float descale_q, descale_k, descale_v;
+  void* vt;
+  int n_pad;
 };
 
 int validate(const ForwardCall& c) {
@@ -265,7 +289,16 @@ int launch_forward(const ForwardCall& c, void* o_out, float* lse_out, int num_sp
   const int kv_rows = kv_tile_rows(d);
   const int o_blocks = (d == 256) ? 2 : d / 64;
   const bool packed = c.cu_seqlens != nullptr;
-  if (packed) {
+  if (c.fp8) {
+    // Q, K: [heads][N][128] bytes; V^T: [H_kv heads][128][n_pad] bytes; O bf16
+    const unsigned long long nd = static_cast<unsigned long long>(N) * d;
+    if (!encode_e4m3_map(&p.tm_q, c.q, N, d, d, nd, ibh, kBlockM) ||
+        !encode_e4m3_map(&p.tm_k, c.k, N, d, d, nd, ibh_kv, kBlockN) ||
+        !encode_e4m3_map(&p.tm_v, c.vt, d, c.n_pad, c.n_pad,
+                         static_cast<unsigned long long>(d) * c.n_pad, ibh_kv, d) ||
+        !encode_qkvo_map(&p.tm_o, o_out, N, d, ibh, true, kBlockM, o_blocks))
+      return FA_ERR_CUDA;
+  } else if (packed) {
     if (!encode_packed_map(&p.tm_q, c.q, c.total, c.H, d, bf16, kBlockM, d / 64) ||
         !encode_packed_map(&p.tm_k, c.k, c.total, c.H_kv, d, bf16, kv_rows, d / 64) ||
         !encode_packed_map(&p.tm_v, c.v, c.total, c.H_kv, d, bf16, kv_rows, d / 64) ||
@@ -298,6 +331,12 @@ int launch_forward(const ForwardCall& c, void* o_out, float* lse_out, int num_sp
   p.num_splits = num_splits;
   p.split_tiles = split_tiles;
   p.scale_log2 = static_cast<float>(static_cast<double>(c.scale) * 1.4426950408889634);
+  p.descale_v = 1.f;
+  if (c.fp8) {
+    p.scale_log2 = static_cast<float>(static_cast<double>(c.scale) * c.descale_q * c.descale_k *
+                                      1.4426950408889634);
+    p.descale_v = c.descale_v;
+  }
 
   int grid = info->num_sms;
   const int cap = g_max_ctas.load();
@@ -316,6 +355,11 @@ int launch_forward(const ForwardCall& c, void* o_out, float* lse_out, int num_sp
   if (p.num_units < grid) grid = p.num_units;
 
   cudaStream_t s = static_cast<cudaStream_t>(c.stream);
+  if (c.fp8) {
+    cudaError_t e = launch_transpose_v_e4m3(c.v, c.vt, ibh_kv, N, c.n_pad, d, info->num_sms, s);
+    if (e == cudaSuccess) e = launch_fwd_d128_fp8(p, c.causal != 0, grid, s);
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  }
   cudaError_t e = (d == 64)    ? launch_fwd_d64(p, c.causal != 0, bf16, grid, s)
                   : (d == 128) ? launch_fwd_d128(p, c.causal != 0, bf16, grid, s)
                                : launch_fwd_d256(p, c.causal != 0, bf16, grid, s);
@@ -699,6 +743,44 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
                 : launch_bwd_d128(p_kv, p_q, o, dout, lse, lse2, dsum, causal != 0, bf16,
                                   grid_kv, grid_q, info->num_sms, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_fwd_fp8_workspace_bytes(int B, int H_kv, int N, int d, unsigned long long* bytes) {
+  if (bytes == nullptr) return FA_ERR_INVALID_ARG;
+  *bytes = 0;
+  if (B < 0 || H_kv < 0 || N < 0) return FA_ERR_INVALID_ARG;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  const unsigned long long n_pad = (static_cast<unsigned long long>(N) + 127ull) / 128ull * 128ull;
+  *bytes = static_cast<unsigned long long>(B) * static_cast<unsigned long long>(H_kv) * d * n_pad;
+  return FA_OK;
+}
+
+int fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+               int H_kv, int N, int d, float scale, float descale_q, float descale_k,
+               float descale_v, int causal, int window_left, int window_right, void* workspace,
+               unsigned long long workspace_bytes, void* stream) {
+  using namespace fa;
+  ForwardCall c{q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, window_left,
+                window_right, FA_DTYPE_BF16, stream};
+  int st = validate(c);
+  if (st != FA_OK) return st;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  for (float x : {descale_q, descale_k, descale_v})
+    if (!(std::isfinite(x) && x > 0.f)) return FA_ERR_INVALID_ARG;
+  if (empty_problem(c)) return FA_OK;
+  st = check_pointers(c);
+  if (st != FA_OK) return st;
+  unsigned long long need = 0;
+  fa_fwd_fp8_workspace_bytes(B, H_kv, N, d, &need);
+  if (workspace == nullptr || workspace_bytes < need) return FA_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return FA_ERR_MISALIGNED;
+  c.fp8 = true;
+  c.descale_q = descale_q;
+  c.descale_k = descale_k;
+  c.descale_v = descale_v;
+  c.vt = workspace;
+  c.n_pad = static_cast<int>((static_cast<long long>(N) + 127) / 128 * 128);
+  return launch_forward(c, o, lse, 1, 0);
 }
 
 int fa_get_device_status(void* stream, int* site) {

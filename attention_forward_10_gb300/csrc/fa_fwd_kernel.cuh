@@ -80,17 +80,23 @@ constexpr int kMmaWarp = 9;
 constexpr int kStoreWarp = 10;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr float kFp8Threshold = 2.0f;      // log2 units (FP8 P)
+constexpr float kFp8POffset = 6.0f;        // log2 units (FP8 P)
 
-template <int D>
+// FP8: E4M3 Q, K and V^T tiles (one byte per element, 128-byte rows), so
+// twice the ring slots; the output stays 16-bit.
+template <int D, bool FP8 = false>
 struct Layout {
   static_assert(D == 64 || D == 128, "head dim");
-  static constexpr uint32_t kTileBytes = kBlockM * D * 2;  // == kBlockN * D * 2
-  static constexpr int kStages = (D == 64) ? 6 : 4;
+  static_assert(!FP8 || D == 128, "FP8 tiles are 128-byte rows");
+  static constexpr uint32_t kTileBytes = kBlockM * D * (FP8 ? 1 : 2);  // Q, K or V tile
+  static constexpr uint32_t kOTileBytes = kBlockM * D * 2;             // 16-bit O tile
+  static constexpr int kStages = FP8 ? 8 : (D == 64) ? 6 : 4;
   static_assert(kStages % 2 == 0, "K and V share the ring in pairs");
   static constexpr uint32_t kQOff = 0;
   static constexpr uint32_t kKVOff = kQOff + 2 * kTileBytes;
   static constexpr uint32_t kStageOff = kKVOff + kStages * kTileBytes;
-  static constexpr uint32_t kBarOff = kStageOff + kTileBytes;
+  static constexpr uint32_t kBarOff = kStageOff + kOTileBytes;
   // barrier indices
   static constexpr int kQFull = 0;
   static constexpr int kQEmpty = 2;
@@ -231,10 +237,48 @@ __device__ __forceinline__ float exp_tile_to_tmem(const float (&s)[kBlockN], flo
   return a0 + a1;
 }
 
-template <int D, bool CAUSAL, bool BF16, bool PACKED>
+// FP8: Q, K E4M3 and V^T E4M3 ([heads][D][keys], see the launcher) with the
+// products in kind::f8f6f4; P goes to tensor memory as E4M3 scaled by
+// 2^kFp8POffset; O (16-bit, BF16 must be true) is multiplied by the V
+// descale in the epilogue.
+// FP8 form of exp_tile_to_tmem: p = 2^(s*scale*log2e - m) (m includes the
+// P offset), packed four per 32-bit column as E4M3 into tensor memory at tS
+// (32 columns).  Returns the row sum of the unrounded p.
+__device__ __forceinline__ float exp_tile_to_tmem_e4m3(const float (&s)[kBlockN],
+                                                       float scale_log2, float m, uint32_t tS) {
+  const uint64_t scale2 = pack_f32x2(scale_log2, scale_log2);
+  const uint64_t neg_m2 = pack_f32x2(-m, -m);
+  uint64_t acc_a = pack_f32x2(0.f, 0.f), acc_b = acc_a;
+  uint32_t pk[32];
+#pragma unroll
+  for (int c = 0; c < kBlockN; c += 4) {
+    float p[4];
+#pragma unroll
+    for (int e = 0; e < 4; e += 2) {
+      float x0, x1;
+      unpack_f32x2(fma_f32x2(pack_f32x2(s[c + e], s[c + e + 1]), scale2, neg_m2), x0, x1);
+      p[e] = ex2_approx(x0);
+      p[e + 1] = ex2_approx(x1);
+    }
+    acc_a = add_f32x2(acc_a, pack_f32x2(p[0], p[1]));
+    acc_b = add_f32x2(acc_b, pack_f32x2(p[2], p[3]));
+    pk[c / 4] = pack4_e4m3(p[0], p[1], p[2], p[3]);
+  }
+  tmem_st_x32(tS, pk);
+  float a0, a1;
+  unpack_f32x2(add_f32x2(acc_a, acc_b), a0, a1);
+  return a0 + a1;
+}
+
+template <int D, bool CAUSAL, bool BF16, bool PACKED, bool FP8 = false>
 __global__ void __launch_bounds__(kNumThreads, 1)
     fa_fwd_kernel(const __grid_constant__ FaParams p) {
-  using L = Layout<D>;
+  using L = Layout<D, FP8>;
+  static_assert(!FP8 || (BF16 && !PACKED), "FP8 runs the [B,H,N,d] layout with a bf16 output");
+  // P = 2^(x - m + offset) stays below 2^(threshold + offset) <= 256 < 448,
+  // the largest E4M3 value; the offset keeps small probabilities above the
+  // E4M3 subnormal floor.
+  constexpr float kThreshold = FP8 ? kFp8Threshold : kRescaleThreshold;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -314,9 +358,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             }
             if (!ok) break;
             mbar_arrive_expect_tx(bar(L::kKVFull + slot), L::kTileBytes);
-            tma_load_4d(sbase + L::kKVOff + slot * L::kTileBytes, kv ? &p.tm_v : &p.tm_k,
-                        bar(L::kKVFull + slot), 0, w.sv.row_base + n * kBlockN, 0,
-                        w.sv.kv_head);
+            if (FP8 && kv)  // V^T: all d rows of key block n
+              tma_load_4d(sbase + L::kKVOff + slot * L::kTileBytes, &p.tm_v,
+                          bar(L::kKVFull + slot), 0, 0, n, w.sv.kv_head);
+            else
+              tma_load_4d(sbase + L::kKVOff + slot * L::kTileBytes, kv ? &p.tm_v : &p.tm_k,
+                          bar(L::kKVFull + slot), 0, w.sv.row_base + n * kBlockN, 0,
+                          w.sv.kv_head);
             ++kv_it;
           }
         }
@@ -336,8 +384,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     // The issuing thread does as little as possible between MMA groups: the
     // tensor pipe holds only a couple of queued MMAs.
     if (lane == 0) {
-      constexpr uint32_t kIdescS = make_idesc_f16(kBlockM, kBlockN, BF16, false);
-      constexpr uint32_t kIdescO = make_idesc_f16(kBlockM, D, BF16, true);
+      // (FP8: the E4M3 format code is 0, B of the P V product K-major V^T)
+      constexpr uint32_t kIdescS = make_idesc_f16(kBlockM, kBlockN, FP8 ? false : BF16, false);
+      constexpr uint32_t kIdescO = make_idesc_f16(kBlockM, D, FP8 ? false : BF16, !FP8);
       constexpr uint32_t kSlotStep = L::kTileBytes >> 4;  // descriptor units
       // Descriptors of slot 0 / query tile 0; other slots and tiles are fixed
       // offsets in the 14-bit start-address field (no carry: smem < 256 KB).
@@ -345,7 +394,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       const uint64_t k_desc0 = smem_desc_sw128(sbase + L::kKVOff, 16, 1024);
       // V is MN-major (d contiguous): 64-wide d blocks 128 keys apart (LBO),
       // 8-key groups 1024 B apart (SBO).
-      const uint64_t v_desc0 = smem_desc_sw128(sbase + L::kKVOff, kBlockN * 128, 1024);
+      const uint64_t v_desc0 = FP8 ? smem_desc_sw128(sbase + L::kKVOff, 16, 1024)
+                                   : smem_desc_sw128(sbase + L::kKVOff, kBlockN * 128, 1024);
       uint32_t slot = 0, phase = 0;  // next K/V ring position
       uint32_t step = 0;             // K/V stream step (for the release groups)
       uint32_t q_par[2] = {0, 0}, p_par[2] = {0, 0}, o_cnt[2] = {0, 0};
@@ -383,8 +433,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             p_par[g] ^= 1u;
             if (!ok) break;
             tc_fence_after_sync();
-            mma_ts_mnmajor_x8(tmem + L::o_col(g), tmem + L::s_col(g),
-                              v_desc0 + prev_vslot * kSlotStep, kIdescO, prev_acc[g] ? 1u : 0u);
+            if constexpr (FP8)
+              mma_f8_ts_kmajor_x4(tmem + L::o_col(g), tmem + L::s_col(g),
+                                  v_desc0 + prev_vslot * kSlotStep, kIdescO,
+                                  prev_acc[g] ? 1u : 0u);
+            else
+              mma_ts_mnmajor_x8(tmem + L::o_col(g), tmem + L::s_col(g),
+                                v_desc0 + prev_vslot * kSlotStep, kIdescO, prev_acc[g] ? 1u : 0u);
             tc_commit(bar(L::kODone + g));
             ++o_cnt[g];
           }
@@ -399,7 +454,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             tc_fence_after_sync();
             const uint64_t a = q_desc0 + g * kSlotStep;
             const uint64_t b = k_desc0 + kslot * kSlotStep;
-            if constexpr (D == 128)
+            if constexpr (FP8)
+              mma_f8_ss_kmajor_x4(tmem + L::s_col(g), a, b, kIdescS, 0u);
+            else if constexpr (D == 128)
               mma_ss_kmajor_x8(tmem + L::s_col(g), a, b, kIdescS, 0u);
             else
               mma_ss_kmajor_x4(tmem + L::s_col(g), a, b, kIdescS, 0u);
@@ -496,7 +553,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             if (c >= hi || c < lo) s[c] = -INFINITY;
         }
         const float m_tile = tile_max(s) * scale_log2;
-        if (__any_sync(0xffffffffu, m_tile > m_ref + kRescaleThreshold)) {
+        if (__any_sync(0xffffffffu, m_tile > m_ref + kThreshold)) {
           const float m_new = fmaxf(m_ref, m_tile);
           const float factor = (m_new == -INFINITY) ? 1.f : ex2_approx(m_ref - m_new);
           if (n > t_n0) {
@@ -520,7 +577,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           l *= factor;
           m_ref = m_new;
         }
-        l += exp_tile_to_tmem<BF16>(s, scale_log2, (m_ref == -INFINITY) ? 0.f : m_ref, tS);
+        if constexpr (FP8)
+          l += exp_tile_to_tmem_e4m3(s, scale_log2,
+                                     ((m_ref == -INFINITY) ? 0.f : m_ref) - kFp8POffset, tS);
+        else
+          l += exp_tile_to_tmem<BF16>(s, scale_log2, (m_ref == -INFINITY) ? 0.f : m_ref, tS);
         tmem_wait_st();
         tc_fence_before_sync();
         mbar_arrive(bar(L::kPFull + g));
@@ -536,7 +597,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       if (!ok) break;
       tc_fence_after_sync();
 
-      const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+      // (FP8: l carries the 2^offset of P; O also takes the V descale)
+      const float inv_l = (l > 0.f) ? (FP8 ? p.descale_v : 1.f) / l : 0.f;
 #pragma unroll
       for (int c = 0; c < D; c += 32) {
         uint32_t o[32];
@@ -556,7 +618,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       }
       if (p.lse != nullptr && row < len) {
         p.lse[lse_base<PACKED>(p, w.sv) + row] =
-            (l > 0.f) ? (m_ref + log2f(l)) * 0.6931471805599453f : -INFINITY;
+            (l > 0.f) ? (m_ref + log2f(l) - (FP8 ? kFp8POffset : 0.f)) * 0.6931471805599453f
+                      : -INFINITY;
       }
       fence_proxy_async_smem();
       mbar_arrive(bar(L::kStageFull));

@@ -40,6 +40,12 @@ cudaError_t launch_bwd_d128(const BwdParams& p_kv, const BwdParams& p_q, const v
                             bool causal, bool bf16, int grid_kv, int grid_q, int num_sms,
                             cudaStream_t stream);
 
+// FP8 forward: V^T ([heads][d][n_pad] bytes, zero past N) from V
+// ([heads][N][d] bytes), then the d=128 E4M3 kernel (p.tm_v maps V^T).
+cudaError_t launch_transpose_v_e4m3(const void* v, void* vt, int num_heads, int N, int n_pad,
+                                    int d, int num_sms, cudaStream_t stream);
+cudaError_t launch_fwd_d128_fp8(const FaParams& p, bool causal, int grid, cudaStream_t stream);
+
 // Shape of a split-KV merge: num_bh heads of N rows of d columns; split s
 // holds keys [s * split_keys, (s + 1) * split_keys); query i may see keys
 // i - win_left .. i + win_right (both already clamped to [0, N]).

@@ -60,6 +60,7 @@ struct FaParams {  // 64-byte aligned through CUtensorMap
   int total_rows;    // rows of the packed tensors
   uint16_t* o_ptr;   // O (packed rows), for the row-by-row store of the last
                      // query tile of a sequence
+  float descale_v;   // FP8 kernels: V descale, applied to O in the epilogue
 };
 
 // Split-KV: unit u is split u % num_splits of base unit u / num_splits; the

@@ -516,6 +516,72 @@ __device__ __forceinline__ float ex2_approx(float x) {
 
 // Pack two floats (round to nearest even) into one 32-bit word: `lo` in the
 // low half, `hi` in the high half.
+// 4 back-to-back K=32 MMAs of kind::f8f6f4 (FP8 E4M3 x E4M3 -> fp32), both
+// operands K-major 128B-swizzled tiles in shared memory with 128-byte rows:
+// step k reads bytes [32k, 32k + 32) of every row (descriptor + 2k).  The
+// first step overwrites D unless `accumulate`.
+__device__ __forceinline__ void mma_f8_ss_kmajor_x4(uint32_t d_tmem, uint64_t a_desc,
+                                                    uint64_t b_desc, uint32_t idesc,
+                                                    uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred pf, pt;\n\t.reg .b64 ak, bk;\n\t"
+      "setp.ne.b32 pf, %4, 0;\n\t"
+      "setp.eq.b32 pt, %4, %4;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, pf;\n\t"
+      "add.s64 ak, %1, 2;\n\t"
+      "add.s64 bk, %2, 2;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], ak, bk, %3, pt;\n\t"
+      "add.s64 ak, %1, 4;\n\t"
+      "add.s64 bk, %2, 4;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], ak, bk, %3, pt;\n\t"
+      "add.s64 ak, %1, 6;\n\t"
+      "add.s64 bk, %2, 6;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], ak, bk, %3, pt;\n\t"
+      "}"
+      :
+      : "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// 4 back-to-back K=32 MMAs of kind::f8f6f4 with A in tensor memory (four
+// E4M3 elements per 32-bit column, so step k reads columns a_tmem + 8k) and
+// B a K-major 128B-swizzled tile with 128-byte rows (descriptor + 2k).
+__device__ __forceinline__ void mma_f8_ts_kmajor_x4(uint32_t d_tmem, uint32_t a_tmem,
+                                                    uint64_t b_desc, uint32_t idesc,
+                                                    uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred pf, pt;\n\t.reg .b64 bk;\n\t.reg .b32 ak;\n\t"
+      "setp.ne.b32 pf, %4, 0;\n\t"
+      "setp.eq.b32 pt, %4, %4;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, pf;\n\t"
+      "add.u32 ak, %1, 8;\n\t"
+      "add.s64 bk, %2, 2;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [ak], bk, %3, pt;\n\t"
+      "add.u32 ak, %1, 16;\n\t"
+      "add.s64 bk, %2, 4;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [ak], bk, %3, pt;\n\t"
+      "add.u32 ak, %1, 24;\n\t"
+      "add.s64 bk, %2, 6;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [ak], bk, %3, pt;\n\t"
+      "}"
+      :
+      : "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Four fp32 values rounded to nearest FP8 E4M3 (saturating to +-448), packed
+// into one 32-bit word, element k in byte k.
+__device__ __forceinline__ uint32_t pack4_e4m3(float a, float b, float c, float d) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(r)
+      : "f"(a), "f"(b), "f"(c), "f"(d));
+  return r;
+}
+
 // The low / high 16-bit element of a packed pair, widened to fp32 (exact).
 template <bool BF16>
 __device__ __forceinline__ float unpack_lo(uint32_t w) {

@@ -19,7 +19,9 @@ Workload 6 (one causal head of 32768 rows) runs through the split-KV entry
 point with the automatic split count (two launches per step: the split
 forward and the merge); its line adds the unsplit forward's time on the
 same inputs.  Workload 7 (16 causal sequences of 697..3646 rows packed along
-the rows) runs through the variable-length entry point.
+the rows) runs through the variable-length entry point, workload 8 (the
+headline shape with FP8 E4M3 inputs) through the FP8 entry point, whose
+roofline peak is the measured bf16 rate times the nominal fp8/bf16 ratio 2.
 
 ``--impl reference`` times the fp64 CPU oracle (the only other place this
 script runs it) on rank 0, on bounded row samples of the same workload.
@@ -308,7 +310,8 @@ def run_ours(args, wl):
         qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
         if i > 0:   # distinct copies (same values) so that no step hits L2
             qd, kd, vd = qd.clone(), kd.clone(), vd.clone()
-        sets.append((qd, kd, vd, torch.empty_like(qd),
+        sets.append((qd, kd, vd, torch.empty(qd.shape, dtype=torch.bfloat16, device=dev)
+                     if wl.dtype == "fp8" else torch.empty_like(qd),
                      torch.empty(lse_shape, dtype=torch.float32, device=dev)))
     stream = torch.cuda.Stream(device=dev)
     handle = stream.cuda_stream
@@ -331,7 +334,11 @@ def run_ours(args, wl):
         return need
 
     def call(qp, kp, vp, op, lp, Bc, Hc, plain=False):
-        if wl.varlen:
+        if wl.dtype == "fp8":
+            st_ = fa.fa_fwd_fp8(qp, kp, vp, op, lp, Bc, Hc, Hc, N, d, wl.scale, 1.0, 1.0, 1.0,
+                                int(wl.causal), -1, -1, fp8_ws.data_ptr(), fp8_ws.numel(),
+                                handle)
+        elif wl.varlen:
             st_ = fa.fa_fwd_varlen(qp, kp, vp, op, lp, cu_dev.data_ptr(), B, max_len, total, H,
                                    H, d, wl.scale, int(wl.causal), -1, -1, dcode, handle)
         elif wl.splitkv and not plain:
@@ -344,6 +351,13 @@ def run_ours(args, wl):
                             dcode, handle)
         if st_ != fa.FA_OK:
             raise RuntimeError(f"forward failed: {fa.fa_status_string(st_)}")
+
+    fp8_ws = None
+    if wl.dtype == "fp8":
+        # (two launches per call: the V transpose and the forward)
+        st_, need_ = fa.fa_fwd_fp8_workspace_bytes(B, H, N, d)
+        fp8_ws = torch.empty(max(need_, 256), dtype=torch.uint8, device=dev)
+        launches_per_call = 2
 
     splits_used = 1
     if wl.splitkv:
@@ -432,14 +446,16 @@ def run_ours(args, wl):
     else:
         rows_e2e, row_shape, l_shape = B * H, (B * H, N, d), (B * H, N)
     q_h, k_h, v_h = (t.reshape(row_shape).pin_memory() for t in (q, k, v))
-    o_h = torch.empty(row_shape, dtype=q.dtype).pin_memory()
+    o_h = torch.empty(row_shape, dtype=torch.bfloat16 if wl.dtype == "fp8" else q.dtype)
+    o_h = o_h.pin_memory()
     l_h = torch.empty(l_shape, dtype=torch.float32).pin_memory()
     if wl.varlen:
         q_h, k_h, v_h, o_h, l_h = (t.unsqueeze(0) for t in (q_h, k_h, v_h, o_h, l_h))
     n_chunks = max(1, min(8, rows_e2e))
     bounds = [(c * rows_e2e // n_chunks, (c + 1) * rows_e2e // n_chunks)
               for c in range(n_chunks)]
-    dq, dk, dv, do_ = (sets[0][t].view(q_h.shape) for t in range(4))
+    dq, dk, dv = (sets[0][t].view(q_h.shape) for t in range(3))
+    do_ = sets[0][3].view(o_h.shape)
     dl = sets[0][4].view(l_h.shape)
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     e2e_steps = max(1, min(args.steps, 20))
@@ -481,11 +497,17 @@ def run_ours(args, wl):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_ms = float(t.item())
     h2d = 3 * q.numel() * q.element_size()
-    d2h = q.numel() * q.element_size() + H * total * 4
+    d2h = o_h.numel() * o_h.element_size() + H * total * 4
 
     if rank == 0:
         peaks, src = _peaks()
         peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+        peak_note = f"{src} bf16_tflops (burst; kernel timed alone)"
+        if wl.dtype == "fp8":
+            # FP8 dense tensor rate: the bf16 measurement times the nominal
+            # 4.5 / 2.25 PFLOP/s ratio
+            peak *= 2.0
+            peak_note = f"{src} bf16_tflops x 2 (nominal fp8/bf16 dense ratio)"
         achieved = wl.flops / (ms_per_step / 1e3) / 1e12
         traffic, traffic_src = _profiled_traffic(wl.name)
         line = {
@@ -498,7 +520,7 @@ def run_ours(args, wl):
             "pct_of_peak": 100.0 * achieved / peak,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak,
-                         "peak_source": f"{src} bf16_tflops (burst; kernel timed alone)",
+                         "peak_source": peak_note,
                          "traffic": traffic, "traffic_source": traffic_src,
                          "algorithmic_hbm_bytes": wl.hbm_bytes},
             "e2e": {"value": world * wl.flops / (e2e_ms / 1e3) / 1e12, "unit": UNIT,

@@ -243,6 +243,40 @@ FA_API int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, v
                                   int dtype, int num_splits, void* stream);
 
 /*
+ * fa_fwd_fp8 -- attention forward on FP8 E4M3 inputs with descale factors.
+ *
+ * Source: flash-attention "hopper/flash_fwd_kernel.h" (its FP8 path:
+ * E4M3 Q, K, V with descale_q/k/v, the Q K^T descales folded into the
+ * softmax scale, P rounded to FP8 after an exponent offset ("Max_offset"),
+ * V's descale applied to O, a 16-bit output).
+ *
+ *   q        device pointer, contiguous [B][H][N][d] E4M3 bytes.
+ *   k, v     contiguous [B][H_kv][N][d] E4M3 bytes (grouped heads as in
+ *            fa_fwd_ext).  The real inputs are descale_q * q, descale_k * k,
+ *            descale_v * v (each factor finite and > 0).
+ *   o        contiguous [B][H][N][d] bfloat16 (written).
+ *   lse      [B][H][N] float32 natural-log LSE of the descaled scores, or NULL.
+ *   d        128 (else FA_ERR_UNSUPPORTED).
+ *   workspace  device scratch of at least fa_fwd_fp8_workspace_bytes()
+ *            bytes, 256-byte aligned: receives V transposed
+ *            ([B*H_kv][d][N rounded up to 128] bytes); need not be
+ *            initialised.
+ * P is rounded to E4M3 (3 mantissa bits) before the P V product: O carries
+ * a relative error of up to 2^-4 of the V values it averages (typically far
+ * less), while LSE is as accurate as in fa_fwd.  Enqueues two kernels (the V
+ * transpose, the forward).  Other arguments, alignment and errors as in
+ * fa_fwd_ext.
+ */
+FA_API int fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                      int H, int H_kv, int N, int d, float scale, float descale_q,
+                      float descale_k, float descale_v, int causal, int window_left,
+                      int window_right, void* workspace, unsigned long long workspace_bytes,
+                      void* stream);
+
+/* Workspace bytes of fa_fwd_fp8 for these sizes (written to *bytes). */
+FA_API int fa_fwd_fp8_workspace_bytes(int B, int H_kv, int N, int d, unsigned long long* bytes);
+
+/*
  * fa_bwd -- attention backward pass: dQ, dK, dV from Q, K, V, the forward's
  * O and LSE, and dO.
  *

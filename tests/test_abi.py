@@ -260,3 +260,31 @@ def test_bwd_argument_errors(fa, kw, code):
 
 def test_bwd_empty_is_noop(fa):
     assert _call_bwd(fa, N=0, ws=0, ws_bytes=0) == fa.FA_OK
+
+
+# -------------------------------------------------------------------- FP8
+def _call_fp8(fa, ws=0x100000, ws_bytes=1 << 30, dq=1.0, dk=1.0, dv=1.0, **kw):
+    a = dict(GOOD, H=2)
+    a.update(kw)
+    return fa.fa_fwd_fp8(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"],
+                         a.get("H_kv", a["H"]), a["N"], a["d"], a["scale"], dq, dk, dv,
+                         a["causal"], -1, -1, ws, ws_bytes, a["stream"])
+
+
+def test_fp8_workspace_size(fa):
+    st, n = fa.fa_fwd_fp8_workspace_bytes(2, 3, 300, 128)
+    assert st == fa.FA_OK and n == 2 * 3 * 128 * 384
+    assert fa.fa_fwd_fp8_workspace_bytes(2, 3, 300, 64)[0] == fa.FA_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=64), 2), (dict(d=256), 2), (dict(ws=0), 1), (dict(ws_bytes=16), 1),
+    (dict(ws=0x100080), 3), (dict(dq=0.0), 1), (dict(dk=float("nan")), 1), (dict(dv=-1.0), 1),
+    (dict(q=0x1008), 3), (dict(H_kv=3), 1),
+])
+def test_fp8_argument_errors(fa, kw, code):
+    assert _call_fp8(fa, **kw) == code
+
+
+def test_fp8_empty_is_noop(fa):
+    assert _call_fp8(fa, N=0, ws=0, ws_bytes=0) == fa.FA_OK

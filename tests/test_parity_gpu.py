@@ -265,9 +265,29 @@ def _varlen_workload_case(fa, wl):
     return err
 
 
+def _fp8_workload_case(fa, wl):
+    """E4M3 inputs (descales 1): LSE to 1e-3 and O within the E4M3 bound on P
+    (|dO| <= 2^-4 max|v| + 2^-8 max|O|, rms <= 2^-4/sqrt(3) rms(v)), in full."""
+    q, k, v = make_qkv(wl)
+    o, lse = fa.fwd_fp8(q.cuda(), k.cuda(), v.cuda(), scale=wl.scale, causal=wl.causal)
+    torch.cuda.synchronize()
+    st, site = fa.fa_get_device_status(None)
+    assert st == fa.FA_OK, f"device status {fa.fa_status_string(st)} at site {site}"
+    o_ref, l_ref = oracle.attention_fp8(q, k, v, wl.scale, 1.0, 1.0, 1.0, wl.causal)
+    o_np, l_np = o.float().cpu().numpy(), lse.cpu().numpy()
+    assert np.abs(l_np - l_ref).max() <= LSE_TOL
+    vv = v.float().numpy()
+    diff = np.abs(o_np - o_ref)
+    assert diff.max() <= 2.0 ** -4 * np.abs(vv).max() + 2.0 ** -8 * np.abs(o_ref).max()
+    assert np.sqrt((diff ** 2).mean()) <= 2.0 ** -4 / math.sqrt(3) * np.sqrt((vv ** 2).mean())
+    return float(diff.max()), float(np.abs(l_np - l_ref).max())
+
+
 def _workload_case(fa, wl, full):
     if wl.varlen:
         return _varlen_workload_case(fa, wl)
+    if wl.dtype == "fp8":
+        return _fp8_workload_case(fa, wl)
     q, k, v = make_qkv(wl)
     if wl.splitkv:
         o, lse = fa.fwd_splitkv(q.cuda(), k.cuda(), v.cuda(), scale=wl.scale,

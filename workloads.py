@@ -7,8 +7,9 @@ checks take their inputs from here, so the two sides always see the same
 
 Recipe: Q, K, V are drawn in that order from one ``torch.Generator`` seeded
 with ``1000 + config_index`` as float32 standard normals of shape [B,H,N,d],
-then rounded to nearest-even into the workload's 16-bit type.  The
-"peaky" workload multiplies Q and K by 2 after rounding (exact in bf16/fp16).
+then rounded to nearest-even into the workload's 16-bit type (or to FP8
+E4M3, saturating, for the fp8 workload).  The "peaky" workload multiplies Q
+and K by 2 after rounding (exact in bf16/fp16).
 Row samples for large workloads come from a second generator seeded with
 ``2000 + config_index``.
 """
@@ -28,7 +29,7 @@ class Workload:
     H: int
     N: int
     d: int
-    dtype: str            # "fp16" or "bf16"
+    dtype: str            # "fp16", "bf16" or "fp8" (E4M3 inputs, bf16 output)
     causal: bool
     qk_mult: float = 1.0  # Q and K multiplied by this after rounding
     splitkv: bool = False  # run through the split-KV entry point (automatic count)
@@ -55,7 +56,8 @@ class Workload:
 
     @property
     def torch_dtype(self):
-        return torch.float16 if self.dtype == "fp16" else torch.bfloat16
+        return {"fp16": torch.float16, "bf16": torch.bfloat16,
+                "fp8": torch.float8_e4m3fn}[self.dtype]
 
     @property
     def flops(self) -> float:
@@ -68,7 +70,8 @@ class Workload:
     def hbm_bytes(self) -> int:
         """Algorithmic HBM bytes: read Q, K, V; write O (16-bit) and LSE (fp32)."""
         rows = self.H * sum(self.seqlens())
-        return 4 * rows * self.d * 2 + rows * 4
+        in_bytes = 1 if self.dtype == "fp8" else 2
+        return 3 * rows * self.d * in_bytes + rows * self.d * 2 + rows * 4
 
     def describe(self) -> str:
         mask = "causal" if self.causal else "full"
@@ -95,6 +98,8 @@ WORKLOADS = [
     # 16 causal sequences of 256..4096 rows packed along the rows (a
     # variable-length training batch)
     Workload(7, "bf16_d128_varlen16_causal", 16, 16, 4096, 128, "bf16", True, varlen=True),
+    # the headline shape with FP8 E4M3 inputs (descale factors 1)
+    Workload(8, "fp8_d128_n2048", 4, 16, 2048, 128, "fp8", False),
 ]
 
 
