@@ -100,3 +100,26 @@ def test_deterministic(fa):
     torch.cuda.synchronize()
     st, _ = fa.fa_get_device_status(None)
     assert st == fa.FA_OK
+
+
+@pytest.mark.parametrize("index", [2, 3])
+def test_workload_size_heads(fa, index):
+    """The backward on a whole workload (B*H heads launched together); the
+    gradients of the first and the last head checked against the oracle run
+    on those heads alone."""
+    from workloads import make_qkv, workload
+    wl = workload(index)
+    q, k, v = make_qkv(wl)
+    do = torch.randn(q.shape, generator=torch.Generator().manual_seed(4000 + wl.index))
+    do = do.to(q.dtype)
+    qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
+    o, lse = fa.fwd(qd, kd, vd, scale=wl.scale, causal=wl.causal)
+    dq, dk, dv = fa.bwd(qd, kd, vd, o, lse, dod, scale=wl.scale, causal=wl.causal)
+    torch.cuda.synchronize()
+    st, site = fa.fa_get_device_status(None)
+    assert st == fa.FA_OK, f"device status {fa.fa_status_string(st)} at site {site}"
+    for (b, h) in ((0, 0), (wl.B - 1, wl.H - 1)):
+        sl = lambda t: t[b:b + 1, h:h + 1].contiguous()
+        ref = oracle.attention_bwd(sl(q), sl(k), sl(v), sl(do), wl.scale, wl.causal)
+        got = tuple(g[b:b + 1, h:h + 1] for g in (dq, dk, dv))
+        _check(got, ref, f"{wl.name} head ({b},{h})")
