@@ -45,6 +45,8 @@ SIGNATURES = {
     "fa_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _ull, _i, _i, _i, _i, _i, _f,
                 _i, _i, _i, _i, _vp], _i),
     "fa_bwd_workspace_bytes": ([_i, _i, _i, ctypes.POINTER(_ull)], _i),
+    "fa_bwd_varlen": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i,
+                       _f, _i, _i, _i, _i, _vp, _ull, _vp], _i),
     "fa_fwd_varlen": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _i, _i,
                        _vp], _i),
     "fa_fwd_splitkv": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _i, _i, _i,
@@ -132,6 +134,17 @@ def fa_bwd(q: int, k: int, v: int, o: int, lse: int, dout: int, dq: int, dk: int
     return int(_lib.fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, workspace or None,
                            int(workspace_bytes), B, H, H_kv, N, d, scale, causal, window_left,
                            window_right, dtype, stream or None))
+
+
+def fa_bwd_varlen(q: int, k: int, v: int, o: int, lse: int, dout: int, dq: int, dk: int,
+                  dv: int, cu_seqlens: int, batch: int, max_seqlen: int, total: int, H: int,
+                  H_kv: int, d: int, scale: float, causal: int, window_left: int,
+                  window_right: int, dtype: int, workspace: int | None, workspace_bytes: int,
+                  stream: int | None) -> int:
+    return int(_lib.fa_bwd_varlen(q, k, v, o, lse, dout, dq, dk, dv, cu_seqlens or None, batch,
+                                  max_seqlen, total, H, H_kv, d, scale, causal, window_left,
+                                  window_right, dtype, workspace or None, int(workspace_bytes),
+                                  stream or None))
 
 
 def fa_bwd_workspace_bytes(B: int, H: int, N: int) -> tuple[int, int]:
@@ -389,6 +402,37 @@ def bwd(q, k, v, o, lse, dout, *, scale: float | None = None, causal: bool = Fal
     return dq, dk, dv
 
 
+def bwd_varlen(q, k, v, o, lse, dout, cu_seqlens, max_seqlen: int, *,
+               scale: float | None = None, causal: bool = False,
+               window: tuple[int, int] = (-1, -1), workspace=None, stream=None):
+    """Gradients (dq, dk, dv) of ``fwd_varlen`` for packed sequences: q, o, dout
+    [total, H, d], k, v [total, H_kv, d], lse [H, total]."""
+    import torch
+    total, H, d = (int(x) for x in q.shape)
+    batch = int(cu_seqlens.numel()) - 1
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    with torch.cuda.device(q.device):
+        st, need = fa_bwd_workspace_bytes(max(batch, 0), H, int(max_seqlen))
+        if st != FA_OK:
+            raise FaError(st, "fa_bwd_workspace_bytes")
+        if workspace is None:
+            workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+        st = fa_bwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                           lse.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                           dv.data_ptr(), cu_seqlens.data_ptr(), max(batch, 0), int(max_seqlen),
+                           total, H, int(k.shape[1]), d, float(scale), int(bool(causal)),
+                           int(window[0]), int(window[1]), _dtype_code(q), workspace.data_ptr(),
+                           workspace.numel(), handle)
+    if st != FA_OK:
+        raise FaError(st, "fa_bwd_varlen")
+    return dq, dk, dv
+
+
 def fwd_splitkv(q, k, v, *, num_splits: int = 0, scale: float | None = None,
                 causal: bool = False, window: tuple[int, int] = (-1, -1), out=None,
                 lse=None, return_lse: bool = True, workspace=None, stream=None):
@@ -427,7 +471,7 @@ def fwd_splitkv(q, k, v, *, num_splits: int = 0, scale: float | None = None,
 __all__ = [
     "LIB_PATH", "SIGNATURES", "FaError", "fwd", "bwd", "fwd_fp8", "fwd_varlen", "fwd_splitkv",
     "fa_fwd", "fa_fwd_fp8", "fa_fwd_fp8_workspace_bytes",
-    "fa_bwd", "fa_bwd_workspace_bytes",
+    "fa_bwd", "fa_bwd_workspace_bytes", "fa_bwd_varlen", "bwd_varlen",
     "fa_fwd_ext", "fa_fwd_varlen",
     "fa_fwd_splitkv", "fa_splitkv_workspace_bytes", "fa_fwd_splitkv_noalloc",
     "fa_status_string",

@@ -665,25 +665,33 @@ int fa_bwd_workspace_bytes(int B, int H, int N, unsigned long long* bytes) {
   return FA_OK;
 }
 
-int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
-           const void* dout, void* dq, void* dk, void* dv, void* workspace,
-           unsigned long long workspace_bytes, int B, int H, int H_kv, int N, int d,
-           float scale, int causal, int window_left, int window_right, int dtype,
-           void* stream) {
-  using namespace fa;
+}  // extern "C"
+
+namespace fa {
+namespace {
+
+// fa_bwd and fa_bwd_varlen: B sequences of N rows ([B][H][N][d]), or, with
+// cu_seqlens, B packed sequences of at most N rows ([total][H][d]).
+int bwd_launch(const void* q, const void* k, const void* v, const void* o, const float* lse,
+               const void* dout, void* dq, void* dk, void* dv, void* workspace,
+               unsigned long long workspace_bytes, int B, int H, int H_kv, int N, int d,
+               float scale, int causal, int window_left, int window_right, int dtype,
+               void* stream, const int* cu_seqlens, int total) {
   const ForwardCall c{q, k, v, dq, nullptr, B, H, H_kv, N, d, scale, causal, window_left,
                       window_right, dtype, stream};
   int st = validate(c);
   if (st != FA_OK) return st;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-  if (empty_problem(c)) return FA_OK;
+  const bool packed = cu_seqlens != nullptr;
+  if (packed && total < 0) return FA_ERR_INVALID_ARG;
+  if (empty_problem(c) || (packed && total == 0)) return FA_OK;
   st = check_pointers(c);
   if (st != FA_OK) return st;
   if (o == nullptr || lse == nullptr || dout == nullptr || dk == nullptr || dv == nullptr ||
       workspace == nullptr)
     return FA_ERR_INVALID_ARG;
   if (!aligned(o, 16) || !aligned(dout, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
-      !aligned(lse, 4) || !aligned(workspace, 256))
+      !aligned(lse, 4) || !aligned(workspace, 256) || (packed && !aligned(cu_seqlens, 4)))
     return FA_ERR_MISALIGNED;
   unsigned long long need = 0;
   fa_bwd_workspace_bytes(B, H, N, &need);
@@ -700,11 +708,18 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
   const bool bf16 = dtype == FA_DTYPE_BF16;
   const int ibh = static_cast<int>(bh), ibkv = B * H_kv;
   BwdParams p;
-  if (!encode_qkvo_map(&p.tm_q, q, N, d, ibh, bf16, 128, d / 64) ||
-      !encode_qkvo_map(&p.tm_k, k, N, d, ibkv, bf16, 128, d / 64) ||
-      !encode_qkvo_map(&p.tm_v, v, N, d, ibkv, bf16, 128, d / 64) ||
-      !encode_qkvo_map(&p.tm_do, dout, N, d, ibh, bf16, 128, d / 64))
+  if (packed) {
+    if (!encode_packed_map(&p.tm_q, q, total, H, d, bf16, 128, d / 64) ||
+        !encode_packed_map(&p.tm_k, k, total, H_kv, d, bf16, 128, d / 64) ||
+        !encode_packed_map(&p.tm_v, v, total, H_kv, d, bf16, 128, d / 64) ||
+        !encode_packed_map(&p.tm_do, dout, total, H, d, bf16, 128, d / 64))
+      return FA_ERR_CUDA;
+  } else if (!encode_qkvo_map(&p.tm_q, q, N, d, ibh, bf16, 128, d / 64) ||
+             !encode_qkvo_map(&p.tm_k, k, N, d, ibkv, bf16, 128, d / 64) ||
+             !encode_qkvo_map(&p.tm_v, v, N, d, ibkv, bf16, 128, d / 64) ||
+             !encode_qkvo_map(&p.tm_do, dout, N, d, ibh, bf16, 128, d / 64)) {
     return FA_ERR_CUDA;
+  }
   const int n_pad = static_cast<int>(n_tiles * 128);
   float* lse2 = static_cast<float*>(workspace);
   float* dsum = lse2 + static_cast<long long>(ibh) * n_pad;
@@ -728,6 +743,8 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
   if (causal) p.win_right = 0;
   p.scale = scale;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.cu_seqlens = cu_seqlens;
+  p.total_rows = packed ? total : 0;
   BwdParams p_kv = p, p_q = p;
   p_kv.num_units = static_cast<int>(static_cast<long long>(ibkv) * n_tiles);
   p_q.num_units = static_cast<int>(bh * n_tiles);
@@ -743,6 +760,38 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
                 : launch_bwd_d128(p_kv, p_q, o, dout, lse, lse2, dsum, causal != 0, bf16,
                                   grid_kv, grid_q, info->num_sms, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" {
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+           const void* dout, void* dq, void* dk, void* dv, void* workspace,
+           unsigned long long workspace_bytes, int B, int H, int H_kv, int N, int d,
+           float scale, int causal, int window_left, int window_right, int dtype,
+           void* stream) {
+  return fa::bwd_launch(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, B, H,
+                        H_kv, N, d, scale, causal, window_left, window_right, dtype, stream,
+                        nullptr, 0);
+}
+
+int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                  const void* dout, void* dq, void* dk, void* dv, const int* cu_seqlens,
+                  int batch, int max_seqlen, int total, int H, int H_kv, int d, float scale,
+                  int causal, int window_left, int window_right, int dtype, void* workspace,
+                  unsigned long long workspace_bytes, void* stream) {
+  if (batch > 0 && H > 0 && max_seqlen > 0 && total > 0 && cu_seqlens == nullptr)
+    return FA_ERR_INVALID_ARG;
+  if (cu_seqlens == nullptr) {
+    // nothing to do only if the problem is empty; the checks are shared
+    if (batch < 0 || H < 0 || max_seqlen < 0 || total < 0) return FA_ERR_INVALID_ARG;
+    return FA_OK;
+  }
+  return fa::bwd_launch(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, batch,
+                        H, H_kv, max_seqlen, d, scale, causal, window_left, window_right, dtype,
+                        stream, cu_seqlens, total);
 }
 
 int fa_fwd_fp8_workspace_bytes(int B, int H_kv, int N, int d, unsigned long long* bytes) {

@@ -1,4 +1,5 @@
-// fa_bwd_d128.cu -- instantiations and launcher of the backward kernels, head dim 128.
+// fa_bwd_d128.cu -- instantiations and launcher of the backward kernels,
+// head dim 128.
 #include "fa_bwd_kernel.cuh"
 #include "fa_launch.h"
 
@@ -14,14 +15,14 @@ cudaError_t launch_all(const BwdParams& p_kv, const BwdParams& p_q, const void* 
   long long blocks = (threads + 255) / 256;
   if (blocks > static_cast<long long>(num_sms) * 8) blocks = static_cast<long long>(num_sms) * 8;
   if (blocks < 1) blocks = 1;
-  bwd::fa_bwd_prepass_kernel<128, BF16><<<static_cast<int>(blocks), 256, 0, stream>>>(
+  bwd::fa_bwd_prepass_kernel<128, BF16, false><<<static_cast<int>(blocks), 256, 0, stream>>>(
       static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), lse, lse2, dsum,
-      p_q.num_bh, p_q.N, p_q.n_pad);
+      p_q.num_bh, p_q.N, p_q.n_pad, p_q);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   constexpr int kSmem = bwd::Layout<128>::kSmemBytes;
-  auto kv = bwd::fa_bwd_dkdv_kernel<128, CAUSAL, BF16>;
-  auto dq = bwd::fa_bwd_dq_kernel<128, CAUSAL, BF16>;
+  auto kv = bwd::fa_bwd_dkdv_kernel<128, CAUSAL, BF16, false>;
+  auto dq = bwd::fa_bwd_dq_kernel<128, CAUSAL, BF16, false>;
   e = cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(dq, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
@@ -39,6 +40,9 @@ cudaError_t launch_bwd_d128(const BwdParams& p_kv, const BwdParams& p_q, const v
                             const void* dout, const float* lse, float* lse2, float* dsum,
                             bool causal, bool bf16, int grid_kv, int grid_q, int num_sms,
                             cudaStream_t stream) {
+  if (p_q.cu_seqlens != nullptr)
+    return launch_bwd_d128_packed(p_kv, p_q, o, dout, lse, lse2, dsum, causal, bf16, grid_kv,
+                                  grid_q, num_sms, stream);
   if (causal)
     return bf16 ? launch_all<true, true>(p_kv, p_q, o, dout, lse, lse2, dsum, grid_kv, grid_q,
                                          num_sms, stream)

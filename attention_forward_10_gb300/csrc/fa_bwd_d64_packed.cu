@@ -1,0 +1,54 @@
+// fa_bwd_d64_packed.cu -- instantiations and launcher of the backward kernels,
+// head dim 64 (packed variable-length batches).
+#include "fa_bwd_kernel.cuh"
+#include "fa_launch.h"
+
+namespace fa {
+namespace {
+
+template <bool CAUSAL, bool BF16>
+cudaError_t launch_all(const BwdParams& p_kv, const BwdParams& p_q, const void* o,
+                       const void* dout, const float* lse, float* lse2, float* dsum,
+                       int grid_kv, int grid_q, int num_sms, cudaStream_t stream) {
+  // pre-pass: D/8 threads per padded row, grid-stride over num_sms * 8 blocks
+  const long long threads = static_cast<long long>(p_q.num_bh) * p_q.n_pad * (64 / 8);
+  long long blocks = (threads + 255) / 256;
+  if (blocks > static_cast<long long>(num_sms) * 8) blocks = static_cast<long long>(num_sms) * 8;
+  if (blocks < 1) blocks = 1;
+  bwd::fa_bwd_prepass_kernel<64, BF16, true><<<static_cast<int>(blocks), 256, 0, stream>>>(
+      static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), lse, lse2, dsum,
+      p_q.num_bh, p_q.N, p_q.n_pad, p_q);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  constexpr int kSmem = bwd::Layout<64>::kSmemBytes;
+  auto kv = bwd::fa_bwd_dkdv_kernel<64, CAUSAL, BF16, true>;
+  auto dq = bwd::fa_bwd_dq_kernel<64, CAUSAL, BF16, true>;
+  e = cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(dq, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
+  kv<<<grid_kv, bwd::kThreads, kSmem, stream>>>(p_kv);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  dq<<<grid_q, bwd::kThreads, kSmem, stream>>>(p_q);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_d64_packed(const BwdParams& p_kv, const BwdParams& p_q, const void* o,
+                                  const void* dout, const float* lse, float* lse2, float* dsum,
+                                  bool causal, bool bf16, int grid_kv, int grid_q, int num_sms,
+                                  cudaStream_t stream) {
+  if (causal)
+    return bf16 ? launch_all<true, true>(p_kv, p_q, o, dout, lse, lse2, dsum, grid_kv, grid_q,
+                                         num_sms, stream)
+                : launch_all<true, false>(p_kv, p_q, o, dout, lse, lse2, dsum, grid_kv, grid_q,
+                                          num_sms, stream);
+  return bf16 ? launch_all<false, true>(p_kv, p_q, o, dout, lse, lse2, dsum, grid_kv, grid_q,
+                                        num_sms, stream)
+              : launch_all<false, false>(p_kv, p_q, o, dout, lse, lse2, dsum, grid_kv, grid_q,
+                                         num_sms, stream);
+}
+
+}  // namespace fa

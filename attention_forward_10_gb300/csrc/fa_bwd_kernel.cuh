@@ -81,11 +81,14 @@ __device__ __forceinline__ bool admissible(int i, int j, int N, int wl, int wr) 
 // nlse2[bh][i] = -LSE * log2(e) and ndsum[bh][i] = -sum_c dO[i][c] O[i][c]
 // for i < N; -inf and 0 for the padding rows up to n_pad.  d/8 threads per
 // row.
-template <int D, bool BF16>
+// (PACKED: O and dO are [total][H][d], LSE [H][total]; row i of sequence b
+// is packed row cu_seqlens[b] + i, and rows past the sequence are padding.)
+template <int D, bool BF16, bool PACKED>
 __global__ void __launch_bounds__(256)
     fa_bwd_prepass_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
                           const float* __restrict__ lse, float* __restrict__ lse2,
-                          float* __restrict__ dsum, int num_bh, int N, int n_pad) {
+                          float* __restrict__ dsum, int num_bh, int N, int n_pad,
+                          const BwdParams p) {
   constexpr int kTpr = D / 8;
   const long long rows = static_cast<long long>(num_bh) * n_pad;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
@@ -97,10 +100,18 @@ __global__ void __launch_bounds__(256)
     const int part = static_cast<int>(gid % kTpr);
     const bool live = r < rows;
     const int bh = live ? static_cast<int>(r / n_pad) : 0;
-    const int i = live ? static_cast<int>(r % n_pad) : N;
+    const int i = live ? static_cast<int>(r % n_pad) : n_pad;
+    int row_base = 0, len = N;
+    if (PACKED && live) bwd_sequence<true>(p, bh / p.H, &row_base, &len);
+    const bool valid = i < len;
+    // element offset of row i of head bh, and the LSE index
+    const long long off =
+        PACKED ? ((static_cast<long long>(row_base) + i) * p.H + bh % p.H) * D + part * 8
+               : (static_cast<long long>(bh) * N + i) * D + part * 8;
+    const long long lidx = PACKED ? static_cast<long long>(bh % p.H) * p.total_rows + row_base + i
+                                  : static_cast<long long>(bh) * N + i;
     float acc = 0.f;
-    if (i < N) {
-      const long long off = (static_cast<long long>(bh) * N + i) * D + part * 8;
+    if (valid) {
       const uint4 a = *reinterpret_cast<const uint4*>(o + off);
       const uint4 b = *reinterpret_cast<const uint4*>(dout + off);
       const uint32_t wa[4] = {a.x, a.y, a.z, a.w};
@@ -114,8 +125,7 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
     for (int off = kTpr / 2; off > 0; off /= 2) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (live && part == 0) {
-      lse2[r] = (i < N) ? lse[static_cast<long long>(bh) * N + i] * -1.4426950408889634f
-                        : -INFINITY;
+      lse2[r] = valid ? lse[lidx] * -1.4426950408889634f : -INFINITY;
       dsum[r] = -acc;
     }
   }
@@ -173,10 +183,12 @@ struct KvUnit {
   int bkv;        // K/V head (b * H_kv + h_kv)
   int n;          // key tile
   int m_lo, nm;   // query tiles [m_lo, m_lo + nm) per query head
-  int steps;      // group * nm
+  int steps;      // group * nm (0: nothing to do)
+  int row_base;   // first row of the sequence (packed batches; else 0)
+  int len;        // rows of the sequence (N unless packed)
 };
 
-template <bool CAUSAL>
+template <bool CAUSAL, bool PACKED>
 __device__ __forceinline__ KvUnit decode_kv_unit(int u, const BwdParams& p) {
   KvUnit w;
   if (CAUSAL) {
@@ -187,17 +199,18 @@ __device__ __forceinline__ KvUnit decode_kv_unit(int u, const BwdParams& p) {
     w.bkv = u / p.n_tiles;
     w.n = u % p.n_tiles;
   }
+  bwd_sequence<PACKED>(p, w.bkv / p.H_kv, &w.row_base, &w.len);
   const long long lo = static_cast<long long>(w.n) * 128 - p.win_right;
   const long long hi = static_cast<long long>(w.n) * 128 + 128 + p.win_left;  // exclusive
   const int row_lo = lo < 0 ? 0 : static_cast<int>(lo);
-  const int row_hi = hi > p.N ? p.N : static_cast<int>(hi);
+  const int row_hi = hi > w.len ? w.len : static_cast<int>(hi);
   w.m_lo = row_lo / 128;
-  w.nm = row_hi > row_lo ? (row_hi + 127) / 128 - w.m_lo : 0;
+  w.nm = (row_hi > row_lo && w.n * 128 < w.len) ? (row_hi + 127) / 128 - w.m_lo : 0;
   w.steps = p.group * w.nm;
   return w;
 }
 
-template <int D, bool CAUSAL, bool BF16>
+template <int D, bool CAUSAL, bool BF16, bool PACKED>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
   using L = Layout<D>;
@@ -247,14 +260,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t it = 0, units = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++units) {
-        const KvUnit w = decode_kv_unit<CAUSAL>(u, p);
-        ok = wait_bar(bar(L::kFixEmpty), (units & 1u) ^ 1u, ctl, kSiteProducerKV);
+      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+        const KvUnit w = decode_kv_unit<CAUSAL, PACKED>(u, p);
+        if (w.steps == 0) continue;  // a key tile past a shorter sequence's end
+        const uint32_t uix = units++;
+        ok = wait_bar(bar(L::kFixEmpty), (uix & 1u) ^ 1u, ctl, kSiteProducerKV);
         if (!ok) break;
         mbar_arrive_expect_tx(bar(L::kFixFull), 2 * L::kTile);
-        tma_load_4d(sbase + kKOff, &p.tm_k, bar(L::kFixFull), 0, w.n * 128, 0, w.bkv);
-        tma_load_4d(sbase + kVOff, &p.tm_v, bar(L::kFixFull), 0, w.n * 128, 0, w.bkv);
         const int b = w.bkv / p.H_kv, hk = w.bkv % p.H_kv;
+        // (packed: rows of the sequence, heads within the row)
+        const int kv_head_c = PACKED ? hk : w.bkv;
+        tma_load_4d(sbase + kKOff, &p.tm_k, bar(L::kFixFull), 0, w.row_base + w.n * 128, 0,
+                    kv_head_c);
+        tma_load_4d(sbase + kVOff, &p.tm_v, bar(L::kFixFull), 0, w.row_base + w.n * 128, 0,
+                    kv_head_c);
         for (int s = 0; s < w.steps && ok; ++s, ++it) {
           const int bh = b * p.H + hk * p.group + s / w.nm;
           const int m = w.m_lo + s % w.nm;
@@ -265,8 +284,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t ring = sbase + L::kRingOff + st * 2 * L::kTile;
           const uint32_t vec = sbase + L::kVecOff + st * 1024;
           mbar_arrive_expect_tx(bar(L::kRingFull + st), 2 * L::kTile + 1024);
-          tma_load_4d(ring, &p.tm_q, bar(L::kRingFull + st), 0, m * 128, 0, bh);
-          tma_load_4d(ring + L::kTile, &p.tm_do, bar(L::kRingFull + st), 0, m * 128, 0, bh);
+          const int q_head_c = PACKED ? bh % p.H : bh;
+          tma_load_4d(ring, &p.tm_q, bar(L::kRingFull + st), 0, w.row_base + m * 128, 0,
+                      q_head_c);
+          tma_load_4d(ring + L::kTile, &p.tm_do, bar(L::kRingFull + st), 0,
+                      w.row_base + m * 128, 0, q_head_c);
           const long long voff = static_cast<long long>(bh) * p.n_pad + m * 128;
           bulk_load_1d(vec, p.lse2 + voff, 512, bar(L::kRingFull + st));
           bulk_load_1d(vec + 512, p.dsum + voff, 512, bar(L::kRingFull + st));
@@ -288,9 +310,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t v_desc = smem_desc_sw128(sbase + kVOff, 16, 1024);
       uint32_t it = 0, units = 0, pr = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++units) {
-        const KvUnit w = decode_kv_unit<CAUSAL>(u, p);
-        ok = wait_bar(bar(L::kFixFull), units & 1u, ctl, kSiteMmaK);
+      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+        const KvUnit w = decode_kv_unit<CAUSAL, PACKED>(u, p);
+        if (w.steps == 0) continue;  // a key tile past a shorter sequence's end
+        const uint32_t uix = units++;
+        ok = wait_bar(bar(L::kFixFull), uix & 1u, ctl, kSiteMmaK);
         if (!ok) break;
         for (int s = 0; s < w.steps; ++s, ++it) {
           const uint32_t st = it % L::kStages;
@@ -312,9 +336,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = wait_bar(bar(L::kPReady), pr, ctl, kSiteMmaP);
           pr ^= 1u;
           if (!ok) break;
-          if (s == 0 && units > 0) {
+          if (s == 0 && uix > 0) {
             // the previous unit's dK, dV must have been read out
-            ok = wait_bar(bar(L::kAccFree), (units - 1) & 1u, ctl, kSiteMmaO);
+            ok = wait_bar(bar(L::kAccFree), (uix - 1) & 1u, ctl, kSiteMmaO);
             if (!ok) break;
           }
           tc_fence_after_sync();
@@ -349,8 +373,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = p.scale_log2;
     uint32_t it = 0, units = 0, sf = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++units) {
-      const KvUnit w = decode_kv_unit<CAUSAL>(u, p);
+    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+      const KvUnit w = decode_kv_unit<CAUSAL, PACKED>(u, p);
+      if (w.steps == 0) continue;
+      const uint32_t uix = units++;
       const int j = w.n * 128 + t;  // this thread's key
       for (int s = 0; s < w.steps; ++s, ++it) {
         const uint32_t st = it % L::kStages;
@@ -365,8 +391,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float* ndsum = nlse2 + 128;
         const int i0 = m * 128 + c;  // query of column c
         const bool need_mask = (w.n * 128 + 127 - i0 > p.win_right) ||
-                               (w.n * 128 - (i0 + 63) < -p.win_left) || (w.n * 128 + 128 > p.N);
-        const int N = p.N, wl = p.win_left, wr = p.win_right;
+                               (w.n * 128 - (i0 + 63) < -p.win_left) ||
+                               (w.n * 128 + 128 > w.len);
+        const int N = w.len, wl = p.win_left, wr = p.win_right;
         auto keep = [&](int e) { return admissible(i0 + e, j, N, wl, wr); };
         if (need_mask)
           p_ds_half<BF16, true, true, true>(tS, tDP, tDP + c, c, sl2, nlse2, ndsum, 0.f, 0.f, keep);
@@ -379,11 +406,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       // ---- epilogue: warps 0-3 write dV, warps 4-7 scale * dK (this thread's key row)
-      ok = wait_bar(bar(L::kAccDone), units & 1u, ctl, kSiteEpilogueO);
+      ok = wait_bar(bar(L::kAccDone), uix & 1u, ctl, kSiteEpilogueO);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after_sync();
-      const long long row = static_cast<long long>(w.bkv) * p.N + j;
+      // dV / dK row j of K/V head bkv ([B*H_kv][N][d], or packed [total][H_kv][d])
+      const long long row = PACKED ? (static_cast<long long>(w.row_base) + j) * p.H_kv +
+                                         w.bkv % p.H_kv
+                                   : static_cast<long long>(w.bkv) * p.N + j;
       uint16_t* dst = (half == 0 ? p.dv : p.dk) + row * D;
       const float mul = half == 0 ? 1.f : p.scale;
 #pragma unroll 1
@@ -394,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e)
           w4[e] = pack2<BF16>(__uint_as_float(r[2 * e]) * mul, __uint_as_float(r[2 * e + 1]) * mul);
-        if (j < p.N) {
+        if (j < w.len) {
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4)
             *reinterpret_cast<uint4*>(dst + c0 + q4 * 8) =
@@ -417,13 +447,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // --------------------------------------------------------------- dQ kernel
 struct QUnit {
-  int bh;      // query head
-  int bkv;     // its K/V head
-  int m;       // query tile
-  int n0, n1;  // key tiles [n0, n1)
+  int bh;        // query head
+  int bkv;       // its K/V head
+  int m;         // query tile
+  int n0, n1;    // key tiles [n0, n1) (empty: nothing to do)
+  int row_base;  // first row of the sequence (packed batches; else 0)
+  int len;       // rows of the sequence (N unless packed)
 };
 
-template <bool CAUSAL>
+template <bool CAUSAL, bool PACKED>
 __device__ __forceinline__ QUnit decode_q_unit(int u, const BwdParams& p) {
   QUnit w;
   if (CAUSAL) {
@@ -434,12 +466,22 @@ __device__ __forceinline__ QUnit decode_q_unit(int u, const BwdParams& p) {
     w.m = u % p.n_tiles;
   }
   w.bkv = kv_head(w.bh, p.H, p.group);
-  key_tile_range(w.m * 128, min(p.N, w.m * 128 + 128), p.N, p.win_left, p.win_right, 128,
+  bwd_sequence<PACKED>(p, w.bh / p.H, &w.row_base, &w.len);
+  if (PACKED && CAUSAL) {
+    // count the tiles from each sequence's end (its heaviest tiles first)
+    w.m = (w.len + 127) / 128 - 1 - (p.n_tiles - 1 - w.m);
+    if (w.m < 0) w.m = p.n_tiles;
+  }
+  if (w.m * 128 >= w.len) {
+    w.n0 = w.n1 = 0;
+    return w;
+  }
+  key_tile_range(w.m * 128, min(w.len, w.m * 128 + 128), w.len, p.win_left, p.win_right, 128,
                  &w.n0, &w.n1);
   return w;
 }
 
-template <int D, bool CAUSAL, bool BF16>
+template <int D, bool CAUSAL, bool BF16, bool PACKED>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
   using L = Layout<D>;
@@ -489,13 +531,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t it = 0, units = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++units) {
-        const QUnit w = decode_q_unit<CAUSAL>(u, p);
-        ok = wait_bar(bar(L::kFixEmpty), (units & 1u) ^ 1u, ctl, kSiteProducerQ);
+      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+        const QUnit w = decode_q_unit<CAUSAL, PACKED>(u, p);
+        if (w.n1 == w.n0) continue;  // a query tile past a shorter sequence's end
+        const uint32_t uix = units++;
+        ok = wait_bar(bar(L::kFixEmpty), (uix & 1u) ^ 1u, ctl, kSiteProducerQ);
         if (!ok) break;
         mbar_arrive_expect_tx(bar(L::kFixFull), 2 * L::kTile);
-        tma_load_4d(sbase + kQOff, &p.tm_q, bar(L::kFixFull), 0, w.m * 128, 0, w.bh);
-        tma_load_4d(sbase + kDOOff, &p.tm_do, bar(L::kFixFull), 0, w.m * 128, 0, w.bh);
+        // (packed: rows of the sequence, heads within the row)
+        const int q_head_c = PACKED ? w.bh % p.H : w.bh;
+        const int kv_head_c = PACKED ? w.bkv % p.H_kv : w.bkv;
+        tma_load_4d(sbase + kQOff, &p.tm_q, bar(L::kFixFull), 0, w.row_base + w.m * 128, 0,
+                    q_head_c);
+        tma_load_4d(sbase + kDOOff, &p.tm_do, bar(L::kFixFull), 0, w.row_base + w.m * 128, 0,
+                    q_head_c);
         for (int n = w.n0; n < w.n1 && ok; ++n, ++it) {
           const uint32_t st = it % L::kStages;
           ok = wait_bar(bar(L::kRingEmpty + st), ((it / L::kStages) & 1u) ^ 1u, ctl,
@@ -503,8 +552,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           const uint32_t ring = sbase + L::kRingOff + st * 2 * L::kTile;
           mbar_arrive_expect_tx(bar(L::kRingFull + st), 2 * L::kTile);
-          tma_load_4d(ring, &p.tm_k, bar(L::kRingFull + st), 0, n * 128, 0, w.bkv);
-          tma_load_4d(ring + L::kTile, &p.tm_v, bar(L::kRingFull + st), 0, n * 128, 0, w.bkv);
+          tma_load_4d(ring, &p.tm_k, bar(L::kRingFull + st), 0, w.row_base + n * 128, 0,
+                      kv_head_c);
+          tma_load_4d(ring + L::kTile, &p.tm_v, bar(L::kRingFull + st), 0, w.row_base + n * 128,
+                      0, kv_head_c);
         }
       }
       const uint32_t first = it > (uint32_t)L::kStages ? it - L::kStages : 0u;
@@ -522,9 +573,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t do_desc = smem_desc_sw128(sbase + kDOOff, 16, 1024);
       uint32_t it = 0, units = 0, pr = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++units) {
-        const QUnit w = decode_q_unit<CAUSAL>(u, p);
-        ok = wait_bar(bar(L::kFixFull), units & 1u, ctl, kSiteMmaQ);
+      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+        const QUnit w = decode_q_unit<CAUSAL, PACKED>(u, p);
+        if (w.n1 == w.n0) continue;  // a query tile past a shorter sequence's end
+        const uint32_t uix = units++;
+        ok = wait_bar(bar(L::kFixFull), uix & 1u, ctl, kSiteMmaQ);
         if (!ok) break;
         for (int n = w.n0; n < w.n1; ++n, ++it) {
           const uint32_t st = it % L::kStages;
@@ -547,8 +600,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = wait_bar(bar(L::kPReady), pr, ctl, kSiteMmaP);
           pr ^= 1u;
           if (!ok) break;
-          if (n == w.n0 && units > 0) {
-            ok = wait_bar(bar(L::kAccFree), (units - 1) & 1u, ctl, kSiteMmaO);
+          if (n == w.n0 && uix > 0) {
+            ok = wait_bar(bar(L::kAccFree), (uix - 1) & 1u, ctl, kSiteMmaO);
             if (!ok) break;
           }
           tc_fence_after_sync();
@@ -577,13 +630,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = p.scale_log2;
     uint32_t units = 0, sf = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x, ++units) {
-      const QUnit w = decode_q_unit<CAUSAL>(u, p);
+    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+      const QUnit w = decode_q_unit<CAUSAL, PACKED>(u, p);
+      if (w.n1 == w.n0) continue;
+      const uint32_t uix = units++;
       const int i = w.m * 128 + t;
       const long long vrow = static_cast<long long>(w.bh) * p.n_pad + i;
       const float nlse2 = p.lse2[vrow];
       const float ndsum = p.dsum[vrow];
-      const int row_end = min(p.N, w.m * 128 + 128);
+      const int row_end = min(w.len, w.m * 128 + 128);
       for (int n = w.n0; n < w.n1; ++n) {
         ok = wait_bar(bar(L::kSFull), sf, ctl, kSiteSoftmaxS);
         sf ^= 1u;
@@ -591,9 +646,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc_fence_after_sync();
         const int kbase = n * 128 + c;  // key of column c
-        const bool need_mask = (kbase + 64 > p.N) || (kbase + 63 > w.m * 128 + p.win_right) ||
+        const bool need_mask = (kbase + 64 > w.len) ||
+                               (kbase + 63 > w.m * 128 + p.win_right) ||
                                (kbase < row_end - 1 - p.win_left);
-        const int N = p.N, wl = p.win_left, wr = p.win_right;
+        const int N = w.len, wl = p.win_left, wr = p.win_right;
         auto keep = [&](int e) { return admissible(i, kbase + e, N, wl, wr); };
         if (need_mask)
           p_ds_half<BF16, true, false, false>(tS, tDP, tS + c, c, sl2, nullptr, nullptr, nlse2,
@@ -607,11 +663,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       // ---- epilogue: scale * dQ, columns [D/2 half, +D/2) of this thread's row
-      ok = wait_bar(bar(L::kAccDone), units & 1u, ctl, kSiteEpilogueO);
+      ok = wait_bar(bar(L::kAccDone), uix & 1u, ctl, kSiteEpilogueO);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after_sync();
-      uint16_t* dst = p.dq + (static_cast<long long>(w.bh) * p.N + i) * D + half * (D / 2);
+      // dQ row i of head bh ([B*H][N][d], or packed [total][H][d])
+      const long long qrow = PACKED ? (static_cast<long long>(w.row_base) + i) * p.H + w.bh % p.H
+                                    : static_cast<long long>(w.bh) * p.N + i;
+      uint16_t* dst = p.dq + qrow * D + half * (D / 2);
 #pragma unroll 1
       for (int c0 = 0; c0 < D / 2; c0 += 32) {
         uint32_t r[32];
@@ -621,7 +680,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 16; ++e)
           w4[e] = pack2<BF16>(__uint_as_float(r[2 * e]) * p.scale,
                               __uint_as_float(r[2 * e + 1]) * p.scale);
-        if (i < p.N) {
+        if (i < w.len) {
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4)
             *reinterpret_cast<uint4*>(dst + c0 + q4 * 8) =

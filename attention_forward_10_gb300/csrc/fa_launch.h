@@ -39,6 +39,16 @@ cudaError_t launch_bwd_d128(const BwdParams& p_kv, const BwdParams& p_q, const v
                             const void* dout, const float* lse, float* lse2, float* dsum,
                             bool causal, bool bf16, int grid_kv, int grid_q, int num_sms,
                             cudaStream_t stream);
+// The same for packed variable-length batches (p.cu_seqlens set); the two
+// launchers above forward to these.
+cudaError_t launch_bwd_d64_packed(const BwdParams& p_kv, const BwdParams& p_q, const void* o,
+                                  const void* dout, const float* lse, float* lse2, float* dsum,
+                                  bool causal, bool bf16, int grid_kv, int grid_q, int num_sms,
+                                  cudaStream_t stream);
+cudaError_t launch_bwd_d128_packed(const BwdParams& p_kv, const BwdParams& p_q, const void* o,
+                                   const void* dout, const float* lse, float* lse2,
+                                   float* dsum, bool causal, bool bf16, int grid_kv, int grid_q,
+                                   int num_sms, cudaStream_t stream);
 
 // FP8 forward: V^T ([heads][d][n_pad] bytes, zero past N) from V
 // ([heads][N][d] bytes), then the d=128 E4M3 kernel (p.tm_v maps V^T).

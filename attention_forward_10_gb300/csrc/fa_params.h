@@ -92,7 +92,29 @@ struct BwdParams {  // 64-byte aligned through CUtensorMap
   int H, H_kv, group;
   int win_left, win_right;  // clamped to [0, N]; win_right = 0 when causal
   float scale, scale_log2;
+  // packed variable-length batches (nullptr / 0 otherwise): tensors are
+  // [total_rows][heads][d], sequence b is rows cu_seqlens[b] .. cu_seqlens[b+1]-1,
+  // N is the longest sequence and num_bh = batch * H
+  const int* cu_seqlens;
+  int total_rows;
 };
+
+// Row offset and length of sequence b of a backward launch (clamped as in
+// seq_view: a malformed cu_seqlens only shortens sequences).
+template <bool PACKED>
+__device__ __forceinline__ void bwd_sequence(const BwdParams& p, int b, int* row_base,
+                                             int* len) {
+  if constexpr (!PACKED) {
+    *row_base = 0;
+    *len = p.N;
+  } else {
+    int r0 = p.cu_seqlens[b], r1 = p.cu_seqlens[b + 1];
+    r0 = r0 < 0 ? 0 : (r0 > p.total_rows ? p.total_rows : r0);
+    r1 = r1 < r0 ? r0 : (r1 > p.total_rows ? p.total_rows : r1);
+    *row_base = r0;
+    *len = (r1 - r0 < p.N) ? r1 - r0 : p.N;
+  }
+}
 
 // Rows of one (b, h) attention problem: its sequence's first packed row, its
 // length, and the head coordinates of its Q, O and K/V in the tensor maps.

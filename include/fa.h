@@ -306,6 +306,21 @@ FA_API int fa_bwd(const void* q, const void* k, const void* v, const void* o,
                   int H_kv, int N, int d, float scale, int causal, int window_left,
                   int window_right, int dtype, void* stream);
 
+/*
+ * fa_bwd_varlen -- fa_bwd over packed variable-length batches: q, o, dout, dq
+ * are [total][H][d], k, v, dk, dv [total][H_kv][d], lse [H][total] (as written
+ * by fa_fwd_varlen), with cu_seqlens, batch, max_seqlen and total as in
+ * fa_fwd_varlen (offsets clamped by the kernels).  The workspace is
+ * fa_bwd_workspace_bytes(batch, H, max_seqlen).  Rows outside every sequence
+ * are not written.  Other rules as in fa_bwd.
+ */
+FA_API int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                         const int* cu_seqlens, int batch, int max_seqlen, int total, int H,
+                         int H_kv, int d, float scale, int causal, int window_left,
+                         int window_right, int dtype, void* workspace,
+                         unsigned long long workspace_bytes, void* stream);
+
 /* Workspace bytes of fa_bwd for these sizes (written to *bytes). */
 FA_API int fa_bwd_workspace_bytes(int B, int H, int N, unsigned long long* bytes);
 

@@ -288,3 +288,20 @@ def test_fp8_argument_errors(fa, kw, code):
 
 def test_fp8_empty_is_noop(fa):
     assert _call_fp8(fa, N=0, ws=0, ws_bytes=0) == fa.FA_OK
+
+
+def test_bwd_varlen_argument_errors(fa):
+    args = dict(q=0x1000, k=0x2000, v=0x3000, o=0x7000, lse=0x8000, do=0x9000, dq=0xA000,
+                dk=0xB000, dv=0xC000)
+    base = [args[n] for n in ("q", "k", "v", "o", "lse", "do", "dq", "dk", "dv")]
+    call = lambda cu, batch=2, ms=300, total=500, H=4, H_kv=2, d=128, ws=0x100000: \
+        fa.fa_bwd_varlen(*base, cu, batch, ms, total, H, H_kv, d, 0.1, 0, -1, -1, 1, ws,
+                         1 << 30, None)
+    assert call(0) == fa.FA_ERR_INVALID_ARG              # no offsets
+    assert call(0x6002) == fa.FA_ERR_MISALIGNED          # misaligned offsets
+    assert call(0x6000, d=256) == fa.FA_ERR_UNSUPPORTED
+    assert call(0x6000, H_kv=3) == fa.FA_ERR_INVALID_ARG
+    assert call(0x6000, total=-1) == fa.FA_ERR_INVALID_ARG
+    assert call(0x6000, ws=0x100010) == fa.FA_ERR_MISALIGNED
+    assert call(0x6000, total=0) == fa.FA_OK             # empty
+    assert call(0, batch=0) == fa.FA_OK

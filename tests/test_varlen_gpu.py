@@ -169,3 +169,60 @@ def test_malformed_offsets_stay_in_bounds(fa):
     assert (og == 0x7FC1).all()
     lg = torch.cat([lbuf[:G], lbuf[G + H * total:]]).cpu()
     assert (lg == -7.25).all()
+
+
+# ---------------------------------------------------------------- backward
+def _bwd_check(fa, lens, H, H_kv, d, causal, window, seed):
+    q, k, v, cu = _packed(lens, H, H_kv, d, torch.bfloat16, seed=seed)
+    g = torch.Generator().manual_seed(seed + 1)
+    do = torch.randn(q.shape, generator=g).to(torch.bfloat16)
+    cu_t = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    ms = max(lens)
+    qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
+    o, lse = fa.fwd_varlen(qd, kd, vd, cu_t, ms, causal=causal, window=window)
+    dq, dk, dv = fa.bwd_varlen(qd, kd, vd, o, lse, dod, cu_t, ms, causal=causal, window=window)
+    torch.cuda.synchronize()
+    st, site = fa.fa_get_device_status(None)
+    assert st == fa.FA_OK, f"device status {fa.fa_status_string(st)} at site {site}"
+    scale = d ** -0.5
+    for b, n in enumerate(lens):
+        if n == 0:
+            continue
+        s0 = cu[b]
+        view = lambda t: t[s0:s0 + n].permute(1, 0, 2).unsqueeze(0).contiguous()
+        ref = oracle.attention_bwd(view(q), view(k), view(v), view(do), scale, causal, *window)
+        got = [t[s0:s0 + n].permute(1, 0, 2).unsqueeze(0).float().cpu().numpy()
+               for t in (dq, dk, dv)]
+        for name, gt, r in zip(("dQ", "dK", "dV"), got, ref):
+            err = float(np.abs(gt - r).max())
+            bound = 2e-2 * float(np.abs(r).max()) + 1e-4
+            assert err <= bound, f"seq {b} (n={n}) {name}: {err:.3e} > {bound:.3e}"
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+def test_backward_ragged(fa, d, causal):
+    _bwd_check(fa, [1, 127, 300, 0, 129, 513], 4, 2, d, causal, (-1, -1), seed=660 + d)
+
+
+@pytest.mark.parametrize("window", [(40, 40), (200, 0)])
+def test_backward_windows(fa, window):
+    _bwd_check(fa, [700, 3, 260], 2, 2, 128, False, window, seed=670)
+
+
+def test_backward_equal_lengths_equal_the_batched_backward(fa):
+    """Equal-length packed sequences give fa_bwd's gradients bit for bit."""
+    N, d = 256, 128
+    q, k, v = make_random_qkv(2, 2, N, d, torch.bfloat16, seed=680)
+    do = torch.randn(q.shape, generator=torch.Generator().manual_seed(681)).to(torch.bfloat16)
+    qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
+    o, lse = fa.fwd(qd, kd, vd, causal=True)
+    ref = fa.bwd(qd, kd, vd, o, lse, dod, causal=True)
+    pack = lambda t: t.permute(0, 2, 1, 3).reshape(2 * N, 2, d).contiguous()
+    cu_t = torch.tensor([0, N, 2 * N], dtype=torch.int32, device="cuda")
+    lse_p = lse.permute(1, 0, 2).reshape(2, 2 * N).contiguous()
+    got = fa.bwd_varlen(pack(qd), pack(kd), pack(vd), pack(o), lse_p, pack(dod), cu_t, N,
+                        causal=True)
+    torch.cuda.synchronize()
+    for g_, r_ in zip(got, ref):
+        assert torch.equal(g_, pack(r_))
