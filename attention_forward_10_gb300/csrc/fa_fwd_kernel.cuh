@@ -28,7 +28,9 @@
 // MMA issue order.  The MMAs are issued as alternating per-tile groups
 //   [P_0(j-1) V_(j-1), Q_0 K_j^T]  [P_1(j-1) V_(j-1), Q_1 K_j^T]  ...
 // over the stream of K/V tiles j (continuing across work units), so that
-// each tile's softmax runs while the other tile's two MMAs execute.  P_g lives
+// each tile's softmax runs while the other tile's two MMAs execute.  P_g is
+// handed over in two 64-key halves (one mbarrier each), so the first half of
+// P_g V starts while the softmax still computes the second.  P_g lives
 // in S_g's tensor-memory columns; Q_g K_j^T follows P_g(j-1) V without a
 // completion wait, relying on the tensor pipe running one CTA's MMAs in issue
 // order (each has read its operands before a later one writes its
@@ -105,8 +107,9 @@ struct Layout {
   // arrives on group j % (kStages / 2)
   static constexpr int kKVEmpty = kKVFull + kStages;
   static constexpr int kSFull = kKVEmpty + kStages / 2;
+  // P_g ready, per 64-key half: kPFull + 2 g + half
   static constexpr int kPFull = kSFull + 2;
-  static constexpr int kODone = kPFull + 2;
+  static constexpr int kODone = kPFull + 4;
   static constexpr int kDrain = kODone + 2;
   static constexpr int kStageFull = kDrain + 1;       // O tile written to staging
   static constexpr int kStageEmpty = kStageFull + 1;  // staging read by the store
@@ -208,14 +211,15 @@ __device__ __forceinline__ float tile_max(const float (&s)[kBlockN]) {
 // then the exponentials; P (16-bit, packed in pairs) goes to tensor memory
 // at tS, over the first half of the row's scores.  Returns the row sum of p
 // (kept as two packed partial sums).
-template <bool BF16>
+// Columns [C_BEGIN, C_END) only, so that P can be handed over in halves.
+template <bool BF16, int C_BEGIN = 0, int C_END = kBlockN>
 __device__ __forceinline__ float exp_tile_to_tmem(const float (&s)[kBlockN], float scale_log2,
                                                   float m, uint32_t tS) {
   const uint64_t scale2 = pack_f32x2(scale_log2, scale_log2);
   const uint64_t neg_m2 = pack_f32x2(-m, -m);
   uint64_t acc_a = pack_f32x2(0.f, 0.f), acc_b = acc_a;
 #pragma unroll
-  for (int c0 = 0; c0 < kBlockN; c0 += 32) {
+  for (int c0 = C_BEGIN; c0 < C_END; c0 += 32) {
     uint32_t pk[16];
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
@@ -297,7 +301,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       mbar_init(bar(L::kQFull + g), 1);
       mbar_init(bar(L::kQEmpty + g), 1);
       mbar_init(bar(L::kSFull + g), 1);
-      mbar_init(bar(L::kPFull + g), 128);
+      mbar_init(bar(L::kPFull + 2 * g), 128);
+      mbar_init(bar(L::kPFull + 2 * g + 1), 128);
       mbar_init(bar(L::kODone + g), 1);
     }
     for (int s = 0; s < L::kStages; ++s) mbar_init(bar(L::kKVFull + s), 1);
@@ -429,17 +434,29 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         for (int g = 0; g < 2; ++g) {
           // ---- O_g += P_g(j-1) V(j-1)
           if (prev_valid && prev_active[g]) {
-            ok = wait_bar(bar(L::kPFull + g), p_par[g], ctl, kSiteMmaP);
+            const uint32_t par = p_par[g];
             p_par[g] ^= 1u;
+            ok = wait_bar(bar(L::kPFull + 2 * g), par, ctl, kSiteMmaP);
             if (!ok) break;
-            tc_fence_after_sync();
-            if constexpr (FP8)
+            if constexpr (FP8) {
+              ok = wait_bar(bar(L::kPFull + 2 * g + 1), par, ctl, kSiteMmaP);
+              if (!ok) break;
+              tc_fence_after_sync();
               mma_f8_ts_kmajor_x4(tmem + L::o_col(g), tmem + L::s_col(g),
                                   v_desc0 + prev_vslot * kSlotStep, kIdescO,
                                   prev_acc[g] ? 1u : 0u);
-            else
-              mma_ts_mnmajor_x8(tmem + L::o_col(g), tmem + L::s_col(g),
+            } else {
+              tc_fence_after_sync();
+              // keys 0-63: P columns +0, V rows 0-63
+              mma_ts_mnmajor_x4(tmem + L::o_col(g), tmem + L::s_col(g),
                                 v_desc0 + prev_vslot * kSlotStep, kIdescO, prev_acc[g] ? 1u : 0u);
+              ok = wait_bar(bar(L::kPFull + 2 * g + 1), par, ctl, kSiteMmaP);
+              if (!ok) break;
+              tc_fence_after_sync();
+              // keys 64-127: P columns +32, V rows 64-127 (4 steps of 2 KB on)
+              mma_ts_mnmajor_x4(tmem + L::o_col(g), tmem + L::s_col(g) + 32,
+                                v_desc0 + prev_vslot * kSlotStep + 512, kIdescO, 1u);
+            }
             tc_commit(bar(L::kODone + g));
             ++o_cnt[g];
           }
@@ -577,14 +594,25 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           l *= factor;
           m_ref = m_new;
         }
-        if constexpr (FP8)
+        if constexpr (FP8) {
           l += exp_tile_to_tmem_e4m3(s, scale_log2,
                                      ((m_ref == -INFINITY) ? 0.f : m_ref) - kFp8POffset, tS);
-        else
-          l += exp_tile_to_tmem<BF16>(s, scale_log2, (m_ref == -INFINITY) ? 0.f : m_ref, tS);
-        tmem_wait_st();
+          tmem_wait_st();
+          tc_fence_before_sync();
+          mbar_arrive(bar(L::kPFull + 2 * g));
+        } else {
+          const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+          // keys 0-63 first: their P V product can start while the rest runs
+          float lsum = exp_tile_to_tmem<BF16, 0, kBlockN / 2>(s, scale_log2, m_use, tS);
+          tmem_wait_st();
+          tc_fence_before_sync();
+          mbar_arrive(bar(L::kPFull + 2 * g));
+          lsum += exp_tile_to_tmem<BF16, kBlockN / 2, kBlockN>(s, scale_log2, m_use, tS);
+          l += lsum;
+          tmem_wait_st();
+        }
         tc_fence_before_sync();
-        mbar_arrive(bar(L::kPFull + g));
+        mbar_arrive(bar(L::kPFull + 2 * g + 1));
         ++pv_cnt;
       }
       if (!ok) break;
