@@ -461,6 +461,14 @@ def run_ours(args, wl):
     e2e_steps = max(1, min(args.steps, 20))
 
     def e2e_step():
+        """One step: fork the three streams from the current one, copy chunk c
+        in, run it, copy it out (chunk c + 1's input copy overlapping chunk
+        c's kernel and output copy), join back.  Steps do not overlap."""
+        root = torch.cuda.current_stream(dev)
+        ev0 = torch.cuda.Event()
+        ev0.record(root)
+        for st_ in (s_in, stream, s_out):
+            st_.wait_event(ev0)
         for (a0, a1) in bounds:
             with torch.cuda.stream(s_in):
                 for dst, src in ((dq, q_h), (dk, k_h), (dv, v_h)):
@@ -476,20 +484,41 @@ def run_ours(args, wl):
                 s_out.wait_event(ev_c)
                 o_h[a0:a1].copy_(do_[a0:a1], non_blocking=True)
                 l_h[a0:a1].copy_(dl[a0:a1], non_blocking=True)
+        for st_ in (s_in, stream, s_out):
+            ev = torch.cuda.Event()
+            ev.record(st_)
+            root.wait_event(ev)
 
     if wl.splitkv:
         for (a0, a1) in bounds:
             ensure_workspace(1, a1 - a0)
     e2e_step()
     torch.cuda.synchronize(dev)
+    # The step's launches are captured once into a CUDA graph and replayed
+    # (host work per step: one graph launch); if capture is refused, the
+    # steps are issued eagerly.
+    graph = None
+    try:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        graph.replay()
+        torch.cuda.synchronize(dev)
+    except Exception:  # noqa: BLE001 - any capture failure: run eagerly
+        graph = None
+        torch.cuda.synchronize(dev)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(s_in)
+    root = torch.cuda.current_stream(dev)
+    e0.record(root)
     for _ in range(e2e_steps):
-        e2e_step()
-    # the last D2H copy closes the timed region
-    s_in.wait_stream(s_out)
-    e1.record(s_in)
+        if graph is not None:
+            graph.replay()
+        else:
+            e2e_step()
+    # the last D2H copy (joined into the current stream) closes the timed region
+    e1.record(root)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     if world > 1:
@@ -525,7 +554,8 @@ def run_ours(args, wl):
                          "algorithmic_hbm_bytes": wl.hbm_bytes},
             "e2e": {"value": world * wl.flops / (e2e_ms / 1e3) / 1e12, "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "ms_per_step": e2e_ms, "pipelined_chunks": n_chunks},
+                    "ms_per_step": e2e_ms, "pipelined_chunks": n_chunks,
+                    "cuda_graph": graph is not None},
             "gpu_launches": args.steps * launches_per_call,
             "clocks": clocks,
         }
