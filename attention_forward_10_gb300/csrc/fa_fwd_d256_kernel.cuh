@@ -314,14 +314,12 @@ __global__ void __launch_bounds__(d256::kThreads, 1)
         if (!ok) break;
         tc_fence_after_sync();
         float s[kBN];
+        float mblk[2];  // per-32-column maxima, reduced by the load itself
         {
-          uint32_t r[32];
-          tmem_ld_x32_sync(tS, r);
+          uint32_t r[kBN];
+          tmem_ld_max_x32x2_sync(tS, r, mblk);
 #pragma unroll
-          for (int c = 0; c < 32; ++c) s[c] = __uint_as_float(r[c]);
-          tmem_ld_x32_sync(tS + 32, r);
-#pragma unroll
-          for (int c = 0; c < 32; ++c) s[32 + c] = __uint_as_float(r[c]);
+          for (int c = 0; c < kBN; ++c) s[c] = __uint_as_float(r[c]);
         }
         // keys row - win_left .. row + win_right, below N
         const int kbase = n * kBN;
@@ -335,15 +333,20 @@ __global__ void __launch_bounds__(d256::kThreads, 1)
           for (int c = 0; c < kBN; ++c)
             if (c >= hi || c < lo) s[c] = -INFINITY;
         }
-        float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+        float m_raw = fmaxf(mblk[0], mblk[1]);
+        if (need_mask) {
+          // a masked tile takes its maximum over the kept columns only
+          float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
-        for (int c = 4; c < kBN; c += 4) {
-          mx0 = fmaxf(mx0, s[c]);
-          mx1 = fmaxf(mx1, s[c + 1]);
-          mx2 = fmaxf(mx2, s[c + 2]);
-          mx3 = fmaxf(mx3, s[c + 3]);
+          for (int c = 4; c < kBN; c += 4) {
+            mx0 = fmaxf(mx0, s[c]);
+            mx1 = fmaxf(mx1, s[c + 1]);
+            mx2 = fmaxf(mx2, s[c + 2]);
+            mx3 = fmaxf(mx3, s[c + 3]);
+          }
+          m_raw = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
         }
-        const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * scale_log2;
+        const float m_tile = m_raw * scale_log2;
 
         const bool need = m_tile > m_ref + kRescaleThreshold;
         if (__any_sync(0xffffffffu, need)) {

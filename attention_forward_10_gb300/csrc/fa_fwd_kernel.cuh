@@ -552,7 +552,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         tc_fence_after_sync();
 
         uint32_t sraw[kBlockN];
-        tmem_ld_x32x4_sync(tS, sraw);
+        float mblk[4];  // per-32-column maxima, reduced by the load itself
+        tmem_ld_max_x32x4_sync(tS, sraw, mblk);
         float s[kBlockN];
 #pragma unroll
         for (int c = 0; c < kBlockN; ++c) s[c] = __uint_as_float(sraw[c]);
@@ -569,7 +570,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           for (int c = 0; c < kBlockN; ++c)
             if (c >= hi || c < lo) s[c] = -INFINITY;
         }
-        const float m_tile = tile_max(s) * scale_log2;
+        // a masked tile takes its maximum over the kept columns only
+        const float m_tile =
+            (need_mask ? tile_max(s)
+                       : fmaxf(fmaxf(mblk[0], mblk[1]), fmaxf(mblk[2], mblk[3]))) *
+            scale_log2;
         if (__any_sync(0xffffffffu, m_tile > m_ref + kThreshold)) {
           const float m_new = fmaxf(m_ref, m_tile);
           const float factor = (m_new == -INFINITY) ? 1.f : ex2_approx(m_ref - m_new);
