@@ -624,30 +624,36 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
       // ---------------------------------------------------------- epilogue
       ok = wait_bar(bar(L::kODone + g), (pv_cnt - 1) & 1u, ctl, kSiteEpilogueO);
-      // the staging tile must have been read by the store before this one
-      ok = ok && wait_bar(bar(L::kStageEmpty), (my_store - 1) & 1u, ctl, kSiteEpilogueO);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after_sync();
 
+      // O_g is final: read the row (one wait for all its loads), normalise
+      // and pack it before waiting for the staging tile, so that this work
+      // overlaps the store of the other warpgroup's tile.
       // (FP8: l carries the 2^offset of P; O also takes the V descale)
       const float inv_l = (l > 0.f) ? (FP8 ? p.descale_v : 1.f) / l : 0.f;
+      uint32_t pk[D / 2];
+      {
+        uint32_t o[D];
+        if constexpr (D == 128)
+          tmem_ld_x32x4_sync(tO, o);
+        else
+          tmem_ld_2x32_sync(tO, o, tO + 32, o + 32);
 #pragma unroll
-      for (int c = 0; c < D; c += 32) {
-        uint32_t o[32];
-        tmem_ld_x32_sync(tO + c, o);
+        for (int e = 0; e < D / 2; ++e)
+          pk[e] = pack2<BF16>(__uint_as_float(o[2 * e]) * inv_l,
+                              __uint_as_float(o[2 * e + 1]) * inv_l);
+      }
+      // the staging tile must have been read by the store before this one
+      ok = wait_bar(bar(L::kStageEmpty), (my_store - 1) & 1u, ctl, kSiteEpilogueO);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t w4[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            w4[e] = pack2<BF16>(__uint_as_float(o[8 * j + 2 * e]) * inv_l,
-                                __uint_as_float(o[8 * j + 2 * e + 1]) * inv_l);
-          const int c16 = c / 8 + j;  // 16-byte chunk index along the row
-          const uint32_t addr = stage + (c16 / 8) * (kBlockM * 128) + t * 128 +
-                                (((c16 % 8) ^ (t & 7)) << 4);
-          st_shared_v4(addr, w4[0], w4[1], w4[2], w4[3]);
-        }
+      for (int c16 = 0; c16 < D / 8; ++c16) {  // 16-byte chunks along the row
+        const uint32_t addr = stage + (c16 / 8) * (kBlockM * 128) + t * 128 +
+                              (((c16 % 8) ^ (t & 7)) << 4);
+        st_shared_v4(addr, pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
       }
       if (p.lse != nullptr && row < len) {
         p.lse[lse_base<PACKED>(p, w.sv) + row] =
