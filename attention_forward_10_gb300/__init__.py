@@ -42,6 +42,9 @@ SIGNATURES = {
     "fa_fwd_fp8": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _f, _f, _f, _i, _i, _i,
                     _vp, _ull, _vp], _i),
     "fa_fwd_fp8_workspace_bytes": ([_i, _i, _i, _i, ctypes.POINTER(_ull)], _i),
+    "fa_fwd_host": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _i, _i, _vp, _ull,
+                     _vp], _i),
+    "fa_fwd_host_workspace_bytes": ([_i, _i, _i, _i, _i, _i, ctypes.POINTER(_ull)], _i),
     "fa_bwd": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _ull, _i, _i, _i, _i, _i, _f,
                 _i, _i, _i, _i, _vp], _i),
     "fa_bwd_workspace_bytes": ([_i, _i, _i, ctypes.POINTER(_ull)], _i),
@@ -124,6 +127,22 @@ def fa_fwd_fp8(q: int, k: int, v: int, o: int, lse: int | None, B: int, H: int, 
 def fa_fwd_fp8_workspace_bytes(B: int, H_kv: int, N: int, d: int) -> tuple[int, int]:
     out = ctypes.c_ulonglong(0)
     st = int(_lib.fa_fwd_fp8_workspace_bytes(B, H_kv, N, d, ctypes.byref(out)))
+    return st, int(out.value)
+
+
+def fa_fwd_host(q: int, k: int, v: int, o: int, lse: int | None, B: int, H: int, H_kv: int,
+                N: int, d: int, scale: float, causal: int, window_left: int,
+                window_right: int, dtype: int, workspace: int | None, workspace_bytes: int,
+                stream: int | None) -> int:
+    return int(_lib.fa_fwd_host(q, k, v, o, lse or None, B, H, H_kv, N, d, scale, causal,
+                                window_left, window_right, dtype, workspace or None,
+                                int(workspace_bytes), stream or None))
+
+
+def fa_fwd_host_workspace_bytes(B: int, H: int, H_kv: int, N: int, d: int,
+                                with_lse: int) -> tuple[int, int]:
+    out = ctypes.c_ulonglong(0)
+    st = int(_lib.fa_fwd_host_workspace_bytes(B, H, H_kv, N, d, with_lse, ctypes.byref(out)))
     return st, int(out.value)
 
 
@@ -277,6 +296,63 @@ def fwd(q, k, v, *, scale: float | None = None, causal: bool = False,
                         int(window[0]), int(window[1]), _dtype_code(q), handle)
     if st != FA_OK:
         raise FaError(st, "fa_fwd")
+    return out, (lse if return_lse else None)
+
+
+def fwd_host(q, k, v, *, scale: float | None = None, causal: bool = False,
+             window: tuple[int, int] = (-1, -1), out=None, lse=None, return_lse: bool = True,
+             workspace=None, device=None, stream=None):
+    """Attention forward on HOST (CPU) tensors q [B, H, N, d] and k, v
+    [B, H_kv, N, d] through fa_fwd_host: the library stages chunks through
+    device memory and writes o (and lse) back to host memory.
+
+    Returns ``(o, lse)`` as CPU tensors (page-locked when allocated here),
+    valid once ``stream`` (default: torch's current stream of ``device``,
+    default the current CUDA device) has finished the call's work.  Page-lock
+    q, k, v (``pin_memory()``) for the copies to overlap the computation.
+    ``workspace``: a CUDA uint8 tensor of at least
+    fa_fwd_host_workspace_bytes() bytes (allocated here when None).
+    """
+    import torch
+    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape:
+        raise ValueError("q must be [B, H, N, d] and k, v one [B, H_kv, N, d] shape")
+    if (k.shape[0], k.shape[2], k.shape[3]) != (q.shape[0], q.shape[2], q.shape[3]):
+        raise ValueError("k, v must match q in B, N and d")
+    if any(t.device.type != "cpu" for t in (q, k, v)):
+        raise ValueError("fwd_host takes host (CPU) tensors; use fwd for CUDA tensors")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k, v must share one dtype")
+    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("q, k, v must be contiguous")
+    B, H, N, d = (int(x) for x in q.shape)
+    H_kv = int(k.shape[1])
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None \
+        else torch.device(device)
+    pin = q.is_pinned()
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, pin_memory=pin)
+    if return_lse and lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, pin_memory=pin)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    with torch.cuda.device(dev):
+        if workspace is None:
+            st, need = fa_fwd_host_workspace_bytes(B, H, H_kv, N, d, int(bool(return_lse)))
+            if st != FA_OK:
+                raise FaError(st, "fa_fwd_host_workspace_bytes")
+            workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+            if hasattr(stream, "cuda_stream") and stream != torch.cuda.current_stream(dev):
+                workspace.record_stream(stream)
+        st = fa_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                         lse.data_ptr() if (return_lse and lse is not None) else None,
+                         B, H, H_kv, N, d, float(scale), int(bool(causal)), int(window[0]),
+                         int(window[1]), _dtype_code(q), workspace.data_ptr(),
+                         workspace.numel(), handle)
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_host")
     return out, (lse if return_lse else None)
 
 

@@ -656,6 +656,237 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
   return launch_forward(c, o, lse, 1, 0);
 }
 
+}  // extern "C"
+
+// ------------------------------------------------------------------------
+// Forward on host buffers: chunks of whole K/V-head groups are copied in,
+// computed and copied out through a ring of device staging slots, with the
+// copies in each direction on a helper stream of their own.
+// ------------------------------------------------------------------------
+namespace fa {
+namespace {
+
+constexpr int kHostSlots = 3;   // ring depth: copy-in, compute, copy-out in flight
+constexpr int kHostChunks = 8;  // chunks a problem is cut into by default
+constexpr unsigned long long kHostMinChunkBytes = 4ull << 20;  // input bytes per chunk
+
+struct HostPlan {
+  long long groups;     // B * H_kv: a K/V head with the query heads that read it
+  long long per_chunk;  // groups per chunk
+  long long chunks;
+  int slots;
+  unsigned long long q_bytes, kv_bytes, lse_bytes, slot_bytes;  // per slot
+};
+
+unsigned long long align256(unsigned long long x) { return (x + 255ull) & ~255ull; }
+
+// Sub-buffers of one slot: Q and O (per_chunk * group query heads), K, V
+// (per_chunk K/V heads), LSE; each starts on a 256-byte boundary.
+void host_slot_layout(const ForwardCall& c, long long per_chunk, bool with_lse, HostPlan* pl) {
+  const unsigned long long grp = static_cast<unsigned long long>(c.H / c.H_kv);
+  const unsigned long long nd = static_cast<unsigned long long>(c.N) * c.d;
+  const unsigned long long pc = static_cast<unsigned long long>(per_chunk);
+  pl->per_chunk = per_chunk;
+  pl->chunks = (pl->groups + per_chunk - 1) / per_chunk;
+  pl->slots = static_cast<int>(std::min<long long>(kHostSlots, pl->chunks));
+  pl->q_bytes = align256(pc * grp * nd * 2);
+  pl->kv_bytes = align256(pc * nd * 2);
+  pl->lse_bytes = with_lse ? align256(pc * grp * c.N * 4) : 0;
+  pl->slot_bytes = 2 * pl->q_bytes + 2 * pl->kv_bytes + pl->lse_bytes;
+}
+
+// About kHostChunks chunks, each with at least kHostMinChunkBytes of input
+// (small problems run as fewer, larger chunks).
+void host_default_plan(const ForwardCall& c, bool with_lse, HostPlan* pl) {
+  pl->groups = static_cast<long long>(c.B) * c.H_kv;
+  const unsigned long long grp = static_cast<unsigned long long>(c.H / c.H_kv);
+  const unsigned long long in_per_group = (grp + 2) * static_cast<unsigned long long>(c.N) * c.d * 2;
+  long long per = (pl->groups + kHostChunks - 1) / kHostChunks;
+  const long long min_per =
+      static_cast<long long>((kHostMinChunkBytes + in_per_group - 1) / in_per_group);
+  per = std::min(std::max(per, min_per), pl->groups);
+  host_slot_layout(c, per, with_lse, pl);
+}
+
+// The default plan, shrunk (fewer groups per chunk, then fewer slots) until
+// its slots fit in `ws_bytes`.  False when not even one group fits.
+bool host_plan_for(const ForwardCall& c, bool with_lse, unsigned long long ws_bytes,
+                   HostPlan* pl) {
+  host_default_plan(c, with_lse, pl);
+  const long long per0 = pl->per_chunk;
+  for (int slots = pl->slots; slots >= 1; --slots) {
+    long long lo = 1, hi = per0, best = 0;  // the largest fitting count
+    while (lo <= hi) {
+      const long long mid = lo + (hi - lo) / 2;
+      host_slot_layout(c, mid, with_lse, pl);
+      if (pl->slot_bytes * std::min(pl->slots, slots) <= ws_bytes) {
+        best = mid;
+        lo = mid + 1;
+      } else {
+        hi = mid - 1;
+      }
+    }
+    if (best > 0) {
+      host_slot_layout(c, best, with_lse, pl);
+      pl->slots = std::min(pl->slots, slots);
+      return true;
+    }
+  }
+  return false;
+}
+
+// Helper streams and events of one device, made on first use and kept for
+// the life of the process; the mutex serialises the enqueue of concurrent
+// calls (which then share the streams in order).
+struct HostPipe {
+  std::once_flag once;
+  cudaError_t init_rc = cudaSuccess;
+  cudaStream_t s_in = nullptr, s_out = nullptr;
+  cudaEvent_t fork = nullptr, join_in = nullptr, join_out = nullptr;
+  cudaEvent_t in[kHostSlots] = {}, done[kHostSlots] = {}, out[kHostSlots] = {};
+  std::mutex mu;
+};
+HostPipe g_host_pipes[kMaxDevices];
+
+HostPipe* host_pipe(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  HostPipe* hp = &g_host_pipes[dev];
+  std::call_once(hp->once, [hp] {
+    cudaError_t e = cudaStreamCreateWithFlags(&hp->s_in, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&hp->s_out, cudaStreamNonBlocking);
+    cudaEvent_t* evs[3 + 3 * kHostSlots] = {&hp->fork, &hp->join_in, &hp->join_out};
+    for (int i = 0; i < kHostSlots; ++i) {
+      evs[3 + i] = &hp->in[i];
+      evs[3 + kHostSlots + i] = &hp->done[i];
+      evs[3 + 2 * kHostSlots + i] = &hp->out[i];
+    }
+    for (cudaEvent_t* ev : evs)
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+    hp->init_rc = e;
+  });
+  return hp->init_rc == cudaSuccess ? hp : nullptr;
+}
+
+int host_forward(const ForwardCall& c, const HostPlan& pl, const char* q_h, const char* k_h,
+                 const char* v_h, char* o_h, float* lse_h, char* ws) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  HostPipe* hp = host_pipe(dev);
+  if (hp == nullptr) return FA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(hp->mu);
+  cudaStream_t s = static_cast<cudaStream_t>(c.stream);
+  const unsigned long long grp = static_cast<unsigned long long>(c.H / c.H_kv);
+  const unsigned long long nd = static_cast<unsigned long long>(c.N) * c.d;
+  const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
+
+  // fork: the helper streams start behind everything already on `s`
+  // (earlier users of the workspace included)
+  cudaError_t e = cudaEventRecord(hp->fork, s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->s_in, hp->fork, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->s_out, hp->fork, 0);
+  int st = FA_OK;
+  for (long long i = 0; i < pl.chunks && e == cudaSuccess; ++i) {
+    const int slot = static_cast<int>(i % pl.slots);
+    const long long g0 = i * pl.per_chunk;
+    const unsigned long long ng =
+        static_cast<unsigned long long>(std::min(pl.groups, g0 + pl.per_chunk) - g0);
+    const unsigned long long q_off = static_cast<unsigned long long>(g0) * grp * nd * 2;
+    const unsigned long long kv_off = static_cast<unsigned long long>(g0) * nd * 2;
+    const unsigned long long qb = ng * grp * nd * 2, kvb = ng * nd * 2;
+    char* const dq = ws + static_cast<unsigned long long>(slot) * pl.slot_bytes;
+    char* const dout = dq + pl.q_bytes;
+    char* const dk = dout + pl.q_bytes;
+    char* const dv = dk + pl.kv_bytes;
+    float* const dl = lse_h != nullptr ? reinterpret_cast<float*>(dv + pl.kv_bytes) : nullptr;
+
+    // copy in, once the slot's previous chunk has been copied out
+    if (i >= pl.slots) e = cudaStreamWaitEvent(hp->s_in, hp->out[slot], 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dq, q_h + q_off, qb, h2d, hp->s_in);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dk, k_h + kv_off, kvb, h2d, hp->s_in);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dv, v_h + kv_off, kvb, h2d, hp->s_in);
+    if (e == cudaSuccess) e = cudaEventRecord(hp->in[slot], hp->s_in);
+    // compute on the caller's stream: the chunk's groups as ng heads of
+    // K/V with grp query heads each
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, hp->in[slot], 0);
+    if (e != cudaSuccess) break;
+    ForwardCall cc = c;
+    cc.q = dq;
+    cc.k = dk;
+    cc.v = dv;
+    cc.o = dout;
+    cc.lse = dl;
+    cc.B = static_cast<int>(ng);
+    cc.H = static_cast<int>(grp);
+    cc.H_kv = 1;
+    st = launch_forward(cc, dout, dl, 1, 0);
+    if (st != FA_OK) break;
+    // copy out
+    e = cudaEventRecord(hp->done[slot], s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->s_out, hp->done[slot], 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(o_h + q_off, dout, qb, d2h, hp->s_out);
+    if (e == cudaSuccess && dl != nullptr)
+      e = cudaMemcpyAsync(lse_h + static_cast<unsigned long long>(g0) * grp * c.N, dl,
+                          ng * grp * c.N * 4, d2h, hp->s_out);
+    if (e == cudaSuccess) e = cudaEventRecord(hp->out[slot], hp->s_out);
+  }
+  // join both helper streams back into `s` (after a failure too)
+  cudaError_t j = cudaEventRecord(hp->join_in, hp->s_in);
+  if (j == cudaSuccess) j = cudaStreamWaitEvent(s, hp->join_in, 0);
+  if (j == cudaSuccess) j = cudaEventRecord(hp->join_out, hp->s_out);
+  if (j == cudaSuccess) j = cudaStreamWaitEvent(s, hp->join_out, 0);
+  if (st != FA_OK) return st;
+  return (e == cudaSuccess && j == cudaSuccess) ? FA_OK : FA_ERR_CUDA;
+}
+
+int host_validate(const ForwardCall& c) {
+  const int st = validate(c);
+  if (st != FA_OK) return st;
+  if (c.window_left < -1 || c.window_right < -1) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" {
+
+int fa_fwd_host_workspace_bytes(int B, int H, int H_kv, int N, int d, int with_lse,
+                                unsigned long long* bytes) {
+  using namespace fa;
+  if (bytes == nullptr) return FA_ERR_INVALID_ARG;
+  *bytes = 0;
+  if (with_lse != 0 && with_lse != 1) return FA_ERR_INVALID_ARG;
+  const ForwardCall c{nullptr, nullptr, nullptr, nullptr, nullptr, B, H, H_kv, N, d, 1.f, 0, -1,
+                      -1, FA_DTYPE_BF16, nullptr};
+  const int st = host_validate(c);
+  if (st != FA_OK) return st;
+  if (empty_problem(c)) return FA_OK;
+  HostPlan pl;
+  host_default_plan(c, with_lse != 0, &pl);
+  *bytes = pl.slot_bytes * pl.slots;
+  return FA_OK;
+}
+
+int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                int H, int H_kv, int N, int d, float scale, int causal, int window_left,
+                int window_right, int dtype, void* workspace,
+                unsigned long long workspace_bytes, void* stream) {
+  using namespace fa;
+  const ForwardCall c{q, k, v, o, lse, B, H, H_kv, N, d, scale, causal, window_left,
+                      window_right, dtype, stream};
+  int st = host_validate(c);
+  if (st != FA_OK) return st;
+  if (empty_problem(c)) return FA_OK;
+  if (q == nullptr || k == nullptr || v == nullptr || o == nullptr || workspace == nullptr)
+    return FA_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return FA_ERR_MISALIGNED;
+  HostPlan pl;
+  if (!host_plan_for(c, lse != nullptr, workspace_bytes, &pl)) return FA_ERR_INVALID_ARG;
+  return host_forward(c, pl, static_cast<const char*>(q), static_cast<const char*>(k),
+                      static_cast<const char*>(v), static_cast<char*>(o), lse,
+                      static_cast<char*>(workspace));
+}
+
 int fa_bwd_workspace_bytes(int B, int H, int N, unsigned long long* bytes) {
   if (bytes == nullptr) return FA_ERR_INVALID_ARG;
   *bytes = 0;

@@ -438,9 +438,13 @@ def run_ours(args, wl):
 
     # End to end through the public API with host buffers: each step copies
     # Q, K, V from pinned host memory, runs the forward pass and copies O and
-    # LSE back.  The B*H heads are cut into chunks and the copies of one chunk
-    # overlap the kernel of the previous one (three streams: H2D, compute, D2H).
-    # Packed (varlen) batches interleave heads within rows: one chunk.
+    # LSE back.  Dense bf16/fp16 workloads make one fa_fwd_host call per step
+    # (the library chunks the heads and overlaps copies with the kernels).
+    # The others (split-KV, packed, FP8) do the same here: the B*H heads are
+    # cut into chunks and the copies of one chunk overlap the kernel of the
+    # previous one (three streams: H2D, compute, D2H); packed (varlen) batches
+    # interleave heads within rows: one chunk.
+    host_api = not (wl.splitkv or wl.varlen or wl.dtype == "fp8")
     if wl.varlen:
         rows_e2e, row_shape, l_shape = 1, (total * H * d,), (H * total,)
     else:
@@ -489,6 +493,27 @@ def run_ours(args, wl):
             ev.record(st_)
             root.wait_event(ev)
 
+    if host_api:
+        H_kv = int(k.shape[1])
+        q_h, k_h, v_h = (t.pin_memory() for t in (q, k, v))
+        o_h = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+        l_h = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+        st_, ws_bytes = fa.fa_fwd_host_workspace_bytes(B, H, H_kv, N, d, 1)
+        if st_ != fa.FA_OK:
+            raise RuntimeError(f"fa_fwd_host_workspace_bytes: {fa.fa_status_string(st_)}")
+        host_ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+        n_chunks = None
+
+        def e2e_step():
+            """One step: a single fa_fwd_host call on the current stream."""
+            root = torch.cuda.current_stream(dev)
+            st_ = fa.fa_fwd_host(q_h.data_ptr(), k_h.data_ptr(), v_h.data_ptr(),
+                                 o_h.data_ptr(), l_h.data_ptr(), B, H, H_kv, N, d, wl.scale,
+                                 int(wl.causal), -1, -1, dcode, host_ws.data_ptr(),
+                                 host_ws.numel(), root.cuda_stream)
+            if st_ != fa.FA_OK:
+                raise RuntimeError(f"fa_fwd_host: {fa.fa_status_string(st_)}")
+
     if wl.splitkv:
         for (a0, a1) in bounds:
             ensure_workspace(1, a1 - a0)
@@ -525,7 +550,7 @@ def run_ours(args, wl):
         t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_ms = float(t.item())
-    h2d = 3 * q.numel() * q.element_size()
+    h2d = q_h.numel() * q_h.element_size() + 2 * k_h.numel() * k_h.element_size()
     d2h = o_h.numel() * o_h.element_size() + H * total * 4
 
     if rank == 0:
@@ -554,8 +579,10 @@ def run_ours(args, wl):
                          "algorithmic_hbm_bytes": wl.hbm_bytes},
             "e2e": {"value": world * wl.flops / (e2e_ms / 1e3) / 1e12, "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "ms_per_step": e2e_ms, "pipelined_chunks": n_chunks,
-                    "cuda_graph": graph is not None},
+                    "ms_per_step": e2e_ms, "cuda_graph": graph is not None,
+                    "api": ("fa_fwd_host (C ABI on host buffers)" if host_api else
+                            f"{n_chunks} chunks: cudaMemcpyAsync in/out around the "
+                            f"C ABI forward")},
             "gpu_launches": args.steps * launches_per_call,
             "clocks": clocks,
         }

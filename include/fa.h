@@ -277,6 +277,55 @@ FA_API int fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, floa
 FA_API int fa_fwd_fp8_workspace_bytes(int B, int H_kv, int N, int d, unsigned long long* bytes);
 
 /*
+ * fa_fwd_host -- fa_fwd_ext on HOST buffers: the same operation (sources
+ * as for fa_fwd_ext), with q, k, v read from host memory and o, lse written
+ * back to host memory.
+ *
+ * The problem is cut into chunks of whole K/V-head groups (a K/V head with
+ * the H / H_kv query heads that read it; about 8 chunks, each with at least
+ * 4 MiB of input).  Each chunk is copied into a device staging slot, computed
+ * by the forward kernel and copied back; up to three slots form a ring, so
+ * that copying chunk i+1 in, computing chunk i and copying chunk i-1 out
+ * overlap.  Copies run on two helper streams the library creates per device
+ * on first use (kept for the life of the process), forked from `stream` and
+ * joined back into it: the call is asynchronous, and all of its work,
+ * copies included, is ordered after earlier work on `stream` and before
+ * later work on it.  The result is bit-for-bit that of fa_fwd_ext on the
+ * same inputs.
+ *
+ *   q, k, v, o, lse  host pointers with the layouts of fa_fwd_ext (lse may
+ *            be NULL).  They should be page-locked (cudaHostAlloc or
+ *            cudaHostRegister) for the copies to overlap; pageable memory
+ *            works but each copy then runs synchronously with the host, and
+ *            cannot be captured into a CUDA graph (FA_ERR_CUDA).  o and lse
+ *            hold the result once `stream` has reached the end of the call's
+ *            work; they must not overlap q, k or v.
+ *   workspace, workspace_bytes
+ *            device staging memory, 256-byte aligned (else
+ *            FA_ERR_MISALIGNED); fa_fwd_host_workspace_bytes() gives the
+ *            size of the default plan.  A smaller workspace is used with
+ *            fewer groups per chunk, then fewer slots; FA_ERR_INVALID_ARG if
+ *            one slot of one group does not fit.  Overwritten; need not be
+ *            initialised; must not be used by other work until the call's
+ *            work on `stream` is done.
+ *   dtype    FA_DTYPE_F16 or FA_DTYPE_BF16.
+ * Other arguments, validation and errors as in fa_fwd_ext; window bounds
+ * below -1 are rejected (FA_ERR_INVALID_ARG).  Argument errors are reported
+ * before anything is enqueued.  Concurrent calls on one device share the
+ * helper streams (their enqueue is serialised by a lock).
+ */
+FA_API int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int H, int H_kv, int N, int d, float scale, int causal, int window_left,
+                       int window_right, int dtype, void* workspace,
+                       unsigned long long workspace_bytes, void* stream);
+
+/* Device staging bytes of fa_fwd_host's default plan for these sizes
+ * (written to *bytes; with_lse 1 when lse is not NULL, else 0).  Empty
+ * problems need 0 bytes. */
+FA_API int fa_fwd_host_workspace_bytes(int B, int H, int H_kv, int N, int d, int with_lse,
+                                       unsigned long long* bytes);
+
+/*
  * fa_bwd -- attention backward pass: dQ, dK, dV from Q, K, V, the forward's
  * O and LSE, and dO.
  *

@@ -305,3 +305,70 @@ def test_bwd_varlen_argument_errors(fa):
     assert call(0x6000, ws=0x100010) == fa.FA_ERR_MISALIGNED
     assert call(0x6000, total=0) == fa.FA_OK             # empty
     assert call(0, batch=0) == fa.FA_OK
+
+
+# ------------------------------------------------------------ host buffers
+HOST = dict(q=0x1000, k=0x2000, v=0x3000, o=0x4000, lse=0x5000, B=1, H=4, H_kv=2, N=512,
+            d=128, scale=0.088, causal=0, wl=-1, wr=-1, dtype=1, ws=0x100000,
+            ws_bytes=1 << 30, stream=None)
+
+
+def _host(fa, **kw):
+    a = dict(HOST)
+    a.update(kw)
+    return fa.fa_fwd_host(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["H_kv"],
+                          a["N"], a["d"], a["scale"], a["causal"], a["wl"], a["wr"], a["dtype"],
+                          a["ws"], a["ws_bytes"], a["stream"])
+
+
+def _host_plan_bytes(B, H, H_kv, N, d, with_lse):
+    """The documented default plan, restated: chunks of whole K/V-head
+    groups, about 8 of them and each at least 4 MiB of input, up to 3
+    staging slots; per slot Q, O, K, V (and LSE) each rounded up to 256 B."""
+    a256 = lambda x: (x + 255) // 256 * 256
+    groups, grp = B * H_kv, H // H_kv
+    in_per_group = (grp + 2) * N * d * 2
+    per = max(-(-groups // 8), -(-(4 << 20) // in_per_group))
+    per = min(per, groups)
+    chunks = -(-groups // per)
+    slot = 2 * a256(per * grp * N * d * 2) + 2 * a256(per * N * d * 2) + \
+        (a256(per * grp * N * 4) if with_lse else 0)
+    return min(3, chunks) * slot
+
+
+@pytest.mark.parametrize("shape", [(4, 16, 16, 2048, 128), (1, 7, 7, 128, 128),
+                                   (2, 8, 2, 4096, 64), (1, 32, 32, 32768, 128),
+                                   (3, 6, 1, 1000, 256), (1, 1, 1, 1, 64)])
+@pytest.mark.parametrize("with_lse", [0, 1])
+def test_host_workspace_size(fa, shape, with_lse):
+    st, n = fa.fa_fwd_host_workspace_bytes(*shape, with_lse)
+    assert st == fa.FA_OK
+    assert n == _host_plan_bytes(*shape, with_lse)
+
+
+@pytest.mark.parametrize("args,code", [
+    ((1, 3, 2, 10, 128, 1), 1), ((1, 2, 2, 10, 96, 1), 2), ((-1, 2, 2, 10, 128, 1), 1),
+    ((1, 2, 2, 10, 128, 2), 1)])
+def test_host_workspace_size_errors(fa, args, code):
+    assert fa.fa_fwd_host_workspace_bytes(*args)[0] == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), 1), (dict(k=None), 1), (dict(v=None), 1), (dict(o=None), 1),
+    (dict(ws=None), 1), (dict(d=96), 2), (dict(H=3), 1), (dict(scale=0.0), 1),
+    (dict(causal=2), 1), (dict(dtype=5), 1), (dict(wl=-2), 1), (dict(wr=-7), 1),
+    (dict(ws=0x100010), 3), (dict(ws_bytes=1024), 1)])
+def test_host_argument_errors(fa, kw, code):
+    assert _host(fa, **kw) == code
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(H=0, H_kv=1), dict(N=0)])
+def test_host_empty_is_noop(fa, kw):
+    assert _host(fa, q=None, k=None, v=None, o=None, lse=None, ws=None, **kw) == fa.FA_OK
+
+
+def test_host_wrapper_rejects_cuda_tensors(fa):
+    import torch
+    q = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa.fwd_host(q, q, q.to("meta"))
