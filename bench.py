@@ -52,6 +52,26 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
                   "bf16_tflops_sustained": 1700.0}
 
 
+def _max_over_ranks(x: float, device) -> float:
+    """The largest x over all ranks of the default process group (x itself
+    without one).  `device` holds the reduction tensor: the rank's GPU under
+    NCCL, "cpu" under gloo."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _whole_job_tflops(world: int, flops_per_step: float, steps: int, ms: float) -> float:
+    """Replicas: every rank runs `steps` steps of the workload; the job's
+    rate is all ranks' FLOPs over the slowest rank's time (ms for all
+    steps)."""
+    return world * flops_per_step * steps / (ms / 1e3) / 1e12
+
+
 def _dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -387,10 +407,7 @@ def run_ours(args, wl):
         e1.synchronize()
         per = max(e0.elapsed_time(e1) / 5, 1e-3)
         args.steps = int(min(20000, max(20, 2000.0 / per)))
-        if world > 1:
-            t = torch.tensor([args.steps], dtype=torch.int64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            args.steps = int(t.item())
+        args.steps = int(_max_over_ranks(args.steps, dev))
 
     sampler = ClockSampler(_gpu_id_for_smi(torch, dev.index)) if rank == 0 else None
     time.sleep(0.25 if sampler else 0)
@@ -412,16 +429,13 @@ def run_ours(args, wl):
     st, site = fa.fa_get_device_status(handle)
     if st != fa.FA_OK:
         raise RuntimeError(f"device status {fa.fa_status_string(st)} (site {site})")
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = _max_over_ranks(ms, dev)
     clocks = sampler.summary(t_host0, t_host1) if sampler else None
     if sampler:
         sampler.stop()
 
     ms_per_step = ms / args.steps
-    value = world * wl.flops * args.steps / (ms / 1e3) / 1e12
+    value = _whole_job_tflops(world, wl.flops, args.steps, ms)
 
     plain_ms = None
     if wl.splitkv:
@@ -545,11 +559,7 @@ def run_ours(args, wl):
     # the last D2H copy (joined into the current stream) closes the timed region
     e1.record(root)
     torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = _max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dev)
     h2d = q_h.numel() * q_h.element_size() + 2 * k_h.numel() * k_h.element_size()
     d2h = o_h.numel() * o_h.element_size() + H * total * 4
 
@@ -577,7 +587,7 @@ def run_ours(args, wl):
                          "peak_source": peak_note,
                          "traffic": traffic, "traffic_source": traffic_src,
                          "algorithmic_hbm_bytes": wl.hbm_bytes},
-            "e2e": {"value": world * wl.flops / (e2e_ms / 1e3) / 1e12, "unit": UNIT,
+            "e2e": {"value": _whole_job_tflops(world, wl.flops, 1, e2e_ms), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms, "cuda_graph": graph is not None,
                     "api": ("fa_fwd_host (C ABI on host buffers)" if host_api else
@@ -606,9 +616,12 @@ def run_backward(args, wl):
     """Time fa_bwd (pre-pass + dK/dV + dQ kernels) on the workload's shapes,
     with Q, K, V, O, LSE and dO resident on the device."""
     import torch
+    import torch.distributed as dist
     rank, world, local = _dist_env()
     dev = torch.device(f"cuda:{local}" if world > 1 else "cuda:0")
     torch.cuda.set_device(dev)
+    if world > 1:   # replicas: every rank runs the whole workload
+        dist.init_process_group("nccl", device_id=dev)
     import attention_forward_10_gb300 as fa
     from workloads import make_qkv
     if wl.varlen or wl.splitkv or wl.d not in (64, 128):
@@ -645,9 +658,12 @@ def run_backward(args, wl):
         e1.record(stream)
         e1.synchronize()
         args.steps = int(min(5000, max(10, 2000.0 / max(e0.elapsed_time(e1) / 3, 1e-3))))
-    sampler = ClockSampler(_gpu_id_for_smi(torch, dev.index))
-    time.sleep(0.25)
+        args.steps = int(_max_over_ranks(args.steps, dev))
+    sampler = ClockSampler(_gpu_id_for_smi(torch, dev.index)) if rank == 0 else None
+    time.sleep(0.25 if sampler else 0)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
     torch.cuda.synchronize(dev)
     t0 = time.time()
     start.record(stream)
@@ -656,18 +672,27 @@ def run_backward(args, wl):
     end.record(stream)
     torch.cuda.synchronize(dev)
     t1 = time.time()
-    clocks = sampler.summary(t0, t1)
-    sampler.stop()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.summary(t0, t1) if sampler else None
+    if sampler:
+        sampler.stop()
     st, site = fa.fa_get_device_status(stream.cuda_stream)
     if st != fa.FA_OK:
         raise RuntimeError(f"device status {fa.fa_status_string(st)} (site {site})")
-    ms = start.elapsed_time(end) / args.steps
+    ms_all = _max_over_ranks(start.elapsed_time(end), dev)
+    ms = ms_all / args.steps
     flops = 2.5 * wl.flops
     peaks, src = _peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    achieved = flops / (ms / 1e3) / 1e12
+    achieved = flops / (ms / 1e3) / 1e12  # one replica
+    value = _whole_job_tflops(world, flops, args.steps, ms_all)
+    if world > 1:
+        dist.destroy_process_group()
+    if rank != 0:
+        return 0
     line = {
-        "metric": BWD_METRIC, "value": achieved, "unit": UNIT, "n_gpus": 1,
+        "metric": BWD_METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
         "config": _config(wl, "inputs resident; each step reads the same inputs"),
@@ -689,8 +714,9 @@ def main():
                     help="timed steps (default: about two seconds of work)")
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", type=int, default=2,
-                    help="1..7 (default 2: B=4 H=16 N=2048 d=128 bf16 full; "
-                         "6: the split-KV case; 7: a packed variable-length batch)")
+                    help="1..8 (default 2: B=4 H=16 N=2048 d=128 bf16 full; "
+                         "6: the split-KV case; 7: a packed variable-length batch; "
+                         "8: FP8)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--backward", action="store_true",
