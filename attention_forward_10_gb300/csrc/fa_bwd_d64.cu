@@ -15,10 +15,10 @@ cudaError_t launch_all(const BwdParams& p_kv, const BwdParams& p_q, const void* 
   long long blocks = (threads + 255) / 256;
   if (blocks > static_cast<long long>(num_sms) * 8) blocks = static_cast<long long>(num_sms) * 8;
   if (blocks < 1) blocks = 1;
-  bwd::fa_bwd_prepass_kernel<64, BF16, false><<<static_cast<int>(blocks), 256, 0, stream>>>(
-      static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout), lse, lse2, dsum,
-      p_q.num_bh, p_q.N, p_q.n_pad, p_q);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(bwd::fa_bwd_prepass_kernel<64, BF16, false>,
+                             dim3(static_cast<int>(blocks)), dim3(256), 0, stream,
+                             static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout),
+                             lse, lse2, dsum, p_q.num_bh, p_q.N, p_q.n_pad, p_q);
   if (e != cudaSuccess) return e;
   constexpr int kSmem = bwd::Layout<64>::kSmemBytes;
   auto kv = bwd::fa_bwd_dkdv_kernel<64, CAUSAL, BF16, false>;
@@ -27,11 +27,9 @@ cudaError_t launch_all(const BwdParams& p_kv, const BwdParams& p_q, const void* 
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(dq, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
-  kv<<<grid_kv, bwd::kThreads, kSmem, stream>>>(p_kv);
-  e = cudaGetLastError();
+  e = launch_pdl(kv, dim3(grid_kv), dim3(bwd::kThreads), kSmem, stream, p_kv);
   if (e != cudaSuccess) return e;
-  dq<<<grid_q, bwd::kThreads, kSmem, stream>>>(p_q);
-  return cudaGetLastError();
+  return launch_pdl(dq, dim3(grid_q), dim3(bwd::kThreads), kSmem, stream, p_q);
 }
 
 }  // namespace

@@ -89,6 +89,8 @@ __global__ void __launch_bounds__(256)
                           const float* __restrict__ lse, float* __restrict__ lse2,
                           float* __restrict__ dsum, int num_bh, int N, int n_pad,
                           const BwdParams p) {
+  griddep_wait();  // (programmatic dependent launch: see fa_launch.h)
+  griddep_launch_dependents();
   constexpr int kTpr = D / 8;
   const long long rows = static_cast<long long>(num_bh) * n_pad;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
@@ -254,6 +256,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  // The set-up above may overlap the stream's previous kernel (programmatic
+  // dependent launch); global memory is touched only after it completed.
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (warp == kProducerWarp) {
     // ---------------------------------------------------------------- TMA
@@ -525,6 +531,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  // The set-up above may overlap the stream's previous kernel (programmatic
+  // dependent launch); global memory is touched only after it completed.
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (warp == kProducerWarp) {
     // ---------------------------------------------------------------- TMA

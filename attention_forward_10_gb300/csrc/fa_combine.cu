@@ -37,6 +37,8 @@ __global__ void __launch_bounds__(256)
     fa_splitkv_combine_kernel(const uint16_t* __restrict__ o_part,
                               const float* __restrict__ lse_part, uint16_t* __restrict__ o,
                               float* __restrict__ lse, CombineArgs a) {
+  griddep_wait();  // (programmatic dependent launch: see fa_launch.h)
+  griddep_launch_dependents();
   const int tpr = a.d / 8;
   const long long rows = static_cast<long long>(a.num_bh) * a.N;
   const long long total = rows * tpr;
@@ -108,13 +110,11 @@ cudaError_t launch_splitkv_combine(const void* o_part, const float* lse_part, vo
   if (blocks < 1) blocks = 1;
   const auto* op = static_cast<const uint16_t*>(o_part);
   auto* out = static_cast<uint16_t*>(o);
-  if (bf16)
-    fa_splitkv_combine_kernel<true><<<static_cast<int>(blocks), 256, 0, stream>>>(
-        op, lse_part, out, lse, a);
-  else
-    fa_splitkv_combine_kernel<false><<<static_cast<int>(blocks), 256, 0, stream>>>(
-        op, lse_part, out, lse, a);
-  return cudaGetLastError();
+  const dim3 g(static_cast<int>(blocks)), b(256);
+  return bf16 ? launch_pdl(fa_splitkv_combine_kernel<true>, g, b, 0, stream, op, lse_part, out,
+                           lse, a)
+              : launch_pdl(fa_splitkv_combine_kernel<false>, g, b, 0, stream, op, lse_part,
+                           out, lse, a);
 }
 
 }  // namespace fa

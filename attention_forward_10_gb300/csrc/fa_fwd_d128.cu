@@ -12,8 +12,7 @@ cudaError_t launch_one(const FaParams& p, int grid, cudaStream_t stream) {
   cudaError_t e =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
-  kernel<<<grid, kNumThreads, kSmem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(kernel, dim3(grid), dim3(kNumThreads), kSmem, stream, p);
 }
 
 }  // namespace

@@ -172,6 +172,10 @@ __global__ void __launch_bounds__(d256::kThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  // The set-up above may overlap the stream's previous kernel (programmatic
+  // dependent launch); global memory is touched only after it completed.
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (warp == kProducerWarp) {
     // ---------------------------------------------------------------- TMA

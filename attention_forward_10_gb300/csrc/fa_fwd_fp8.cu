@@ -20,6 +20,8 @@ namespace {
 __global__ void __launch_bounds__(256)
     fa_transpose_v_e4m3_kernel(const uint8_t* __restrict__ v, uint8_t* __restrict__ vt,
                                int num_heads, int N, int n_pad, int d) {
+  griddep_wait();  // (programmatic dependent launch: see fa_launch.h)
+  griddep_launch_dependents();
   __shared__ uint8_t tile[64][64 + 16];
   const int t = threadIdx.x;
   const int kt = n_pad / 64, ct = d / 64;
@@ -60,8 +62,7 @@ cudaError_t launch_one(const FaParams& p, int grid, cudaStream_t stream) {
   cudaError_t e =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
-  kernel<<<grid, kNumThreads, kSmem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(kernel, dim3(grid), dim3(kNumThreads), kSmem, stream, p);
 }
 
 }  // namespace
@@ -72,9 +73,9 @@ cudaError_t launch_transpose_v_e4m3(const void* v, void* vt, int num_heads, int 
   long long blocks = tiles < static_cast<long long>(num_sms) * 8 ? tiles
                                                                : static_cast<long long>(num_sms) * 8;
   if (blocks < 1) blocks = 1;
-  fa_transpose_v_e4m3_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
-      static_cast<const uint8_t*>(v), static_cast<uint8_t*>(vt), num_heads, N, n_pad, d);
-  return cudaGetLastError();
+  return launch_pdl(fa_transpose_v_e4m3_kernel, dim3(static_cast<int>(blocks)), dim3(256), 0,
+                    stream, static_cast<const uint8_t*>(v), static_cast<uint8_t*>(vt),
+                    num_heads, N, n_pad, d);
 }
 
 cudaError_t launch_fwd_d128_fp8(const FaParams& p, bool causal, int grid, cudaStream_t stream) {

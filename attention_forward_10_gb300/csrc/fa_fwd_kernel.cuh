@@ -327,6 +327,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  // The set-up above may overlap the stream's previous kernel (programmatic
+  // dependent launch); global memory is touched only after it completed.
+  griddep_wait();
+  griddep_launch_dependents();
 
   // Each role changes its register budget inside its own branch, so that no
   // code is reachable under two different budgets.

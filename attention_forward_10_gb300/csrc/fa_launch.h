@@ -4,9 +4,31 @@
 
 #include <cuda_runtime.h>
 
+#include <utility>
+
 #include "fa_params.h"
 
 namespace fa {
+
+// Launch `kernel` on `stream` with programmatic stream serialisation: the
+// grid may start launching while the stream's previous kernel finishes (its
+// CTAs wait in griddep_wait before touching global memory), so that the
+// set-up of back-to-back launches overlaps the previous kernel's tail.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 
 // Enqueue the forward kernel for head dim 64 / 128 with `grid` persistent CTAs

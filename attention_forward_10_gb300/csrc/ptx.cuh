@@ -71,6 +71,20 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 }
 
 // Named barrier over `count` threads (ids 1..15; id 0 is __syncthreads).
+// Programmatic dependent launch.  griddep_wait: block until the grid this
+// one depends on (the previous kernel of the stream, when this one was
+// launched with programmatic stream serialisation) has completed and its
+// memory is visible; a no-op otherwise.  griddep_launch_dependents: let the
+// next such kernel of the stream start launching once every CTA of this
+// grid has issued it (or exited).
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
