@@ -507,6 +507,62 @@ def run_ours(args, wl):
             ev.record(st_)
             root.wait_event(ev)
 
+    if wl.varlen:
+        # Packed batch: chunks of whole sequences (about 8, balanced by
+        # rows).  Each chunk's rows are copied into the same rows of the
+        # full-size device tensors and fa_fwd_varlen runs on its sequences
+        # (cu_seqlens from the chunk's first sequence on, row offsets still
+        # global); the [H][total] LSE, strided per chunk, is copied once at
+        # the end.
+        cu = wl.cu_seqlens()
+        target = max(1, total // 8)
+        groups, b0 = [], 0
+        for b in range(1, B + 1):
+            if cu[b] - cu[b0] >= target or b == B:
+                groups.append((b0, b))
+                b0 = b
+        lens = wl.seqlens()
+        q_v, k_v, v_v = (t.pin_memory() for t in (q, k, v))      # [total, H, d]
+        o_v = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+        l_v = torch.empty((H, total), dtype=torch.float32).pin_memory()
+        dq_v, dk_v, dv_v, do_v, dl_v = sets[0]
+        n_chunks = len(groups)
+
+        def e2e_step():
+            """One step: fork, per chunk copy in / compute / copy out, join."""
+            root = torch.cuda.current_stream(dev)
+            ev0 = torch.cuda.Event()
+            ev0.record(root)
+            for st_ in (s_in, stream, s_out):
+                st_.wait_event(ev0)
+            for (g0, g1) in groups:
+                r0, r1 = cu[g0], cu[g1]
+                with torch.cuda.stream(s_in):
+                    for dst, src in ((dq_v, q_v), (dk_v, k_v), (dv_v, v_v)):
+                        dst[r0:r1].copy_(src[r0:r1], non_blocking=True)
+                    ev_in = torch.cuda.Event()
+                    ev_in.record(s_in)
+                stream.wait_event(ev_in)
+                st_ = fa.fa_fwd_varlen(dq_v.data_ptr(), dk_v.data_ptr(), dv_v.data_ptr(),
+                                       do_v.data_ptr(), dl_v.data_ptr(),
+                                       cu_dev.data_ptr() + 4 * g0, g1 - g0,
+                                       max(lens[g0:g1]), total, H, H, d, wl.scale,
+                                       int(wl.causal), -1, -1, dcode, handle)
+                if st_ != fa.FA_OK:
+                    raise RuntimeError(f"fa_fwd_varlen: {fa.fa_status_string(st_)}")
+                ev_c = torch.cuda.Event()
+                ev_c.record(stream)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(ev_c)
+                    o_v[r0:r1].copy_(do_v[r0:r1], non_blocking=True)
+            with torch.cuda.stream(s_out):
+                s_out.wait_stream(stream)
+                l_v.copy_(dl_v, non_blocking=True)
+            for st_ in (s_in, stream, s_out):
+                ev = torch.cuda.Event()
+                ev.record(st_)
+                root.wait_event(ev)
+
     if host_api:
         H_kv = int(k.shape[1])
         q_h, k_h, v_h = (t.pin_memory() for t in (q, k, v))
@@ -591,8 +647,9 @@ def run_ours(args, wl):
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms, "cuda_graph": graph is not None,
                     "api": ("fa_fwd_host (C ABI on host buffers)" if host_api else
-                            f"{n_chunks} chunks: cudaMemcpyAsync in/out around the "
-                            f"C ABI forward")},
+                            f"{n_chunks} chunks of "
+                            f"{'sequences' if wl.varlen else 'heads'}: cudaMemcpyAsync "
+                            f"in/out around the C ABI forward")},
             "gpu_launches": args.steps * launches_per_call,
             "clocks": clocks,
         }

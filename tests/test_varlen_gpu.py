@@ -139,6 +139,34 @@ def test_rows_outside_sequences_and_guards_untouched(fa):
     assert (lg == -7.25).all()
 
 
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+@pytest.mark.parametrize("d", [64, 128])
+def test_subset_of_sequences_matches_the_full_call(fa, causal, d):
+    """A call over sequences b0 .. b1-1 only (cu_seqlens from entry b0 on,
+    row offsets still those of the whole packed tensor, total unchanged)
+    writes exactly those sequences' rows, bit for bit as the call over all
+    sequences does, and nothing else."""
+    lens = [300, 129, 700, 64, 1000, 3]
+    H = 4
+    q, k, v, cu = _packed(lens, H, H, d, torch.bfloat16, seed=2300 + d)
+    total = cu[-1]
+    o_full, l_full = _run(fa, q, k, v, cu, 0.1, causal)
+    cu_t = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    for b0, b1 in ((1, 3), (0, 1), (2, 6), (5, 6)):
+        o = torch.full((total, H, d), 7.0, dtype=torch.bfloat16, device="cuda")
+        lse = torch.full((H, total), 7.0, dtype=torch.float32, device="cuda")
+        fa.fwd_varlen(q.cuda(), k.cuda(), v.cuda(), cu_t[b0:b1 + 1], max(lens[b0:b1]),
+                      scale=0.1, causal=causal, out=o, lse=lse)
+        torch.cuda.synchronize()
+        st, site = fa.fa_get_device_status(None)
+        assert st == fa.FA_OK, f"device status {fa.fa_status_string(st)} at site {site}"
+        r0, r1 = cu[b0], cu[b1]
+        assert torch.equal(o[r0:r1], o_full[r0:r1]), (b0, b1)
+        assert torch.equal(lse[:, r0:r1], l_full[:, r0:r1]), (b0, b1)
+        assert bool((o[:r0] == 7.0).all()) and bool((o[r1:] == 7.0).all()), (b0, b1)
+        assert bool((lse[:, :r0] == 7.0).all()) and bool((lse[:, r1:] == 7.0).all()), (b0, b1)
+
+
 def test_malformed_offsets_stay_in_bounds(fa):
     """Offsets past `total`, a decreasing pair and a sequence longer than
     max_seqlen are clamped by the kernels: the rows they still cover are
