@@ -210,6 +210,12 @@ def _oracle_rows(wl, q, k, v, rows):
     Returns the FLOPs of the rows (4*d per admissible key)."""
     import oracle
     lens = wl.seqlens()
+    if wl.dtype == "fp8":
+        # Every E4M3 value is a bfloat16 value: widened exactly, the inputs
+        # (descales 1) define the same scores, P and O as the FP8 oracle's,
+        # which has no row-sampled form.
+        import torch
+        q, k, v = (t.to(torch.bfloat16) for t in (q, k, v))
     if not wl.varlen:
         oracle.attention_rows(q, k, v, wl.scale, wl.causal, rows)
     else:

@@ -80,3 +80,27 @@ def test_reference_arm_under_torchrun():
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["n_gpus"] == 2
     assert line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+@pytest.mark.parametrize("workload", [1, 2, 3, 4, 5, 6, 7, 8])
+def test_reference_arm_runs_every_workload(workload):
+    cmd = [sys.executable, "bench.py", "--impl", "reference", "--steps", "1", "--warmup", "0",
+           "--workload", str(workload)]
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["value"] > 0 and line["dtype"] == "f64"
+
+
+def test_e4m3_widens_exactly_to_bfloat16():
+    """The reference arm evaluates the FP8 workload's sampled rows on
+    bfloat16-widened inputs: every E4M3 code must survive the widening."""
+    import torch
+    codes = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn)
+    f32 = codes.to(torch.float32)
+    bf = codes.to(torch.bfloat16).to(torch.float32)
+    nan = torch.isnan(f32)
+    assert torch.equal(nan, torch.isnan(bf))
+    assert torch.equal(f32[~nan], bf[~nan])
