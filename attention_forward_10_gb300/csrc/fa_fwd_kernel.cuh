@@ -440,9 +440,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           if (prev_valid && prev_active[g]) {
             const uint32_t par = p_par[g];
             p_par[g] ^= 1u;
-            ok = wait_bar(bar(L::kPFull + 2 * g), par, ctl, kSiteMmaP);
-            if (!ok) break;
             if constexpr (FP8) {
+              // the FP8 softmax arrives on both halves after all of P: one
+              // wait (every wait in this thread delays the tensor pipe)
               ok = wait_bar(bar(L::kPFull + 2 * g + 1), par, ctl, kSiteMmaP);
               if (!ok) break;
               tc_fence_after_sync();
@@ -450,6 +450,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                                   v_desc0 + prev_vslot * kSlotStep, kIdescO,
                                   prev_acc[g] ? 1u : 0u);
             } else {
+              ok = wait_bar(bar(L::kPFull + 2 * g), par, ctl, kSiteMmaP);
+              if (!ok) break;
               tc_fence_after_sync();
               // keys 0-63: P columns +0, V rows 0-63
               mma_ts_mnmajor_x4(tmem + L::o_col(g), tmem + L::s_col(g),
