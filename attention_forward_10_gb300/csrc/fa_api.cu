@@ -225,13 +225,13 @@ struct ForwardCall {
   void* stream;
   // variable-length batches: B sequences packed along the rows, N = the
   // longest; nullptr / 0 for the [B][H][N][d] layout
-  const int* cu_seqlens;
-  int total;
+  const int* cu_seqlens = nullptr;
+  int total = 0;
   // FP8 (E4M3) inputs: descale factors and the V^T workspace
-  bool fp8;
-  float descale_q, descale_k, descale_v;
-  void* vt;
-  int n_pad;
+  bool fp8 = false;
+  float descale_q = 1.f, descale_k = 1.f, descale_v = 1.f;
+  void* vt = nullptr;
+  int n_pad = 0;
 };
 
 int validate(const ForwardCall& c) {

@@ -26,8 +26,9 @@
 //   warp  7    spare
 //
 // With three S buffers, S(G) overwrites the columns of P(G-3), whose P V
-// product was issued two MMA groups earlier, so the wait for it is hidden;
-// the softmax of tile G-1 runs while S(G) executes.
+// product was issued two MMA groups earlier; the tensor pipe runs one CTA's
+// MMAs in issue order, so S(G) needs no wait for it.  The softmax of tile
+// G-1 runs while S(G) executes.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -248,11 +249,10 @@ __global__ void __launch_bounds__(d256::kThreads, 1)
           ok = wait_bar(bar(kKVFull + kslot), phase, ctl, kSiteMmaK);
           if (!ok) break;
           if (++slot == (uint32_t)kStages) { slot = 0; phase ^= 1u; }
-          if (G >= (uint32_t)kSBufs) {
-            // P(G-3) occupied buffer b: its P V product must have completed
-            ok = wait_bar(bar(kODone + b), ((G - kSBufs) / kSBufs) & 1u, ctl, kSiteMmaO);
-            if (!ok) break;
-          }
+          // P(G-3) occupied buffer b; its P V product was issued two steps
+          // ago, and the tensor pipe runs one CTA's MMAs in issue order, so it
+          // has read P before this product overwrites the buffer (no wait:
+          // each wait in this thread delays the pipe)
           tc_fence_after_sync();
           mma_ss_kmajor_x16_q128_k64(tmem + b * kBN, q_desc, k_desc0 + kslot * kSlotStep,
                                      kIdescS, 0u);

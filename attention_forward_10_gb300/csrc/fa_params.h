@@ -26,7 +26,6 @@ enum WaitSite : int {
   kSiteSoftmaxS = 8,
   kSiteSoftmaxO = 9,
   kSiteEpilogueO = 10,
-  kSitePair = 11,
   kSiteStore = 12,
   kSiteSelftest = 15,
 };
