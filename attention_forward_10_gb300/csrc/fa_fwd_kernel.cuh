@@ -102,6 +102,8 @@ struct Layout {
   // barrier indices
   static constexpr int kQFull = 0;
   static constexpr int kQEmpty = 2;
+  // step barriers: B(j) = kKVFull + j % (kStages / 2) completes when the
+  // two tiles K/V step j first reads have landed: V(j-1) and K(j)
   static constexpr int kKVFull = 4;
   // release groups: the commit of K/V step j frees K(j) and V(j-1) and
   // arrives on group j % (kStages / 2)
@@ -305,7 +307,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       mbar_init(bar(L::kPFull + 2 * g + 1), 128);
       mbar_init(bar(L::kODone + g), 1);
     }
-    for (int s = 0; s < L::kStages; ++s) mbar_init(bar(L::kKVFull + s), 1);
+    for (int s = 0; s < L::kStages / 2; ++s) mbar_init(bar(L::kKVFull + s), 1);
     for (int s = 0; s < L::kStages / 2; ++s) mbar_init(bar(L::kKVEmpty + s), 1);
     mbar_init(bar(L::kDrain), 1);
     mbar_init(bar(L::kStageFull), 128);
@@ -366,23 +368,52 @@ __global__ void __launch_bounds__(kNumThreads, 1)
               }
             }
             if (!ok) break;
-            mbar_arrive_expect_tx(bar(L::kKVFull + slot), L::kTileBytes);
+            // K(j) and V(j - 1) complete step barrier B(j), V(j) completes
+            // B(j + 1); B(j) is armed (both tiles) as K(j) goes out, which
+            // may be after V(j - 1) has landed (the transaction count then
+            // runs negative until the arming).  B(0) has K(0) alone.
+            // A barrier's next phase may only receive copies once its previous
+            // one completed: for V(j) with j >= h and K(j) with j >= h the slot
+            // release above implies it (the MMA waited B(j + 1 - h), B(j - h)
+            // before that release); V(h - 1), the first to reuse B(0)'s
+            // object, waits for B(0) itself.
+            constexpr int h = L::kStages / 2;
+            const int j = static_cast<int>(kv_it / 2);
+            const uint32_t sb = bar(L::kKVFull + (j + kv) % h);
+            if (kv && j == h - 1) {
+              ok = wait_bar(bar(L::kKVFull), 0u, ctl, kSiteProducerKV);
+              if (!ok) break;
+            }
+            if (!kv) mbar_arrive_expect_tx(sb, (j == 0 ? 1u : 2u) * L::kTileBytes);
             if (FP8 && kv)  // V^T: all d rows of key block n
-              tma_load_4d(sbase + L::kKVOff + slot * L::kTileBytes, &p.tm_v,
-                          bar(L::kKVFull + slot), 0, 0, n, w.sv.kv_head);
+              tma_load_4d(sbase + L::kKVOff + slot * L::kTileBytes, &p.tm_v, sb, 0, 0, n,
+                          w.sv.kv_head);
             else
               tma_load_4d(sbase + L::kKVOff + slot * L::kTileBytes, kv ? &p.tm_v : &p.tm_k,
-                          bar(L::kKVFull + slot), 0, w.sv.row_base + n * kBlockN, 0,
-                          w.sv.kv_head);
+                          sb, 0, w.sv.row_base + n * kBlockN, 0, w.sv.kv_head);
             ++kv_it;
           }
         }
       }
-      // Let every copy this warp issued land before the CTA may exit.
-      const uint32_t first = kv_it > (uint32_t)L::kStages ? kv_it - L::kStages : 0u;
-      for (uint32_t it = first; it < kv_it; ++it)
-        wait_drain(bar(L::kKVFull + it % L::kStages), (it / L::kStages) & 1u,
-                   p.timeout_ns);
+      constexpr uint32_t h = L::kStages / 2;
+      const uint32_t steps = kv_it / 2;  // K/V steps with both tiles issued
+      if (kv_it > 0) {
+        // The stream's last V(steps - 1) completes B(steps) alone: arm it
+        // (an odd count means K(steps) went out, and armed it, last).  B's
+        // previous phase, B(steps - h), completed before V(steps - 1) could
+        // be issued into its released slot.
+        if (kv_it % 2 == 0) mbar_arrive_expect_tx(bar(L::kKVFull + steps % h), L::kTileBytes);
+        // Let every copy this warp issued land before the CTA may exit:
+        // those of the last h step barriers B(steps + 1 - h) .. B(steps),
+        // h distinct objects (an older phase of the same object could not be
+        // told apart by its parity once the newer one has completed).  Older
+        // copies have landed: K(steps - h) before the slot of the last V was
+        // released (the MMA waited B(steps - h)), K(0) before V(h - 1) went
+        // out.
+        const uint32_t first = steps + 1 > h ? steps + 1 - h : 0u;
+        for (uint32_t jj = first; jj <= steps; ++jj)
+          wait_drain(bar(L::kKVFull + jj % h), (jj / h) & 1u, p.timeout_ns);
+      }
       for (int g = 0; g < 2; ++g)
         if (q_it[g] > 0) wait_drain(bar(L::kQFull + g), (q_it[g] - 1) & 1u, p.timeout_ns);
     }
@@ -405,7 +436,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       // 8-key groups 1024 B apart (SBO).
       const uint64_t v_desc0 = FP8 ? smem_desc_sw128(sbase + L::kKVOff, 16, 1024)
                                    : smem_desc_sw128(sbase + L::kKVOff, kBlockN * 128, 1024);
-      uint32_t slot = 0, phase = 0;  // next K/V ring position
+      uint32_t slot = 0;  // next K/V ring position
       uint32_t step = 0;             // K/V stream step (for the release groups)
       uint32_t q_par[2] = {0, 0}, p_par[2] = {0, 0}, o_cnt[2] = {0, 0};
       bool ok = true;
@@ -433,8 +464,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           }
           if (!ok) break;
         }
-        const uint32_t kslot = slot, kphase = phase;
-        bool k_ready = false;  // K(j) is waited for just before its first use
+        const uint32_t kslot = slot;
+        // V(j-1) and K(j), the two tiles this step reads: one wait
+        ok = wait_bar(bar(L::kKVFull + step % (L::kStages / 2)), (step / (L::kStages / 2)) & 1u,
+                      ctl, kSiteMmaK);
+        if (!ok) break;
         for (int g = 0; g < 2; ++g) {
           // ---- O_g += P_g(j-1) V(j-1)
           if (prev_valid && prev_active[g]) {
@@ -469,11 +503,6 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           // ---- S_g = Q_g K_j^T, issued right behind P_g(j-1) V, which
           //      reads P_g(j-1) from the columns this overwrites
           if (cur_valid && n >= w.n0[g] && n < w.n1[g]) {
-            if (!k_ready) {
-              ok = wait_bar(bar(L::kKVFull + kslot), kphase, ctl, kSiteMmaK);
-              if (!ok) break;
-              k_ready = true;
-            }
             tc_fence_after_sync();
             const uint64_t a = q_desc0 + g * kSlotStep;
             const uint64_t b = k_desc0 + kslot * kSlotStep;
@@ -493,12 +522,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         tc_commit(bar(L::kKVEmpty + step % (L::kStages / 2)));
         ++step;
         if (!cur_valid) break;
-        if (++slot == (uint32_t)L::kStages) { slot = 0; phase ^= 1u; }
-        // V(j): waited for now, used (and released) in step j+1
+        if (++slot == (uint32_t)L::kStages) slot = 0;
+        // V(j): used (and released) in step j+1, whose barrier covers it
         const uint32_t vslot = slot;
-        ok = wait_bar(bar(L::kKVFull + vslot), phase, ctl, kSiteMmaV);
-        if (!ok) break;
-        if (++slot == (uint32_t)L::kStages) { slot = 0; phase ^= 1u; }
+        if (++slot == (uint32_t)L::kStages) slot = 0;
         prev_valid = true;
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
