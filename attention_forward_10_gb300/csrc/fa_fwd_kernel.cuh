@@ -38,6 +38,16 @@
 // for the commit's round trip twice per step (5% at N = 2048); repeated
 // full-size runs are checked to be bit-identical.
 //
+// K/V stream.  K(j) and V(j) go to ring slots 2(j % h) and 2(j % h) + 1
+// (h = STAGES / 2).  One "full" barrier per step, B(j), completes when the
+// two tiles step j first reads have landed, V(j-1) and K(j), so the MMA
+// issuer waits once per step; one commit per step releases K(j) and V(j-1)
+// for the producer (release group j % h).
+//
+// Row maximum.  A softmax thread loads its row of S with tcgen05.ld.red.max,
+// which also returns the maximum of the loaded columns (unmasked tiles use
+// it; masked tiles take the maximum over the kept columns).
+//
 // Tensor memory (512 columns x 128 lanes, fp32):
 //   [0,128)    S_0 (scores of tile 0); P_0 (16-bit, packed in pairs) is
 //              written over its first 64 columns after the row is read

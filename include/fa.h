@@ -23,6 +23,14 @@
  *
  * All entry points are plain C: pointers and sizes, no C++ or framework types,
  * no exceptions.  Every function returns an fa_status_t code (or a string).
+ *
+ * Launches: every kernel is launched with programmatic stream serialisation
+ * (programmatic dependent launch).  It may begin its set-up while the
+ * previous kernel of the stream finishes, but reads and writes global memory
+ * only after that kernel has completed; stream order is therefore unchanged
+ * for the caller.  A caller's own kernel launched the same way right after
+ * one of these must wait (griddepcontrol.wait) before using its results, as
+ * with any programmatic dependent launch.
  */
 #ifndef FA_GB300_H
 #define FA_GB300_H
