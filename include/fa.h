@@ -141,7 +141,11 @@ FA_API int fa_fwd_ext(const void* q, const void* k, const void* v, void* o, floa
  *               sequence longer than max_seqlen; the kernels clamp offsets
  *               and lengths to those bounds, so a malformed array can only
  *               leave rows unwritten, never touch memory outside the tensors.
- *               Rows outside every sequence are not written.
+ *               Rows outside every sequence are not written.  The offsets are
+ *               absolute row indices, so a pointer into a longer offset array
+ *               (with batch counting from there) runs a subset of consecutive
+ *               sequences alone, writing exactly their rows, bit for bit as
+ *               the call over all of them would.
  *   batch, max_seqlen, total
  *               number of sequences, the longest length, and the packed row
  *               count; any of them 0: nothing is done (FA_OK).  Negative:
