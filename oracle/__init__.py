@@ -97,6 +97,10 @@ def _bind(path: str):
     lib.attn_ref_varlen_u16.argtypes = [vp, vp, vp, c_int, vp, c_long, c_long, c_long, c_long,
                                         c_long, c_double, c_int, c_long, c_long, vp, vp, c_int]
     lib.attn_ref_varlen_u16.restype = c_int
+    lib.attn_ref_varlen_qk_u16.argtypes = [vp, vp, vp, c_int, vp, vp, vp, vp, c_long, c_long,
+                                           c_long, c_long, c_long, c_long, c_double, c_int,
+                                           c_long, c_long, vp, vp, c_int]
+    lib.attn_ref_varlen_qk_u16.restype = c_int
     lib.attn_ref_bwd_u16.argtypes = [vp, vp, vp, vp, c_int, c_long, c_long, c_long, c_long,
                                      c_long, c_double, c_int, c_long, c_long, vp, vp, vp, c_int]
     lib.attn_ref_bwd_u16.restype = c_int
@@ -299,6 +303,46 @@ def attention_varlen(q, k, v, cu_seqlens, scale: float, causal: bool, window_lef
                                      _ptr(o), _ptr(lse), int(nthreads))
     if rc != 0:
         raise RuntimeError("oracle attn_ref_varlen_u16 failed")
+    return o, lse
+
+
+def attention_varlen_qk(q, k, v, cu_seqlens_q, cu_seqlens_k, scale: float, causal: bool,
+                        window_left: int = -1, window_right: int = -1, seqused_q=None,
+                        seqused_k=None, nthreads: int = 0):
+    """Separate query and key sequences packed along the rows: q [total_q, H,
+    d], k, v [total_k, H_kv, d]; sequence b has seqused_q[b] queries (all of
+    rows cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 when seqused_q is None) and
+    seqused_k[b] keys likewise, masks bottom-right aligned (query i at key
+    position i + n_k - n_q).  Returns O [total_q, H, d] and LSE [H, total_q]
+    (float64); rows outside every sequence's used queries are NaN, queries
+    with no admissible key get O = 0 and LSE = -inf."""
+    qw, is_bf16 = _u16_view(q)
+    kw, kb = _u16_view(k)
+    vw, vb = _u16_view(v)
+    if not (is_bf16 == kb == vb):
+        raise TypeError("q, k, v must share one dtype")
+    total_q, H, d = (int(x) for x in q.shape)
+    if k.shape != v.shape or k.shape[2] != d or H % int(k.shape[1]):
+        raise ValueError("k, v must be [total_k, H_kv, d] with H a multiple of H_kv")
+    total_k, H_kv = int(k.shape[0]), int(k.shape[1])
+
+    def arr(x):
+        return None if x is None else np.ascontiguousarray(
+            np.asarray(x, dtype=np.int64).reshape(-1))
+    cu_q, cu_k = arr(cu_seqlens_q), arr(cu_seqlens_k)
+    used_q, used_k = arr(seqused_q), arr(seqused_k)
+    batch = cu_q.size - 1
+    if cu_k.size != cu_q.size or any(u is not None and u.size < batch for u in (used_q, used_k)):
+        raise ValueError("cu_seqlens_q/k need batch + 1 entries, seqused_q/k batch entries")
+    o = np.full((total_q, H, d), np.nan, dtype=np.float64)
+    lse = np.full((H, total_q), np.nan, dtype=np.float64)
+    rc = _load().attn_ref_varlen_qk_u16(
+        _ptr(qw), _ptr(kw), _ptr(vw), int(is_bf16), _ptr(cu_q), _ptr(cu_k),
+        None if used_q is None else _ptr(used_q), None if used_k is None else _ptr(used_k),
+        batch, total_q, total_k, H, H_kv, d, float(scale), int(bool(causal)), int(window_left),
+        int(window_right), _ptr(o), _ptr(lse), int(nthreads))
+    if rc != 0:
+        raise RuntimeError("oracle attn_ref_varlen_qk_u16 failed")
     return o, lse
 
 

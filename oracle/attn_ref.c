@@ -51,7 +51,9 @@
  * lengths packed along the rows of [total][H][d] tensors, sequence b being
  * rows cu[b] .. cu[b+1]-1 -- the cu_seqlens mode of the Hopper pages.  Each
  * sequence is the definition above on its own rows, positions counted from
- * its first row.
+ * its first row.  attn_ref_varlen_qk_u16 generalises it to separate query
+ * and key offsets and used lengths (cross-attention, a KV cache), with the
+ * pages' bottom-right alignment of the masks.
  *
  * Inputs are the caller's 16-bit words (IEEE binary16 or bfloat16), widened
  * exactly to double here; every product, sum and exponential is in double.
@@ -413,17 +415,25 @@ int attn_ref_rows_u16_ex(const uint16_t *q, const uint16_t *k,
 }
 
 /*
- * Variable-length batch: sequences packed along the rows (self-attention,
- * each sequence's queries see that sequence's keys only) -- the cu_seqlens
- * mode of flash-attention "hopper/flash_fwd_kernel.h" and
- * "hopper/mainloop_bwd_sm90_tma_gmma_ws.hpp".
- *   q, o : [total][H][d];  k, v : [total][H_kv][d];  lse : [H][total]
- *   cu   : batch + 1 row offsets; sequence b is rows cu[b] .. cu[b+1]-1,
- *          and its row i (counted from the sequence start) sees the keys
- *          J(i) of that sequence under the mask and window of the _ex path.
- * Rows outside every sequence are not written.  Returns 0, or -1 on bad
- * arguments (offsets not non-decreasing within [0, total]) or allocation
- * failure.
+ * Variable-length batch with separate query and key sequences -- the
+ * cu_seqlens_q / cu_seqlens_k / seqused_q / seqused_k arguments of
+ * flash-attention "hopper/mainloop_bwd_sm90_tma_gmma_ws.hpp"
+ * (CollectiveMainloopBwd::Arguments, get_seqlen_q / get_seqlen_k) and the
+ * variable-length mode of "hopper/flash_fwd_kernel.h":
+ *   q, o : [total_q][H][d];  k, v : [total_k][H_kv][d];  lse : [H][total_q]
+ *   sequence b has n_q = used_q[b] queries (cu_q[b+1] - cu_q[b] when used_q
+ *   is NULL) in rows cu_q[b] .. cu_q[b] + n_q - 1, and n_k = used_k[b] keys
+ *   (cu_k[b+1] - cu_k[b] when used_k is NULL) in rows cu_k[b] ..
+ *   cu_k[b] + n_k - 1.
+ * Masks are bottom-right aligned, as on the backward page (its causal and
+ * local masking loops shift the query row by seqlen_k - seqlen_q): query i
+ * of the sequence sits at key position i + n_k - n_q, so causal keeps keys
+ * j <= i + n_k - n_q and the window keeps i + n_k - n_q - wl <= j <=
+ * i + n_k - n_q + wr.  A query with no admissible key gets O = 0 and
+ * LSE = -inf (the forward page's store_zero).  Rows of o / lse outside every
+ * sequence's used query rows are not written.  Returns 0, or -1 on bad
+ * arguments (offsets not non-decreasing within [0, total], a used length
+ * beyond its sequence's rows) or allocation failure.
  */
 static void gather_rows(const uint16_t *src, long stride, long rows, long d,
                         double *dst, int is_bf16) {
@@ -431,48 +441,68 @@ static void gather_rows(const uint16_t *src, long stride, long rows, long d,
         widen_slice(src + r * stride, dst + r * d, d, is_bf16);
 }
 
-int attn_ref_varlen_u16(const uint16_t *q, const uint16_t *k,
-                        const uint16_t *v, int is_bf16, const long *cu,
-                        long batch, long total, long H, long H_kv, long d,
-                        double scale, int causal, long wl, long wr, double *o,
-                        double *lse, int nthreads) {
-    if (!q || !k || !v || !cu || !o || !lse || batch < 0 || total < 0 ||
-        H <= 0 || H_kv <= 0 || H % H_kv != 0 || d <= 0)
+/* Rows and used length of sequence b under offsets cu and lengths used. */
+static int seq_rows(const long *cu, const long *used, long b, long total,
+                    long *first, long *n) {
+    if (cu[b] < 0 || cu[b + 1] < cu[b] || cu[b + 1] > total) return -1;
+    *first = cu[b];
+    *n = used ? used[b] : cu[b + 1] - cu[b];
+    if (*n < 0 || *n > cu[b + 1] - cu[b]) return -1;
+    return 0;
+}
+
+int attn_ref_varlen_qk_u16(const uint16_t *q, const uint16_t *k,
+                           const uint16_t *v, int is_bf16, const long *cu_q,
+                           const long *cu_k, const long *used_q,
+                           const long *used_k, long batch, long total_q,
+                           long total_k, long H, long H_kv, long d,
+                           double scale, int causal, long wl, long wr,
+                           double *o, double *lse, int nthreads) {
+    if (!q || !k || !v || !cu_q || !cu_k || !o || !lse || batch < 0 ||
+        total_q < 0 || total_k < 0 || H <= 0 || H_kv <= 0 || H % H_kv != 0 ||
+        d <= 0)
         return -1;
-    long longest = 0;
+    long longest = 1;
     for (long b = 0; b < batch; ++b) {
-        if (cu[b] < 0 || cu[b + 1] < cu[b] || cu[b + 1] > total) return -1;
-        if (cu[b + 1] - cu[b] > longest) longest = cu[b + 1] - cu[b];
+        long q0, nq, k0, nk;
+        if (seq_rows(cu_q, used_q, b, total_q, &q0, &nq) != 0 ||
+            seq_rows(cu_k, used_k, b, total_k, &k0, &nk) != 0)
+            return -1;
+        if (nq > longest) longest = nq;
+        if (nk > longest) longest = nk;
     }
     set_threads(nthreads);
-    long group = H / H_kv, cap = longest > 0 ? longest : 1;
-    double *qd = (double *)malloc(sizeof(double) * (size_t)(cap * d));
-    double *kd = (double *)malloc(sizeof(double) * (size_t)(cap * d));
-    double *vd = (double *)malloc(sizeof(double) * (size_t)(cap * d));
+    long group = H / H_kv;
+    double *qd = (double *)malloc(sizeof(double) * (size_t)(longest * d));
+    double *kd = (double *)malloc(sizeof(double) * (size_t)(longest * d));
+    double *vd = (double *)malloc(sizeof(double) * (size_t)(longest * d));
     if (!qd || !kd || !vd) { free(qd); free(kd); free(vd); return -1; }
     int rc = 0;
     for (long b = 0; b < batch && rc == 0; ++b) {
-        long s0 = cu[b], n = cu[b + 1] - cu[b];
-        if (n == 0) continue;
+        long q0, nq, k0, nk;
+        seq_rows(cu_q, used_q, b, total_q, &q0, &nq);
+        seq_rows(cu_k, used_k, b, total_k, &k0, &nk);
+        if (nq == 0) continue;
         for (long h = 0; h < H && rc == 0; ++h) {
             long hk = h / group;
-            gather_rows(q + (s0 * H + h) * d, H * d, n, d, qd, is_bf16);
-            gather_rows(k + (s0 * H_kv + hk) * d, H_kv * d, n, d, kd, is_bf16);
-            gather_rows(v + (s0 * H_kv + hk) * d, H_kv * d, n, d, vd, is_bf16);
+            gather_rows(q + (q0 * H + h) * d, H * d, nq, d, qd, is_bf16);
+            gather_rows(k + (k0 * H_kv + hk) * d, H_kv * d, nk, d, kd, is_bf16);
+            gather_rows(v + (k0 * H_kv + hk) * d, H_kv * d, nk, d, vd, is_bf16);
 #pragma omp parallel
             {
-                double *scores = (double *)malloc(sizeof(double) * (size_t)n);
+                double *scores = (double *)malloc(sizeof(double) * (size_t)longest);
                 if (!scores) {
 #pragma omp atomic write
                     rc = -1;
                 } else {
 #pragma omp for schedule(dynamic, 4)
-                    for (long i = 0; i < n; ++i) {
+                    for (long i = 0; i < nq; ++i) {
                         long j0, j1;
-                        key_range(n, i, causal, wl, wr, &j0, &j1);
+                        /* bottom-right: query i at key position i + nk - nq */
+                        key_range(nk, i + nk - nq, causal, wl, wr, &j0, &j1);
                         attend_range(qd + i * d, kd, vd, d, j0, j1, scale, scores,
-                                     o + ((s0 + i) * H + h) * d,
-                                     lse + h * total + s0 + i);
+                                     o + ((q0 + i) * H + h) * d,
+                                     lse + h * total_q + q0 + i);
                     }
                     free(scores);
                 }
@@ -481,6 +511,22 @@ int attn_ref_varlen_u16(const uint16_t *q, const uint16_t *k,
     }
     free(qd); free(kd); free(vd);
     return rc;
+}
+
+/*
+ * Variable-length batch of self-attention sequences: one set of offsets for
+ * queries and keys (sequence b is rows cu[b] .. cu[b+1]-1 of q, k, v, o;
+ * lse [H][total]), i.e. attn_ref_varlen_qk_u16 with cu_k = cu_q and no used
+ * lengths, where the bottom-right alignment is the plain diagonal.
+ */
+int attn_ref_varlen_u16(const uint16_t *q, const uint16_t *k,
+                        const uint16_t *v, int is_bf16, const long *cu,
+                        long batch, long total, long H, long H_kv, long d,
+                        double scale, int causal, long wl, long wr, double *o,
+                        double *lse, int nthreads) {
+    return attn_ref_varlen_qk_u16(q, k, v, is_bf16, cu, cu, NULL, NULL, batch,
+                                  total, total, H, H_kv, d, scale, causal, wl,
+                                  wr, o, lse, nthreads);
 }
 
 /*

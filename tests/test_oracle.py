@@ -478,6 +478,159 @@ def test_varlen_rejects_malformed_offsets():
             oracle.attention_varlen(q, q, q, cu, 0.5, False)
 
 
+# ------------------- separate query / key sequences, used lengths (KV cache)
+def _sdpa_qk(qs, ks, vs, scale, causal, window):
+    """torch float64 attention of one sequence with n_q queries ([n_q, H, d])
+    and n_k keys ([n_k, H_kv, d]); the mask is built from its bottom-right
+    definition (query i at key position i + n_k - n_q).  Rows with no
+    admissible key are returned as O = 0, LSE = -inf."""
+    nq, H, _ = qs.shape
+    nk = ks.shape[0]
+    group = H // ks.shape[1]
+    pos = torch.arange(nq)[:, None] + (nk - nq)
+    j = torch.arange(nk)[None, :]
+    allowed = torch.ones(nq, nk, dtype=torch.bool)
+    if causal:
+        allowed &= j <= pos
+    if window[0] >= 0:
+        allowed &= j >= pos - window[0]
+    if window[1] >= 0:
+        allowed &= j <= pos + window[1]
+    qd = qs.double().permute(1, 0, 2)
+    kd = ks.double().repeat_interleave(group, 1).permute(1, 0, 2)
+    vd = vs.double().repeat_interleave(group, 1).permute(1, 0, 2)
+    s = scale * qd @ kd.transpose(-1, -2)
+    lse = torch.logsumexp(s.masked_fill(~allowed, float("-inf")), -1)
+    p = torch.softmax(s.masked_fill(~allowed, float("-inf")), -1)
+    p = torch.nan_to_num(p, nan=0.0)   # rows without keys: all weights 0
+    o = p @ vd
+    return o.permute(1, 0, 2).numpy(), lse.numpy(), allowed.any(1).numpy()
+
+
+QK_CASES = [
+    # (n_q per sequence, n_k per sequence): cross-attention, decode, prefill
+    # continuation, fewer keys than queries, an empty query sequence
+    ([5, 1, 17, 0, 9], [12, 40, 17, 6, 3]),
+    ([1, 1, 1], [64, 1, 33]),
+    ([33, 8], [20, 8]),
+]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("window", [(-1, -1), (4, 2), (0, -1)])
+@pytest.mark.parametrize("case", range(len(QK_CASES)))
+def test_varlen_qk_matches_torch_per_sequence(causal, window, case):
+    """Separate query and key offsets against torch's float64 attention of
+    each sequence with the bottom-right mask; rows past the last sequence
+    stay unwritten."""
+    lq, lk = QK_CASES[case]
+    cu_q = np.concatenate([[0], np.cumsum(lq)]).tolist()
+    cu_k = np.concatenate([[0], np.cumsum(lk)]).tolist()
+    total_q, total_k = cu_q[-1] + 2, cu_k[-1] + 5
+    g = torch.Generator().manual_seed(440 + case)
+    q = torch.randn(total_q, 4, 16, generator=g).to(torch.bfloat16)
+    k = torch.randn(total_k, 2, 16, generator=g).to(torch.bfloat16)
+    v = torch.randn(total_k, 2, 16, generator=g).to(torch.bfloat16)
+    o, lse = oracle.attention_varlen_qk(q, k, v, cu_q, cu_k, 0.31, causal, *window)
+    for b in range(len(lq)):
+        if lq[b] == 0:
+            continue
+        q0, k0 = cu_q[b], cu_k[b]
+        o_ref, l_ref, _ = _sdpa_qk(q[q0:q0 + lq[b]], k[k0:k0 + lk[b]], v[k0:k0 + lk[b]], 0.31,
+                                   causal, window)
+        np.testing.assert_allclose(o[q0:q0 + lq[b]], o_ref, rtol=0, atol=1e-12)
+        np.testing.assert_array_equal(np.isinf(lse[:, q0:q0 + lq[b]]), np.isinf(l_ref))
+        fin = np.isfinite(l_ref)
+        np.testing.assert_allclose(lse[:, q0:q0 + lq[b]][fin], l_ref[fin], rtol=0, atol=1e-12)
+    assert np.isnan(o[cu_q[-1]:]).all() and np.isnan(lse[:, cu_q[-1]:]).all()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_qk_used_lengths_are_a_prefix(causal):
+    """seqused_q / seqused_k: only the first used rows of each sequence's
+    buffer rows take part (a KV cache with spare capacity); the result equals
+    the same call on buffers packed with the used rows alone, and query rows
+    past the used count stay unwritten."""
+    cap_q, cap_k = [6, 4, 9], [30, 16, 25]
+    used_q, used_k = [3, 4, 1], [21, 9, 25]
+    cu_q = np.concatenate([[0], np.cumsum(cap_q)]).tolist()
+    cu_k = np.concatenate([[0], np.cumsum(cap_k)]).tolist()
+    g = torch.Generator().manual_seed(450)
+    q = torch.randn(cu_q[-1], 2, 16, generator=g).to(torch.float16)
+    k = torch.randn(cu_k[-1], 1, 16, generator=g).to(torch.float16)
+    v = torch.randn(cu_k[-1], 1, 16, generator=g).to(torch.float16)
+    o, lse = oracle.attention_varlen_qk(q, k, v, cu_q, cu_k, 0.4, causal, seqused_q=used_q,
+                                        seqused_k=used_k)
+    take_q = np.concatenate([np.arange(cu_q[b], cu_q[b] + used_q[b]) for b in range(3)])
+    take_k = np.concatenate([np.arange(cu_k[b], cu_k[b] + used_k[b]) for b in range(3)])
+    pq = np.concatenate([[0], np.cumsum(used_q)]).tolist()
+    pk = np.concatenate([[0], np.cumsum(used_k)]).tolist()
+    o2, l2 = oracle.attention_varlen_qk(q[take_q], k[take_k], v[take_k], pq, pk, 0.4, causal)
+    np.testing.assert_array_equal(o[take_q], o2)
+    np.testing.assert_array_equal(lse[:, take_q], l2)
+    rest = np.setdiff1d(np.arange(cu_q[-1]), take_q)
+    assert np.isnan(o[rest]).all() and np.isnan(lse[:, rest]).all()
+    # and the torch reference on the used rows of sequence 0
+    o_ref, l_ref, _ = _sdpa_qk(q[0:3], k[0:21], v[0:21], 0.4, causal, (-1, -1))
+    np.testing.assert_allclose(o[0:3], o_ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse[:, 0:3], l_ref, rtol=0, atol=1e-12)
+
+
+def test_varlen_qk_decode_and_zero_query_closed_forms():
+    """One query per sequence (decode) under the causal mask sees every key
+    of its sequence: with Q = 0 its O is the mean of the sequence's V rows
+    and LSE = ln n_k; a window of w keeps the last w + 1 keys; with fewer
+    keys than queries the first n_q - n_k causal rows have no key (O = 0,
+    LSE = -inf) and row n_q - n_k + t sees keys 0..t."""
+    lk = [7, 30, 1]
+    cu_k = np.concatenate([[0], np.cumsum(lk)]).tolist()
+    g = torch.Generator().manual_seed(460)
+    k = torch.randn(cu_k[-1], 1, 16, generator=g).to(torch.bfloat16)
+    v = torch.randn(cu_k[-1], 1, 16, generator=g).to(torch.bfloat16)
+    q = torch.zeros(3, 3, 16, dtype=torch.bfloat16)
+    vd = v.double().numpy()[:, 0]
+    for window in ((-1, -1), (5, -1)):
+        o, lse = oracle.attention_varlen_qk(q, k, v, [0, 1, 2, 3], cu_k, 0.7, True, *window)
+        for b in range(3):
+            n = lk[b]
+            lo = 0 if window[0] < 0 else max(0, n - 1 - window[0])
+            for h in range(3):
+                np.testing.assert_allclose(o[b, h], vd[cu_k[b] + lo:cu_k[b] + n].mean(0),
+                                           rtol=0, atol=1e-13)
+                np.testing.assert_allclose(lse[h, b], math.log(n - lo), rtol=0, atol=1e-13)
+    # more queries than keys, causal
+    qz = torch.zeros(10, 1, 16, dtype=torch.bfloat16)
+    o, lse = oracle.attention_varlen_qk(qz, k, v, [0, 10], [0, 7], 0.7, True)
+    assert (o[:3] == 0).all() and np.isneginf(lse[0, :3]).all()
+    for t in range(7):
+        np.testing.assert_allclose(o[3 + t, 0], vd[0:t + 1].mean(0), rtol=0, atol=1e-13)
+        np.testing.assert_allclose(lse[0, 3 + t], math.log(t + 1), rtol=0, atol=1e-13)
+
+
+def test_varlen_qk_equal_offsets_is_the_self_attention_mode():
+    """cu_seqlens_k = cu_seqlens_q and no used lengths: the self-attention
+    packed mode, checked against the [B,H,N,d] definition."""
+    q, _, _ = make_random_qkv(2, 2, 23, 16, torch.bfloat16, seed=470)
+    _, k, v = make_random_qkv(2, 1, 23, 16, torch.bfloat16, seed=471)
+    o, lse = oracle.attention_ex(q, k, v, 0.3, True, 6, -1)
+    o_v, l_v = oracle.attention_varlen_qk(_pack(q), _pack(k), _pack(v), [0, 23, 46], [0, 23, 46],
+                                          0.3, True, 6, -1)
+    np.testing.assert_array_equal(o_v, o.transpose(0, 2, 1, 3).reshape(46, 2, 16))
+    np.testing.assert_array_equal(l_v, lse.transpose(1, 0, 2).reshape(2, 46))
+
+
+def test_varlen_qk_rejects_malformed_lengths():
+    q = torch.zeros(10, 1, 16, dtype=torch.bfloat16)
+    k = torch.zeros(12, 1, 16, dtype=torch.bfloat16)
+    bad = [dict(cu_seqlens_q=[0, 6, 4], cu_seqlens_k=[0, 6, 12]),
+           dict(cu_seqlens_q=[0, 5, 10], cu_seqlens_k=[0, 6, 13]),
+           dict(cu_seqlens_q=[0, 5, 10], cu_seqlens_k=[0, 6, 12], seqused_k=[7, 1]),
+           dict(cu_seqlens_q=[0, 5, 10], cu_seqlens_k=[0, 6, 12], seqused_q=[1, -1])]
+    for kw in bad:
+        with pytest.raises(RuntimeError):
+            oracle.attention_varlen_qk(q, k, k, scale=0.5, causal=False, **kw)
+
+
 # --------------------------------------------------------------- backward
 def _torch_attention_f64(q, k, v, scale, causal, window):
     """Reference forward in torch float64 with an explicit mask (autograd)."""

@@ -21,7 +21,7 @@ MUTANTS = {
     "values_as_keys": ("const double *k_row = kmat + j * d;",
                        "const double *k_row = vmat + j * d;"),
     "causal_reversed": ("if (causal && i + 1 < hi) hi = i + 1;",
-                        "if (causal) lo = i;"),
+                        "if (causal && i > lo) lo = i;"),
     "causal_no_diagonal": ("if (causal && i + 1 < hi) hi = i + 1;",
                            "if (causal && i + 1 < hi) hi = (i > 0 ? i : 1);"),
     "window_left_off_by_one": ("if (wl >= 0 && i - wl > lo) lo = i - wl;",
@@ -35,15 +35,21 @@ MUTANTS = {
     "no_max_subtraction": ("sum += exp(scores[j] - m);", "sum += exp(scores[j]);"),
     "unnormalised_output": ("double p = exp(scores[j] - lse);",
                             "double p = exp(scores[j] - m);"),
-    "varlen_kv_head": ("gather_rows(k + (s0 * H_kv + hk) * d",
-                       "gather_rows(k + (s0 * H_kv + h % H_kv) * d"),
-    "varlen_row_stride": ("gather_rows(q + (s0 * H + h) * d, H * d,",
-                          "gather_rows(q + (s0 * H + h) * d, d,"),
-    "varlen_lse_layout": ("lse + h * total + s0 + i", "lse + (s0 + i) * H + h"),
-    "varlen_global_positions": ("key_range(n, i, causal, wl, wr, &j0, &j1);\n"
-                                "                        attend_range(qd + i * d, kd, vd, d, j0, j1",
-                                "key_range(n, i + s0 < n ? i + s0 : n - 1, causal, wl, wr, &j0, &j1);\n"
-                                "                        attend_range(qd + i * d, kd, vd, d, j0, j1"),
+    "varlen_kv_head": ("gather_rows(k + (k0 * H_kv + hk) * d",
+                       "gather_rows(k + (k0 * H_kv + h % H_kv) * d"),
+    "varlen_row_stride": ("gather_rows(q + (q0 * H + h) * d, H * d,",
+                          "gather_rows(q + (q0 * H + h) * d, d,"),
+    "varlen_lse_layout": ("lse + h * total_q + q0 + i", "lse + (q0 + i) * H + h"),
+    "varlen_global_positions": ("key_range(nk, i + nk - nq, causal, wl, wr, &j0, &j1);",
+                                "key_range(nk, i + q0 + nk - nq < nk ? i + q0 + nk - nq : nk - 1,"
+                                " causal, wl, wr, &j0, &j1);"),
+    "varlen_top_left_alignment": ("key_range(nk, i + nk - nq, causal, wl, wr, &j0, &j1);",
+                                  "key_range(nk, i, causal, wl, wr, &j0, &j1);"),
+    "varlen_used_k_ignored": ("seq_rows(cu_k, used_k,", "seq_rows(cu_k, NULL,"),
+    "varlen_key_rows_from_query_offsets": ("        seq_rows(cu_k, used_k, b, total_k, &k0, &nk);\n"
+                                           "        if (nq == 0) continue;",
+                                           "        seq_rows(cu_k, used_k, b, total_k, &k0, &nk);\n"
+                                           "        k0 = q0;\n        if (nq == 0) continue;"),
     "bwd_dk_unscaled": ("dkj[c] += scale * ds * qi[c];", "dkj[c] += ds * qi[c];"),
     "bwd_rowsum_without_p": ("dsi += exp(s[j] - l) * dp;", "dsi += dp;"),
     "bwd_dv_from_ds": ("dvj[c] += p * doi[c];", "dvj[c] += ds * doi[c];"),
@@ -82,6 +88,9 @@ PIN_CALLS = [
      dict(causal=True, window=(5, 3))),
     (pins.test_varlen_matches_torch_per_sequence, dict(causal=True, window=(4, 2))),
     (pins.test_varlen_zero_queries_closed_form, {}),
+    (pins.test_varlen_qk_matches_torch_per_sequence, dict(causal=True, window=(4, 2), case=0)),
+    (pins.test_varlen_qk_used_lengths_are_a_prefix, dict(causal=True)),
+    (pins.test_varlen_qk_decode_and_zero_query_closed_forms, {}),
     (pins.test_bwd_matches_torch_autograd, dict(causal=True, window=(6, 3), H=4, H_kv=2)),
     (pins.test_bwd_directional_finite_difference, dict(causal=True)),
     (pins.test_bwd_sum_identities, dict(causal=False, window=(5, 2))),
