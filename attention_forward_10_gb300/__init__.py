@@ -52,6 +52,8 @@ SIGNATURES = {
                        _f, _i, _i, _i, _i, _vp, _ull, _vp], _i),
     "fa_fwd_varlen": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _i, _i,
                        _vp], _i),
+    "fa_fwd_varlen_qk": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i,
+                          _i, _i, _f, _i, _i, _i, _i, _vp], _i),
     "fa_fwd_splitkv": ([_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _i, _i, _i,
                         _vp, _ull, _vp], _i),
     "fa_splitkv_workspace_bytes": ([_i, _i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(_ull)], _i),
@@ -170,6 +172,19 @@ def fa_bwd_workspace_bytes(B: int, H: int, N: int) -> tuple[int, int]:
     out = ctypes.c_ulonglong(0)
     st = int(_lib.fa_bwd_workspace_bytes(B, H, N, ctypes.byref(out)))
     return st, int(out.value)
+
+
+def fa_fwd_varlen_qk(q: int, k: int, v: int, o: int, lse: int | None, cu_seqlens_q: int,
+                     cu_seqlens_k: int, seqused_q: int | None, seqused_k: int | None,
+                     batch: int, max_seqlen_q: int, max_seqlen_k: int, total_q: int,
+                     total_k: int, H: int, H_kv: int, d: int, scale: float, causal: int,
+                     window_left: int, window_right: int, dtype: int,
+                     stream: int | None) -> int:
+    return int(_lib.fa_fwd_varlen_qk(q, k, v, o, lse or None, cu_seqlens_q or None,
+                                     cu_seqlens_k or None, seqused_q or None, seqused_k or None,
+                                     batch, max_seqlen_q, max_seqlen_k, total_q, total_k, H,
+                                     H_kv, d, scale, causal, window_left, window_right, dtype,
+                                     stream or None))
 
 
 def fa_fwd_varlen(q: int, k: int, v: int, o: int, lse: int | None, cu_seqlens: int,
@@ -398,6 +413,63 @@ def fwd_varlen(q, k, v, cu_seqlens, max_seqlen: int, *, scale: float | None = No
                            int(window[0]), int(window[1]), _dtype_code(q), handle)
     if st != FA_OK:
         raise FaError(st, "fa_fwd_varlen")
+    return out, (lse if return_lse else None)
+
+
+def fwd_varlen_qk(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int,
+                  *, seqused_q=None, seqused_k=None, scale: float | None = None,
+                  causal: bool = False, window: tuple[int, int] = (-1, -1), out=None,
+                  lse=None, return_lse: bool = True, stream=None):
+    """Attention forward over packed sequences with separate query and key
+    rows (cross-attention, KV caches).
+
+    q is [total_q, H, d], k and v [total_k, H_kv, d] CUDA tensors; sequence
+    b has query rows cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 and key rows
+    cu_seqlens_k[b] .. cu_seqlens_k[b+1]-1 (int32 CUDA tensors of batch + 1
+    offsets), cut to their first seqused_q[b] / seqused_k[b] rows when those
+    int32 CUDA tensors are given.  Masks are bottom-right aligned.  Returns
+    ``(o, lse)`` with o [total_q, H, d] and lse float32 [H, total_q]; query
+    rows outside every sequence's used rows are left as they were in
+    ``out`` / ``lse``.
+    """
+    import torch
+    if q.dim() != 3 or k.dim() != 3 or v.shape != k.shape or k.shape[2] != q.shape[2]:
+        raise ValueError("q must be [total_q, H, d] and k, v one [total_k, H_kv, d] shape")
+    idx = [t for t in (cu_seqlens_q, cu_seqlens_k, seqused_q, seqused_k) if t is not None]
+    if not all(t.is_cuda for t in (q, k, v, *idx)):
+        raise ValueError("q, k, v and the offset tensors must be CUDA tensors (no CPU path)")
+    if any(t.dtype != torch.int32 or t.dim() != 1 or not t.is_contiguous() for t in idx):
+        raise ValueError("offsets and used lengths must be contiguous 1-D int32 tensors")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k, v must share one dtype")
+    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("q, k, v must be contiguous")
+    total_q, H, d = (int(x) for x in q.shape)
+    total_k = int(k.shape[0])
+    batch = int(cu_seqlens_q.numel()) - 1
+    if int(cu_seqlens_k.numel()) != batch + 1 or any(
+            t is not None and int(t.numel()) < batch for t in (seqused_q, seqused_k)):
+        raise ValueError("cu_seqlens_k needs batch + 1 offsets, seqused_q/k batch lengths")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if return_lse and lse is None:
+        lse = torch.empty((H, total_q), dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    ptr = lambda t: t.data_ptr() if t is not None else None  # noqa: E731
+    with torch.cuda.device(q.device):
+        st = fa_fwd_varlen_qk(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                              lse.data_ptr() if (return_lse and lse is not None) else None,
+                              cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(), ptr(seqused_q),
+                              ptr(seqused_k), max(batch, 0), int(max_seqlen_q),
+                              int(max_seqlen_k), total_q, total_k, H, int(k.shape[1]), d,
+                              float(scale), int(bool(causal)), int(window[0]), int(window[1]),
+                              _dtype_code(q), handle)
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_varlen_qk")
     return out, (lse if return_lse else None)
 
 

@@ -46,6 +46,22 @@ cudaError_t launch_watchdog_selftest(int* status, unsigned long long timeout_ns,
 }
 
 namespace {
+PFN_cuCtxGetCurrent_v4000 ctx_current_fn();
+PFN_cuCtxGetId_v12000 ctx_id_fn();
+}  // namespace
+
+unsigned long long current_context_id() {
+  auto get = ctx_current_fn();
+  auto get_id = ctx_id_fn();
+  if (get == nullptr || get_id == nullptr) return 0;
+  CUcontext ctx = nullptr;
+  if (get(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  unsigned long long id = 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+namespace {
 
 constexpr int kMaxDevices = 64;
 
@@ -56,13 +72,26 @@ struct DeviceInfo {
   std::once_flag once;
   int ok = 0;           // 1: usable sm_103 device
   int num_sms = 0;
-  int* status = nullptr;
+  int* status = nullptr;  // status word of the context `status_ctx`
+  unsigned long long status_ctx = 0;
+  std::mutex mu;
 };
 DeviceInfo g_dev[kMaxDevices];
 
 // Per-device set-up with that device current: capability check, SM count and
-// the device address of the status word.
-DeviceInfo* device_info(int dev) {
+// the device address of the status word.  The address belongs to the
+// device's current context: it is looked up again whenever the calling
+// thread's context differs from the one it was taken in (after
+// cudaDeviceReset, or under another driver context), so no kernel is handed
+// the address of a destroyed context.
+// What a call needs of its device, copied under the device's lock.
+struct DevState {
+  int ok = 0;
+  int num_sms = 0;
+  int* status = nullptr;
+};
+
+DevState* device_info(int dev, DevState* out) {
   if (dev < 0 || dev >= kMaxDevices) return nullptr;
   DeviceInfo& info = g_dev[dev];
   std::call_once(info.once, [&] {
@@ -71,13 +100,53 @@ DeviceInfo* device_info(int dev) {
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return;
-    void* addr = nullptr;
-    if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess) return;
     info.num_sms = sms;
-    info.status = static_cast<int*>(addr);
     info.ok = (major == 10 && minor == 3) ? 1 : 0;
   });
-  return &info;
+  std::lock_guard<std::mutex> lock(info.mu);
+  const unsigned long long ctx = current_context_id();
+  if (info.status == nullptr || ctx == 0 || ctx != info.status_ctx) {
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess) {
+      cudaGetLastError();  // leave no stale error for the caller's next check
+      info.status = nullptr;
+      info.status_ctx = 0;
+    } else {
+      info.status = static_cast<int*>(addr);
+      // (read after the look-up, which makes the primary context current)
+      info.status_ctx = current_context_id();
+    }
+  }
+  out->ok = info.ok;
+  out->num_sms = info.num_sms;
+  out->status = info.status;
+  return out;
+}
+
+PFN_cuCtxGetCurrent_v4000 ctx_current_fn() {
+  static PFN_cuCtxGetCurrent_v4000 fn = [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 4000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      ptr = nullptr;
+    return reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(ptr);
+  }();
+  return fn;
+}
+
+PFN_cuCtxGetId_v12000 ctx_id_fn() {
+  static PFN_cuCtxGetId_v12000 fn = [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &ptr, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      ptr = nullptr;
+    return reinterpret_cast<PFN_cuCtxGetId_v12000>(ptr);
+  }();
+  return fn;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -196,7 +265,8 @@ int fa_set_max_ctas(int max_ctas) {
 int fa_num_sms(void) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return -1;
-  fa::DeviceInfo* info = fa::device_info(dev);
+  fa::DevState dev_state;
+  fa::DevState* info = fa::device_info(dev, &dev_state);
   return (info != nullptr && info->num_sms > 0) ? info->num_sms : -1;
 }
 
@@ -224,9 +294,16 @@ struct ForwardCall {
   int causal, window_left, window_right, dtype;
   void* stream;
   // variable-length batches: B sequences packed along the rows, N = the
-  // longest; nullptr / 0 for the [B][H][N][d] layout
+  // longest query sequence; nullptr / 0 for the [B][H][N][d] layout.  Keys
+  // have their own offsets, total and longest length (the query ones for
+  // self-attention) and both sides optional used lengths.
   const int* cu_seqlens = nullptr;
   int total = 0;
+  const int* cu_seqlens_k = nullptr;
+  int total_k = 0;
+  int N_k = 0;
+  const int* seqused_q = nullptr;
+  const int* seqused_k = nullptr;
   // FP8 (E4M3) inputs: descale factors and the V^T workspace
   bool fp8 = false;
   float descale_q = 1.f, descale_k = 1.f, descale_v = 1.f;
@@ -276,7 +353,8 @@ int launch_forward(const ForwardCall& c, void* o_out, float* lse_out, int num_sp
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
-  DeviceInfo* info = device_info(dev);
+  DevState dev_state;
+  DevState* info = device_info(dev, &dev_state);
   if (info == nullptr || info->status == nullptr) return FA_ERR_CUDA;
   if (!info->ok) return FA_ERR_UNSUPPORTED;
 
@@ -299,9 +377,15 @@ int launch_forward(const ForwardCall& c, void* o_out, float* lse_out, int num_sp
         !encode_qkvo_map(&p.tm_o, o_out, N, d, ibh, true, kBlockM, o_blocks))
       return FA_ERR_CUDA;
   } else if (packed) {
+    // no key rows at all: every query row is fully masked, and the K/V maps
+    // (read, then masked out) view the query buffer instead
+    const bool no_keys = c.total_k == 0;
+    const void* kb = no_keys ? c.q : c.k;
+    const void* vb = no_keys ? c.q : c.v;
+    const int k_rows = no_keys ? c.total : c.total_k;
     if (!encode_packed_map(&p.tm_q, c.q, c.total, c.H, d, bf16, kBlockM, d / 64) ||
-        !encode_packed_map(&p.tm_k, c.k, c.total, c.H_kv, d, bf16, kv_rows, d / 64) ||
-        !encode_packed_map(&p.tm_v, c.v, c.total, c.H_kv, d, bf16, kv_rows, d / 64) ||
+        !encode_packed_map(&p.tm_k, kb, k_rows, c.H_kv, d, bf16, kv_rows, d / 64) ||
+        !encode_packed_map(&p.tm_v, vb, k_rows, c.H_kv, d, bf16, kv_rows, d / 64) ||
         !encode_packed_map(&p.tm_o, o_out, c.total, c.H, d, bf16, kBlockM, o_blocks))
       return FA_ERR_CUDA;
   } else if (!encode_qkvo_map(&p.tm_q, c.q, N, d, ibh, bf16, kBlockM, d / 64) ||
@@ -311,7 +395,13 @@ int launch_forward(const ForwardCall& c, void* o_out, float* lse_out, int num_sp
     return FA_ERR_CUDA;
   }
   p.cu_seqlens = c.cu_seqlens;
+  p.cu_seqlens_k = packed ? (c.cu_seqlens_k != nullptr ? c.cu_seqlens_k : c.cu_seqlens) : nullptr;
+  p.seqused_q = packed ? c.seqused_q : nullptr;
+  p.seqused_k = packed ? c.seqused_k : nullptr;
   p.total_rows = packed ? c.total : 0;
+  p.total_rows_k = packed ? (c.cu_seqlens_k != nullptr ? c.total_k : c.total) : 0;
+  const int N_k = (packed && c.cu_seqlens_k != nullptr) ? c.N_k : N;
+  p.N_k = N_k;
   p.o_ptr = static_cast<uint16_t*>(o_out);
   p.lse = lse_out;
   p.status = info->status;
@@ -323,10 +413,12 @@ int launch_forward(const ForwardCall& c, void* o_out, float* lse_out, int num_sp
   p.n_ktiles = (N + kv_rows - 1) / kv_rows;
   p.H = c.H;
   p.group = c.H / c.H_kv;
-  // window bounds: negative or beyond N means unbounded (= N); causal caps
-  // the right bound at 0
-  p.win_left = (c.window_left < 0 || c.window_left > N) ? N : c.window_left;
-  p.win_right = (c.window_right < 0 || c.window_right > N) ? N : c.window_right;
+  // window bounds: negative or beyond N + N_k means unbounded (= N + N_k,
+  // wider than any query's distance to any key); causal caps the right
+  // bound at 0
+  const int unbounded = N + N_k;
+  p.win_left = (c.window_left < 0 || c.window_left > unbounded) ? unbounded : c.window_left;
+  p.win_right = (c.window_right < 0 || c.window_right > unbounded) ? unbounded : c.window_right;
   if (c.causal) p.win_right = 0;
   p.num_splits = num_splits;
   p.split_tiles = split_tiles;
@@ -641,18 +733,38 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
                   const int* cu_seqlens, int batch, int max_seqlen, int total, int H, int H_kv,
                   int d, float scale, int causal, int window_left, int window_right, int dtype,
                   void* stream) {
+  // self-attention within each sequence: the keys share the query offsets
+  return fa_fwd_varlen_qk(q, k, v, o, lse, cu_seqlens, cu_seqlens, nullptr, nullptr, batch,
+                          max_seqlen, max_seqlen, total, total, H, H_kv, d, scale, causal,
+                          window_left, window_right, dtype, stream);
+}
+
+int fa_fwd_varlen_qk(const void* q, const void* k, const void* v, void* o, float* lse,
+                     const int* cu_seqlens_q, const int* cu_seqlens_k, const int* seqused_q,
+                     const int* seqused_k, int batch, int max_seqlen_q, int max_seqlen_k,
+                     int total_q, int total_k, int H, int H_kv, int d, float scale, int causal,
+                     int window_left, int window_right, int dtype, void* stream) {
   using namespace fa;
-  // B = batch and N = max_seqlen in the shared checks
-  const ForwardCall c{q, k, v, o, lse, batch, H, H_kv, max_seqlen, d, scale, causal,
-                      window_left, window_right, dtype, stream, cu_seqlens, total};
-  if (total < 0) return FA_ERR_INVALID_ARG;
+  // B = batch and N = max_seqlen_q in the shared checks
+  ForwardCall c{q, k, v, o, lse, batch, H, H_kv, max_seqlen_q, d, scale, causal,
+                window_left, window_right, dtype, stream, cu_seqlens_q, total_q};
+  c.cu_seqlens_k = cu_seqlens_k;
+  c.total_k = total_k;
+  c.N_k = max_seqlen_k;
+  c.seqused_q = seqused_q;
+  c.seqused_k = seqused_k;
+  if (total_q < 0 || total_k < 0 || max_seqlen_k < 0) return FA_ERR_INVALID_ARG;
+  // positions and window bounds stay far from int overflow
+  if (max_seqlen_q >= (1 << 30) || max_seqlen_k >= (1 << 30)) return FA_ERR_INVALID_ARG;
   int st = validate(c);
   if (st != FA_OK) return st;
-  if (empty_problem(c) || total == 0) return FA_OK;
+  if (empty_problem(c) || total_q == 0) return FA_OK;
   st = check_pointers(c);
   if (st != FA_OK) return st;
-  if (cu_seqlens == nullptr) return FA_ERR_INVALID_ARG;
-  if (!aligned(cu_seqlens, 4)) return FA_ERR_MISALIGNED;
+  if (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr) return FA_ERR_INVALID_ARG;
+  if (!aligned(cu_seqlens_q, 4) || !aligned(cu_seqlens_k, 4) || !aligned(seqused_q, 4) ||
+      !aligned(seqused_k, 4))
+    return FA_ERR_MISALIGNED;
   return launch_forward(c, o, lse, 1, 0);
 }
 
@@ -933,7 +1045,8 @@ int bwd_launch(const void* q, const void* k, const void* v, const void* o, const
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
-  DeviceInfo* info = device_info(dev);
+  DevState dev_state;
+  DevState* info = device_info(dev, &dev_state);
   if (info == nullptr || info->status == nullptr) return FA_ERR_CUDA;
   if (!info->ok) return FA_ERR_UNSUPPORTED;
   const bool bf16 = dtype == FA_DTYPE_BF16;
@@ -1070,7 +1183,8 @@ int fa_get_device_status(void* stream, int* site) {
     return FA_ERR_CUDA;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
-  DeviceInfo* info = device_info(dev);
+  DevState dev_state;
+  DevState* info = device_info(dev, &dev_state);
   if (info == nullptr || info->status == nullptr) return FA_ERR_CUDA;
   int word = 0;
   if (cudaMemcpy(&word, info->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
@@ -1088,7 +1202,8 @@ int fa_selftest_watchdog(long long timeout_us, void* stream) {
   if (timeout_us < 1) return FA_ERR_INVALID_ARG;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
-  DeviceInfo* info = device_info(dev);
+  DevState dev_state;
+  DevState* info = device_info(dev, &dev_state);
   if (info == nullptr || info->status == nullptr) return FA_ERR_CUDA;
   if (!info->ok) return FA_ERR_UNSUPPORTED;
   cudaError_t e = launch_watchdog_selftest(

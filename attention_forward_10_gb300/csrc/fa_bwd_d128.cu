@@ -21,11 +21,11 @@ cudaError_t launch_all(const BwdParams& p_kv, const BwdParams& p_q, const void* 
                              lse, lse2, dsum, p_q.num_bh, p_q.N, p_q.n_pad, p_q);
   if (e != cudaSuccess) return e;
   constexpr int kSmem = bwd::Layout<128>::kSmemBytes;
-  auto kv = bwd::fa_bwd_dkdv_kernel<128, CAUSAL, BF16, false>;
-  auto dq = bwd::fa_bwd_dq_kernel<128, CAUSAL, BF16, false>;
-  e = cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  constexpr auto kv = bwd::fa_bwd_dkdv_kernel<128, CAUSAL, BF16, false>;
+  constexpr auto dq = bwd::fa_bwd_dq_kernel<128, CAUSAL, BF16, false>;
+  e = smem_attribute_once<kv>(kSmem);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(dq, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  e = smem_attribute_once<dq>(kSmem);
   if (e != cudaSuccess) return e;
   e = launch_pdl(kv, dim3(grid_kv), dim3(bwd::kThreads), kSmem, stream, p_kv);
   if (e != cudaSuccess) return e;

@@ -26,10 +26,12 @@
 // [0,128) S, [128,256) dP, then the fp32 accumulators: dV and dK (dK/dV
 // kernel) or dQ (dQ kernel), D columns each.  Each column half writes its
 // 16-bit P (or dS) packed over the first 32 of its own 64 S (or dP) columns,
-// so the P V-style products take their A operand in two 64-key pieces.  As in the forward kernels, an MMA that
-// overwrites columns an earlier MMA reads as its A operand is issued right
-// behind it without a completion wait (the tensor pipe runs one CTA's MMAs in
-// issue order).  Every mbarrier wait is bounded.
+// so the P V-style products take their A operand in two 64-key pieces.  The
+// next step's S and dP products overwrite those A operands; the PTX ISA
+// orders two tcgen05.mma of one thread only when they share the accumulator
+// and shape, so the issuer first waits for the commit of the previous step's
+// accumulating products (its ring-release barrier).  Every mbarrier wait is
+// bounded.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -326,6 +328,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t st = it % L::kStages;
           ok = wait_bar(bar(L::kRingFull + st), (it / L::kStages) & 1u, ctl, kSiteMmaQ);
           if (!ok) break;
+          if (it > 0) {
+            // the previous step's dV, dK products read P^T, dS^T from the
+            // columns S^T, dP^T overwrite: wait for their commit
+            const uint32_t pst = (it - 1) % L::kStages;
+            ok = wait_bar(bar(L::kRingEmpty + pst), ((it - 1) / L::kStages) & 1u, ctl, kSiteMmaO);
+            if (!ok) break;
+          }
           tc_fence_after_sync();
           const uint32_t ring = sbase + L::kRingOff + st * 2 * L::kTile;
           const uint64_t q_kdesc = smem_desc_sw128(ring, 16, 1024);
@@ -593,6 +602,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t st = it % L::kStages;
           ok = wait_bar(bar(L::kRingFull + st), (it / L::kStages) & 1u, ctl, kSiteMmaK);
           if (!ok) break;
+          if (it > 0) {
+            // the previous step's dQ product read dS from the columns S
+            // overwrites: wait for its commit
+            const uint32_t pst = (it - 1) % L::kStages;
+            ok = wait_bar(bar(L::kRingEmpty + pst), ((it - 1) / L::kStages) & 1u, ctl, kSiteMmaO);
+            if (!ok) break;
+          }
           tc_fence_after_sync();
           const uint32_t ring = sbase + L::kRingOff + st * 2 * L::kTile;
           const uint64_t k_kdesc = smem_desc_sw128(ring, 16, 1024);

@@ -25,10 +25,12 @@
 //              tile, in two halves)
 //   warp  7    spare
 //
-// With three S buffers, S(G) overwrites the columns of P(G-3), whose P V
-// product was issued two MMA groups earlier; the tensor pipe runs one CTA's
-// MMAs in issue order, so S(G) needs no wait for it.  The softmax of tile
-// G-1 runs while S(G) executes.
+// With three S buffers, S(G) overwrites the columns of P(G-3), the A
+// operand of P(G-3) V, issued two MMA groups earlier.  The PTX ISA orders two
+// tcgen05.mma of one thread only when they share the accumulator and shape,
+// so S(G) first waits for that product's commit (barrier ODone of the
+// buffer); two MMA groups later it has normally completed, so the wait costs
+// the tensor pipe nothing.  The softmax of tile G-1 runs while S(G) executes.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -114,9 +116,17 @@ __device__ __forceinline__ Unit decode_unit(int u, const FaParams& p) {
     w.n0 = w.n1 = 0;  // past the end of a shorter packed sequence
     return w;
   }
-  key_tile_range(w.row0, min(len, w.row0 + kBlockM), len, p.win_left, p.win_right, kBN,
-                 &w.n0, &w.n1);
-  if (p.num_splits > 1) clip_to_split(split, p.split_tiles, &w.n0, &w.n1);
+  // rows row0 .. sit at key positions row0 + k_off .. (bottom-right alignment)
+  key_tile_range(w.row0 + w.sv.k_off, min(len, w.row0 + kBlockM) + w.sv.k_off, w.sv.k_len,
+                 p.win_left, p.win_right, kBN, &w.n0, &w.n1);
+  if (p.num_splits > 1) {
+    clip_to_split(split, p.split_tiles, &w.n0, &w.n1);
+  } else if (w.n1 == w.n0) {
+    // no row of the tile has a key: one fully masked key tile gives its rows
+    // O = 0 and LSE = -inf through the ordinary path
+    w.n0 = 0;
+    w.n1 = 1;
+  }
   return w;
 }
 
@@ -198,7 +208,7 @@ __global__ void __launch_bounds__(d256::kThreads, 1)
             if (!ok) break;
             mbar_arrive_expect_tx(bar(kKVFull + slot), kKVBytes);
             tma_load_4d(sbase + kKVOff + slot * kKVBytes, kv ? &p.tm_v : &p.tm_k,
-                        bar(kKVFull + slot), 0, w.sv.row_base + n * kBN, 0, w.sv.kv_head);
+                        bar(kKVFull + slot), 0, w.sv.k_row_base + n * kBN, 0, w.sv.kv_head);
             ++issued;
             if (++slot == (uint32_t)kStages) { slot = 0; phase ^= 1u; }
           }
@@ -249,10 +259,12 @@ __global__ void __launch_bounds__(d256::kThreads, 1)
           ok = wait_bar(bar(kKVFull + kslot), phase, ctl, kSiteMmaK);
           if (!ok) break;
           if (++slot == (uint32_t)kStages) { slot = 0; phase ^= 1u; }
-          // P(G-3) occupied buffer b; its P V product was issued two steps
-          // ago, and the tensor pipe runs one CTA's MMAs in issue order, so it
-          // has read P before this product overwrites the buffer (no wait:
-          // each wait in this thread delays the pipe)
+          // P(G-3) occupied buffer b: its P V product (issued two groups
+          // ago) must have read it before this product overwrites it
+          if (G >= (uint32_t)kSBufs) {
+            ok = wait_bar(bar(kODone + b), ((G - kSBufs) / kSBufs) & 1u, ctl, kSiteMmaO);
+            if (!ok) break;
+          }
           tc_fence_after_sync();
           mma_ss_kmajor_x16_q128_k64(tmem + b * kBN, q_desc, k_desc0 + kslot * kSlotStep,
                                      kIdescS, 0u);
@@ -309,6 +321,7 @@ __global__ void __launch_bounds__(d256::kThreads, 1)
       const int row = w.row0 + t;
       float m_ref = -INFINITY, l = 0.f;
       const int len = w.sv.len;
+      const int k_len = w.sv.k_len, k_off = w.sv.k_off;
       const int row_end = min(len, w.row0 + kBlockM);
       for (int n = w.n0; n < w.n1; ++n, ++G) {
         const uint32_t b = G % kSBufs;
@@ -325,14 +338,16 @@ __global__ void __launch_bounds__(d256::kThreads, 1)
 #pragma unroll
           for (int c = 0; c < kBN; ++c) s[c] = __uint_as_float(r[c]);
         }
-        // keys row - win_left .. row + win_right, below N
+        // keys pos - win_left .. pos + win_right below k_len, where
+        // pos = row + k_off is the row's key position
         const int kbase = n * kBN;
-        const bool need_mask = (kbase + kBN > len) ||
-                               (kbase + kBN - 1 > w.row0 + p.win_right) ||
-                               (kbase < row_end - 1 - p.win_left);
+        const bool need_mask = (kbase + kBN > k_len) ||
+                               (kbase + kBN - 1 > w.row0 + k_off + p.win_right) ||
+                               (kbase < row_end - 1 + k_off - p.win_left);
         if (need_mask) {
-          const int hi = min(len - kbase, row + p.win_right + 1 - kbase);  // c < hi
-          const int lo = row - p.win_left - kbase;                         // c >= lo
+          const int pos = row + k_off;
+          const int hi = min(k_len - kbase, pos + p.win_right + 1 - kbase);  // c < hi
+          const int lo = pos - p.win_left - kbase;                           // c >= lo
 #pragma unroll
           for (int c = 0; c < kBN; ++c)
             if (c >= hi || c < lo) s[c] = -INFINITY;

@@ -8,9 +8,8 @@ namespace {
 template <bool CAUSAL, bool BF16>
 cudaError_t launch_one(const FaParams& p, int grid, cudaStream_t stream) {
   constexpr int kSmem = d256::kSmemBytes;
-  auto kernel = fa_fwd_d256_kernel<CAUSAL, BF16, true>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  constexpr auto kernel = fa_fwd_d256_kernel<CAUSAL, BF16, true>;
+  cudaError_t e = smem_attribute_once<kernel>(kSmem);
   if (e != cudaSuccess) return e;
   return launch_pdl(kernel, dim3(grid), dim3(d256::kThreads), kSmem, stream, p);
 }

@@ -8,9 +8,8 @@ namespace {
 template <bool CAUSAL, bool BF16>
 cudaError_t launch_one(const FaParams& p, int grid, cudaStream_t stream) {
   constexpr int kSmem = Layout<64>::kSmemBytes;
-  auto kernel = fa_fwd_kernel<64, CAUSAL, BF16, false>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  constexpr auto kernel = fa_fwd_kernel<64, CAUSAL, BF16, false>;
+  cudaError_t e = smem_attribute_once<kernel>(kSmem);
   if (e != cudaSuccess) return e;
   return launch_pdl(kernel, dim3(grid), dim3(kNumThreads), kSmem, stream, p);
 }

@@ -58,9 +58,8 @@ __global__ void __launch_bounds__(256)
 template <bool CAUSAL>
 cudaError_t launch_one(const FaParams& p, int grid, cudaStream_t stream) {
   constexpr int kSmem = Layout<128, true>::kSmemBytes;
-  auto kernel = fa_fwd_kernel<128, CAUSAL, true, false, true>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  constexpr auto kernel = fa_fwd_kernel<128, CAUSAL, true, false, true>;
+  cudaError_t e = smem_attribute_once<kernel>(kSmem);
   if (e != cudaSuccess) return e;
   return launch_pdl(kernel, dim3(grid), dim3(kNumThreads), kSmem, stream, p);
 }

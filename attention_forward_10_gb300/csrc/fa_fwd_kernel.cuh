@@ -31,12 +31,12 @@
 // each tile's softmax runs while the other tile's two MMAs execute.  P_g is
 // handed over in two 64-key halves (one mbarrier each), so the first half of
 // P_g V starts while the softmax still computes the second.  P_g lives
-// in S_g's tensor-memory columns; Q_g K_j^T follows P_g(j-1) V without a
-// completion wait, relying on the tensor pipe running one CTA's MMAs in issue
-// order (each has read its operands before a later one writes its
-// accumulator).  Waiting for the P V commit there instead left the pipe idle
-// for the commit's round trip twice per step (5% at N = 2048); repeated
-// full-size runs are checked to be bit-identical.
+// in S_g's tensor-memory columns, so Q_g K_j^T overwrites the A operand of
+// P_g(j-1) V.  The PTX ISA orders two tcgen05.mma of one thread only when
+// they share the accumulator and shape (its list of implicitly pipelined
+// tcgen05 instruction pairs); these two have different accumulators (O_g,
+// S_g), so the issuer waits for the commit of the last P_g V (barrier
+// ODone_g) before it issues Q_g K_j^T.
 //
 // K/V stream.  K(j) and V(j) go to ring slots 2(j % h) and 2(j % h) + 1
 // (h = STAGES / 2).  One "full" barrier per step, B(j), completes when the
@@ -84,7 +84,7 @@ namespace fa {
 constexpr int kNumThreads = 384;
 constexpr uint32_t kSoftmaxRegs = 216;  // per thread, warpgroups 0 and 1
 constexpr uint32_t kControlRegs = 72;   // per thread, warpgroup 2
-// Launch budget: 384 threads x 168 registers; 2*128*216 + 128*56 fits in it.
+// Launch budget: 384 threads x 168 registers; 2*128*216 + 128*72 fits in it.
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kNumThreads * 168,
               "register split exceeds the launch budget");
 constexpr int kProducerWarp = 8;
@@ -193,9 +193,18 @@ __device__ __forceinline__ Unit decode_unit(int u, const FaParams& p) {
     if (r0 >= len || (single >= 0 && g == 1)) {
       w.n0[g] = w.n1[g] = 0;
     } else {
-      key_tile_range(r0, min(len, r0 + kBlockM), len, p.win_left, p.win_right, kBlockN,
-                     &w.n0[g], &w.n1[g]);
-      if (p.num_splits > 1) clip_to_split(split, p.split_tiles, &w.n0[g], &w.n1[g]);
+      // rows r0 .. sit at key positions r0 + k_off .. (bottom-right alignment)
+      key_tile_range(r0 + w.sv.k_off, min(len, r0 + kBlockM) + w.sv.k_off, w.sv.k_len,
+                     p.win_left, p.win_right, kBlockN, &w.n0[g], &w.n1[g]);
+      if (p.num_splits > 1) {
+        clip_to_split(split, p.split_tiles, &w.n0[g], &w.n1[g]);
+      } else if (w.n1[g] == w.n0[g]) {
+        // no row of the tile has a key (fewer keys than queries, or a
+        // window past the keys): one fully masked key tile gives its rows
+        // O = 0 and LSE = -inf through the ordinary path
+        w.n0[g] = 0;
+        w.n1[g] = 1;
+      }
     }
     if (w.n1[g] > w.n0[g]) {
       w.n_beg = min(w.n_beg, w.n0[g]);
@@ -400,7 +409,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                           w.sv.kv_head);
             else
               tma_load_4d(sbase + L::kKVOff + slot * L::kTileBytes, kv ? &p.tm_v : &p.tm_k,
-                          sb, 0, w.sv.row_base + n * kBlockN, 0, w.sv.kv_head);
+                          sb, 0, w.sv.k_row_base + n * kBlockN, 0, w.sv.kv_head);
             ++kv_it;
           }
         }
@@ -409,10 +418,20 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       const uint32_t steps = kv_it / 2;  // K/V steps with both tiles issued
       if (kv_it > 0) {
         // The stream's last V(steps - 1) completes B(steps) alone: arm it
-        // (an odd count means K(steps) went out, and armed it, last).  B's
-        // previous phase, B(steps - h), completed before V(steps - 1) could
-        // be issued into its released slot.
-        if (kv_it % 2 == 0) mbar_arrive_expect_tx(bar(L::kKVFull + steps % h), L::kTileBytes);
+        // (an odd count means K(steps) went out, and armed it, last).  A
+        // parity wait cannot tell a phase from the one two later, so B(steps)
+        // may only complete once the MMA issuer has waited for the object's
+        // previous phase, B(steps - h).  For steps > h the release of
+        // V(steps - 1 - h)'s slot, waited for above, came after that wait.
+        // For steps == h, V(h - 1) went into a fresh slot and K(h), which
+        // would otherwise hold B(h) back until slot 0 is released, does not
+        // exist: wait here for the release of step 0, which the issuer
+        // commits after waiting for B(0).
+        if (kv_it % 2 == 0) {
+          bool armed_ok = true;
+          if (steps == h) armed_ok = wait_bar(bar(L::kKVEmpty), 0u, ctl, kSiteProducerKV);
+          if (armed_ok) mbar_arrive_expect_tx(bar(L::kKVFull + steps % h), L::kTileBytes);
+        }
         // Let every copy this warp issued land before the CTA may exit:
         // those of the last h step barriers B(steps + 1 - h) .. B(steps),
         // h distinct objects (an older phase of the same object could not be
@@ -449,6 +468,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       uint32_t slot = 0;  // next K/V ring position
       uint32_t step = 0;             // K/V stream step (for the release groups)
       uint32_t q_par[2] = {0, 0}, p_par[2] = {0, 0}, o_cnt[2] = {0, 0};
+      // P_g V products issued / known complete (ODone_g phases waited for)
+      uint32_t o_seen[2] = {0, 0};
       bool ok = true;
       // Step j of the K/V stream is (unit u, tile n); prev_* describe step
       // j-1, whose P V products are issued in step j.
@@ -510,9 +531,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             tc_commit(bar(L::kODone + g));
             ++o_cnt[g];
           }
-          // ---- S_g = Q_g K_j^T, issued right behind P_g(j-1) V, which
-          //      reads P_g(j-1) from the columns this overwrites
+          // ---- S_g = Q_g K_j^T.  It overwrites the columns every earlier
+          //      P_g V read its A operand from: wait for the latest one's
+          //      commit (the commit tracks all earlier MMAs of this thread).
           if (cur_valid && n >= w.n0[g] && n < w.n1[g]) {
+            if (o_seen[g] != o_cnt[g]) {
+              ok = wait_bar(bar(L::kODone + g), (o_cnt[g] - 1) & 1u, ctl, kSiteMmaO);
+              if (!ok) break;
+              o_seen[g] = o_cnt[g];
+            }
             tc_fence_after_sync();
             const uint64_t a = q_desc0 + g * kSlotStep;
             const uint64_t b = k_desc0 + kslot * kSlotStep;
@@ -586,6 +613,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       float l = 0.f;            // running row sum relative to m_ref
 
       const int len = w.sv.len;
+      const int k_len = w.sv.k_len, k_off = w.sv.k_off;
       const int row_end = min(len, t_row0 + kBlockM);
       for (int n = t_n0; n < t_n1; ++n) {
         ok = wait_bar(bar(L::kSFull + g), s_par, ctl, kSiteSoftmaxS);
@@ -601,14 +629,16 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 #pragma unroll
         for (int c = 0; c < kBlockN; ++c) s[c] = __uint_as_float(sraw[c]);
 
-        // keys row - win_left .. row + win_right, below N
+        // keys pos - win_left .. pos + win_right below k_len, where
+        // pos = row + k_off is the row's key position
         const int kbase = n * kBlockN;
-        const bool need_mask = (kbase + kBlockN > len) ||
-                               (kbase + kBlockN - 1 > t_row0 + p.win_right) ||
-                               (kbase < row_end - 1 - p.win_left);
+        const bool need_mask = (kbase + kBlockN > k_len) ||
+                               (kbase + kBlockN - 1 > t_row0 + k_off + p.win_right) ||
+                               (kbase < row_end - 1 + k_off - p.win_left);
         if (need_mask) {
-          const int hi = min(len - kbase, row + p.win_right + 1 - kbase);  // c < hi
-          const int lo = row - p.win_left - kbase;                         // c >= lo
+          const int pos = row + k_off;
+          const int hi = min(k_len - kbase, pos + p.win_right + 1 - kbase);  // c < hi
+          const int lo = pos - p.win_left - kbase;                           // c >= lo
 #pragma unroll
           for (int c = 0; c < kBlockN; ++c)
             if (c >= hi || c < lo) s[c] = -INFINITY;

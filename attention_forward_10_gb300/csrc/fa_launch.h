@@ -4,11 +4,32 @@
 
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <utility>
 
 #include "fa_params.h"
 
 namespace fa {
+
+unsigned long long current_context_id();
+
+// Raise the dynamic shared-memory limit of `Kernel` to `bytes`, once per
+// device and context (the attribute belongs to the function in one context;
+// setting it before every launch would cost a driver call each time).
+template <auto Kernel>
+cudaError_t smem_attribute_once(int bytes) {
+  constexpr int kDevices = 64;
+  static std::atomic<unsigned long long> done[kDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long ctx = current_context_id();
+  const bool cacheable = ctx != 0 && dev >= 0 && dev < kDevices;
+  if (cacheable && done[dev].load(std::memory_order_acquire) == ctx) return cudaSuccess;
+  e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && cacheable) done[dev].store(ctx, std::memory_order_release);
+  return e;
+}
 
 // Launch `kernel` on `stream` with programmatic stream serialisation: the
 // grid may start launching while the stream's previous kernel finishes (its
@@ -93,9 +114,14 @@ cudaError_t launch_splitkv_combine(const void* o_part, const float* lse_part, vo
                                    float* lse, const CombineArgs& a, bool bf16, int num_sms,
                                    cudaStream_t stream);
 
+// Unique id of the calling thread's current CUDA context (cuCtxGetId), 0 if
+// there is none or it cannot be read.  Ids are never reused within a process.
+unsigned long long current_context_id();
+
 // Device address of the fixed split-KV scratch of the current device `dev`
 // (FA_NOALLOC_SCRATCH_BYTES bytes, 256-byte aligned), looked up on the first
-// call per device; nullptr with the CUDA error in *rc if that fails.
+// call per device and context; nullptr with the CUDA error in *rc if that
+// fails (the runtime's last error is cleared).
 void* noalloc_scratch(int dev, cudaError_t* rc);
 
 // Enqueue the watchdog self-test kernel (one CTA).

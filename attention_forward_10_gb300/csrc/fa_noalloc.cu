@@ -16,7 +16,6 @@
 // not by every user of the library.
 #include <cuda_runtime.h>
 
-#include <atomic>
 #include <mutex>
 
 #include "fa.h"
@@ -31,7 +30,14 @@ namespace fa {
 namespace {
 
 constexpr int kScratchDevices = 64;
-std::atomic<void*> g_scratch_addr[kScratchDevices];
+
+// The scratch address of each device, with the id of the context it was
+// looked up in.
+struct ScratchAddr {
+  void* ptr = nullptr;
+  unsigned long long ctx = 0;
+};
+ScratchAddr g_scratch[kScratchDevices];
 std::mutex g_scratch_mutex;
 
 }  // namespace
@@ -42,16 +48,28 @@ void* noalloc_scratch(int dev, cudaError_t* rc) {
     *rc = cudaErrorInvalidDevice;
     return nullptr;
   }
-  void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
-  if (p != nullptr) return p;
-  // First call on this device (which is current): look the array up.  A
-  // failure is not cached, so a later call tries again.
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  p = g_scratch_addr[dev].load(std::memory_order_relaxed);
-  if (p != nullptr) return p;
+  ScratchAddr& a = g_scratch[dev];
+  // The address is a device address of one context: a call made under
+  // another one (a new primary context after cudaDeviceReset, or a driver
+  // context of the caller's own) looks it up again instead of handing the
+  // kernels an address of a context that may be gone.
+  const unsigned long long ctx = current_context_id();
+  if (a.ptr != nullptr && ctx != 0 && ctx == a.ctx) return a.ptr;
+  // First call on this device and context (which is current): look the
+  // array up.  A failure is not cached, so a later call tries again, and the
+  // runtime's error state is cleared so that it is not reported against an
+  // unrelated later call.
+  void* p = nullptr;
   *rc = cudaGetSymbolAddress(&p, g_fa_noalloc_scratch);
-  if (*rc != cudaSuccess) return nullptr;
-  g_scratch_addr[dev].store(p, std::memory_order_release);
+  if (*rc != cudaSuccess) {
+    cudaGetLastError();
+    a.ptr = nullptr;
+    a.ctx = 0;
+    return nullptr;
+  }
+  a.ptr = p;
+  a.ctx = current_context_id();
   return p;
 }
 

@@ -53,10 +53,19 @@ struct FaParams {  // 64-byte aligned through CUtensorMap
   int split_tiles;   // K/V tiles per key split
   float scale_log2;  // softmax scale * log2(e)
   // Variable-length batches (packed rows; nullptr / 0 otherwise): sequence
-  // b holds rows [cu_seqlens[b], cu_seqlens[b+1]) of the packed [rows][H][d]
-  // tensors; N is then the longest sequence and num_bh = batch * H.
+  // b holds query rows [cu_seqlens[b], cu_seqlens[b+1]) of the packed
+  // [rows][H][d] Q and O and key rows [cu_seqlens_k[b], cu_seqlens_k[b+1])
+  // of the packed K and V (the same array for self-attention); seqused_q /
+  // seqused_k (nullptr: all rows) cut each to its first used rows.  N is
+  // then the longest query sequence, N_k the longest key sequence and
+  // num_bh = batch * H.
   const int* cu_seqlens;
-  int total_rows;    // rows of the packed tensors
+  const int* cu_seqlens_k;
+  const int* seqused_q;
+  const int* seqused_k;
+  int total_rows;    // rows of the packed Q and O
+  int total_rows_k;  // rows of the packed K and V
+  int N_k;           // longest key sequence (N when not packed)
   uint16_t* o_ptr;   // O (packed rows), for the row-by-row store of the last
                      // query tile of a sequence
   float descale_v;   // FP8 kernels: V descale, applied to O in the epilogue
@@ -115,11 +124,17 @@ __device__ __forceinline__ void bwd_sequence(const BwdParams& p, int b, int* row
   }
 }
 
-// Rows of one (b, h) attention problem: its sequence's first packed row, its
-// length, and the head coordinates of its Q, O and K/V in the tensor maps.
+// Rows of one (b, h) attention problem: the first packed row and the length
+// of its queries and of its keys, the head coordinates of its Q, O and K/V
+// in the tensor maps, and the bottom-right alignment of the masks: query i
+// sits at key position i + k_off (flash-attention's causal and local masks
+// shift the query row by seqlen_k - seqlen_q).
 struct SeqView {
-  int row_base;   // 0, or the sequence's first packed row
-  int len;        // N, or the sequence's length (clamped to the buffers)
+  int row_base;   // 0, or the sequence's first packed query row
+  int len;        // N, or the sequence's used query rows (clamped to the buffers)
+  int k_row_base; // 0, or the sequence's first packed key row
+  int k_len;      // N, or the sequence's used key rows (clamped to the buffers)
+  int k_off;      // k_len - len (0 for self-attention)
   int q_head;     // head coordinate of Q (bh, or h when packed)
   int o_head;     // head coordinate of O (out_head, or h when packed)
   int kv_head;    // head coordinate of K and V
@@ -136,23 +151,40 @@ __host__ __device__ inline int kv_head(int bh, int H, int group) {
 // variable-length batches (cu_seqlens set).  For packed batches the
 // offsets are clamped so that a malformed cu_seqlens can only shorten a
 // sequence (to at most N rows), never move a row outside [0, total_rows).
+// First row and used length of sequence b under offsets cu (clamped to
+// [0, total]) and optional used lengths, capped at cap rows.
+__device__ __forceinline__ void packed_rows(const int* cu, const int* used, int b, int total,
+                                            int cap, int* first, int* len) {
+  int r0 = cu[b], r1 = cu[b + 1];
+  r0 = r0 < 0 ? 0 : (r0 > total ? total : r0);
+  r1 = r1 < r0 ? r0 : (r1 > total ? total : r1);
+  int n = r1 - r0;
+  if (used != nullptr) {
+    const int u = used[b];
+    n = u < 0 ? 0 : (u < n ? u : n);
+  }
+  *first = r0;
+  *len = n < cap ? n : cap;
+}
+
 template <bool PACKED>
 __device__ __forceinline__ SeqView seq_view(const FaParams& p, int bh, int out_head) {
   SeqView v;
   if constexpr (!PACKED) {
     v.row_base = 0;
     v.len = p.N;
+    v.k_row_base = 0;
+    v.k_len = p.N;
+    v.k_off = 0;
     v.q_head = bh;
     v.o_head = out_head;
     v.kv_head = kv_head(bh, p.H, p.group);
     return v;
   }
   const int b = bh / p.H, h = bh % p.H;
-  int r0 = p.cu_seqlens[b], r1 = p.cu_seqlens[b + 1];
-  r0 = r0 < 0 ? 0 : (r0 > p.total_rows ? p.total_rows : r0);
-  r1 = r1 < r0 ? r0 : (r1 > p.total_rows ? p.total_rows : r1);
-  v.row_base = r0;
-  v.len = (r1 - r0 < p.N) ? r1 - r0 : p.N;
+  packed_rows(p.cu_seqlens, p.seqused_q, b, p.total_rows, p.N, &v.row_base, &v.len);
+  packed_rows(p.cu_seqlens_k, p.seqused_k, b, p.total_rows_k, p.N_k, &v.k_row_base, &v.k_len);
+  v.k_off = v.k_len - v.len;
   v.q_head = h;
   v.o_head = h;
   v.kv_head = h / p.group;

@@ -34,7 +34,6 @@ import hashlib
 import json
 import math
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -101,21 +100,25 @@ def _kernel_source_hash() -> str:
 
 
 def _profiled_traffic(wl_name: str):
-    """DRAM bytes per launch from the committed ncu summary, if still current.
+    """DRAM bytes per launch of the workload's dominant kernel, from the
+    machine-readable record (``profiles/*.json``) written beside each ncu
+    summary, if it is still current.
 
-    The summary records the kernel-source hash it was captured with; once the
-    kernel changes the figure no longer applies and None is returned.
+    Each record holds the workload name, the kernel-source hash the capture
+    was taken at and ``dram_bytes_per_launch``; once the kernel sources
+    change the figure no longer applies and None is returned.
     """
-    for path in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
-        with open(path) as f:
-            text = f.read()
-        m_w = re.search(r"^workload:\s*(\S+)", text, re.M)
-        m_h = re.search(r"^kernel_source_hash:\s*(\S+)", text, re.M)
-        m_t = re.search(r"^dram_bytes_per_launch:\s*([0-9.eE+]+)", text, re.M)
-        if m_w and m_h and m_t and m_w.group(1) == wl_name:
-            if m_h.group(1) == _kernel_source_hash():
-                return float(m_t.group(1)), os.path.relpath(path, ROOT)
-            return None, os.path.relpath(path, ROOT) + " (stale: kernel changed)"
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.json"))):
+        try:
+            with open(path) as f:
+                rec = json.load(f)
+        except (OSError, ValueError):
+            continue
+        if rec.get("workload") != wl_name or rec.get("dram_bytes_per_launch") is None:
+            continue
+        if rec.get("kernel_source_hash") == _kernel_source_hash():
+            return float(rec["dram_bytes_per_launch"]), os.path.relpath(path, ROOT)
+        return None, os.path.relpath(path, ROOT) + " (stale: kernel sources changed)"
     return None, None
 
 
@@ -306,6 +309,86 @@ def _config(wl, l2_note):
             "input_dtype": wl.dtype, "l2": l2_note, "parallelism": "replicas"}
 
 
+def _time_dense(fa, torch, wl, dev, sampler, budget_s: float = 0.3, warmup: int = 5):
+    """Device time of fa_fwd on a dense workload (inputs resident, rotating
+    over enough copies to exceed twice the L2 when one copy does not), for
+    the per-workload lines that follow the headline."""
+    from workloads import make_qkv
+    q, k, v = make_qkv(wl)
+    set_bytes = 4 * q.numel() * q.element_size() + wl.B * wl.H * wl.N * 4
+    n_sets = max(1, min(8, math.ceil(2.2 * L2_BYTES / set_bytes)))
+    sets = []
+    for i in range(n_sets):
+        qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+        if i > 0:
+            qd, kd, vd = qd.clone(), kd.clone(), vd.clone()
+        sets.append((qd, kd, vd, torch.empty_like(qd),
+                     torch.empty((wl.B, wl.H, wl.N), dtype=torch.float32, device=dev)))
+    stream = torch.cuda.Stream(device=dev)
+    dcode = fa.FA_DTYPE_BF16 if wl.dtype == "bf16" else fa.FA_DTYPE_F16
+
+    def step(i):
+        qd, kd, vd, od, ld = sets[i % n_sets]
+        st_ = fa.fa_fwd(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), od.data_ptr(),
+                        ld.data_ptr(), wl.B, wl.H, wl.N, wl.d, wl.scale, int(wl.causal), dcode,
+                        stream.cuda_stream)
+        if st_ != fa.FA_OK:
+            raise RuntimeError(f"forward failed: {fa.fa_status_string(st_)}")
+
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(warmup):
+        step(i)
+    e0.record(stream)
+    for i in range(3):
+        step(i)
+    e1.record(stream)
+    e1.synchronize()
+    per = max(e0.elapsed_time(e1) / 3, 1e-3)
+    steps = int(min(20000, max(10, budget_s * 1e3 / per)))
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    e0.record(stream)
+    for i in range(steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    st, site = fa.fa_get_device_status(stream.cuda_stream)
+    if st != fa.FA_OK:
+        raise RuntimeError(f"device status {fa.fa_status_string(st)} (site {site})")
+    ms = e0.elapsed_time(e1) / steps
+    del sets
+    return {"ms_per_step": ms, "steps": steps,
+            "tflops": wl.flops / (ms / 1e3) / 1e12,
+            "hbm_gbs": wl.hbm_bytes / (ms / 1e3) / 1e9,
+            "l2": (f"{n_sets} rotating input sets ({n_sets * set_bytes / 2**20:.0f} MiB)"
+                   + (" > L2" if n_sets * set_bytes > L2_BYTES else ", L2-resident")),
+            "clocks": sampler.summary(t0, t1) if sampler else None}
+
+
+def _sweep(fa, torch, dev, indices, peak: float, peak_note: str, gpu_id):
+    """The other dense workloads, each timed on its own after the headline
+    (same process, same GPU): one entry per workload."""
+    from workloads import workload
+    sampler = ClockSampler(gpu_id)
+    time.sleep(0.25)
+    out = []
+    try:
+        for idx in indices:
+            w = workload(idx)
+            r = _time_dense(fa, torch, w, dev, sampler)
+            r.update({"workload": w.name, "describe": w.describe(),
+                      "flops_per_step": w.flops, "hbm_bytes_per_step": w.hbm_bytes,
+                      "frac": r["tflops"] / peak, "peak": peak, "peak_source": peak_note})
+            traffic, src = _profiled_traffic(w.name)
+            r["traffic"] = traffic
+            r["traffic_source"] = src
+            out.append(r)
+    finally:
+        sampler.stop()
+    return out
+
+
 def run_ours(args, wl):
     import torch
     import torch.distributed as dist
@@ -402,23 +485,38 @@ def run_ours(args, wl):
     st, site = fa.fa_get_device_status(handle)
     if st != fa.FA_OK:
         raise RuntimeError(f"device status {fa.fa_status_string(st)} (site {site})")
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(5):
+        step(i)
+    e1.record(stream)
+    e1.synchronize()
+    per_step_ms = max(e0.elapsed_time(e1) / 5, 1e-3)
     if args.steps is None:
         # about two seconds of timed work, so the clock sampler sees the load
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for i in range(5):
-            step(i)
-        e1.record(stream)
-        e1.synchronize()
-        per = max(e0.elapsed_time(e1) / 5, 1e-3)
-        args.steps = int(min(20000, max(20, 2000.0 / per)))
+        args.steps = int(min(20000, max(20, 2000.0 / per_step_ms)))
         args.steps = int(_max_over_ranks(args.steps, dev))
 
     sampler = ClockSampler(_gpu_id_for_smi(torch, dev.index)) if rank == 0 else None
     time.sleep(0.25 if sampler else 0)
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
+    # Soak: at least one second of the same steps, untimed for the metric,
+    # right before the timed region, so that the clock record shows the
+    # GPU under sustained load (a short timed region sees a cold, boosted
+    # GPU); its own rate and clock samples are reported separately.
+    soak_steps = int(min(200000, max(args.steps, math.ceil(args.soak_s / max(per_step_ms, 1e-3)
+                                                          * 1e3))))
+    torch.cuda.synchronize(dev)
+    t_soak0 = time.time()
+    start.record(stream)
+    for i in range(soak_steps):
+        step(i)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    t_soak1 = time.time()
+    soak_ms = start.elapsed_time(end)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
@@ -437,7 +535,14 @@ def run_ours(args, wl):
         raise RuntimeError(f"device status {fa.fa_status_string(st)} (site {site})")
     ms = _max_over_ranks(ms, dev)
     clocks = sampler.summary(t_host0, t_host1) if sampler else None
+    soak = None
     if sampler:
+        soak = {"steps": soak_steps, "seconds": soak_ms / 1e3,
+                "tflops": wl.flops * soak_steps / (soak_ms / 1e3) / 1e12,
+                "ms_per_step": soak_ms / soak_steps,
+                "clocks": sampler.summary(t_soak0, t_soak1),
+                "note": "untimed for the metric: the same steps for >= "
+                        f"{args.soak_s:g} s right before the timed region"}
         sampler.stop()
 
     ms_per_step = ms / args.steps
@@ -456,174 +561,184 @@ def run_ours(args, wl):
         torch.cuda.synchronize(dev)
         plain_ms = start.elapsed_time(end) / args.steps
 
-    # End to end through the public API with host buffers: each step copies
-    # Q, K, V from pinned host memory, runs the forward pass and copies O and
-    # LSE back.  Dense bf16/fp16 workloads make one fa_fwd_host call per step
-    # (the library chunks the heads and overlaps copies with the kernels).
-    # The others (split-KV, packed, FP8) do the same here: the B*H heads are
-    # cut into chunks and the copies of one chunk overlap the kernel of the
-    # previous one (three streams: H2D, compute, D2H); packed (varlen) batches
-    # interleave heads within rows: one chunk.
-    host_api = not (wl.splitkv or wl.varlen or wl.dtype == "fp8")
-    if wl.varlen:
-        rows_e2e, row_shape, l_shape = 1, (total * H * d,), (H * total,)
-    else:
-        rows_e2e, row_shape, l_shape = B * H, (B * H, N, d), (B * H, N)
-    q_h, k_h, v_h = (t.reshape(row_shape).pin_memory() for t in (q, k, v))
-    o_h = torch.empty(row_shape, dtype=torch.bfloat16 if wl.dtype == "fp8" else q.dtype)
-    o_h = o_h.pin_memory()
-    l_h = torch.empty(l_shape, dtype=torch.float32).pin_memory()
-    if wl.varlen:
-        q_h, k_h, v_h, o_h, l_h = (t.unsqueeze(0) for t in (q_h, k_h, v_h, o_h, l_h))
-    n_chunks = max(1, min(8, rows_e2e))
-    bounds = [(c * rows_e2e // n_chunks, (c + 1) * rows_e2e // n_chunks)
-              for c in range(n_chunks)]
-    dq, dk, dv = (sets[0][t].view(q_h.shape) for t in range(3))
-    do_ = sets[0][3].view(o_h.shape)
-    dl = sets[0][4].view(l_h.shape)
-    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    e2e_steps = max(1, min(args.steps, 20))
-
-    def e2e_step():
-        """One step: fork the three streams from the current one, copy chunk c
-        in, run it, copy it out (chunk c + 1's input copy overlapping chunk
-        c's kernel and output copy), join back.  Steps do not overlap."""
-        root = torch.cuda.current_stream(dev)
-        ev0 = torch.cuda.Event()
-        ev0.record(root)
-        for st_ in (s_in, stream, s_out):
-            st_.wait_event(ev0)
-        for (a0, a1) in bounds:
-            with torch.cuda.stream(s_in):
-                for dst, src in ((dq, q_h), (dk, k_h), (dv, v_h)):
-                    dst[a0:a1].copy_(src[a0:a1], non_blocking=True)
-                ev_in = torch.cuda.Event()
-                ev_in.record(s_in)
-            stream.wait_event(ev_in)
-            call(dq[a0].data_ptr(), dk[a0].data_ptr(), dv[a0].data_ptr(),
-                 do_[a0].data_ptr(), dl[a0].data_ptr(), 1, a1 - a0)
-            ev_c = torch.cuda.Event()
-            ev_c.record(stream)
-            with torch.cuda.stream(s_out):
-                s_out.wait_event(ev_c)
-                o_h[a0:a1].copy_(do_[a0:a1], non_blocking=True)
-                l_h[a0:a1].copy_(dl[a0:a1], non_blocking=True)
-        for st_ in (s_in, stream, s_out):
-            ev = torch.cuda.Event()
-            ev.record(st_)
-            root.wait_event(ev)
-
-    if wl.varlen:
-        # Packed batch: chunks of whole sequences (about 8, balanced by
-        # rows).  Each chunk's rows are copied into the same rows of the
-        # full-size device tensors and fa_fwd_varlen runs on its sequences
-        # (cu_seqlens from the chunk's first sequence on, row offsets still
-        # global); the [H][total] LSE, strided per chunk, is copied once at
-        # the end.
-        cu = wl.cu_seqlens()
-        target = max(1, total // 8)
-        groups, b0 = [], 0
-        for b in range(1, B + 1):
-            if cu[b] - cu[b0] >= target or b == B:
-                groups.append((b0, b))
-                b0 = b
-        lens = wl.seqlens()
-        q_v, k_v, v_v = (t.pin_memory() for t in (q, k, v))      # [total, H, d]
-        o_v = torch.empty(q.shape, dtype=q.dtype).pin_memory()
-        l_v = torch.empty((H, total), dtype=torch.float32).pin_memory()
-        dq_v, dk_v, dv_v, do_v, dl_v = sets[0]
-        n_chunks = len(groups)
+    def measure_e2e():
+        # End to end through the public API with host buffers: each step copies
+        # Q, K, V from pinned host memory, runs the forward pass and copies O and
+        # LSE back.  Dense bf16/fp16 workloads make one fa_fwd_host call per step
+        # (the library chunks the heads and overlaps copies with the kernels).
+        # The others (split-KV, packed, FP8) do the same here: the B*H heads are
+        # cut into chunks and the copies of one chunk overlap the kernel of the
+        # previous one (three streams: H2D, compute, D2H); packed (varlen) batches
+        # interleave heads within rows: one chunk.
+        host_api = not (wl.splitkv or wl.varlen or wl.dtype == "fp8")
+        if wl.varlen:
+            rows_e2e, row_shape, l_shape = 1, (total * H * d,), (H * total,)
+        else:
+            rows_e2e, row_shape, l_shape = B * H, (B * H, N, d), (B * H, N)
+        q_h, k_h, v_h = (t.reshape(row_shape).pin_memory() for t in (q, k, v))
+        o_h = torch.empty(row_shape, dtype=torch.bfloat16 if wl.dtype == "fp8" else q.dtype)
+        o_h = o_h.pin_memory()
+        l_h = torch.empty(l_shape, dtype=torch.float32).pin_memory()
+        if wl.varlen:
+            q_h, k_h, v_h, o_h, l_h = (t.unsqueeze(0) for t in (q_h, k_h, v_h, o_h, l_h))
+        n_chunks = max(1, min(8, rows_e2e))
+        bounds = [(c * rows_e2e // n_chunks, (c + 1) * rows_e2e // n_chunks)
+                  for c in range(n_chunks)]
+        dq, dk, dv = (sets[0][t].view(q_h.shape) for t in range(3))
+        do_ = sets[0][3].view(o_h.shape)
+        dl = sets[0][4].view(l_h.shape)
+        s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        e2e_steps = max(1, min(args.steps, 20))
 
         def e2e_step():
-            """One step: fork, per chunk copy in / compute / copy out, join."""
+            """One step: fork the three streams from the current one, copy chunk c
+            in, run it, copy it out (chunk c + 1's input copy overlapping chunk
+            c's kernel and output copy), join back.  Steps do not overlap."""
             root = torch.cuda.current_stream(dev)
             ev0 = torch.cuda.Event()
             ev0.record(root)
             for st_ in (s_in, stream, s_out):
                 st_.wait_event(ev0)
-            for (g0, g1) in groups:
-                r0, r1 = cu[g0], cu[g1]
+            for (a0, a1) in bounds:
                 with torch.cuda.stream(s_in):
-                    for dst, src in ((dq_v, q_v), (dk_v, k_v), (dv_v, v_v)):
-                        dst[r0:r1].copy_(src[r0:r1], non_blocking=True)
+                    for dst, src in ((dq, q_h), (dk, k_h), (dv, v_h)):
+                        dst[a0:a1].copy_(src[a0:a1], non_blocking=True)
                     ev_in = torch.cuda.Event()
                     ev_in.record(s_in)
                 stream.wait_event(ev_in)
-                st_ = fa.fa_fwd_varlen(dq_v.data_ptr(), dk_v.data_ptr(), dv_v.data_ptr(),
-                                       do_v.data_ptr(), dl_v.data_ptr(),
-                                       cu_dev.data_ptr() + 4 * g0, g1 - g0,
-                                       max(lens[g0:g1]), total, H, H, d, wl.scale,
-                                       int(wl.causal), -1, -1, dcode, handle)
-                if st_ != fa.FA_OK:
-                    raise RuntimeError(f"fa_fwd_varlen: {fa.fa_status_string(st_)}")
+                call(dq[a0].data_ptr(), dk[a0].data_ptr(), dv[a0].data_ptr(),
+                     do_[a0].data_ptr(), dl[a0].data_ptr(), 1, a1 - a0)
                 ev_c = torch.cuda.Event()
                 ev_c.record(stream)
                 with torch.cuda.stream(s_out):
                     s_out.wait_event(ev_c)
-                    o_v[r0:r1].copy_(do_v[r0:r1], non_blocking=True)
-            with torch.cuda.stream(s_out):
-                s_out.wait_stream(stream)
-                l_v.copy_(dl_v, non_blocking=True)
+                    o_h[a0:a1].copy_(do_[a0:a1], non_blocking=True)
+                    l_h[a0:a1].copy_(dl[a0:a1], non_blocking=True)
             for st_ in (s_in, stream, s_out):
                 ev = torch.cuda.Event()
                 ev.record(st_)
                 root.wait_event(ev)
 
-    if host_api:
-        H_kv = int(k.shape[1])
-        q_h, k_h, v_h = (t.pin_memory() for t in (q, k, v))
-        o_h = torch.empty(q.shape, dtype=q.dtype).pin_memory()
-        l_h = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
-        st_, ws_bytes = fa.fa_fwd_host_workspace_bytes(B, H, H_kv, N, d, 1)
-        if st_ != fa.FA_OK:
-            raise RuntimeError(f"fa_fwd_host_workspace_bytes: {fa.fa_status_string(st_)}")
-        host_ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
-        n_chunks = None
+        if wl.varlen:
+            # Packed batch: chunks of whole sequences (about 8, balanced by
+            # rows).  Each chunk's rows are copied into the same rows of the
+            # full-size device tensors and fa_fwd_varlen runs on its sequences
+            # (cu_seqlens from the chunk's first sequence on, row offsets still
+            # global); the [H][total] LSE, strided per chunk, is copied once at
+            # the end.
+            cu = wl.cu_seqlens()
+            target = max(1, total // 8)
+            groups, b0 = [], 0
+            for b in range(1, B + 1):
+                if cu[b] - cu[b0] >= target or b == B:
+                    groups.append((b0, b))
+                    b0 = b
+            lens = wl.seqlens()
+            q_v, k_v, v_v = (t.pin_memory() for t in (q, k, v))      # [total, H, d]
+            o_v = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+            l_v = torch.empty((H, total), dtype=torch.float32).pin_memory()
+            dq_v, dk_v, dv_v, do_v, dl_v = sets[0]
+            n_chunks = len(groups)
 
-        def e2e_step():
-            """One step: a single fa_fwd_host call on the current stream."""
-            root = torch.cuda.current_stream(dev)
-            st_ = fa.fa_fwd_host(q_h.data_ptr(), k_h.data_ptr(), v_h.data_ptr(),
-                                 o_h.data_ptr(), l_h.data_ptr(), B, H, H_kv, N, d, wl.scale,
-                                 int(wl.causal), -1, -1, dcode, host_ws.data_ptr(),
-                                 host_ws.numel(), root.cuda_stream)
+            def e2e_step():
+                """One step: fork, per chunk copy in / compute / copy out, join."""
+                root = torch.cuda.current_stream(dev)
+                ev0 = torch.cuda.Event()
+                ev0.record(root)
+                for st_ in (s_in, stream, s_out):
+                    st_.wait_event(ev0)
+                for (g0, g1) in groups:
+                    r0, r1 = cu[g0], cu[g1]
+                    with torch.cuda.stream(s_in):
+                        for dst, src in ((dq_v, q_v), (dk_v, k_v), (dv_v, v_v)):
+                            dst[r0:r1].copy_(src[r0:r1], non_blocking=True)
+                        ev_in = torch.cuda.Event()
+                        ev_in.record(s_in)
+                    stream.wait_event(ev_in)
+                    st_ = fa.fa_fwd_varlen(dq_v.data_ptr(), dk_v.data_ptr(), dv_v.data_ptr(),
+                                           do_v.data_ptr(), dl_v.data_ptr(),
+                                           cu_dev.data_ptr() + 4 * g0, g1 - g0,
+                                           max(lens[g0:g1]), total, H, H, d, wl.scale,
+                                           int(wl.causal), -1, -1, dcode, handle)
+                    if st_ != fa.FA_OK:
+                        raise RuntimeError(f"fa_fwd_varlen: {fa.fa_status_string(st_)}")
+                    ev_c = torch.cuda.Event()
+                    ev_c.record(stream)
+                    with torch.cuda.stream(s_out):
+                        s_out.wait_event(ev_c)
+                        o_v[r0:r1].copy_(do_v[r0:r1], non_blocking=True)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_stream(stream)
+                    l_v.copy_(dl_v, non_blocking=True)
+                for st_ in (s_in, stream, s_out):
+                    ev = torch.cuda.Event()
+                    ev.record(st_)
+                    root.wait_event(ev)
+
+        if host_api:
+            H_kv = int(k.shape[1])
+            q_h, k_h, v_h = (t.pin_memory() for t in (q, k, v))
+            o_h = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+            l_h = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+            st_, ws_bytes = fa.fa_fwd_host_workspace_bytes(B, H, H_kv, N, d, 1)
             if st_ != fa.FA_OK:
-                raise RuntimeError(f"fa_fwd_host: {fa.fa_status_string(st_)}")
+                raise RuntimeError(f"fa_fwd_host_workspace_bytes: {fa.fa_status_string(st_)}")
+            host_ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+            n_chunks = None
 
-    if wl.splitkv:
-        for (a0, a1) in bounds:
-            ensure_workspace(1, a1 - a0)
-    e2e_step()
-    torch.cuda.synchronize(dev)
-    # The step's launches are captured once into a CUDA graph and replayed
-    # (host work per step: one graph launch); if capture is refused, the
-    # steps are issued eagerly.
-    graph = None
-    try:
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            e2e_step()
+            def e2e_step():
+                """One step: a single fa_fwd_host call on the current stream."""
+                root = torch.cuda.current_stream(dev)
+                st_ = fa.fa_fwd_host(q_h.data_ptr(), k_h.data_ptr(), v_h.data_ptr(),
+                                     o_h.data_ptr(), l_h.data_ptr(), B, H, H_kv, N, d, wl.scale,
+                                     int(wl.causal), -1, -1, dcode, host_ws.data_ptr(),
+                                     host_ws.numel(), root.cuda_stream)
+                if st_ != fa.FA_OK:
+                    raise RuntimeError(f"fa_fwd_host: {fa.fa_status_string(st_)}")
+
+        if wl.splitkv:
+            for (a0, a1) in bounds:
+                ensure_workspace(1, a1 - a0)
+        e2e_step()
         torch.cuda.synchronize(dev)
-        graph.replay()
-        torch.cuda.synchronize(dev)
-    except Exception:  # noqa: BLE001 - any capture failure: run eagerly
+        # The step's launches are captured once into a CUDA graph and replayed
+        # (host work per step: one graph launch); if capture is refused, the
+        # steps are issued eagerly.
         graph = None
-        torch.cuda.synchronize(dev)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    root = torch.cuda.current_stream(dev)
-    e0.record(root)
-    for _ in range(e2e_steps):
-        if graph is not None:
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                e2e_step()
+            torch.cuda.synchronize(dev)
             graph.replay()
-        else:
-            e2e_step()
-    # the last D2H copy (joined into the current stream) closes the timed region
-    e1.record(root)
-    torch.cuda.synchronize(dev)
-    e2e_ms = _max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dev)
-    h2d = q_h.numel() * q_h.element_size() + 2 * k_h.numel() * k_h.element_size()
-    d2h = o_h.numel() * o_h.element_size() + H * total * 4
+            torch.cuda.synchronize(dev)
+        except Exception:  # noqa: BLE001 - any capture failure: run eagerly
+            graph = None
+            torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        root = torch.cuda.current_stream(dev)
+        e0.record(root)
+        for _ in range(e2e_steps):
+            if graph is not None:
+                graph.replay()
+            else:
+                e2e_step()
+        # the last D2H copy (joined into the current stream) closes the timed region
+        e1.record(root)
+        torch.cuda.synchronize(dev)
+        e2e_ms = _max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dev)
+        h2d = q_h.numel() * q_h.element_size() + 2 * k_h.numel() * k_h.element_size()
+        d2h = o_h.numel() * o_h.element_size() + H * total * 4
+        return {"value": _whole_job_tflops(world, wl.flops, 1, e2e_ms), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms, "cuda_graph": graph is not None,
+                "api": ("fa_fwd_host (C ABI on host buffers)" if host_api else
+                        f"{n_chunks} chunks of "
+                        f"{'sequences' if wl.varlen else 'heads'}: cudaMemcpyAsync "
+                        f"in/out around the C ABI forward")}
+
+    e2e = measure_e2e() if args.e2e else None
 
     if rank == 0:
         peaks, src = _peaks()
@@ -649,20 +764,19 @@ def run_ours(args, wl):
                          "peak_source": peak_note,
                          "traffic": traffic, "traffic_source": traffic_src,
                          "algorithmic_hbm_bytes": wl.hbm_bytes},
-            "e2e": {"value": _whole_job_tflops(world, wl.flops, 1, e2e_ms), "unit": UNIT,
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "ms_per_step": e2e_ms, "cuda_graph": graph is not None,
-                    "api": ("fa_fwd_host (C ABI on host buffers)" if host_api else
-                            f"{n_chunks} chunks of "
-                            f"{'sequences' if wl.varlen else 'heads'}: cudaMemcpyAsync "
-                            f"in/out around the C ABI forward")},
+            "e2e": e2e,
             "gpu_launches": args.steps * launches_per_call,
             "clocks": clocks,
+            "soak": soak,
         }
         if wl.splitkv:
             line["splitkv"] = {"num_splits": splits_used,
                                "unsplit_fa_fwd_ms_per_step": plain_ms,
                                "unsplit_tflops": wl.flops / (plain_ms / 1e3) / 1e12}
+        if world == 1 and args.sweep and wl.index == 2:
+            # the other dense workloads of the metric, timed after the headline
+            line["workloads"] = _sweep(fa, torch, dev, (1, 3, 4, 5), peak, peak_note,
+                                       _gpu_id_for_smi(torch, dev.index))
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = _cpu_baseline(wl)
         print(json.dumps(line), flush=True)
@@ -782,6 +896,13 @@ def main():
                          "8: FP8)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", dest="sweep", action="store_false",
+                    help="with the default workload, do not time workloads 1, 3, 4 and 5 "
+                         "after it")
+    ap.add_argument("--no-e2e", dest="e2e", action="store_false",
+                    help="skip the end-to-end measurement through host buffers")
+    ap.add_argument("--soak-s", type=float, default=1.0,
+                    help="seconds of untimed identical steps right before the timed region")
     ap.add_argument("--backward", action="store_true",
                     help="time the backward pass (fa_bwd) instead of the forward")
     args = ap.parse_args()

@@ -164,6 +164,62 @@ FA_API int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, f
                          int window_right, int dtype, void* stream);
 
 /*
+ * fa_fwd_varlen_qk -- the variable-length forward with separate query and
+ * key sequences: cross-attention, a prefill continuing a cached prefix, or
+ * decoding a few query rows against a KV cache with spare capacity.
+ *
+ * Source: flash-attention "hopper/mainloop_bwd_sm90_tma_gmma_ws.hpp"
+ * (CollectiveMainloopBwd::Arguments: cu_seqlens_q, cu_seqlens_k,
+ * seqused_k; get_seqlen_q / get_seqlen_k, which take a used length when one
+ * is given and the offset difference otherwise; the causal and local masks
+ * shifted by seqlen_k - seqlen_q) and the variable-length mode of
+ * "hopper/flash_fwd_kernel.h" (rows without a key stored as O = 0,
+ * LSE = -inf: store_zero).
+ *
+ *   q, o          contiguous [total_q][H][d] of `dtype`; lse [H][total_q]
+ *                 float32 or NULL.
+ *   k, v          contiguous [total_k][H_kv][d]; grouped heads as in
+ *                 fa_fwd_ext.
+ *   cu_seqlens_q, cu_seqlens_k
+ *                 device pointers to batch + 1 int32 row offsets each
+ *                 (4-byte aligned): sequence b owns query rows
+ *                 [cu_seqlens_q[b], cu_seqlens_q[b+1]) and key rows
+ *                 [cu_seqlens_k[b], cu_seqlens_k[b+1]).  Passing one array for
+ *                 both (with equal totals) is fa_fwd_varlen.
+ *   seqused_q, seqused_k
+ *                 NULL, or device pointers to batch int32 used lengths: only
+ *                 the first seqused_q[b] query rows and seqused_k[b] key rows
+ *                 of sequence b take part (a cache whose rows past the used
+ *                 length hold anything).  Query rows past the used length are
+ *                 not written.
+ *   batch, max_seqlen_q, max_seqlen_k, total_q, total_k
+ *                 sequence count, the longest used query and key lengths, and
+ *                 the packed row counts.  batch, max_seqlen_q or total_q 0:
+ *                 nothing is done (FA_OK).  max_seqlen_k or total_k 0 is
+ *                 allowed: every query row then has no key.  Negative, or a
+ *                 longest length of 2^30 or more: FA_ERR_INVALID_ARG.
+ *   causal, window_left, window_right
+ *                 bottom-right aligned: query i of a sequence with n_q used
+ *                 queries and n_k used keys sits at key position
+ *                 i + n_k - n_q, so causal keeps keys j <= i + n_k - n_q and
+ *                 the window keeps i + n_k - n_q - window_left <= j <=
+ *                 i + n_k - n_q + window_right (n_q = n_k: fa_fwd_varlen).
+ *                 A query row with no admissible key gets O = 0 and
+ *                 LSE = -inf.
+ * Offsets and used lengths are clamped by the kernels to the packed tensors
+ * and to max_seqlen_q / max_seqlen_k (a malformed array only shortens
+ * sequences).  Tiles read up to 127 rows past a sequence's used rows (masked
+ * out): the packed tensors must hold finite values.  Alignment, ownership,
+ * scale, dtype and error behaviour are those of fa_fwd.
+ */
+FA_API int fa_fwd_varlen_qk(const void* q, const void* k, const void* v, void* o, float* lse,
+                            const int* cu_seqlens_q, const int* cu_seqlens_k,
+                            const int* seqused_q, const int* seqused_k, int batch,
+                            int max_seqlen_q, int max_seqlen_k, int total_q, int total_k,
+                            int H, int H_kv, int d, float scale, int causal, int window_left,
+                            int window_right, int dtype, void* stream);
+
+/*
  * fa_fwd_splitkv -- fa_fwd_ext with the keys of every query row cut into
  * `num_splits` contiguous ranges that run as separate work units, then merged.
  *
@@ -233,13 +289,23 @@ FA_API int fa_splitkv_workspace_bytes(int B, int H, int N, int d, int causal,
  *               enqueued; 0 takes the automatic count, lowered to the largest
  *               count whose partials fit.  A count that resolves to 1 split
  *               is the plain forward (no scratch used).
+ *               S splits take S * B*H*N * (2d + 4) bytes (plus at most 255
+ *               bytes of alignment), so at most
+ *               floor(FA_NOALLOC_SCRATCH_BYTES / (B*H*N * (2d + 4))) fit:
+ *               for example 3 for one head of 32768 rows at d = 128, where
+ *               the automatic count of fa_fwd_splitkv is 13 on a 152-SM
+ *               GB300.  fa_splitkv_workspace_bytes with an explicit count
+ *               tells whether that count fits.
  * Every other argument, layout, alignment rule and error is that of
  * fa_fwd_splitkv.
  *
  * Set-up: the first call on each device looks up that device's scratch
- * address (cudaGetSymbolAddress, which can load the library's device code);
- * make that first call before capturing any stream.  A failed look-up
- * returns FA_ERR_CUDA and is retried by the next call.
+ * address (cudaGetSymbolAddress, which can load the library's device code),
+ * and so does the first call after the device's context changed (a new
+ * primary context after cudaDeviceReset, or a driver context the caller
+ * made current); make that first call before capturing any stream.  A failed
+ * look-up returns FA_ERR_CUDA, clears the runtime's last error and is retried
+ * by the next call.
  *
  * Nothing in the scratch has to start at zero: each call writes every
  * partial it later reads.  All calls on one device share the one scratch, so

@@ -1,0 +1,199 @@
+"""GPU parity of fa_fwd_varlen_qk (separate query and key sequences, used
+lengths, bottom-right aligned masks) against the fp64 oracle's
+attention_varlen_qk, element by element over every used query row.
+
+Tolerances as for the plain forward: max |dO| <= 2e-2, max |dLSE| <= 1e-3 on
+rows with at least one key; rows without a key must come out as exactly
+O = 0 and LSE = -inf; query rows outside every sequence's used rows must
+keep the sentinel values they held before the call.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+O_TOL = 2e-2
+LSE_TOL = 1e-3
+SENTINEL_O = 3.0
+SENTINEL_L = 7.0
+
+
+@pytest.fixture(scope="module")
+def fa():
+    from attention_forward_10_gb300 import build
+    build.build()
+    import attention_forward_10_gb300 as fa_mod
+    fa_mod.fa_set_max_ctas(0)
+    fa_mod.fa_set_wait_timeout_us(2_000_000)
+    return fa_mod
+
+
+def _offsets(lens):
+    return np.concatenate([[0], np.cumsum(lens)]).astype(np.int64).tolist()
+
+
+def _inputs(total_q, total_k, H, H_kv, d, dtype, seed):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn(total_q, H, d, generator=g).to(dtype)
+    k = torch.randn(total_k, H_kv, d, generator=g).to(dtype)
+    v = torch.randn(total_k, H_kv, d, generator=g).to(dtype)
+    return q, k, v
+
+
+def _run(fa, q, k, v, cu_q, cu_k, used_q, used_k, causal, window, scale):
+    dev = "cuda"
+    t32 = lambda x: None if x is None else torch.tensor(x, dtype=torch.int32, device=dev)  # noqa
+    lq = [cu_q[i + 1] - cu_q[i] for i in range(len(cu_q) - 1)]
+    lk = [cu_k[i + 1] - cu_k[i] for i in range(len(cu_k) - 1)]
+    mq = max(used_q) if used_q is not None else max(lq)
+    mk = max(used_k) if used_k is not None else max(lk)
+    out = torch.full(q.shape, SENTINEL_O, dtype=q.dtype, device=dev)
+    lse = torch.full((q.shape[1], q.shape[0]), SENTINEL_L, dtype=torch.float32, device=dev)
+    o, l = fa.fwd_varlen_qk(q.to(dev), k.to(dev), v.to(dev), t32(cu_q), t32(cu_k), mq, mk,
+                            seqused_q=t32(used_q), seqused_k=t32(used_k), scale=scale,
+                            causal=causal, window=window, out=out, lse=lse)
+    torch.cuda.synchronize()
+    st, site = fa.fa_get_device_status(None)
+    assert st == fa.FA_OK, f"device status {fa.fa_status_string(st)} at site {site}"
+    return o.float().cpu().numpy(), l.cpu().numpy()
+
+
+def _check(o, lse, o_ref, l_ref, cu_q, used_q, what):
+    B = len(cu_q) - 1
+    nq = [used_q[b] if used_q is not None else cu_q[b + 1] - cu_q[b] for b in range(B)]
+    rows = np.concatenate([np.arange(cu_q[b], cu_q[b] + nq[b]) for b in range(B)] +
+                          [np.zeros(0, dtype=np.int64)]).astype(np.int64)
+    empty = np.isneginf(l_ref[:, rows])            # [H, rows]: no admissible key
+    lg = lse[:, rows]
+    assert (np.isneginf(lg) == empty).all(), f"{what}: -inf LSE rows differ"
+    og = o[rows].transpose(1, 0, 2)                # [H, rows, d]
+    assert (og[empty] == 0).all(), f"{what}: rows without keys must have O = 0"
+    if (~empty).any():
+        err_l = float(np.abs(lg[~empty] - l_ref[:, rows][~empty]).max())
+        err_o = float(np.abs(og[~empty] - o_ref[rows].transpose(1, 0, 2)[~empty]).max())
+        assert err_o <= O_TOL and err_l <= LSE_TOL, (what, err_o, err_l)
+    rest = np.setdiff1d(np.arange(o.shape[0]), rows)
+    assert (o[rest] == SENTINEL_O).all() and (lse[:, rest] == SENTINEL_L).all(), \
+        f"{what}: rows outside the used sequences were written"
+
+
+CROSS = [
+    # (query lengths, key lengths): cross-attention and decode shapes, a
+    # prefill continuing a cache, fewer keys than queries, an empty query
+    # sequence and a sequence without keys
+    ([5, 1, 17, 0, 9, 300, 130], [12, 40, 17, 6, 3, 1000, 0]),
+    ([1, 1, 1, 1, 64, 16], [2000, 1, 333, 129, 900, 4000]),
+    ([700, 260], [200, 700]),
+]
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+@pytest.mark.parametrize("case", range(len(CROSS)))
+def test_separate_query_and_key_sequences(fa, d, causal, case):
+    lq, lk = CROSS[case]
+    cu_q, cu_k = _offsets(lq), _offsets(lk)
+    q, k, v = _inputs(cu_q[-1] + 3, cu_k[-1] + 5, 4, 2, d, torch.bfloat16, seed=700 + case)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = _run(fa, q, k, v, cu_q, cu_k, None, None, causal, (-1, -1), scale)
+    o_ref, l_ref = oracle.attention_varlen_qk(q, k, v, cu_q, cu_k, scale, causal)
+    _check(o, lse, o_ref, l_ref, cu_q, None, f"case {case} d={d} causal={causal}")
+
+
+@pytest.mark.parametrize("window", [(100, 0), (0, 50), (300, 300)])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16], ids=["bf16", "fp16"])
+def test_windows_bottom_right(fa, window, dtype):
+    lq, lk = [200, 1, 90, 513], [450, 700, 30, 513]
+    cu_q, cu_k = _offsets(lq), _offsets(lk)
+    q, k, v = _inputs(cu_q[-1], cu_k[-1], 2, 2, 128, dtype, seed=710)
+    o, lse = _run(fa, q, k, v, cu_q, cu_k, None, None, False, window, 0.09)
+    o_ref, l_ref = oracle.attention_varlen_qk(q, k, v, cu_q, cu_k, 0.09, False, *window)
+    _check(o, lse, o_ref, l_ref, cu_q, None, f"window={window}")
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+def test_kv_cache_used_lengths(fa, d, causal):
+    """A KV cache with spare capacity: each sequence owns cap_k rows of K/V
+    but only its first used_k take part; queries likewise (rows past used_q
+    keep their sentinel)."""
+    cap_q, cap_k = [8, 64, 3, 200], [1024, 512, 2048, 300]
+    used_q, used_k = [3, 64, 0, 130], [1000, 1, 1500, 300]
+    cu_q, cu_k = _offsets(cap_q), _offsets(cap_k)
+    q, k, v = _inputs(cu_q[-1], cu_k[-1], 8, 1, d, torch.bfloat16, seed=720 + d)
+    # cache rows past the used lengths hold values that would change the
+    # result if they were read into the softmax
+    for b in range(4):
+        k[cu_k[b] + used_k[b]:cu_k[b + 1]] = 30.0
+        v[cu_k[b] + used_k[b]:cu_k[b + 1]] = -50.0
+    scale = 1.0 / math.sqrt(d)
+    o, lse = _run(fa, q, k, v, cu_q, cu_k, used_q, used_k, causal, (-1, -1), scale)
+    o_ref, l_ref = oracle.attention_varlen_qk(q, k, v, cu_q, cu_k, scale, causal,
+                                              seqused_q=used_q, seqused_k=used_k)
+    _check(o, lse, o_ref, l_ref, cu_q, used_q, f"d={d} causal={causal}")
+
+
+def test_decode_gqa_many_heads(fa):
+    """Decode-shaped: a few query rows per sequence against long caches with
+    8 query heads per K/V head."""
+    lq, lk = [1, 4, 16, 64, 2, 33], [8192, 3000, 5000, 8192, 777, 4096]
+    cu_q, cu_k = _offsets(lq), _offsets(lk)
+    q, k, v = _inputs(cu_q[-1], cu_k[-1], 16, 2, 128, torch.bfloat16, seed=730)
+    o, lse = _run(fa, q, k, v, cu_q, cu_k, None, None, True, (-1, -1), 0.088)
+    o_ref, l_ref = oracle.attention_varlen_qk(q, k, v, cu_q, cu_k, 0.088, True)
+    _check(o, lse, o_ref, l_ref, cu_q, None, "decode gqa")
+
+
+def test_no_key_rows_at_all(fa):
+    """total_k = 0: every used query row has no key (O = 0, LSE = -inf)."""
+    dev = "cuda"
+    q = torch.randn(140, 2, 128).to(torch.bfloat16).to(dev)
+    kd = torch.empty(1, 2, 128, dtype=torch.bfloat16, device=dev)
+    cu_q = torch.tensor([0, 5, 140], dtype=torch.int32, device=dev)
+    cu_k = torch.tensor([0, 0, 0], dtype=torch.int32, device=dev)
+    out = torch.full(q.shape, SENTINEL_O, dtype=q.dtype, device=dev)
+    lse = torch.full((2, 140), SENTINEL_L, dtype=torch.float32, device=dev)
+    st = fa.fa_fwd_varlen_qk(q.data_ptr(), kd.data_ptr(), kd.data_ptr(), out.data_ptr(),
+                             lse.data_ptr(), cu_q.data_ptr(), cu_k.data_ptr(), None, None, 2,
+                             135, 0, 140, 0, 2, 2, 128, 0.1, 0, -1, -1, fa.FA_DTYPE_BF16, None)
+    assert st == fa.FA_OK, fa.fa_status_string(st)
+    torch.cuda.synchronize()
+    st, site = fa.fa_get_device_status(None)
+    assert st == fa.FA_OK, (st, site)
+    assert (out == 0).all() and torch.isneginf(lse).all()
+
+
+def test_equal_offsets_match_the_self_attention_call_bit_for_bit(fa):
+    lens = [1, 127, 128, 129, 300, 0, 640]
+    cu = _offsets(lens)
+    q, k, v = _inputs(cu[-1], cu[-1], 4, 2, 128, torch.bfloat16, seed=740)
+    o1, l1 = _run(fa, q, k, v, cu, cu, None, None, True, (-1, -1), 0.1)
+    cu_t = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    o2, l2 = fa.fwd_varlen(q.cuda(), k.cuda(), v.cuda(), cu_t, max(lens), scale=0.1, causal=True)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(o1, o2.float().cpu().numpy())
+    np.testing.assert_array_equal(l1, l2.cpu().numpy())
+
+
+def test_argument_errors(fa):
+    z = torch.zeros(16, 1, 128, dtype=torch.bfloat16, device="cuda")
+    cu = torch.tensor([0, 16], dtype=torch.int32, device="cuda")
+    args = dict(q=z.data_ptr(), k=z.data_ptr(), v=z.data_ptr(), o=z.data_ptr(), lse=None,
+                cu_seqlens_q=cu.data_ptr(), cu_seqlens_k=cu.data_ptr(), seqused_q=None,
+                seqused_k=None, batch=1, max_seqlen_q=16, max_seqlen_k=16, total_q=16,
+                total_k=16, H=1, H_kv=1, d=128, scale=0.1, causal=0, window_left=-1,
+                window_right=-1, dtype=fa.FA_DTYPE_BF16, stream=None)
+    for key, val, want in (("total_k", -1, fa.FA_ERR_INVALID_ARG),
+                           ("max_seqlen_k", -1, fa.FA_ERR_INVALID_ARG),
+                           ("max_seqlen_k", 1 << 30, fa.FA_ERR_INVALID_ARG),
+                           ("cu_seqlens_k", None, fa.FA_ERR_INVALID_ARG),
+                           ("seqused_k", cu.data_ptr() + 2, fa.FA_ERR_MISALIGNED),
+                           ("d", 96, fa.FA_ERR_UNSUPPORTED)):
+        bad = dict(args, **{key: val})
+        assert fa.fa_fwd_varlen_qk(*bad.values()) == want, key
+    torch.cuda.synchronize()

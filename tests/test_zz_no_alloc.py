@@ -3,15 +3,22 @@ partials in the library's fixed per-device scratch instead of a caller
 workspace.
 
 Each case calls it through the C ABI twice in a row on the same inputs and
-compares both results with the existing entry points: within the parity
-tolerances (max |dO| <= 2e-2, max |dLSE| <= 1e-3) of the unsplit fa_fwd_ext,
-and bit for bit with fa_fwd_splitkv run with the same split count on a
-torch-allocated workspace.  The file sorts last so that it also runs after
-every other test in one session; it depends on no state they leave.
+compares both results with the fp64 oracle and with the existing entry
+points: within the parity tolerances (max |dO| <= 2e-2, max |dLSE| <= 1e-3)
+of the oracle (every row, or 512 seeded rows plus the edge rows of the
+long case) and of the unsplit fa_fwd_ext, and bit for bit with
+fa_fwd_splitkv run with the same split count on a torch-allocated
+workspace.  For the automatic count the case is one where the planned
+count does not fit the scratch, and the comparison is with fa_fwd_splitkv
+at the count the library must lower it to.  The file sorts last so that it
+also runs after every other test in one session; it depends on no state
+they leave.
 """
+import numpy as np
 import pytest
 import torch
 
+import oracle
 from workloads import make_random_qkv
 
 pytestmark = pytest.mark.gpu
@@ -88,6 +95,47 @@ CASES = [
 ]
 
 
+def _oracle_check(q, k, v, scale, causal, window, results):
+    """Both results against the fp64 oracle: every row of the small cases,
+    512 seeded rows plus the edge rows of the long one."""
+    B, H, N, _ = q.shape
+    qc, kc, vc = q.cpu(), k.cpu(), v.cpu()
+    if N <= 4096:
+        o_ref, l_ref = oracle.attention_ex(qc, kc, vc, scale, causal, *window)
+        pick = lambda o, lse: (o.float().cpu().numpy(), lse.cpu().numpy())
+    else:
+        g = torch.Generator().manual_seed(520)
+        rows = {(b, h, i) for b in range(B) for h in range(H)
+                for i in (0, 1, 127, 128, N // 2, N - 2, N - 1)}
+        rows |= {(int(torch.randint(B, (1,), generator=g)), int(torch.randint(H, (1,), generator=g)),
+                  int(torch.randint(N, (1,), generator=g))) for _ in range(512)}
+        rows = sorted(rows)
+        o_ref, l_ref = oracle.attention_rows_ex(qc, kc, vc, scale, causal, rows, *window)
+        idx = tuple(np.array(rows).T)
+        pick = lambda o, lse: (o.float().cpu().numpy()[idx], lse.cpu().numpy()[idx])
+    for o, lse in results:
+        o_np, l_np = pick(o, lse)
+        err_o = float(np.abs(o_np - o_ref).max())
+        err_l = float(np.abs(l_np - l_ref).max())
+        assert err_o <= O_TOL and err_l <= LSE_TOL, ("oracle", err_o, err_l)
+
+
+def _lowered_count(fa, B, H, N, d, causal, window):
+    """The automatic split count and the count fa_fwd_splitkv_noalloc must
+    lower it to: the largest count (as resolved by the planner) whose
+    partials fit the scratch."""
+    st, auto_bytes = fa.fa_splitkv_workspace_bytes(B, H, N, d, int(causal), *window, 0)
+    assert st == fa.FA_OK
+    per_split = B * H * N * (2 * d + 4)
+    auto = auto_bytes // per_split
+    for want in range(auto, 0, -1):
+        st, need = fa.fa_splitkv_workspace_bytes(B, H, N, d, int(causal), *window, want)
+        assert st == fa.FA_OK
+        if need <= fa.FA_NOALLOC_SCRATCH_BYTES:
+            return auto_bytes, want
+    return auto_bytes, 1
+
+
 @pytest.mark.parametrize("case", CASES, ids=[f"N{c[3]}_d{c[4]}_S{c[8]}" for c in CASES])
 def test_noalloc_twice_matches_existing_entry_points(fa, case):
     B, H, H_kv, N, d, dtype, causal, window, S = case
@@ -106,11 +154,17 @@ def test_noalloc_twice_matches_existing_entry_points(fa, case):
         err_l = (lse - l_ref).abs().max().item()
         assert err_o <= O_TOL and err_l <= LSE_TOL, (err_o, err_l)
     assert torch.equal(first[0], second[0]) and torch.equal(first[1], second[1])
-    if S > 0:
-        o_w, l_w, need = _with_workspace(fa, q, k, v, scale, causal, window, S)
-        _sync_ok(fa)
-        assert 0 < need <= fa.FA_NOALLOC_SCRATCH_BYTES
-        assert torch.equal(first[0], o_w) and torch.equal(first[1], l_w)
+    _oracle_check(q, k, v, scale, causal, window, (first, second))
+    explicit = S
+    if S == 0:
+        # the planned count must not fit, so that the lowering really ran
+        auto_bytes, explicit = _lowered_count(fa, B, H, N, d, causal, window)
+        assert auto_bytes > fa.FA_NOALLOC_SCRATCH_BYTES, auto_bytes
+        assert explicit > 1
+    o_w, l_w, need = _with_workspace(fa, q, k, v, scale, causal, window, explicit)
+    _sync_ok(fa)
+    assert 0 < need <= fa.FA_NOALLOC_SCRATCH_BYTES
+    assert torch.equal(first[0], o_w) and torch.equal(first[1], l_w)
 
 
 def test_noalloc_beyond_the_scratch_is_rejected_untouched(fa):
