@@ -63,6 +63,7 @@ SIGNATURES = {
     "fa_get_device_status": ([_vp, ctypes.POINTER(_i)], _i),
     "fa_set_wait_timeout_us": ([_ll], _i),
     "fa_set_max_ctas": ([_i], _i),
+    "fa_set_gqa_pack": ([_i], _i),
     "fa_selftest_watchdog": ([_ll, _vp], _i),
     "fa_num_sms": ([], _i),
 }
@@ -240,6 +241,10 @@ def fa_set_wait_timeout_us(timeout_us: int) -> int:
 
 def fa_set_max_ctas(max_ctas: int) -> int:
     return int(_lib.fa_set_max_ctas(int(max_ctas)))
+
+
+def fa_set_gqa_pack(enable: int) -> int:
+    return int(_lib.fa_set_gqa_pack(enable))
 
 
 def fa_selftest_watchdog(timeout_us: int, stream: int | None = None) -> int:

@@ -67,6 +67,7 @@ constexpr int kMaxDevices = 64;
 
 std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
 std::atomic<int> g_max_ctas{0};
+std::atomic<int> g_gqa_pack{1};
 
 struct DeviceInfo {
   std::once_flag once;
@@ -209,6 +210,32 @@ bool encode_packed_map(CUtensorMap* map, const void* base, int rows, int heads, 
   return r == CUDA_SUCCESS;
 }
 
+// 5-D view of a packed [rows][H][d] 16-bit tensor whose query heads come in
+// groups of `g` (grouped-query packing): dim0 = 64 elements, dim1 = the g
+// heads of a group (stride d*2 B), dim2 = rows (stride H*d*2 B), dim3 = d/64
+// column blocks (stride 128 B), dim4 = groups (stride g*d*2 B).  The box {64,
+// g, 128/g, d/64, 1} lands in shared memory as [d/64][128/g rows][g][64]:
+// the [blocks][tile rows][64] order of the 4-D views, tile row = row * g +
+// head.
+bool encode_packed_gqa_map(CUtensorMap* map, const void* base, int rows, int H, int g, int d,
+                           bool bf16) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t hd = static_cast<cuuint64_t>(d) * 2;
+  cuuint64_t dims[5] = {64, static_cast<cuuint64_t>(g), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(d / 64), static_cast<cuuint64_t>(H / g)};
+  cuuint64_t strides[4] = {hd, static_cast<cuuint64_t>(H) * hd, 128,
+                           static_cast<cuuint64_t>(g) * hd};
+  cuuint32_t box[5] = {64, static_cast<cuuint32_t>(g), static_cast<cuuint32_t>(kBlockM / g),
+                       static_cast<cuuint32_t>(d / 64), 1};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                  5, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // 4-D byte view for the FP8 kernel's 128-byte-row tiles: dim0 = 128 bytes
 // (innermost), dim1 = rows (stride row_stride), dim2 = 128-byte blocks
 // (stride 128), dim3 = heads (stride head_stride); box {128, box_rows, 1, 1}.
@@ -259,6 +286,12 @@ int fa_set_wait_timeout_us(long long timeout_us) {
 int fa_set_max_ctas(int max_ctas) {
   if (max_ctas < 0) return FA_ERR_INVALID_ARG;
   fa::g_max_ctas.store(max_ctas);
+  return FA_OK;
+}
+
+int fa_set_gqa_pack(int enable) {
+  if (enable != 0 && enable != 1) return FA_ERR_INVALID_ARG;
+  fa::g_gqa_pack.store(enable);
   return FA_OK;
 }
 
@@ -342,11 +375,31 @@ long long units_per_head(int N, int d) {
   return (static_cast<long long>(N) + rows - 1) / rows;
 }
 
+// log2 of the query heads packed per tile row group for this call (0: no
+// grouped-query packing).  Packed batches with d <= 128 whose query heads
+// share K/V heads in groups of 2..16 (a power of two) pack a group's heads
+// into each tile, so a group streams its K/V once and short query
+// sequences (decoding) still fill the 128 tile rows.
+int gqa_pack_log2(const ForwardCall& c) {
+  if (c.cu_seqlens == nullptr || c.fp8 || c.d > 128 || g_gqa_pack.load() == 0) return 0;
+  const int g = c.H / c.H_kv;
+  if (g < 2 || g > 16 || (g & (g - 1)) != 0) return 0;
+  int lg = 0;
+  while ((1 << lg) < g) ++lg;
+  return lg;
+}
+
 int launch_forward(const ForwardCall& c, void* o_out, float* lse_out, int num_splits,
                    int split_tiles) {
   using namespace fa;
-  const long long bh = static_cast<long long>(c.B) * c.H;
-  const long long pairs = units_per_head(c.N, c.d);
+  const int gqa_log2 = gqa_pack_log2(c);
+  // (grouped-query packing: problems are (sequence, K/V head) pairs whose
+  // rows are positions x heads of the group)
+  const long long bh = static_cast<long long>(c.B) * (c.H >> gqa_log2);
+  const long long pairs = units_per_head(static_cast<int>(std::min<long long>(
+                                             static_cast<long long>(c.N) << gqa_log2,
+                                             (1ll << 31) - 1)),
+                                         c.d);
   // (headroom: the last-wave split below may add up to one wave of units)
   if (bh >= (1ll << 31) || bh * pairs * num_splits + 4096 >= (1ll << 31))
     return FA_ERR_INVALID_ARG;
@@ -383,10 +436,16 @@ int launch_forward(const ForwardCall& c, void* o_out, float* lse_out, int num_sp
     const void* kb = no_keys ? c.q : c.k;
     const void* vb = no_keys ? c.q : c.v;
     const int k_rows = no_keys ? c.total : c.total_k;
-    if (!encode_packed_map(&p.tm_q, c.q, c.total, c.H, d, bf16, kBlockM, d / 64) ||
+    const bool q_ok =
+        gqa_log2 ? encode_packed_gqa_map(&p.tm_q, c.q, c.total, c.H, 1 << gqa_log2, d, bf16) &&
+                       encode_packed_gqa_map(&p.tm_o, o_out, c.total, c.H, 1 << gqa_log2, d,
+                                             bf16)
+                 : encode_packed_map(&p.tm_q, c.q, c.total, c.H, d, bf16, kBlockM, d / 64) &&
+                       encode_packed_map(&p.tm_o, o_out, c.total, c.H, d, bf16, kBlockM,
+                                         o_blocks);
+    if (!q_ok ||
         !encode_packed_map(&p.tm_k, kb, k_rows, c.H_kv, d, bf16, kv_rows, d / 64) ||
-        !encode_packed_map(&p.tm_v, vb, k_rows, c.H_kv, d, bf16, kv_rows, d / 64) ||
-        !encode_packed_map(&p.tm_o, o_out, c.total, c.H, d, bf16, kBlockM, o_blocks))
+        !encode_packed_map(&p.tm_v, vb, k_rows, c.H_kv, d, bf16, kv_rows, d / 64))
       return FA_ERR_CUDA;
   } else if (!encode_qkvo_map(&p.tm_q, c.q, N, d, ibh, bf16, kBlockM, d / 64) ||
              !encode_qkvo_map(&p.tm_k, c.k, N, d, ibh_kv, bf16, kv_rows, d / 64) ||
@@ -402,6 +461,7 @@ int launch_forward(const ForwardCall& c, void* o_out, float* lse_out, int num_sp
   p.total_rows_k = packed ? (c.cu_seqlens_k != nullptr ? c.total_k : c.total) : 0;
   const int N_k = (packed && c.cu_seqlens_k != nullptr) ? c.N_k : N;
   p.N_k = N_k;
+  p.gqa_log2 = gqa_log2;
   p.o_ptr = static_cast<uint16_t*>(o_out);
   p.lse = lse_out;
   p.status = info->status;

@@ -433,7 +433,31 @@ __global__ void __launch_bounds__(d256::kThreads, 1)
       if (!ok) break;
       tc_fence_after_sync();
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-      for (int half = 0; half < 2 && ok; ++half) {
+      if (PACKED && len - w.row0 < kBlockM) {
+        // the last tile of a packed sequence, whose 128-row TMA box would
+        // run into the next sequence's rows: each thread stores its own row
+        // (16-byte stores); no staging, no store warp
+#pragma unroll 1
+        for (int c = 0; c < 256; c += 32) {
+          uint32_t o[32];
+          tmem_ld_x32_sync(tO + c, o);
+          if (row < len) {
+            uint4* dst = reinterpret_cast<uint4*>(
+                p.o_ptr + ((static_cast<long long>(w.sv.row_base) + row) * p.H + w.sv.o_head) *
+                              256 + c);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              uint32_t w4[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                w4[e] = pack2<BF16>(__uint_as_float(o[8 * j + 2 * e]) * inv_l,
+                                    __uint_as_float(o[8 * j + 2 * e + 1]) * inv_l);
+              dst[j] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
+          }
+        }
+      }
+      for (int half = 0; half < 2 && ok && !(PACKED && len - w.row0 < kBlockM); ++half) {
         // the staging tile must have been read by the store before this one
         ok = wait_bar(bar(kStageEmpty), (n_stores - 1) & 1u, ctl, kSiteEpilogueO);
         ok = __all_sync(0xffffffffu, ok);
@@ -467,37 +491,25 @@ __global__ void __launch_bounds__(d256::kThreads, 1)
     __syncwarp();
   } else if (warp == kStoreWarp) {
     // ------------------------------------------------------------ O store
-    // Lane 0 waits and issues the TMA stores; the last query tile of a
-    // packed sequence, whose 128-row box would run into the next sequence's
-    // rows, is copied row by row by the whole warp instead.
+    // Lane 0 waits and issues the TMA stores of the two staged halves of
+    // each tile (the partial last tiles of packed sequences are stored by
+    // the softmax threads).
     uint32_t full_par = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+    for (int u = blockIdx.x; u < p.num_units && ok && lane == 0; u += gridDim.x) {
       const Unit w = decode_unit<CAUSAL, PACKED>(u, p);
       if (w.n1 == w.n0) continue;
-      const int rows = w.sv.len - w.row0;
+      if (PACKED && w.sv.len - w.row0 < kBlockM) continue;
       for (int half = 0; half < 2 && ok; ++half) {
-        if (lane == 0) ok = wait_bar(bar(kStageFull), full_par, ctl, kSiteStore);
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        ok = wait_bar(bar(kStageFull), full_par, ctl, kSiteStore);
         full_par ^= 1u;
         if (!ok) break;
-        if (PACKED && rows < kBlockM) {
-          const long long row_stride = static_cast<long long>(p.H) * 256;
-          uint16_t* dst = p.o_ptr + (static_cast<long long>(w.sv.row_base) + w.row0) *
-                                        row_stride + static_cast<long long>(w.sv.o_head) * 256 +
-                          half * 128;
-          copy_staged_rows(sbase + kStageOff, rows, 16, dst, row_stride, lane);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(kStageEmpty));
-        } else if (lane == 0) {
-          // columns [128*half, 128*half + 128) = d blocks 2*half, 2*half + 1
-          tma_store_4d(&p.tm_o, sbase + kStageOff, 0, w.sv.row_base + w.row0, 2 * half,
-                       w.sv.o_head);
-          bulk_commit_group();
-          bulk_wait_read_all();
-          mbar_arrive(bar(kStageEmpty));
-        }
-        __syncwarp();
+        // columns [128*half, 128*half + 128) = d blocks 2*half, 2*half + 1
+        tma_store_4d(&p.tm_o, sbase + kStageOff, 0, w.sv.row_base + w.row0, 2 * half,
+                     w.sv.o_head);
+        bulk_commit_group();
+        bulk_wait_read_all();
+        mbar_arrive(bar(kStageEmpty));
       }
     }
     if (lane == 0) bulk_wait_all();

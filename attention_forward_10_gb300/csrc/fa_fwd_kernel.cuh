@@ -176,10 +176,14 @@ __device__ __forceinline__ Unit decode_unit(int u, const FaParams& p) {
   }
   w.sv = seq_view<PACKED>(p, w.bh, split * p.num_bh + w.bh);
   const int len = w.sv.len;
+  // query positions per tile and per unit (fewer with grouped-query packing,
+  // where a tile row is a (position, head) pair)
+  const int pk = PACKED ? p.gqa_log2 : 0;
+  const int tile_pos = kBlockM >> pk, unit_pos = kRowsPerUnit >> pk;
   if (PACKED && CAUSAL) {
     // sequences differ in length: count the pairs from each sequence's end,
     // so that every sequence's heaviest (last) pairs come first
-    pair = (len + kRowsPerUnit - 1) / kRowsPerUnit - 1 - (p.num_pairs - 1 - pair);
+    pair = (len + unit_pos - 1) / unit_pos - 1 - (p.num_pairs - 1 - pair);
     if (pair < 0) pair = p.num_pairs;  // no such pair: an empty unit
   }
   w.n_beg = 0x7fffffff;
@@ -187,14 +191,15 @@ __device__ __forceinline__ Unit decode_unit(int u, const FaParams& p) {
 #pragma unroll
   for (int g = 0; g < 2; ++g) {
     // a single-tile unit carries its tile in slot 0
-    const int r0 = (single < 0) ? pair * kRowsPerUnit + g * kBlockM
-                                : pair * kRowsPerUnit + single * kBlockM;
+    const int r0 = (single < 0) ? pair * unit_pos + g * tile_pos
+                                : pair * unit_pos + single * tile_pos;
     w.row0[g] = r0;
     if (r0 >= len || (single >= 0 && g == 1)) {
       w.n0[g] = w.n1[g] = 0;
     } else {
-      // rows r0 .. sit at key positions r0 + k_off .. (bottom-right alignment)
-      key_tile_range(r0 + w.sv.k_off, min(len, r0 + kBlockM) + w.sv.k_off, w.sv.k_len,
+      // positions r0 .. sit at key positions r0 + k_off .. (bottom-right
+      // alignment)
+      key_tile_range(r0 + w.sv.k_off, min(len, r0 + tile_pos) + w.sv.k_off, w.sv.k_len,
                      p.win_left, p.win_right, kBlockN, &w.n0[g], &w.n1[g]);
       if (p.num_splits > 1) {
         clip_to_split(split, p.split_tiles, &w.n0[g], &w.n1[g]);
@@ -213,6 +218,16 @@ __device__ __forceinline__ Unit decode_unit(int u, const FaParams& p) {
   }
   if (w.n_end == 0) w.n_beg = 0;  // nothing to stream
   return w;
+}
+
+// Whether tile g of unit w goes through the staging tile and a TMA store:
+// every tile with keys, except (packed batches) a sequence's partial last
+// tile, which the softmax threads store row by row.
+template <bool PACKED>
+__device__ __forceinline__ bool staged_tile(const FaParams& p, const Unit& w, int g) {
+  const bool valid = g ? (w.n1[1] > w.n0[1]) : (w.n1[0] > w.n0[0]);
+  if (!PACKED) return valid;
+  return valid && (w.sv.len - (g ? w.row0[1] : w.row0[0]) >= (kBlockM >> p.gqa_log2));
 }
 
 // Maximum of a row of scores: four independent chains.
@@ -368,8 +383,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           ok = wait_bar(bar(L::kQEmpty + g), (q_it[g] & 1u) ^ 1u, ctl, kSiteProducerQ);
           if (!ok) break;
           mbar_arrive_expect_tx(bar(L::kQFull + g), L::kTileBytes);
-          tma_load_4d(sbase + L::kQOff + g * L::kTileBytes, &p.tm_q, bar(L::kQFull + g), 0,
-                      w.sv.row_base + w.row0[g], 0, w.sv.q_head);
+          if (PACKED && p.gqa_log2)  // {64, heads of the group, positions, d/64, K/V head}
+            tma_load_5d(sbase + L::kQOff + g * L::kTileBytes, &p.tm_q, bar(L::kQFull + g), 0, 0,
+                        w.sv.row_base + w.row0[g], 0, w.sv.kv_head);
+          else
+            tma_load_4d(sbase + L::kQOff + g * L::kTileBytes, &p.tm_q, bar(L::kQFull + g), 0,
+                        w.sv.row_base + w.row0[g], 0, w.sv.q_head);
           ++q_it[g];
         }
         for (int n = w.n_beg; n < w.n_end && ok; ++n) {
@@ -599,22 +618,27 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
     for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
       const Unit w = decode_unit<CAUSAL, PACKED>(u, p);
-      // the staging tile is used by tile 0 then tile 1 of each unit
-      const bool valid0 = w.n1[0] > w.n0[0], valid1 = w.n1[1] > w.n0[1];
-      const uint32_t my_store = n_stores + ((g == 1 && valid0) ? 1u : 0u);
-      n_stores += (valid0 ? 1u : 0u) + (valid1 ? 1u : 0u);
+      // the staging tile is used by tile 0 then tile 1 of each unit (the
+      // partial last tiles of packed sequences are written directly)
+      const bool staged0 = staged_tile<PACKED>(p, w, 0), staged1 = staged_tile<PACKED>(p, w, 1);
+      const uint32_t my_store = n_stores + ((g == 1 && staged0) ? 1u : 0u);
+      n_stores += (staged0 ? 1u : 0u) + (staged1 ? 1u : 0u);
       // this warpgroup's tile (g is per warp: selects, not indexed loads)
       const int t_n0 = g ? w.n0[1] : w.n0[0];
       const int t_n1 = g ? w.n1[1] : w.n1[0];
       const int t_row0 = g ? w.row0[1] : w.row0[0];
       if (t_n1 == t_n0) continue;
-      const int row = t_row0 + t;
+      // this thread's query position and output head (with grouped-query
+      // packing, tile row t is head t % group of position t / group)
+      const int gq = PACKED ? p.gqa_log2 : 0;
+      const int row = t_row0 + (t >> gq);
+      const int o_head = w.sv.o_head + (t & ((1 << gq) - 1));
       float m_ref = -INFINITY;  // reference maximum (log2 units, scaled)
       float l = 0.f;            // running row sum relative to m_ref
 
       const int len = w.sv.len;
       const int k_len = w.sv.k_len, k_off = w.sv.k_off;
-      const int row_end = min(len, t_row0 + kBlockM);
+      const int row_end = min(len, t_row0 + (kBlockM >> gq));
       for (int n = t_n0; n < t_n1; ++n) {
         ok = wait_bar(bar(L::kSFull + g), s_par, ctl, kSiteSoftmaxS);
         s_par ^= 1u;
@@ -718,6 +742,25 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           pk[e] = pack2<BF16>(__uint_as_float(o[2 * e]) * inv_l,
                               __uint_as_float(o[2 * e + 1]) * inv_l);
       }
+      if (p.lse != nullptr && row < len) {
+        p.lse[(PACKED ? static_cast<long long>(o_head) * p.total_rows + w.sv.row_base
+                      : lse_base<PACKED>(p, w.sv)) + row] =
+            (l > 0.f) ? (m_ref + log2f(l) - (FP8 ? kFp8POffset : 0.f)) * 0.6931471805599453f
+                      : -INFINITY;
+      }
+      if (!(g ? staged1 : staged0)) {
+        // the last tile of a packed sequence, whose 128-row TMA box would
+        // run into the next sequence's rows: each thread stores its own row
+        // (16-byte stores); no staging, no store warp
+        if (row < len) {
+          uint4* dst = reinterpret_cast<uint4*>(
+              p.o_ptr + ((static_cast<long long>(w.sv.row_base) + row) * p.H + o_head) * D);
+#pragma unroll
+          for (int c16 = 0; c16 < D / 8; ++c16)
+            dst[c16] = make_uint4(pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
+        }
+        continue;
+      }
       // the staging tile must have been read by the store before this one
       ok = wait_bar(bar(L::kStageEmpty), (my_store - 1) & 1u, ctl, kSiteEpilogueO);
       ok = __all_sync(0xffffffffu, ok);
@@ -728,11 +771,6 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                               (((c16 % 8) ^ (t & 7)) << 4);
         st_shared_v4(addr, pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
       }
-      if (p.lse != nullptr && row < len) {
-        p.lse[lse_base<PACKED>(p, w.sv) + row] =
-            (l > 0.f) ? (m_ref + log2f(l) - (FP8 ? kFp8POffset : 0.f)) * 0.6931471805599453f
-                      : -INFINITY;
-      }
       fence_proxy_async_smem();
       mbar_arrive(bar(L::kStageFull));
     }
@@ -740,38 +778,26 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   } else if (warp == kStoreWarp) {
     regs_decrease<kControlRegs>();
     // ------------------------------------------------------------ O store
-    // Lane 0 waits and issues the TMA store of each staged tile.  The last
-    // query tile of a packed sequence, whose 128-row box would run into the
-    // next sequence's rows, is copied row by row by the whole warp instead.
+    // Lane 0 waits and issues the TMA store of each staged tile (the partial
+    // last tiles of packed sequences are stored by the softmax threads).
     uint32_t full_par = 0;
     bool ok = true;
-    // (lanes other than 0 take part only for packed batches)
-    constexpr bool whole_warp = PACKED;
-    for (int u = blockIdx.x; u < p.num_units && ok && (whole_warp || lane == 0);
-         u += gridDim.x) {
+    for (int u = blockIdx.x; u < p.num_units && ok && lane == 0; u += gridDim.x) {
       const Unit w = decode_unit<CAUSAL, PACKED>(u, p);
       for (int g = 0; g < 2 && ok; ++g) {
-        if (w.n1[g] == w.n0[g]) continue;
-        if (lane == 0) ok = wait_bar(bar(L::kStageFull), full_par, ctl, kSiteStore);
-        if (whole_warp) ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!staged_tile<PACKED>(p, w, g)) continue;
+        ok = wait_bar(bar(L::kStageFull), full_par, ctl, kSiteStore);
         full_par ^= 1u;
         if (!ok) break;
-        const int rows = w.sv.len - w.row0[g];
-        if (whole_warp && rows < kBlockM) {
-          const long long row_stride = static_cast<long long>(p.H) * D;
-          uint16_t* dst = p.o_ptr + (static_cast<long long>(w.sv.row_base) + w.row0[g]) *
-                                        row_stride + static_cast<long long>(w.sv.o_head) * D;
-          copy_staged_rows(sbase + L::kStageOff, rows, D / 8, dst, row_stride, lane);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(L::kStageEmpty));
-        } else if (lane == 0) {
+        if (PACKED && p.gqa_log2)
+          tma_store_5d(&p.tm_o, sbase + L::kStageOff, 0, 0, w.sv.row_base + w.row0[g], 0,
+                       w.sv.kv_head);
+        else
           tma_store_4d(&p.tm_o, sbase + L::kStageOff, 0, w.sv.row_base + w.row0[g], 0,
                        w.sv.o_head);
-          bulk_commit_group();
-          bulk_wait_read_all();  // the staging tile may be rewritten
-          mbar_arrive(bar(L::kStageEmpty));
-        }
-        if (whole_warp) __syncwarp();
+        bulk_commit_group();
+        bulk_wait_read_all();  // the staging tile may be rewritten
+        mbar_arrive(bar(L::kStageEmpty));
       }
     }
     if (lane == 0) bulk_wait_all();

@@ -66,6 +66,13 @@ struct FaParams {  // 64-byte aligned through CUtensorMap
   int total_rows;    // rows of the packed Q and O
   int total_rows_k;  // rows of the packed K and V
   int N_k;           // longest key sequence (N when not packed)
+  // Grouped-query packing (packed batches, d <= 128; 0 otherwise): log2 of
+  // the query heads of one K/V head that share a 128-row tile.  A tile then
+  // holds 128 >> gqa_log2 positions of all those heads (row = position *
+  // heads + head), units count (b, K/V head) problems, tm_q / tm_o are 5-D
+  // views {64, heads of a group, rows, d/64, K/V heads} and num_bh = batch
+  // * H_kv.
+  int gqa_log2;
   uint16_t* o_ptr;   // O (packed rows), for the row-by-row store of the last
                      // query tile of a sequence
   float descale_v;   // FP8 kernels: V descale, applied to O in the epilogue
@@ -181,13 +188,16 @@ __device__ __forceinline__ SeqView seq_view(const FaParams& p, int bh, int out_h
     v.kv_head = kv_head(bh, p.H, p.group);
     return v;
   }
-  const int b = bh / p.H, h = bh % p.H;
+  // (grouped-query packing: problem bh is K/V head hk of sequence b, and
+  // its tiles hold all the query heads hk * group .. of that K/V head)
+  const int heads = p.H >> p.gqa_log2;
+  const int b = bh / heads, h = bh % heads;
   packed_rows(p.cu_seqlens, p.seqused_q, b, p.total_rows, p.N, &v.row_base, &v.len);
   packed_rows(p.cu_seqlens_k, p.seqused_k, b, p.total_rows_k, p.N_k, &v.k_row_base, &v.k_len);
   v.k_off = v.k_len - v.len;
-  v.q_head = h;
-  v.o_head = h;
-  v.kv_head = h / p.group;
+  v.q_head = h << p.gqa_log2;
+  v.o_head = h << p.gqa_log2;
+  v.kv_head = p.gqa_log2 ? h : h / p.group;
   return v;
 }
 

@@ -103,6 +103,27 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* map, uint3
       : "memory");
 }
 
+// 5-D tiled load global -> shared, completion signalled on `bar` (tx bytes).
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const void* map, uint32_t bar,
+                                            int c0, int c1, int c2, int c3, int c4) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
+      "r"(bar)
+      : "memory");
+}
+
+// 5-D tiled store shared -> global (bulk-group completion).
+__device__ __forceinline__ void tma_store_5d(const void* map, uint32_t src, int c0, int c1,
+                                             int c2, int c3, int c4) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.global.shared::cta.tile.bulk_group"
+      " [%0, {%2, %3, %4, %5, %6}], [%1];" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+      : "memory");
+}
+
 // 4-D tiled store shared -> global (bulk-group completion).
 // 1-D bulk copy global -> shared, completing `bytes` on mbarrier `bar`
 // (both addresses 16-byte aligned, bytes a multiple of 16).
@@ -142,30 +163,6 @@ __device__ __forceinline__ void bulk_wait_all() {
 // async-proxy (TMA / tcgen05) accesses.
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr)
-               : "memory");
-  return v;
-}
-
-// Copy the first `rows` rows of a staged 128-row output tile to global
-// memory, 16 bytes per lane and step: the tile is [chunks/8 column blocks]
-// [128 rows][128 B] with the 128-byte swizzle (16-byte chunk c of row t at
-// chunk (c ^ t) mod 8 of its block); row t goes to dst + t * row_stride.
-__device__ __forceinline__ void copy_staged_rows(uint32_t stage, int rows, int chunks,
-                                                 uint16_t* dst, long long row_stride,
-                                                 int lane) {
-  for (int idx = lane; idx < rows * chunks; idx += 32) {
-    const int t = idx / chunks, c16 = idx % chunks;
-    const uint32_t addr = stage + (c16 / 8) * (128u * 128u) + t * 128u +
-                          (static_cast<uint32_t>((c16 % 8) ^ (t & 7)) << 4);
-    *reinterpret_cast<uint4*>(dst + t * row_stride + c16 * 8) = ld_shared_v4(addr);
-  }
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b,

@@ -213,6 +213,15 @@ def _oracle_rows(wl, q, k, v, rows):
     Returns the FLOPs of the rows (4*d per admissible key)."""
     import oracle
     lens = wl.seqlens()
+    if wl.decode:
+        # whole sequences (all heads and query rows) of the sampled rows
+        nq, N = wl.n_q, wl.N
+        seqs = sorted(set(r[0] for r in rows))
+        for b in seqs:
+            oracle.attention_varlen_qk(q[b * nq:(b + 1) * nq], k[b * N:(b + 1) * N],
+                                       v[b * N:(b + 1) * N], [0, nq], [0, N], wl.scale,
+                                       wl.causal)
+        return wl.flops / wl.B * len(seqs)
     if wl.dtype == "fp8":
         # Every E4M3 value is a bfloat16 value: widened exactly, the inputs
         # (descales 1) define the same scores, P and O as the FP8 oracle's,
@@ -236,6 +245,19 @@ def _cpu_baseline(wl, budget_s: float = 12.0):
     from workloads import make_qkv
     q, k, v = make_qkv(wl)
     lens = wl.seqlens()
+    if wl.decode:
+        # whole sequences, as many as the budget allows (at least one)
+        t0 = time.perf_counter()
+        flops = _oracle_rows(wl, q, k, v, [(0, 0, 0)])
+        n = 1
+        while time.perf_counter() - t0 < budget_s and n < wl.B:
+            flops += _oracle_rows(wl, q, k, v, [(n, 0, 0)])
+            n += 1
+        dt = time.perf_counter() - t0
+        return {"value": flops / dt / 1e12, "unit": UNIT, "cores": oracle.max_threads(),
+                "kind": "oracle",
+                "sample": f"{n} whole sequences (all heads and query rows) of "
+                          f"{wl.describe()}, fp64, {dt:.1f} s"}
     # calibrate on 64 rows of head (0,0), then size the sample to the budget
     probe = [(0, 0, i) for i in range(0, lens[0], max(1, lens[0] // 64))][:64]
     t0 = time.perf_counter()
@@ -274,7 +296,10 @@ def run_reference(args, wl):
     step_rows = []
     for s in range(args.warmup + args.steps):
         rows = []
-        for _ in range(rows_per_step):
+        if wl.decode:
+            # decode: one whole sequence per step (all heads and query rows)
+            rows.append((rng.randrange(wl.B), 0, 0))
+        for _ in range(0 if wl.decode else rows_per_step):
             b = rng.randrange(wl.B)
             rows.append((b, rng.randrange(wl.H), rng.randrange(lens[b])))
         step_rows.append(rows)
@@ -294,8 +319,10 @@ def run_reference(args, wl):
         "config": _config(wl, "host cores, fp64 oracle"),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(),
                          "kind": "oracle",
-                         "sample": f"{rows_per_step} seeded random query rows per step of "
-                                   f"{wl.describe()}"},
+                         "sample": (f"one seeded random sequence per step of {wl.describe()}"
+                                    if wl.decode else
+                                    f"{rows_per_step} seeded random query rows per step of "
+                                    f"{wl.describe()}")},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -407,12 +434,18 @@ def run_ours(args, wl):
     warmup = max(3, args.warmup)
     q, k, v = make_qkv(wl)
     B, H, N, d = wl.B, wl.H, wl.N, wl.d
-    # packed (varlen) workloads: [total, H, d] tensors, LSE [H, total]
-    total = sum(wl.seqlens())
-    lse_shape = (H, total) if wl.varlen else (B, H, N)
+    # packed (varlen) workloads: [total, H, d] tensors, LSE [H, total];
+    # decode workloads: q [B*n_q, H, d], k, v [B*N, H_kv, d], LSE [H, B*n_q]
+    total = wl.B * wl.n_q if wl.decode else sum(wl.seqlens())
+    lse_shape = (H, total) if (wl.varlen or wl.decode) else (B, H, N)
     cu_dev = torch.tensor(wl.cu_seqlens(), dtype=torch.int32, device=dev) if wl.varlen else None
     max_len = max(wl.seqlens())
-    set_bytes = 4 * q.numel() * q.element_size() + H * total * 4
+    cu_q_dev = cu_k_dev = None
+    if wl.decode:
+        cu_q_dev = torch.arange(0, B + 1, dtype=torch.int32, device=dev) * wl.n_q
+        cu_k_dev = torch.arange(0, B + 1, dtype=torch.int32, device=dev) * N
+    set_bytes = (sum(t.numel() * t.element_size() for t in (q, k, v)) +
+                 q.numel() * q.element_size() + H * total * 4)
     n_sets = max(1, min(8, math.ceil(2.2 * L2_BYTES / set_bytes)))
     sets = []
     for i in range(n_sets):
@@ -450,6 +483,11 @@ def run_ours(args, wl):
         elif wl.varlen:
             st_ = fa.fa_fwd_varlen(qp, kp, vp, op, lp, cu_dev.data_ptr(), B, max_len, total, H,
                                    H, d, wl.scale, int(wl.causal), -1, -1, dcode, handle)
+        elif wl.decode:
+            st_ = fa.fa_fwd_varlen_qk(qp, kp, vp, op, lp, cu_q_dev.data_ptr(),
+                                      cu_k_dev.data_ptr(), None, None, B, wl.n_q, N, total,
+                                      B * N, H, wl.kv_heads, d, wl.scale, int(wl.causal), -1,
+                                      -1, dcode, handle)
         elif wl.splitkv and not plain:
             st_ = fa.fa_fwd_splitkv(qp, kp, vp, op, lp, Bc, Hc, Hc, N, d, wl.scale,
                                     int(wl.causal), -1, -1, dcode, 0,
@@ -561,7 +599,92 @@ def run_ours(args, wl):
         torch.cuda.synchronize(dev)
         plain_ms = start.elapsed_time(end) / args.steps
 
+    def measure_e2e_decode():
+        """Decode workload end to end: chunks of whole sequences (about 8);
+        each chunk's query rows and cached K/V rows are copied in, computed
+        through fa_fwd_varlen_qk on those sequences (offset pointers into
+        the device offset arrays, absolute rows), and its O rows copied out;
+        the [H][B*n_q] LSE is copied once at the end."""
+        nq = wl.n_q
+        q_h, k_h, v_h = (t.pin_memory() for t in (q, k, v))
+        o_h = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+        l_h = torch.empty((H, total), dtype=torch.float32).pin_memory()
+        dq_, dk_, dv_, do_, dl_ = sets[0]
+        per = max(1, B // 8)
+        groups = [(b0, min(B, b0 + per)) for b0 in range(0, B, per)]
+        s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+        def e2e_step():
+            root = torch.cuda.current_stream(dev)
+            ev0 = torch.cuda.Event()
+            ev0.record(root)
+            for st_ in (s_in, stream, s_out):
+                st_.wait_event(ev0)
+            for (g0, g1) in groups:
+                with torch.cuda.stream(s_in):
+                    dq_[g0 * nq:g1 * nq].copy_(q_h[g0 * nq:g1 * nq], non_blocking=True)
+                    dk_[g0 * N:g1 * N].copy_(k_h[g0 * N:g1 * N], non_blocking=True)
+                    dv_[g0 * N:g1 * N].copy_(v_h[g0 * N:g1 * N], non_blocking=True)
+                    ev_in = torch.cuda.Event()
+                    ev_in.record(s_in)
+                stream.wait_event(ev_in)
+                st_ = fa.fa_fwd_varlen_qk(dq_.data_ptr(), dk_.data_ptr(), dv_.data_ptr(),
+                                          do_.data_ptr(), dl_.data_ptr(),
+                                          cu_q_dev.data_ptr() + 4 * g0,
+                                          cu_k_dev.data_ptr() + 4 * g0, None, None, g1 - g0,
+                                          nq, N, total, B * N, H, wl.kv_heads, d, wl.scale,
+                                          int(wl.causal), -1, -1, dcode, handle)
+                if st_ != fa.FA_OK:
+                    raise RuntimeError(f"fa_fwd_varlen_qk: {fa.fa_status_string(st_)}")
+                ev_c = torch.cuda.Event()
+                ev_c.record(stream)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(ev_c)
+                    o_h[g0 * nq:g1 * nq].copy_(do_[g0 * nq:g1 * nq], non_blocking=True)
+            with torch.cuda.stream(s_out):
+                s_out.wait_stream(stream)
+                l_h.copy_(dl_, non_blocking=True)
+            for st_ in (s_in, stream, s_out):
+                ev = torch.cuda.Event()
+                ev.record(st_)
+                root.wait_event(ev)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        graph = None
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                e2e_step()
+            torch.cuda.synchronize(dev)
+            graph.replay()
+            torch.cuda.synchronize(dev)
+        except Exception:  # noqa: BLE001 - any capture failure: run eagerly
+            graph = None
+            torch.cuda.synchronize(dev)
+        steps_ = max(1, min(args.steps, 20))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        root = torch.cuda.current_stream(dev)
+        e0.record(root)
+        for _ in range(steps_):
+            if graph is not None:
+                graph.replay()
+            else:
+                e2e_step()
+        e1.record(root)
+        torch.cuda.synchronize(dev)
+        e2e_ms = _max_over_ranks(e0.elapsed_time(e1) / steps_, dev)
+        h2d = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h))
+        d2h = o_h.numel() * o_h.element_size() + l_h.numel() * 4
+        return {"value": _whole_job_tflops(world, wl.flops, 1, e2e_ms), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "cuda_graph": graph is not None,
+                "api": f"{len(groups)} chunks of sequences: cudaMemcpyAsync in/out around "
+                       f"fa_fwd_varlen_qk"}
+
     def measure_e2e():
+        if wl.decode:
+            return measure_e2e_decode()
         # End to end through the public API with host buffers: each step copies
         # Q, K, V from pinned host memory, runs the forward pass and copies O and
         # LSE back.  Dense bf16/fp16 workloads make one fa_fwd_host call per step
@@ -751,6 +874,19 @@ def run_ours(args, wl):
             peak_note = f"{src} bf16_tflops x 2 (nominal fp8/bf16 dense ratio)"
         achieved = wl.flops / (ms_per_step / 1e3) / 1e12
         traffic, traffic_src = _profiled_traffic(wl.name)
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak,
+                    "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": peak_note,
+                    "traffic": traffic, "traffic_source": traffic_src,
+                    "algorithmic_hbm_bytes": wl.hbm_bytes}
+        if wl.flops / wl.hbm_bytes < peak * 1e12 / (float(peaks.get("hbm_gbs", 6800.0)) * 1e9):
+            # below the ridge point (the decode workload reads its cache once):
+            # bound by HBM bandwidth
+            gbs = wl.hbm_bytes / (ms_per_step / 1e3) / 1e9
+            hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+            roofline = {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                        "frac": gbs / hbm_peak, "peak_source": f"{src} hbm_gbs",
+                        "traffic": traffic, "traffic_source": traffic_src,
+                        "algorithmic_hbm_bytes": wl.hbm_bytes, "tflops": achieved}
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": warmup, "ms_per_step": ms_per_step,
@@ -759,11 +895,8 @@ def run_ours(args, wl):
             "config": _config(wl, f"{n_sets} rotating input sets "
                                   f"({n_sets * set_bytes / 2**20:.0f} MiB) > L2"),
             "pct_of_peak": 100.0 * achieved / peak,
-            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
-                         "unit": "TFLOP/s", "frac": achieved / peak,
-                         "peak_source": peak_note,
-                         "traffic": traffic, "traffic_source": traffic_src,
-                         "algorithmic_hbm_bytes": wl.hbm_bytes},
+            "pct_of_peak_note": "of the tensor peak (the roofline key names the bound)",
+            "roofline": roofline,
             "e2e": e2e,
             "gpu_launches": args.steps * launches_per_call,
             "clocks": clocks,
@@ -891,9 +1024,9 @@ def main():
                     help="timed steps (default: about two seconds of work)")
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", type=int, default=2,
-                    help="1..8 (default 2: B=4 H=16 N=2048 d=128 bf16 full; "
+                    help="1..9 (default 2: B=4 H=16 N=2048 d=128 bf16 full; "
                          "6: the split-KV case; 7: a packed variable-length batch; "
-                         "8: FP8)")
+                         "8: FP8; 9: decode against a KV cache, GQA 8:1)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", dest="sweep", action="store_false",
@@ -905,7 +1038,13 @@ def main():
                     help="seconds of untimed identical steps right before the timed region")
     ap.add_argument("--backward", action="store_true",
                     help="time the backward pass (fa_bwd) instead of the forward")
+    ap.add_argument("--print-kernel-hash", action="store_true",
+                    help="print the hash of the kernel sources (the key of the ncu records "
+                         "in profiles/) and exit")
     args = ap.parse_args()
+    if args.print_kernel_hash:
+        print(_kernel_source_hash())
+        return 0
     from workloads import workload
     wl = workload(args.workload)
     if args.backward:

@@ -206,6 +206,7 @@ FA_API int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, f
  *                 i + n_k - n_q + window_right (n_q = n_k: fa_fwd_varlen).
  *                 A query row with no admissible key gets O = 0 and
  *                 LSE = -inf.
+ * Grouped query heads are packed into shared tiles (fa_set_gqa_pack).
  * Offsets and used lengths are clamped by the kernels to the packed tensors
  * and to max_seqlen_q / max_seqlen_k (a malformed array only shortens
  * sequences).  Tiles read up to 127 rows past a sequence's used rows (masked
@@ -484,6 +485,20 @@ FA_API int fa_set_max_ctas(int max_ctas);
  * with fa_get_device_status().  Faults nothing and traps nothing.
  */
 FA_API int fa_selftest_watchdog(long long timeout_us, void* stream);
+
+/*
+ * Grouped-query packing of the packed-sequence forwards (fa_fwd_varlen,
+ * fa_fwd_varlen_qk) at d <= 128: with enable = 1 (the default), when the
+ * query heads share each K/V head in groups of 2, 4, 8 or 16, the g heads of
+ * a group are packed into every 128-row tile (128 / g positions x g heads),
+ * so that a group streams its keys and values once and short query
+ * sequences (decoding) still fill the tiles; 0 computes each query head in
+ * its own tiles.  The results agree within the parity tolerances (the
+ * lazy rescale may pick a different reference maximum, so they are not bit
+ * for bit the same).  A process-wide setting for later calls; FA_OK, or
+ * FA_ERR_INVALID_ARG for another value.
+ */
+FA_API int fa_set_gqa_pack(int enable);
 
 /* Number of SMs the persistent grid is sized from (current device), or -1. */
 FA_API int fa_num_sms(void);

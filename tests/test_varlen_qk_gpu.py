@@ -197,3 +197,37 @@ def test_argument_errors(fa):
         bad = dict(args, **{key: val})
         assert fa.fa_fwd_varlen_qk(*bad.values()) == want, key
     torch.cuda.synchronize()
+
+
+GQA_CASES = [
+    # (H, H_kv): groups of 2, 4, 8 and 16 are packed into shared tiles, 32
+    # is not
+    (4, 2), (8, 2), (16, 2), (32, 2), (16, 1), (32, 1),
+]
+
+
+@pytest.mark.parametrize("pack", [1, 0], ids=["packed", "unpacked"])
+@pytest.mark.parametrize("heads", GQA_CASES, ids=[f"H{h}_Hkv{k}" for h, k in GQA_CASES])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+def test_grouped_query_packing(fa, pack, heads, d, causal):
+    """Decode and prefill shapes with grouped query heads, with the packing
+    of a group's heads into shared tiles on and off: both against the
+    oracle (full and partial tiles, several tiles per sequence)."""
+    H, H_kv = heads
+    lq, lk = [1, 7, 40, 3, 300, 129], [2048, 700, 4000, 3, 300, 517]
+    cu_q, cu_k = _offsets(lq), _offsets(lk)
+    q, k, v = _inputs(cu_q[-1], cu_k[-1], H, H_kv, d, torch.bfloat16, seed=750 + H + d)
+    fa.fa_set_gqa_pack(pack)
+    try:
+        o, lse = _run(fa, q, k, v, cu_q, cu_k, None, None, causal, (-1, -1), d ** -0.5)
+    finally:
+        fa.fa_set_gqa_pack(1)
+    o_ref, l_ref = oracle.attention_varlen_qk(q, k, v, cu_q, cu_k, d ** -0.5, causal)
+    _check(o, lse, o_ref, l_ref, cu_q, None, f"H={H}/{H_kv} d={d} pack={pack}")
+
+
+def test_gqa_pack_setting_rejects_other_values(fa):
+    assert fa.fa_set_gqa_pack(2) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_set_gqa_pack(-1) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_set_gqa_pack(1) == fa.FA_OK

@@ -34,6 +34,11 @@ class Workload:
     qk_mult: float = 1.0  # Q and K multiplied by this after rounding
     splitkv: bool = False  # run through the split-KV entry point (automatic count)
     varlen: bool = False   # B sequences of seeded lengths in [N/16, N], packed along rows
+    # decode against a cache: B sequences of n_q query rows each, packed
+    # [B*n_q, H, d], attending to N cached keys each (packed [B*N, H_kv, d]),
+    # masks bottom-right aligned (fa_fwd_varlen_qk); 0 otherwise
+    n_q: int = 0
+    H_kv: int = 0
 
     def seqlens(self) -> list[int]:
         """Lengths of the packed sequences (varlen workloads): B integers drawn
@@ -60,21 +65,44 @@ class Workload:
                 "fp8": torch.float8_e4m3fn}[self.dtype]
 
     @property
+    def decode(self) -> bool:
+        return self.n_q > 0
+
+    @property
+    def kv_heads(self) -> int:
+        return self.H_kv if self.H_kv > 0 else self.H
+
+    @property
     def flops(self) -> float:
         """Algorithmic FLOPs of the metric: 4*H*d*sum_b n_b^2 (4*B*H*N^2*d for
-        equal lengths), halved when causal."""
+        equal lengths), halved when causal.  Decode workloads count 4*H*d per
+        admissible (query, key) pair: n_q * N without a mask, and
+        n_q * (N - n_q) + n_q (n_q + 1) / 2 per sequence under the
+        bottom-right causal mask."""
+        if self.decode:
+            nq, nk = float(self.n_q), float(self.N)
+            pairs = nq * (nk - nq) + nq * (nq + 1) / 2 if self.causal else nq * nk
+            return 4.0 * self.H * self.d * self.B * pairs
         f = 4.0 * self.H * self.d * sum(float(n) * n for n in self.seqlens())
         return f / 2 if self.causal else f
 
     @property
     def hbm_bytes(self) -> int:
         """Algorithmic HBM bytes: read Q, K, V; write O (16-bit) and LSE (fp32)."""
+        if self.decode:
+            q_rows = self.B * self.n_q * self.H
+            kv_rows = self.B * self.N * self.kv_heads
+            return q_rows * self.d * 2 * 2 + 2 * kv_rows * self.d * 2 + q_rows * 4
         rows = self.H * sum(self.seqlens())
         in_bytes = 1 if self.dtype == "fp8" else 2
         return 3 * rows * self.d * in_bytes + rows * self.d * 2 + rows * 4
 
     def describe(self) -> str:
         mask = "causal" if self.causal else "full"
+        if self.decode:
+            return (f"{self.B} sequences of {self.n_q} query rows against {self.N} cached keys, "
+                    f"H={self.H} H_kv={self.kv_heads} d={self.d} {self.dtype} {mask} "
+                    f"(bottom-right)")
         extra = f", Q,K x{self.qk_mult:g}" if self.qk_mult != 1.0 else ""
         extra += ", split-KV" if self.splitkv else ""
         if self.varlen:
@@ -100,6 +128,10 @@ WORKLOADS = [
     Workload(7, "bf16_d128_varlen16_causal", 16, 16, 4096, 128, "bf16", True, varlen=True),
     # the headline shape with FP8 E4M3 inputs (descale factors 1)
     Workload(8, "fp8_d128_n2048", 4, 16, 2048, 128, "fp8", False),
+    # decode-shaped: 32 sequences of 32 query rows against 8192 cached keys,
+    # 8 query heads per K/V head (fa_fwd_varlen_qk)
+    Workload(9, "bf16_d128_decode_q32_k8192_gqa8", 32, 32, 8192, 128, "bf16", True,
+             n_q=32, H_kv=4),
 ]
 
 
@@ -109,11 +141,16 @@ def workload(index: int) -> Workload:
 
 def make_qkv(wl: Workload, seed: int | None = None):
     """CPU tensors q, k, v in the workload's dtype, drawn as the recipe says
-    ([B, H, N, d]; packed [total, H, d] for varlen workloads)."""
+    ([B, H, N, d]; packed [total, H, d] for varlen workloads; for decode
+    workloads q [B*n_q, H, d] and k, v [B*N, H_kv, d])."""
     g = torch.Generator().manual_seed(1000 + wl.index if seed is None else seed)
-    shape = (sum(wl.seqlens()), wl.H, wl.d) if wl.varlen else (wl.B, wl.H, wl.N, wl.d)
+    if wl.decode:
+        shapes = [(wl.B * wl.n_q, wl.H, wl.d)] + [(wl.B * wl.N, wl.kv_heads, wl.d)] * 2
+    else:
+        shape = (sum(wl.seqlens()), wl.H, wl.d) if wl.varlen else (wl.B, wl.H, wl.N, wl.d)
+        shapes = [shape] * 3
     out = []
-    for _ in range(3):
+    for shape in shapes:
         out.append(torch.randn(shape, generator=g, dtype=torch.float32)
                    .to(wl.torch_dtype))
     q, k, v = out
