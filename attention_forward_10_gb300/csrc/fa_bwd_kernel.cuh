@@ -24,14 +24,25 @@
 // warps 4-7 for the last 64, and split the epilogue the same way; warp 8
 // issues TMA copies; warp 9 issues the MMAs.  Tensor memory, columns:
 // [0,128) S, [128,256) dP, then the fp32 accumulators: dV and dK (dK/dV
-// kernel) or dQ (dQ kernel), D columns each.  Each column half writes its
-// 16-bit P (or dS) packed over the first 32 of its own 64 S (or dP) columns,
-// so the P V-style products take their A operand in two 64-key pieces.  The
-// next step's S and dP products overwrite those A operands; the PTX ISA
-// orders two tcgen05.mma of one thread only when they share the accumulator
-// and shape, so the issuer first waits for the commit of the previous step's
-// accumulating products (its ring-release barrier).  Every mbarrier wait is
-// bounded.
+// kernel) or dQ (dQ kernel), D columns each, and in the dQ kernel dS at
+// [384,480).
+//
+// Each step's elementwise work runs in two phases, P from S (phase A) and dS
+// from dP and P (phase B), each overlapping a product on the tensor pipe:
+//   * dK/dV kernel, per step: S^T, dP^T, dV += P^T dO, dK += dS^T Q.  Phase A
+//     starts when S^T has completed and runs while dP^T is computed; it
+//     stores P^T (16-bit) over the first 32 of each half's 64 S^T columns,
+//     and the dV product starts; phase B runs meanwhile and stores dS^T the
+//     same way over dP^T's columns for the dK product.
+//   * dQ kernel: the issuer runs one step ahead.  After step j's S has been
+//     read by every thread (phase A), S of step j+1 is issued; phase B of
+//     step j writes dS to its own columns, then dQ += dS K of step j and dP
+//     of step j+1 are issued.  The next dS store waits for that dP's commit,
+//     which also covers the dQ product that read the previous dS.
+// A product that overwrites tensor-memory columns an earlier product read
+// (S^T over P^T, dP^T over dS^T) is issued only after that product's commit
+// has arrived: the PTX ISA orders two tcgen05.mma of one thread only when
+// they share the accumulator and shape.  Every mbarrier wait is bounded.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -43,35 +54,90 @@
 namespace fa {
 namespace bwd {
 
+// Entry check failure of the backward kernels (not a wait): the status word
+// gets FA_ERR_MISALIGNED with this site code.
+constexpr int kStatusMisaligned = 3;  // == FA_ERR_MISALIGNED
+constexpr int kSiteSmemBase = 13;
+
 constexpr int kThreads = 320;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kEwThreads = 256;  // warps 0-7
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColDP = 128, kColAcc = 256;
+constexpr uint32_t kColDS = 384;  // dQ kernel: dS (96 columns)
+// dK/dV kernel: S^T and dP^T alternate between the regions at 0 and 128
+// from step to step (step j: S^T at region(j), dP^T at region(j + 1)).
+__device__ __forceinline__ uint32_t region(uint32_t step) { return (step & 1u) * 128u; }
 
-// Shared memory layout of both kernels: two 128-row tiles that stay for the
-// whole unit (K,V or Q,dO), a 2-stage ring of the two streamed tiles, and
-// per stage 128 LSE2 and 128 D values (dK/dV kernel).
+// Shared memory layout of both kernels (tiles 1024-byte aligned for the
+// 128-byte swizzle): two 128-row tiles that stay for the whole unit (K, V or
+// Q, dO); ring A, three stages of the streamed tile needed first in a step
+// (Q in the dK/dV kernel, K in the dQ kernel); ring B, two stages of the
+// other one (dO, with the stage's 128 LSE2 and 128 D values, or V); then
+// the barriers.  The dynamic shared memory base must be 1024-byte aligned:
+// no slack is reserved (the kernels check and give up with
+// FA_ERR_MISALIGNED otherwise).
 template <int D>
 struct Layout {
   static_assert(D == 64 || D == 128, "head dim");
   static constexpr uint32_t kTile = 128 * D * 2;
-  static constexpr int kStages = 2;
-  static constexpr uint32_t kFixOff = 0;                       // 2 tiles
-  static constexpr uint32_t kRingOff = 2 * kTile;              // stage s: 2 tiles
-  static constexpr uint32_t kVecOff = kRingOff + kStages * 2 * kTile;  // stage s: 1 KB
-  static constexpr uint32_t kBarOff = kVecOff + kStages * 1024;
+  static constexpr int kStagesA = 3, kStagesB = 2;
+  static constexpr uint32_t kFixOff = 0;                                 // 2 tiles
+  static constexpr uint32_t kRingAOff = 2 * kTile;                       // stage s: 1 tile
+  static constexpr uint32_t kRingBOff = kRingAOff + kStagesA * kTile;    // stage s: 1 tile
+  static constexpr uint32_t kVecOff = kRingBOff + kStagesB * kTile;      // stage s: 1 KB
+  static constexpr uint32_t kBarOff = kVecOff + kStagesB * 1024;
   // barriers
   static constexpr int kFixFull = 0, kFixEmpty = 1;
-  static constexpr int kRingFull = 2;   // + stage
-  static constexpr int kRingEmpty = 4;  // + stage
-  static constexpr int kSFull = 6, kPReady = 7, kAccDone = 8, kAccFree = 9, kDrain = 10;
-  static constexpr int kNumBars = 11;
+  static constexpr int kAFull = 2;    // + stage
+  static constexpr int kAEmpty = 5;   // + stage
+  static constexpr int kBFull = 8;    // + stage
+  static constexpr int kBEmpty = 10;  // + stage
+  static constexpr int kSDone = 12;     // the S (S^T) product has completed
+  static constexpr int kDPDone = 13;    // the dP (dP^T) product has completed
+  static constexpr int kPStored = 14;   // dK/dV: P^T is in tensor memory (256 arrivals)
+  static constexpr int kDSStored = 15;  // dS (dS^T) is in tensor memory (256 arrivals)
+  static constexpr int kSRead = 16;     // dQ: S has been read by every thread (256 arrivals)
+  static constexpr int kDPRead = 17;    // dK/dV: dP^T has been read by every thread (256)
+  static constexpr int kAccDone = 18, kAccFree = 19, kDrain = 20;
+  static constexpr int kNumBars = 21;
   static constexpr uint32_t kCtlOff = kBarOff + kNumBars * 8;
-  static constexpr uint32_t kSmemBytes = kCtlOff + 16 + 1024;
+  static constexpr uint32_t kSmemBytes = kCtlOff + 16;
   static_assert(kSmemBytes <= 232448, "exceeds the shared memory of one CTA");
 };
+
+template <typename L, typename Bar>
+__device__ __forceinline__ void init_barriers(Bar bar) {
+  mbar_init(bar(L::kFixFull), 1);
+  mbar_init(bar(L::kFixEmpty), 1);
+  for (int s = 0; s < L::kStagesA; ++s) {
+    mbar_init(bar(L::kAFull + s), 1);
+    mbar_init(bar(L::kAEmpty + s), 1);
+  }
+  for (int s = 0; s < L::kStagesB; ++s) {
+    mbar_init(bar(L::kBFull + s), 1);
+    mbar_init(bar(L::kBEmpty + s), 1);
+  }
+  mbar_init(bar(L::kSDone), 1);
+  mbar_init(bar(L::kDPDone), 1);
+  mbar_init(bar(L::kPStored), kEwThreads);
+  mbar_init(bar(L::kDSStored), kEwThreads);
+  mbar_init(bar(L::kSRead), kEwThreads);
+  mbar_init(bar(L::kDPRead), kEwThreads);
+  mbar_init(bar(L::kAccDone), 1);
+  mbar_init(bar(L::kAccFree), kEwThreads);
+  mbar_init(bar(L::kDrain), 1);
+}
+
+// Entry check of both kernels: the layout above needs a 1024-byte aligned
+// shared memory base.  False (after recording FA_ERR_MISALIGNED in the
+// status word) means the CTA must return at once.
+__device__ __forceinline__ bool smem_base_ok(uint32_t sbase, int* status) {
+  if ((sbase & 1023u) == 0) return true;
+  if (threadIdx.x == 0) atomicCAS(status, 0, kStatusMisaligned | (kSiteSmemBase << 8));
+  return false;
+}
 
 // Masks of the backward: key j is admissible for query i when
 // i - win_left <= j <= i + win_right (causal: win_right = 0), both < N.
@@ -135,51 +201,62 @@ __global__ void __launch_bounds__(256)
   }
 }
 
-// P and dS for one 64-column half of a tile, one row per thread:
-//   p  = 2^(s * scale_log2 + nlse2),   ds = p * (dp + ndsum)
+// The elementwise work of one 64-column half of a tile, one row per thread,
+// in two phases so that each overlaps a matrix product:
+//   phase A (p_half):  p  = 2^(s * scale_log2 + nlse2)  (masked columns 0)
+//   phase B (ds_half): ds = p * (dp + ndsum)
 // (nlse2 = -LSE log2 e, ndsum = -D per column in the dK/dV kernel, per row in
-// the dQ kernel), in two 32-column steps whose S and dP columns (at tS + c,
-// tDP + c) arrive with one wait each; P (when WRITE_P) goes packed to tS + c
-// and dS to `tds`, over columns already read.  `keep(e)` is the mask of
+// the dQ kernel).  Phase A reads the half's 64 S columns at tS + c and, when
+// WRITE_P, stores P packed to 16 bits over the first 32 of them; phase B
+// takes the half's 64 dP values (loaded by the caller) and stores dS packed
+// into 32 columns at `tds`.  p stays in registers between the phases.  `keep(e)` is the mask of
 // column c + e (only called when MASK).
 template <bool BF16, bool MASK, bool WRITE_P, bool COLUMN_VECS, typename Keep>
-__device__ __forceinline__ void p_ds_half(uint32_t tS, uint32_t tDP, uint32_t tds, int c,
-                                          float sl2, const float* nlse2, const float* ndsum,
-                                          float nlse2_row, float ndsum_row, Keep keep) {
+__device__ __forceinline__ void p_half(uint32_t tS, int c, float sl2, const float* nlse2,
+                                       float nlse2_row, Keep keep, float (&p)[64]) {
+  uint32_t sr[64];
+  tmem_ld_2x32_sync(tS + c, sr, tS + c + 32, sr + 32);
   const uint64_t sl2x2 = pack_f32x2(sl2, sl2);
-  const uint64_t zero2 = pack_f32x2(0.f, 0.f);
-#pragma unroll 1
-  for (int q = 0; q < 64; q += 32) {
-    uint32_t sr[32], dpr[32];
-    tmem_ld_2x32_sync(tS + c + q, sr, tDP + c + q, dpr);
-    uint32_t pk[16], dk[16];
 #pragma unroll
-    for (int e = 0; e < 32; e += 2) {
-      const int col = c + q + e;
-      const uint64_t nl = COLUMN_VECS ? *reinterpret_cast<const uint64_t*>(nlse2 + col)
-                                      : pack_f32x2(nlse2_row, nlse2_row);
-      const uint64_t nd = COLUMN_VECS ? *reinterpret_cast<const uint64_t*>(ndsum + col)
-                                      : pack_f32x2(ndsum_row, ndsum_row);
-      float x0, x1;
-      unpack_f32x2(fma_f32x2(pack_f32x2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
-                             sl2x2, nl),
-                   x0, x1);
-      float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-      if (MASK) {
-        if (!keep(q + e)) p0 = 0.f;
-        if (!keep(q + e + 1)) p1 = 0.f;
-      }
-      const uint64_t pp = pack_f32x2(p0, p1);
-      const uint64_t t = add_f32x2(
-          pack_f32x2(__uint_as_float(dpr[e]), __uint_as_float(dpr[e + 1])), nd);
-      float d0, d1;
-      unpack_f32x2(fma_f32x2(pp, t, zero2), d0, d1);
-      if (WRITE_P) pk[e / 2] = pack2<BF16>(p0, p1);
-      dk[e / 2] = pack2<BF16>(d0, d1);
+  for (int e = 0; e < 64; e += 2) {
+    const uint64_t nl = COLUMN_VECS ? *reinterpret_cast<const uint64_t*>(nlse2 + c + e)
+                                    : pack_f32x2(nlse2_row, nlse2_row);
+    float x0, x1;
+    unpack_f32x2(
+        fma_f32x2(pack_f32x2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), sl2x2, nl),
+        x0, x1);
+    p[e] = ex2_approx(x0);
+    p[e + 1] = ex2_approx(x1);
+    if (MASK) {
+      if (!keep(e)) p[e] = 0.f;
+      if (!keep(e + 1)) p[e + 1] = 0.f;
     }
-    if (WRITE_P) tmem_st_x16(tS + c + q / 2, pk);
-    tmem_st_x16(tds + q / 2, dk);
   }
+  if (WRITE_P) {
+    uint32_t pk[32];
+#pragma unroll
+    for (int e = 0; e < 64; e += 2) pk[e / 2] = pack2<BF16>(p[e], p[e + 1]);
+    tmem_st_x32(tS + c, pk);
+  }
+}
+
+template <bool BF16, bool COLUMN_VECS>
+__device__ __forceinline__ void ds_half(const uint32_t (&dpr)[64], uint32_t tds, int c,
+                                        const float* ndsum, float ndsum_row,
+                                        const float (&p)[64]) {
+  const uint64_t zero2 = pack_f32x2(0.f, 0.f);
+  uint32_t dk[32];
+#pragma unroll
+  for (int e = 0; e < 64; e += 2) {
+    const uint64_t nd = COLUMN_VECS ? *reinterpret_cast<const uint64_t*>(ndsum + c + e)
+                                    : pack_f32x2(ndsum_row, ndsum_row);
+    const uint64_t t =
+        add_f32x2(pack_f32x2(__uint_as_float(dpr[e]), __uint_as_float(dpr[e + 1])), nd);
+    float d0, d1;
+    unpack_f32x2(fma_f32x2(pack_f32x2(p[e], p[e + 1]), t, zero2), d0, d1);
+    dk[e / 2] = pack2<BF16>(d0, d1);
+  }
+  tmem_st_x32(tds, dk);
 }
 
 // ---------------------------------------------------------- dK / dV kernel
@@ -218,11 +295,10 @@ template <int D, bool CAUSAL, bool BF16, bool PACKED>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
   using L = Layout<D>;
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw_addr = smem_u32(smem_raw);
-  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (!smem_base_ok(sbase, p.status)) return;
   auto bar = [&](int i) -> uint32_t { return sbase + L::kBarOff + 8u * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kCtlOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kCtlOff + 4);
@@ -230,17 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kKOff = L::kFixOff, kVOff = L::kFixOff + L::kTile;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(L::kFixFull), 1);
-    mbar_init(bar(L::kFixEmpty), 1);
-    for (int s = 0; s < L::kStages; ++s) {
-      mbar_init(bar(L::kRingFull + s), 1);
-      mbar_init(bar(L::kRingEmpty + s), 1);
-    }
-    mbar_init(bar(L::kSFull), 1);
-    mbar_init(bar(L::kPReady), kEwThreads);
-    mbar_init(bar(L::kAccDone), 1);
-    mbar_init(bar(L::kAccFree), kEwThreads);
-    mbar_init(bar(L::kDrain), 1);
+    init_barriers<L>(bar);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -266,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kProducerWarp) {
     // ---------------------------------------------------------------- TMA
     if (lane == 0) {
-      uint32_t it = 0, units = 0;
+      uint32_t na = 0, nb = 0, units = 0;  // ring A / ring B stages filled, units
       bool ok = true;
       for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
         const KvUnit w = decode_kv_unit<CAUSAL, PACKED>(u, p);
@@ -282,96 +348,131 @@ __global__ void __launch_bounds__(kThreads, 1)
                     kv_head_c);
         tma_load_4d(sbase + kVOff, &p.tm_v, bar(L::kFixFull), 0, w.row_base + w.n * 128, 0,
                     kv_head_c);
-        for (int s = 0; s < w.steps && ok; ++s, ++it) {
+        for (int s = 0; s < w.steps && ok; ++s) {
           const int bh = b * p.H + hk * p.group + s / w.nm;
           const int m = w.m_lo + s % w.nm;
-          const uint32_t st = it % L::kStages;
-          ok = wait_bar(bar(L::kRingEmpty + st), ((it / L::kStages) & 1u) ^ 1u, ctl,
-                        kSiteProducerQ);
-          if (!ok) break;
-          const uint32_t ring = sbase + L::kRingOff + st * 2 * L::kTile;
-          const uint32_t vec = sbase + L::kVecOff + st * 1024;
-          mbar_arrive_expect_tx(bar(L::kRingFull + st), 2 * L::kTile + 1024);
           const int q_head_c = PACKED ? bh % p.H : bh;
-          tma_load_4d(ring, &p.tm_q, bar(L::kRingFull + st), 0, w.row_base + m * 128, 0,
-                      q_head_c);
-          tma_load_4d(ring + L::kTile, &p.tm_do, bar(L::kRingFull + st), 0,
+          // Q into ring A
+          const uint32_t sa = na % L::kStagesA;
+          ok = wait_bar(bar(L::kAEmpty + sa), ((na / L::kStagesA) & 1u) ^ 1u, ctl, kSiteProducerQ);
+          if (!ok) break;
+          mbar_arrive_expect_tx(bar(L::kAFull + sa), L::kTile);
+          tma_load_4d(sbase + L::kRingAOff + sa * L::kTile, &p.tm_q, bar(L::kAFull + sa), 0,
+                      w.row_base + m * 128, 0, q_head_c);
+          ++na;
+          // dO and the stage's LSE2, D values into ring B
+          const uint32_t sb = nb % L::kStagesB;
+          ok = wait_bar(bar(L::kBEmpty + sb), ((nb / L::kStagesB) & 1u) ^ 1u, ctl, kSiteProducerQ);
+          if (!ok) break;
+          const uint32_t vec = sbase + L::kVecOff + sb * 1024;
+          mbar_arrive_expect_tx(bar(L::kBFull + sb), L::kTile + 1024);
+          tma_load_4d(sbase + L::kRingBOff + sb * L::kTile, &p.tm_do, bar(L::kBFull + sb), 0,
                       w.row_base + m * 128, 0, q_head_c);
           const long long voff = static_cast<long long>(bh) * p.n_pad + m * 128;
-          bulk_load_1d(vec, p.lse2 + voff, 512, bar(L::kRingFull + st));
-          bulk_load_1d(vec + 512, p.dsum + voff, 512, bar(L::kRingFull + st));
+          bulk_load_1d(vec, p.lse2 + voff, 512, bar(L::kBFull + sb));
+          bulk_load_1d(vec + 512, p.dsum + voff, 512, bar(L::kBFull + sb));
+          ++nb;
         }
       }
       // let the copies in flight land before the CTA may exit
-      const uint32_t first = it > (uint32_t)L::kStages ? it - L::kStages : 0u;
-      for (uint32_t j = first; j < it; ++j)
-        wait_drain(bar(L::kRingFull + j % L::kStages), (j / L::kStages) & 1u, p.timeout_ns);
+      for (uint32_t j = na > (uint32_t)L::kStagesA ? na - L::kStagesA : 0u; j < na; ++j)
+        wait_drain(bar(L::kAFull + j % L::kStagesA), (j / L::kStagesA) & 1u, p.timeout_ns);
+      for (uint32_t j = nb > (uint32_t)L::kStagesB ? nb - L::kStagesB : 0u; j < nb; ++j)
+        wait_drain(bar(L::kBFull + j % L::kStagesB), (j / L::kStagesB) & 1u, p.timeout_ns);
       if (units > 0) wait_drain(bar(L::kFixFull), (units - 1) & 1u, p.timeout_ns);
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA
+    // Per step j, in issue order: dP^T(j), dV += P^T(j) dO, S^T(j + 1),
+    // dK += dS^T(j) Q; S^T(j) was issued in step j - 1 (or the unit's start).
     if (lane == 0) {
       constexpr uint32_t kIdescS = make_idesc_f16(128, 128, BF16, false);
       constexpr uint32_t kIdescAcc = make_idesc_f16(128, D, BF16, true);
       const uint64_t k_desc = smem_desc_sw128(sbase + kKOff, 16, 1024);
       const uint64_t v_desc = smem_desc_sw128(sbase + kVOff, 16, 1024);
-      uint32_t it = 0, units = 0, pr = 0;
+      // S^T = K Q^T of `step` (keys on the lanes) into region(step)
+      auto issue_s = [&](uint32_t step) {
+        const uint64_t q_kdesc =
+            smem_desc_sw128(sbase + L::kRingAOff + (step % L::kStagesA) * L::kTile, 16, 1024);
+        if constexpr (D == 128)
+          mma_ss_kmajor_x8(tmem + region(step), k_desc, q_kdesc, kIdescS, 0u);
+        else
+          mma_ss_kmajor_x4(tmem + region(step), k_desc, q_kdesc, kIdescS, 0u);
+        tc_commit(bar(L::kSDone));
+      };
+      uint32_t it = 0, units = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
         const KvUnit w = decode_kv_unit<CAUSAL, PACKED>(u, p);
         if (w.steps == 0) continue;  // a key tile past a shorter sequence's end
         const uint32_t uix = units++;
         ok = wait_bar(bar(L::kFixFull), uix & 1u, ctl, kSiteMmaK);
+        ok = ok && wait_bar(bar(L::kAFull + it % L::kStagesA), (it / L::kStagesA) & 1u, ctl,
+                            kSiteMmaQ);
+        // region(it) held the previous step's dP^T: wait until it was read
+        if (ok && it > 0) ok = wait_bar(bar(L::kDPRead), (it - 1) & 1u, ctl, kSiteMmaO);
         if (!ok) break;
+        tc_fence_after_sync();
+        issue_s(it);
         for (int s = 0; s < w.steps; ++s, ++it) {
-          const uint32_t st = it % L::kStages;
-          ok = wait_bar(bar(L::kRingFull + st), (it / L::kStages) & 1u, ctl, kSiteMmaQ);
-          if (!ok) break;
-          if (it > 0) {
-            // the previous step's dV, dK products read P^T, dS^T from the
-            // columns S^T, dP^T overwrite: wait for their commit
-            const uint32_t pst = (it - 1) % L::kStages;
-            ok = wait_bar(bar(L::kRingEmpty + pst), ((it - 1) / L::kStages) & 1u, ctl, kSiteMmaO);
-            if (!ok) break;
+          const uint32_t sa = it % L::kStagesA, sb = it % L::kStagesB;
+          const uint32_t x = tmem + region(it);
+          ok = wait_bar(bar(L::kBFull + sb), (it / L::kStagesB) & 1u, ctl, kSiteMmaQ);
+          // dP^T goes to region(it + 1), where the previous step's P^T and
+          // dS^T were read by its dV, dK products (the dK product's commit
+          // to its ring-A release covers both)
+          if (ok && it > 0) {
+            const uint32_t pa = (it - 1) % L::kStagesA;
+            ok = wait_bar(bar(L::kAEmpty + pa), ((it - 1) / L::kStagesA) & 1u, ctl, kSiteMmaO);
           }
+          if (!ok) break;
           tc_fence_after_sync();
-          const uint32_t ring = sbase + L::kRingOff + st * 2 * L::kTile;
-          const uint64_t q_kdesc = smem_desc_sw128(ring, 16, 1024);
-          const uint64_t do_kdesc = smem_desc_sw128(ring + L::kTile, 16, 1024);
-          // S^T = K Q^T and dP^T = V dO^T (keys on the lanes)
-          if constexpr (D == 128) {
-            mma_ss_kmajor_x8(tmem + kColS, k_desc, q_kdesc, kIdescS, 0u);
-            mma_ss_kmajor_x8(tmem + kColDP, v_desc, do_kdesc, kIdescS, 0u);
-          } else {
-            mma_ss_kmajor_x4(tmem + kColS, k_desc, q_kdesc, kIdescS, 0u);
-            mma_ss_kmajor_x4(tmem + kColDP, v_desc, do_kdesc, kIdescS, 0u);
-          }
-          tc_commit(bar(L::kSFull));
-          ok = wait_bar(bar(L::kPReady), pr, ctl, kSiteMmaP);
-          pr ^= 1u;
-          if (!ok) break;
-          if (s == 0 && uix > 0) {
+          const uint32_t do_addr = sbase + L::kRingBOff + sb * L::kTile;
+          // dP^T = V dO^T
+          if constexpr (D == 128)
+            mma_ss_kmajor_x8(tmem + region(it + 1), v_desc, smem_desc_sw128(do_addr, 16, 1024),
+                             kIdescS, 0u);
+          else
+            mma_ss_kmajor_x4(tmem + region(it + 1), v_desc, smem_desc_sw128(do_addr, 16, 1024),
+                             kIdescS, 0u);
+          tc_commit(bar(L::kDPDone));
+          if (s == w.steps - 1) tc_commit(bar(L::kFixEmpty));  // K and V read for the last time
+          ok = wait_bar(bar(L::kPStored), it & 1u, ctl, kSiteMmaP);
+          if (ok && s == 0 && uix > 0) {
             // the previous unit's dK, dV must have been read out
             ok = wait_bar(bar(L::kAccFree), (uix - 1) & 1u, ctl, kSiteMmaO);
-            if (!ok) break;
           }
+          if (!ok) break;
           tc_fence_after_sync();
-          // dV += P^T dO and dK += dS^T Q (dO, Q as MN-major B operands)
-          const uint64_t do_mdesc = smem_desc_sw128(ring + L::kTile, 128 * 128, 1024);
-          const uint64_t q_mdesc = smem_desc_sw128(ring, 128 * 128, 1024);
-          // (P^T and dS^T of queries 0-63 at columns +0, of 64-127 at +64;
-          //  the second half of dO / Q is 64 rows = 512 descriptor units on)
-          mma_ts_mnmajor_x4(tmem + kColAcc, tmem + kColS, do_mdesc, kIdescAcc, s > 0 ? 1u : 0u);
-          mma_ts_mnmajor_x4(tmem + kColAcc, tmem + kColS + 64, do_mdesc + 512, kIdescAcc, 1u);
-          mma_ts_mnmajor_x4(tmem + kColAcc + D, tmem + kColDP, q_mdesc, kIdescAcc,
-                            s > 0 ? 1u : 0u);
-          mma_ts_mnmajor_x4(tmem + kColAcc + D, tmem + kColDP + 64, q_mdesc + 512, kIdescAcc, 1u);
-          tc_commit(bar(L::kRingEmpty + st));
+          // dV += P^T dO (dO as the MN-major B operand; P^T of queries 0-63 at
+          // x + 0, of 64-127 at x + 64; the second half of dO is 64 rows =
+          // 512 descriptor units on)
+          const uint64_t do_mdesc = smem_desc_sw128(do_addr, 128 * 128, 1024);
+          mma_ts_mnmajor_x4(tmem + kColAcc, x, do_mdesc, kIdescAcc, s > 0 ? 1u : 0u);
+          mma_ts_mnmajor_x4(tmem + kColAcc, x + 64, do_mdesc + 512, kIdescAcc, 1u);
+          if (s + 1 < w.steps) {
+            // the next step's S^T into region(it + 1) once dP^T was read
+            ok = wait_bar(bar(L::kAFull + (it + 1) % L::kStagesA), ((it + 1) / L::kStagesA) & 1u,
+                          ctl, kSiteMmaQ);
+            ok = ok && wait_bar(bar(L::kDPRead), it & 1u, ctl, kSiteMmaO);
+            if (!ok) break;
+            tc_fence_after_sync();
+            issue_s(it + 1);
+          }
+          ok = wait_bar(bar(L::kDSStored), it & 1u, ctl, kSiteMmaP);
+          if (!ok) break;
+          tc_fence_after_sync();
+          // dK += dS^T Q (dS^T of queries 0-63 at x + 32, of 64-127 at x + 96)
+          const uint64_t q_mdesc =
+              smem_desc_sw128(sbase + L::kRingAOff + sa * L::kTile, 128 * 128, 1024);
+          mma_ts_mnmajor_x4(tmem + kColAcc + D, x + 32, q_mdesc, kIdescAcc, s > 0 ? 1u : 0u);
+          mma_ts_mnmajor_x4(tmem + kColAcc + D, x + 96, q_mdesc + 512, kIdescAcc, 1u);
+          tc_commit(bar(L::kAEmpty + sa));
+          tc_commit(bar(L::kBEmpty + sb));
         }
         if (!ok) break;
         tc_commit(bar(L::kAccDone));
-        tc_commit(bar(L::kFixEmpty));
       }
       tc_commit(bar(L::kDrain));
       wait_drain(bar(L::kDrain), 0, p.timeout_ns);
@@ -382,11 +483,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int half = warp / 4;                 // query columns [64 half, +64)
     const int t = (warp % 4) * 32 + lane;      // key row within the tile == lane
     const uint32_t lane_base = static_cast<uint32_t>((warp % 4) * 32) << 16;
-    const uint32_t tS = tmem + lane_base + kColS;
-    const uint32_t tDP = tmem + lane_base + kColDP;
     const int c = half * 64;
     const float sl2 = p.scale_log2;
-    uint32_t it = 0, units = 0, sf = 0;
+    uint32_t it = 0, units = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
       const KvUnit w = decode_kv_unit<CAUSAL, PACKED>(u, p);
@@ -394,15 +493,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t uix = units++;
       const int j = w.n * 128 + t;  // this thread's key
       for (int s = 0; s < w.steps; ++s, ++it) {
-        const uint32_t st = it % L::kStages;
+        const uint32_t sb = it % L::kStagesB, ph = it & 1u;
+        const uint32_t x = tmem + lane_base + region(it);
+        const uint32_t y = tmem + lane_base + region(it + 1);
         const int m = w.m_lo + s % w.nm;
-        ok = wait_bar(bar(L::kRingFull + st), (it / L::kStages) & 1u, ctl, kSiteSoftmaxS);
-        ok = ok && wait_bar(bar(L::kSFull), sf, ctl, kSiteSoftmaxS);
-        sf ^= 1u;
+        ok = wait_bar(bar(L::kBFull + sb), (it / L::kStagesB) & 1u, ctl, kSiteSoftmaxS);
+        ok = ok && wait_bar(bar(L::kSDone), ph, ctl, kSiteSoftmaxS);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after_sync();
-        const float* nlse2 = reinterpret_cast<const float*>(smem + L::kVecOff + st * 1024);
+        const float* nlse2 = reinterpret_cast<const float*>(smem + L::kVecOff + sb * 1024);
         const float* ndsum = nlse2 + 128;
         const int i0 = m * 128 + c;  // query of column c
         const bool need_mask = (w.n * 128 + 127 - i0 > p.win_right) ||
@@ -410,14 +510,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                                (w.n * 128 + 128 > w.len);
         const int N = w.len, wl = p.win_left, wr = p.win_right;
         auto keep = [&](int e) { return admissible(i0 + e, j, N, wl, wr); };
+        // phase A: P^T over the first 32 of the half's S^T columns (while
+        // dP^T is computed)
+        float pv[64];
         if (need_mask)
-          p_ds_half<BF16, true, true, true>(tS, tDP, tDP + c, c, sl2, nlse2, ndsum, 0.f, 0.f, keep);
+          p_half<BF16, true, true, true>(x, c, sl2, nlse2, 0.f, keep, pv);
         else
-          p_ds_half<BF16, false, true, true>(tS, tDP, tDP + c, c, sl2, nlse2, ndsum, 0.f, 0.f,
-                                             keep);
+          p_half<BF16, false, true, true>(x, c, sl2, nlse2, 0.f, keep, pv);
         tmem_wait_st();
         tc_fence_before_sync();
-        mbar_arrive(bar(L::kPReady));
+        mbar_arrive(bar(L::kPStored));
+        // phase B: dS^T over the last 32 (while dV += P^T dO runs)
+        ok = wait_bar(bar(L::kDPDone), ph, ctl, kSiteSoftmaxS);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after_sync();
+        uint32_t dpr[64];
+        tmem_ld_2x32_sync(y + c, dpr, y + c + 32, dpr + 32);
+        tc_fence_before_sync();
+        mbar_arrive(bar(L::kDPRead));
+        ds_half<BF16, true>(dpr, x + c + 32, c, ndsum, 0.f, pv);
+        tmem_wait_st();
+        tc_fence_before_sync();
+        mbar_arrive(bar(L::kDSStored));
       }
       if (!ok) break;
       // ---- epilogue: warps 0-3 write dV, warps 4-7 scale * dK (this thread's key row)
@@ -449,7 +564,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before_sync();
       mbar_arrive(bar(L::kAccFree));
     }
-    (void)it;
   }
 
   tc_fence_before_sync();
@@ -500,11 +614,10 @@ template <int D, bool CAUSAL, bool BF16, bool PACKED>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
   using L = Layout<D>;
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw_addr = smem_u32(smem_raw);
-  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (!smem_base_ok(sbase, p.status)) return;
   auto bar = [&](int i) -> uint32_t { return sbase + L::kBarOff + 8u * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kCtlOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kCtlOff + 4);
@@ -512,17 +625,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kQOff = L::kFixOff, kDOOff = L::kFixOff + L::kTile;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(L::kFixFull), 1);
-    mbar_init(bar(L::kFixEmpty), 1);
-    for (int s = 0; s < L::kStages; ++s) {
-      mbar_init(bar(L::kRingFull + s), 1);
-      mbar_init(bar(L::kRingEmpty + s), 1);
-    }
-    mbar_init(bar(L::kSFull), 1);
-    mbar_init(bar(L::kPReady), kEwThreads);
-    mbar_init(bar(L::kAccDone), 1);
-    mbar_init(bar(L::kAccFree), kEwThreads);
-    mbar_init(bar(L::kDrain), 1);
+    init_barriers<L>(bar);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -548,7 +651,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kProducerWarp) {
     // ---------------------------------------------------------------- TMA
     if (lane == 0) {
-      uint32_t it = 0, units = 0;
+      uint32_t na = 0, nb = 0, units = 0;  // ring A / ring B stages filled, units
       bool ok = true;
       for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
         const QUnit w = decode_q_unit<CAUSAL, PACKED>(u, p);
@@ -564,79 +667,120 @@ __global__ void __launch_bounds__(kThreads, 1)
                     q_head_c);
         tma_load_4d(sbase + kDOOff, &p.tm_do, bar(L::kFixFull), 0, w.row_base + w.m * 128, 0,
                     q_head_c);
-        for (int n = w.n0; n < w.n1 && ok; ++n, ++it) {
-          const uint32_t st = it % L::kStages;
-          ok = wait_bar(bar(L::kRingEmpty + st), ((it / L::kStages) & 1u) ^ 1u, ctl,
+        for (int n = w.n0; n < w.n1 && ok; ++n) {
+          // K into ring A
+          const uint32_t sa = na % L::kStagesA;
+          ok = wait_bar(bar(L::kAEmpty + sa), ((na / L::kStagesA) & 1u) ^ 1u, ctl,
                         kSiteProducerKV);
           if (!ok) break;
-          const uint32_t ring = sbase + L::kRingOff + st * 2 * L::kTile;
-          mbar_arrive_expect_tx(bar(L::kRingFull + st), 2 * L::kTile);
-          tma_load_4d(ring, &p.tm_k, bar(L::kRingFull + st), 0, w.row_base + n * 128, 0,
-                      kv_head_c);
-          tma_load_4d(ring + L::kTile, &p.tm_v, bar(L::kRingFull + st), 0, w.row_base + n * 128,
-                      0, kv_head_c);
+          mbar_arrive_expect_tx(bar(L::kAFull + sa), L::kTile);
+          tma_load_4d(sbase + L::kRingAOff + sa * L::kTile, &p.tm_k, bar(L::kAFull + sa), 0,
+                      w.row_base + n * 128, 0, kv_head_c);
+          ++na;
+          // V into ring B
+          const uint32_t sb = nb % L::kStagesB;
+          ok = wait_bar(bar(L::kBEmpty + sb), ((nb / L::kStagesB) & 1u) ^ 1u, ctl,
+                        kSiteProducerKV);
+          if (!ok) break;
+          mbar_arrive_expect_tx(bar(L::kBFull + sb), L::kTile);
+          tma_load_4d(sbase + L::kRingBOff + sb * L::kTile, &p.tm_v, bar(L::kBFull + sb), 0,
+                      w.row_base + n * 128, 0, kv_head_c);
+          ++nb;
         }
       }
-      const uint32_t first = it > (uint32_t)L::kStages ? it - L::kStages : 0u;
-      for (uint32_t j = first; j < it; ++j)
-        wait_drain(bar(L::kRingFull + j % L::kStages), (j / L::kStages) & 1u, p.timeout_ns);
+      for (uint32_t j = na > (uint32_t)L::kStagesA ? na - L::kStagesA : 0u; j < na; ++j)
+        wait_drain(bar(L::kAFull + j % L::kStagesA), (j / L::kStagesA) & 1u, p.timeout_ns);
+      for (uint32_t j = nb > (uint32_t)L::kStagesB ? nb - L::kStagesB : 0u; j < nb; ++j)
+        wait_drain(bar(L::kBFull + j % L::kStagesB), (j / L::kStagesB) & 1u, p.timeout_ns);
       if (units > 0) wait_drain(bar(L::kFixFull), (units - 1) & 1u, p.timeout_ns);
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA
+    // Per step j, in issue order: S(j + 1), dQ += dS(j) K, dP(j + 1); S(j)
+    // and dP(j) were issued in step j - 1 (or the unit's start).
     if (lane == 0) {
       constexpr uint32_t kIdescS = make_idesc_f16(128, 128, BF16, false);
       constexpr uint32_t kIdescAcc = make_idesc_f16(128, D, BF16, true);
       const uint64_t q_desc = smem_desc_sw128(sbase + kQOff, 16, 1024);
       const uint64_t do_desc = smem_desc_sw128(sbase + kDOOff, 16, 1024);
-      uint32_t it = 0, units = 0, pr = 0;
+      uint32_t it = 0, units = 0;
       bool ok = true;
+      // S = Q K^T of `step` (queries on the lanes; K in its ring-A stage)
+      auto issue_s = [&](uint32_t step) {
+        const uint64_t k_kdesc =
+            smem_desc_sw128(sbase + L::kRingAOff + (step % L::kStagesA) * L::kTile, 16, 1024);
+        if constexpr (D == 128)
+          mma_ss_kmajor_x8(tmem + kColS, q_desc, k_kdesc, kIdescS, 0u);
+        else
+          mma_ss_kmajor_x4(tmem + kColS, q_desc, k_kdesc, kIdescS, 0u);
+        tc_commit(bar(L::kSDone));
+      };
+      // dP = dO V^T of `step` (V in its ring-B stage, read only here)
+      auto issue_dp = [&](uint32_t step) {
+        const uint32_t sb = step % L::kStagesB;
+        const uint64_t v_kdesc = smem_desc_sw128(sbase + L::kRingBOff + sb * L::kTile, 16, 1024);
+        if constexpr (D == 128)
+          mma_ss_kmajor_x8(tmem + kColDP, do_desc, v_kdesc, kIdescS, 0u);
+        else
+          mma_ss_kmajor_x4(tmem + kColDP, do_desc, v_kdesc, kIdescS, 0u);
+        tc_commit(bar(L::kDPDone));
+        tc_commit(bar(L::kBEmpty + sb));
+      };
       for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
         const QUnit w = decode_q_unit<CAUSAL, PACKED>(u, p);
         if (w.n1 == w.n0) continue;  // a query tile past a shorter sequence's end
         const uint32_t uix = units++;
         ok = wait_bar(bar(L::kFixFull), uix & 1u, ctl, kSiteMmaQ);
+        ok = ok && wait_bar(bar(L::kAFull + it % L::kStagesA), (it / L::kStagesA) & 1u, ctl,
+                            kSiteMmaK);
+        // S overwrites the columns the previous step's S was read from
+        if (ok && it > 0) ok = wait_bar(bar(L::kSRead), (it - 1) & 1u, ctl, kSiteMmaO);
         if (!ok) break;
+        tc_fence_after_sync();
+        issue_s(it);
+        // (dP's columns were read before the previous step's dS was stored,
+        // which the issuer waited for before that step's dQ product)
+        ok = wait_bar(bar(L::kBFull + it % L::kStagesB), (it / L::kStagesB) & 1u, ctl, kSiteMmaV);
+        if (!ok) break;
+        tc_fence_after_sync();
+        issue_dp(it);
+        if (w.n1 - w.n0 == 1) tc_commit(bar(L::kFixEmpty));  // Q and dO read for the last time
         for (int n = w.n0; n < w.n1; ++n, ++it) {
-          const uint32_t st = it % L::kStages;
-          ok = wait_bar(bar(L::kRingFull + st), (it / L::kStages) & 1u, ctl, kSiteMmaK);
-          if (!ok) break;
-          if (it > 0) {
-            // the previous step's dQ product read dS from the columns S
-            // overwrites: wait for its commit
-            const uint32_t pst = (it - 1) % L::kStages;
-            ok = wait_bar(bar(L::kRingEmpty + pst), ((it - 1) / L::kStages) & 1u, ctl, kSiteMmaO);
+          const uint32_t sa = it % L::kStagesA;
+          const bool more = n + 1 < w.n1;
+          if (more) {
+            // the next step's S, while this step's dS is computed
+            ok = wait_bar(bar(L::kAFull + (it + 1) % L::kStagesA), ((it + 1) / L::kStagesA) & 1u,
+                          ctl, kSiteMmaK);
+            ok = ok && wait_bar(bar(L::kSRead), it & 1u, ctl, kSiteMmaO);
             if (!ok) break;
+            tc_fence_after_sync();
+            issue_s(it + 1);
           }
-          tc_fence_after_sync();
-          const uint32_t ring = sbase + L::kRingOff + st * 2 * L::kTile;
-          const uint64_t k_kdesc = smem_desc_sw128(ring, 16, 1024);
-          const uint64_t v_kdesc = smem_desc_sw128(ring + L::kTile, 16, 1024);
-          // S = Q K^T and dP = dO V^T (queries on the lanes)
-          if constexpr (D == 128) {
-            mma_ss_kmajor_x8(tmem + kColS, q_desc, k_kdesc, kIdescS, 0u);
-            mma_ss_kmajor_x8(tmem + kColDP, do_desc, v_kdesc, kIdescS, 0u);
-          } else {
-            mma_ss_kmajor_x4(tmem + kColS, q_desc, k_kdesc, kIdescS, 0u);
-            mma_ss_kmajor_x4(tmem + kColDP, do_desc, v_kdesc, kIdescS, 0u);
-          }
-          tc_commit(bar(L::kSFull));
-          if (n == w.n1 - 1) tc_commit(bar(L::kFixEmpty));  // Q and dO read for the last time
-          ok = wait_bar(bar(L::kPReady), pr, ctl, kSiteMmaP);
-          pr ^= 1u;
-          if (!ok) break;
-          if (n == w.n0 && uix > 0) {
+          ok = wait_bar(bar(L::kDSStored), it & 1u, ctl, kSiteMmaP);
+          if (ok && n == w.n0 && uix > 0)
             ok = wait_bar(bar(L::kAccFree), (uix - 1) & 1u, ctl, kSiteMmaO);
-            if (!ok) break;
-          }
+          if (!ok) break;
           tc_fence_after_sync();
-          // dQ += dS K (K as the MN-major B operand)
-          const uint64_t k_mdesc = smem_desc_sw128(ring, 128 * 128, 1024);
-          mma_ts_mnmajor_x4(tmem + kColAcc, tmem + kColS, k_mdesc, kIdescAcc,
+          // dQ += dS K (dS from its own columns, K as the MN-major B operand)
+          const uint64_t k_mdesc =
+              smem_desc_sw128(sbase + L::kRingAOff + sa * L::kTile, 128 * 128, 1024);
+          mma_ts_mnmajor_x4(tmem + kColAcc, tmem + kColDS, k_mdesc, kIdescAcc,
                             n > w.n0 ? 1u : 0u);
-          mma_ts_mnmajor_x4(tmem + kColAcc, tmem + kColS + 64, k_mdesc + 512, kIdescAcc, 1u);
-          tc_commit(bar(L::kRingEmpty + st));
+          mma_ts_mnmajor_x4(tmem + kColAcc, tmem + kColDS + 64, k_mdesc + 512, kIdescAcc, 1u);
+          tc_commit(bar(L::kAEmpty + sa));
+          if (more) {
+            // the next step's dP (this step's dP was read before its dS was
+            // stored); its commit also covers the dQ product above, which
+            // the next dS store must follow
+            ok = wait_bar(bar(L::kBFull + (it + 1) % L::kStagesB), ((it + 1) / L::kStagesB) & 1u,
+                          ctl, kSiteMmaV);
+            if (!ok) break;
+            tc_fence_after_sync();
+            issue_dp(it + 1);
+            if (n + 2 == w.n1) tc_commit(bar(L::kFixEmpty));
+          }
         }
         if (!ok) break;
         tc_commit(bar(L::kAccDone));
@@ -654,7 +798,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tDP = tmem + lane_base + kColDP;
     const int c = half * 64;
     const float sl2 = p.scale_log2;
-    uint32_t units = 0, sf = 0;
+    uint32_t it = 0, units = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
       const QUnit w = decode_q_unit<CAUSAL, PACKED>(u, p);
@@ -665,9 +809,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float nlse2 = p.lse2[vrow];
       const float ndsum = p.dsum[vrow];
       const int row_end = min(w.len, w.m * 128 + 128);
-      for (int n = w.n0; n < w.n1; ++n) {
-        ok = wait_bar(bar(L::kSFull), sf, ctl, kSiteSoftmaxS);
-        sf ^= 1u;
+      for (int n = w.n0; n < w.n1; ++n, ++it) {
+        const uint32_t ph = it & 1u;
+        ok = wait_bar(bar(L::kSDone), ph, ctl, kSiteSoftmaxS);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after_sync();
@@ -677,15 +821,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                                (kbase < row_end - 1 - p.win_left);
         const int N = w.len, wl = p.win_left, wr = p.win_right;
         auto keep = [&](int e) { return admissible(i, kbase + e, N, wl, wr); };
+        // phase A: P (S may be overwritten once every thread has read it)
+        float pv[64];
         if (need_mask)
-          p_ds_half<BF16, true, false, false>(tS, tDP, tS + c, c, sl2, nullptr, nullptr, nlse2,
-                                              ndsum, keep);
+          p_half<BF16, true, false, false>(tS, c, sl2, nullptr, nlse2, keep, pv);
         else
-          p_ds_half<BF16, false, false, false>(tS, tDP, tS + c, c, sl2, nullptr, nullptr, nlse2,
-                                               ndsum, keep);
+          p_half<BF16, false, false, false>(tS, c, sl2, nullptr, nlse2, keep, pv);
+        tc_fence_before_sync();
+        mbar_arrive(bar(L::kSRead));
+        // phase B: dS into its own columns
+        ok = wait_bar(bar(L::kDPDone), ph, ctl, kSiteSoftmaxS);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after_sync();
+        uint32_t dpr[64];
+        tmem_ld_2x32_sync(tDP + c, dpr, tDP + c + 32, dpr + 32);
+        ds_half<BF16, false>(dpr, tmem + lane_base + kColDS + c, c, nullptr, ndsum, pv);
         tmem_wait_st();
         tc_fence_before_sync();
-        mbar_arrive(bar(L::kPReady));
+        mbar_arrive(bar(L::kDSStored));
       }
       if (!ok) break;
       // ---- epilogue: scale * dQ, columns [D/2 half, +D/2) of this thread's row

@@ -458,7 +458,9 @@ FA_API const char* fa_status_string(int status);
 /*
  * Synchronise `stream`, then read and clear the device status word that the
  * kernels' bounded waits set when one runs out.  Returns FA_OK,
- * FA_ERR_DEVICE_TIMEOUT, or FA_ERR_CUDA if the synchronisation failed.
+ * FA_ERR_DEVICE_TIMEOUT, or FA_ERR_CUDA if the synchronisation failed; also
+ * FA_ERR_MISALIGNED (site 13) if a backward kernel found its dynamic shared
+ * memory not 1024-byte aligned and returned without doing anything.
  * `site` (may be NULL) receives the code of the wait that ran out (0 if none).
  */
 FA_API int fa_get_device_status(void* stream, int* site);
