@@ -59,9 +59,10 @@ namespace bwd {
 constexpr int kStatusMisaligned = 3;  // == FA_ERR_MISALIGNED
 constexpr int kSiteSmemBase = 13;
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMmaWarp = 9;    // issues the S (S^T) and dP (dP^T) products
+constexpr int kGradWarp = 10;  // issues the gradient products (dV and dK, or dQ)
 constexpr int kEwThreads = 256;  // warps 0-7
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColDP = 128, kColAcc = 256;
@@ -99,9 +100,11 @@ struct Layout {
   static constexpr int kPStored = 14;   // dK/dV: P^T is in tensor memory (256 arrivals)
   static constexpr int kDSStored = 15;  // dS (dS^T) is in tensor memory (256 arrivals)
   static constexpr int kSRead = 16;     // dQ: S has been read by every thread (256 arrivals)
-  static constexpr int kDPRead = 17;    // dK/dV: dP^T has been read by every thread (256)
-  static constexpr int kAccDone = 18, kAccFree = 19, kDrain = 20;
-  static constexpr int kNumBars = 21;
+  static constexpr int kDPRead = 17;    // dP (dP^T) has been read by every thread (256)
+  static constexpr int kVDone = 18;     // dK/dV: the dV product has completed
+  static constexpr int kAccDone = 19, kAccFree = 20;
+  static constexpr int kDrain = 21;     // both issuing threads' last products (2 arrivals)
+  static constexpr int kNumBars = 22;
   static constexpr uint32_t kCtlOff = kBarOff + kNumBars * 8;
   static constexpr uint32_t kSmemBytes = kCtlOff + 16;
   static_assert(kSmemBytes <= 232448, "exceeds the shared memory of one CTA");
@@ -125,9 +128,28 @@ __device__ __forceinline__ void init_barriers(Bar bar) {
   mbar_init(bar(L::kDSStored), kEwThreads);
   mbar_init(bar(L::kSRead), kEwThreads);
   mbar_init(bar(L::kDPRead), kEwThreads);
+  mbar_init(bar(L::kVDone), 1);
   mbar_init(bar(L::kAccDone), 1);
   mbar_init(bar(L::kAccFree), kEwThreads);
-  mbar_init(bar(L::kDrain), 1);
+  mbar_init(bar(L::kDrain), 2);
+}
+
+// Bounded wait for two phases; the fast path tests both with back-to-back
+// try_waits (one round trip instead of two when both have completed).
+__device__ __forceinline__ bool wait_bar2(uint32_t a, uint32_t pa, uint32_t b, uint32_t pb,
+                                          const Ctl& ctl, int site) {
+  uint32_t both;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 q, [%3], %4;\n\t"
+      "and.pred p, p, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(both)
+      : "r"(a), "r"(pa), "r"(b), "r"(pb)
+      : "memory");
+  if (both) return true;
+  return wait_bar(a, pa, ctl, site) && wait_bar(b, pb, ctl, site);
 }
 
 // Entry check of both kernels: the layout above needs a 1024-byte aligned
@@ -259,6 +281,43 @@ __device__ __forceinline__ void ds_half(const uint32_t (&dpr)[64], uint32_t tds,
   tmem_st_x32(tds, dk);
 }
 
+// Epilogue store of 32 columns (16 packed words w) of the rows of one warp,
+// one row per lane: a 4x4 transpose of 16-byte chunks within each group of
+// four lanes (two shfl_xor stages) leaves lane 4g + i with chunk i of the
+// rows of lanes 4g .. 4g + 3, so that each of the four stores writes 8 rows'
+// 64 contiguous bytes (whole 32-byte sectors) instead of 32 rows' 16 bytes.
+// row_ptr(r): where lane r's 32 columns go (nullptr: that row is not stored).
+template <typename RowPtr>
+__device__ __forceinline__ void store_rows_x32(uint32_t (&w)[16], int lane, RowPtr row_ptr) {
+#pragma unroll
+  for (int m = 1; m <= 2; m <<= 1) {
+    const bool hi = (lane & m) != 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (j & m) continue;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        // the low lane of the pair keeps chunk j and sends chunk j|m, the
+        // high lane keeps j|m and sends j
+        const uint32_t send = hi ? w[4 * j + e] : w[4 * (j | m) + e];
+        const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, m);
+        if (hi)
+          w[4 * j + e] = recv;
+        else
+          w[4 * (j | m) + e] = recv;
+      }
+    }
+  }
+  const int g = lane >> 2, i = lane & 3;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    uint16_t* dst = row_ptr(4 * g + k);
+    if (dst != nullptr)
+      *reinterpret_cast<uint4*>(dst + 8 * i) =
+          make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+  }
+}
+
 // ---------------------------------------------------------- dK / dV kernel
 struct KvUnit {
   int bkv;        // K/V head (b * H_kv + h_kv)
@@ -383,12 +442,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
-    // ---------------------------------------------------------------- MMA
-    // Per step j, in issue order: dP^T(j), dV += P^T(j) dO, S^T(j + 1),
-    // dK += dS^T(j) Q; S^T(j) was issued in step j - 1 (or the unit's start).
+    // ------------------------------------------------- S^T and dP^T products
+    // Per step j: dP^T(j), then S^T(j + 1) (S^T(j) came in step j - 1 or
+    // at the unit's start).
     if (lane == 0) {
       constexpr uint32_t kIdescS = make_idesc_f16(128, 128, BF16, false);
-      constexpr uint32_t kIdescAcc = make_idesc_f16(128, D, BF16, true);
       const uint64_t k_desc = smem_desc_sw128(sbase + kKOff, 16, 1024);
       const uint64_t v_desc = smem_desc_sw128(sbase + kVOff, 16, 1024);
       // S^T = K Q^T of `step` (keys on the lanes) into region(step)
@@ -408,37 +466,65 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (w.steps == 0) continue;  // a key tile past a shorter sequence's end
         const uint32_t uix = units++;
         ok = wait_bar(bar(L::kFixFull), uix & 1u, ctl, kSiteMmaK);
-        ok = ok && wait_bar(bar(L::kAFull + it % L::kStagesA), (it / L::kStagesA) & 1u, ctl,
-                            kSiteMmaQ);
         // region(it) held the previous step's dP^T: wait until it was read
-        if (ok && it > 0) ok = wait_bar(bar(L::kDPRead), (it - 1) & 1u, ctl, kSiteMmaO);
+        ok = ok && (it == 0 ? wait_bar(bar(L::kAFull), 0u, ctl, kSiteMmaQ)
+                            : wait_bar2(bar(L::kAFull + it % L::kStagesA),
+                                        (it / L::kStagesA) & 1u, bar(L::kDPRead),
+                                        (it - 1) & 1u, ctl, kSiteMmaQ));
         if (!ok) break;
         tc_fence_after_sync();
         issue_s(it);
         for (int s = 0; s < w.steps; ++s, ++it) {
-          const uint32_t sa = it % L::kStagesA, sb = it % L::kStagesB;
-          const uint32_t x = tmem + region(it);
-          ok = wait_bar(bar(L::kBFull + sb), (it / L::kStagesB) & 1u, ctl, kSiteMmaQ);
+          const uint32_t sb = it % L::kStagesB;
           // dP^T goes to region(it + 1), where the previous step's P^T and
-          // dS^T were read by its dV, dK products (the dK product's commit
-          // to its ring-A release covers both)
-          if (ok && it > 0) {
-            const uint32_t pa = (it - 1) % L::kStagesA;
-            ok = wait_bar(bar(L::kAEmpty + pa), ((it - 1) / L::kStagesA) & 1u, ctl, kSiteMmaO);
-          }
+          // dS^T were read by its dV and dK products (the dK product's
+          // commit to its ring-A release covers both)
+          ok = it == 0 ? wait_bar(bar(L::kBFull), 0u, ctl, kSiteMmaO)
+                       : wait_bar2(bar(L::kBFull + sb), (it / L::kStagesB) & 1u,
+                                   bar(L::kAEmpty + (it - 1) % L::kStagesA),
+                                   ((it - 1) / L::kStagesA) & 1u, ctl, kSiteMmaO);
           if (!ok) break;
           tc_fence_after_sync();
-          const uint32_t do_addr = sbase + L::kRingBOff + sb * L::kTile;
           // dP^T = V dO^T
+          const uint64_t do_kdesc =
+              smem_desc_sw128(sbase + L::kRingBOff + sb * L::kTile, 16, 1024);
           if constexpr (D == 128)
-            mma_ss_kmajor_x8(tmem + region(it + 1), v_desc, smem_desc_sw128(do_addr, 16, 1024),
-                             kIdescS, 0u);
+            mma_ss_kmajor_x8(tmem + region(it + 1), v_desc, do_kdesc, kIdescS, 0u);
           else
-            mma_ss_kmajor_x4(tmem + region(it + 1), v_desc, smem_desc_sw128(do_addr, 16, 1024),
-                             kIdescS, 0u);
+            mma_ss_kmajor_x4(tmem + region(it + 1), v_desc, do_kdesc, kIdescS, 0u);
           tc_commit(bar(L::kDPDone));
-          if (s == w.steps - 1) tc_commit(bar(L::kFixEmpty));  // K and V read for the last time
-          ok = wait_bar(bar(L::kPStored), it & 1u, ctl, kSiteMmaP);
+          if (s == w.steps - 1) {
+            tc_commit(bar(L::kFixEmpty));  // K and V read for the last time
+          } else {
+            // the next step's S^T into region(it + 1) once dP^T was read
+            ok = wait_bar2(bar(L::kAFull + (it + 1) % L::kStagesA), ((it + 1) / L::kStagesA) & 1u,
+                           bar(L::kDPRead), it & 1u, ctl, kSiteMmaQ);
+            if (!ok) break;
+            tc_fence_after_sync();
+            issue_s(it + 1);
+          }
+        }
+      }
+      tc_commit(bar(L::kDrain));
+      wait_drain(bar(L::kDrain), 0, p.timeout_ns);
+    }
+    __syncwarp();
+  } else if (warp == kGradWarp) {
+    // --------------------------------------------- dV and dK products
+    if (lane == 0) {
+      constexpr uint32_t kIdescAcc = make_idesc_f16(128, D, BF16, true);
+      uint32_t it = 0, units = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+        const KvUnit w = decode_kv_unit<CAUSAL, PACKED>(u, p);
+        if (w.steps == 0) continue;
+        const uint32_t uix = units++;
+        for (int s = 0; s < w.steps; ++s, ++it) {
+          const uint32_t sa = it % L::kStagesA, sb = it % L::kStagesB;
+          const uint32_t x = tmem + region(it);
+          // P^T stored (and dO landed: this thread reads it)
+          ok = wait_bar2(bar(L::kPStored), it & 1u, bar(L::kBFull + sb), (it / L::kStagesB) & 1u,
+                         ctl, kSiteMmaP);
           if (ok && s == 0 && uix > 0) {
             // the previous unit's dK, dV must have been read out
             ok = wait_bar(bar(L::kAccFree), (uix - 1) & 1u, ctl, kSiteMmaO);
@@ -448,19 +534,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           // dV += P^T dO (dO as the MN-major B operand; P^T of queries 0-63 at
           // x + 0, of 64-127 at x + 64; the second half of dO is 64 rows =
           // 512 descriptor units on)
-          const uint64_t do_mdesc = smem_desc_sw128(do_addr, 128 * 128, 1024);
+          const uint64_t do_mdesc =
+              smem_desc_sw128(sbase + L::kRingBOff + sb * L::kTile, 128 * 128, 1024);
           mma_ts_mnmajor_x4(tmem + kColAcc, x, do_mdesc, kIdescAcc, s > 0 ? 1u : 0u);
           mma_ts_mnmajor_x4(tmem + kColAcc, x + 64, do_mdesc + 512, kIdescAcc, 1u);
-          if (s + 1 < w.steps) {
-            // the next step's S^T into region(it + 1) once dP^T was read
-            ok = wait_bar(bar(L::kAFull + (it + 1) % L::kStagesA), ((it + 1) / L::kStagesA) & 1u,
-                          ctl, kSiteMmaQ);
-            ok = ok && wait_bar(bar(L::kDPRead), it & 1u, ctl, kSiteMmaO);
-            if (!ok) break;
-            tc_fence_after_sync();
-            issue_s(it + 1);
-          }
-          ok = wait_bar(bar(L::kDSStored), it & 1u, ctl, kSiteMmaP);
+          tc_commit(bar(L::kVDone));
+          ok = wait_bar2(bar(L::kDSStored), it & 1u, bar(L::kAFull + sa), (it / L::kStagesA) & 1u,
+                         ctl, kSiteMmaP);
           if (!ok) break;
           tc_fence_after_sync();
           // dK += dS^T Q (dS^T of queries 0-63 at x + 32, of 64-127 at x + 96)
@@ -468,6 +548,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               smem_desc_sw128(sbase + L::kRingAOff + sa * L::kTile, 128 * 128, 1024);
           mma_ts_mnmajor_x4(tmem + kColAcc + D, x + 32, q_mdesc, kIdescAcc, s > 0 ? 1u : 0u);
           mma_ts_mnmajor_x4(tmem + kColAcc + D, x + 96, q_mdesc + 512, kIdescAcc, 1u);
+          // (S^T and dP^T of this step, which also read these stages, have
+          // completed: dS^T was stored after dP^T's commit)
           tc_commit(bar(L::kAEmpty + sa));
           tc_commit(bar(L::kBEmpty + sb));
         }
@@ -478,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait_drain(bar(L::kDrain), 0, p.timeout_ns);
     }
     __syncwarp();
-  } else {
+  } else if (warp < kEwThreads / 32) {
     // ------------------------------------------ P^T, dS^T and the epilogue
     const int half = warp / 4;                 // query columns [64 half, +64)
     const int t = (warp % 4) * 32 + lane;      // key row within the tile == lane
@@ -518,6 +600,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         else
           p_half<BF16, false, true, true>(x, c, sl2, nlse2, 0.f, keep, pv);
         tmem_wait_st();
+        // (the previous step's dV product has completed before this P^T is
+        // announced, so the issuing thread cannot miss a phase of kPStored)
+        if (it > 0) {
+          ok = wait_bar(bar(L::kVDone), (it - 1) & 1u, ctl, kSiteSoftmaxS);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+        }
         tc_fence_before_sync();
         mbar_arrive(bar(L::kPStored));
         // phase B: dS^T over the last 32 (while dV += P^T dO runs)
@@ -541,11 +630,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after_sync();
       // dV / dK row j of K/V head bkv ([B*H_kv][N][d], or packed [total][H_kv][d])
-      const long long row = PACKED ? (static_cast<long long>(w.row_base) + j) * p.H_kv +
-                                         w.bkv % p.H_kv
-                                   : static_cast<long long>(w.bkv) * p.N + j;
-      uint16_t* dst = (half == 0 ? p.dv : p.dk) + row * D;
+      uint16_t* const base = half == 0 ? p.dv : p.dk;
       const float mul = half == 0 ? 1.f : p.scale;
+      const int j_warp = w.n * 128 + (warp % 4) * 32;  // key of lane 0's row
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t r[32];
@@ -554,12 +641,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e)
           w4[e] = pack2<BF16>(__uint_as_float(r[2 * e]) * mul, __uint_as_float(r[2 * e + 1]) * mul);
-        if (j < w.len) {
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4)
-            *reinterpret_cast<uint4*>(dst + c0 + q4 * 8) =
-                make_uint4(w4[4 * q4], w4[4 * q4 + 1], w4[4 * q4 + 2], w4[4 * q4 + 3]);
-        }
+        store_rows_x32(w4, lane, [&](int rl) -> uint16_t* {
+          const int jr = j_warp + rl;
+          if (jr >= w.len) return nullptr;
+          const long long row = PACKED ? (static_cast<long long>(w.row_base) + jr) * p.H_kv +
+                                             w.bkv % p.H_kv
+                                       : static_cast<long long>(w.bkv) * p.N + jr;
+          return base + row * D + c0;
+        });
       }
       tc_fence_before_sync();
       mbar_arrive(bar(L::kAccFree));
@@ -696,69 +785,68 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
-    // ---------------------------------------------------------------- MMA
-    // Per step j, in issue order: S(j + 1), dQ += dS(j) K, dP(j + 1); S(j)
-    // and dP(j) were issued in step j - 1 (or the unit's start).
+    // --------------------------------------------------- S and dP products
     if (lane == 0) {
       constexpr uint32_t kIdescS = make_idesc_f16(128, 128, BF16, false);
-      constexpr uint32_t kIdescAcc = make_idesc_f16(128, D, BF16, true);
       const uint64_t q_desc = smem_desc_sw128(sbase + kQOff, 16, 1024);
       const uint64_t do_desc = smem_desc_sw128(sbase + kDOOff, 16, 1024);
       uint32_t it = 0, units = 0;
       bool ok = true;
-      // S = Q K^T of `step` (queries on the lanes; K in its ring-A stage)
-      auto issue_s = [&](uint32_t step) {
-        const uint64_t k_kdesc =
-            smem_desc_sw128(sbase + L::kRingAOff + (step % L::kStagesA) * L::kTile, 16, 1024);
-        if constexpr (D == 128)
-          mma_ss_kmajor_x8(tmem + kColS, q_desc, k_kdesc, kIdescS, 0u);
-        else
-          mma_ss_kmajor_x4(tmem + kColS, q_desc, k_kdesc, kIdescS, 0u);
-        tc_commit(bar(L::kSDone));
-      };
-      // dP = dO V^T of `step` (V in its ring-B stage, read only here)
-      auto issue_dp = [&](uint32_t step) {
-        const uint32_t sb = step % L::kStagesB;
-        const uint64_t v_kdesc = smem_desc_sw128(sbase + L::kRingBOff + sb * L::kTile, 16, 1024);
-        if constexpr (D == 128)
-          mma_ss_kmajor_x8(tmem + kColDP, do_desc, v_kdesc, kIdescS, 0u);
-        else
-          mma_ss_kmajor_x4(tmem + kColDP, do_desc, v_kdesc, kIdescS, 0u);
-        tc_commit(bar(L::kDPDone));
-        tc_commit(bar(L::kBEmpty + sb));
-      };
       for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
         const QUnit w = decode_q_unit<CAUSAL, PACKED>(u, p);
         if (w.n1 == w.n0) continue;  // a query tile past a shorter sequence's end
         const uint32_t uix = units++;
         ok = wait_bar(bar(L::kFixFull), uix & 1u, ctl, kSiteMmaQ);
-        ok = ok && wait_bar(bar(L::kAFull + it % L::kStagesA), (it / L::kStagesA) & 1u, ctl,
-                            kSiteMmaK);
-        // S overwrites the columns the previous step's S was read from
-        if (ok && it > 0) ok = wait_bar(bar(L::kSRead), (it - 1) & 1u, ctl, kSiteMmaO);
-        if (!ok) break;
-        tc_fence_after_sync();
-        issue_s(it);
-        // (dP's columns were read before the previous step's dS was stored,
-        // which the issuer waited for before that step's dQ product)
-        ok = wait_bar(bar(L::kBFull + it % L::kStagesB), (it / L::kStagesB) & 1u, ctl, kSiteMmaV);
-        if (!ok) break;
-        tc_fence_after_sync();
-        issue_dp(it);
-        if (w.n1 - w.n0 == 1) tc_commit(bar(L::kFixEmpty));  // Q and dO read for the last time
+        for (int n = w.n0; n < w.n1 && ok; ++n, ++it) {
+          const uint32_t sa = it % L::kStagesA, sb = it % L::kStagesB;
+          // S = Q K^T (queries on the lanes) over the previous step's S,
+          // once every thread has read that
+          ok = it == 0 ? wait_bar(bar(L::kAFull), 0u, ctl, kSiteMmaK)
+                       : wait_bar2(bar(L::kAFull + sa), (it / L::kStagesA) & 1u, bar(L::kSRead),
+                                   (it - 1) & 1u, ctl, kSiteMmaK);
+          if (!ok) break;
+          tc_fence_after_sync();
+          const uint64_t k_kdesc = smem_desc_sw128(sbase + L::kRingAOff + sa * L::kTile, 16, 1024);
+          if constexpr (D == 128)
+            mma_ss_kmajor_x8(tmem + kColS, q_desc, k_kdesc, kIdescS, 0u);
+          else
+            mma_ss_kmajor_x4(tmem + kColS, q_desc, k_kdesc, kIdescS, 0u);
+          tc_commit(bar(L::kSDone));
+          // dP = dO V^T over the previous step's dP, once read
+          ok = it == 0 ? wait_bar(bar(L::kBFull), 0u, ctl, kSiteMmaV)
+                       : wait_bar2(bar(L::kBFull + sb), (it / L::kStagesB) & 1u, bar(L::kDPRead),
+                                   (it - 1) & 1u, ctl, kSiteMmaV);
+          if (!ok) break;
+          tc_fence_after_sync();
+          const uint64_t v_kdesc = smem_desc_sw128(sbase + L::kRingBOff + sb * L::kTile, 16, 1024);
+          if constexpr (D == 128)
+            mma_ss_kmajor_x8(tmem + kColDP, do_desc, v_kdesc, kIdescS, 0u);
+          else
+            mma_ss_kmajor_x4(tmem + kColDP, do_desc, v_kdesc, kIdescS, 0u);
+          tc_commit(bar(L::kDPDone));
+          tc_commit(bar(L::kBEmpty + sb));                     // V read for the last time
+          if (n == w.n1 - 1) tc_commit(bar(L::kFixEmpty));  // Q and dO too
+        }
+      }
+      tc_commit(bar(L::kDrain));
+      wait_drain(bar(L::kDrain), 0, p.timeout_ns);
+    }
+    __syncwarp();
+  } else if (warp == kGradWarp) {
+    // ------------------------------------------------------- dQ products
+    if (lane == 0) {
+      constexpr uint32_t kIdescAcc = make_idesc_f16(128, D, BF16, true);
+      uint32_t it = 0, units = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+        const QUnit w = decode_q_unit<CAUSAL, PACKED>(u, p);
+        if (w.n1 == w.n0) continue;
+        const uint32_t uix = units++;
         for (int n = w.n0; n < w.n1; ++n, ++it) {
           const uint32_t sa = it % L::kStagesA;
-          const bool more = n + 1 < w.n1;
-          if (more) {
-            // the next step's S, while this step's dS is computed
-            ok = wait_bar(bar(L::kAFull + (it + 1) % L::kStagesA), ((it + 1) / L::kStagesA) & 1u,
-                          ctl, kSiteMmaK);
-            ok = ok && wait_bar(bar(L::kSRead), it & 1u, ctl, kSiteMmaO);
-            if (!ok) break;
-            tc_fence_after_sync();
-            issue_s(it + 1);
-          }
-          ok = wait_bar(bar(L::kDSStored), it & 1u, ctl, kSiteMmaP);
+          // dS stored (and K landed: this thread reads it)
+          ok = wait_bar2(bar(L::kDSStored), it & 1u, bar(L::kAFull + sa), (it / L::kStagesA) & 1u,
+                         ctl, kSiteMmaP);
           if (ok && n == w.n0 && uix > 0)
             ok = wait_bar(bar(L::kAccFree), (uix - 1) & 1u, ctl, kSiteMmaO);
           if (!ok) break;
@@ -769,18 +857,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ts_mnmajor_x4(tmem + kColAcc, tmem + kColDS, k_mdesc, kIdescAcc,
                             n > w.n0 ? 1u : 0u);
           mma_ts_mnmajor_x4(tmem + kColAcc, tmem + kColDS + 64, k_mdesc + 512, kIdescAcc, 1u);
+          // (S of this step, which also read this stage, has completed: dS
+          // was stored after dP's commit)
           tc_commit(bar(L::kAEmpty + sa));
-          if (more) {
-            // the next step's dP (this step's dP was read before its dS was
-            // stored); its commit also covers the dQ product above, which
-            // the next dS store must follow
-            ok = wait_bar(bar(L::kBFull + (it + 1) % L::kStagesB), ((it + 1) / L::kStagesB) & 1u,
-                          ctl, kSiteMmaV);
-            if (!ok) break;
-            tc_fence_after_sync();
-            issue_dp(it + 1);
-            if (n + 2 == w.n1) tc_commit(bar(L::kFixEmpty));
-          }
         }
         if (!ok) break;
         tc_commit(bar(L::kAccDone));
@@ -789,7 +868,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait_drain(bar(L::kDrain), 0, p.timeout_ns);
     }
     __syncwarp();
-  } else {
+  } else if (warp < kEwThreads / 32) {
     // ------------------------------------------------ dS and the epilogue
     const int half = warp / 4;              // key columns [64 half, +64)
     const int t = (warp % 4) * 32 + lane;   // query row within the tile == lane
@@ -836,6 +915,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after_sync();
         uint32_t dpr[64];
         tmem_ld_2x32_sync(tDP + c, dpr, tDP + c + 32, dpr + 32);
+        tc_fence_before_sync();
+        mbar_arrive(bar(L::kDPRead));
+        // the previous step's dQ product read dS: wait for its commit (also
+        // keeps this store from running ahead of the dQ issuer)
+        if (it > 0) {
+          ok = wait_bar(bar(L::kAEmpty + (it - 1) % L::kStagesA), ((it - 1) / L::kStagesA) & 1u,
+                        ctl, kSiteSoftmaxS);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          tc_fence_after_sync();
+        }
         ds_half<BF16, false>(dpr, tmem + lane_base + kColDS + c, c, nullptr, ndsum, pv);
         tmem_wait_st();
         tc_fence_before_sync();
@@ -848,9 +938,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after_sync();
       // dQ row i of head bh ([B*H][N][d], or packed [total][H][d])
-      const long long qrow = PACKED ? (static_cast<long long>(w.row_base) + i) * p.H + w.bh % p.H
-                                    : static_cast<long long>(w.bh) * p.N + i;
-      uint16_t* dst = p.dq + qrow * D + half * (D / 2);
+      const int i_warp = w.m * 128 + (warp % 4) * 32;  // query of lane 0's row
 #pragma unroll 1
       for (int c0 = 0; c0 < D / 2; c0 += 32) {
         uint32_t r[32];
@@ -860,12 +948,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 16; ++e)
           w4[e] = pack2<BF16>(__uint_as_float(r[2 * e]) * p.scale,
                               __uint_as_float(r[2 * e + 1]) * p.scale);
-        if (i < w.len) {
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4)
-            *reinterpret_cast<uint4*>(dst + c0 + q4 * 8) =
-                make_uint4(w4[4 * q4], w4[4 * q4 + 1], w4[4 * q4 + 2], w4[4 * q4 + 3]);
-        }
+        store_rows_x32(w4, lane, [&](int rl) -> uint16_t* {
+          const int ir = i_warp + rl;
+          if (ir >= w.len) return nullptr;
+          const long long qrow = PACKED
+                                     ? (static_cast<long long>(w.row_base) + ir) * p.H + w.bh % p.H
+                                     : static_cast<long long>(w.bh) * p.N + ir;
+          return p.dq + qrow * D + half * (D / 2) + c0;
+        });
       }
       tc_fence_before_sync();
       mbar_arrive(bar(L::kAccFree));
