@@ -879,14 +879,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = p.scale_log2;
     uint32_t it = 0, units = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
-      const QUnit w = decode_q_unit<CAUSAL, PACKED>(u, p);
-      if (w.n1 == w.n0) continue;
+    // the first unit at or after u with key tiles to visit (num_units: none)
+    auto next_unit = [&](int u, QUnit& w) -> int {
+      for (; u < p.num_units; u += gridDim.x) {
+        w = decode_q_unit<CAUSAL, PACKED>(u, p);
+        if (w.n1 != w.n0) break;
+      }
+      return u;
+    };
+    // this thread's -LSE2 and -D of unit w
+    auto row_values = [&](const QUnit& w, float& nl, float& nd) {
+      const long long vrow = static_cast<long long>(w.bh) * p.n_pad + w.m * 128 + t;
+      nl = p.lse2[vrow];
+      nd = p.dsum[vrow];
+    };
+    QUnit w{};
+    int u = next_unit(blockIdx.x, w);
+    float nlse2 = 0.f, ndsum = 0.f;
+    if (u < p.num_units) row_values(w, nlse2, ndsum);
+    while (u < p.num_units && ok) {
       const uint32_t uix = units++;
       const int i = w.m * 128 + t;
-      const long long vrow = static_cast<long long>(w.bh) * p.n_pad + i;
-      const float nlse2 = p.lse2[vrow];
-      const float ndsum = p.dsum[vrow];
       const int row_end = min(w.len, w.m * 128 + 128);
       for (int n = w.n0; n < w.n1; ++n, ++it) {
         const uint32_t ph = it & 1u;
@@ -932,6 +945,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(bar(L::kDSStored));
       }
       if (!ok) break;
+      // the next unit's row values, loaded before this unit's epilogue
+      QUnit wn{};
+      const int un = next_unit(u + static_cast<int>(gridDim.x), wn);
+      float nl_next = 0.f, nd_next = 0.f;
+      if (un < p.num_units) row_values(wn, nl_next, nd_next);
       // ---- epilogue: scale * dQ, columns [D/2 half, +D/2) of this thread's row
       ok = wait_bar(bar(L::kAccDone), uix & 1u, ctl, kSiteEpilogueO);
       ok = __all_sync(0xffffffffu, ok);
@@ -959,6 +977,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before_sync();
       mbar_arrive(bar(L::kAccFree));
+      u = un;
+      w = wn;
+      nlse2 = nl_next;
+      ndsum = nd_next;
     }
   }
 
