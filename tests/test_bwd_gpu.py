@@ -86,6 +86,26 @@ def test_persistent_loop(fa, ctas):
     _check(got, ref, f"ctas={ctas}")
 
 
+@pytest.mark.parametrize("ctas", [1, 2, 5])
+@pytest.mark.parametrize("d,H,H_kv,N,causal,window", [
+    (128, 4, 2, 700, False, (-1, -1)),   # units spanning two query heads
+    (64, 4, 1, 513, True, (-1, -1)),     # d = 64, four query heads per unit
+    (128, 2, 2, 600, True, (0, 0)),      # one-step units (diagonal only)
+    (128, 2, 1, 900, False, (100, 50)),  # banded: units of two or three steps
+])
+def test_many_units_per_cta(fa, ctas, d, H, H_kv, N, causal, window):
+    """Every CTA walks many units: the per-step barriers, the unit tiles and
+    the rings carry their phases across unit boundaries, and the pipelines run
+    ahead into the next unit."""
+    fa.fa_set_max_ctas(ctas)
+    try:
+        got, ref = _case(fa, 1, H, H_kv, N, d, torch.bfloat16, causal, window,
+                         seed=70 + ctas + d + H_kv)
+    finally:
+        fa.fa_set_max_ctas(0)
+    _check(got, ref, f"ctas={ctas} d={d} H={H}/{H_kv} N={N} causal={causal} window={window}")
+
+
 def test_deterministic(fa):
     """No atomics: repeated launches give identical bits."""
     q, k, v = (t.cuda() for t in make_random_qkv(2, 4, 1000, 128, torch.bfloat16, seed=60))

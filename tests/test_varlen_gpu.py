@@ -238,6 +238,19 @@ def test_backward_windows(fa, window):
     _bwd_check(fa, [700, 3, 260], 2, 2, 128, False, window, seed=670)
 
 
+@pytest.mark.parametrize("ctas", [1, 4])
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+def test_backward_ragged_many_units_per_cta(fa, ctas, causal):
+    """A small grid walks every (sequence, head) unit of a ragged batch,
+    including the empty units of short and empty sequences."""
+    fa.fa_set_max_ctas(ctas)
+    try:
+        _bwd_check(fa, [1, 127, 300, 0, 129, 513, 260], 4, 2, 128, causal, (-1, -1),
+                   seed=690 + ctas)
+    finally:
+        fa.fa_set_max_ctas(0)
+
+
 def test_backward_equal_lengths_equal_the_batched_backward(fa):
     """Equal-length packed sequences give fa_bwd's gradients bit for bit."""
     N, d = 256, 128
