@@ -58,7 +58,8 @@
 //   Q_0, Q_1       [D/64][128 rows][64]   one tile each
 //   K/V ring       STAGES slots of [D/64][128 keys][64]
 //   O staging      one tile, shared by the two query tiles in turn (TMA
-//                  store source)
+//                  store source; packed batches store O from the softmax
+//                  threads instead)
 //   mbarriers
 //
 // Online softmax in the log2 domain (scale folded into scale*log2 e, as the
@@ -221,13 +222,13 @@ __device__ __forceinline__ Unit decode_unit(int u, const FaParams& p) {
 }
 
 // Whether tile g of unit w goes through the staging tile and a TMA store:
-// every tile with keys, except (packed batches) a sequence's partial last
-// tile, which the softmax threads store row by row.
+// every tile with keys of the dense layout.  Packed batches store their
+// tiles from the softmax threads (a coalesced row store per warp), which
+// measured faster there than the shared staging tile.
 template <bool PACKED>
 __device__ __forceinline__ bool staged_tile(const FaParams& p, const Unit& w, int g) {
-  const bool valid = g ? (w.n1[1] > w.n0[1]) : (w.n1[0] > w.n0[0]);
-  if (!PACKED) return valid;
-  return valid && (w.sv.len - (g ? w.row0[1] : w.row0[0]) >= (kBlockM >> p.gqa_log2));
+  (void)p;
+  return !PACKED && (g ? (w.n1[1] > w.n0[1]) : (w.n1[0] > w.n0[0]));
 }
 
 // Maximum of a row of scores: four independent chains.
@@ -618,8 +619,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
     for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
       const Unit w = decode_unit<CAUSAL, PACKED>(u, p);
-      // the staging tile is used by tile 0 then tile 1 of each unit (the
-      // partial last tiles of packed sequences are written directly)
+      // the staging tile is used by tile 0 then tile 1 of each unit (tiles of
+      // packed batches are written directly)
       const bool staged0 = staged_tile<PACKED>(p, w, 0), staged1 = staged_tile<PACKED>(p, w, 1);
       const uint32_t my_store = n_stores + ((g == 1 && staged0) ? 1u : 0u);
       n_stores += (staged0 ? 1u : 0u) + (staged1 ? 1u : 0u);
@@ -748,10 +749,29 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             (l > 0.f) ? (m_ref + log2f(l) - (FP8 ? kFp8POffset : 0.f)) * 0.6931471805599453f
                       : -INFINITY;
       }
-      if (!(g ? staged1 : staged0)) {
-        // the last tile of a packed sequence, whose 128-row TMA box would
-        // run into the next sequence's rows: each thread stores its own row
-        // (16-byte stores); no staging, no store warp
+      if constexpr (PACKED) {
+        // a packed tile (whose 128-row TMA box could run into the next
+        // sequence's rows): the warp stores its rows itself, 64 contiguous
+        // bytes per row and store; no staging, no store warp
+        const int t_warp = t & ~31;  // tile row of lane 0
+#pragma unroll
+        for (int c0 = 0; c0 < D / 2; c0 += 16) {  // 16 packed words = 32 columns
+          uint32_t w16[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) w16[e] = pk[c0 + e];
+          store_rows_x32(w16, threadIdx.x & 31, [&](int rl) -> uint16_t* {
+            const int tr = t_warp + rl;
+            const int r_row = t_row0 + (tr >> gq);
+            if (r_row >= len) return nullptr;
+            const int r_head = w.sv.o_head + (tr & ((1 << gq) - 1));
+            return p.o_ptr +
+                   ((static_cast<long long>(w.sv.row_base) + r_row) * p.H + r_head) * D + 2 * c0;
+          });
+        }
+        continue;
+      } else if (!(g ? staged1 : staged0)) {
+        // (dense layout: every tile with keys is staged; a tile that is not
+        // is stored row by row)
         if (row < len) {
           uint4* dst = reinterpret_cast<uint4*>(
               p.o_ptr + ((static_cast<long long>(w.sv.row_base) + row) * p.H + o_head) * D);
@@ -778,8 +798,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   } else if (warp == kStoreWarp) {
     regs_decrease<kControlRegs>();
     // ------------------------------------------------------------ O store
-    // Lane 0 waits and issues the TMA store of each staged tile (the partial
-    // last tiles of packed sequences are stored by the softmax threads).
+    // Lane 0 waits and issues the TMA store of each staged tile (tiles of
+    // packed batches are stored by the softmax threads).
     uint32_t full_par = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < p.num_units && ok && lane == 0; u += gridDim.x) {
