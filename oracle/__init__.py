@@ -104,6 +104,10 @@ def _bind(path: str):
     lib.attn_ref_bwd_u16.argtypes = [vp, vp, vp, vp, c_int, c_long, c_long, c_long, c_long,
                                      c_long, c_double, c_int, c_long, c_long, vp, vp, vp, c_int]
     lib.attn_ref_bwd_u16.restype = c_int
+    lib.attn_ref_bwd_qk_u16.argtypes = [vp, vp, vp, vp, c_int, c_long, c_long, c_long, c_long,
+                                        c_long, c_long, c_double, c_int, c_long, c_long, vp, vp,
+                                        vp, c_int]
+    lib.attn_ref_bwd_qk_u16.restype = c_int
     lib.attn_ref_e4m3.argtypes = [ctypes.c_uint8]
     lib.attn_ref_e4m3.restype = c_double
     lib.attn_ref_fwd_fp8.argtypes = [vp, vp, vp, c_long, c_long, c_long, c_long, c_long,
@@ -370,6 +374,40 @@ def attention_bwd(q, k, v, dout, scale: float, causal: bool, window_left: int = 
                                   _ptr(dv), int(nthreads))
     if rc != 0:
         raise RuntimeError("oracle attn_ref_bwd_u16 failed")
+    return dq, dk, dv
+
+
+def attention_bwd_qk(q, k, v, dout, scale: float, causal: bool, window_left: int = -1,
+                     window_right: int = -1, nthreads: int = 0):
+    """Gradients of attention with Nq query rows and Nk key rows per head:
+    q, dout [B,H,Nq,d], k, v [B,H_kv,Nk,d]; dQ [B,H,Nq,d], dK, dV [B,H_kv,Nk,d]
+    (float64).  Masks and windows are aligned bottom-right (query i at key
+    position i + Nk - Nq, the shift of the backward page's masking loops); a
+    query row that sees no key contributes nothing and gets dQ = 0."""
+    qw, is_bf16 = _u16_view(q)
+    kw, kb = _u16_view(k)
+    vw, vb = _u16_view(v)
+    gw, gb = _u16_view(dout)
+    if not (is_bf16 == kb == vb == gb):
+        raise TypeError("q, k, v, dout must share one dtype")
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("expected [B,H,N,d] tensors")
+    B, H, Nq, d = (int(x) for x in q.shape)
+    _, H_kv, Nk, dk_ = (int(x) for x in k.shape)
+    if (tuple(v.shape) != tuple(k.shape) or int(k.shape[0]) != B or dk_ != d or H_kv < 1
+            or H % H_kv != 0):
+        raise ValueError("k and v must be [B,H_kv,Nk,d] with H a multiple of H_kv")
+    if tuple(dout.shape) != tuple(q.shape):
+        raise ValueError("dout must have q's shape")
+    dq = np.empty((B, H, Nq, d), dtype=np.float64)
+    dk = np.empty((B, H_kv, Nk, d), dtype=np.float64)
+    dv = np.empty((B, H_kv, Nk, d), dtype=np.float64)
+    rc = _load().attn_ref_bwd_qk_u16(_ptr(qw), _ptr(kw), _ptr(vw), _ptr(gw), int(is_bf16), B,
+                                     H, H_kv, Nq, Nk, d, float(scale), int(bool(causal)),
+                                     int(window_left), int(window_right), _ptr(dq), _ptr(dk),
+                                     _ptr(dv), int(nthreads))
+    if rc != 0:
+        raise RuntimeError("oracle attn_ref_bwd_qk_u16 failed")
     return dq, dk, dv
 
 

@@ -43,9 +43,10 @@
  * FP8 inputs (attn_ref_fwd_fp8): E4M3 bytes times one descale factor per
  * tensor, decoded exactly here; then the same definition.
  *
- * Backward (attn_ref_bwd_u16): the gradients dQ, dK, dV of the definition
- * above against dO, as the same backward page computes them (P, dP, the row
- * sums D_i = sum_j P_ij dP_ij, dS = P (dP - D)), in double.
+ * Backward (attn_ref_bwd_u16, and attn_ref_bwd_qk_u16 for separate query and
+ * key lengths, bottom-right aligned): the gradients dQ, dK, dV of the
+ * definition above against dO, as the same backward page computes them (P,
+ * dP, the row sums D_i = sum_j P_ij dP_ij, dS = P (dP - D)), in double.
  *
  * Variable-length batches (attn_ref_varlen_u16): sequences of different
  * lengths packed along the rows of [total][H][d] tensors, sequence b being
@@ -545,56 +546,64 @@ int attn_ref_varlen_u16(const uint16_t *q, const uint16_t *k,
  * with s_ij and LSE_i those of the forward definition above (recomputed here
  * in double from the 16-bit inputs).  With grouped heads, dK and dV of a K/V
  * head sum over the query heads that read it.
- *   q, dout, dq : [B][H][N][d];  k, v, dk, dv : [B][H_kv][N][d]
+ *
+ * attn_ref_bwd_qk_u16 takes Nq query rows and Nk key rows per (b, h), with
+ * the masks aligned bottom-right as the backward page's masking loops shift
+ * them by seqlen_k - seqlen_q (query i at key position i + Nk - Nq, as the
+ * forward's attn_ref_varlen_qk_u16); a query row that sees no key has P = 0
+ * in every column, so its dQ row is 0 and it adds nothing to dK, dV.
+ *   q, dout, dq : [B][H][Nq][d];  k, v, dk, dv : [B][H_kv][Nk][d]
  * Pass 1 (rows i in parallel): LSE_i, D_i and dQ_i.  Pass 2 (keys j in
  * parallel): dK_j and dV_j from the stored LSE_i and D_i.
  */
-int attn_ref_bwd_u16(const uint16_t *q, const uint16_t *k, const uint16_t *v,
-                     const uint16_t *dout, int is_bf16, long B, long H, long H_kv,
-                     long N, long d, double scale, int causal, long wl, long wr,
-                     double *dq, double *dk, double *dv, int nthreads) {
+int attn_ref_bwd_qk_u16(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                        const uint16_t *dout, int is_bf16, long B, long H, long H_kv,
+                        long Nq, long Nk, long d, double scale, int causal, long wl,
+                        long wr, double *dq, double *dk, double *dv, int nthreads) {
     if (!q || !k || !v || !dout || !dq || !dk || !dv || B < 0 || H <= 0 ||
-        H_kv <= 0 || H % H_kv != 0 || N < 0 || d <= 0)
+        H_kv <= 0 || H % H_kv != 0 || Nq < 0 || Nk < 0 || d <= 0)
         return -1;
     set_threads(nthreads);
-    long slice = N * d, group = H / H_kv, cap = slice > 0 ? slice : 1;
-    double *kd = (double *)malloc(sizeof(double) * (size_t)cap);
-    double *vd = (double *)malloc(sizeof(double) * (size_t)cap);
-    double *qd = (double *)malloc(sizeof(double) * (size_t)(cap * group));
-    double *dod = (double *)malloc(sizeof(double) * (size_t)(cap * group));
-    double *lse = (double *)malloc(sizeof(double) * (size_t)((N > 0 ? N : 1) * group));
-    double *dsum = (double *)malloc(sizeof(double) * (size_t)((N > 0 ? N : 1) * group));
+    long qslice = Nq * d, kslice = Nk * d, group = H / H_kv;
+    long qcap = qslice > 0 ? qslice : 1, kcap = kslice > 0 ? kslice : 1;
+    double *kd = (double *)malloc(sizeof(double) * (size_t)kcap);
+    double *vd = (double *)malloc(sizeof(double) * (size_t)kcap);
+    double *qd = (double *)malloc(sizeof(double) * (size_t)(qcap * group));
+    double *dod = (double *)malloc(sizeof(double) * (size_t)(qcap * group));
+    double *lse = (double *)malloc(sizeof(double) * (size_t)((Nq > 0 ? Nq : 1) * group));
+    double *dsum = (double *)malloc(sizeof(double) * (size_t)((Nq > 0 ? Nq : 1) * group));
     if (!kd || !vd || !qd || !dod || !lse || !dsum) {
         free(kd); free(vd); free(qd); free(dod); free(lse); free(dsum);
         return -1;
     }
+    const long shift = Nk - Nq;  /* key position of query row i: i + shift */
     int rc = 0;
     for (long b = 0; b < B && rc == 0; ++b) {
         for (long hk = 0; hk < H_kv && rc == 0; ++hk) {
             long bkv = b * H_kv + hk;
-            widen_slice(k + bkv * slice, kd, slice, is_bf16);
-            widen_slice(v + bkv * slice, vd, slice, is_bf16);
+            widen_slice(k + bkv * kslice, kd, kslice, is_bf16);
+            widen_slice(v + bkv * kslice, vd, kslice, is_bf16);
             for (long g = 0; g < group; ++g) {
                 long bh = b * H + hk * group + g;
-                widen_slice(q + bh * slice, qd + g * slice, slice, is_bf16);
-                widen_slice(dout + bh * slice, dod + g * slice, slice, is_bf16);
+                widen_slice(q + bh * qslice, qd + g * qslice, qslice, is_bf16);
+                widen_slice(dout + bh * qslice, dod + g * qslice, qslice, is_bf16);
             }
             /* pass 1: per query row i of every head of the group */
 #pragma omp parallel
             {
-                double *s = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+                double *s = (double *)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
                 if (!s) {
 #pragma omp atomic write
                     rc = -1;
                 } else {
 #pragma omp for schedule(dynamic, 4)
-                    for (long gi = 0; gi < group * N; ++gi) {
-                        long g = gi / N, i = gi % N;
-                        const double *qi = qd + g * slice + i * d;
-                        const double *doi = dod + g * slice + i * d;
-                        double *dqi = dq + ((b * H + hk * group + g) * N + i) * d;
+                    for (long gi = 0; gi < group * Nq; ++gi) {
+                        long g = gi / Nq, i = gi % Nq;
+                        const double *qi = qd + g * qslice + i * d;
+                        const double *doi = dod + g * qslice + i * d;
+                        double *dqi = dq + ((b * H + hk * group + g) * Nq + i) * d;
                         long j0, j1;
-                        key_range(N, i, causal, wl, wr, &j0, &j1);
+                        key_range(Nk, i + shift, causal, wl, wr, &j0, &j1);
                         for (long c = 0; c < d; ++c) dqi[c] = 0.0;
                         if (j1 <= j0) {
                             lse[gi] = -INFINITY;
@@ -632,17 +641,17 @@ int attn_ref_bwd_u16(const uint16_t *q, const uint16_t *k, const uint16_t *v,
             if (rc != 0) break;
             /* pass 2: per key row j, summed over the group's query rows */
 #pragma omp parallel for schedule(dynamic, 4)
-            for (long j = 0; j < N; ++j) {
-                double *dkj = dk + (bkv * N + j) * d;
-                double *dvj = dv + (bkv * N + j) * d;
+            for (long j = 0; j < Nk; ++j) {
+                double *dkj = dk + (bkv * Nk + j) * d;
+                double *dvj = dv + (bkv * Nk + j) * d;
                 for (long c = 0; c < d; ++c) { dkj[c] = 0.0; dvj[c] = 0.0; }
-                for (long gi = 0; gi < group * N; ++gi) {
-                    long g = gi / N, i = gi % N;
+                for (long gi = 0; gi < group * Nq; ++gi) {
+                    long g = gi / Nq, i = gi % Nq;
                     long j0, j1;
-                    key_range(N, i, causal, wl, wr, &j0, &j1);
+                    key_range(Nk, i + shift, causal, wl, wr, &j0, &j1);
                     if (j < j0 || j >= j1) continue;
-                    const double *qi = qd + g * slice + i * d;
-                    const double *doi = dod + g * slice + i * d;
+                    const double *qi = qd + g * qslice + i * d;
+                    const double *doi = dod + g * qslice + i * d;
                     double dot = 0.0, dp = 0.0;
                     for (long c = 0; c < d; ++c) {
                         dot += qi[c] * kd[j * d + c];
@@ -660,6 +669,16 @@ int attn_ref_bwd_u16(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     }
     free(kd); free(vd); free(qd); free(dod); free(lse); free(dsum);
     return rc;
+}
+
+/* Equal query and key lengths (the bottom-right alignment is the plain
+ * diagonal):  q, dout, dq : [B][H][N][d];  k, v, dk, dv : [B][H_kv][N][d]. */
+int attn_ref_bwd_u16(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                     const uint16_t *dout, int is_bf16, long B, long H, long H_kv,
+                     long N, long d, double scale, int causal, long wl, long wr,
+                     double *dq, double *dk, double *dv, int nthreads) {
+    return attn_ref_bwd_qk_u16(q, k, v, dout, is_bf16, B, H, H_kv, N, N, d, scale, causal,
+                               wl, wr, dq, dk, dv, nthreads);
 }
 
 /*

@@ -707,6 +707,76 @@ def test_bwd_sum_identities(causal, window):
     assert np.abs(dq).max() > 1e-3
 
 
+def _torch_attention_qk_f64(q, k, v, scale, causal, window):
+    """Reference forward in torch float64 for Nq query and Nk key rows, masks
+    aligned bottom-right (query i at key position i + Nk - Nq); a row without
+    keys outputs 0 (its softmax runs unmasked and is multiplied by 0, so
+    autograd sees no NaN)."""
+    Nq, Nk = q.shape[-2], k.shape[-2]
+    group = q.shape[1] // k.shape[1]
+    pos = torch.arange(Nq)[:, None] + (Nk - Nq)
+    j = torch.arange(Nk)[None, :]
+    allowed = torch.ones(Nq, Nk, dtype=torch.bool)
+    if causal:
+        allowed &= j <= pos
+    if window[0] >= 0:
+        allowed &= j >= pos - window[0]
+    if window[1] >= 0:
+        allowed &= j <= pos + window[1]
+    has_key = allowed.any(-1, keepdim=True)
+    allowed = allowed | ~has_key
+    kr = k.repeat_interleave(group, 1)
+    vr = v.repeat_interleave(group, 1)
+    s = scale * q @ kr.transpose(-1, -2)
+    p = torch.softmax(s.masked_fill(~allowed, float("-inf")), -1) * has_key
+    return p @ vr
+
+
+@pytest.mark.parametrize("Nq,Nk", [(9, 23), (23, 9), (1, 30), (17, 17)])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("window", [(-1, -1), (4, 2)])
+def test_bwd_qk_matches_torch_autograd(Nq, Nk, causal, window):
+    """Separate query and key lengths: dQ, dK, dV equal torch float64
+    autograd through the bottom-right masked softmax attention."""
+    q, _, _ = make_random_qkv(1, 4, Nq, 16, torch.bfloat16, seed=730 + Nq)
+    _, k, v = make_random_qkv(1, 2, Nk, 16, torch.bfloat16, seed=731 + Nk)
+    do = torch.randn(q.shape, generator=torch.Generator().manual_seed(732)).to(torch.bfloat16)
+    dq, dk, dv = oracle.attention_bwd_qk(q, k, v, do, 0.3, causal, *window)
+    qd, kd, vd = (t.double().requires_grad_() for t in (q, k, v))
+    o = _torch_attention_qk_f64(qd, kd, vd, 0.3, causal, window)
+    o.backward(do.double())
+    np.testing.assert_allclose(dq, qd.grad.numpy(), rtol=0, atol=1e-11)
+    np.testing.assert_allclose(dk, kd.grad.numpy(), rtol=0, atol=1e-11)
+    np.testing.assert_allclose(dv, vd.grad.numpy(), rtol=0, atol=1e-11)
+
+
+def test_bwd_qk_keyless_rows_drop_out():
+    """Causal with more queries than keys: the first Nq - Nk rows see no key,
+    so their dQ is exactly 0 and dK, dV are those of the last Nk rows alone
+    (which then align on the plain diagonal)."""
+    Nq, Nk = 29, 12
+    q, _, _ = make_random_qkv(1, 2, Nq, 16, torch.float16, seed=740)
+    _, k, v = make_random_qkv(1, 2, Nk, 16, torch.float16, seed=741)
+    do = torch.randn(q.shape, generator=torch.Generator().manual_seed(742)).to(torch.float16)
+    dq, dk, dv = oracle.attention_bwd_qk(q, k, v, do, 0.4, True)
+    assert (dq[:, :, :Nq - Nk] == 0).all()
+    tail = lambda t: t[:, :, Nq - Nk:].contiguous()
+    dq2, dk2, dv2 = oracle.attention_bwd(tail(q), k, v, tail(do), 0.4, True)
+    np.testing.assert_allclose(dq[:, :, Nq - Nk:], dq2, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(dk, dk2, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(dv, dv2, rtol=0, atol=1e-13)
+
+
+def test_bwd_qk_equal_lengths_is_the_backward():
+    q, k, v = make_random_qkv(2, 2, 19, 8, torch.bfloat16, seed=750)
+    do = torch.randn(q.shape, generator=torch.Generator().manual_seed(751)).to(torch.bfloat16)
+    for causal, window in ((False, (-1, -1)), (True, (-1, -1)), (False, (3, 5))):
+        a = oracle.attention_bwd_qk(q, k, v, do, 0.5, causal, *window)
+        b = oracle.attention_bwd(q, k, v, do, 0.5, causal, *window)
+        for x, y in zip(a, b):
+            np.testing.assert_array_equal(x, y)
+
+
 # ------------------------------------------------------------ FP8 inputs
 def test_e4m3_decoder_exhaustive():
     """All 256 E4M3 codes decode as PyTorch's float8_e4m3fn does (NaN codes

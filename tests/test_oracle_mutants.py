@@ -56,6 +56,12 @@ MUTANTS = {
     "bwd_key_mask_ignored": ("if (j < j0 || j >= j1) continue;", "if (j < 0) continue;"),
     "bwd_dq_transposed": ("dqi[c] += scale * ds * kd[j * d + c];",
                           "dqi[c] += scale * ds * vd[j * d + c];"),
+    "bwd_qk_top_left_alignment": ("const long shift = Nk - Nq;", "const long shift = 0;"),
+    "bwd_qk_shift_sign": ("const long shift = Nk - Nq;", "const long shift = Nq - Nk;"),
+    "bwd_qk_key_pass_unshifted": ("key_range(Nk, i + shift, causal, wl, wr, &j0, &j1);\n"
+                                  "                    if (j < j0 || j >= j1) continue;",
+                                  "key_range(Nk, i, causal, wl, wr, &j0, &j1);\n"
+                                  "                    if (j < j0 || j >= j1) continue;"),
     "e4m3_bias": ("else mag = ldexp(8.0 + mant, expo - 10);",
                   "else mag = ldexp(8.0 + mant, expo - 11);"),
     "e4m3_subnormal": ("if (expo == 0) mag = ldexp((double)mant, -9);",
@@ -94,6 +100,9 @@ PIN_CALLS = [
     (pins.test_bwd_matches_torch_autograd, dict(causal=True, window=(6, 3), H=4, H_kv=2)),
     (pins.test_bwd_directional_finite_difference, dict(causal=True)),
     (pins.test_bwd_sum_identities, dict(causal=False, window=(5, 2))),
+    (pins.test_bwd_qk_matches_torch_autograd, dict(Nq=23, Nk=9, causal=True, window=(4, 2))),
+    (pins.test_bwd_qk_matches_torch_autograd, dict(Nq=9, Nk=23, causal=True, window=(-1, -1))),
+    (pins.test_bwd_qk_keyless_rows_drop_out, {}),
     (pins.test_e4m3_decoder_exhaustive, {}),
     (pins.test_fp8_matches_torch_on_decoded_inputs, dict(causal=True)),
     (pins.test_fp8_descale_folds_into_scale, {}),
