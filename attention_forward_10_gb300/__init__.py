@@ -50,6 +50,8 @@ SIGNATURES = {
     "fa_bwd_workspace_bytes": ([_i, _i, _i, ctypes.POINTER(_ull)], _i),
     "fa_bwd_varlen": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i,
                        _f, _i, _i, _i, _i, _vp, _ull, _vp], _i),
+    "fa_bwd_varlen_qk": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i,
+                          _i, _i, _i, _i, _i, _i, _i, _f, _i, _i, _i, _i, _vp, _ull, _vp], _i),
     "fa_fwd_varlen": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _i, _i,
                        _vp], _i),
     "fa_fwd_varlen_qk": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i,
@@ -167,6 +169,19 @@ def fa_bwd_varlen(q: int, k: int, v: int, o: int, lse: int, dout: int, dq: int, 
                                   max_seqlen, total, H, H_kv, d, scale, causal, window_left,
                                   window_right, dtype, workspace or None, int(workspace_bytes),
                                   stream or None))
+
+
+def fa_bwd_varlen_qk(q: int, k: int, v: int, o: int, lse: int, dout: int, dq: int, dk: int,
+                     dv: int, cu_seqlens_q: int, cu_seqlens_k: int, seqused_q: int | None,
+                     seqused_k: int | None, batch: int, max_seqlen_q: int, max_seqlen_k: int,
+                     total_q: int, total_k: int, H: int, H_kv: int, d: int, scale: float,
+                     causal: int, window_left: int, window_right: int, dtype: int,
+                     workspace: int | None, workspace_bytes: int, stream: int | None) -> int:
+    return int(_lib.fa_bwd_varlen_qk(q, k, v, o, lse, dout, dq, dk, dv, cu_seqlens_q or None,
+                                     cu_seqlens_k or None, seqused_q or None, seqused_k or None,
+                                     batch, max_seqlen_q, max_seqlen_k, total_q, total_k, H,
+                                     H_kv, d, scale, causal, window_left, window_right, dtype,
+                                     workspace or None, int(workspace_bytes), stream or None))
 
 
 def fa_bwd_workspace_bytes(B: int, H: int, N: int) -> tuple[int, int]:
@@ -586,6 +601,45 @@ def bwd_varlen(q, k, v, o, lse, dout, cu_seqlens, max_seqlen: int, *,
     return dq, dk, dv
 
 
+def bwd_varlen_qk(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
+                  max_seqlen_k: int, *, seqused_q=None, seqused_k=None,
+                  scale: float | None = None, causal: bool = False,
+                  window: tuple[int, int] = (-1, -1), workspace=None, stream=None):
+    """Gradients (dq, dk, dv) of ``fwd_varlen_qk``: q, o, dout [total_q, H, d],
+    k, v [total_k, H_kv, d], lse [H, total_q]; separate query and key offsets
+    (int32 CUDA tensors of batch + 1 entries) and optional used lengths.
+    Rows past the used lengths are left as torch.empty_like made them."""
+    import torch
+    total_q, H, d = (int(x) for x in q.shape)
+    total_k = int(k.shape[0])
+    batch = int(cu_seqlens_q.numel()) - 1
+    if int(cu_seqlens_k.numel()) != batch + 1:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must have the same length")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    with torch.cuda.device(q.device):
+        st, need = fa_bwd_workspace_bytes(max(batch, 0), H, int(max_seqlen_q))
+        if st != FA_OK:
+            raise FaError(st, "fa_bwd_workspace_bytes")
+        if workspace is None:
+            workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+        st = fa_bwd_varlen_qk(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+            dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), cu_seqlens_q.data_ptr(),
+            cu_seqlens_k.data_ptr(), seqused_q.data_ptr() if seqused_q is not None else None,
+            seqused_k.data_ptr() if seqused_k is not None else None, max(batch, 0),
+            int(max_seqlen_q), int(max_seqlen_k), total_q, total_k, H, int(k.shape[1]), d,
+            float(scale), int(bool(causal)), int(window[0]), int(window[1]), _dtype_code(q),
+            workspace.data_ptr(), workspace.numel(), handle)
+    if st != FA_OK:
+        raise FaError(st, "fa_bwd_varlen_qk")
+    return dq, dk, dv
+
+
 def fwd_splitkv(q, k, v, *, num_splits: int = 0, scale: float | None = None,
                 causal: bool = False, window: tuple[int, int] = (-1, -1), out=None,
                 lse=None, return_lse: bool = True, workspace=None, stream=None):
@@ -624,7 +678,8 @@ def fwd_splitkv(q, k, v, *, num_splits: int = 0, scale: float | None = None,
 __all__ = [
     "LIB_PATH", "SIGNATURES", "FaError", "fwd", "bwd", "fwd_fp8", "fwd_varlen", "fwd_splitkv",
     "fa_fwd", "fa_fwd_fp8", "fa_fwd_fp8_workspace_bytes",
-    "fa_bwd", "fa_bwd_workspace_bytes", "fa_bwd_varlen", "bwd_varlen",
+    "fa_bwd", "fa_bwd_workspace_bytes", "fa_bwd_varlen", "bwd_varlen", "fa_bwd_varlen_qk",
+    "bwd_varlen_qk",
     "fa_fwd_ext", "fa_fwd_varlen",
     "fa_fwd_splitkv", "fa_splitkv_workspace_bytes", "fa_fwd_splitkv_noalloc",
     "fa_status_string",

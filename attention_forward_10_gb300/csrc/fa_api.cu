@@ -1073,23 +1073,41 @@ int fa_bwd_workspace_bytes(int B, int H, int N, unsigned long long* bytes) {
 namespace fa {
 namespace {
 
-// fa_bwd and fa_bwd_varlen: B sequences of N rows ([B][H][N][d]), or, with
-// cu_seqlens, B packed sequences of at most N rows ([total][H][d]).
+// The packed-batch arguments of a backward launch (all nullptr / 0 for the
+// [B][H][N][d] layout): query offsets and rows, key offsets and rows (the
+// query ones for self-attention), used lengths, the longest key length.
+struct BwdPacked {
+  const int* cu_q = nullptr;
+  const int* cu_k = nullptr;
+  const int* used_q = nullptr;
+  const int* used_k = nullptr;
+  int total_q = 0, total_k = 0, N_k = 0;
+};
+
+// fa_bwd and fa_bwd_varlen(_qk): B sequences of N rows ([B][H][N][d]), or,
+// with cu_q, B packed sequences of at most N query and N_k key rows.
 int bwd_launch(const void* q, const void* k, const void* v, const void* o, const float* lse,
                const void* dout, void* dq, void* dk, void* dv, void* workspace,
                unsigned long long workspace_bytes, int B, int H, int H_kv, int N, int d,
                float scale, int causal, int window_left, int window_right, int dtype,
-               void* stream, const int* cu_seqlens, int total) {
+               void* stream, const BwdPacked& pk) {
+  const int* cu_seqlens = pk.cu_q;
+  const int total = pk.total_q;
   const ForwardCall c{q, k, v, dq, nullptr, B, H, H_kv, N, d, scale, causal, window_left,
                       window_right, dtype, stream};
   int st = validate(c);
   if (st != FA_OK) return st;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   const bool packed = cu_seqlens != nullptr;
-  if (packed && total < 0) return FA_ERR_INVALID_ARG;
+  if (packed && (total < 0 || pk.total_k < 0 || pk.N_k < 0 || pk.cu_k == nullptr))
+    return FA_ERR_INVALID_ARG;
   if (empty_problem(c) || (packed && total == 0)) return FA_OK;
   st = check_pointers(c);
   if (st != FA_OK) return st;
+  if (packed && (!aligned(pk.cu_k, 4) || !aligned(pk.used_q, 4) || !aligned(pk.used_k, 4)))
+    return FA_ERR_MISALIGNED;
+  const int N_k = packed ? pk.N_k : N;
+  const int total_k = packed ? pk.total_k : 0;
   if (o == nullptr || lse == nullptr || dout == nullptr || dk == nullptr || dv == nullptr ||
       workspace == nullptr)
     return FA_ERR_INVALID_ARG;
@@ -1101,7 +1119,9 @@ int bwd_launch(const void* q, const void* k, const void* v, const void* o, const
   if (workspace_bytes < need) return FA_ERR_INVALID_ARG;
   const long long bh = static_cast<long long>(B) * H;
   const long long n_tiles = (static_cast<long long>(N) + 127) / 128;
-  if (bh * n_tiles >= (1ll << 31)) return FA_ERR_INVALID_ARG;
+  const long long n_tiles_k = (static_cast<long long>(N_k) + 127) / 128;
+  if (bh * n_tiles >= (1ll << 31) || static_cast<long long>(B) * H_kv * n_tiles_k >= (1ll << 31))
+    return FA_ERR_INVALID_ARG;
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
@@ -1113,9 +1133,15 @@ int bwd_launch(const void* q, const void* k, const void* v, const void* o, const
   const int ibh = static_cast<int>(bh), ibkv = B * H_kv;
   BwdParams p;
   if (packed) {
+    // (no key rows at all: the K/V maps view the query memory; every key
+    // tile is then empty and nothing reads through them)
+    const void* kb = total_k > 0 ? k : q;
+    const void* vb = total_k > 0 ? v : q;
+    const int k_rows = total_k > 0 ? total_k : total;
+    const int kv_heads = total_k > 0 ? H_kv : H;
     if (!encode_packed_map(&p.tm_q, q, total, H, d, bf16, 128, d / 64) ||
-        !encode_packed_map(&p.tm_k, k, total, H_kv, d, bf16, 128, d / 64) ||
-        !encode_packed_map(&p.tm_v, v, total, H_kv, d, bf16, 128, d / 64) ||
+        !encode_packed_map(&p.tm_k, kb, k_rows, kv_heads, d, bf16, 128, d / 64) ||
+        !encode_packed_map(&p.tm_v, vb, k_rows, kv_heads, d, bf16, 128, d / 64) ||
         !encode_packed_map(&p.tm_do, dout, total, H, d, bf16, 128, d / 64))
       return FA_ERR_CUDA;
   } else if (!encode_qkvo_map(&p.tm_q, q, N, d, ibh, bf16, 128, d / 64) ||
@@ -1142,15 +1168,23 @@ int bwd_launch(const void* q, const void* k, const void* v, const void* o, const
   p.H = H;
   p.H_kv = H_kv;
   p.group = H / H_kv;
-  p.win_left = (window_left < 0 || window_left > N) ? N : window_left;
-  p.win_right = (window_right < 0 || window_right > N) ? N : window_right;
+  // (an unbounded window reaches every key: N + N_k covers any shift)
+  const int unbounded = N + N_k;
+  p.win_left = (window_left < 0 || window_left > unbounded) ? unbounded : window_left;
+  p.win_right = (window_right < 0 || window_right > unbounded) ? unbounded : window_right;
   if (causal) p.win_right = 0;
   p.scale = scale;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.cu_seqlens = cu_seqlens;
+  p.cu_seqlens_k = packed ? pk.cu_k : nullptr;
+  p.seqused_q = packed ? pk.used_q : nullptr;
+  p.seqused_k = packed ? pk.used_k : nullptr;
   p.total_rows = packed ? total : 0;
+  p.total_rows_k = total_k;
+  p.N_k = N_k;
+  p.n_tiles_k = static_cast<int>(n_tiles_k);
   BwdParams p_kv = p, p_q = p;
-  p_kv.num_units = static_cast<int>(static_cast<long long>(ibkv) * n_tiles);
+  p_kv.num_units = static_cast<int>(static_cast<long long>(ibkv) * n_tiles_k);
   p_q.num_units = static_cast<int>(bh * n_tiles);
   int grid = info->num_sms;
   const int cap = g_max_ctas.load();
@@ -1178,7 +1212,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
            void* stream) {
   return fa::bwd_launch(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, B, H,
                         H_kv, N, d, scale, causal, window_left, window_right, dtype, stream,
-                        nullptr, 0);
+                        fa::BwdPacked{});
 }
 
 int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -1193,9 +1227,46 @@ int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, co
     if (batch < 0 || H < 0 || max_seqlen < 0 || total < 0) return FA_ERR_INVALID_ARG;
     return FA_OK;
   }
+  fa::BwdPacked pk;
+  pk.cu_q = cu_seqlens;
+  pk.cu_k = cu_seqlens;
+  pk.total_q = total;
+  pk.total_k = total;
+  pk.N_k = max_seqlen;
   return fa::bwd_launch(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, batch,
                         H, H_kv, max_seqlen, d, scale, causal, window_left, window_right, dtype,
-                        stream, cu_seqlens, total);
+                        stream, pk);
+}
+
+int fa_bwd_varlen_qk(const void* q, const void* k, const void* v, const void* o,
+                     const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                     const int* cu_seqlens_q, const int* cu_seqlens_k, const int* seqused_q,
+                     const int* seqused_k, int batch, int max_seqlen_q, int max_seqlen_k,
+                     int total_q, int total_k, int H, int H_kv, int d, float scale, int causal,
+                     int window_left, int window_right, int dtype, void* workspace,
+                     unsigned long long workspace_bytes, void* stream) {
+  if (batch < 0 || H < 0 || max_seqlen_q < 0 || max_seqlen_k < 0 || total_q < 0 || total_k < 0)
+    return FA_ERR_INVALID_ARG;
+  // positions and window bounds stay far from int overflow
+  if (max_seqlen_q >= (1 << 30) || max_seqlen_k >= (1 << 30)) return FA_ERR_INVALID_ARG;
+  if (batch == 0 || H == 0 || max_seqlen_q == 0 || total_q == 0) {
+    // nothing to do; the shared checks of the other arguments still apply
+    return fa::bwd_launch(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, batch,
+                          H, H_kv, max_seqlen_q, d, scale, causal, window_left, window_right,
+                          dtype, stream, fa::BwdPacked{});
+  }
+  if (cu_seqlens_q == nullptr || cu_seqlens_k == nullptr) return FA_ERR_INVALID_ARG;
+  fa::BwdPacked pk;
+  pk.cu_q = cu_seqlens_q;
+  pk.cu_k = cu_seqlens_k;
+  pk.used_q = seqused_q;
+  pk.used_k = seqused_k;
+  pk.total_q = total_q;
+  pk.total_k = total_k;
+  pk.N_k = max_seqlen_k;
+  return fa::bwd_launch(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, batch,
+                        H, H_kv, max_seqlen_q, d, scale, causal, window_left, window_right,
+                        dtype, stream, pk);
 }
 
 int fa_fwd_fp8_workspace_bytes(int B, int H_kv, int N, int d, unsigned long long* bytes) {

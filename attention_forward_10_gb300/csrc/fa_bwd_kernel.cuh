@@ -161,10 +161,13 @@ __device__ __forceinline__ bool smem_base_ok(uint32_t sbase, int* status) {
   return false;
 }
 
-// Masks of the backward: key j is admissible for query i when
-// i - win_left <= j <= i + win_right (causal: win_right = 0), both < N.
-__device__ __forceinline__ bool admissible(int i, int j, int N, int wl, int wr) {
-  return j < N && i < N && j <= i + wr && j >= i - wl;
+// Masks of the backward: key j is admissible for query i of a sequence with
+// len query rows and k_len key rows when i < len, j < k_len and
+// i + shift - win_left <= j <= i + shift + win_right, shift = k_len - len
+// (bottom-right alignment; causal: win_right = 0).
+__device__ __forceinline__ bool admissible(int i, int j, int len, int k_len, int shift, int wl,
+                                           int wr) {
+  return j < k_len && i < len && j <= i + shift + wr && j >= i + shift - wl;
 }
 
 // ---------------------------------------------------------------- pre-pass
@@ -217,7 +220,9 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
     for (int off = kTpr / 2; off > 0; off /= 2) acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (live && part == 0) {
-      lse2[r] = valid ? lse[lidx] * -1.4426950408889634f : -INFINITY;
+      // (a row without keys has LSE = -inf: P = 0 in every column)
+      const float lv = valid ? lse[lidx] : -INFINITY;
+      lse2[r] = lv > -INFINITY ? lv * -1.4426950408889634f : -INFINITY;
       dsum[r] = -acc;
     }
   }
@@ -286,9 +291,12 @@ struct KvUnit {
   int bkv;        // K/V head (b * H_kv + h_kv)
   int n;          // key tile
   int m_lo, nm;   // query tiles [m_lo, m_lo + nm) per query head
-  int steps;      // group * nm (0: nothing to do)
-  int row_base;   // first row of the sequence (packed batches; else 0)
-  int len;        // rows of the sequence (N unless packed)
+  int steps;      // group * nm (0: no query sees these keys)
+  int row_base;   // first query row of the sequence (packed batches; else 0)
+  int len;        // query rows of the sequence (N unless packed)
+  int k_row_base; // first key row of the sequence (packed batches; else 0)
+  int k_len;      // key rows of the sequence (N unless packed)
+  bool rows;      // the tile holds key rows of the sequence (steps 0: write zeros)
 };
 
 template <bool CAUSAL, bool PACKED>
@@ -299,16 +307,20 @@ __device__ __forceinline__ KvUnit decode_kv_unit(int u, const BwdParams& p) {
     w.n = u / p.num_bkv;
     w.bkv = u % p.num_bkv;
   } else {
-    w.bkv = u / p.n_tiles;
-    w.n = u % p.n_tiles;
+    w.bkv = u / p.n_tiles_k;
+    w.n = u % p.n_tiles_k;
   }
   bwd_sequence<PACKED>(p, w.bkv / p.H_kv, &w.row_base, &w.len);
-  const long long lo = static_cast<long long>(w.n) * 128 - p.win_right;
-  const long long hi = static_cast<long long>(w.n) * 128 + 128 + p.win_left;  // exclusive
-  const int row_lo = lo < 0 ? 0 : static_cast<int>(lo);
-  const int row_hi = hi > w.len ? w.len : static_cast<int>(hi);
+  bwd_keys<PACKED>(p, w.bkv / p.H_kv, &w.k_row_base, &w.k_len);
+  w.rows = w.n * 128 < w.k_len;
+  // key j is seen by queries j - shift - win_right .. j - shift + win_left
+  const long long shift = static_cast<long long>(w.k_len) - w.len;
+  const long long lo = static_cast<long long>(w.n) * 128 - shift - p.win_right;
+  const long long hi = static_cast<long long>(w.n) * 128 + 128 - shift + p.win_left;  // exclusive
+  const int row_lo = lo < 0 ? 0 : (lo > w.len ? w.len : static_cast<int>(lo));
+  const int row_hi = hi > w.len ? w.len : (hi < 0 ? 0 : static_cast<int>(hi));
   w.m_lo = row_lo / 128;
-  w.nm = (row_hi > row_lo && w.n * 128 < w.len) ? (row_hi + 127) / 128 - w.m_lo : 0;
+  w.nm = (row_hi > row_lo && w.rows) ? (row_hi + 127) / 128 - w.m_lo : 0;
   w.steps = p.group * w.nm;
   return w;
 }
@@ -358,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
         const KvUnit w = decode_kv_unit<CAUSAL, PACKED>(u, p);
-        if (w.steps == 0) continue;  // a key tile past a shorter sequence's end
+        if (w.steps == 0) continue;  // no key rows, or keys no query sees
         const uint32_t uix = units++;
         ok = wait_bar(bar(L::kFixEmpty), (uix & 1u) ^ 1u, ctl, kSiteProducerKV);
         if (!ok) break;
@@ -366,9 +378,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int b = w.bkv / p.H_kv, hk = w.bkv % p.H_kv;
         // (packed: rows of the sequence, heads within the row)
         const int kv_head_c = PACKED ? hk : w.bkv;
-        tma_load_4d(sbase + kKOff, &p.tm_k, bar(L::kFixFull), 0, w.row_base + w.n * 128, 0,
+        tma_load_4d(sbase + kKOff, &p.tm_k, bar(L::kFixFull), 0, w.k_row_base + w.n * 128, 0,
                     kv_head_c);
-        tma_load_4d(sbase + kVOff, &p.tm_v, bar(L::kFixFull), 0, w.row_base + w.n * 128, 0,
+        tma_load_4d(sbase + kVOff, &p.tm_v, bar(L::kFixFull), 0, w.k_row_base + w.n * 128, 0,
                     kv_head_c);
         for (int s = 0; s < w.steps && ok; ++s) {
           const int bh = b * p.H + hk * p.group + s / w.nm;
@@ -426,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
         const KvUnit w = decode_kv_unit<CAUSAL, PACKED>(u, p);
-        if (w.steps == 0) continue;  // a key tile past a shorter sequence's end
+        if (w.steps == 0) continue;  // no key rows, or keys no query sees
         const uint32_t uix = units++;
         ok = wait_bar(bar(L::kFixFull), uix & 1u, ctl, kSiteMmaK);
         // region(it) held the previous step's dP^T: wait until it was read
@@ -534,9 +546,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
       const KvUnit w = decode_kv_unit<CAUSAL, PACKED>(u, p);
-      if (w.steps == 0) continue;
+      // dV / dK rows of key tile n of K/V head bkv ([B*H_kv][N][d], or
+      // packed [total_k][H_kv][d]): 32 columns of the rows of this warp
+      const int j_warp = w.n * 128 + (warp % 4) * 32;  // key of lane 0's row
+      auto rows_at = [&](uint16_t* base, int c0) {
+        return [&, base, c0](int rl) -> uint16_t* {
+          const int jr = j_warp + rl;
+          if (jr >= w.k_len) return nullptr;
+          const long long row = PACKED ? (static_cast<long long>(w.k_row_base) + jr) * p.H_kv +
+                                             w.bkv % p.H_kv
+                                       : static_cast<long long>(w.bkv) * p.N + jr;
+          return base + row * D + c0;
+        };
+      };
+      if (w.steps == 0) {
+        // keys that no query sees (separate query and key lengths with a
+        // window): dV = dK = 0, written without the pipeline
+        if (w.rows) {
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t z[16] = {};
+            store_rows_x32(z, lane, rows_at(half == 0 ? p.dv : p.dk, c0));
+          }
+        }
+        continue;
+      }
       const uint32_t uix = units++;
       const int j = w.n * 128 + t;  // this thread's key
+      const int shift = w.k_len - w.len;  // key position of query 0
       for (int s = 0; s < w.steps; ++s, ++it) {
         const uint32_t sb = it % L::kStagesB, ph = it & 1u;
         const uint32_t x = tmem + lane_base + region(it);
@@ -550,11 +587,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float* nlse2 = reinterpret_cast<const float*>(smem + L::kVecOff + sb * 1024);
         const float* ndsum = nlse2 + 128;
         const int i0 = m * 128 + c;  // query of column c
-        const bool need_mask = (w.n * 128 + 127 - i0 > p.win_right) ||
-                               (w.n * 128 - (i0 + 63) < -p.win_left) ||
-                               (w.n * 128 + 128 > w.len);
-        const int N = w.len, wl = p.win_left, wr = p.win_right;
-        auto keep = [&](int e) { return admissible(i0 + e, j, N, wl, wr); };
+        const bool need_mask = (w.n * 128 + 127 - (i0 + shift) > p.win_right) ||
+                               (w.n * 128 - (i0 + 63 + shift) < -p.win_left) ||
+                               (w.n * 128 + 128 > w.k_len);
+        const int len = w.len, k_len = w.k_len, wl = p.win_left, wr = p.win_right;
+        auto keep = [&](int e) { return admissible(i0 + e, j, len, k_len, shift, wl, wr); };
         // phase A: P^T over the first 32 of the half's S^T columns (while
         // dP^T is computed)
         float pv[64];
@@ -592,10 +629,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after_sync();
-      // dV / dK row j of K/V head bkv ([B*H_kv][N][d], or packed [total][H_kv][d])
       uint16_t* const base = half == 0 ? p.dv : p.dk;
       const float mul = half == 0 ? 1.f : p.scale;
-      const int j_warp = w.n * 128 + (warp % 4) * 32;  // key of lane 0's row
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t r[32];
@@ -604,14 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e)
           w4[e] = pack2<BF16>(__uint_as_float(r[2 * e]) * mul, __uint_as_float(r[2 * e + 1]) * mul);
-        store_rows_x32(w4, lane, [&](int rl) -> uint16_t* {
-          const int jr = j_warp + rl;
-          if (jr >= w.len) return nullptr;
-          const long long row = PACKED ? (static_cast<long long>(w.row_base) + jr) * p.H_kv +
-                                             w.bkv % p.H_kv
-                                       : static_cast<long long>(w.bkv) * p.N + jr;
-          return base + row * D + c0;
-        });
+        store_rows_x32(w4, lane, rows_at(base, c0));
       }
       tc_fence_before_sync();
       mbar_arrive(bar(L::kAccFree));
@@ -628,12 +656,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // --------------------------------------------------------------- dQ kernel
 struct QUnit {
-  int bh;        // query head
-  int bkv;       // its K/V head
-  int m;         // query tile
-  int n0, n1;    // key tiles [n0, n1) (empty: nothing to do)
-  int row_base;  // first row of the sequence (packed batches; else 0)
-  int len;       // rows of the sequence (N unless packed)
+  int bh;         // query head
+  int bkv;        // its K/V head
+  int m;          // query tile
+  int n0, n1;     // key tiles [n0, n1) (empty: no product to run)
+  int row_base;   // first query row of the sequence (packed batches; else 0)
+  int len;        // query rows of the sequence (N unless packed)
+  int k_row_base; // first key row of the sequence (packed batches; else 0)
+  int k_len;      // key rows of the sequence (N unless packed)
+  bool rows;      // the tile holds query rows of the sequence (no keys: dQ = 0)
 };
 
 template <bool CAUSAL, bool PACKED>
@@ -648,17 +679,21 @@ __device__ __forceinline__ QUnit decode_q_unit(int u, const BwdParams& p) {
   }
   w.bkv = kv_head(w.bh, p.H, p.group);
   bwd_sequence<PACKED>(p, w.bh / p.H, &w.row_base, &w.len);
+  bwd_keys<PACKED>(p, w.bh / p.H, &w.k_row_base, &w.k_len);
   if (PACKED && CAUSAL) {
     // count the tiles from each sequence's end (its heaviest tiles first)
     w.m = (w.len + 127) / 128 - 1 - (p.n_tiles - 1 - w.m);
     if (w.m < 0) w.m = p.n_tiles;
   }
-  if (w.m * 128 >= w.len) {
+  w.rows = w.m * 128 < w.len;
+  if (!w.rows) {
     w.n0 = w.n1 = 0;
     return w;
   }
-  key_tile_range(w.m * 128, min(w.len, w.m * 128 + 128), w.len, p.win_left, p.win_right, 128,
-                 &w.n0, &w.n1);
+  // rows m*128 .. sit at key positions m*128 + shift .. (bottom-right)
+  const int shift = w.k_len - w.len;
+  key_tile_range(w.m * 128 + shift, min(w.len, w.m * 128 + 128) + shift, w.k_len, p.win_left,
+                 p.win_right, 128, &w.n0, &w.n1);
   return w;
 }
 
@@ -707,7 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
         const QUnit w = decode_q_unit<CAUSAL, PACKED>(u, p);
-        if (w.n1 == w.n0) continue;  // a query tile past a shorter sequence's end
+        if (w.n1 == w.n0) continue;  // no query rows, or rows without keys
         const uint32_t uix = units++;
         ok = wait_bar(bar(L::kFixEmpty), (uix & 1u) ^ 1u, ctl, kSiteProducerQ);
         if (!ok) break;
@@ -727,7 +762,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           mbar_arrive_expect_tx(bar(L::kAFull + sa), L::kTile);
           tma_load_4d(sbase + L::kRingAOff + sa * L::kTile, &p.tm_k, bar(L::kAFull + sa), 0,
-                      w.row_base + n * 128, 0, kv_head_c);
+                      w.k_row_base + n * 128, 0, kv_head_c);
           ++na;
           // V into ring B
           const uint32_t sb = nb % L::kStagesB;
@@ -736,7 +771,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           mbar_arrive_expect_tx(bar(L::kBFull + sb), L::kTile);
           tma_load_4d(sbase + L::kRingBOff + sb * L::kTile, &p.tm_v, bar(L::kBFull + sb), 0,
-                      w.row_base + n * 128, 0, kv_head_c);
+                      w.k_row_base + n * 128, 0, kv_head_c);
           ++nb;
         }
       }
@@ -757,7 +792,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
         const QUnit w = decode_q_unit<CAUSAL, PACKED>(u, p);
-        if (w.n1 == w.n0) continue;  // a query tile past a shorter sequence's end
+        if (w.n1 == w.n0) continue;  // no query rows, or rows without keys
         const uint32_t uix = units++;
         ok = wait_bar(bar(L::kFixFull), uix & 1u, ctl, kSiteMmaQ);
         for (int n = w.n0; n < w.n1 && ok; ++n, ++it) {
@@ -842,11 +877,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = p.scale_log2;
     uint32_t it = 0, units = 0;
     bool ok = true;
-    // the first unit at or after u with key tiles to visit (num_units: none)
+    // the first unit at or after u with query rows (num_units: none)
     auto next_unit = [&](int u, QUnit& w) -> int {
       for (; u < p.num_units; u += gridDim.x) {
         w = decode_q_unit<CAUSAL, PACKED>(u, p);
-        if (w.n1 != w.n0) break;
+        if (w.rows) break;
       }
       return u;
     };
@@ -861,8 +896,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     float nlse2 = 0.f, ndsum = 0.f;
     if (u < p.num_units) row_values(w, nlse2, ndsum);
     while (u < p.num_units && ok) {
+      // dQ rows of query tile m of head bh ([B*H][N][d], or packed
+      // [total][H][d]): 32 columns of the rows of this warp
+      const int i_warp = w.m * 128 + (warp % 4) * 32;  // query of lane 0's row
+      auto rows_at = [&](int c0) {
+        return [&, c0](int rl) -> uint16_t* {
+          const int ir = i_warp + rl;
+          if (ir >= w.len) return nullptr;
+          const long long qrow = PACKED
+                                     ? (static_cast<long long>(w.row_base) + ir) * p.H + w.bh % p.H
+                                     : static_cast<long long>(w.bh) * p.N + ir;
+          return p.dq + qrow * D + half * (D / 2) + c0;
+        };
+      };
+      if (w.n1 == w.n0) {
+        // query rows that see no key (separate query and key lengths): dQ = 0
+#pragma unroll 1
+        for (int c0 = 0; c0 < D / 2; c0 += 32) {
+          uint32_t z[16] = {};
+          store_rows_x32(z, lane, rows_at(c0));
+        }
+        QUnit wn{};
+        const int un = next_unit(u + static_cast<int>(gridDim.x), wn);
+        if (un < p.num_units) row_values(wn, nlse2, ndsum);
+        u = un;
+        w = wn;
+        continue;
+      }
       const uint32_t uix = units++;
       const int i = w.m * 128 + t;
+      const int shift = w.k_len - w.len;  // key position of query 0
       const int row_end = min(w.len, w.m * 128 + 128);
       for (int n = w.n0; n < w.n1; ++n, ++it) {
         const uint32_t ph = it & 1u;
@@ -871,11 +934,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc_fence_after_sync();
         const int kbase = n * 128 + c;  // key of column c
-        const bool need_mask = (kbase + 64 > w.len) ||
-                               (kbase + 63 > w.m * 128 + p.win_right) ||
-                               (kbase < row_end - 1 - p.win_left);
-        const int N = w.len, wl = p.win_left, wr = p.win_right;
-        auto keep = [&](int e) { return admissible(i, kbase + e, N, wl, wr); };
+        const bool need_mask = (kbase + 64 > w.k_len) ||
+                               (kbase + 63 > w.m * 128 + shift + p.win_right) ||
+                               (kbase < row_end - 1 + shift - p.win_left);
+        const int len = w.len, k_len = w.k_len, wl = p.win_left, wr = p.win_right;
+        auto keep = [&](int e) { return admissible(i, kbase + e, len, k_len, shift, wl, wr); };
         // phase A: P (S may be overwritten once every thread has read it)
         float pv[64];
         if (need_mask)
@@ -918,8 +981,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after_sync();
-      // dQ row i of head bh ([B*H][N][d], or packed [total][H][d])
-      const int i_warp = w.m * 128 + (warp % 4) * 32;  // query of lane 0's row
 #pragma unroll 1
       for (int c0 = 0; c0 < D / 2; c0 += 32) {
         uint32_t r[32];
@@ -929,14 +990,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 16; ++e)
           w4[e] = pack2<BF16>(__uint_as_float(r[2 * e]) * p.scale,
                               __uint_as_float(r[2 * e + 1]) * p.scale);
-        store_rows_x32(w4, lane, [&](int rl) -> uint16_t* {
-          const int ir = i_warp + rl;
-          if (ir >= w.len) return nullptr;
-          const long long qrow = PACKED
-                                     ? (static_cast<long long>(w.row_base) + ir) * p.H + w.bh % p.H
-                                     : static_cast<long long>(w.bh) * p.N + ir;
-          return p.dq + qrow * D + half * (D / 2) + c0;
-        });
+        store_rows_x32(w4, lane, rows_at(c0));
       }
       tc_fence_before_sync();
       mbar_arrive(bar(L::kAccFree));

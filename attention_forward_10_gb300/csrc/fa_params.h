@@ -105,31 +105,22 @@ struct BwdParams {  // 64-byte aligned through CUtensorMap
   int num_bh, num_bkv;    // B*H, B*H_kv
   int num_units;          // work units of the launched kernel
   int H, H_kv, group;
-  int win_left, win_right;  // clamped to [0, N]; win_right = 0 when causal
+  int win_left, win_right;  // clamped to [0, N + N_k]; win_right = 0 when causal
   float scale, scale_log2;
-  // packed variable-length batches (nullptr / 0 otherwise): tensors are
-  // [total_rows][heads][d], sequence b is rows cu_seqlens[b] .. cu_seqlens[b+1]-1,
-  // N is the longest sequence and num_bh = batch * H
+  // packed variable-length batches (nullptr / 0 otherwise): Q, O, dO, dQ are
+  // [total_rows][H][d] and K, V, dK, dV [total_rows_k][H_kv][d]; sequence b
+  // owns query rows cu_seqlens[b] .. cu_seqlens[b+1]-1 and key rows
+  // cu_seqlens_k[b] .. (the same offsets for self-attention), cut to
+  // seqused_q[b] / seqused_k[b] rows when given; N and N_k are the longest
+  // query and key lengths and num_bh = batch * H.  Masks are aligned
+  // bottom-right: query i of a sequence sits at key position i + k_len - len.
   const int* cu_seqlens;
-  int total_rows;
+  const int* cu_seqlens_k;
+  const int* seqused_q;
+  const int* seqused_k;
+  int total_rows, total_rows_k;
+  int N_k, n_tiles_k;  // longest key length (N unless packed) and its 128-key tiles
 };
-
-// Row offset and length of sequence b of a backward launch (clamped as in
-// seq_view: a malformed cu_seqlens only shortens sequences).
-template <bool PACKED>
-__device__ __forceinline__ void bwd_sequence(const BwdParams& p, int b, int* row_base,
-                                             int* len) {
-  if constexpr (!PACKED) {
-    *row_base = 0;
-    *len = p.N;
-  } else {
-    int r0 = p.cu_seqlens[b], r1 = p.cu_seqlens[b + 1];
-    r0 = r0 < 0 ? 0 : (r0 > p.total_rows ? p.total_rows : r0);
-    r1 = r1 < r0 ? r0 : (r1 > p.total_rows ? p.total_rows : r1);
-    *row_base = r0;
-    *len = (r1 - r0 < p.N) ? r1 - r0 : p.N;
-  }
-}
 
 // Rows of one (b, h) attention problem: the first packed row and the length
 // of its queries and of its keys, the head coordinates of its Q, O and K/V
@@ -172,6 +163,30 @@ __device__ __forceinline__ void packed_rows(const int* cu, const int* used, int 
   }
   *first = r0;
   *len = n < cap ? n : cap;
+}
+
+// Query rows (first packed row and used length) and key rows of sequence b
+// of a backward launch, clamped as packed_rows clamps them.
+template <bool PACKED>
+__device__ __forceinline__ void bwd_sequence(const BwdParams& p, int b, int* row_base,
+                                             int* len) {
+  if constexpr (!PACKED) {
+    *row_base = 0;
+    *len = p.N;
+  } else {
+    packed_rows(p.cu_seqlens, p.seqused_q, b, p.total_rows, p.N, row_base, len);
+  }
+}
+
+template <bool PACKED>
+__device__ __forceinline__ void bwd_keys(const BwdParams& p, int b, int* k_row_base,
+                                         int* k_len) {
+  if constexpr (!PACKED) {
+    *k_row_base = 0;
+    *k_len = p.N;
+  } else {
+    packed_rows(p.cu_seqlens_k, p.seqused_k, b, p.total_rows_k, p.N_k, k_row_base, k_len);
+  }
 }
 
 template <bool PACKED>

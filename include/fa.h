@@ -449,6 +449,39 @@ FA_API int fa_bwd_varlen(const void* q, const void* k, const void* v, const void
                          int window_right, int dtype, void* workspace,
                          unsigned long long workspace_bytes, void* stream);
 
+/*
+ * fa_bwd_varlen_qk -- the backward of fa_fwd_varlen_qk: separate query and key
+ * sequences with optional used lengths (cross-attention, padded batches).
+ *
+ * Source: flash-attention "hopper/mainloop_bwd_sm90_tma_gmma_ws.hpp"
+ * (CollectiveMainloopBwd::Arguments: cu_seqlens_q, cu_seqlens_k, seqused_q,
+ * seqused_k; get_seqlen_q / get_seqlen_k; the causal and local masks shifted
+ * by seqlen_k - seqlen_q).
+ *
+ *   q, o, dout, dq  [total_q][H][d]; lse [H][total_q] as written by
+ *                   fa_fwd_varlen_qk (a row without keys has LSE = -inf).
+ *   k, v, dk, dv    [total_k][H_kv][d].
+ *   cu_seqlens_q, cu_seqlens_k, seqused_q, seqused_k, batch, max_seqlen_q,
+ *   max_seqlen_k, total_q, total_k, causal, window_left, window_right
+ *                   as in fa_fwd_varlen_qk (bottom-right aligned masks).
+ *                   batch, max_seqlen_q or total_q 0: nothing is done.
+ *   workspace       fa_bwd_workspace_bytes(batch, H, max_seqlen_q) bytes.
+ *
+ * Written: dQ for the used query rows of every sequence (0 for a row that
+ * sees no key), dK and dV for the used key rows (0 for a key no query sees).
+ * Rows past the used lengths and rows outside every sequence are not
+ * written.  Passing one offset array for both (equal totals, no used
+ * lengths) is fa_bwd_varlen.  Other rules as in fa_bwd.
+ */
+FA_API int fa_bwd_varlen_qk(const void* q, const void* k, const void* v, const void* o,
+                            const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                            const int* cu_seqlens_q, const int* cu_seqlens_k,
+                            const int* seqused_q, const int* seqused_k, int batch,
+                            int max_seqlen_q, int max_seqlen_k, int total_q, int total_k,
+                            int H, int H_kv, int d, float scale, int causal, int window_left,
+                            int window_right, int dtype, void* workspace,
+                            unsigned long long workspace_bytes, void* stream);
+
 /* Workspace bytes of fa_bwd for these sizes (written to *bytes). */
 FA_API int fa_bwd_workspace_bytes(int B, int H, int N, unsigned long long* bytes);
 

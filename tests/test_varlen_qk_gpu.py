@@ -231,3 +231,143 @@ def test_gqa_pack_setting_rejects_other_values(fa):
     assert fa.fa_set_gqa_pack(2) == fa.FA_ERR_INVALID_ARG
     assert fa.fa_set_gqa_pack(-1) == fa.FA_ERR_INVALID_ARG
     assert fa.fa_set_gqa_pack(1) == fa.FA_OK
+
+
+# ---------------------------------------------------------------- backward
+BWD_REL = 2e-2
+BWD_FLOOR = 1e-4
+SENTINEL_G = 5.0
+
+
+def _bwd_case(fa, lens_q, lens_k, H, H_kv, d, causal, window, seed, used_q=None, used_k=None):
+    """fa.bwd_varlen_qk against oracle.attention_bwd_qk sequence by sequence,
+    on the used rows (a sequence without used queries or keys: its used rows
+    of the other side must be exactly 0)."""
+    cu_q, cu_k = _offsets(lens_q), _offsets(lens_k)
+    total_q, total_k = cu_q[-1], cu_k[-1]
+    q, k, v = _inputs(total_q, total_k, H, H_kv, d, torch.bfloat16, seed)
+    do = torch.randn(q.shape, generator=torch.Generator().manual_seed(seed + 1)).to(torch.bfloat16)
+    dev = "cuda"
+    t32 = lambda x: None if x is None else torch.tensor(x, dtype=torch.int32, device=dev)  # noqa
+    nq = used_q if used_q is not None else lens_q
+    nk = used_k if used_k is not None else lens_k
+    mq, mk = max(nq), max(nk)
+    scale = d ** -0.5
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    o, lse = fa.fwd_varlen_qk(qd, kd, vd, t32(cu_q), t32(cu_k), mq, mk, seqused_q=t32(used_q),
+                              seqused_k=t32(used_k), scale=scale, causal=causal, window=window)
+    dq, dk, dv = fa.bwd_varlen_qk(qd, kd, vd, o, lse, dod, t32(cu_q), t32(cu_k), mq, mk,
+                                  seqused_q=t32(used_q), seqused_k=t32(used_k), scale=scale,
+                                  causal=causal, window=window)
+    torch.cuda.synchronize()
+    st, site = fa.fa_get_device_status(None)
+    assert st == fa.FA_OK, f"device status {fa.fa_status_string(st)} at site {site}"
+    dq, dk, dv = (t.float().cpu().numpy() for t in (dq, dk, dv))
+    for b in range(len(lens_q)):
+        q0, k0 = cu_q[b], cu_k[b]
+        if nq[b] == 0 or nk[b] == 0:
+            assert (dq[q0:q0 + nq[b]] == 0).all(), f"seq {b}: dQ of rows without keys"
+            assert (dk[k0:k0 + nk[b]] == 0).all(), f"seq {b}: dK of keys without queries"
+            assert (dv[k0:k0 + nk[b]] == 0).all(), f"seq {b}: dV of keys without queries"
+            continue
+        vq = lambda t: t[q0:q0 + nq[b]].permute(1, 0, 2).unsqueeze(0).contiguous()  # noqa
+        vk = lambda t: t[k0:k0 + nk[b]].permute(1, 0, 2).unsqueeze(0).contiguous()  # noqa
+        ref = oracle.attention_bwd_qk(vq(q), vk(k), vk(v), vq(do), scale, causal, *window)
+        got = (dq[q0:q0 + nq[b]].transpose(1, 0, 2)[None], dk[k0:k0 + nk[b]].transpose(1, 0, 2)[None],
+               dv[k0:k0 + nk[b]].transpose(1, 0, 2)[None])
+        # the mask (bottom-right aligned): query rows without a key and keys
+        # that no query sees have exactly zero gradients
+        pos = np.arange(nq[b])[:, None] + (nk[b] - nq[b])
+        j = np.arange(nk[b])[None, :]
+        adm = np.ones((nq[b], nk[b]), dtype=bool)
+        if causal:
+            adm &= j <= pos
+        if window[0] >= 0:
+            adm &= j >= pos - window[0]
+        if window[1] >= 0:
+            adm &= j <= pos + window[1]
+        idle = {"dQ": ~adm.any(1), "dK": ~adm.any(0), "dV": ~adm.any(0)}
+        for name, g_, r in zip(("dQ", "dK", "dV"), got, ref):
+            if r.size == 0:
+                continue
+            assert np.isfinite(g_).all(), f"seq {b} {name}: non-finite"
+            err = float(np.abs(g_ - r).max())
+            bound = BWD_REL * float(np.abs(r).max()) + BWD_FLOOR
+            assert err <= bound, f"seq {b} (nq={nq[b]}, nk={nk[b]}) {name}: {err:.3e} > {bound:.3e}"
+            assert (g_[:, :, idle[name]] == 0).all(), f"seq {b} {name}: rows without work must be 0"
+    return q, k
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+def test_backward_cross_attention(fa, d, causal):
+    """Query and key sequences of different lengths (longer and shorter
+    queries, one sequence without queries, a causal case with queries that
+    see no key)."""
+    _bwd_case(fa, [200, 1, 0, 300, 129], [130, 260, 40, 100, 500], 4, 2, d, causal, (-1, -1),
+              seed=900 + d)
+
+
+@pytest.mark.parametrize("window", [(40, 10), (0, 0), (300, 0)])
+def test_backward_cross_attention_windows(fa, window):
+    """Windows at bottom-right aligned positions; with a narrow window some
+    keys are seen by no query and get dK = dV = 0."""
+    _bwd_case(fa, [64, 300, 7], [400, 120, 260], 2, 2, 128, False, window, seed=910)
+
+
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+def test_backward_used_lengths(fa, causal):
+    """Used lengths below the allocated rows (a padded batch): only the used
+    rows take part."""
+    _bwd_case(fa, [300, 200, 129], [260, 400, 129], 4, 1, 128, causal, (-1, -1), seed=920,
+              used_q=[250, 1, 0], used_k=[100, 399, 129])
+
+
+@pytest.mark.parametrize("ctas", [1, 3])
+def test_backward_cross_attention_many_units_per_cta(fa, ctas):
+    fa.fa_set_max_ctas(ctas)
+    try:
+        _bwd_case(fa, [200, 1, 300, 129], [130, 260, 100, 500], 4, 2, 128, True, (-1, -1),
+                  seed=930 + ctas)
+    finally:
+        fa.fa_set_max_ctas(0)
+
+
+def test_backward_equal_offsets_is_bwd_varlen(fa):
+    """One offset array for queries and keys, no used lengths: bit for bit
+    the gradients of fa_bwd_varlen."""
+    lens = [300, 129, 1, 256]
+    cu = _offsets(lens)
+    q, k, v = _inputs(cu[-1], cu[-1], 4, 2, 128, torch.bfloat16, 940)
+    do = torch.randn(q.shape, generator=torch.Generator().manual_seed(941)).to(torch.bfloat16)
+    cu_t = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
+    for causal in (False, True):
+        o, lse = fa.fwd_varlen(qd, kd, vd, cu_t, max(lens), causal=causal)
+        a = fa.bwd_varlen(qd, kd, vd, o, lse, dod, cu_t, max(lens), causal=causal)
+        b = fa.bwd_varlen_qk(qd, kd, vd, o, lse, dod, cu_t, cu_t, max(lens), max(lens),
+                             causal=causal)
+        torch.cuda.synchronize()
+        for x, y in zip(a, b):
+            assert torch.equal(x, y)
+
+
+def test_backward_argument_errors(fa):
+    q = torch.zeros(10, 2, 64, dtype=torch.bfloat16, device="cuda")
+    cu = torch.tensor([0, 10], dtype=torch.int32, device="cuda")
+    ws = torch.empty(1 << 16, dtype=torch.uint8, device="cuda")
+    base = [q.data_ptr()] * 9
+    # a missing key offset array, a negative total, an over-long length
+    assert fa.fa_bwd_varlen_qk(*base, cu.data_ptr(), 0, None, None, 1, 10, 10, 10, 10, 2, 2, 64,
+                               0.1, 0, -1, -1, fa.FA_DTYPE_BF16, ws.data_ptr(), ws.numel(),
+                               None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_bwd_varlen_qk(*base, cu.data_ptr(), cu.data_ptr(), None, None, 1, 10, 10, 10,
+                               -1, 2, 2, 64, 0.1, 0, -1, -1, fa.FA_DTYPE_BF16, ws.data_ptr(),
+                               ws.numel(), None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_bwd_varlen_qk(*base, cu.data_ptr(), cu.data_ptr(), None, None, 1, 10, 1 << 30,
+                               10, 10, 2, 2, 64, 0.1, 0, -1, -1, fa.FA_DTYPE_BF16, ws.data_ptr(),
+                               ws.numel(), None) == fa.FA_ERR_INVALID_ARG
+    # nothing to do
+    assert fa.fa_bwd_varlen_qk(*base, cu.data_ptr(), cu.data_ptr(), None, None, 0, 10, 10, 10,
+                               10, 2, 2, 64, 0.1, 0, -1, -1, fa.FA_DTYPE_BF16, ws.data_ptr(),
+                               ws.numel(), None) == fa.FA_OK
