@@ -521,8 +521,8 @@ int launch_forward(const ForwardCall& c, void* o_out, float* lse_out, int num_sp
 // Longest CTA of a persistent launch with `splits` key splits of
 // `split_tiles` K/V tiles each, in K/V tile steps: work item i (base unit
 // i / splits, split i % splits, in the kernels' unit order) runs on CTA
-// i % grid, and an item costs its tiles of each query tile plus one step of
-// set-up and epilogue.
+// i % grid (causal: wave_order(i) % grid, the slot that runs it), and an item
+// costs its tiles of each query tile plus one step of set-up and epilogue.
 long long estimate_makespan(const ForwardCall& c, int win_left, int win_right, int splits,
                             int split_tiles, int grid) {
   const int rows = (c.d == 256) ? kBlockM : kRowsPerUnit;
@@ -551,7 +551,11 @@ long long estimate_makespan(const ForwardCall& c, int win_left, int win_right, i
       // d = 256 tiles hold 64 keys: count in 128-key steps
       if (kv != kBlockN) cost = (cost + 1) / 2;
       if (cost == 0) continue;
-      long long& t = cta_cost[(u * splits + sp) % grid];
+      const long long item = u * splits + sp;
+      const long long slot =
+          c.causal ? wave_order(static_cast<int>(item), static_cast<int>(base_units * splits), grid)
+                   : item;
+      long long& t = cta_cost[slot % grid];
       t += cost + 1;
       worst = std::max(worst, t);
     }

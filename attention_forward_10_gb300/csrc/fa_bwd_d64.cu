@@ -10,8 +10,8 @@ template <bool CAUSAL, bool BF16>
 cudaError_t launch_all(const BwdParams& p_kv, const BwdParams& p_q, const void* o,
                        const void* dout, const float* lse, float* lse2, float* dsum,
                        int grid_kv, int grid_q, int num_sms, cudaStream_t stream) {
-  // pre-pass: D/8 threads per padded row, grid-stride over num_sms * 8 blocks
-  const long long threads = static_cast<long long>(p_q.num_bh) * p_q.n_pad * (64 / 8);
+  // pre-pass: D/16 threads per padded row, grid-stride over num_sms * 8 blocks
+  const long long threads = static_cast<long long>(p_q.num_bh) * p_q.n_pad * (64 / 16);
   long long blocks = (threads + 255) / 256;
   if (blocks > static_cast<long long>(num_sms) * 8) blocks = static_cast<long long>(num_sms) * 8;
   if (blocks < 1) blocks = 1;

@@ -172,8 +172,9 @@ __device__ __forceinline__ bool admissible(int i, int j, int len, int k_len, int
 
 // ---------------------------------------------------------------- pre-pass
 // nlse2[bh][i] = -LSE * log2(e) and ndsum[bh][i] = -sum_c dO[i][c] O[i][c]
-// for i < N; -inf and 0 for the padding rows up to n_pad.  d/8 threads per
-// row.
+// for i < N; -inf and 0 for the padding rows up to n_pad.  d/16 threads per
+// row, each with two 16-byte loads of O and two of dO in flight (a resident
+// grid holds enough bytes in flight to keep HBM busy).
 // (PACKED: O and dO are [total][H][d], LSE [H][total]; row i of sequence b
 // is packed row cu_seqlens[b] + i, and rows past the sequence are padding.)
 template <int D, bool BF16, bool PACKED>
@@ -184,7 +185,7 @@ __global__ void __launch_bounds__(256)
                           const BwdParams p) {
   griddep_wait();  // (programmatic dependent launch: see fa_launch.h)
   griddep_launch_dependents();
-  constexpr int kTpr = D / 8;
+  constexpr int kTpr = D / 16;
   const long long rows = static_cast<long long>(num_bh) * n_pad;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   // every lane runs the same number of iterations (the shuffles need all)
@@ -201,18 +202,19 @@ __global__ void __launch_bounds__(256)
     const bool valid = i < len;
     // element offset of row i of head bh, and the LSE index
     const long long off =
-        PACKED ? ((static_cast<long long>(row_base) + i) * p.H + bh % p.H) * D + part * 8
-               : (static_cast<long long>(bh) * N + i) * D + part * 8;
+        PACKED ? ((static_cast<long long>(row_base) + i) * p.H + bh % p.H) * D + part * 16
+               : (static_cast<long long>(bh) * N + i) * D + part * 16;
     const long long lidx = PACKED ? static_cast<long long>(bh % p.H) * p.total_rows + row_base + i
                                   : static_cast<long long>(bh) * N + i;
     float acc = 0.f;
     if (valid) {
-      const uint4 a = *reinterpret_cast<const uint4*>(o + off);
-      const uint4 b = *reinterpret_cast<const uint4*>(dout + off);
-      const uint32_t wa[4] = {a.x, a.y, a.z, a.w};
-      const uint32_t wb[4] = {b.x, b.y, b.z, b.w};
+      const uint4* po = reinterpret_cast<const uint4*>(o + off);
+      const uint4* pd = reinterpret_cast<const uint4*>(dout + off);
+      const uint4 a0 = po[0], a1 = po[1], b0 = pd[0], b1 = pd[1];
+      const uint32_t wa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const uint32_t wb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
+      for (int e = 0; e < 8; ++e) {
         acc += unpack_lo<BF16>(wa[e]) * unpack_lo<BF16>(wb[e]);
         acc += unpack_hi<BF16>(wa[e]) * unpack_hi<BF16>(wb[e]);
       }
@@ -302,6 +304,9 @@ struct KvUnit {
 template <bool CAUSAL, bool PACKED>
 __device__ __forceinline__ KvUnit decode_kv_unit(int u, const BwdParams& p) {
   KvUnit w;
+  // (slot u of the persistent loop; dense causal launches alternate the
+  // direction of their waves)
+  if (CAUSAL && !PACKED && u < p.num_units) u = wave_order(u, p.num_units, gridDim.x);
   if (CAUSAL) {
     // heaviest first: the first key tiles see the most query tiles
     w.n = u / p.num_bkv;
@@ -670,6 +675,7 @@ struct QUnit {
 template <bool CAUSAL, bool PACKED>
 __device__ __forceinline__ QUnit decode_q_unit(int u, const BwdParams& p) {
   QUnit w;
+  if (CAUSAL && !PACKED && u < p.num_units) u = wave_order(u, p.num_units, gridDim.x);
   if (CAUSAL) {
     w.m = p.n_tiles - 1 - u / p.num_bh;  // heaviest first
     w.bh = u % p.num_bh;

@@ -90,6 +90,7 @@ struct Unit {
 template <bool CAUSAL, bool PACKED>
 __device__ __forceinline__ Unit decode_unit(int u, const FaParams& p) {
   Unit w;
+  if (CAUSAL && !PACKED && u < p.num_units) u = wave_order(u, p.num_units, gridDim.x);
   int split = 0;
   if (p.num_splits > 1) {
     split = u % p.num_splits;

@@ -147,6 +147,8 @@ struct Unit {
   int n_beg, n_end;
 };
 
+// Slot u of the persistent loop (CTA c takes slots c, c + grid, ...) runs
+// unit u, or for dense causal launches unit wave_order(u).
 // Units [0, num_pair_units) are query-tile pairs.  When the pairs do not
 // fill the last wave of CTAs evenly, the pairs of that partial wave are split
 // instead into single-tile units (tile 0 only), one per CTA, which halves
@@ -154,6 +156,7 @@ struct Unit {
 template <bool CAUSAL, bool PACKED>
 __device__ __forceinline__ Unit decode_unit(int u, const FaParams& p) {
   Unit w;
+  if (CAUSAL && !PACKED && u < p.num_units) u = wave_order(u, p.num_units, gridDim.x);
   int split = 0;
   if (p.num_splits > 1) {
     split = u % p.num_splits;

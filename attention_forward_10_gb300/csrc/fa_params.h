@@ -139,6 +139,21 @@ struct SeqView {
 };
 
 // K/V head of query head bh = b*H + h (grouped heads: h / group).
+// Order in which a persistent grid of `grid` CTAs takes its work units: CTA
+// c runs slots c, c + grid, c + 2 grid, ... and slot s runs unit
+// wave_order(s).  Causal units are numbered heaviest first, so slots taken
+// round robin would hand CTA 0 the heaviest unit of every wave; every other
+// wave is reversed instead (CTA 0 takes the heaviest unit of even waves and
+// the lightest of odd ones), which evens out the CTAs' totals.  A bijection
+// of [0, num_units): a last, partial wave is reversed within itself.
+__host__ __device__ inline int wave_order(int s, int num_units, int grid) {
+  const int k = s / grid;
+  if ((k & 1) == 0) return s;
+  const int first = k * grid;
+  const int size = (num_units - first < grid) ? num_units - first : grid;
+  return first + (size - 1 - (s - first));
+}
+
 __host__ __device__ inline int kv_head(int bh, int H, int group) {
   const int H_kv = H / group;
   return (bh / H) * H_kv + (bh % H) / group;

@@ -76,8 +76,11 @@ def test_grouped_heads_and_windows(fa, d, H, H_kv, causal, window):
     _check(got, ref, f"d={d} H={H}/{H_kv} causal={causal} window={window}")
 
 
-@pytest.mark.parametrize("ctas", [1, 3])
+@pytest.mark.parametrize("ctas", [1, 3, 4, 5])
 def test_persistent_loop(fa, ctas):
+    """18 units of each kernel on 1-5 CTAs: with 4 the last wave (even) is
+    partial, with 5 the last wave is partial and odd, so it runs reversed
+    within itself."""
     fa.fa_set_max_ctas(ctas)
     try:
         got, ref = _case(fa, 1, 3, 3, 700, 128, torch.bfloat16, True, seed=50 + ctas)

@@ -119,9 +119,12 @@ def test_causal_first_row_is_first_value_row(fa, d):
 
 # ------------------------------------------- persistent scheduler, streams
 @pytest.mark.parametrize("d", [64, 128, 256])
-@pytest.mark.parametrize("ctas", [1, 2, 3, 7])
+@pytest.mark.parametrize("ctas", [1, 2, 3, 5, 7])
 @pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
 def test_persistent_loop_many_units_per_cta(fa, ctas, causal, d):
+    """Many units per CTA; causal launches reverse every other wave (with 7
+    CTAs the 27 units of d <= 128 end in a partial odd wave, with 5 the 48
+    units of d = 256 do)."""
     q, k, v = make_random_qkv(2, 3, 1000, d, torch.bfloat16, seed=50 + ctas)
     scale = 1.0 / math.sqrt(d)
     fa.fa_set_max_ctas(ctas)
