@@ -462,6 +462,12 @@ int launch_forward(const ForwardCall& c, void* o_out, float* lse_out, int num_sp
   const int N_k = (packed && c.cu_seqlens_k != nullptr) ? c.N_k : N;
   p.N_k = N_k;
   p.gqa_log2 = gqa_log2;
+  // (one pair per problem: the table's order is the plain one, and building
+  // it would only delay the start)
+  p.unit_table = (packed && c.causal && d != 256 && num_splits == 1 && c.B <= kTableSeqs &&
+                  pairs > 1 && pairs <= kTablePairs)
+                     ? 1
+                     : 0;
   p.o_ptr = static_cast<uint16_t*>(o_out);
   p.lse = lse_out;
   p.status = info->status;

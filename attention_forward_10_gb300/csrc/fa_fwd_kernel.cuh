@@ -128,13 +128,75 @@ struct Layout {
   static constexpr int kStageEmpty = kStageFull + 1;  // staging read by the store
   static constexpr int kNumBars = kStageEmpty + 1;
   static constexpr uint32_t kCtlOff = kBarOff + kNumBars * 8;
-  static constexpr uint32_t kUsedBytes = kCtlOff + 16;
+  // unit table of packed causal launches: sequence ids (bytes), then the
+  // cumulative unit counts of the pair groups (ints)
+  static constexpr uint32_t kTableIdsOff = kCtlOff + 16;
+  static constexpr uint32_t kTableCumOff = kTableIdsOff + kTableSeqs;
+  static constexpr uint32_t kUsedBytes = kTableCumOff + 4 * (kTablePairs + 1);
   static constexpr uint32_t kSmemBytes = kUsedBytes + 1024;  // alignment slack
   static_assert(kSmemBytes <= 232448, "exceeds the shared memory of one CTA");
   // tensor-memory columns of S_g / P_g and of O_g
   __device__ static constexpr uint32_t s_col(int g) { return g * 128u; }
   __device__ static constexpr uint32_t o_col(int g) { return 256u + g * D; }
 };
+
+// Unit table of a packed causal launch (shared memory, built once per CTA).
+// A unit's cost grows with its pair index from the sequence start (its rows
+// see the keys up to their own position), so units are taken in groups of
+// equal pair index, highest first: group k holds pair P-1-k of every
+// sequence that has it (ids[0 .. q_k), the sequences sorted by their pair
+// count, longest first) and every problem head, cum[k] units precede it and
+// cum[P] units exist in all; slots past cum[P] are empty units.
+struct UnitTable {
+  const uint8_t* ids;
+  const int* cum;
+};
+
+// Builds the table (one warp; every lane calls it).  Sequences beyond the
+// batch count have no pairs.
+__device__ __forceinline__ void build_unit_table(const FaParams& p, uint8_t* ids, int* cum,
+                                                 int lane) {
+  const int heads = p.H >> p.gqa_log2;
+  const int batch = p.num_bh / heads;
+  const int unit_pos = kRowsPerUnit >> p.gqa_log2;
+  int np[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int b = lane + 32 * i;
+    np[i] = -1;
+    if (b < batch) {
+      int first, len;
+      packed_rows(p.cu_seqlens, p.seqused_q, b, p.total_rows, p.N, &first, &len);
+      np[i] = (len + unit_pos - 1) / unit_pos;
+    }
+  }
+  // rank of each sequence: more pairs first, then lower index
+  int rank[2] = {0, 0};
+  for (int b2 = 0; b2 < batch; ++b2) {
+    const int v0 = __shfl_sync(0xffffffffu, np[0], b2 & 31);
+    const int v1 = __shfl_sync(0xffffffffu, np[1], b2 & 31);
+    const int n2 = b2 < 32 ? v0 : v1;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int b = lane + 32 * i;
+      rank[i] += (n2 > np[i] || (n2 == np[i] && b2 < b)) ? 1 : 0;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+    if (lane + 32 * i < batch) ids[rank[i]] = static_cast<uint8_t>(lane + 32 * i);
+  // group k = pair P-1-k: the sequences with more than P-1-k pairs, times
+  // the heads
+  int running = 0;
+  if (lane == 0) cum[0] = 0;
+  for (int k = 0; k < p.num_pairs; ++k) {
+    const int pr = p.num_pairs - 1 - k;
+    const int cnt = __popc(__ballot_sync(0xffffffffu, np[0] > pr)) +
+                    __popc(__ballot_sync(0xffffffffu, np[1] > pr));
+    running += cnt * heads;
+    if (lane == 0) cum[k + 1] = running;
+  }
+}
 
 // One work unit: 256 query rows of one (b,h) = two 128-row query tiles.
 // Tile g visits K/V tiles [n0[g], n1[g]) (empty when n1 == n0); the unit
@@ -154,9 +216,10 @@ struct Unit {
 // instead into single-tile units (tile 0 only), one per CTA, which halves
 // the length of the last wave.
 template <bool CAUSAL, bool PACKED>
-__device__ __forceinline__ Unit decode_unit(int u, const FaParams& p) {
+__device__ __forceinline__ Unit decode_unit(int u, const FaParams& p, const UnitTable& tab) {
   Unit w;
-  if (CAUSAL && !PACKED && u < p.num_units) u = wave_order(u, p.num_units, gridDim.x);
+  if (CAUSAL && u < p.num_units && (!PACKED || p.unit_table))
+    u = wave_order(u, p.num_units, gridDim.x);
   int split = 0;
   if (p.num_splits > 1) {
     split = u % p.num_splits;
@@ -168,7 +231,28 @@ __device__ __forceinline__ Unit decode_unit(int u, const FaParams& p) {
     single = (u - p.num_pair_units) % 2;
   }
   int pair;
-  if (CAUSAL) {
+  bool from_table = false;
+  if (PACKED && CAUSAL && p.unit_table) {
+    // the pu-th unit of the table's order (pu < num_units)
+    from_table = true;
+    const int heads = p.H >> p.gqa_log2;
+    if (pu >= tab.cum[p.num_pairs]) {
+      w.bh = 0;
+      pair = p.num_pairs;  // past the units that exist: an empty unit
+    } else {
+      int lo = 0, hi = p.num_pairs - 1;  // the group k with cum[k] <= pu < cum[k+1]
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (tab.cum[mid] <= pu)
+          lo = mid;
+        else
+          hi = mid - 1;
+      }
+      const int r = pu - tab.cum[lo];
+      w.bh = tab.ids[r / heads] * heads + r % heads;
+      pair = p.num_pairs - 1 - lo;
+    }
+  } else if (CAUSAL) {
     // heaviest first: the last query pairs of every head come first
     pair = p.num_pairs - 1 - pu / p.num_bh;
     w.bh = pu % p.num_bh;
@@ -184,7 +268,7 @@ __device__ __forceinline__ Unit decode_unit(int u, const FaParams& p) {
   // where a tile row is a (position, head) pair)
   const int pk = PACKED ? p.gqa_log2 : 0;
   const int tile_pos = kBlockM >> pk, unit_pos = kRowsPerUnit >> pk;
-  if (PACKED && CAUSAL) {
+  if (PACKED && CAUSAL && !from_table) {
     // sequences differ in length: count the pairs from each sequence's end,
     // so that every sequence's heaviest (last) pairs come first
     pair = (len + unit_pos - 1) / unit_pos - 1 - (p.num_pairs - 1 - pair);
@@ -371,6 +455,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   // dependent launch); global memory is touched only after it completed.
   griddep_wait();
   griddep_launch_dependents();
+  const UnitTable tab{smem + L::kTableIdsOff, reinterpret_cast<const int*>(smem + L::kTableCumOff)};
+  if (PACKED && CAUSAL && p.unit_table) {
+    if (warp == 0)
+      build_unit_table(p, smem + L::kTableIdsOff, reinterpret_cast<int*>(smem + L::kTableCumOff),
+                       lane);
+    __syncthreads();
+  }
 
   // Each role changes its register budget inside its own branch, so that no
   // code is reachable under two different budgets.
@@ -381,7 +472,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       uint32_t kv_it = 0, q_it[2] = {0, 0};
       bool ok = true;
       for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
-        const Unit w = decode_unit<CAUSAL, PACKED>(u, p);
+        const Unit w = decode_unit<CAUSAL, PACKED>(u, p, tab);
         for (int g = 0; g < 2 && ok; ++g) {
           if (w.n1[g] == w.n0[g]) continue;
           ok = wait_bar(bar(L::kQEmpty + g), (q_it[g] & 1u) ^ 1u, ctl, kSiteProducerQ);
@@ -500,11 +591,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       bool prev_active[2] = {false, false}, prev_acc[2] = {false, false};
       uint32_t prev_vslot = 0;
       int u = blockIdx.x;
-      Unit w = decode_unit<CAUSAL, PACKED>(u < p.num_units ? u : 0, p);
+      Unit w = decode_unit<CAUSAL, PACKED>(u < p.num_units ? u : 0, p, tab);
       // units without K/V tiles (a split-off tile past N) stream nothing
       while (u < p.num_units && w.n_end == w.n_beg) {
         u += gridDim.x;
-        if (u < p.num_units) w = decode_unit<CAUSAL, PACKED>(u, p);
+        if (u < p.num_units) w = decode_unit<CAUSAL, PACKED>(u, p, tab);
       }
       int n = w.n_beg;
       while (ok) {
@@ -596,7 +687,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         if (++n == w.n_end) {
           do {
             u += gridDim.x;
-            if (u < p.num_units) w = decode_unit<CAUSAL, PACKED>(u, p);
+            if (u < p.num_units) w = decode_unit<CAUSAL, PACKED>(u, p, tab);
           } while (u < p.num_units && w.n_end == w.n_beg);
           n = w.n_beg;
         }
@@ -621,7 +712,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     bool ok = true;
 
     for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
-      const Unit w = decode_unit<CAUSAL, PACKED>(u, p);
+      const Unit w = decode_unit<CAUSAL, PACKED>(u, p, tab);
       // the staging tile is used by tile 0 then tile 1 of each unit (tiles of
       // packed batches are written directly)
       const bool staged0 = staged_tile<PACKED>(p, w, 0), staged1 = staged_tile<PACKED>(p, w, 1);
@@ -806,7 +897,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     uint32_t full_par = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < p.num_units && ok && lane == 0; u += gridDim.x) {
-      const Unit w = decode_unit<CAUSAL, PACKED>(u, p);
+      const Unit w = decode_unit<CAUSAL, PACKED>(u, p, tab);
       for (int g = 0; g < 2 && ok; ++g) {
         if (!staged_tile<PACKED>(p, w, g)) continue;
         ok = wait_bar(bar(L::kStageFull), full_par, ctl, kSiteStore);

@@ -13,6 +13,9 @@ constexpr int kBlockM = 128;
 constexpr int kBlockN = 128;
 // Two query tiles (256 rows) per work unit: one per softmax warpgroup.
 constexpr int kRowsPerUnit = 2 * kBlockM;
+// Limits of the per-CTA unit table of packed causal launches.
+constexpr int kTableSeqs = 64;
+constexpr int kTablePairs = 256;
 
 // Site codes recorded in the status word when a bounded wait runs out.
 enum WaitSite : int {
@@ -73,6 +76,11 @@ struct FaParams {  // 64-byte aligned through CUtensorMap
   // views {64, heads of a group, rows, d/64, K/V heads} and num_bh = batch
   // * H_kv.
   int gqa_log2;
+  // Packed causal launches of the d <= 128 kernel with at most
+  // kTableSeqs sequences and 2 .. kTablePairs units per problem: 1 when
+  // every CTA builds the unit table (units ordered by their pair index from
+  // the sequence start, heaviest first; see the kernel), 0 otherwise.
+  int unit_table;
   uint16_t* o_ptr;   // O (packed rows), for the row-by-row store of the last
                      // query tile of a sequence
   float descale_v;   // FP8 kernels: V descale, applied to O in the epilogue

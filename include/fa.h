@@ -293,9 +293,9 @@ FA_API int fa_splitkv_workspace_bytes(int B, int H, int N, int d, int causal,
  *               S splits take S * B*H*N * (2d + 4) bytes (plus at most 255
  *               bytes of alignment), so at most
  *               floor(FA_NOALLOC_SCRATCH_BYTES / (B*H*N * (2d + 4))) fit:
- *               for example 2 for one head of 49152 rows at d = 128, where
- *               the automatic count of fa_fwd_splitkv is 8 on a 152-SM
- *               GB300.  fa_splitkv_workspace_bytes with an explicit count
+ *               for example 3 for one head of 32768 rows at d = 128, where
+ *               the automatic count of fa_fwd_splitkv without a mask is 7
+ *               on a 152-SM GB300.  fa_splitkv_workspace_bytes with an explicit count
  *               tells whether that count fits.
  * Every other argument, layout, alignment rule and error is that of
  * fa_fwd_splitkv.

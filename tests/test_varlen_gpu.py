@@ -105,6 +105,32 @@ def test_persistent_loop(fa, ctas, d):
     _check(o, lse, o_ref, l_ref, cu, f"ctas={ctas} d={d}")
 
 
+@pytest.mark.parametrize("nseq,max_seqlen,H_kv", [
+    (64, None, 2), (64, None, 1),   # the table's limit (H_kv 1: grouped heads packed)
+    (65, None, 2),                  # one sequence more: pairs counted from each end
+    (20, 5000, 1),                  # max_seqlen far above every length: empty pair groups
+    (20, 70000, 2),                 # more than 256 units per problem: counted from each end
+])
+@pytest.mark.parametrize("ctas", [0, 5])
+def test_causal_unit_table_and_fallback(fa, nseq, max_seqlen, H_kv, ctas):
+    """Packed causal launches of the d <= 128 kernel with at most 64
+    sequences and 256 units per problem take their units from a per-CTA
+    table (groups of equal pair index, heaviest first, every other wave
+    reversed); past either limit the pairs are counted from each sequence's
+    end.  Both sides of both limits, on every SM and on 5 CTAs (many
+    waves)."""
+    g = torch.Generator().manual_seed(640 + nseq)
+    lens = torch.randint(0, 700, (nseq,), generator=g).tolist()
+    q, k, v, cu = _packed(lens, 2, H_kv, 128, torch.bfloat16, seed=641 + nseq)
+    fa.fa_set_max_ctas(ctas)
+    try:
+        o, lse = _run(fa, q, k, v, cu, 0.09, True, max_seqlen=max_seqlen)
+    finally:
+        fa.fa_set_max_ctas(0)
+    o_ref, l_ref = oracle.attention_varlen(q, k, v, cu, 0.09, True)
+    _check(o, lse, o_ref, l_ref, cu, f"nseq={nseq} max_seqlen={max_seqlen} H_kv={H_kv}")
+
+
 @pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("N", [256, 333])
 def test_equal_lengths_equal_the_batched_forward(fa, d, N):
