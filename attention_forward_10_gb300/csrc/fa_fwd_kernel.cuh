@@ -215,11 +215,11 @@ struct Unit {
 // fill the last wave of CTAs evenly, the pairs of that partial wave are split
 // instead into single-tile units (tile 0 only), one per CTA, which halves
 // the length of the last wave.
-template <bool CAUSAL, bool PACKED>
+template <bool CAUSAL, bool PACKED, bool TABLE>
 __device__ __forceinline__ Unit decode_unit(int u, const FaParams& p, const UnitTable& tab) {
+  static_assert(!TABLE || (CAUSAL && PACKED), "the unit table orders packed causal units");
   Unit w;
-  if (CAUSAL && u < p.num_units && (!PACKED || p.unit_table))
-    u = wave_order(u, p.num_units, gridDim.x);
+  if (CAUSAL && (!PACKED || TABLE) && u < p.num_units) u = wave_order(u, p.num_units, gridDim.x);
   int split = 0;
   if (p.num_splits > 1) {
     split = u % p.num_splits;
@@ -231,10 +231,8 @@ __device__ __forceinline__ Unit decode_unit(int u, const FaParams& p, const Unit
     single = (u - p.num_pair_units) % 2;
   }
   int pair;
-  bool from_table = false;
-  if (PACKED && CAUSAL && p.unit_table) {
+  if constexpr (TABLE) {
     // the pu-th unit of the table's order (pu < num_units)
-    from_table = true;
     const int heads = p.H >> p.gqa_log2;
     if (pu >= tab.cum[p.num_pairs]) {
       w.bh = 0;
@@ -268,7 +266,7 @@ __device__ __forceinline__ Unit decode_unit(int u, const FaParams& p, const Unit
   // where a tile row is a (position, head) pair)
   const int pk = PACKED ? p.gqa_log2 : 0;
   const int tile_pos = kBlockM >> pk, unit_pos = kRowsPerUnit >> pk;
-  if (PACKED && CAUSAL && !from_table) {
+  if (PACKED && CAUSAL && !TABLE) {
     // sequences differ in length: count the pairs from each sequence's end,
     // so that every sequence's heaviest (last) pairs come first
     pair = (len + unit_pos - 1) / unit_pos - 1 - (p.num_pairs - 1 - pair);
@@ -398,7 +396,9 @@ __device__ __forceinline__ float exp_tile_to_tmem_e4m3(const float (&s)[kBlockN]
   return a0 + a1;
 }
 
-template <int D, bool CAUSAL, bool BF16, bool PACKED, bool FP8 = false>
+// TABLE: packed causal launches that take their units from the per-CTA unit
+// table (p.unit_table set).
+template <int D, bool CAUSAL, bool BF16, bool PACKED, bool FP8 = false, bool TABLE = false>
 __global__ void __launch_bounds__(kNumThreads, 1)
     fa_fwd_kernel(const __grid_constant__ FaParams p) {
   using L = Layout<D, FP8>;
@@ -456,7 +456,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   griddep_wait();
   griddep_launch_dependents();
   const UnitTable tab{smem + L::kTableIdsOff, reinterpret_cast<const int*>(smem + L::kTableCumOff)};
-  if (PACKED && CAUSAL && p.unit_table) {
+  if constexpr (TABLE) {
     if (warp == 0)
       build_unit_table(p, smem + L::kTableIdsOff, reinterpret_cast<int*>(smem + L::kTableCumOff),
                        lane);
@@ -472,7 +472,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       uint32_t kv_it = 0, q_it[2] = {0, 0};
       bool ok = true;
       for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
-        const Unit w = decode_unit<CAUSAL, PACKED>(u, p, tab);
+        const Unit w = decode_unit<CAUSAL, PACKED, TABLE>(u, p, tab);
         for (int g = 0; g < 2 && ok; ++g) {
           if (w.n1[g] == w.n0[g]) continue;
           ok = wait_bar(bar(L::kQEmpty + g), (q_it[g] & 1u) ^ 1u, ctl, kSiteProducerQ);
@@ -591,11 +591,11 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       bool prev_active[2] = {false, false}, prev_acc[2] = {false, false};
       uint32_t prev_vslot = 0;
       int u = blockIdx.x;
-      Unit w = decode_unit<CAUSAL, PACKED>(u < p.num_units ? u : 0, p, tab);
+      Unit w = decode_unit<CAUSAL, PACKED, TABLE>(u < p.num_units ? u : 0, p, tab);
       // units without K/V tiles (a split-off tile past N) stream nothing
       while (u < p.num_units && w.n_end == w.n_beg) {
         u += gridDim.x;
-        if (u < p.num_units) w = decode_unit<CAUSAL, PACKED>(u, p, tab);
+        if (u < p.num_units) w = decode_unit<CAUSAL, PACKED, TABLE>(u, p, tab);
       }
       int n = w.n_beg;
       while (ok) {
@@ -687,7 +687,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         if (++n == w.n_end) {
           do {
             u += gridDim.x;
-            if (u < p.num_units) w = decode_unit<CAUSAL, PACKED>(u, p, tab);
+            if (u < p.num_units) w = decode_unit<CAUSAL, PACKED, TABLE>(u, p, tab);
           } while (u < p.num_units && w.n_end == w.n_beg);
           n = w.n_beg;
         }
@@ -712,7 +712,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     bool ok = true;
 
     for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
-      const Unit w = decode_unit<CAUSAL, PACKED>(u, p, tab);
+      const Unit w = decode_unit<CAUSAL, PACKED, TABLE>(u, p, tab);
       // the staging tile is used by tile 0 then tile 1 of each unit (tiles of
       // packed batches are written directly)
       const bool staged0 = staged_tile<PACKED>(p, w, 0), staged1 = staged_tile<PACKED>(p, w, 1);
@@ -897,7 +897,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     uint32_t full_par = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < p.num_units && ok && lane == 0; u += gridDim.x) {
-      const Unit w = decode_unit<CAUSAL, PACKED>(u, p, tab);
+      const Unit w = decode_unit<CAUSAL, PACKED, TABLE>(u, p, tab);
       for (int g = 0; g < 2 && ok; ++g) {
         if (!staged_tile<PACKED>(p, w, g)) continue;
         ok = wait_bar(bar(L::kStageFull), full_par, ctl, kSiteStore);
