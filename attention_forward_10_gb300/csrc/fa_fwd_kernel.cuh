@@ -307,13 +307,17 @@ __device__ __forceinline__ Unit decode_unit(int u, const FaParams& p, const Unit
 }
 
 // Whether tile g of unit w goes through the staging tile and a TMA store:
-// every tile with keys of the dense layout.  Packed batches store their
-// tiles from the softmax threads (a coalesced row store per warp), which
-// measured faster there than the shared staging tile.
-template <bool PACKED>
+// the dense layout's tiles with keys, but for tile 1 of a causal unit.
+// That tile and the tiles of packed batches are stored from the softmax
+// threads (a coalesced row store per warp), so that a causal unit's tile 1
+// does not wait for tile 0's TMA store to free the one staging tile (both
+// measured faster; for units whose two tiles end together, staging both
+// measured faster).
+template <bool CAUSAL, bool PACKED>
 __device__ __forceinline__ bool staged_tile(const FaParams& p, const Unit& w, int g) {
   (void)p;
-  return !PACKED && (g ? (w.n1[1] > w.n0[1]) : (w.n1[0] > w.n0[0]));
+  if (PACKED || (CAUSAL && g == 1)) return false;
+  return g ? (w.n1[1] > w.n0[1]) : (w.n1[0] > w.n0[0]);
 }
 
 // Maximum of a row of scores: four independent chains.
@@ -715,7 +719,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       const Unit w = decode_unit<CAUSAL, PACKED, TABLE>(u, p, tab);
       // the staging tile is used by tile 0 then tile 1 of each unit (tiles of
       // packed batches are written directly)
-      const bool staged0 = staged_tile<PACKED>(p, w, 0), staged1 = staged_tile<PACKED>(p, w, 1);
+      const bool staged0 = staged_tile<CAUSAL, PACKED>(p, w, 0), staged1 = staged_tile<CAUSAL, PACKED>(p, w, 1);
       const uint32_t my_store = n_stores + ((g == 1 && staged0) ? 1u : 0u);
       n_stores += (staged0 ? 1u : 0u) + (staged1 ? 1u : 0u);
       // this warpgroup's tile (g is per warp: selects, not indexed loads)
@@ -864,14 +868,20 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         }
         continue;
       } else if (!(g ? staged1 : staged0)) {
-        // (dense layout: every tile with keys is staged; a tile that is not
-        // is stored row by row)
-        if (row < len) {
-          uint4* dst = reinterpret_cast<uint4*>(
-              p.o_ptr + ((static_cast<long long>(w.sv.row_base) + row) * p.H + o_head) * D);
+        // a dense tile not staged (tile 1 of a causal unit): the warp stores
+        // its rows of [heads][N][d] itself, 64 contiguous bytes per row and
+        // store
+        const int t_warp = t & ~31;  // tile row of lane 0
 #pragma unroll
-          for (int c16 = 0; c16 < D / 8; ++c16)
-            dst[c16] = make_uint4(pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]);
+        for (int c0 = 0; c0 < D / 2; c0 += 16) {  // 16 packed words = 32 columns
+          uint32_t w16[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) w16[e] = pk[c0 + e];
+          store_rows_x32(w16, threadIdx.x & 31, [&](int rl) -> uint16_t* {
+            const int r_row = t_row0 + t_warp + rl;
+            if (r_row >= len) return nullptr;
+            return p.o_ptr + (static_cast<long long>(w.sv.o_head) * p.N + r_row) * D + 2 * c0;
+          });
         }
         continue;
       }
@@ -899,7 +909,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     for (int u = blockIdx.x; u < p.num_units && ok && lane == 0; u += gridDim.x) {
       const Unit w = decode_unit<CAUSAL, PACKED, TABLE>(u, p, tab);
       for (int g = 0; g < 2 && ok; ++g) {
-        if (!staged_tile<PACKED>(p, w, g)) continue;
+        if (!staged_tile<CAUSAL, PACKED>(p, w, g)) continue;
         ok = wait_bar(bar(L::kStageFull), full_par, ctl, kSiteStore);
         full_par ^= 1u;
         if (!ok) break;
