@@ -502,12 +502,21 @@ int launch_forward(const ForwardCall& c, void* o_out, float* lse_out, int num_sp
   p.num_pair_units = p.num_units;
   if (d != 256 && num_splits == 1 && !packed) {
     // Balance the last wave: its L pair units become 2L single-tile units
-    // when those fit in one wave.
+    // when those fit in one wave.  With fewer pair units than CTAs, as many
+    // pairs as there are idle CTAs become two single-tile units each (a
+    // small launch then ends sooner; packed launches, whose decode units
+    // are bound by HBM, measured no faster).
     const long long pair_units = bh * pairs;
-    const long long partial = pair_units % grid;
-    if (pair_units > grid && partial > 0 && 2 * partial <= grid) {
-      p.num_pair_units = static_cast<int>(pair_units - partial);
-      p.num_units = static_cast<int>(pair_units + partial);
+    long long split = 0;
+    if (pair_units > grid) {
+      const long long partial = pair_units % grid;
+      if (partial > 0 && 2 * partial <= grid) split = partial;
+    } else {
+      split = std::min(pair_units, grid - pair_units);
+    }
+    if (split > 0) {
+      p.num_pair_units = static_cast<int>(pair_units - split);
+      p.num_units = static_cast<int>(pair_units + split);
     }
   }
   if (p.num_units < grid) grid = p.num_units;

@@ -2,7 +2,8 @@
 against the fp64 oracle.
 
 When the 256-row query-pair units do not fill the last wave of CTAs, each
-pair of that wave runs as two single-tile units, one per CTA.  The grid is
+pair of that wave runs as two single-tile units, one per CTA; with fewer
+pairs than CTAs, as many pairs as there are idle CTAs are split.  The grid is
 capped with fa_set_max_ctas so that small problems take this path; every case
 asserts that its shape does.  The cases add to the split tests of the main
 parity file: d = 64, both parities of the key-tile count, heads with a
@@ -171,3 +172,23 @@ def test_split_fp8(fa, causal):
     vv = v.float().numpy()
     bound = 2.0 ** -4 * float(np.abs(vv).max()) + 2.0 ** -8 * float(np.abs(o_ref).max())
     assert float(np.abs(o_np - o_ref).max()) <= bound
+
+
+# ----------------------------------------------- fewer pairs than CTAs
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+@pytest.mark.parametrize("B,H,N,ctas", [
+    (1, 3, 256, 5),    # 3 pairs, 2 idle CTAs: 2 pairs split, 1 kept
+    (1, 2, 1000, 0),   # 8 pairs on every SM: all split
+    (1, 1, 300, 3),    # 2 pairs, the second holding a ragged 44-row tile
+])
+def test_first_wave_split(fa, B, H, N, ctas, causal, d):
+    """With fewer 256-row pair units than CTAs, as many pairs as there are
+    idle CTAs run as two single-tile units each."""
+    q, k, v = make_random_qkv(B, H, N, d, torch.bfloat16, seed=90 + N + d)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = _run(fa, q, k, v, scale, causal, (-1, -1), ctas)
+    o_ref, l_ref = oracle.attention(q, k, v, scale, causal)
+    err_o = float(np.abs(o.float().cpu().numpy() - o_ref).max())
+    err_l = float(np.abs(lse.cpu().numpy() - l_ref).max())
+    assert err_o <= O_TOL and err_l <= LSE_TOL, (err_o, err_l)
