@@ -21,8 +21,9 @@
 //   warp  4    TMA producer
 //   warp  5    MMA issuer: S(G) = Q K_G^T into buffer G mod 3, then
 //              P(G-1) V_(G-1) into O, over the stream of K tiles G
-//   warp  6    O store (the 128x256 output leaves through a 128x128 staging
-//              tile, in two halves)
+//   warp  6    O store (TMA store of the 128x128 staging tile: columns
+//              0-127 of a dense tile, both halves of a whole packed tile;
+//              the softmax threads store the rest themselves)
 //   warp  7    spare
 //
 // With three S buffers, S(G) overwrites the columns of P(G-3), the A
@@ -458,7 +459,14 @@ __global__ void __launch_bounds__(d256::kThreads, 1)
           }
         }
       }
-      for (int half = 0; half < 2 && ok && !(PACKED && len - w.row0 < kBlockM); ++half) {
+      // Dense layout: columns 0-127 through the staging tile and a TMA
+      // store, columns 128-255 stored by the warps themselves (coalesced
+      // 64-byte row segments), so that the second half does not wait for
+      // the first half's store to free the staging tile.  Whole packed
+      // tiles stage both halves.
+      const int staged_halves = PACKED ? 2 : 1;
+      for (int half = 0; half < staged_halves && ok && !(PACKED && len - w.row0 < kBlockM);
+           ++half) {
         // the staging tile must have been read by the store before this one
         ok = wait_bar(bar(kStageEmpty), (n_stores - 1) & 1u, ctl, kSiteEpilogueO);
         ok = __all_sync(0xffffffffu, ok);
@@ -484,6 +492,24 @@ __global__ void __launch_bounds__(d256::kThreads, 1)
         fence_proxy_async_smem();
         mbar_arrive(bar(kStageFull));
       }
+      if (!PACKED && ok) {
+        const int t_warp = t & ~31;  // tile row of lane 0
+#pragma unroll 1
+        for (int c = 0; c < 128; c += 32) {
+          uint32_t o[32];
+          tmem_ld_x32_sync(tO + 128 + c, o);
+          uint32_t w16[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            w16[e] = pack2<BF16>(__uint_as_float(o[2 * e]) * inv_l,
+                                 __uint_as_float(o[2 * e + 1]) * inv_l);
+          store_rows_x32(w16, lane, [&](int rl) -> uint16_t* {
+            const int r_row = w.row0 + t_warp + rl;
+            if (r_row >= len) return nullptr;
+            return p.o_ptr + (static_cast<long long>(w.sv.o_head) * p.N + r_row) * 256 + 128 + c;
+          });
+        }
+      }
       if (p.lse != nullptr && row < len) {
         p.lse[lse_base<PACKED>(p, w.sv) + row] =
             (l > 0.f) ? (m_ref + log2f(l)) * 0.6931471805599453f : -INFINITY;
@@ -492,16 +518,17 @@ __global__ void __launch_bounds__(d256::kThreads, 1)
     __syncwarp();
   } else if (warp == kStoreWarp) {
     // ------------------------------------------------------------ O store
-    // Lane 0 waits and issues the TMA stores of the two staged halves of
-    // each tile (the partial last tiles of packed sequences are stored by
-    // the softmax threads).
+    // Lane 0 waits and issues the TMA stores of the staged halves of each
+    // tile: columns 0-127 of a dense tile, both halves of a whole packed
+    // tile (the partial last tiles of packed sequences are stored by the
+    // softmax threads).
     uint32_t full_par = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < p.num_units && ok && lane == 0; u += gridDim.x) {
       const Unit w = decode_unit<CAUSAL, PACKED>(u, p);
       if (w.n1 == w.n0) continue;
       if (PACKED && w.sv.len - w.row0 < kBlockM) continue;
-      for (int half = 0; half < 2 && ok; ++half) {
+      for (int half = 0; half < (PACKED ? 2 : 1) && ok; ++half) {
         ok = wait_bar(bar(kStageFull), full_par, ctl, kSiteStore);
         full_par ^= 1u;
         if (!ok) break;
