@@ -1205,6 +1205,15 @@ int bwd_launch(const void* q, const void* k, const void* v, const void* o, const
   BwdParams p_kv = p, p_q = p;
   p_kv.num_units = static_cast<int>(static_cast<long long>(ibkv) * n_tiles_k);
   p_q.num_units = static_cast<int>(bh * n_tiles);
+  // packed causal launches order their units from a per-CTA table (both
+  // kernels, or neither)
+  const long long max_tiles = n_tiles > n_tiles_k ? n_tiles : n_tiles_k;
+  const int table = (packed && causal && B <= kTableSeqs && max_tiles > 1 &&
+                     max_tiles <= kBwdTableTiles)
+                        ? 1
+                        : 0;
+  p_kv.unit_table = table;
+  p_q.unit_table = table;
   int grid = info->num_sms;
   const int cap = g_max_ctas.load();
   if (cap > 0 && cap < grid) grid = cap;

@@ -6,7 +6,7 @@
 namespace fa {
 namespace {
 
-template <bool CAUSAL, bool BF16>
+template <bool CAUSAL, bool BF16, bool TABLE = false>
 cudaError_t launch_all(const BwdParams& p_kv, const BwdParams& p_q, const void* o,
                        const void* dout, const float* lse, float* lse2, float* dsum,
                        int grid_kv, int grid_q, int num_sms, cudaStream_t stream) {
@@ -21,8 +21,8 @@ cudaError_t launch_all(const BwdParams& p_kv, const BwdParams& p_q, const void* 
                              lse, lse2, dsum, p_q.num_bh, p_q.N, p_q.n_pad, p_q);
   if (e != cudaSuccess) return e;
   constexpr int kSmem = bwd::Layout<64>::kSmemBytes;
-  constexpr auto kv = bwd::fa_bwd_dkdv_kernel<64, CAUSAL, BF16, true>;
-  constexpr auto dq = bwd::fa_bwd_dq_kernel<64, CAUSAL, BF16, true>;
+  constexpr auto kv = bwd::fa_bwd_dkdv_kernel<64, CAUSAL, BF16, true, TABLE>;
+  constexpr auto dq = bwd::fa_bwd_dq_kernel<64, CAUSAL, BF16, true, TABLE>;
   e = smem_attribute_once<kv>(kSmem);
   if (e != cudaSuccess) return e;
   e = smem_attribute_once<dq>(kSmem);
@@ -38,6 +38,11 @@ cudaError_t launch_bwd_d64_packed(const BwdParams& p_kv, const BwdParams& p_q, c
                                   const void* dout, const float* lse, float* lse2, float* dsum,
                                   bool causal, bool bf16, int grid_kv, int grid_q, int num_sms,
                                   cudaStream_t stream) {
+  if (causal && p_kv.unit_table)  // units from the per-CTA unit tables
+    return bf16 ? launch_all<true, true, true>(p_kv, p_q, o, dout, lse, lse2, dsum, grid_kv,
+                                               grid_q, num_sms, stream)
+                : launch_all<true, false, true>(p_kv, p_q, o, dout, lse, lse2, dsum, grid_kv,
+                                                grid_q, num_sms, stream);
   if (causal)
     return bf16 ? launch_all<true, true>(p_kv, p_q, o, dout, lse, lse2, dsum, grid_kv, grid_q,
                                          num_sms, stream)

@@ -106,9 +106,81 @@ struct Layout {
   static constexpr int kDrain = 21;     // both issuing threads' last products (2 arrivals)
   static constexpr int kNumBars = 22;
   static constexpr uint32_t kCtlOff = kBarOff + kNumBars * 8;
-  static constexpr uint32_t kSmemBytes = kCtlOff + 16;
+  // unit table of packed causal launches: sequence ids (bytes), then the
+  // cumulative unit counts of the tile groups (ints)
+  static constexpr uint32_t kTableIdsOff = kCtlOff + 16;
+  static constexpr uint32_t kTableCumOff = kTableIdsOff + kTableSeqs;
+  static constexpr uint32_t kSmemBytes = kTableCumOff + 4 * (kBwdTableTiles + 1);
   static_assert(kSmemBytes <= 232448, "exceeds the shared memory of one CTA");
 };
+
+// Unit table of a packed causal launch (shared memory, built once per CTA).
+// Sequence b has cnt(b) units per head, unit x of it costing more as x
+// grows (dQ: query tile x sees key tiles 0 .. x; dK/dV: key tile
+// cnt(b) - 1 - x is seen by x + 1 query tiles).  Units are taken in groups
+// of equal x, highest first: group k (x = P - 1 - k) holds unit x of every
+// sequence that has one (ids[0 .. q_k), the sequences sorted by cnt,
+// largest first) for every head; cum[k] units precede group k, cum[P] exist
+// in all, and slots past cum[P] are empty units.
+struct BwdTable {
+  const uint8_t* ids;
+  const int* cum;
+};
+
+// Builds the table (one warp; every lane calls it) for `batch` sequences
+// (at most kTableSeqs) and P groups (at most kBwdTableTiles).
+template <typename Cnt>
+__device__ __forceinline__ void build_bwd_table(int batch, int P, int heads, Cnt cnt,
+                                                uint8_t* ids, int* cum, int lane) {
+  int np[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int b = lane + 32 * i;
+    np[i] = b < batch ? cnt(b) : -1;
+  }
+  int rank[2] = {0, 0};
+  for (int b2 = 0; b2 < batch; ++b2) {
+    const int v0 = __shfl_sync(0xffffffffu, np[0], b2 & 31);
+    const int v1 = __shfl_sync(0xffffffffu, np[1], b2 & 31);
+    const int n2 = b2 < 32 ? v0 : v1;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int b = lane + 32 * i;
+      rank[i] += (n2 > np[i] || (n2 == np[i] && b2 < b)) ? 1 : 0;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+    if (lane + 32 * i < batch) ids[rank[i]] = static_cast<uint8_t>(lane + 32 * i);
+  int running = 0;
+  if (lane == 0) cum[0] = 0;
+  for (int k = 0; k < P; ++k) {
+    const int x = P - 1 - k;
+    const int c = __popc(__ballot_sync(0xffffffffu, np[0] > x)) +
+                  __popc(__ballot_sync(0xffffffffu, np[1] > x));
+    running += c * heads;
+    if (lane == 0) cum[k + 1] = running;
+  }
+}
+
+// Slot u (< num_units) of a table launch: -1 for an empty unit, else the
+// sequence (*b), head (*h) and the unit's x.
+__device__ __forceinline__ int bwd_table_unit(int u, int P, int heads, const BwdTable& tab,
+                                              int* b, int* h) {
+  if (u >= tab.cum[P]) return -1;
+  int lo = 0, hi = P - 1;  // the group k with cum[k] <= u < cum[k+1]
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (tab.cum[mid] <= u)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  const int r = u - tab.cum[lo];
+  *b = tab.ids[r / heads];
+  *h = r % heads;
+  return P - 1 - lo;
+}
 
 template <typename L, typename Bar>
 __device__ __forceinline__ void init_barriers(Bar bar) {
@@ -301,13 +373,23 @@ struct KvUnit {
   bool rows;      // the tile holds key rows of the sequence (steps 0: write zeros)
 };
 
-template <bool CAUSAL, bool PACKED>
-__device__ __forceinline__ KvUnit decode_kv_unit(int u, const BwdParams& p) {
+template <bool CAUSAL, bool PACKED, bool TABLE>
+__device__ __forceinline__ KvUnit decode_kv_unit(int u, const BwdParams& p,
+                                                 const BwdTable& tab) {
+  static_assert(!TABLE || (CAUSAL && PACKED), "the unit table orders packed causal units");
   KvUnit w;
-  // (slot u of the persistent loop; dense causal launches alternate the
-  // direction of their waves)
-  if (CAUSAL && !PACKED && u < p.num_units) u = wave_order(u, p.num_units, gridDim.x);
-  if (CAUSAL) {
+  // (slot u of the persistent loop; dense causal launches and table
+  // launches alternate the direction of their waves)
+  if (CAUSAL && (!PACKED || TABLE) && u < p.num_units) u = wave_order(u, p.num_units, gridDim.x);
+  if constexpr (TABLE) {
+    // key tile cnt - 1 - x of head h of sequence b, cnt its key tiles
+    int b = 0, h = 0;
+    const int x = u < p.num_units ? bwd_table_unit(u, p.n_tiles_k, p.H_kv, tab, &b, &h) : -1;
+    w.bkv = b * p.H_kv + h;
+    int kb, kl;
+    bwd_keys<PACKED>(p, b, &kb, &kl);
+    w.n = x < 0 ? p.n_tiles_k : (kl + 127) / 128 - 1 - x;
+  } else if (CAUSAL) {
     // heaviest first: the first key tiles see the most query tiles
     w.n = u / p.num_bkv;
     w.bkv = u % p.num_bkv;
@@ -330,7 +412,9 @@ __device__ __forceinline__ KvUnit decode_kv_unit(int u, const BwdParams& p) {
   return w;
 }
 
-template <int D, bool CAUSAL, bool BF16, bool PACKED>
+// TABLE: packed causal launches that order their units from the per-CTA
+// unit table (p.unit_table set).
+template <int D, bool CAUSAL, bool BF16, bool PACKED, bool TABLE = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
   using L = Layout<D>;
@@ -367,6 +451,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   // dependent launch); global memory is touched only after it completed.
   griddep_wait();
   griddep_launch_dependents();
+  const BwdTable tab{smem + L::kTableIdsOff,
+                     reinterpret_cast<const int*>(smem + L::kTableCumOff)};
+  if constexpr (TABLE) {
+    if (warp == 0)
+      build_bwd_table(
+          p.num_bkv / p.H_kv, p.n_tiles_k, p.H_kv,
+          [&](int b) {
+            int kb, kl;
+            bwd_keys<PACKED>(p, b, &kb, &kl);
+            return (kl + 127) / 128;
+          },
+          smem + L::kTableIdsOff, reinterpret_cast<int*>(smem + L::kTableCumOff), lane);
+    __syncthreads();
+  }
 
   if (warp == kProducerWarp) {
     // ---------------------------------------------------------------- TMA
@@ -374,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t na = 0, nb = 0, units = 0;  // ring A / ring B stages filled, units
       bool ok = true;
       for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
-        const KvUnit w = decode_kv_unit<CAUSAL, PACKED>(u, p);
+        const KvUnit w = decode_kv_unit<CAUSAL, PACKED, TABLE>(u, p, tab);
         if (w.steps == 0) continue;  // no key rows, or keys no query sees
         const uint32_t uix = units++;
         ok = wait_bar(bar(L::kFixEmpty), (uix & 1u) ^ 1u, ctl, kSiteProducerKV);
@@ -442,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it = 0, units = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
-        const KvUnit w = decode_kv_unit<CAUSAL, PACKED>(u, p);
+        const KvUnit w = decode_kv_unit<CAUSAL, PACKED, TABLE>(u, p, tab);
         if (w.steps == 0) continue;  // no key rows, or keys no query sees
         const uint32_t uix = units++;
         ok = wait_bar(bar(L::kFixFull), uix & 1u, ctl, kSiteMmaK);
@@ -496,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it = 0, units = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
-        const KvUnit w = decode_kv_unit<CAUSAL, PACKED>(u, p);
+        const KvUnit w = decode_kv_unit<CAUSAL, PACKED, TABLE>(u, p, tab);
         if (w.steps == 0) continue;
         const uint32_t uix = units++;
         for (int s = 0; s < w.steps; ++s, ++it) {
@@ -550,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t it = 0, units = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
-      const KvUnit w = decode_kv_unit<CAUSAL, PACKED>(u, p);
+      const KvUnit w = decode_kv_unit<CAUSAL, PACKED, TABLE>(u, p, tab);
       // dV / dK rows of key tile n of K/V head bkv ([B*H_kv][N][d], or
       // packed [total_k][H_kv][d]): 32 columns of the rows of this warp
       const int j_warp = w.n * 128 + (warp % 4) * 32;  // key of lane 0's row
@@ -672,11 +770,18 @@ struct QUnit {
   bool rows;      // the tile holds query rows of the sequence (no keys: dQ = 0)
 };
 
-template <bool CAUSAL, bool PACKED>
-__device__ __forceinline__ QUnit decode_q_unit(int u, const BwdParams& p) {
+template <bool CAUSAL, bool PACKED, bool TABLE>
+__device__ __forceinline__ QUnit decode_q_unit(int u, const BwdParams& p, const BwdTable& tab) {
+  static_assert(!TABLE || (CAUSAL && PACKED), "the unit table orders packed causal units");
   QUnit w;
-  if (CAUSAL && !PACKED && u < p.num_units) u = wave_order(u, p.num_units, gridDim.x);
-  if (CAUSAL) {
+  if (CAUSAL && (!PACKED || TABLE) && u < p.num_units) u = wave_order(u, p.num_units, gridDim.x);
+  if constexpr (TABLE) {
+    // query tile x of head h of sequence b
+    int b = 0, h = 0;
+    const int x = u < p.num_units ? bwd_table_unit(u, p.n_tiles, p.H, tab, &b, &h) : -1;
+    w.bh = b * p.H + h;
+    w.m = x < 0 ? p.n_tiles : x;
+  } else if (CAUSAL) {
     w.m = p.n_tiles - 1 - u / p.num_bh;  // heaviest first
     w.bh = u % p.num_bh;
   } else {
@@ -686,7 +791,7 @@ __device__ __forceinline__ QUnit decode_q_unit(int u, const BwdParams& p) {
   w.bkv = kv_head(w.bh, p.H, p.group);
   bwd_sequence<PACKED>(p, w.bh / p.H, &w.row_base, &w.len);
   bwd_keys<PACKED>(p, w.bh / p.H, &w.k_row_base, &w.k_len);
-  if (PACKED && CAUSAL) {
+  if (PACKED && CAUSAL && !TABLE) {
     // count the tiles from each sequence's end (its heaviest tiles first)
     w.m = (w.len + 127) / 128 - 1 - (p.n_tiles - 1 - w.m);
     if (w.m < 0) w.m = p.n_tiles;
@@ -703,7 +808,7 @@ __device__ __forceinline__ QUnit decode_q_unit(int u, const BwdParams& p) {
   return w;
 }
 
-template <int D, bool CAUSAL, bool BF16, bool PACKED>
+template <int D, bool CAUSAL, bool BF16, bool PACKED, bool TABLE = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
   using L = Layout<D>;
@@ -740,6 +845,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   // dependent launch); global memory is touched only after it completed.
   griddep_wait();
   griddep_launch_dependents();
+  const BwdTable tab{smem + L::kTableIdsOff,
+                     reinterpret_cast<const int*>(smem + L::kTableCumOff)};
+  if constexpr (TABLE) {
+    if (warp == 0)
+      build_bwd_table(
+          p.num_bh / p.H, p.n_tiles, p.H,
+          [&](int b) {
+            int rb, rl;
+            bwd_sequence<PACKED>(p, b, &rb, &rl);
+            return (rl + 127) / 128;
+          },
+          smem + L::kTableIdsOff, reinterpret_cast<int*>(smem + L::kTableCumOff), lane);
+    __syncthreads();
+  }
 
   if (warp == kProducerWarp) {
     // ---------------------------------------------------------------- TMA
@@ -747,7 +866,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t na = 0, nb = 0, units = 0;  // ring A / ring B stages filled, units
       bool ok = true;
       for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
-        const QUnit w = decode_q_unit<CAUSAL, PACKED>(u, p);
+        const QUnit w = decode_q_unit<CAUSAL, PACKED, TABLE>(u, p, tab);
         if (w.n1 == w.n0) continue;  // no query rows, or rows without keys
         const uint32_t uix = units++;
         ok = wait_bar(bar(L::kFixEmpty), (uix & 1u) ^ 1u, ctl, kSiteProducerQ);
@@ -797,7 +916,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it = 0, units = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
-        const QUnit w = decode_q_unit<CAUSAL, PACKED>(u, p);
+        const QUnit w = decode_q_unit<CAUSAL, PACKED, TABLE>(u, p, tab);
         if (w.n1 == w.n0) continue;  // no query rows, or rows without keys
         const uint32_t uix = units++;
         ok = wait_bar(bar(L::kFixFull), uix & 1u, ctl, kSiteMmaQ);
@@ -843,7 +962,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it = 0, units = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
-        const QUnit w = decode_q_unit<CAUSAL, PACKED>(u, p);
+        const QUnit w = decode_q_unit<CAUSAL, PACKED, TABLE>(u, p, tab);
         if (w.n1 == w.n0) continue;
         const uint32_t uix = units++;
         for (int n = w.n0; n < w.n1; ++n, ++it) {
@@ -886,7 +1005,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the first unit at or after u with query rows (num_units: none)
     auto next_unit = [&](int u, QUnit& w) -> int {
       for (; u < p.num_units; u += gridDim.x) {
-        w = decode_q_unit<CAUSAL, PACKED>(u, p);
+        w = decode_q_unit<CAUSAL, PACKED, TABLE>(u, p, tab);
         if (w.rows) break;
       }
       return u;

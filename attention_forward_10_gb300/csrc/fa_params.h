@@ -16,6 +16,7 @@ constexpr int kRowsPerUnit = 2 * kBlockM;
 // Limits of the per-CTA unit table of packed causal launches.
 constexpr int kTableSeqs = 64;
 constexpr int kTablePairs = 256;
+constexpr int kBwdTableTiles = 128;  // backward: tiles per problem
 
 // Site codes recorded in the status word when a bounded wait runs out.
 enum WaitSite : int {
@@ -128,6 +129,10 @@ struct BwdParams {  // 64-byte aligned through CUtensorMap
   const int* seqused_k;
   int total_rows, total_rows_k;
   int N_k, n_tiles_k;  // longest key length (N unless packed) and its 128-key tiles
+  // Packed causal launches with at most kTableSeqs sequences and 2 ..
+  // kBwdTableTiles tiles per problem: 1 when every CTA orders its units from
+  // a unit table (see the kernels), 0 otherwise.
+  int unit_table;
 };
 
 // Rows of one (b, h) attention problem: the first packed row and the length

@@ -980,25 +980,39 @@ def run_backward(args, wl):
         dist.init_process_group("nccl", device_id=dev)
     import attention_forward_10_gb300 as fa
     from workloads import make_qkv
-    if wl.varlen or wl.splitkv or wl.d not in (64, 128):
-        raise SystemExit("--backward runs the [B,H,N,d] workloads with d = 64 or 128")
+    if wl.splitkv or wl.decode or wl.dtype == "fp8" or wl.d not in (64, 128):
+        raise SystemExit("--backward runs the [B,H,N,d] and packed workloads with d = 64 or 128")
     fa.fa_set_max_ctas(0)
     warmup = max(3, args.warmup)
     q, k, v = (t.to(dev) for t in make_qkv(wl))
     dout = torch.randn(q.shape, generator=torch.Generator().manual_seed(4000 + wl.index))
     dout = dout.to(q.dtype).to(dev)
-    o, lse = fa.fwd(q, k, v, scale=wl.scale, causal=wl.causal)
-    st, need = fa.fa_bwd_workspace_bytes(wl.B, wl.H, wl.N)
+    if wl.varlen:
+        # packed batch ([total, H, d]) through fa_bwd_varlen
+        lens = wl.seqlens()
+        cu_dev = torch.tensor(wl.cu_seqlens(), dtype=torch.int32, device=dev)
+        o, lse = fa.fwd_varlen(q, k, v, cu_dev, max(lens), scale=wl.scale, causal=wl.causal)
+        st, need = fa.fa_bwd_workspace_bytes(wl.B, wl.H, max(lens))
+    else:
+        o, lse = fa.fwd(q, k, v, scale=wl.scale, causal=wl.causal)
+        st, need = fa.fa_bwd_workspace_bytes(wl.B, wl.H, wl.N)
     ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     stream = torch.cuda.Stream(device=dev)
     dcode = fa.FA_DTYPE_BF16 if wl.dtype == "bf16" else fa.FA_DTYPE_F16
 
     def step():
-        st_ = fa.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                        dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
-                        ws.data_ptr(), ws.numel(), wl.B, wl.H, wl.H, wl.N, wl.d, wl.scale,
-                        int(wl.causal), -1, -1, dcode, stream.cuda_stream)
+        if wl.varlen:
+            st_ = fa.fa_bwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                   lse.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                   dv.data_ptr(), cu_dev.data_ptr(), wl.B, max(lens),
+                                   int(q.shape[0]), wl.H, wl.H, wl.d, wl.scale, int(wl.causal),
+                                   -1, -1, dcode, ws.data_ptr(), ws.numel(), stream.cuda_stream)
+        else:
+            st_ = fa.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                            lse.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                            dv.data_ptr(), ws.data_ptr(), ws.numel(), wl.B, wl.H, wl.H, wl.N,
+                            wl.d, wl.scale, int(wl.causal), -1, -1, dcode, stream.cuda_stream)
         if st_ != fa.FA_OK:
             raise RuntimeError(f"fa_bwd failed: {fa.fa_status_string(st_)}")
 

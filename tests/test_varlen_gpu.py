@@ -277,6 +277,22 @@ def test_backward_ragged_many_units_per_cta(fa, ctas, causal):
         fa.fa_set_max_ctas(0)
 
 
+@pytest.mark.parametrize("nseq,H_kv", [(64, 2), (64, 1), (65, 2)])
+@pytest.mark.parametrize("ctas", [0, 5])
+def test_backward_unit_table_and_fallback(fa, nseq, H_kv, ctas):
+    """Packed causal backward launches with at most 64 sequences order the
+    units of both kernels from a per-CTA table (groups of equal tile index,
+    heaviest first, every other wave reversed); with 65 sequences they keep
+    the plain order.  On every SM and on 5 CTAs (many waves)."""
+    g = torch.Generator().manual_seed(700 + nseq)
+    lens = torch.randint(0, 400, (nseq,), generator=g).tolist()
+    fa.fa_set_max_ctas(ctas)
+    try:
+        _bwd_check(fa, lens, 2, H_kv, 128, True, (-1, -1), seed=701 + nseq + H_kv)
+    finally:
+        fa.fa_set_max_ctas(0)
+
+
 def test_backward_equal_lengths_equal_the_batched_backward(fa):
     """Equal-length packed sequences give fa_bwd's gradients bit for bit."""
     N, d = 256, 128
