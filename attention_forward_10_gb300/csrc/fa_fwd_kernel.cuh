@@ -58,8 +58,8 @@
 //   Q_0, Q_1       [D/64][128 rows][64]   one tile each
 //   K/V ring       STAGES slots of [D/64][128 keys][64]
 //   O staging      one tile, shared by the two query tiles in turn (TMA
-//                  store source; packed batches store O from the softmax
-//                  threads instead)
+//                  store source; tile 1 of a causal unit and the tiles of
+//                  packed batches are stored by the softmax threads instead)
 //   mbarriers
 //
 // Online softmax in the log2 domain (scale folded into scale*log2 e, as the
