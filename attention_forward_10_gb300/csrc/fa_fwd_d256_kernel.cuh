@@ -19,19 +19,23 @@
 //
 //   warps 0-3  softmax (one query row per thread)
 //   warp  4    TMA producer
-//   warp  5    MMA issuer: S(G) = Q K_G^T into buffer G mod 3, then
-//              P(G-1) V_(G-1) into O, over the stream of K tiles G
+//   warp  5    S issuer: S(G) = Q K_G^T into buffer G mod 3, over the
+//              stream of K tiles G
 //   warp  6    O store (TMA store of the 128x128 staging tile: columns
 //              0-127 of a dense tile, both halves of a whole packed tile;
 //              the softmax threads store the rest themselves)
-//   warp  7    spare
+//   warp  7    P V issuer: O += P(G) V_G once the softmax has written P(G)
 //
-// With three S buffers, S(G) overwrites the columns of P(G-3), the A
-// operand of P(G-3) V, issued two MMA groups earlier.  The PTX ISA orders two
-// tcgen05.mma of one thread only when they share the accumulator and shape,
-// so S(G) first waits for that product's commit (barrier ODone of the
-// buffer); two MMA groups later it has normally completed, so the wait costs
-// the tensor pipe nothing.  The softmax of tile G-1 runs while S(G) executes.
+// The tensor pipe accepts only a few MMAs ahead of the one it executes, so
+// a single issuing thread that waits on a barrier (a K tile, a P tile) lets
+// the pipe run dry; with the two products issued from two warps, one
+// issuer's waits overlap the other's MMAs.  The two streams meet only
+// through barriers: P V(G) waits for the softmax of tile G (which waited for
+// S(G)), and with three S buffers S(G) overwrites the columns of P(G-3), the
+// A operand of P(G-3) V, so S(G) first waits for that product's commit
+// (barrier ODone of the buffer; the PTX ISA orders tcgen05.mma of one thread
+// only when they share the accumulator and shape, and these are issued by
+// different threads).  The softmax of tile G-1 runs while S(G) executes.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -50,6 +54,7 @@ constexpr int kThreads = 256;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kStoreWarp = 6;
+constexpr int kPvWarp = 7;
 constexpr int kSBufs = 3;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -73,7 +78,8 @@ constexpr int kODone = kPFull + kSBufs;       // per S buffer: P(G) V done
 constexpr int kStageFull = kODone + kSBufs;
 constexpr int kStageEmpty = kStageFull + 1;
 constexpr int kDrain = kStageEmpty + 1;
-constexpr int kNumBars = kDrain + 1;
+constexpr int kDrainPv = kDrain + 1;
+constexpr int kNumBars = kDrainPv + 1;
 constexpr uint32_t kCtlOff = kBarOff + kNumBars * 8;
 constexpr uint32_t kUsedBytes = kCtlOff + 16;
 constexpr uint32_t kSmemBytes = kUsedBytes + 1024;  // alignment slack
@@ -168,6 +174,7 @@ __global__ void __launch_bounds__(d256::kThreads, 1)
     mbar_init(bar(kStageFull), 128);
     mbar_init(bar(kStageEmpty), 1);
     mbar_init(bar(kDrain), 1);
+    mbar_init(bar(kDrainPv), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -224,45 +231,28 @@ __global__ void __launch_bounds__(d256::kThreads, 1)
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
-    // ---------------------------------------------------------------- MMA
+    // ------------------------------------------------------------ S = Q K^T
     if (lane == 0) {
       constexpr uint32_t kIdescS = make_idesc_f16(kBlockM, kBN, BF16, false);
-      constexpr uint32_t kIdescO = make_idesc_f16(kBlockM, D, BF16, true);
       constexpr uint32_t kSlotStep = kKVBytes >> 4;  // descriptor units
       const uint64_t q_desc = smem_desc_sw128(sbase + kQOff, 16, 1024);
       const uint64_t k_desc0 = smem_desc_sw128(sbase + kKVOff, 16, 1024);
-      // V (64 keys x 256): MN-major, 64-wide d blocks 64 keys x 128 B apart
-      // (LBO), 8-key groups 1024 B apart (SBO)
-      const uint64_t v_desc0 = smem_desc_sw128(sbase + kKVOff, kBN * 128, 1024);
-      uint32_t slot = 0, phase = 0, q_par = 0;
-      uint32_t G = 0;  // global index of the next K tile (S tile) of this CTA
+      uint32_t q_par = 0;
+      uint32_t G = 0;  // global index of this CTA's K tiles (S tiles)
       bool ok = true;
-      // pending P V product: the previous K tile
-      bool pv_pending = false, pv_acc = false;
-      uint32_t pv_vslot = 0, pv_vphase = 0;
-      int u = blockIdx.x;
-      Unit w = decode_unit<CAUSAL, PACKED>(u < p.num_units ? u : 0, p);
-      while (u < p.num_units && w.n1 == w.n0) {  // empty key split: nothing to do
-        u += gridDim.x;
-        if (u < p.num_units) w = decode_unit<CAUSAL, PACKED>(u, p);
-      }
-      int n = w.n0;
-      while (ok) {
-        const bool cur_valid = u < p.num_units;
-        if (cur_valid) {
-          // ---- S(G) = Q K_G^T into buffer G mod 3
+      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+        const Unit w = decode_unit<CAUSAL, PACKED>(u, p);
+        if (w.n1 == w.n0) continue;  // empty key split: nothing to do
+        ok = wait_bar(bar(kQFull), q_par, ctl, kSiteMmaQ);
+        q_par ^= 1u;
+        for (int n = w.n0; n < w.n1 && ok; ++n, ++G) {
+          // K(G) is load 2G of the ring
           const uint32_t b = G % kSBufs;
-          if (n == w.n0) {
-            ok = wait_bar(bar(kQFull), q_par, ctl, kSiteMmaQ);
-            q_par ^= 1u;
-            if (!ok) break;
-          }
-          const uint32_t kslot = slot;
-          ok = wait_bar(bar(kKVFull + kslot), phase, ctl, kSiteMmaK);
+          const uint32_t kslot = (2u * G) % kStages;
+          ok = wait_bar(bar(kKVFull + kslot), ((2u * G) / kStages) & 1u, ctl, kSiteMmaK);
           if (!ok) break;
-          if (++slot == (uint32_t)kStages) { slot = 0; phase ^= 1u; }
-          // P(G-3) occupied buffer b: its P V product (issued two groups
-          // ago) must have read it before this product overwrites it
+          // P(G-3) occupied buffer b: its P V product must have read it
+          // before this product overwrites it
           if (G >= (uint32_t)kSBufs) {
             ok = wait_bar(bar(kODone + b), ((G - kSBufs) / kSBufs) & 1u, ctl, kSiteMmaO);
             if (!ok) break;
@@ -274,37 +264,40 @@ __global__ void __launch_bounds__(d256::kThreads, 1)
           tc_commit(bar(kKVEmpty + kslot));
           if (n == w.n1 - 1) tc_commit(bar(kQEmpty));
         }
-        if (pv_pending) {
-          // ---- O += P(G-1) V_(G-1)
-          const uint32_t pb = (G - 1) % kSBufs;
-          ok = wait_bar(bar(kKVFull + pv_vslot), pv_vphase, ctl, kSiteMmaV);
-          ok = ok && wait_bar(bar(kPFull + pb), ((G - 1) / kSBufs) & 1u, ctl, kSiteMmaP);
-          if (!ok) break;
-          tc_fence_after_sync();
-          mma_ts_mnmajor_x4(tmem + kOCol, tmem + pb * kBN, v_desc0 + pv_vslot * kSlotStep,
-                            kIdescO, pv_acc ? 1u : 0u);
-          tc_commit(bar(kODone + pb));
-          tc_commit(bar(kKVEmpty + pv_vslot));
-          pv_pending = false;
-        }
-        if (!cur_valid) break;
-        // V(G) is used in the next iteration
-        pv_pending = true;
-        pv_acc = n > w.n0;
-        pv_vslot = slot;
-        pv_vphase = phase;
-        if (++slot == (uint32_t)kStages) { slot = 0; phase ^= 1u; }
-        ++G;
-        if (++n == w.n1) {
-          do {
-            u += gridDim.x;
-            if (u < p.num_units) w = decode_unit<CAUSAL, PACKED>(u, p);
-          } while (u < p.num_units && w.n1 == w.n0);
-          n = w.n0;
-        }
       }
       tc_commit(bar(kDrain));
       wait_drain(bar(kDrain), 0, p.timeout_ns);
+    }
+    __syncwarp();
+  } else if (warp == kPvWarp) {
+    // ----------------------------------------------------------- O += P V
+    if (lane == 0) {
+      constexpr uint32_t kIdescO = make_idesc_f16(kBlockM, D, BF16, true);
+      constexpr uint32_t kSlotStep = kKVBytes >> 4;  // descriptor units
+      // V (64 keys x 256): MN-major, 64-wide d blocks 64 keys x 128 B apart
+      // (LBO), 8-key groups 1024 B apart (SBO)
+      const uint64_t v_desc0 = smem_desc_sw128(sbase + kKVOff, kBN * 128, 1024);
+      uint32_t G = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+        const Unit w = decode_unit<CAUSAL, PACKED>(u, p);
+        if (w.n1 == w.n0) continue;
+        for (int n = w.n0; n < w.n1 && ok; ++n, ++G) {
+          // V(G) is load 2G + 1 of the ring; P(G) sits in buffer G mod 3
+          const uint32_t pb = G % kSBufs;
+          const uint32_t vslot = (2u * G + 1u) % kStages;
+          ok = wait_bar(bar(kKVFull + vslot), ((2u * G + 1u) / kStages) & 1u, ctl, kSiteMmaV);
+          ok = ok && wait_bar(bar(kPFull + pb), (G / kSBufs) & 1u, ctl, kSiteMmaP);
+          if (!ok) break;
+          tc_fence_after_sync();
+          mma_ts_mnmajor_x4(tmem + kOCol, tmem + pb * kBN, v_desc0 + vslot * kSlotStep, kIdescO,
+                            n > w.n0 ? 1u : 0u);
+          tc_commit(bar(kODone + pb));
+          tc_commit(bar(kKVEmpty + vslot));
+        }
+      }
+      tc_commit(bar(kDrainPv));
+      wait_drain(bar(kDrainPv), 0, p.timeout_ns);
     }
     __syncwarp();
   } else if (warp < 4) {
