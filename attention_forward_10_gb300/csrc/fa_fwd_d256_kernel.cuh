@@ -18,13 +18,14 @@
 //     [256,512)                   O (running output, fp32)
 //
 //   warps 0-3  softmax (one query row per thread)
-//   warp  4    TMA producer
+//   warp  4    TMA producer of Q and the K tiles
 //   warp  5    S issuer: S(G) = Q K_G^T into buffer G mod 3, over the
 //              stream of K tiles G
 //   warp  6    O store (TMA store of the 128x128 staging tile: columns
 //              0-127 of a dense tile, both halves of a whole packed tile;
 //              the softmax threads store the rest themselves)
 //   warp  7    P V issuer: O += P(G) V_G once the softmax has written P(G)
+//   warp  8    TMA producer of the V tiles
 //
 // The tensor pipe accepts only a few MMAs ahead of the one it executes, so
 // a single issuing thread that waits on a barrier (a K tile, a P tile) lets
@@ -50,11 +51,12 @@ namespace d256 {
 
 constexpr int D = 256;
 constexpr int kBN = 64;                 // keys per K/V tile
-constexpr int kThreads = 256;
+constexpr int kThreads = 288;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kStoreWarp = 6;
 constexpr int kPvWarp = 7;
+constexpr int kVProducerWarp = 8;
 constexpr int kSBufs = 3;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -197,36 +199,38 @@ __global__ void __launch_bounds__(d256::kThreads, 1)
   griddep_wait();
   griddep_launch_dependents();
 
-  if (warp == kProducerWarp) {
+  if (warp == kProducerWarp || warp == kVProducerWarp) {
     // ---------------------------------------------------------------- TMA
+    // K(G) goes to ring slot 2 (G mod 2), V(G) to slot 2 (G mod 2) + 1; warp
+    // 4 loads Q and the K tiles, warp 8 the V tiles, so that a K tile never
+    // waits behind a V tile whose slot the slower P V chain still holds.
     if (lane == 0) {
-      uint32_t slot = 0, phase = 0, q_it = 0, issued = 0;
+      const bool is_v = warp == kVProducerWarp;
+      uint32_t q_it = 0, G = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
         const Unit w = decode_unit<CAUSAL, PACKED>(u, p);
         if (w.n1 == w.n0) continue;
-        ok = wait_bar(bar(kQEmpty), (q_it & 1u) ^ 1u, ctl, kSiteProducerQ);
-        if (!ok) break;
-        mbar_arrive_expect_tx(bar(kQFull), kQBytes);
-        tma_load_4d(sbase + kQOff, &p.tm_q, bar(kQFull), 0, w.sv.row_base + w.row0, 0,
-                    w.sv.q_head);
-        ++q_it;
-        for (int n = w.n0; n < w.n1 && ok; ++n) {
-          for (int kv = 0; kv < 2; ++kv) {
-            ok = wait_bar(bar(kKVEmpty + slot), phase ^ 1u, ctl, kSiteProducerKV);
-            if (!ok) break;
-            mbar_arrive_expect_tx(bar(kKVFull + slot), kKVBytes);
-            tma_load_4d(sbase + kKVOff + slot * kKVBytes, kv ? &p.tm_v : &p.tm_k,
-                        bar(kKVFull + slot), 0, w.sv.k_row_base + n * kBN, 0, w.sv.kv_head);
-            ++issued;
-            if (++slot == (uint32_t)kStages) { slot = 0; phase ^= 1u; }
-          }
+        if (!is_v) {
+          ok = wait_bar(bar(kQEmpty), (q_it & 1u) ^ 1u, ctl, kSiteProducerQ);
+          if (!ok) break;
+          mbar_arrive_expect_tx(bar(kQFull), kQBytes);
+          tma_load_4d(sbase + kQOff, &p.tm_q, bar(kQFull), 0, w.sv.row_base + w.row0, 0,
+                      w.sv.q_head);
+          ++q_it;
+        }
+        for (int n = w.n0; n < w.n1 && ok; ++n, ++G) {
+          const uint32_t slot = 2u * (G % 2u) + (is_v ? 1u : 0u);
+          ok = wait_bar(bar(kKVEmpty + slot), ((G / 2u) & 1u) ^ 1u, ctl, kSiteProducerKV);
+          if (!ok) break;
+          mbar_arrive_expect_tx(bar(kKVFull + slot), kKVBytes);
+          tma_load_4d(sbase + kKVOff + slot * kKVBytes, is_v ? &p.tm_v : &p.tm_k,
+                      bar(kKVFull + slot), 0, w.sv.k_row_base + n * kBN, 0, w.sv.kv_head);
         }
       }
-      // Let every copy this warp issued land before the CTA may exit.
-      const uint32_t first = issued > (uint32_t)kStages ? issued - kStages : 0u;
-      for (uint32_t it = first; it < issued; ++it)
-        wait_drain(bar(kKVFull + it % kStages), (it / kStages) & 1u, p.timeout_ns);
+      // Let every copy this thread issued land before the CTA may exit.
+      for (uint32_t g = G > 2u ? G - 2u : 0u; g < G; ++g)
+        wait_drain(bar(kKVFull + 2u * (g % 2u) + (is_v ? 1u : 0u)), (g / 2u) & 1u, p.timeout_ns);
       if (q_it > 0) wait_drain(bar(kQFull), (q_it - 1) & 1u, p.timeout_ns);
     }
     __syncwarp();
