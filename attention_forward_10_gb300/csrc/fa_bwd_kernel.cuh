@@ -19,10 +19,11 @@
 // A pre-pass writes -LSE_i * log2(e) and -D_i into a workspace padded to
 // whole 128-row tiles (padding: -inf and 0, so padded query rows get P = 0).
 //
-// Warp roles (320 threads): warps 0-7 compute P and dS, one tensor-memory
+// Warp roles (352 threads): warps 0-7 compute P and dS, one tensor-memory
 // lane (row) per thread, warps 0-3 for the first 64 columns of a tile and
 // warps 4-7 for the last 64, and split the epilogue the same way; warp 8
-// issues TMA copies; warp 9 issues the MMAs.  Tensor memory, columns:
+// issues TMA copies; warp 9 issues the S and dP products, warp 10 the
+// gradient products.  Tensor memory, columns:
 // [0,128) S, [128,256) dP, then the fp32 accumulators: dV and dK (dK/dV
 // kernel) or dQ (dQ kernel), D columns each, and in the dQ kernel dS at
 // [384,480).
