@@ -12,14 +12,14 @@
 //   work unit  one 128-row query tile of one (b,h)
 //   K/V tiles  64 keys (32 KB each at d = 256), a 4-slot ring in shared memory
 //   tensor memory (512 columns):
-//     [0,64) [64,128) [128,192)   S buffers 0,1,2 (scores of three
+//     [0,64) ... [192,256)        S buffers 0-3 (scores of four
 //                                  consecutive K tiles; P, packed 16-bit,
 //                                  is written over the first 32 columns)
 //     [256,512)                   O (running output, fp32)
 //
 //   warps 0-3  softmax (one query row per thread)
 //   warp  4    TMA producer of Q and the K tiles
-//   warp  5    S issuer: S(G) = Q K_G^T into buffer G mod 3, over the
+//   warp  5    S issuer: S(G) = Q K_G^T into buffer G mod 4, over the
 //              stream of K tiles G
 //   warp  6    O store (TMA store of the 128x128 staging tile: columns
 //              0-127 of a dense tile, both halves of a whole packed tile;
@@ -32,8 +32,8 @@
 // the pipe run dry; with the two products issued from two warps, one
 // issuer's waits overlap the other's MMAs.  The two streams meet only
 // through barriers: P V(G) waits for the softmax of tile G (which waited for
-// S(G)), and with three S buffers S(G) overwrites the columns of P(G-3), the
-// A operand of P(G-3) V, so S(G) first waits for that product's commit
+// S(G)), and with four S buffers S(G) overwrites the columns of P(G-4), the
+// A operand of P(G-4) V, so S(G) first waits for that product's commit
 // (barrier ODone of the buffer; the PTX ISA orders tcgen05.mma of one thread
 // only when they share the accumulator and shape, and these are issued by
 // different threads).  The softmax of tile G-1 runs while S(G) executes.
@@ -57,7 +57,7 @@ constexpr int kMmaWarp = 5;
 constexpr int kStoreWarp = 6;
 constexpr int kPvWarp = 7;
 constexpr int kVProducerWarp = 8;
-constexpr int kSBufs = 3;
+constexpr int kSBufs = 4;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(d256::kThreads, 1)
           const uint32_t kslot = (2u * G) % kStages;
           ok = wait_bar(bar(kKVFull + kslot), ((2u * G) / kStages) & 1u, ctl, kSiteMmaK);
           if (!ok) break;
-          // P(G-3) occupied buffer b: its P V product must have read it
+          // P(G-4) occupied buffer b: its P V product must have read it
           // before this product overwrites it
           if (G >= (uint32_t)kSBufs) {
             ok = wait_bar(bar(kODone + b), ((G - kSBufs) / kSBufs) & 1u, ctl, kSiteMmaO);
@@ -287,7 +287,7 @@ __global__ void __launch_bounds__(d256::kThreads, 1)
         const Unit w = decode_unit<CAUSAL, PACKED>(u, p);
         if (w.n1 == w.n0) continue;
         for (int n = w.n0; n < w.n1 && ok; ++n, ++G) {
-          // V(G) is load 2G + 1 of the ring; P(G) sits in buffer G mod 3
+          // V(G) is load 2G + 1 of the ring; P(G) sits in buffer G mod 4
           const uint32_t pb = G % kSBufs;
           const uint32_t vslot = (2u * G + 1u) % kStages;
           ok = wait_bar(bar(kKVFull + vslot), ((2u * G + 1u) / kStages) & 1u, ctl, kSiteMmaV);
