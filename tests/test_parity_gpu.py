@@ -209,17 +209,21 @@ def test_grouped_heads_and_window(fa, d, H, H_kv, causal, window):
     _check(o, lse, o_ref, lse_ref, f"d={d} H={H}/{H_kv} causal={causal} window={window}")
 
 
+@pytest.mark.parametrize("d", [128, 256])
 @pytest.mark.parametrize("ctas", [1, 3])
 @pytest.mark.parametrize("window", [(64, 64), (500, 0)])
-def test_window_persistent_loop(fa, ctas, window):
-    q, k, v = make_random_qkv(1, 3, 1500, 128, torch.float16, seed=95 + ctas)
+def test_window_persistent_loop(fa, ctas, window, d):
+    """Windowed units see different numbers of key tiles, so the K/V ring's
+    slots and phases (and, at d = 256, the separate K and V producers and
+    the S and P V issuers) run on across units of uneven length."""
+    q, k, v = make_random_qkv(1, 3, 1500, d, torch.float16, seed=95 + ctas)
     fa.fa_set_max_ctas(ctas)
     try:
         o, lse = _run_ext(fa, q, k, v, 0.09, False, window)
     finally:
         fa.fa_set_max_ctas(0)
     o_ref, lse_ref = oracle.attention_ex(q, k, v, 0.09, False, *window)
-    _check(o, lse, o_ref, lse_ref, f"ctas={ctas} window={window}")
+    _check(o, lse, o_ref, lse_ref, f"d={d} ctas={ctas} window={window}")
 
 
 # ------------------------------------------------------------- watchdog
